@@ -1,0 +1,109 @@
+"""Pins of the oracle's RoPE against facts that do not come from it."""
+
+import math
+
+import numpy as np
+import pytest
+
+from oracle import rope
+
+F32 = np.float32
+
+
+def _complex_rotate(x, angle):
+    """Independent formulation: pairs (x_i, x_{i+d/2}) as complex numbers times e^{i angle}."""
+    half = x.shape[-1] // 2
+    z = (x[..., :half].astype(np.complex128) + 1j * x[..., half:]) * np.exp(1j * angle)
+    return np.concatenate([z.real, z.imag], axis=-1)
+
+
+def test_rotation_is_complex_multiplication():
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((64, 128))
+    ang = rng.uniform(-50, 50, (64, 64))
+    assert np.allclose(rope.rotate64(x, ang), _complex_rotate(x, ang), atol=1e-12, rtol=0)
+    # the fp32 table variant agrees to fp32 rounding
+    rt = rope.RopeTable("default", 128, 4096, base=10000.0)
+    pos = rng.integers(0, 4096, 64)
+    x32 = x.astype(F32)
+    got = rope.rotate(x32, rt.cos[pos], rt.sin[pos]).astype(np.float64)
+    ang32 = (pos.astype(F32)[:, None] * rt.inv_freq[None, :]).astype(F32).astype(np.float64)
+    want = _complex_rotate(x32.astype(np.float64), ang32)
+    assert np.allclose(got, want, atol=4e-6, rtol=4e-6)
+
+
+def test_position_zero_is_identity():
+    rt = rope.RopeTable("llama3", 64, 8, base=5e5, factor=32, low_freq_factor=1,
+                        high_freq_factor=4, original_max_position=8192)
+    x = np.random.default_rng(1).standard_normal((5, 64)).astype(np.float16)
+    assert np.array_equal(rt.apply(x, 0).view(np.uint16), x.view(np.uint16))
+    assert np.all(rt.cos[0] == 1) and np.all(rt.sin[0] == 0)
+
+
+def test_inverse_of_forward_is_identity():
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((32, 128))
+    ang = rng.uniform(-1e4, 1e4, (32, 64))
+    back = rope.rotate64(rope.rotate64(x, ang), ang, inverse=True)
+    assert np.allclose(back, x, atol=1e-13, rtol=0)
+    rt = rope.RopeTable("default", 128, 40000, base=5e5)
+    pos = rng.integers(0, 40000, 32)
+    x32 = x.astype(F32)
+    c, s = rt.cos[pos], rt.sin[pos]
+    back32 = rope.rotate(rope.rotate(x32, c, s), c, s, inverse=True)
+    ulp = np.spacing(np.abs(x32).max())
+    assert np.max(np.abs(back32 - x32)) <= 8 * ulp
+
+
+def test_pair_norms_preserved():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((16, 64))
+    y = rope.rotate64(x, rng.uniform(0, 100, (16, 32)))
+    n0 = x[:, :32] ** 2 + x[:, 32:] ** 2
+    n1 = y[:, :32] ** 2 + y[:, 32:] ** 2
+    assert np.allclose(n0, n1, rtol=1e-13, atol=0)
+
+
+def test_llama3_bands_closed_form():
+    d, base, L, factor, lf, hf = 64, 5e5, 8192, 32.0, 1.0, 4.0
+    default = rope.inv_freq("default", base, d)
+    l3 = rope.inv_freq("llama3", base, d, factor, lf, hf, L)
+    wl = 2 * math.pi / default.astype(np.float64)
+    high = wl < L / hf              # short wavelengths: unchanged
+    low = wl > L / lf               # long wavelengths: divided by the factor
+    assert high.any() and low.any() and (~high & ~low).any()
+    assert np.array_equal(l3[high], default[high])
+    ratio = default[low].astype(np.float64) / l3[low].astype(np.float64)
+    assert np.allclose(ratio, factor, rtol=2 ** -22)
+    # the mixed band lies strictly between the two unmixed values and is monotone in i
+    mid = ~high & ~low
+    assert np.all(l3[mid] < default[mid]) and np.all(l3[mid] > default[mid] / factor)
+    assert np.all(np.diff(l3.astype(np.float64)) < 0)
+
+
+def test_scores_depend_only_on_relative_distance():
+    rng = np.random.default_rng(4)
+    q, k = rng.standard_normal(128), rng.standard_normal(128)
+    inv = rope.inv_freq("default", 1e4, 128).astype(np.float64)
+    dot = lambda P, j: rope.rotate64(q, P * inv) @ rope.rotate64(k, j * inv)
+    for P, j, shift in [(100, 7, 13), (5000, 4000, -3000), (64, 64, 1000)]:
+        assert math.isclose(dot(P, j), dot(P + shift, j + shift), rel_tol=1e-9, abs_tol=1e-9)
+
+
+def test_reposition_matches_direct_rotation_to_fp16_rounding():
+    rng = np.random.default_rng(5)
+    rt = rope.RopeTable("default", 128, 40000, base=5e5)
+    x = rng.standard_normal((200, 128)).astype(np.float16)
+    old = rng.integers(1000, 40000, 200)
+    new = rng.integers(0, 1000, 200)
+    k_old = rt.apply(x, old)
+    k_new = rt.reposition(k_old.astype(F32), old, new)
+    direct = rt.apply(x, new)
+    diff = np.abs(k_new.astype(np.float64) - direct.astype(np.float64))
+    # two fp16 roundings on the way; a rotation mixes a pair, so the bound is a few fp16
+    # ulps of the pair's norm
+    dd = direct.astype(np.float64)
+    r = np.sqrt(dd[:, :64] ** 2 + dd[:, 64:] ** 2)
+    tol = 3 * np.spacing(r.astype(np.float16)).astype(np.float64) + 2.0 ** -24
+    tol = np.concatenate([tol, tol], axis=1)
+    assert np.all(diff <= tol)
