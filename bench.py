@@ -1,0 +1,391 @@
+#!/usr/bin/env python
+"""Decode-attention throughput of the FADE tiered KV cache on one GB300 per rank.
+
+Workload (default): the Llama-3-8B-shaped aggressive-mode sweep — 32 layers, batch 64,
+32 query / 8 KV heads, head_dim 128, 32768-token context per row, n_sink 4, recent window 64,
+middle tier INT4 K / INT2 V (group 32, fp16 scales), position eviction to int4_budget 4096.
+Synthetic seeded data (no weights, no dataset).
+
+A timed step is one pass of the whole hot path over all layers: RoPE of the step's q and k,
+demote + quantise-pack, evict + re-RoPE, append, split-KV decode attention + combine (and
+H2O/EMA accumulation for the policies that use it). ``value`` = batch x steps x ranks /
+(max over ranks of the device time of the timed steps). The compressed cache (8 GB) is far
+larger than L2, so no L2 flush is needed between steps.
+
+--impl reference runs the oracle (plain numpy CPU restatement of the method) on the same
+workload: each step is one full-size (layer, row, KV head) unit's decode step, scaled to a
+whole step by the number of units.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn tokens/s (batch×steps) and achieved HBM GB/s vs GB300 peak"
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="4")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def workload(key):
+    from synth import get_workload
+
+    return get_workload(int(key) if key.isdigit() else key)
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- bytes
+def attention_bytes(cfg, layer):
+    """Algorithmic bytes of one fade_decode_attention call: every held token once (middle at
+    its packed size with scales, FP16 tiers at 4d) plus q read and out written."""
+    d = cfg.head_dim
+    mid_tok = d * (cfg.middle_k_bits + cfg.middle_v_bits) // 8 + 2 * 2 * (d // 32)
+    units_fp16 = int((layer.h_n_sink + layer.h_n_recent).sum()) * cfg.num_kv_heads
+    units_mid = int(layer.h_n_mid.sum()) * cfg.num_kv_heads
+    return units_mid * mid_tok + units_fp16 * 4 * d + 2 * cfg.batch * cfg.num_q_heads * d * 2
+
+
+def evict_bytes(cfg, layer, n_ev=1):
+    """Algorithmic bytes of one steady-state fade_evict_rerope call: the middle tier (codes,
+    scales, scores) read once and its survivors written once to the other buffer, plus the
+    recent keys read and rewritten in place."""
+    d = cfg.head_dim
+    mid_tok = d * (cfg.middle_k_bits + cfg.middle_v_bits) // 8 + 2 * 2 * (d // 32) + 4
+    H = cfg.num_kv_heads
+    n_mid_after = int(layer.h_n_mid.sum())
+    read = (n_mid_after + n_ev * cfg.batch) * mid_tok * H
+    write = n_mid_after * mid_tok * H
+    rec = int(layer.h_n_recent.sum()) * H * d * 2 * 2
+    return read + write + rec
+
+
+def load_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+_CPU_SNIPPET = r"""
+import json, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+from oracle.cache import Params, UnitCache
+from oracle.rope import RopeTable
+from synth import draw_vectors, get_workload
+wl = get_workload({key!r})
+P = int({P})
+u = UnitCache(Params.from_workload(wl), RopeTable.from_workload(wl, P + 4096))
+k = draw_vectors(wl, "k", (P, wl.head_dim), "cpu_sample")
+v = draw_vectors(wl, "v", (P, wl.head_dim), "cpu_sample")
+u.prefill(k, v, mass=np.ones(P) if wl.policy == "h2o" else None)
+steps, warm, budget_s = {steps}, {warmup}, {budget_s}
+G = wl.group
+times = []
+i = 0
+t_start = time.perf_counter()
+while True:
+    q = draw_vectors(wl, "q", (G, wl.head_dim), "cpu_step", i)
+    kk = draw_vectors(wl, "k", (wl.head_dim,), "cpu_step", i)
+    vv = draw_vectors(wl, "v", (wl.head_dim,), "cpu_step", i)
+    t0 = time.perf_counter()
+    u.step(q, kk, vv)
+    dt = time.perf_counter() - t0
+    if i >= warm:
+        times.append(dt)
+    i += 1
+    if len(times) >= steps or (time.perf_counter() - t_start > budget_s and len(times) >= 1):
+        break
+print(json.dumps({{"unit_step_s": float(np.mean(times)), "n": len(times)}}))
+"""
+
+
+def run_oracle_sample(key, steps, warmup, budget_s=25.0):
+    wl = workload(key)
+    P = wl.ragged[1] if wl.ragged else wl.prompt_len
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = _CPU_SNIPPET.format(root=ROOT, key=key if not key.isdigit() else int(key), P=P,
+                               steps=steps, warmup=warmup, budget_s=budget_s)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError("oracle sample failed: " + r.stderr[-2000:])
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    units = wl.layers * wl.batch * wl.num_kv_heads
+    step_s = res["unit_step_s"] * units
+    return {
+        "value": wl.batch / step_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        "sample": (f"{res['n']} decode steps of one full-size (layer, row, KV head) unit "
+                   f"(prompt {P}); time x {units} units = one whole step"),
+        "ms_per_step": step_s * 1e3,
+    }
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_ours(args, rank, world):
+    import torch
+
+    from tiered_mixed_precision_gb300 import Config, build
+    from tiered_mixed_precision_gb300.model import FadeCache
+    from synth import draw_prompt, draw_vectors, ragged_context_lengths
+
+    build.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    wl = workload(args.workload)
+    if world > 1:
+        wl = wl.scaled(seed=wl.seed + 1000 * rank)   # weak scaling: each rank its own batch
+    cfg = Config.from_workload(wl)
+    lens = ragged_context_lengths(wl)
+    maxP = int(lens.max())
+    K, W = args.steps, args.warmup
+    nsteps = K + W + (K if not args.no_e2e else 0) + 1
+    max_pos = maxP + nsteps + 16
+    fc = FadeCache(cfg, wl.layers, maxP, max_pos, dev)
+    mass = None
+    for layer in range(wl.layers):
+        pr = draw_prompt(wl, layer, maxP, backend="torch", device=dev)
+        if wl.policy == "h2o" and wl.int4_budget >= 0:
+            mass = torch.ones((wl.batch, wl.num_kv_heads, maxP), dtype=torch.float32, device=dev)
+        fc.prefill(layer, pr["k"], pr["v"], lens, mass)
+        del pr
+    torch.cuda.synchronize()
+    L, B, Hq, Hkv, d = wl.layers, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+    q_all = draw_vectors(wl, "q", (K + W, L, B, Hq, d), "bench", backend="torch", device=dev)
+    k_all = draw_vectors(wl, "k", (K + W, L, B, Hkv, d), "bench", backend="torch", device=dev)
+    v_all = draw_vectors(wl, "v", (K + W, L, B, Hkv, d), "bench", backend="torch", device=dev)
+    out = torch.empty((L, B, Hq, d), dtype=torch.float16, device=dev)
+
+    def step(s):
+        fc.set_positions(fc.next_positions())
+        for layer in range(L):
+            fc.step_layer(layer, q_all[s, layer], k_all[s, layer], v_all[s, layer], out[layer])
+
+    for s in range(W):
+        step(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    fc.timers = {}
+    fc.launches = 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for s in range(W, W + K):
+        step(s)
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    launches = fc.launches
+    ms = e0.elapsed_time(e1)
+    ms_max = max_over_ranks(ms, world)
+    per_call = {name: [a.elapsed_time(b) for a, b in pairs] for name, pairs in fc.timers.items()}
+    fc.timers = None
+
+    # roofline of the attention call and of the eviction call
+    peaks = load_peaks()
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    peak_src = "measured" if peaks else "fallback"
+    lay0 = fc.layers[0]
+    rl = {}
+    attn_b = attention_bytes(cfg, lay0)
+    if "attention" in per_call:
+        t = float(np.mean(per_call["attention"])) / 1e3
+        rl["attention"] = {"bound": "hbm", "achieved": attn_b / t / 1e9, "peak": peak,
+                           "unit": "GB/s", "frac": attn_b / t / 1e9 / peak, "traffic": None,
+                           "bytes_per_launch": attn_b, "ms_per_launch": t * 1e3,
+                           "peak_source": peak_src, "time_share": sum(per_call["attention"]) / ms}
+    if "evict" in per_call:
+        eb = evict_bytes(cfg, lay0)
+        t = float(np.mean(per_call["evict"])) / 1e3
+        rl["evict_rerope"] = {"bound": "hbm", "achieved": eb / t / 1e9, "peak": peak,
+                              "unit": "GB/s", "frac": eb / t / 1e9 / peak, "traffic": None,
+                              "bytes_per_launch": eb, "ms_per_launch": t * 1e3,
+                              "peak_source": peak_src, "time_share": sum(per_call["evict"]) / ms}
+    dominant = max(rl, key=lambda n: rl[n]["time_share"]) if rl else None
+
+    # end to end: inputs copied from pinned host memory and outputs read back every step
+    e2e = None
+    if not args.no_e2e:
+        qh = q_all[W:].cpu().pin_memory()
+        kh = k_all[W:].cpu().pin_memory()
+        vh = v_all[W:].cpu().pin_memory()
+        oh = torch.empty((K, L, B, Hq, d), dtype=torch.float16).pin_memory()
+        qd, kd, vd = torch.empty_like(q_all[0]), torch.empty_like(k_all[0]), torch.empty_like(v_all[0])
+        torch.cuda.synchronize()
+        barrier(world)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record()
+        for s in range(K):
+            qd.copy_(qh[s], non_blocking=True)
+            kd.copy_(kh[s], non_blocking=True)
+            vd.copy_(vh[s], non_blocking=True)
+            fc.set_positions(fc.next_positions())
+            for layer in range(L):
+                fc.step_layer(layer, qd[layer], kd[layer], vd[layer], out[layer])
+            oh[s].copy_(out, non_blocking=True)
+        f1.record()
+        torch.cuda.synchronize()
+        ems = max_over_ranks(f0.elapsed_time(f1), world)
+        e2e = {"value": B * K * world / (ems / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(qd.nbytes + kd.nbytes + vd.nbytes),
+               "d2h_bytes_per_step": int(out.nbytes), "ms_per_step": ems / K}
+
+    value = B * K * world / (ms_max / 1e3)
+    res = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "layers": L, "batch": B, "num_q_heads": Hq,
+                   "num_kv_heads": Hkv, "head_dim": d, "context": maxP, "n_sink": wl.n_sink,
+                   "recent_window": wl.recent_window, "int4_budget": wl.int4_budget,
+                   "policy": wl.policy, "k_bits": wl.middle_k_bits, "v_bits": wl.middle_v_bits,
+                   "storage": "fp16 sinks/recent, packed INT4 K / INT2 V middle",
+                   "l2": "no flush: the compressed cache read per step is far larger than L2",
+                   "parallelism": f"replicas x{world} (rows independent, no collective)"},
+        "roofline": dict(rl[dominant], kernel=dominant) if dominant else None,
+        "roofline_by_call": rl,
+        "attention_only": {
+            "value": B * K * world / (sum(per_call.get("attention", [np.nan])) / 1e3),
+            "unit": "tokens/s", "gbs": rl.get("attention", {}).get("achieved")},
+        "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+    }
+    return res
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    if args.impl == "reference":
+        if rank == 0:
+            ref = run_oracle_sample(args.workload, args.steps, args.warmup)
+            wl = workload(args.workload)
+            line = {"impl": "reference", "metric": METRIC, "value": ref["value"],
+                    "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                    "warmup": args.warmup, "ms_per_step": ref["ms_per_step"],
+                    "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                    "dtype": "f64", "data": "synthetic",
+                    "config": {"workload": wl.name},
+                    "cpu_baseline": {k: ref[k] for k in ("value", "unit", "cores", "kind", "sample")},
+                    "e2e": {"value": ref["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}}
+            print(json.dumps(line), flush=True)
+        return
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            cb = run_oracle_sample(args.workload, steps=3, warmup=1, budget_s=20.0)
+            res["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,264 @@
+/*
+ * fade.h — C ABI of libfade: the decode-attention hot path of the FADE tiered KV cache on
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * Sources cited below:
+ *   FADE-zh  page "FADE：面向LLM推理的注意力感知分层KV缓存压缩技术"
+ *   FADE-en  page "FADE: Attention-Aware Hierarchical KV Cache Compression for LLM Inference"
+ *   KVLong   page "探秘Transformer系列之（25）--- KV Cache优化之处理长文本序列"
+ *
+ * The cache of one layer holds, per (row, KV head) "unit":
+ *   - FP16 sinks: the first n_sink tokens (FADE-zh §第一层);
+ *   - FP16 recent window: the last recent_window tokens, stored as a ring (FADE-zh §第一层);
+ *   - the middle tier: symmetric absmax codes, K at middle_k_bits and V at middle_v_bits
+ *     (4 or 2), one fp16 scale per 32 channels, packed little-endian into bytes
+ *     (FADE-zh §第二层, §第三层, §量化与Bit-Packing), in two buffers used alternately by
+ *     eviction (live buffer = meta field CUR);
+ *   - one fp32 importance score per held token (FADE-zh §四种驱逐策略详解).
+ * Keys are stored RoPE'd at their cache index (StreamingLLM positions, KVLong §1.2.2).
+ *
+ * Conventions for every call:
+ *   - All device memory is allocated and owned by the caller; sizes come from fade_layout().
+ *     The library allocates no device memory and keeps no global state except the
+ *     thread-local error string.
+ *   - Calls are asynchronous on the given stream (cudaStream_t passed as void*; NULL = the
+ *     legacy default stream). Argument, shape and capacity errors are detected on the host
+ *     before any launch and returned synchronously; nothing is enqueued then. A launch
+ *     failure returns FADE_ERR_CUDA. fade_last_error() describes the last failure of the
+ *     calling thread.
+ *   - fp16 data is passed as raw IEEE binary16 (uint16 bits). Row-major layouts throughout.
+ *   - The host keeps a mirror of per-row tier counts in the fade_layer_t (h_* arrays); each
+ *     call updates it as it enqueues work, so the caller never synchronises to learn sizes.
+ *   - Kernels never trap or spin: all waits in the library are stream order.
+ */
+#ifndef FADE_H_
+#define FADE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FADE_OK = 0,
+  FADE_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad shape, out-of-range value */
+  FADE_ERR_UNSUPPORTED = 2,      /* a valid configuration this build does not implement */
+  FADE_ERR_CAPACITY = 3,         /* a tier or workspace would overflow its buffer */
+  FADE_ERR_CUDA = 4              /* a CUDA call or kernel launch failed */
+} fade_status_t;
+
+/* RoPE schemes (FADE-zh §RoPE方案兼容性). NONE: positions are not encoded in K (ALiBi
+ * models), so re-positioning is the identity. */
+typedef enum { FADE_ROPE_NONE = 0, FADE_ROPE_DEFAULT = 1, FADE_ROPE_LLAMA3 = 2 } fade_rope_kind_t;
+
+/* Eviction policies (FADE-zh §四种驱逐策略详解 1-3). NONE = safe mode (no eviction). */
+typedef enum {
+  FADE_EVICT_NONE = 0,
+  FADE_EVICT_H2O = 1,
+  FADE_EVICT_EMA = 2,
+  FADE_EVICT_POSITION = 3
+} fade_policy_t;
+
+typedef struct {
+  int32_t kind;                  /* fade_rope_kind_t */
+  int32_t original_max_position; /* llama3 only */
+  double base;                   /* theta base, e.g. 10000, 500000 */
+  double factor;                 /* llama3 only */
+  double low_freq_factor;        /* llama3 only */
+  double high_freq_factor;       /* llama3 only */
+} fade_rope_t;
+
+/* One layer's cache configuration (FADE-zh §自定义配置: n_sink, recent_window, int4_budget,
+ * eviction_policy, middle_k_bits, middle_v_bits). */
+typedef struct {
+  int32_t batch;          /* rows, 1..FADE_MAX_BATCH; fixed for the cache's lifetime */
+  int32_t num_q_heads;    /* Hq; a multiple of num_kv_heads, Hq/Hkv <= 8 */
+  int32_t num_kv_heads;   /* Hkv */
+  int32_t head_dim;       /* d: 64 or 128 */
+  int32_t n_sink;         /* FP16 sink tokens kept per unit, >= 0 */
+  int32_t recent_window;  /* FP16 recent tokens kept per unit, >= 1 */
+  int32_t int4_budget;    /* middle tokens kept per unit when evicting; < 0: unbounded */
+  int32_t middle_k_bits;  /* 4 (2 is accepted too) */
+  int32_t middle_v_bits;  /* 2 or 4 */
+  int32_t mid_capacity;   /* middle slots allocated per unit (>= budget + 1 when evicting) */
+  int32_t policy;         /* fade_policy_t */
+  float ema_decay;        /* EMA decay delta in [0, 1) */
+  fade_rope_t rope;
+} fade_config_t;
+
+#define FADE_MAX_BATCH 256
+#define FADE_GROUP 32
+
+/* Per-unit device metadata: int32 [batch][num_kv_heads][FADE_META_FIELDS]. */
+enum {
+  FADE_META_N_SINK = 0,   /* sinks held */
+  FADE_META_N_MID = 1,    /* middle tokens held (slots 0..N_MID-1 of buffer CUR) */
+  FADE_META_N_RECENT = 2, /* recent tokens held */
+  FADE_META_HEAD = 3,     /* ring slot of the oldest recent token */
+  FADE_META_CUR = 4,      /* live middle buffer, 0 or 1 */
+  FADE_META_N_EV = 5,     /* evictions chosen and not yet committed (internal) */
+  FADE_META_P0 = 6,       /* internal (prefill) */
+  FADE_META_P1 = 7,       /* internal (prefill) */
+  FADE_META_FIELDS = 8
+};
+
+/* Caller-owned buffers of one layer. Device pointers unless marked host. Shapes use
+ * B = batch, H = num_kv_heads, S = n_sink, W = recent_window, C = mid_capacity, d. */
+typedef struct {
+  uint16_t* sink_k;          /* fp16 [B][H][S][d] */
+  uint16_t* sink_v;          /* fp16 [B][H][S][d] */
+  uint16_t* recent_k;        /* fp16 [B][H][W][d], ring */
+  uint16_t* recent_v;        /* fp16 [B][H][W][d], ring */
+  uint8_t* mid_k_codes[2];   /* u8 [B][H][C][d*middle_k_bits/8] */
+  uint16_t* mid_k_scales[2]; /* fp16 [B][H][C][d/32] */
+  uint8_t* mid_v_codes[2];   /* u8 [B][H][C][d*middle_v_bits/8] */
+  uint16_t* mid_v_scales[2]; /* fp16 [B][H][C][d/32] */
+  float* sink_scores;        /* f32 [B][H][S] */
+  float* mid_scores[2];      /* f32 [B][H][C] */
+  float* recent_scores;      /* f32 [B][H][W], indexed by ring slot */
+  int32_t* meta;             /* i32 [B][H][FADE_META_FIELDS] */
+  uint32_t* victims;         /* scratch: u32 [B][H][victim_words] */
+  int32_t* chunk_base;       /* scratch: i32 [B][H][chunk_slots] */
+  int32_t victim_words;      /* from fade_layout_t: sizes the longest prompt / middle tier */
+  int32_t chunk_slots;       /* from fade_layout_t */
+  int32_t* h_n_sink;         /* HOST i32 [B]: mirror of N_SINK (same for every head) */
+  int32_t* h_n_mid;          /* HOST i32 [B]: mirror of N_MID */
+  int32_t* h_n_recent;       /* HOST i32 [B]: mirror of N_RECENT */
+} fade_layer_t;
+
+/* Byte sizes of every buffer of a layer and of the per-call workspaces. */
+typedef struct {
+  size_t sink_k, sink_v, recent_k, recent_v;
+  size_t mid_k_codes, mid_k_scales, mid_v_codes, mid_v_scales; /* each of the two buffers */
+  size_t sink_scores, mid_scores, recent_scores, meta, victims, chunk_base;
+  size_t logits_ws;   /* f32 [B][Hq][S + C + W]: per-token logits for H2O / EMA */
+  size_t ml_ws;       /* f32 [B][Hq][2]: final (max, sum) of each query head's softmax */
+  size_t attn_ws;     /* split-KV partials for fade_decode_attention */
+  int32_t victim_words;  /* u32 words per unit in `victims` */
+  int32_t chunk_slots;   /* i32 entries per unit in `chunk_base` */
+  int32_t max_prompt;    /* the prompt length the scratch sizes were computed for */
+  int32_t max_splits;    /* split-KV partial slots per (row, query head) */
+} fade_layout_t;
+
+/* Validate `cfg` and return the sizes of a layer's buffers for prompts of up to
+ * `max_prompt` tokens per row. Host only, no CUDA calls. */
+fade_status_t fade_layout(const fade_config_t* cfg, int32_t max_prompt, fade_layout_t* out);
+
+/* RoPE table (FADE-zh §RoPE重计算: float32 RoPE math; FADE-zh §RoPE方案兼容性: default and
+ * llama3 scaling). Writes table[pos][i] = (cos, sin) as f32 pairs, [max_pos][d/2][2], for
+ * angle = fp32(pos) * inv_freq_i (one fp32 multiply), inv_freq_i = base^(-2i/d) in fp64
+ * (llama3-adjusted in fp64) rounded to fp32, cos/sin evaluated in fp64 and rounded to fp32.
+ * `table` is device memory of max_pos*d*4 bytes. Not valid for FADE_ROPE_NONE. */
+fade_status_t fade_rope_table_init(const fade_config_t* cfg, float* table, int32_t max_pos,
+                                   void* stream);
+
+/* Rotate fp16 vectors to their positions (the model's RoPE of q and k; KVLong §1.2.2: the
+ * position of a token is its index in the cache). x, y: fp16 [n_groups][group_len][d]
+ * (y may alias x). Vector j of group g is rotated to position
+ * (pos_start ? pos_start[g] : 0) + j * pos_step, with pos_start a device i32 [n_groups].
+ * Rotation pairs channel i with i + d/2; every product and sum is rounded to fp32 (no fused
+ * multiply-add); the result is rounded to fp16. Positions must lie in [0, max_pos). */
+fade_status_t fade_rope_apply(const fade_config_t* cfg, const float* table, int32_t max_pos,
+                              const uint16_t* x, uint16_t* y, int64_t n_groups,
+                              int32_t group_len, const int32_t* pos_start, int32_t pos_step,
+                              void* stream);
+
+/* Quantise and pack (FADE-zh §量化与Bit-Packing: symmetric quantisation with bit-packing).
+ * x: fp16 [n_vec][dim], dim a multiple of 32. Per 32-channel group: a = max|x|,
+ * s = fp16(a / qmax) with qmax = 2^(bits-1)-1 (fp32 IEEE division, round to nearest even);
+ * s = 2^-24 if a > 0 and s rounds to 0; q = clamp(rint(x / s), -qmax, qmax) (fp32
+ * division, ties to even), 0 when a = 0. codes: u8 [n_vec][dim*bits/8], INT4 byte j =
+ * q[2j] | q[2j+1] << 4, INT2 byte j = sum_r q[4j+r] << 2r, two's complement fields.
+ * scales: fp16 [n_vec][dim/32]. bits is 2 or 4. */
+fade_status_t fade_quantize_pack(const uint16_t* x, int64_t n_vec, int32_t dim, int32_t bits,
+                                 uint8_t* codes, uint16_t* scales, void* stream);
+
+/* Inverse codec: out[n][c] = q * s as f32 (exact). Same layouts as fade_quantize_pack. */
+fade_status_t fade_dequantize(const uint8_t* codes, const uint16_t* scales, int64_t n_vec,
+                              int32_t dim, int32_t bits, float* out, void* stream);
+
+/* Empty the cache: zero the device metadata and the host mirror. */
+fade_status_t fade_cache_reset(const fade_config_t* cfg, fade_layer_t* layer, void* stream);
+
+/* Build the tiers from a prompt (FADE-zh §核心机制, §驱逐策略, §四种驱逐策略详解 1: H2O
+ * scores come from prefill attention). k_rot: fp16 [B][H][max_prompt][d], already RoPE'd
+ * at positions 0..P-1; v: fp16 [B][H][max_prompt][d]; h_prompt_len: HOST i32 [B] with
+ * row lengths P (<= max_prompt). Sinks = first n_sink tokens, recent = last recent_window,
+ * the rest are middle candidates. When the candidates exceed int4_budget and the policy
+ * evicts, the excess with the smallest (key, index) is dropped: key = mass (H2O), 0 (EMA,
+ * so the oldest go first) or the index (position). Survivors are re-positioned in fp32 to
+ * contiguous indices and cast to fp16; the middle tier is then quantised once. H2O scores
+ * start at the survivors' mass (mass: device f32 [B][H][max_prompt], required for H2O,
+ * ignored otherwise); other scores start at 0. The cache must be empty (after reset).
+ * `table` may be NULL only for FADE_ROPE_NONE. Uses the layer's scratch buffers. */
+fade_status_t fade_cache_prefill(const fade_config_t* cfg, fade_layer_t* layer,
+                                 const uint16_t* k_rot, const uint16_t* v,
+                                 int32_t max_prompt, const int32_t* h_prompt_len,
+                                 const float* mass, const float* table, int32_t max_pos,
+                                 void* stream);
+
+/* Demote (FADE-zh §第二层: mid-aged tokens go to the quantised tier): in every unit whose
+ * recent window is full, the oldest recent token is quantise-packed (K at middle_k_bits, V
+ * at middle_v_bits) into the next middle slot of the live buffer and its score moves with
+ * it; its cache index is unchanged. FADE_ERR_CAPACITY if a middle slot would overflow. */
+fade_status_t fade_cache_demote(const fade_config_t* cfg, fade_layer_t* layer, void* stream);
+
+/* Evict and re-position (FADE-zh §驱逐策略: on reaching INT4_BUDGET tokens are evicted and
+ * keys are un-RoPE'd at the old position and re-RoPE'd at the contiguous StreamingLLM
+ * position; FADE-zh §RoPE重计算: fp32 math, cast through fp16; FADE-zh §四种驱逐策略详解).
+ * In every unit holding more than int4_budget middle tokens, the excess middle tokens with
+ * the smallest key (score, index) — (index) for the position policy — are dropped (equal
+ * scores: the lower index goes first). Survivors are compacted into the other middle
+ * buffer, which becomes live; every survivor whose index drops is re-positioned: a middle
+ * key is dequantised, rotated back from its old index and forward to its new one in fp32,
+ * cast to fp16 and re-quantised; recent keys are re-positioned in place; V codes, V scales
+ * and scores move unchanged. A no-op for FADE_EVICT_NONE or a negative budget. */
+fade_status_t fade_evict_rerope(const fade_config_t* cfg, fade_layer_t* layer,
+                                const float* table, int32_t max_pos, void* stream);
+
+/* Append (FADE-zh §第一层): the new token of every unit: k_rot, v fp16 [B][H][d], the key
+ * already RoPE'd at fade_next_position(). It becomes a sink while fewer than n_sink sinks
+ * are held, else the newest recent token; its score starts at 0. FADE_ERR_CAPACITY if the
+ * recent window is full (demote first). */
+fade_status_t fade_cache_append(const fade_config_t* cfg, fade_layer_t* layer,
+                                const uint16_t* k_rot, const uint16_t* v, void* stream);
+
+/* Decode attention (FADE-zh §项目结构与代码质量, kernels/: fused INT4 dequant + SDPA; KVLong
+ * §1.2: softmax-weighted average of V). q_rot: fp16 [B][Hq][d] RoPE'd at the new token's
+ * position; out: fp16 [B][Hq][d]. Every query head h attends, with scale 1/sqrt(d), to
+ * every token held by its KV head h / (Hq/Hkv): sinks, middle (dequantised in registers)
+ * and recent. Split-KV over SMs: partials go to `ws` (ws_bytes >= fade_layout().attn_ws),
+ * then a combine writes out and ml_ws = f32 [B][Hq][2] (max logit M, sum L of exp(s - M)).
+ * If logits_ws is not NULL (f32 [B][Hq][S + C + W]) the scaled logits s are stored at the
+ * token's storage slot: sink i at i, middle slot m at S + m, ring slot r at S + C + r. */
+fade_status_t fade_decode_attention(const fade_config_t* cfg, const fade_layer_t* layer,
+                                    const uint16_t* q_rot, uint16_t* out, float* logits_ws,
+                                    float* ml_ws, void* ws, size_t ws_bytes, void* stream);
+
+/* Accumulate attention mass (FADE-zh §四种驱逐策略详解 1 H2O, 2 EMA; KVLong §1.3.1 H2O: the
+ * score of a token sums its attention). With p[h][j] = exp(s[h][j] - M[h]) / L[h] from the
+ * preceding fade_decode_attention's logits_ws and ml_ws: H2O adds sum over the unit's query
+ * heads of p to every held token's score; EMA sets score = delta*score + (1-delta)*sum p.
+ * A no-op for the position and none policies. */
+fade_status_t fade_h2o_accumulate(const fade_config_t* cfg, fade_layer_t* layer,
+                                  const float* logits_ws, const float* ml_ws, void* stream);
+
+/* Host: cache position of row `row`'s next token = held tokens after the next step's
+ * demotion and eviction (KVLong §1.2.2: positions inside the cache). -1 on bad arguments. */
+int32_t fade_next_position(const fade_config_t* cfg, const fade_layer_t* layer, int32_t row);
+
+/* Host: KV bytes held by the layer (FADE-zh §使用注意事项 3, compressed_storage_bytes: KV
+ * storage only): FP16 tokens at 4d bytes, middle tokens at d*(kb+vb)/8 code bytes plus two
+ * fp16 scales per 32 channels. */
+uint64_t fade_compressed_bytes(const fade_config_t* cfg, const fade_layer_t* layer);
+
+/* The calling thread's last error message ("" if none). */
+const char* fade_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FADE_H_ */

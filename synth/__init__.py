@@ -8,6 +8,8 @@ bytes without sharing any method code.
 
 from .workloads import WORKLOADS, Workload, get_workload  # noqa: F401
 from .draws import (  # noqa: F401
+    draw_codec_cases,
+    draw_mass_like,
     draw_decode_tokens,
     draw_prompt,
     draw_scores,

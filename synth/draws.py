@@ -147,3 +147,28 @@ def draw_mass_like(shape, seed: int) -> np.ndarray:
     """Positive fp32 values shaped like accumulated attention mass (for prefill tests)."""
     rng = np.random.Generator(np.random.PCG64(_seed(seed, _KINDS["mass"])))
     return rng.gamma(0.5, 2.0, size=shape).astype(np.float32)
+
+
+def draw_codec_cases(n_vec: int, dim: int, seed: int) -> np.ndarray:
+    """fp16 [n_vec][dim] vectors for codec tests: seeded N(0,1) rows with outlier channels,
+    plus rows that exercise the edge cases of an absmax grid: an all-zero group, a group
+    holding only the smallest subnormal, a group whose largest magnitude is 7 (so that with
+    INT4 the step is exactly 1 and the other entries sit on half-integers), negative zeros,
+    and values near the fp16 maximum."""
+    rng = np.random.Generator(np.random.PCG64(_seed(seed, _KINDS["x"], n_vec, dim)))
+    x = rng.standard_normal((n_vec, dim), dtype=np.float32)
+    x[:, rng.integers(0, dim)] *= 10.0
+    x = x.astype(np.float16)
+    specials = []
+    z = np.zeros(dim, np.float16)
+    specials.append(z.copy())                                   # all zero
+    r = z.copy(); r[min(3, dim - 1)] = np.float16(2.0 ** -24); specials.append(r)
+    r = np.array([7.0] + [(k % 13) - 6.0 + 0.5 for k in range(31)], np.float16)
+    specials.append(np.tile(r, dim // 32)[:dim])                # half-integer steps
+    r = -np.zeros(dim, np.float16); r[0] = np.float16(1.0); specials.append(r)
+    r = rng.uniform(-65504, 65504, dim).astype(np.float16); specials.append(r)
+    r = (rng.standard_normal(dim) * 1e-6).astype(np.float16); specials.append(r)
+    for i, s in enumerate(specials):
+        if i < n_vec:
+            x[(i * 7919) % n_vec] = s
+    return x

@@ -1,0 +1,192 @@
+"""Lockstep runner for parity tests: the CUDA path (through the C ABI) and the oracle step the
+same seeded workload and are compared after every call.
+
+Both sides start from the same raw fp16 draws (``synth``). The oracle never reads anything the
+CUDA path produced; the only value passed from the oracle to the CUDA path is the H2O prefill
+mass, an input of the prefill call that the oracle computes (rounded to fp32 and given to both
+sides so their selections see identical keys).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+from oracle import attention, quant
+from oracle.cache import Params, UnitCache
+from oracle.rope import RopeTable
+from synth import draw_decode_tokens, draw_prompt, ragged_context_lengths
+
+ATOL, RTOL = 2e-3, 1e-2          # the spec's attention / score tolerance (allclose form)
+TIE_RTOL = 1e-5                  # fp32-vs-fp64 score noise that may flip a near-tie
+
+
+def allclose_report(got, ref, atol=ATOL, rtol=RTOL):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = np.abs(got - ref)
+    bad = err > atol + rtol * np.abs(ref)
+    return (not bad.any()), float(err.max(initial=0.0)), int(bad.sum())
+
+
+class Lockstep:
+    """Drives ``FadeCache`` and per-unit oracle caches over a workload."""
+
+    def __init__(self, wl, layers=None, steps=None, device="cuda", mid_capacity=None):
+        import torch
+
+        from tiered_mixed_precision_gb300 import Config
+        from tiered_mixed_precision_gb300.model import FadeCache
+
+        self.torch = torch
+        self.wl = wl
+        self.L = wl.layers if layers is None else layers
+        self.steps = wl.steps if steps is None else steps
+        self.lens = ragged_context_lengths(wl)
+        self.maxP = int(self.lens.max())
+        self.max_pos = self.maxP + self.steps + 8
+        self.cfg = Config.from_workload(wl, mid_capacity=mid_capacity)
+        self.fc = FadeCache(self.cfg, self.L, self.maxP, self.max_pos, device)
+        self.params = Params.from_workload(wl)
+        self.rope = RopeTable.from_workload(wl, self.max_pos)
+        B, H = wl.batch, wl.num_kv_heads
+        self.units = [[[UnitCache(self.params, self.rope) for _ in range(H)] for _ in range(B)]
+                      for _ in range(self.L)]
+        self.diverged = set()            # (layer, row, head) after a near-tie selection flip
+        self.near_ties = 0
+        self.step_index = 0
+
+    # -------------------------------------------------------------------- prefill
+    def prefill_mass32(self, pr, b, h):
+        """fp32 H2O prefill mass of unit (b, h), computed by the oracle."""
+        wl, G, P = self.wl, self.wl.group, int(self.lens[b])
+        pos = np.arange(P)
+        q = np.stack([self.rope.apply(pr["q"][b, h * G + g, :P], pos) for g in range(G)])
+        k = self.rope.apply(pr["k"][b, h, :P], pos)
+        return attention.prefill_mass(q.astype(np.float64), k.astype(np.float64)).astype(np.float32)
+
+    def prefill(self, layer):
+        torch = self.torch
+        wl = self.wl
+        h2o = wl.policy == "h2o" and wl.int4_budget >= 0
+        pr = draw_prompt(wl, layer, self.maxP, with_q=h2o)
+        mass = None
+        if h2o:
+            mass = np.zeros((wl.batch, wl.num_kv_heads, self.maxP), np.float32)
+            for b in range(wl.batch):
+                for h in range(wl.num_kv_heads):
+                    mass[b, h, :self.lens[b]] = self.prefill_mass32(pr, b, h)
+        dev = self.fc.device
+        k = torch.from_numpy(pr["k"]).to(dev)
+        v = torch.from_numpy(pr["v"]).to(dev)
+        md = torch.from_numpy(mass).to(dev) if mass is not None else None
+        self.fc.prefill(layer, k, v, self.lens, md)
+        for b in range(wl.batch):
+            P = int(self.lens[b])
+            for h in range(wl.num_kv_heads):
+                u = self.units[layer][b][h]
+                u.prefill(pr["k"][b, h, :P], pr["v"][b, h, :P],
+                          mass=None if mass is None else mass[b, h, :P].astype(np.float64))
+
+    # -------------------------------------------------------------------- decode
+    def step(self, check_state=True):
+        """One decode step of every layer; returns the max attention error seen."""
+        torch = self.torch
+        wl, G = self.wl, self.wl.group
+        pos = self.fc.next_positions()
+        for b in range(wl.batch):
+            want = self.units[0][b][0].next_position()
+            assert pos[b] == want, f"row {b}: next position {pos[b]} != oracle {want}"
+        self.fc.set_positions(pos)
+        worst = 0.0
+        for layer in range(self.L):
+            t = draw_decode_tokens(wl, layer, self.step_index)
+            dev = self.fc.device
+            q = torch.from_numpy(t["q"].copy()).to(dev)
+            k = torch.from_numpy(t["k"].copy()).to(dev)
+            v = torch.from_numpy(t["v"].copy()).to(dev)
+            out = torch.empty_like(q)
+            self.fc.step_layer(layer, q, k, v, out)
+            victims_gpu = self._gpu_victims(layer)
+            out_h = out.float().cpu().numpy()
+            for b in range(wl.batch):
+                for h in range(wl.num_kv_heads):
+                    key = (layer, b, h)
+                    u = self.units[layer][b][h]
+                    o_ref, tie = self._oracle_step(u, t, b, h, victims_gpu, key)
+                    if key in self.diverged:
+                        continue
+                    ok, err, nbad = allclose_report(out_h[b, h * G:(h + 1) * G], o_ref)
+                    worst = max(worst, err)
+                    assert ok, (f"attention mismatch at step {self.step_index} layer {layer} "
+                                f"row {b} head {h}: max err {err}, {nbad} bad")
+            if check_state:
+                self.check_layer_state(layer)
+        self.step_index += 1
+        return worst
+
+    def _gpu_victims(self, layer):
+        """Victim middle indices chosen by the CUDA path in this step (per unit), read from
+        its selection bitmap, or None for units without an eviction."""
+        return self.fc.layers[layer].victims.cpu().numpy().view(np.uint32)
+
+    def _oracle_step(self, u, t, b, h, bm, key):
+        G = self.wl.group
+        u.demote()
+        n_mid = u.n_mid
+        vic = u.choose_victims()
+        tie = False
+        if vic.size and self.wl.policy in ("h2o", "ema") and key not in self.diverged:
+            words = bm[b, h, :(n_mid + 31) // 32]
+            bits = np.unpackbits(words.view(np.uint8), bitorder="little")[:n_mid]
+            gpu_vic = np.nonzero(bits)[0]
+            if not np.array_equal(np.sort(gpu_vic), np.sort(vic)):
+                keys = u.sigma[u.n_sink:u.n_sink + n_mid]
+                a, g = np.sort(keys[vic]), np.sort(keys[gpu_vic])
+                assert gpu_vic.size == vic.size and np.allclose(
+                    a, g, rtol=TIE_RTOL, atol=1e-7), (
+                    f"selection differs beyond a near-tie at {key}: oracle {vic} {a}, "
+                    f"gpu {gpu_vic} {g}")
+                self.diverged.add(key)
+                self.near_ties += 1
+                tie = True
+        u.evict(vic)
+        pos = u.n_held
+        u.append(u.rope.apply(t["k"][b, h][None], pos), t["v"][b, h])
+        out, p, _ = u.attend(u.rope.apply(t["q"][b, h * G:(h + 1) * G], pos))
+        u.accumulate(p)
+        return out, tie
+
+    # -------------------------------------------------------------------- state
+    def check_layer_state(self, layer):
+        wl = self.wl
+        for b in range(wl.batch):
+            for h in range(wl.num_kv_heads):
+                if (layer, b, h) in self.diverged:
+                    continue
+                self.check_unit_state(layer, b, h)
+
+    def check_unit_state(self, layer, b, h):
+        g = self.fc.unit_state(layer, b, h)
+        u = self.units[layer][b][h]
+        where = f"layer {layer} row {b} head {h} step {self.step_index}"
+        assert (g["n_sink"], g["n_mid"], g["n_recent"]) == (u.n_sink, u.n_mid, u.n_recent), \
+            f"tier counts differ at {where}: gpu {(g['n_sink'], g['n_mid'], g['n_recent'])} " \
+            f"oracle {(u.n_sink, u.n_mid, u.n_recent)}"
+        eq16 = lambda a, r: np.array_equal(np.asarray(a).view(np.uint16), np.asarray(r).view(np.uint16))
+        assert eq16(g["sink_k"], u.sink_k) and eq16(g["sink_v"], u.sink_v), f"sinks differ at {where}"
+        assert eq16(g["recent_v"], u.rec_v), f"recent V differs at {where}"
+        if not eq16(g["recent_k"], u.rec_k):
+            d = np.nonzero(g["recent_k"].view(np.uint16) != u.rec_k.view(np.uint16))
+            raise AssertionError(f"recent K differs at {where}: {len(d[0])} entries, first {d[0][:5]}")
+        kc = quant.pack(u.mid_kq, u.p.k_bits)
+        vc = quant.pack(u.mid_vq, u.p.v_bits)
+        for name, got, ref in (("mid K codes", g["mid_k_codes"], kc),
+                               ("mid V codes", g["mid_v_codes"], vc)):
+            if not np.array_equal(got, ref):
+                rows = np.nonzero((got != ref).any(-1))[0]
+                raise AssertionError(f"{name} differ at {where}: rows {rows[:8]} of {len(rows)}")
+        assert eq16(g["mid_k_scales"], u.mid_ks), f"mid K scales differ at {where}"
+        assert eq16(g["mid_v_scales"], u.mid_vs), f"mid V scales differ at {where}"
+        if self.wl.policy in ("h2o", "ema"):
+            ok, err, nbad = allclose_report(g["scores"], u.sigma)
+            assert ok, f"scores differ at {where}: max err {err}, {nbad} bad"

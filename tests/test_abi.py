@@ -1,0 +1,124 @@
+"""The C ABI without a GPU: the library builds and loads, every declared entry point is
+exported, host-side validation returns the documented errors, and the host-only queries agree
+with the oracle's accounting and step schedule."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fade.h")
+
+
+@pytest.fixture(scope="module")
+def T():
+    import torch  # noqa: F401  (loads the CUDA runtime the library links against)
+
+    from tiered_mixed_precision_gb300 import build
+
+    build.build()
+    import tiered_mixed_precision_gb300 as T
+
+    return T
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fade_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(T):
+    names = declared_functions()
+    assert len(names) >= 15
+    lib = ctypes.CDLL(T.fade.LIB_PATH)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported: {missing}"
+
+
+def _cfg(T, **kw):
+    base = dict(batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128, n_sink=4,
+                recent_window=64, int4_budget=400, middle_k_bits=4, middle_v_bits=2,
+                mid_capacity=401, policy="h2o")
+    base.update(kw)
+    return T.Config(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=96), 2),
+    (dict(num_q_heads=6), 2),
+    (dict(num_q_heads=7), 1),
+    (dict(middle_v_bits=3), 2),
+    (dict(mid_capacity=400), 3),
+    (dict(ema_decay=1.0), 1),
+    (dict(recent_window=0), 1),
+    (dict(batch=0), 1),
+    (dict(batch=257), 1),
+    (dict(rope_base=1.0), 1),
+    (dict(rope_kind="llama3", rope_low_freq_factor=4.0, rope_high_freq_factor=1.0), 1),
+])
+def test_invalid_configs_are_rejected_on_the_host(T, kw, status):
+    with pytest.raises(T.FadeError) as e:
+        T.fade_layout(_cfg(T, **kw), 1024)
+    assert e.value.status == status
+    assert T.fade_last_error()
+
+
+def test_layout_sizes(T):
+    c = _cfg(T)
+    lay = T.fade_layout(c, 2048)
+    units = 2 * 2
+    assert lay.mid_k_codes == units * 401 * 64
+    assert lay.mid_v_codes == units * 401 * 32
+    assert lay.mid_k_scales == units * 401 * 4 * 2
+    assert lay.sink_k == units * 4 * 128 * 2
+    assert lay.recent_k == units * 64 * 128 * 2
+    assert lay.logits_ws == 2 * 8 * (4 + 401 + 64) * 4
+    assert lay.victim_words >= 2048 // 32 + 1
+
+
+def test_null_pointers_rejected_before_any_launch(T):
+    class S:  # a stream object whose handle is never used
+        cuda_stream = 0
+    with pytest.raises(T.FadeError) as e:
+        T.fade_quantize_pack(None, 4, 64, 4, None, None, stream=S())
+    assert e.value.status == 1
+    with pytest.raises(T.FadeError):
+        T.fade_dequantize(None, None, 4, 64, 2, None, stream=S())
+
+
+def test_next_position_and_compressed_bytes_follow_the_oracle(T):
+    """Host mirror queries, on a layer object holding host memory only."""
+    from oracle import accounting
+    from oracle.cache import Params, UnitCache
+    from oracle.rope import RopeTable
+    from synth import Workload, draw_decode_tokens, draw_prompt
+
+    wl = Workload(name="t", layers=1, batch=1, num_q_heads=4, num_kv_heads=1, head_dim=64,
+                  n_sink=2, recent_window=4, int4_budget=3, policy="position", middle_k_bits=4,
+                  middle_v_bits=2, prompt_len=9, steps=12, seed=3)
+    cfg = T.Config.from_workload(wl)
+    layer = T.TieredLayer(cfg, 16, device="cpu")
+    u = UnitCache(Params.from_workload(wl), RopeTable.from_workload(wl, 64))
+    u.prefill(draw_prompt(wl, 0)["k"][0, 0], draw_prompt(wl, 0)["v"][0, 0])
+    for step in range(12):
+        layer.h_n_sink[0], layer.h_n_mid[0], layer.h_n_recent[0] = u.n_sink, u.n_mid, u.n_recent
+        assert T.fade_next_position(layer, 0) == u.next_position()
+        want = accounting.unit_bytes(64, u.n_sink + u.n_recent, u.n_mid, 4, 2)
+        assert T.fade_compressed_bytes(layer) == want
+        t = draw_decode_tokens(wl, 0, step)
+        u.step(t["q"][0], t["k"][0, 0], t["v"][0, 0])
+    with pytest.raises(T.FadeError):
+        T.fade_next_position(layer, 5)
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    import tiered_mixed_precision_gb300.fade as F
+
+    monkeypatch.setattr(F, "_lib", None)
+    monkeypatch.setattr(F, "LIB_PATH", "/nonexistent/libfade.so")
+    with pytest.raises(ImportError):
+        F.lib()

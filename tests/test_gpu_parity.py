@@ -1,0 +1,120 @@
+"""Parity of the CUDA path (through the C ABI) with the oracle on seeded inputs."""
+
+import numpy as np
+import pytest
+
+from harness import Lockstep, allclose_report
+from oracle import quant
+from oracle.rope import RopeTable
+from synth import draw_codec_cases, get_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def T():
+    import torch  # noqa: F401
+
+    import tiered_mixed_precision_gb300 as T
+
+    T.lib()
+    return T
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("dim", [64, 128])
+@pytest.mark.parametrize("n", [1, 7, 1029])
+def test_quantize_pack_and_dequantize_bit_exact(T, bits, dim, n):
+    import torch
+
+    x = draw_codec_cases(n, dim, seed=bits * 1000 + dim + n)
+    xd = torch.from_numpy(x).cuda()
+    codes = torch.zeros((n, dim * bits // 8), dtype=torch.uint8, device="cuda")
+    scales = torch.zeros((n, dim // 32), dtype=torch.float16, device="cuda")
+    T.fade_quantize_pack(xd, n, dim, bits, codes, scales)
+    rc, rs = quant.quantize_pack(x, bits)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint16), rs.view(np.uint16))
+    out = torch.empty((n, dim), dtype=torch.float32, device="cuda")
+    T.fade_dequantize(codes, scales, n, dim, bits, out)
+    q, s = quant.quantize(x, bits)
+    assert np.array_equal(out.cpu().numpy(), quant.dequantize(q, s).astype(np.float32))
+
+
+def test_codec_empty_input_is_a_no_op(T):
+    import torch
+
+    x = torch.zeros((1, 64), dtype=torch.float16, device="cuda")
+    c = torch.full((1, 32), 7, dtype=torch.uint8, device="cuda")
+    s = torch.zeros((1, 2), dtype=torch.float16, device="cuda")
+    T.fade_quantize_pack(x, 0, 64, 4, c, s)
+    torch.cuda.synchronize()
+    assert int(c.sum()) == 7 * 32
+
+
+@pytest.mark.parametrize("key", [1, 3, 4])
+def test_rope_table_and_apply(T, key):
+    import torch
+
+    wl = get_workload(key)
+    cfg = T.Config.from_workload(wl)
+    max_pos = 40000
+    table = torch.empty(max_pos * wl.head_dim, dtype=torch.float32, device="cuda")
+    T.fade_rope_table_init(cfg, table, max_pos)
+    ref = RopeTable.from_workload(wl, max_pos)
+    tab = table.view(max_pos, wl.head_dim // 2, 2).cpu().numpy()
+    for got, want in ((tab[..., 0], ref.cos), (tab[..., 1], ref.sin)):
+        ulps = np.abs(got.view(np.int32).astype(np.int64) - want.view(np.int32).astype(np.int64))
+        assert ulps.max() <= 1, "table entry more than 1 fp32 ulp from the oracle"
+        assert (ulps != 0).mean() < 1e-4
+    rng = np.random.default_rng(key)
+    x = rng.standard_normal((300, wl.head_dim)).astype(np.float16)
+    pos = rng.integers(0, max_pos, 300).astype(np.int32)
+    xd = torch.from_numpy(x).cuda()
+    yd = torch.empty_like(xd)
+    T.fade_rope_apply(cfg, table, max_pos, xd, yd, 300, 1, torch.from_numpy(pos).cuda(), 0)
+    want = ref.apply(x, pos)
+    same = yd.cpu().numpy().view(np.uint16) == want.view(np.uint16)
+    # identical tables give identical bytes; a 1-ulp table entry may move one fp16 rounding
+    assert same.mean() > 0.999
+
+
+def _small(key):
+    if key == "1":
+        return get_workload(1).scaled(steps=6), None
+    if key == "2s":
+        return get_workload(2).scaled(layers=2, prompt_len=300, steps=6), None
+    if key == "3s":
+        return get_workload(3).scaled(layers=1, batch=2, prompt_len=700, int4_budget=200,
+                                      steps=12), None
+    if key == "4s":
+        return get_workload(4).scaled(layers=1, batch=3, num_q_heads=8, num_kv_heads=2,
+                                      prompt_len=1500, int4_budget=600, steps=6), None
+    if key == "5s":
+        return get_workload(5).scaled(layers=1, batch=3, num_q_heads=8, num_kv_heads=2,
+                                      ragged=(900, 1600), prompt_len=1600, int4_budget=700,
+                                      steps=6), None
+    if key == "5bs":
+        return get_workload("5b").scaled(layers=1, batch=3, num_q_heads=8, num_kv_heads=2,
+                                         ragged=(900, 1600), prompt_len=1600, steps=4), None
+    if key == "g2_k2v4":
+        return get_workload(4).scaled(layers=1, batch=2, num_q_heads=4, num_kv_heads=2,
+                                      middle_k_bits=2, middle_v_bits=4, prompt_len=1000,
+                                      int4_budget=300, steps=5), None
+    if key == "g1_h2o_d128":
+        return get_workload(3).scaled(layers=1, batch=2, num_q_heads=4, num_kv_heads=4,
+                                      head_dim=128, prompt_len=600, int4_budget=150,
+                                      steps=8), None
+    raise KeyError(key)
+
+
+@pytest.mark.parametrize("key", ["1", "2s", "3s", "4s", "5s", "5bs", "g2_k2v4", "g1_h2o_d128"])
+def test_lockstep_small_workloads(T, key):
+    wl, cap = _small(key)
+    ls = Lockstep(wl, mid_capacity=cap)
+    for layer in range(ls.L):
+        ls.prefill(layer)
+        ls.check_layer_state(layer)
+    for _ in range(ls.steps):
+        ls.step()
+    assert ls.near_ties <= max(1, wl.batch * wl.num_kv_heads * ls.L // 20)

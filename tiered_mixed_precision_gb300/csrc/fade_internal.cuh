@@ -1,0 +1,136 @@
+// Internal helpers shared by the libfade translation units (host error plumbing and the
+// device arithmetic every kernel must take identically: exact quantisation and fp32 RoPE).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fade.h"
+
+namespace fade {
+
+// ---------------------------------------------------------------- host side
+fade_status_t set_error(fade_status_t st, const char* fmt, ...);
+void clear_error();
+// Maps the last launch error (if any) to FADE_ERR_CUDA with its message.
+fade_status_t launch_status(const char* what);
+// Validates a layer configuration (shapes, bits, policy, RoPE parameters).
+fade_status_t validate_config(const fade_config_t* cfg);
+// Validates the non-null buffers of a layer for the given config.
+fade_status_t validate_layer(const fade_config_t* cfg, const fade_layer_t* layer);
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+constexpr int kGroup = FADE_GROUP;     // channels per quantisation group
+constexpr int kChunk = 1024;           // slots per selection chunk (bitmap prefix unit)
+constexpr float kSubnormalMin = 5.9604644775390625e-08f;  // 2^-24
+
+// Per-row lengths passed by value to kernels (rows <= FADE_MAX_BATCH).
+struct RowLens {
+  int32_t v[FADE_MAX_BATCH];
+};
+
+// ---------------------------------------------------------------- device side
+__device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+__device__ __forceinline__ uint16_t f2h(float f) { return __half_as_ushort(__float2half_rn(f)); }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Quantise one 32-channel group held one value per lane (all 32 lanes active).
+// s = fp16(absmax / qmax) with IEEE fp32 division; s = 2^-24 if it underflows; the code is
+// rint(x / s) (fp32 IEEE division, ties to even) clamped to [-qmax, qmax].
+__device__ __forceinline__ void quant_group_lane(float x, int qmax, uint16_t& s_bits, int& q) {
+  const float a = warp_max(fabsf(x));
+  float s = __half2float(__float2half_rn(__fdiv_rn(a, (float)qmax)));
+  if (a > 0.f && s == 0.f) s = kSubnormalMin;
+  s_bits = f2h(s);
+  q = 0;
+  if (s > 0.f) {
+    float r = rintf(__fdiv_rn(x, s));
+    r = fminf(fmaxf(r, (float)-qmax), (float)qmax);
+    q = (int)r;
+  }
+}
+
+// Pack the group's codes (one per lane) and store them as 32-bit words: INT4 puts 8 lanes in
+// a word (nibble i = lane 8w+i, written by lane 8w), INT2 puts 16 (crumb i = lane 16w+i,
+// written by lane 16w). This is the little-endian byte layout of the codec. `dst` points at
+// the group's first code byte and must be 4-byte aligned.
+template <int BITS>
+__device__ __forceinline__ void pack_group_store(int q, uint8_t* dst) {
+  const int lane = threadIdx.x & 31;
+  constexpr int per = 32 / BITS;   // codes per 32-bit word
+  uint32_t v = (uint32_t(q) & ((1u << BITS) - 1u)) << (BITS * (lane % per));
+#pragma unroll
+  for (int o = 1; o < per; o <<= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane % per == 0) reinterpret_cast<uint32_t*>(dst)[lane / per] = v;
+}
+
+// Sign-extended code of channel c of a packed row.
+template <int BITS>
+__device__ __forceinline__ int unpack_code(const uint8_t* row, int c) {
+  constexpr int per = 8 / BITS;
+  const uint32_t b = row[c / per];
+  const uint32_t u = (b >> (BITS * (c % per))) & ((1u << BITS) - 1u);
+  return int(u) - (int(u >> (BITS - 1)) << BITS);
+}
+
+// fp32 rotation of one pair with every product and sum rounded separately.
+__device__ __forceinline__ void rotate_pair(float x1, float x2, float c, float s, float& y1,
+                                            float& y2) {
+  y1 = __fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, s));
+  y2 = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s));
+}
+
+// Re-position one pair: un-rotate at `pold`, rotate at `pnew` (table = float2 [pos][d/2]).
+__device__ __forceinline__ void reposition_pair(const float2* __restrict__ table, int half,
+                                                int i, int pold, int pnew, float x1, float x2,
+                                                float& y1, float& y2) {
+  const float2 co = table[(size_t)pold * half + i];
+  const float2 cn = table[(size_t)pnew * half + i];
+  float t1, t2;
+  rotate_pair(x1, x2, co.x, -co.y, t1, t2);
+  rotate_pair(t1, t2, cn.x, cn.y, y1, y2);
+}
+
+// Re-position a whole fp32 key held as pairs by a warp and write it quantised (middle tier)
+// or as fp16. Lane l owns channels c1 = 32*gp + l and c2 = c1 + d/2 for gp < d/64.
+template <int D>
+struct WarpKey {
+  float lo[D / 64];  // channel 32*gp + lane
+  float hi[D / 64];  // channel 32*gp + lane + D/2
+};
+
+template <int D, int BITS>
+__device__ __forceinline__ void warp_store_quantized(const WarpKey<D>& k, uint8_t* codes_row,
+                                                     uint16_t* scales_row) {
+  const int lane = threadIdx.x & 31;
+  constexpr int qmax = (1 << (BITS - 1)) - 1;
+  constexpr int bytes_per_group = kGroup * BITS / 8;
+#pragma unroll
+  for (int gp = 0; gp < D / 64; ++gp) {
+    // group gp holds channels [32gp, 32gp+32) -> the `lo` values
+    uint16_t sb;
+    int q;
+    quant_group_lane(__half2float(__float2half_rn(k.lo[gp])), qmax, sb, q);
+    pack_group_store<BITS>(q, codes_row + gp * bytes_per_group);
+    if (lane == 0) scales_row[gp] = sb;
+    // group gp + D/64 holds channels [D/2 + 32gp, ...) -> the `hi` values
+    quant_group_lane(__half2float(__float2half_rn(k.hi[gp])), qmax, sb, q);
+    pack_group_store<BITS>(q, codes_row + (gp + D / 64) * bytes_per_group);
+    if (lane == 0) scales_row[gp + D / 64] = sb;
+  }
+}
+
+}  // namespace fade

@@ -1,0 +1,129 @@
+// RoPE table and rotation of q/k to cache positions.
+// Sources: page "FADE：面向LLM推理的注意力感知分层KV缓存压缩技术", §RoPE重计算 (float32 RoPE math,
+// cast through the model dtype) and §RoPE方案兼容性 (standard RoPE and llama3 scaling); page
+// "探秘Transformer系列之（25）--- KV Cache优化之处理长文本序列", §1.2.2 StreamingLLM (positions are
+// indices inside the cache).
+#include <math.h>
+
+#include "fade_internal.cuh"
+
+namespace fade {
+namespace {
+
+struct InvFreq {
+  float v[64];  // d/2 <= 64
+};
+
+// inv_freq_i = base^(-2i/d) in fp64, llama3-adjusted in fp64, rounded once to fp32.
+// Host code: compiled without floating-point contraction so every step rounds as written.
+InvFreq host_inv_freq(const fade_config_t* c) {
+  InvFreq f{};
+  const int half = c->head_dim / 2;
+  const fade_rope_t& r = c->rope;
+  for (int i = 0; i < half; ++i) {
+    double x = pow(r.base, -(2.0 * i) / c->head_dim);
+    if (r.kind == FADE_ROPE_LLAMA3) {
+      const double lam = 2.0 * M_PI / x;
+      const double L = (double)r.original_max_position;
+      const double low_wl = L / r.low_freq_factor;
+      const double high_wl = L / r.high_freq_factor;
+      if (lam < high_wl) {
+        // unchanged
+      } else if (lam > low_wl) {
+        x = x / r.factor;
+      } else {
+        const double t = (L / lam - r.low_freq_factor) / (r.high_freq_factor - r.low_freq_factor);
+        x = (1.0 - t) * x / r.factor + t * x;
+      }
+    }
+    f.v[i] = (float)x;
+  }
+  return f;
+}
+
+__global__ void rope_table_kernel(InvFreq inv, int half, int max_pos, float2* __restrict__ table) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)max_pos * half) return;
+  const int pos = (int)(i / half);
+  const int k = (int)(i % half);
+  const float ang = __fmul_rn((float)pos, inv.v[k]);
+  const double a = (double)ang;
+  table[i] = make_float2((float)cos(a), (float)sin(a));
+}
+
+__global__ void rope_apply_kernel(const float2* __restrict__ table, int max_pos, int half,
+                                  const uint16_t* __restrict__ x, uint16_t* __restrict__ y,
+                                  long long n_pairs, int group_len,
+                                  const int32_t* __restrict__ pos_start, int pos_step) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_pairs) return;
+  const long long vec = i / half;
+  const int k = (int)(i % half);
+  const long long g = vec / group_len;
+  const int j = (int)(vec % group_len);
+  int pos = (pos_start ? pos_start[g] : 0) + j * pos_step;
+  pos = min(max(pos, 0), max_pos - 1);  // out-of-range positions are clamped (memory safety)
+  const float2 cs = table[(long long)pos * half + k];
+  const long long base = vec * (2LL * half);
+  const float x1 = h2f(x[base + k]), x2 = h2f(x[base + k + half]);
+  float y1, y2;
+  rotate_pair(x1, x2, cs.x, cs.y, y1, y2);
+  y[base + k] = f2h(y1);
+  y[base + k + half] = f2h(y2);
+}
+
+}  // namespace
+}  // namespace fade
+
+using namespace fade;
+
+extern "C" fade_status_t fade_rope_table_init(const fade_config_t* cfg, float* table,
+                                              int32_t max_pos, void* stream) {
+  clear_error();
+  fade_status_t st = validate_config(cfg);
+  if (st) return st;
+  if (cfg->rope.kind == FADE_ROPE_NONE)
+    return set_error(FADE_ERR_INVALID_ARGUMENT, "no RoPE table for FADE_ROPE_NONE");
+  if (!table || max_pos < 1)
+    return set_error(FADE_ERR_INVALID_ARGUMENT, "NULL table or max_pos < 1");
+  if (reinterpret_cast<uintptr_t>(table) & 7)
+    return set_error(FADE_ERR_INVALID_ARGUMENT, "table must be 8-byte aligned");
+  const int half = cfg->head_dim / 2;
+  const long long n = (long long)max_pos * half;
+  rope_table_kernel<<<ceil_div(n, 256), 256, 0, as_stream(stream)>>>(
+      host_inv_freq(cfg), half, max_pos, reinterpret_cast<float2*>(table));
+  return launch_status("fade_rope_table_init");
+}
+
+extern "C" fade_status_t fade_rope_apply(const fade_config_t* cfg, const float* table,
+                                         int32_t max_pos, const uint16_t* x, uint16_t* y,
+                                         int64_t n_groups, int32_t group_len,
+                                         const int32_t* pos_start, int32_t pos_step,
+                                         void* stream) {
+  clear_error();
+  fade_status_t st = validate_config(cfg);
+  if (st) return st;
+  if (!x || !y) return set_error(FADE_ERR_INVALID_ARGUMENT, "NULL x or y");
+  if (n_groups < 0 || group_len < 0)
+    return set_error(FADE_ERR_INVALID_ARGUMENT, "negative n_groups or group_len");
+  const long long n_vec = (long long)n_groups * group_len;
+  if (cfg->rope.kind == FADE_ROPE_NONE) {
+    if (x != y && n_vec)
+      if (cudaMemcpyAsync(y, x, n_vec * cfg->head_dim * 2, cudaMemcpyDeviceToDevice,
+                          as_stream(stream)) != cudaSuccess)
+        return launch_status("fade_rope_apply copy");
+    return FADE_OK;
+  }
+  if (!table || max_pos < 1) return set_error(FADE_ERR_INVALID_ARGUMENT, "NULL RoPE table");
+  if (!pos_start && group_len > 0 && (long long)(group_len - 1) * pos_step >= max_pos)
+    return set_error(FADE_ERR_CAPACITY, "positions up to %lld exceed the table (%d)",
+                     (long long)(group_len - 1) * pos_step, max_pos);
+  if (pos_step < 0) return set_error(FADE_ERR_INVALID_ARGUMENT, "pos_step < 0");
+  if (n_vec == 0) return FADE_OK;
+  const int half = cfg->head_dim / 2;
+  const long long n_pairs = n_vec * half;
+  rope_apply_kernel<<<ceil_div(n_pairs, 256), 256, 0, as_stream(stream)>>>(
+      reinterpret_cast<const float2*>(table), max_pos, half, x, y, n_pairs, group_len,
+      pos_start, pos_step);
+  return launch_status("fade_rope_apply");
+}

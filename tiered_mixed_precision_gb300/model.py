@@ -1,0 +1,140 @@
+"""Multi-layer tiered KV cache driven through the libfade C ABI.
+
+A decode step of one layer enqueues, in the method's order: RoPE of the new q and k at the
+next cache position, demote (quantise-pack the token leaving the recent window), evict +
+re-position, append, decode attention, and H2O / EMA accumulation. Everything runs in the
+CUDA library on the caller's stream; this module only allocates buffers and passes pointers.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import fade as F
+
+
+class FadeCache:
+    """All layers of one model's cache (layers share a config, a RoPE table and workspaces)."""
+
+    def __init__(self, cfg: F.Config, num_layers: int, max_prompt: int, max_pos: int,
+                 device="cuda"):
+        self.cfg = cfg
+        self.device = torch.device(device)
+        self.layers = [F.TieredLayer(cfg, max_prompt, self.device) for _ in range(num_layers)]
+        self.max_pos = max_pos
+        self.max_prompt = max_prompt
+        self.table = None
+        if cfg.rope_kind != "none":
+            self.table = torch.empty(max_pos * cfg.head_dim, dtype=torch.float32, device=self.device)
+            F.fade_rope_table_init(cfg, self.table, max_pos)
+        self.logits, self.ml, self.ws = self.layers[0].workspaces()
+        self.pos = torch.zeros(cfg.batch, dtype=torch.int32, device=self.device)
+        self._pos_host = torch.zeros(cfg.batch, dtype=torch.int32).pin_memory() \
+            if self.device.type == "cuda" else torch.zeros(cfg.batch, dtype=torch.int32)
+        self.needs_logits = cfg.policy in ("h2o", "ema")
+        # rotated copies of the step's q and k (the caller's raw inputs stay intact)
+        self.q_rot = torch.empty((cfg.batch, cfg.num_q_heads, cfg.head_dim), dtype=torch.float16,
+                                 device=self.device)
+        self.k_rot = torch.empty((cfg.batch, cfg.num_kv_heads, cfg.head_dim),
+                                 dtype=torch.float16, device=self.device)
+        self.timers = None      # optional {"attention": [...], "evict": [...]} of event pairs
+        self.launches = 0       # kernels enqueued by step_layer calls
+
+    # ------------------------------------------------------------------ pieces
+    def rope_(self, x: torch.Tensor, n_groups: int, group_len: int, pos_start=None, pos_step=1):
+        """Rotate x in place (fp16 [n_groups][group_len][d])."""
+        F.fade_rope_apply(self.cfg, self.table, self.max_pos, x, x, n_groups, group_len,
+                          pos_start, pos_step)
+        return x
+
+    def prefill(self, layer: int, k_raw: torch.Tensor, v: torch.Tensor, prompt_len=None,
+                mass: torch.Tensor | None = None):
+        """k_raw, v: fp16 [B][Hkv][P][d] device tensors (k pre-RoPE; rotated in place)."""
+        c = self.cfg
+        B, H, P, d = k_raw.shape
+        if prompt_len is None:
+            prompt_len = np.full(B, P, np.int32)
+        self.rope_(k_raw, B * H, P, None, 1)
+        L = self.layers[layer]
+        F.fade_cache_reset(L)
+        F.fade_cache_prefill(L, k_raw, v, P, prompt_len, mass, self.table, self.max_pos)
+
+    def next_positions(self) -> np.ndarray:
+        L = self.layers[0]
+        return np.array([F.fade_next_position(L, b) for b in range(self.cfg.batch)], np.int32)
+
+    def set_positions(self, pos: np.ndarray):
+        self._pos_host.copy_(torch.from_numpy(np.ascontiguousarray(pos, np.int32)))
+        self.pos.copy_(self._pos_host, non_blocking=True)
+
+    def step_layer(self, layer: int, q_raw: torch.Tensor, k_raw: torch.Tensor, v: torch.Tensor,
+                   out: torch.Tensor):
+        """One decode step of one layer. q_raw [B][Hq][d], k_raw/v [B][Hkv][d] fp16, pre-RoPE
+        (rotated into work buffers at the positions last set by ``set_positions``);
+        out [B][Hq][d] fp16."""
+        c = self.cfg
+        L = self.layers[layer]
+        F.fade_rope_apply(c, self.table, self.max_pos, q_raw, self.q_rot, c.batch,
+                          c.num_q_heads, self.pos, 0)
+        F.fade_rope_apply(c, self.table, self.max_pos, k_raw, self.k_rot, c.batch,
+                          c.num_kv_heads, self.pos, 0)
+        n = 2 if c.rope_kind != "none" else 0
+        ring_full = bool((L.h_n_recent == c.recent_window).any())
+        F.fade_cache_demote(L)
+        n += 1 if ring_full else 0
+        evicting = c.evicts and bool((L.h_n_mid > c.int4_budget).any())
+        t = self._tick("evict") if evicting else None
+        F.fade_evict_rerope(L, self.table, self.max_pos)
+        self._tock(t)
+        n += 3 if evicting else 0
+        F.fade_cache_append(L, self.k_rot, v)
+        t = self._tick("attention")
+        F.fade_decode_attention(L, self.q_rot, out, self.logits if self.needs_logits else None,
+                                self.ml, self.ws)
+        self._tock(t)
+        n += 3
+        if self.needs_logits:
+            F.fade_h2o_accumulate(L, self.logits, self.ml)
+            n += 1
+        self.launches += n
+
+    def _tick(self, name):
+        if self.timers is None:
+            return None
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        self.timers.setdefault(name, []).append((e0, e1))
+        return e1
+
+    @staticmethod
+    def _tock(e1):
+        if e1 is not None:
+            e1.record()
+
+    def attention_only(self, layer: int, q_rot: torch.Tensor, out: torch.Tensor):
+        F.fade_decode_attention(self.layers[layer], q_rot, out,
+                                self.logits if self.needs_logits else None, self.ml, self.ws)
+
+    # ------------------------------------------------------------------ inspection
+    def unit_state(self, layer: int, row: int, head: int) -> dict:
+        """One unit's tiers copied to the host, in cache order (for tests and debugging)."""
+        L = self.layers[layer]
+        m = L.meta[row, head].cpu().numpy()
+        n_sink, n_mid, n_rec, head_slot, cur = (int(m[i]) for i in range(5))
+        W = self.cfg.recent_window
+        ring = [(head_slot + i) % W for i in range(n_rec)]
+        g = lambda t: t[row, head].cpu()
+        rk, rv, rs = g(L.recent_k), g(L.recent_v), g(L.recent_scores)
+        return {
+            "n_sink": n_sink, "n_mid": n_mid, "n_recent": n_rec, "cur": cur,
+            "sink_k": g(L.sink_k)[:n_sink].numpy(), "sink_v": g(L.sink_v)[:n_sink].numpy(),
+            "mid_k_codes": g(L.mid_k_codes[cur])[:n_mid].numpy(),
+            "mid_k_scales": g(L.mid_k_scales[cur])[:n_mid].numpy(),
+            "mid_v_codes": g(L.mid_v_codes[cur])[:n_mid].numpy(),
+            "mid_v_scales": g(L.mid_v_scales[cur])[:n_mid].numpy(),
+            "recent_k": rk[ring].numpy(), "recent_v": rv[ring].numpy(),
+            "scores": np.concatenate([g(L.sink_scores)[:n_sink].numpy(),
+                                      g(L.mid_scores[cur])[:n_mid].numpy(),
+                                      rs[ring].numpy()]),
+        }
