@@ -89,6 +89,7 @@ typedef struct {
 } fade_config_t;
 
 #define FADE_MAX_BATCH 256
+#define FADE_STATUS_WORDS 4
 #define FADE_GROUP 32
 
 /* Per-unit device metadata: int32 [batch][num_kv_heads][FADE_META_FIELDS]. */
@@ -105,7 +106,10 @@ enum {
 };
 
 /* Caller-owned buffers of one layer. Device pointers unless marked host. Shapes use
- * B = batch, H = num_kv_heads, S = n_sink, W = recent_window, C = mid_capacity, d. */
+ * B = batch, H = num_kv_heads, S = n_sink, W = recent_window, d, and C = the middle slot
+ * stride: mid_capacity rounded up to a multiple of 64 (fade_layout_t.mid_stride), so every
+ * unit's rows start 16-byte aligned for bulk copies. Only the first mid_capacity slots of a
+ * unit are ever used. */
 typedef struct {
   uint16_t* sink_k;          /* fp16 [B][H][S][d] */
   uint16_t* sink_v;          /* fp16 [B][H][S][d] */
@@ -123,6 +127,9 @@ typedef struct {
   int32_t* chunk_base;       /* scratch: i32 [B][H][chunk_slots] */
   int32_t victim_words;      /* from fade_layout_t: sizes the longest prompt / middle tier */
   int32_t chunk_slots;       /* from fade_layout_t */
+  int32_t* status;           /* i32 [FADE_STATUS_WORDS]: device-side error status, 0 = ok;
+                                zeroed by fade_cache_reset; nonzero after a kernel gave up a
+                                bounded wait (the call's results are then invalid) */
   int32_t* h_n_sink;         /* HOST i32 [B]: mirror of N_SINK (same for every head) */
   int32_t* h_n_mid;          /* HOST i32 [B]: mirror of N_MID */
   int32_t* h_n_recent;       /* HOST i32 [B]: mirror of N_RECENT */
@@ -132,8 +139,9 @@ typedef struct {
 typedef struct {
   size_t sink_k, sink_v, recent_k, recent_v;
   size_t mid_k_codes, mid_k_scales, mid_v_codes, mid_v_scales; /* each of the two buffers */
-  size_t sink_scores, mid_scores, recent_scores, meta, victims, chunk_base;
+  size_t sink_scores, mid_scores, recent_scores, meta, victims, chunk_base, status;
   size_t logits_ws;   /* f32 [B][Hq][S + C + W]: per-token logits for H2O / EMA */
+  int32_t mid_stride;  /* C: middle slots per unit in every middle buffer */
   size_t ml_ws;       /* f32 [B][Hq][2]: final (max, sum) of each query head's softmax */
   size_t attn_ws;     /* split-KV partials for fade_decode_attention */
   int32_t victim_words;  /* u32 words per unit in `victims` */

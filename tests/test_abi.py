@@ -71,12 +71,14 @@ def test_layout_sizes(T):
     c = _cfg(T)
     lay = T.fade_layout(c, 2048)
     units = 2 * 2
-    assert lay.mid_k_codes == units * 401 * 64
-    assert lay.mid_v_codes == units * 401 * 32
-    assert lay.mid_k_scales == units * 401 * 4 * 2
+    C = lay.mid_stride
+    assert C == 448 and C % 64 == 0 and C >= 401          # capacity rounded up to 64 slots
+    assert lay.mid_k_codes == units * C * 64
+    assert lay.mid_v_codes == units * C * 32
+    assert lay.mid_k_scales == units * C * 4 * 2
     assert lay.sink_k == units * 4 * 128 * 2
     assert lay.recent_k == units * 64 * 128 * 2
-    assert lay.logits_ws == 2 * 8 * (4 + 401 + 64) * 4
+    assert lay.logits_ws == 2 * 8 * (4 + C + 64) * 4
     assert lay.victim_words >= 2048 // 32 + 1
 
 

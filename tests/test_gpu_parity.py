@@ -105,10 +105,17 @@ def _small(key):
         return get_workload(3).scaled(layers=1, batch=2, num_q_heads=4, num_kv_heads=4,
                                       head_dim=128, prompt_len=600, int4_budget=150,
                                       steps=8), None
+    if key == "d64_g8":
+        return get_workload(3).scaled(layers=1, batch=2, num_q_heads=16, num_kv_heads=2,
+                                      prompt_len=900, int4_budget=500, steps=6), None
+    if key == "d128_g8":
+        return get_workload(4).scaled(layers=1, batch=2, num_q_heads=16, num_kv_heads=2,
+                                      prompt_len=1300, int4_budget=700, steps=5), None
     raise KeyError(key)
 
 
-@pytest.mark.parametrize("key", ["1", "2s", "3s", "4s", "5s", "5bs", "g2_k2v4", "g1_h2o_d128"])
+@pytest.mark.parametrize("key", ["1", "2s", "3s", "4s", "5s", "5bs", "g2_k2v4", "g1_h2o_d128",
+                                 "d64_g8", "d128_g8"])
 def test_lockstep_small_workloads(T, key):
     wl, cap = _small(key)
     ls = Lockstep(wl, mid_capacity=cap)

@@ -82,8 +82,8 @@ fade_status_t validate_layer(const fade_config_t* c, const fade_layer_t* L) {
     if (!L->mid_k_codes[i] || !L->mid_k_scales[i] || !L->mid_v_codes[i] ||
         !L->mid_v_scales[i] || !L->mid_scores[i])
       return set_error(FADE_ERR_INVALID_ARGUMENT, "middle buffer %d is NULL", i);
-  if (!L->meta || !L->victims || !L->chunk_base)
-    return set_error(FADE_ERR_INVALID_ARGUMENT, "meta or scratch buffers are NULL");
+  if (!L->meta || !L->victims || !L->chunk_base || !L->status)
+    return set_error(FADE_ERR_INVALID_ARGUMENT, "meta, status or scratch buffers are NULL");
   if (!L->h_n_sink || !L->h_n_mid || !L->h_n_recent)
     return set_error(FADE_ERR_INVALID_ARGUMENT, "host mirror arrays are NULL");
   return FADE_OK;
@@ -104,7 +104,7 @@ extern "C" fade_status_t fade_layout(const fade_config_t* c, int32_t max_prompt,
   if (!o) return set_error(FADE_ERR_INVALID_ARGUMENT, "layout output is NULL");
   if (max_prompt < 0) return set_error(FADE_ERR_INVALID_ARGUMENT, "max_prompt < 0");
   const size_t B = c->batch, H = c->num_kv_heads, Hq = c->num_q_heads, d = c->head_dim;
-  const size_t S = c->n_sink, W = c->recent_window, C = c->mid_capacity;
+  const size_t S = c->n_sink, W = c->recent_window, C = mid_stride(c);
   const size_t units = B * H;
   o->sink_k = o->sink_v = units * S * d * 2;
   o->recent_k = o->recent_v = units * W * d * 2;
@@ -120,11 +120,13 @@ extern "C" fade_status_t fade_layout(const fade_config_t* c, int32_t max_prompt,
   o->chunk_slots = ceil_div(span, kChunk) + 1;
   o->victims = units * o->victim_words * 4;
   o->chunk_base = units * o->chunk_slots * 4;
+  o->status = FADE_STATUS_WORDS * 4;
   o->logits_ws = B * Hq * (S + C + W) * 4;
   o->ml_ws = B * Hq * 2 * 4;
   o->max_splits = 1 + ceil_div((long long)C, kMinSplitTokens);
   o->attn_ws = B * Hq * (size_t)o->max_splits * (d + 2) * 4;
   o->max_prompt = max_prompt;
+  o->mid_stride = (int32_t)C;
   return FADE_OK;
 }
 

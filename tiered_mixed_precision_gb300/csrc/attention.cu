@@ -147,12 +147,14 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(AttnArgs a) {
       kst = reinterpret_cast<uint16_t*>(vt + kTile * L::VROWP);
       vst = kst + kTile * L::SROW;
       const size_t r0 = urow_mid + lo + t0;
-      const uint8_t* kg = a.mk[cur] + r0 * L::KROW;
-      const uint8_t* vg = a.mv[cur] + r0 * L::VROW;
+      const uint8_t* kg = (cur ? a.mk[1] : a.mk[0]) + r0 * L::KROW;
+      const uint8_t* vg = (cur ? a.mv[1] : a.mv[0]) + r0 * L::VROW;
       stage_rows(kt, L::KROWP, L::KROW, nt, [&](int t) { return kg + (size_t)t * L::KROW; });
       stage_rows(vt, L::VROWP, L::VROW, nt, [&](int t) { return vg + (size_t)t * L::VROW; });
-      const uint32_t* ksg = reinterpret_cast<const uint32_t*>(a.mks[cur] + r0 * L::SROW);
-      const uint32_t* vsg = reinterpret_cast<const uint32_t*>(a.mvs[cur] + r0 * L::SROW);
+      const uint32_t* ksg =
+          reinterpret_cast<const uint32_t*>((cur ? a.mks[1] : a.mks[0]) + r0 * L::SROW);
+      const uint32_t* vsg =
+          reinterpret_cast<const uint32_t*>((cur ? a.mvs[1] : a.mvs[0]) + r0 * L::SROW);
       const int words = nt * L::SROW / 2;
       for (int i = tid; i < words; i += kThreads) {
         reinterpret_cast<uint32_t*>(kst)[i] = ksg[i];
@@ -299,10 +301,12 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(AttnArgs a) {
     for (int k = 0; k < NSUB; ++k) v += ar[(k * G + h) * D + c];
     a.part_acc[(pbase + (size_t)h * a.nsplit) * D + c] = v;
   }
-  if (tid < G) {
-    a.part_ml[(pbase + (size_t)tid * a.nsplit) * 2 + 0] = m_run[tid];
-    a.part_ml[(pbase + (size_t)tid * a.nsplit) * 2 + 1] = l_run[tid];
-  }
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+    if (tid == h) {
+      a.part_ml[(pbase + (size_t)h * a.nsplit) * 2 + 0] = m_run[h];
+      a.part_ml[(pbase + (size_t)h * a.nsplit) * 2 + 1] = l_run[h];
+    }
 }
 
 // One CTA of D threads per (row, query head): merge the split partials.
@@ -374,46 +378,49 @@ __global__ void h2o_accumulate_kernel(AccArgs a) {
 }
 
 template <int D, int KB, int VB, int G>
-fade_status_t launch_split(const AttnArgs& a, int B, cudaStream_t st) {
+fade_status_t launch_split(const AttnArgs& a, int B, cudaStream_t st, int nx) {
   using L = Smem<D, KB, VB, G>;
   // opt in to more than 48 KB of dynamic shared memory (cheap; done on every launch so it
   // holds for whichever device is current)
   if (cudaFuncSetAttribute(attn_split_kernel<D, KB, VB, G>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL) != cudaSuccess)
     return launch_status("fade_decode_attention shared-memory opt-in");
-  attn_split_kernel<D, KB, VB, G><<<dim3(a.nsplit, a.H, B), kThreads, L::TOTAL, st>>>(a);
+  attn_split_kernel<D, KB, VB, G><<<dim3(nx, a.H, B), kThreads, L::TOTAL, st>>>(a);
   return launch_status("fade_decode_attention split");
 }
 
 template <int D, int KB, int VB>
-fade_status_t launch_split_g(const AttnArgs& a, int G, int B, cudaStream_t st) {
+fade_status_t launch_split_g(const AttnArgs& a, int G, int B, cudaStream_t st, int nx) {
   switch (G) {
-    case 1: return launch_split<D, KB, VB, 1>(a, B, st);
-    case 2: return launch_split<D, KB, VB, 2>(a, B, st);
-    case 4: return launch_split<D, KB, VB, 4>(a, B, st);
-    case 8: return launch_split<D, KB, VB, 8>(a, B, st);
+    case 1: return launch_split<D, KB, VB, 1>(a, B, st, nx);
+    case 2: return launch_split<D, KB, VB, 2>(a, B, st, nx);
+    case 4: return launch_split<D, KB, VB, 4>(a, B, st, nx);
+    case 8: return launch_split<D, KB, VB, 8>(a, B, st, nx);
   }
   return set_error(FADE_ERR_UNSUPPORTED, "query heads per KV head %d", G);
 }
 
-fade_status_t launch_split_any(const fade_config_t* c, const AttnArgs& a, cudaStream_t st) {
+// Launches splits [0, nx) of the CUDA-core kernel.
+fade_status_t launch_split_any(const fade_config_t* c, const AttnArgs& a, cudaStream_t st, int nx) {
   const int G = c->num_q_heads / c->num_kv_heads, B = c->batch;
   const int d = c->head_dim, kb = c->middle_k_bits, vb = c->middle_v_bits;
 #define FADE_CASE(D_, KB_, VB_) \
-  if (d == D_ && kb == KB_ && vb == VB_) return launch_split_g<D_, KB_, VB_>(a, G, B, st);
+  if (d == D_ && kb == KB_ && vb == VB_) return launch_split_g<D_, KB_, VB_>(a, G, B, st, nx);
   FADE_CASE(64, 4, 2) FADE_CASE(64, 4, 4) FADE_CASE(64, 2, 2) FADE_CASE(64, 2, 4)
   FADE_CASE(128, 4, 2) FADE_CASE(128, 4, 4) FADE_CASE(128, 2, 2) FADE_CASE(128, 2, 4)
 #undef FADE_CASE
   return set_error(FADE_ERR_UNSUPPORTED, "unsupported (head_dim, k_bits, v_bits)");
 }
 
-// Middle tokens per split: enough CTAs to fill the GPU several times, in whole tiles.
-int choose_chunk(int max_mid, int units) {
-  const long long target = 8LL * 152;
-  long long ch = ((long long)max_mid * units + target - 1) / target;
-  ch = ((ch + kTile - 1) / kTile) * kTile;
-  if (ch < kTile) ch = kTile;
-  if (ch > 4096) ch = 4096;
+// Middle tokens per split: enough CTAs to fill the GPU several times over, splits of equal
+// size, each a whole number of tiles.
+int choose_chunk(int max_mid, int units, int tile, long long target_ctas) {
+  if (max_mid <= 0) return tile;
+  long long want = ((long long)max_mid * units + target_ctas - 1) / target_ctas;
+  if (want < tile) want = tile;
+  const long long n = (max_mid + want - 1) / want;
+  long long ch = (max_mid + n - 1) / n;
+  ch = ((ch + tile - 1) / tile) * tile;
   return (int)ch;
 }
 
@@ -459,9 +466,11 @@ extern "C" fade_status_t fade_decode_attention(const fade_config_t* c, const fad
   a.H = c->num_kv_heads;
   a.S = c->n_sink;
   a.W = c->recent_window;
-  a.C = c->mid_capacity;
+  a.C = mid_stride(c);
   a.NS = a.S + a.C + a.W;
-  a.chunk = choose_chunk(max_mid, units);
+  const bool mma = mid_mma_supported(c);
+  a.chunk = mma ? choose_chunk(max_mid, units, 256, 6LL * 304)
+                : choose_chunk(max_mid, units, kTile, 8LL * 152);
   a.nsplit = 1 + (max_mid + a.chunk - 1) / a.chunk;
   a.scale = 1.0f / sqrtf((float)c->head_dim);
   const size_t need = (size_t)c->batch * c->num_q_heads * a.nsplit * (c->head_dim + 2) * 4;
@@ -471,7 +480,16 @@ extern "C" fade_status_t fade_decode_attention(const fade_config_t* c, const fad
   a.part_ml = reinterpret_cast<float*>(ws);
   a.part_acc = a.part_ml + (size_t)c->batch * c->num_q_heads * a.nsplit * 2;
   cudaStream_t s = as_stream(stream);
-  if ((st = launch_split_any(c, a, s))) return st;
+  if (mma) {
+    // FP16 tiers on the CUDA cores (split 0), the packed middle tier on the tensor cores
+    AttnArgs a0 = a;
+    if ((st = launch_split_any(c, a0, s, 1))) return st;
+    if ((st = launch_mid_mma(c, L, q_rot, logits_ws, a.part_ml, a.part_acc, a.chunk, a.nsplit,
+                             s)))
+      return st;
+  } else if ((st = launch_split_any(c, a, s, a.nsplit))) {
+    return st;
+  }
   const int bh = c->batch * c->num_q_heads;
   if (c->head_dim == 64)
     attn_combine_kernel<64><<<bh, 64, 0, s>>>(a, out, ml_ws);
@@ -501,7 +519,7 @@ extern "C" fade_status_t fade_h2o_accumulate(const fade_config_t* c, fade_layer_
   a.H = c->num_kv_heads;
   a.S = c->n_sink;
   a.W = c->recent_window;
-  a.C = c->mid_capacity;
+  a.C = mid_stride(c);
   a.NS = a.S + a.C + a.W;
   a.policy = c->policy;
   a.decay = c->ema_decay;

@@ -164,7 +164,7 @@ LayerArgs make_args(const fade_config_t* c, const fade_layer_t* L, const float* 
   a.H = c->num_kv_heads;
   a.S = c->n_sink;
   a.W = c->recent_window;
-  a.C = c->mid_capacity;
+  a.C = mid_stride(c);
   a.budget = c->int4_budget;
   a.policy = c->policy;
   a.evicts = c->policy != FADE_EVICT_NONE && c->int4_budget >= 0;
@@ -276,13 +276,13 @@ __global__ void __launch_bounds__(32) demote_kernel(LayerArgs a) {
   if (n_mid >= a.C || head < 0 || head >= a.W) return;  // host checks capacity; never overrun
   const size_t rrow = ((size_t)unit * a.W + head) * D;
   const size_t mrow = (size_t)unit * a.C + n_mid;
-  warp_quantize_row<D, KB>(a.rec_k + rrow, a.mk[cur] + mrow * (D * KB / 8),
-                           a.mks[cur] + mrow * (D / kGroup));
-  warp_quantize_row<D, VB>(a.rec_v + rrow, a.mv[cur] + mrow * (D * VB / 8),
-                           a.mvs[cur] + mrow * (D / kGroup));
+  warp_quantize_row<D, KB>(a.rec_k + rrow, (cur ? a.mk[1] : a.mk[0]) + mrow * (D * KB / 8),
+                           (cur ? a.mks[1] : a.mks[0]) + mrow * (D / kGroup));
+  warp_quantize_row<D, VB>(a.rec_v + rrow, (cur ? a.mv[1] : a.mv[0]) + mrow * (D * VB / 8),
+                           (cur ? a.mvs[1] : a.mvs[0]) + mrow * (D / kGroup));
   __syncwarp();
   if (threadIdx.x == 0) {
-    a.mid_sc[cur][mrow] = a.rec_sc[(size_t)unit * a.W + head];
+    (cur ? a.mid_sc[1] : a.mid_sc[0])[mrow] = a.rec_sc[(size_t)unit * a.W + head];
     m[FADE_META_N_MID] = n_mid + 1;
     m[FADE_META_N_RECENT] = n_rec - 1;
     m[FADE_META_HEAD] = (head + 1) % a.W;
@@ -338,8 +338,9 @@ __global__ void __launch_bounds__(kSelThreads) evict_select_kernel(LayerArgs a) 
   __syncthreads();
   if (threadIdx.x == 0) m[FADE_META_N_EV] = k;
   if (k == 0) return;
-  const float* keys =
-      (a.policy == FADE_EVICT_POSITION) ? nullptr : a.mid_sc[cur] + (size_t)unit * a.C;
+  const float* keys = (a.policy == FADE_EVICT_POSITION)
+                          ? nullptr
+                          : (cur ? a.mid_sc[1] : a.mid_sc[0]) + (size_t)unit * a.C;
   block_select(keys, n_mid, k, a.victims + (size_t)unit * a.victim_words,
                a.chunk_base + (size_t)unit * a.chunk_slots);
 }
@@ -390,7 +391,18 @@ __global__ void __launch_bounds__(256) evict_compact_kernel(LayerArgs a) {
   }
   __syncthreads();
   const int base = a.chunk_base[(size_t)unit * a.chunk_slots + blockIdx.x];
-  const int src = cur, dst = cur ^ 1;
+  // live (source) and other (destination) buffers, selected without indexing the
+  // parameter arrays by a runtime value
+  const uint8_t* mk_s = cur ? a.mk[1] : a.mk[0];
+  uint8_t* mk_d = cur ? a.mk[0] : a.mk[1];
+  const uint8_t* mv_s = cur ? a.mv[1] : a.mv[0];
+  uint8_t* mv_d = cur ? a.mv[0] : a.mv[1];
+  const uint16_t* mks_s = cur ? a.mks[1] : a.mks[0];
+  uint16_t* mks_d = cur ? a.mks[0] : a.mks[1];
+  const uint16_t* mvs_s = cur ? a.mvs[1] : a.mvs[0];
+  uint16_t* mvs_d = cur ? a.mvs[0] : a.mvs[1];
+  const float* sc_s = cur ? a.mid_sc[1] : a.mid_sc[0];
+  float* sc_d = cur ? a.mid_sc[0] : a.mid_sc[1];
   constexpr int KROW = D * KB / 8, VROW = D * VB / 8, SROW = D / kGroup;
   const size_t ubase = (size_t)unit * a.C;
   for (int wi = warp; wi < nw; wi += 8) {
@@ -402,12 +414,12 @@ __global__ void __launch_bounds__(256) evict_compact_kernel(LayerArgs a) {
     const bool moved = keep && nv != i;
     if (keep) {
       const size_t si = ubase + i, di = ubase + nv;
-      copy_row<VROW>(a.mv[src] + si * VROW, a.mv[dst] + di * VROW);
-      copy_row<SROW * 2>(a.mvs[src] + si * SROW, a.mvs[dst] + di * SROW);
-      a.mid_sc[dst][di] = a.mid_sc[src][si];
+      copy_row<VROW>(mv_s + si * VROW, mv_d + di * VROW);
+      copy_row<SROW * 2>(mvs_s + si * SROW, mvs_d + di * SROW);
+      sc_d[di] = sc_s[si];
       if (!moved) {
-        copy_row<KROW>(a.mk[src] + si * KROW, a.mk[dst] + di * KROW);
-        copy_row<SROW * 2>(a.mks[src] + si * SROW, a.mks[dst] + di * SROW);
+        copy_row<KROW>(mk_s + si * KROW, mk_d + di * KROW);
+        copy_row<SROW * 2>(mks_s + si * SROW, mks_d + di * SROW);
       }
     }
     uint32_t mv = __ballot_sync(0xffffffffu, moved);
@@ -417,9 +429,9 @@ __global__ void __launch_bounds__(256) evict_compact_kernel(LayerArgs a) {
       const int ij = __shfl_sync(0xffffffffu, i, j);
       const int nj = __shfl_sync(0xffffffffu, nv, j);
       const size_t si = ubase + ij, di = ubase + nj;
-      WarpKey<D> k = load_mid_key<D, KB>(a.mk[src] + si * KROW, a.mks[src] + si * SROW);
+      WarpKey<D> k = load_mid_key<D, KB>(mk_s + si * KROW, mks_s + si * SROW);
       reposition_key<D>(a, k, n_sink + ij, n_sink + nj);
-      warp_store_quantized<D, KB>(k, a.mk[dst] + di * KROW, a.mks[dst] + di * SROW);
+      warp_store_quantized<D, KB>(k, mk_d + di * KROW, mks_d + di * SROW);
     }
   }
 }
@@ -606,6 +618,8 @@ extern "C" fade_status_t fade_cache_reset(const fade_config_t* c, fade_layer_t* 
   if (st) return st;
   const int n = c->batch * c->num_kv_heads * FADE_META_FIELDS;
   reset_kernel<<<ceil_div(n, 256), 256, 0, as_stream(stream)>>>(L->meta, n);
+  if ((st = launch_status("fade_cache_reset"))) return st;
+  reset_kernel<<<1, 32, 0, as_stream(stream)>>>(L->status, FADE_STATUS_WORDS);
   for (int b = 0; b < c->batch; ++b) L->h_n_sink[b] = L->h_n_mid[b] = L->h_n_recent[b] = 0;
   return launch_status("fade_cache_reset");
 }

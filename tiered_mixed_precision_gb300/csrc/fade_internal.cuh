@@ -27,10 +27,20 @@ constexpr int kGroup = FADE_GROUP;     // channels per quantisation group
 constexpr int kChunk = 1024;           // slots per selection chunk (bitmap prefix unit)
 constexpr float kSubnormalMin = 5.9604644775390625e-08f;  // 2^-24
 
+// Middle slots per unit in every middle buffer: the capacity rounded up to 64 slots.
+inline int mid_stride(const fade_config_t* c) { return (c->mid_capacity + 63) / 64 * 64; }
+
 // Per-row lengths passed by value to kernels (rows <= FADE_MAX_BATCH).
 struct RowLens {
   int32_t v[FADE_MAX_BATCH];
 };
+
+// Tensor-core attention over the middle tier (INT4 K / INT2 V); writes partial splits
+// 1..nsplit-1 (split 0 holds the FP16 tiers). Defined in attention_mma.cu.
+bool mid_mma_supported(const fade_config_t* c);
+fade_status_t launch_mid_mma(const fade_config_t* c, const fade_layer_t* L, const uint16_t* q,
+                             float* logits, float* part_ml, float* part_acc, int chunk,
+                             int nsplit, cudaStream_t st);
 
 // ---------------------------------------------------------------- device side
 __device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }

@@ -23,6 +23,7 @@ POLICIES = {"none": 0, "h2o": 1, "ema": 2, "position": 3}
 META_FIELDS = 8
 META = {"n_sink": 0, "n_mid": 1, "n_recent": 2, "head": 3, "cur": 4, "n_ev": 5}
 MAX_BATCH = 256
+STATUS_WORDS = 4
 
 
 class FadeError(RuntimeError):
@@ -54,7 +55,7 @@ class LayerT(ctypes.Structure):
                 ("mid_v_codes", c_vp * 2), ("mid_v_scales", c_vp * 2),
                 ("sink_scores", c_vp), ("mid_scores", c_vp * 2), ("recent_scores", c_vp),
                 ("meta", c_vp), ("victims", c_vp), ("chunk_base", c_vp),
-                ("victim_words", c_i32), ("chunk_slots", c_i32),
+                ("victim_words", c_i32), ("chunk_slots", c_i32), ("status", c_vp),
                 ("h_n_sink", c_vp), ("h_n_mid", c_vp), ("h_n_recent", c_vp)]
 
 
@@ -62,7 +63,8 @@ class LayoutT(ctypes.Structure):
     _fields_ = [(n, c_sz) for n in (
         "sink_k", "sink_v", "recent_k", "recent_v", "mid_k_codes", "mid_k_scales",
         "mid_v_codes", "mid_v_scales", "sink_scores", "mid_scores", "recent_scores", "meta",
-        "victims", "chunk_base", "logits_ws", "ml_ws", "attn_ws")] + [
+        "victims", "chunk_base", "status", "logits_ws")] + [("mid_stride", c_i32)] + [
+        (n, c_sz) for n in ("ml_ws", "attn_ws")] + [
         ("victim_words", c_i32), ("chunk_slots", c_i32), ("max_prompt", c_i32),
         ("max_splits", c_i32)]
 
@@ -221,7 +223,7 @@ class TieredLayer:
         self.cfg = cfg
         self.layout = lay = fade_layout(cfg, max_prompt)
         B, H, d = cfg.batch, cfg.num_kv_heads, cfg.head_dim
-        S, W, C = cfg.n_sink, cfg.recent_window, cfg.mid_capacity
+        S, W, C = cfg.n_sink, cfg.recent_window, lay.mid_stride
         dev = torch.device(device)
         u8, f16, f32, i32 = torch.uint8, torch.float16, torch.float32, torch.int32
         z = lambda shape, dt: torch.zeros(shape, dtype=dt, device=dev)
@@ -239,6 +241,7 @@ class TieredLayer:
         self.meta = z((B, H, META_FIELDS), i32)
         self.victims = z((B, H, lay.victim_words), torch.int32)
         self.chunk_base = z((B, H, lay.chunk_slots), i32)
+        self.status = z((STATUS_WORDS,), i32)
         self.h_n_sink = np.zeros(B, np.int32)
         self.h_n_mid = np.zeros(B, np.int32)
         self.h_n_recent = np.zeros(B, np.int32)
@@ -249,7 +252,7 @@ class TieredLayer:
             (c_vp * 2)(*map(p, self.mid_v_codes)), (c_vp * 2)(*map(p, self.mid_v_scales)),
             p(self.sink_scores), (c_vp * 2)(*map(p, self.mid_scores)), p(self.recent_scores),
             p(self.meta), p(self.victims), p(self.chunk_base), lay.victim_words,
-            lay.chunk_slots, self.h_n_sink.ctypes.data, self.h_n_mid.ctypes.data,
+            lay.chunk_slots, p(self.status), self.h_n_sink.ctypes.data, self.h_n_mid.ctypes.data,
             self.h_n_recent.ctypes.data)
 
     def workspaces(self):
