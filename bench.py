@@ -42,6 +42,9 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="4")
+    p.add_argument("--layers", type=int, default=None,
+                   help="override the layer count (profiling captures only; the headline "
+                        "line always runs every layer of the workload)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
@@ -212,6 +215,8 @@ def run_ours(args, rank, world):
     wl = workload(args.workload)
     if world > 1:
         wl = wl.scaled(seed=wl.seed + 1000 * rank)   # weak scaling: each rank its own batch
+    if args.layers:
+        wl = wl.scaled(layers=args.layers)
     cfg = Config.from_workload(wl)
     lens = ragged_context_lengths(wl)
     maxP = int(lens.max())

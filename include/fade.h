@@ -207,6 +207,18 @@ fade_status_t fade_cache_prefill(const fade_config_t* cfg, fade_layer_t* layer,
                                  const float* mass, const float* table, int32_t max_pos,
                                  void* stream);
 
+/* Prefill attention mass (FADE-zh §四种驱逐策略详解 1: H2O needs the attention captured at
+ * prefill; KVLong §1.3.1 H2O: a token's importance is the column sum of the attention
+ * matrix). q_rot: fp16 [B][Hq][max_prompt][d] and k_rot: fp16 [B][H][max_prompt][d], both
+ * RoPE'd at positions 0..P-1; h_prompt_len: HOST i32 [B]. Writes mass: f32
+ * [B][H][max_prompt], mass[b][h][j] = sum over the query heads of KV head h and over the
+ * queries i >= j of softmax_j(q_i . k_j / sqrt(d)) (causal), 0 past a row's length. fp32
+ * arithmetic with atomic column sums (the last bits may differ between runs). The result is
+ * the `mass` argument of fade_cache_prefill. */
+fade_status_t fade_prefill_mass(const fade_config_t* cfg, const uint16_t* q_rot,
+                                const uint16_t* k_rot, int32_t max_prompt,
+                                const int32_t* h_prompt_len, float* mass, void* stream);
+
 /* Demote (FADE-zh §第二层: mid-aged tokens go to the quantised tier): in every unit whose
  * recent window is full, the oldest recent token is quantise-packed (K at middle_k_bits, V
  * at middle_v_bits) into the next middle slot of the live buffer and its score moves with

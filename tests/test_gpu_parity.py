@@ -125,3 +125,39 @@ def test_lockstep_small_workloads(T, key):
     for _ in range(ls.steps):
         ls.step()
     assert ls.near_ties <= max(1, wl.batch * wl.num_kv_heads * ls.L // 20)
+
+
+@pytest.mark.parametrize("key,P", [(3, 700), (3, 130)])
+def test_prefill_mass_matches_oracle(T, key, P):
+    """GPU prefill attention mass vs the oracle's fp64 causal column sums."""
+    import torch
+
+    from oracle import attention
+    from synth import draw_prompt
+
+    wl = get_workload(key).scaled(batch=2, prompt_len=P)
+    cfg = T.Config.from_workload(wl)
+    lens = np.array([P, P - 37], np.int32)
+    pr = draw_prompt(wl, 0, P, with_q=True)
+    rope = RopeTable.from_workload(wl, P)
+    pos = np.arange(P)
+    qd = torch.from_numpy(pr["q"]).cuda()
+    kd = torch.from_numpy(pr["k"]).cuda()
+    table = torch.empty(P * wl.head_dim, dtype=torch.float32, device="cuda")
+    T.fade_rope_table_init(cfg, table, P)
+    B, Hq, Hkv = wl.batch, wl.num_q_heads, wl.num_kv_heads
+    T.fade_rope_apply(cfg, table, P, qd, qd, B * Hq, P, None, 1)
+    T.fade_rope_apply(cfg, table, P, kd, kd, B * Hkv, P, None, 1)
+    mass = torch.full((B, Hkv, P), 7.0, dtype=torch.float32, device="cuda")
+    T.fade_prefill_mass(cfg, qd, kd, P, lens, mass)
+    got = mass.cpu().numpy()
+    G = wl.group
+    for b in range(B):
+        n = int(lens[b])
+        for h in range(Hkv):
+            q = np.stack([rope.apply(pr["q"][b, h * G + g, :n], pos[:n]) for g in range(G)])
+            k = rope.apply(pr["k"][b, h, :n], pos[:n])
+            ref = attention.prefill_mass(q.astype(np.float64), k.astype(np.float64))
+            ok, err, nbad = allclose_report(got[b, h, :n], ref, atol=1e-5, rtol=1e-4)
+            assert ok, f"row {b} head {h}: max err {err}, {nbad} bad"
+            assert np.all(got[b, h, n:] == 0.0)

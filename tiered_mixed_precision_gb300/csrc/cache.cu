@@ -346,10 +346,20 @@ __global__ void __launch_bounds__(kSelThreads) evict_select_kernel(LayerArgs a) 
 }
 
 // Compact survivors of the live middle buffer into the other one, re-positioning keys whose
-// index drops; the last x-block re-positions the recent ring in place. grid = (chunks + 1,
-// H, B), 8 warps; each warp walks 32-slot bitmap words of its chunk.
+// index drops; the last x-block re-positions the recent ring in place.
+// grid = (ceil(max_mid / kCompactTok) + 1, H, B), 256 threads. Middle tokens: one thread per
+// (token, group pair gp): groups gp and gp + D/64 hold the two halves of the rotation pairs
+// (channel 32gp + j pairs with channel D/2 + 32gp + j), so dequantise -> un-RoPE -> re-RoPE ->
+// requantise of a moved key needs no communication between threads.
+template <int D>
+__host__ __device__ constexpr int compact_tok() { return 256 / (D / 64); }
+
 template <int D, int KB, int VB>
 __global__ void __launch_bounds__(256) evict_compact_kernel(LayerArgs a) {
+  constexpr int NGP = D / 64;            // threads per token
+  constexpr int TOK = compact_tok<D>();  // tokens per CTA
+  constexpr int KG = kGroup * KB / 8;    // bytes of one group's K codes
+  constexpr int VROW = D * VB / 8, SROW = D / kGroup, KROW = D * KB / 8;
   const int unit = blockIdx.z * a.H + blockIdx.y;
   const int32_t* m = a.meta + unit * kF;
   const int n_ev = m[FADE_META_N_EV];
@@ -358,9 +368,9 @@ __global__ void __launch_bounds__(256) evict_compact_kernel(LayerArgs a) {
   const int n_sink = m[FADE_META_N_SINK], n_rec = m[FADE_META_N_RECENT];
   const int head = m[FADE_META_HEAD];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nchunks = gridDim.x - 1;
+  const int nblk = gridDim.x - 1;
 
-  if ((int)blockIdx.x == nchunks) {
+  if ((int)blockIdx.x == nblk) {
     // recent ring: every token's index drops by n_ev; rewrite keys in place
     for (int t = warp; t < n_rec; t += 8) {
       const int slot = (head + t) % a.W;
@@ -373,26 +383,36 @@ __global__ void __launch_bounds__(256) evict_compact_kernel(LayerArgs a) {
     return;
   }
 
-  const int lo = blockIdx.x * kChunk;
+  const int lo = blockIdx.x * TOK;
   if (lo >= n_mid) return;
-  const int hi = min(lo + kChunk, n_mid);
+  const int hi = min(lo + TOK, n_mid);
   const uint32_t* bm = a.victims + (size_t)unit * a.victim_words;
-  __shared__ int wpre[kChunk / 32];
-  const int nw = (hi - lo + 31) / 32;
+  __shared__ int wpre[TOK / 32];
+  __shared__ int s_base;
   if (warp == 0) {
-    const int c = lane < nw ? __popc(bm[lo / 32 + lane]) : 0;
-    int incl = c;
+    // victims before `lo`: chunk prefix plus the words of lo's chunk that precede it
+    const int w_lo = lo >> 5, w0 = (lo / kChunk) * (kChunk / 32);
+    int c = (w0 + lane < w_lo) ? __popc(bm[w0 + lane]) : 0;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    const int nw = (hi - lo + 31) / 32;
+    const int wc = lane < nw ? __popc(bm[w_lo + lane]) : 0;
+    int incl = wc;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
+      const int tt = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += tt;
     }
-    wpre[lane] = incl - c;
+    if (lane < TOK / 32) wpre[lane] = incl - wc;
+    if (lane == 0) s_base = a.chunk_base[(size_t)unit * a.chunk_slots + lo / kChunk] + c;
   }
   __syncthreads();
-  const int base = a.chunk_base[(size_t)unit * a.chunk_slots + blockIdx.x];
-  // live (source) and other (destination) buffers, selected without indexing the
-  // parameter arrays by a runtime value
+  const int i = lo + threadIdx.x / NGP, gp = threadIdx.x % NGP;
+  if (i >= hi) return;
+  const uint32_t word = bm[i >> 5];
+  if ((word >> (i & 31)) & 1u) return;  // evicted
+  const int nv = i - (s_base + wpre[(i - lo) >> 5] + __popc(word & ((1u << (i & 31)) - 1u)));
+
   const uint8_t* mk_s = cur ? a.mk[1] : a.mk[0];
   uint8_t* mk_d = cur ? a.mk[0] : a.mk[1];
   const uint8_t* mv_s = cur ? a.mv[1] : a.mv[0];
@@ -403,36 +423,69 @@ __global__ void __launch_bounds__(256) evict_compact_kernel(LayerArgs a) {
   uint16_t* mvs_d = cur ? a.mvs[0] : a.mvs[1];
   const float* sc_s = cur ? a.mid_sc[1] : a.mid_sc[0];
   float* sc_d = cur ? a.mid_sc[0] : a.mid_sc[1];
-  constexpr int KROW = D * KB / 8, VROW = D * VB / 8, SROW = D / kGroup;
-  const size_t ubase = (size_t)unit * a.C;
-  for (int wi = warp; wi < nw; wi += 8) {
-    const uint32_t word = bm[lo / 32 + wi];
-    const int i = lo + wi * 32 + lane;
-    const bool valid = i < hi;
-    const bool keep = valid && !((word >> lane) & 1u);
-    const int nv = i - (base + wpre[wi] + __popc(word & ((1u << lane) - 1u)));
-    const bool moved = keep && nv != i;
-    if (keep) {
-      const size_t si = ubase + i, di = ubase + nv;
-      copy_row<VROW>(mv_s + si * VROW, mv_d + di * VROW);
-      copy_row<SROW * 2>(mvs_s + si * SROW, mvs_d + di * SROW);
-      sc_d[di] = sc_s[si];
-      if (!moved) {
-        copy_row<KROW>(mk_s + si * KROW, mk_d + di * KROW);
-        copy_row<SROW * 2>(mks_s + si * SROW, mks_d + di * SROW);
-      }
+  const size_t si = (size_t)unit * a.C + i, di = (size_t)unit * a.C + nv;
+
+  // V codes (this thread's share of the row), V and K scales of its groups, the score
+  constexpr int VSH = VROW / NGP;
+  copy_row<VSH>(mv_s + si * VROW + gp * VSH, mv_d + di * VROW + gp * VSH);
+  const int g1 = gp, g2 = gp + D / 64;
+  mvs_d[di * SROW + g1] = mvs_s[si * SROW + g1];
+  mvs_d[di * SROW + g2] = mvs_s[si * SROW + g2];
+  if (gp == 0) sc_d[di] = sc_s[si];
+
+  const uint8_t* krow_s = mk_s + si * KROW;
+  uint8_t* krow_d = mk_d + di * KROW;
+  if (nv == i || !a.table) {
+    copy_row<KG>(krow_s + g1 * KG, krow_d + g1 * KG);
+    copy_row<KG>(krow_s + g2 * KG, krow_d + g2 * KG);
+    mks_d[di * SROW + g1] = mks_s[si * SROW + g1];
+    mks_d[di * SROW + g2] = mks_s[si * SROW + g2];
+    return;
+  }
+  // dequantise the two groups (exact in fp32)
+  float x1[32], x2[32];
+  {
+    const float s1 = h2f(mks_s[si * SROW + g1]), s2 = h2f(mks_s[si * SROW + g2]);
+    uint32_t w1[KG / 4], w2[KG / 4];
+#pragma unroll
+    for (int w = 0; w < KG / 4; ++w) {
+      w1[w] = reinterpret_cast<const uint32_t*>(krow_s + g1 * KG)[w];
+      w2[w] = reinterpret_cast<const uint32_t*>(krow_s + g2 * KG)[w];
     }
-    uint32_t mv = __ballot_sync(0xffffffffu, moved);
-    while (mv) {
-      const int j = __ffs(mv) - 1;
-      mv &= mv - 1;
-      const int ij = __shfl_sync(0xffffffffu, i, j);
-      const int nj = __shfl_sync(0xffffffffu, nv, j);
-      const size_t si = ubase + ij, di = ubase + nj;
-      WarpKey<D> k = load_mid_key<D, KB>(mk_s + si * KROW, mks_s + si * SROW);
-      reposition_key<D>(a, k, n_sink + ij, n_sink + nj);
-      warp_store_quantized<D, KB>(k, mk_d + di * KROW, mks_d + di * SROW);
+    constexpr int per = 32 / KB;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t u1 = (w1[j / per] >> (KB * (j % per))) & ((1u << KB) - 1u);
+      const uint32_t u2 = (w2[j / per] >> (KB * (j % per))) & ((1u << KB) - 1u);
+      x1[j] = (float)(int(u1) - (int(u1 >> (KB - 1)) << KB)) * s1;
+      x2[j] = (float)(int(u2) - (int(u2 >> (KB - 1)) << KB)) * s2;
     }
+  }
+  // un-RoPE at the old index, re-RoPE at the new one (fp32, no contraction), cast to fp16
+  const float4* co4 = reinterpret_cast<const float4*>(a.table + (size_t)(n_sink + i) * a.half + 32 * gp);
+  const float4* cn4 = reinterpret_cast<const float4*>(a.table + (size_t)(n_sink + nv) * a.half + 32 * gp);
+#pragma unroll
+  for (int j2 = 0; j2 < 16; ++j2) {
+    const float4 co = __ldg(co4 + j2), cn = __ldg(cn4 + j2);  // pairs 2*j2 and 2*j2+1
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = 2 * j2 + h;
+      const float c_o = h ? co.z : co.x, s_o = h ? co.w : co.y;
+      const float c_n = h ? cn.z : cn.x, s_n = h ? cn.w : cn.y;
+      float t1, t2, y1, y2;
+      rotate_pair(x1[j], x2[j], c_o, -s_o, t1, t2);
+      rotate_pair(t1, t2, c_n, s_n, y1, y2);
+      x1[j] = __half2float(__float2half_rn(y1));
+      x2[j] = __half2float(__float2half_rn(y2));
+    }
+  }
+  uint32_t o1[KG / 4], o2[KG / 4];
+  mks_d[di * SROW + g1] = quant_group_thread<KB>(x1, o1);
+  mks_d[di * SROW + g2] = quant_group_thread<KB>(x2, o2);
+#pragma unroll
+  for (int w = 0; w < KG / 4; ++w) {
+    reinterpret_cast<uint32_t*>(krow_d + g1 * KG)[w] = o1[w];
+    reinterpret_cast<uint32_t*>(krow_d + g2 * KG)[w] = o2[w];
   }
 }
 
@@ -582,7 +635,7 @@ struct DemoteLaunch {
 template <int D, int KB, int VB>
 struct CompactLaunch {
   static fade_status_t run(const LayerArgs& a, int B, int chunks, cudaStream_t st) {
-    evict_compact_kernel<D, KB, VB><<<dim3(chunks + 1, a.H, B), 256, 0, st>>>(a);
+    evict_compact_kernel<D, KB, VB><<<dim3(chunks + 1, a.H, B), 256, 0, st>>>(a);  // chunks of compact_tok<D>() tokens
     return launch_status("fade_evict_rerope compact");
   }
 };
@@ -758,7 +811,8 @@ extern "C" fade_status_t fade_evict_rerope(const fade_config_t* c, fade_layer_t*
   cudaStream_t s = as_stream(stream);
   evict_select_kernel<<<dim3(c->num_kv_heads, c->batch), kSelThreads, 0, s>>>(a);
   if ((st = launch_status("fade_evict_rerope select"))) return st;
-  if ((st = dispatch_dkv<CompactLaunch>(c, a, c->batch, ceil_div(max_mid, kChunk), s))) return st;
+  const int ctok = c->head_dim == 128 ? compact_tok<128>() : compact_tok<64>();
+  if ((st = dispatch_dkv<CompactLaunch>(c, a, c->batch, ceil_div(max_mid, ctok), s))) return st;
   const int units = c->batch * c->num_kv_heads;
   evict_commit_kernel<<<ceil_div(units, 128), 128, 0, s>>>(L->meta, units);
   if ((st = launch_status("fade_evict_rerope commit"))) return st;

@@ -143,4 +143,48 @@ __device__ __forceinline__ void warp_store_quantized(const WarpKey<D>& k, uint8_
   }
 }
 
+// round_half_even(x / s) for fp16-valued x and s > 0, exactly (equal to rint of the IEEE fp32
+// quotient, which cannot land on or cross a half-integer for fp16 operands): a reciprocal
+// estimate gives a candidate within one of the answer, the residual x - q*s is exact in fp32
+// (a 3-bit integer times an 11-bit significand, then a difference spanning under 24 bits), and
+// comparing it with s/2 corrects the candidate and resolves exact ties to the even integer.
+__device__ __forceinline__ float rint_div_exact(float x, float s) {
+  float q = rintf(x * __frcp_rn(s));
+  const float e = fmaf(-q, s, x);
+  const float h = 0.5f * s;
+  const float ae = fabsf(e);
+  if (ae > h) {
+    q += copysignf(1.f, e);
+  } else if (ae == h) {
+    const float q2 = q + copysignf(1.f, e);
+    if (fmodf(q, 2.f) != 0.f) q = q2;  // exact tie: keep the even neighbour
+  }
+  return q;
+}
+
+// Quantise one 32-value group held by one thread; writes the packed codes (4 words for INT4,
+// 2 for INT2) and returns the fp16 scale bits.
+template <int BITS>
+__device__ __forceinline__ uint16_t quant_group_thread(const float (&x)[32], uint32_t* words) {
+  constexpr int qmax = (1 << (BITS - 1)) - 1;
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(x[i]));
+  float s = __half2float(__float2half_rn(__fdiv_rn(a, (float)qmax)));
+  if (a > 0.f && s == 0.f) s = kSubnormalMin;
+  constexpr int per = 32 / BITS;
+#pragma unroll
+  for (int w = 0; w < 32 / per; ++w) {
+    uint32_t v = 0;
+#pragma unroll
+    for (int e = 0; e < per; ++e) {
+      float q = 0.f;
+      if (s > 0.f) q = fminf(fmaxf(rint_div_exact(x[w * per + e], s), (float)-qmax), (float)qmax);
+      v |= (uint32_t((int)q) & ((1u << BITS) - 1u)) << (BITS * e);
+    }
+    words[w] = v;
+  }
+  return __half_as_ushort(__float2half_rn(s));
+}
+
 }  // namespace fade

@@ -91,6 +91,7 @@ def lib():
             "fade_cache_reset": (c_i32, [S(ConfigT), S(LayerT), c_vp]),
             "fade_cache_prefill": (c_i32, [S(ConfigT), S(LayerT), c_vp, c_vp, c_i32, c_vp,
                                            c_vp, c_vp, c_i32, c_vp]),
+            "fade_prefill_mass": (c_i32, [S(ConfigT), c_vp, c_vp, c_i32, c_vp, c_vp, c_vp]),
             "fade_cache_demote": (c_i32, [S(ConfigT), S(LayerT), c_vp]),
             "fade_evict_rerope": (c_i32, [S(ConfigT), S(LayerT), c_vp, c_i32, c_vp]),
             "fade_cache_append": (c_i32, [S(ConfigT), S(LayerT), c_vp, c_vp, c_vp]),
@@ -298,6 +299,12 @@ def fade_cache_prefill(layer: TieredLayer, k_rot, v, max_prompt, prompt_len, mas
     _check(lib().fade_cache_prefill(ctypes.byref(layer.cfg.c()), ctypes.byref(layer.c),
                                     _ptr(k_rot), _ptr(v), max_prompt, lens.ctypes.data,
                                     _ptr(mass), _ptr(table), max_pos, _stream(stream)))
+
+
+def fade_prefill_mass(cfg: Config, q_rot, k_rot, max_prompt, prompt_len, mass, stream=None):
+    lens = np.ascontiguousarray(prompt_len, np.int32)
+    _check(lib().fade_prefill_mass(ctypes.byref(cfg.c()), _ptr(q_rot), _ptr(k_rot), max_prompt,
+                                   lens.ctypes.data, _ptr(mass), _stream(stream)))
 
 
 def fade_cache_demote(layer: TieredLayer, stream=None):

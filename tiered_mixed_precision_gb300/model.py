@@ -49,13 +49,20 @@ class FadeCache:
         return x
 
     def prefill(self, layer: int, k_raw: torch.Tensor, v: torch.Tensor, prompt_len=None,
-                mass: torch.Tensor | None = None):
-        """k_raw, v: fp16 [B][Hkv][P][d] device tensors (k pre-RoPE; rotated in place)."""
+                mass: torch.Tensor | None = None, q_raw: torch.Tensor | None = None):
+        """k_raw, v: fp16 [B][Hkv][P][d] device tensors (k pre-RoPE; rotated in place).
+
+        For H2O either ``mass`` (f32 [B][Hkv][P]) is given, or ``q_raw`` (fp16 [B][Hq][P][d],
+        pre-RoPE, rotated in place) and the prefill attention mass is computed on the GPU."""
         c = self.cfg
         B, H, P, d = k_raw.shape
         if prompt_len is None:
             prompt_len = np.full(B, P, np.int32)
         self.rope_(k_raw, B * H, P, None, 1)
+        if mass is None and q_raw is not None and c.policy == "h2o":
+            self.rope_(q_raw, B * c.num_q_heads, P, None, 1)
+            mass = torch.empty((B, H, P), dtype=torch.float32, device=k_raw.device)
+            F.fade_prefill_mass(c, q_raw, k_raw, P, prompt_len, mass)
         L = self.layers[layer]
         F.fade_cache_reset(L)
         F.fade_cache_prefill(L, k_raw, v, P, prompt_len, mass, self.table, self.max_pos)
