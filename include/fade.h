@@ -155,10 +155,12 @@ typedef struct {
 fade_status_t fade_layout(const fade_config_t* cfg, int32_t max_prompt, fade_layout_t* out);
 
 /* RoPE table (FADE-zh §RoPE重计算: float32 RoPE math; FADE-zh §RoPE方案兼容性: default and
- * llama3 scaling). Writes table[pos][i] = (cos, sin) as f32 pairs, [max_pos][d/2][2], for
+ * llama3 scaling). Writes f32 [max_pos][d/4][4]: block b of position pos holds (cos_{2b},
+ * cos_{2b+1}, sin_{2b}, sin_{2b+1}) of rotation pairs 2b and 2b+1, for
  * angle = fp32(pos) * inv_freq_i (one fp32 multiply), inv_freq_i = base^(-2i/d) in fp64
  * (llama3-adjusted in fp64) rounded to fp32, cos/sin evaluated in fp64 and rounded to fp32.
- * `table` is device memory of max_pos*d*4 bytes. Not valid for FADE_ROPE_NONE. */
+ * `table` is device memory of max_pos*d*4 bytes, 16-byte aligned. Not valid for
+ * FADE_ROPE_NONE. */
 fade_status_t fade_rope_table_init(const fade_config_t* cfg, float* table, int32_t max_pos,
                                    void* stream);
 

@@ -1,0 +1,109 @@
+"""Host-side failure detection of the C ABI, without a GPU: every capacity and argument error
+is returned before anything is enqueued, so these calls run on a layer whose buffers are host
+memory (no kernel is ever launched)."""
+
+import numpy as np
+import pytest
+
+
+@pytest.fixture(scope="module")
+def T():
+    import torch  # noqa: F401
+
+    from tiered_mixed_precision_gb300 import build
+
+    build.build()
+    import tiered_mixed_precision_gb300 as T
+
+    return T
+
+
+class _S:  # a stream handle that is never used (no launch happens)
+    cuda_stream = 0
+
+
+def _layer(T, **kw):
+    base = dict(batch=2, num_q_heads=8, num_kv_heads=2, head_dim=64, n_sink=2,
+                recent_window=4, int4_budget=3, middle_k_bits=4, middle_v_bits=2,
+                mid_capacity=4, policy="h2o")
+    base.update(kw)
+    cfg = T.Config(**base)
+    return T.TieredLayer(cfg, 32, device="cpu")
+
+
+def _expect(T, status, fn, *args, **kw):
+    with pytest.raises(T.FadeError) as e:
+        fn(*args, stream=_S(), **kw)
+    assert e.value.status == status, str(e.value)
+    return str(e.value)
+
+
+def test_append_into_a_full_window_is_a_capacity_error(T):
+    L = _layer(T)
+    L.h_n_sink[:] = 2
+    L.h_n_recent[:] = 4
+    import torch
+    k = torch.zeros((2, 2, 64), dtype=torch.float16)
+    msg = _expect(T, 3, T.fade_cache_append, L, k, k)
+    assert "recent window full" in msg
+    # the host mirror is untouched by a rejected call
+    assert L.h_n_recent.tolist() == [4, 4]
+
+
+def test_demote_into_a_full_middle_tier_is_a_capacity_error(T):
+    L = _layer(T, mid_capacity=4)
+    L.h_n_recent[:] = 4
+    L.h_n_mid[:] = 4
+    _expect(T, 3, T.fade_cache_demote, L)
+
+
+def test_prefill_errors(T):
+    import torch
+    L = _layer(T)
+    k = torch.zeros((2, 2, 16, 64), dtype=torch.float16)
+    # H2O needs the prefill mass
+    _expect(T, 1, T.fade_cache_prefill, L, k, k, 16, np.array([16, 16]), None, k, 64)
+    # a row longer than the prompt buffer
+    m = torch.zeros((2, 2, 16), dtype=torch.float32)
+    _expect(T, 1, T.fade_cache_prefill, L, k, k, 16, np.array([17, 3]), m, k, 64)
+    # the cache must be empty
+    L.h_n_sink[:] = 1
+    _expect(T, 1, T.fade_cache_prefill, L, k, k, 16, np.array([16, 16]), m, k, 64)
+    L.h_n_sink[:] = 0
+    # too many middle survivors for the capacity (no eviction)
+    L2 = _layer(T, policy="none", int4_budget=-1, mid_capacity=4)
+    _expect(T, 3, T.fade_cache_prefill, L2, k, k, 16, np.array([16, 16]), None, k, 64)
+    # a RoPE table too short for the prompt positions
+    _expect(T, 3, T.fade_cache_prefill, L, k, k, 16, np.array([16, 16]), m, k, 8)
+
+
+def test_attention_workspace_and_empty_cache_errors(T):
+    import torch
+    L = _layer(T)
+    q = torch.zeros((2, 8, 64), dtype=torch.float16)
+    ml = torch.zeros(32, dtype=torch.float32)
+    ws = torch.zeros(16, dtype=torch.uint8)
+    _expect(T, 1, T.fade_decode_attention, L, q, q, None, ml, ws)      # empty cache
+    L.h_n_sink[:] = 2
+    L.h_n_recent[:] = 4
+    L.h_n_mid[:] = 3
+    msg = _expect(T, 3, T.fade_decode_attention, L, q, q, None, ml, ws)
+    assert "workspace" in msg
+
+
+def test_rope_apply_position_and_null_errors(T):
+    import torch
+    cfg = T.Config(batch=1, num_q_heads=4, num_kv_heads=1, head_dim=64, mid_capacity=16)
+    x = torch.zeros((1, 40, 64), dtype=torch.float16)
+    tab = torch.zeros(32 * 64, dtype=torch.float32)
+    _expect(T, 3, T.fade_rope_apply, cfg, tab, 32, x, x, 1, 40, None, 1)
+    _expect(T, 1, T.fade_rope_apply, cfg, tab, 32, None, x, 1, 40, None, 1)
+    _expect(T, 1, T.fade_rope_table_init, T.Config(batch=1, num_q_heads=4, num_kv_heads=1,
+                                                   head_dim=64, mid_capacity=16,
+                                                   rope_kind="none"), tab, 32)
+
+
+def test_layer_with_missing_buffers_is_rejected(T):
+    L = _layer(T)
+    L.c.status = None
+    _expect(T, 1, T.fade_cache_demote, L)

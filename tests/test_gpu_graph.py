@@ -1,0 +1,89 @@
+"""A decode step captured once as a CUDA graph and replayed gives, step after step, the same
+bytes as launching every call (steady state: the cache sits at its budget, so each step
+demotes one token, evicts one and appends one)."""
+
+import numpy as np
+import pytest
+
+from synth import draw_prompt, draw_vectors, get_workload
+
+pytestmark = pytest.mark.gpu
+
+
+def _masses(wl):
+    """H2O prefill masses computed once on the GPU (their atomic sums may differ between runs
+    in the last bits, so both caches of a comparison take the same ones)."""
+    import torch
+
+    import tiered_mixed_precision_gb300 as T
+    from tiered_mixed_precision_gb300.model import FadeCache
+
+    if wl.policy != "h2o":
+        return [None] * wl.layers
+    cfg = T.Config.from_workload(wl)
+    fc = FadeCache(cfg, 1, wl.prompt_len, wl.prompt_len + 64, "cuda")
+    B, P = wl.batch, wl.prompt_len
+    out = []
+    for layer in range(wl.layers):
+        pr = draw_prompt(wl, layer, with_q=True)
+        q = torch.from_numpy(pr["q"]).cuda()
+        k = torch.from_numpy(pr["k"]).cuda()
+        fc.rope_(q, B * wl.num_q_heads, P, None, 1)
+        fc.rope_(k, B * wl.num_kv_heads, P, None, 1)
+        m = torch.empty((B, wl.num_kv_heads, P), dtype=torch.float32, device="cuda")
+        T.fade_prefill_mass(cfg, q, k, P, np.full(B, P, np.int32), m)
+        out.append(m)
+    return out
+
+
+def _make(wl, masses):
+    import torch
+
+    import tiered_mixed_precision_gb300 as T
+    from tiered_mixed_precision_gb300.model import FadeCache
+
+    cfg = T.Config.from_workload(wl)
+    fc = FadeCache(cfg, wl.layers, wl.prompt_len, wl.prompt_len + 64, "cuda")
+    for layer in range(wl.layers):
+        pr = draw_prompt(wl, layer)
+        fc.prefill(layer, torch.from_numpy(pr["k"]).cuda(), torch.from_numpy(pr["v"]).cuda(),
+                   mass=masses[layer])
+    return fc
+
+
+@pytest.mark.parametrize("policy", ["position", "h2o"])
+def test_graph_replay_matches_eager_steps(policy):
+    import torch
+
+    wl = get_workload(4).scaled(layers=2, batch=2, num_q_heads=8, num_kv_heads=2,
+                                prompt_len=1200, int4_budget=500, policy=policy)
+    if policy == "h2o":
+        wl = wl.scaled(rope=get_workload(3).rope)
+    masses = _masses(wl)
+    eager, graphed = _make(wl, masses), _make(wl, masses)
+    L, B, Hq, Hkv, d = wl.layers, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+    steps = 4
+    q = torch.from_numpy(draw_vectors(wl, "q", (steps, L, B, Hq, d), "graph")).cuda()
+    k = torch.from_numpy(draw_vectors(wl, "k", (steps, L, B, Hkv, d), "graph")).cuda()
+    v = torch.from_numpy(draw_vectors(wl, "v", (steps, L, B, Hkv, d), "graph")).cuda()
+    out_e = torch.empty((L, B, Hq, d), dtype=torch.float16, device="cuda")
+    out_g = torch.empty_like(out_e)
+    qb, kb, vb = q[0].clone(), k[0].clone(), v[0].clone()
+    g = graphed.capture_step(qb, kb, vb, out_g)
+    for s in range(steps):
+        eager.step_all(q[s], k[s], v[s], out_e)
+        qb.copy_(q[s])
+        kb.copy_(k[s])
+        vb.copy_(v[s])
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out_e.view(torch.int16), out_g.view(torch.int16)), f"step {s}"
+    for layer in range(L):
+        for b in range(B):
+            for h in range(Hkv):
+                a_, b_ = eager.unit_state(layer, b, h), graphed.unit_state(layer, b, h)
+                for key in a_:
+                    if isinstance(a_[key], np.ndarray):
+                        assert np.array_equal(a_[key], b_[key]), (layer, b, h, key)
+                    else:
+                        assert a_[key] == b_[key], (layer, b, h, key)

@@ -62,8 +62,11 @@ def test_rope_table_and_apply(T, key):
     table = torch.empty(max_pos * wl.head_dim, dtype=torch.float32, device="cuda")
     T.fade_rope_table_init(cfg, table, max_pos)
     ref = RopeTable.from_workload(wl, max_pos)
-    tab = table.view(max_pos, wl.head_dim // 2, 2).cpu().numpy()
-    for got, want in ((tab[..., 0], ref.cos), (tab[..., 1], ref.sin)):
+    # layout: per position, blocks of two pairs (cos_2b, cos_2b+1, sin_2b, sin_2b+1)
+    tab = table.view(max_pos, wl.head_dim // 4, 4).cpu().numpy()
+    cos = tab[..., 0:2].reshape(max_pos, wl.head_dim // 2)
+    sin = tab[..., 2:4].reshape(max_pos, wl.head_dim // 2)
+    for got, want in ((cos, ref.cos), (sin, ref.sin)):
         ulps = np.abs(got.view(np.int32).astype(np.int64) - want.view(np.int32).astype(np.int64))
         assert ulps.max() <= 1, "table entry more than 1 fp32 ulp from the oracle"
         assert (ulps != 0).mean() < 1e-4

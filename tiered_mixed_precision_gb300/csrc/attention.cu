@@ -481,9 +481,7 @@ extern "C" fade_status_t fade_decode_attention(const fade_config_t* c, const fad
   a.part_acc = a.part_ml + (size_t)c->batch * c->num_q_heads * a.nsplit * 2;
   cudaStream_t s = as_stream(stream);
   if (mma) {
-    // FP16 tiers on the CUDA cores (split 0), the packed middle tier on the tensor cores
-    AttnArgs a0 = a;
-    if ((st = launch_split_any(c, a0, s, 1))) return st;
+    // one launch: FP16 tiers (split 0) and the packed middle tier (tensor cores)
     if ((st = launch_mid_mma(c, L, q_rot, logits_ws, a.part_ml, a.part_acc, a.chunk, a.nsplit,
                              s)))
       return st;

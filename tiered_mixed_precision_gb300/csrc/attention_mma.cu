@@ -40,6 +40,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 struct MmaArgs {
   const uint16_t* q;                 // [B][Hq][D]
+  const uint16_t *sink_k, *sink_v;   // [B][H][S][D]
+  const uint16_t *rec_k, *rec_v;     // [B][H][W][D], ring
   const uint16_t* ks[2];             // K scales [B*H*C][D/32]
   const uint16_t* vs[2];             // V scales
   const int32_t* meta;
@@ -47,7 +49,7 @@ struct MmaArgs {
   float* part_ml;                    // [B][Hq][nsplit][2]
   float* part_acc;                   // [B][Hq][nsplit][D]
   int32_t* status;
-  int Hq, H, S, C, NS, chunk, nsplit;
+  int Hq, H, S, W, C, NS, chunk, nsplit;
   float inv_sqrt_d;
 };
 
@@ -198,13 +200,15 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
   const uint32_t bar_full = sbase + Cfg::BAR_OFF;          // NSTAGE x 8 bytes
   const uint32_t bar_empty = bar_full + NSTAGE * 8;
 
-  const int split = blockIdx.x + 1, hk = blockIdx.y, b = blockIdx.z;
+  const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const int unit = b * a.H + hk;
   const int32_t* m = a.meta + unit * kF;
   const int n_mid = m[FADE_META_N_MID], cur = m[FADE_META_CUR];
-  const int lo = (split - 1) * a.chunk;
-  const int hi = min(n_mid, lo + a.chunk);
-  const int n_tok = max(0, hi - lo);
+  const int n_sink = m[FADE_META_N_SINK], n_rec = m[FADE_META_N_RECENT];
+  const int head_slot = m[FADE_META_HEAD];
+  const int lo = split > 0 ? (split - 1) * a.chunk : 0;
+  const int hi = split > 0 ? min(n_mid, lo + a.chunk) : 0;
+  const int n_tok = split > 0 ? max(0, hi - lo) : n_sink + n_rec;
   const int n_tiles = (n_tok + kTileTok - 1) / kTileTok;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -223,7 +227,7 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
     return;
   }
 
-  if (threadIdx.x == 0) {
+  if (split > 0 && threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, kConsumers);
@@ -253,7 +257,71 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[s][mm][j][e] = 0.f;
 
-  if (warp == kConsumers) {
+  float* wm = reinterpret_cast<float*>(smem);                  // [kConsumers][8]
+  float* wl = wm + kConsumers * 8;                             // [kConsumers][8]
+  float* wo = wl + kConsumers * 8;                             // [kConsumers][G][D]
+
+  if (split == 0) {
+    // ------------------------------------------------------------ FP16 tiers (CUDA cores)
+    // Warp w takes tokens w, w+4, ...; lane l holds channels l*CPL .. l*CPL+CPL-1.
+    if (warp < kConsumers) {
+      constexpr int CPL = D / 32;
+      float qr[G][CPL], acc[G][CPL], mm_[G], ll[G];
+      const uint16_t* qrow = a.q + (size_t)(b * a.Hq + hq0) * D;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        mm_[h] = -INFINITY;
+        ll[h] = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          qr[h][c] = __half2float(__ushort_as_half(qrow[(size_t)h * D + lane * CPL + c]));
+          acc[h][c] = 0.f;
+        }
+      }
+      const float c2 = a.inv_sqrt_d * kLog2e;
+      for (int u = warp; u < n_tok; u += kConsumers) {
+        const bool is_sink = u < n_sink;
+        const int slot = is_sink ? u : (head_slot + u - n_sink) % a.W;
+        const size_t row = is_sink ? ((size_t)unit * a.S + u) * D : ((size_t)unit * a.W + slot) * D;
+        const uint16_t* kr = (is_sink ? a.sink_k : a.rec_k) + row + lane * CPL;
+        const uint16_t* vr = (is_sink ? a.sink_v : a.rec_v) + row + lane * CPL;
+        float kv[CPL], vv[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          kv[c] = __half2float(__ushort_as_half(kr[c]));
+          vv[c] = __half2float(__ushort_as_half(vr[c]));
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float d = 0.f;
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) d = fmaf(qr[h][c], kv[c], d);
+          d = warp_sum(d);
+          if (a.logits && lane == 0)
+            a.logits[(size_t)(b * a.Hq + hq0 + h) * a.NS + (is_sink ? u : a.S + a.C + slot)] =
+                d * a.inv_sqrt_d;
+          const float s2 = d * c2;
+          const float mn = fmaxf(mm_[h], s2);
+          const float al = exp2f(mm_[h] - mn);   // 0 when the old max is -inf
+          const float p = exp2f(s2 - mn);
+          ll[h] = ll[h] * al + p;
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) acc[h][c] = fmaf(p, vv[c], acc[h][c] * al);
+          mm_[h] = mn;
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        if (lane == 0) {
+          wm[warp * 8 + h] = mm_[h];
+          wl[warp * 8 + h] = ll[h];
+        }
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) wo[(warp * G + h) * D + lane * CPL + c] = acc[h][c];
+      }
+    }
+    __syncthreads();
+  } else if (warp == kConsumers) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const CUtensorMap* mk = cur ? &tk1 : &tk0;
@@ -497,11 +565,8 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
   }
   // Past this barrier every tile is consumed and the producer has drained its copies, so
   // the stage memory can hold the per-warp results.
-  __syncthreads();
-  float* wm = reinterpret_cast<float*>(smem);                  // [kConsumers][8]
-  float* wl = wm + kConsumers * 8;                             // [kConsumers][8]
-  float* wo = wl + kConsumers * 8;                             // [kConsumers][G][D]
-  if (warp < kConsumers) {
+  if (split > 0) __syncthreads();
+  if (split > 0 && warp < kConsumers) {
     const int gsel = g >= 4 ? 1 : 0;  // the column parity that matches row g's group
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
@@ -586,7 +651,7 @@ fade_status_t encode_rows(CUtensorMap* m, const void* base, unsigned long long r
 
 template <int D, int G>
 fade_status_t launch_mma(const fade_config_t* c, const fade_layer_t* L, const MmaArgs& a,
-                         int n_mid_splits, cudaStream_t st) {
+                         int n_splits, cudaStream_t st) {
   using Cfg = MmaCfg<D>;
   const unsigned long long rows = (unsigned long long)c->batch * c->num_kv_heads * a.C;
   CUtensorMap tk[2], tv[2];
@@ -599,7 +664,7 @@ fade_status_t launch_mma(const fade_config_t* c, const fade_layer_t* L, const Mm
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
       cudaSuccess)
     return launch_status("fade_decode_attention (middle tier) shared-memory opt-in");
-  kern<<<dim3(n_mid_splits, c->num_kv_heads, c->batch), kThreadsMma, Cfg::SMEM, st>>>(
+  kern<<<dim3(n_splits, c->num_kv_heads, c->batch), kThreadsMma, Cfg::SMEM, st>>>(
       tk[0], tk[1], tv[0], tv[1], a);
   return launch_status("fade_decode_attention (middle tier)");
 }
@@ -615,6 +680,11 @@ fade_status_t launch_mid_mma(const fade_config_t* c, const fade_layer_t* L, cons
                              int nsplit, cudaStream_t st) {
   MmaArgs a;
   a.q = q;
+  a.sink_k = L->sink_k;
+  a.sink_v = L->sink_v;
+  a.rec_k = L->recent_k;
+  a.rec_v = L->recent_v;
+  a.W = c->recent_window;
   for (int i = 0; i < 2; ++i) {
     a.ks[i] = L->mid_k_scales[i];
     a.vs[i] = L->mid_v_scales[i];
@@ -632,10 +702,9 @@ fade_status_t launch_mid_mma(const fade_config_t* c, const fade_layer_t* L, cons
   a.chunk = chunk;
   a.nsplit = nsplit;
   a.inv_sqrt_d = 1.0f / sqrtf((float)c->head_dim);
-  if (nsplit <= 1) return FADE_OK;
   const int G = c->num_q_heads / c->num_kv_heads;
 #define FADE_CASE(D_, G_) \
-  if (c->head_dim == D_ && G == G_) return launch_mma<D_, G_>(c, L, a, nsplit - 1, st);
+  if (c->head_dim == D_ && G == G_) return launch_mma<D_, G_>(c, L, a, nsplit, st);
   FADE_CASE(64, 1) FADE_CASE(64, 2) FADE_CASE(64, 4) FADE_CASE(64, 8)
   FADE_CASE(128, 1) FADE_CASE(128, 2) FADE_CASE(128, 4) FADE_CASE(128, 8)
 #undef FADE_CASE

@@ -137,7 +137,7 @@ struct LayerArgs {
   int victim_words, chunk_slots;
   int H, S, W, C, budget, policy;
   bool evicts;
-  const float2* table;  // nullptr: RoPE kind NONE (re-positioning is the identity)
+  const float* table;   // nullptr: RoPE kind NONE (re-positioning is the identity)
   int half;
 };
 
@@ -168,7 +168,7 @@ LayerArgs make_args(const fade_config_t* c, const fade_layer_t* L, const float* 
   a.budget = c->int4_budget;
   a.policy = c->policy;
   a.evicts = c->policy != FADE_EVICT_NONE && c->int4_budget >= 0;
-  a.table = (c->rope.kind == FADE_ROPE_NONE) ? nullptr : reinterpret_cast<const float2*>(table);
+  a.table = (c->rope.kind == FADE_ROPE_NONE) ? nullptr : table;
   a.half = c->head_dim / 2;
   return a;
 }
@@ -442,8 +442,9 @@ __global__ void __launch_bounds__(256) evict_compact_kernel(LayerArgs a) {
     mks_d[di * SROW + g2] = mks_s[si * SROW + g2];
     return;
   }
-  // dequantise the two groups (exact in fp32)
-  float x1[32], x2[32];
+  // dequantise the two groups into packed pairs (exact in fp32): the code's offset-binary
+  // value is placed in the mantissa of 2^23, the offset removed, then the scale applied
+  f2x X1[16], X2[16];
   {
     const float s1 = h2f(mks_s[si * SROW + g1]), s2 = h2f(mks_s[si * SROW + g2]);
     uint32_t w1[KG / 4], w2[KG / 4];
@@ -453,35 +454,52 @@ __global__ void __launch_bounds__(256) evict_compact_kernel(LayerArgs a) {
       w2[w] = reinterpret_cast<const uint32_t*>(krow_s + g2 * KG)[w];
     }
     constexpr int per = 32 / KB;
+    constexpr uint32_t msk = (1u << KB) - 1u, flip = 1u << (KB - 1);
+    const float off = 8388608.f + (float)flip;   // 2^23 + 2^(bits-1)
+    const f2x OFF = f2_pack(off, off), S1 = f2_pack(s1, s1), S2 = f2_pack(s2, s2);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const uint32_t u1 = (w1[j / per] >> (KB * (j % per))) & ((1u << KB) - 1u);
-      const uint32_t u2 = (w2[j / per] >> (KB * (j % per))) & ((1u << KB) - 1u);
-      x1[j] = (float)(int(u1) - (int(u1 >> (KB - 1)) << KB)) * s1;
-      x2[j] = (float)(int(u2) - (int(u2 >> (KB - 1)) << KB)) * s2;
+    for (int k = 0; k < 16; ++k) {
+      const int j0 = 2 * k, j1 = 2 * k + 1;
+      const uint32_t a0 = ((w1[j0 / per] >> (KB * (j0 % per))) & msk) ^ flip;
+      const uint32_t a1 = ((w1[j1 / per] >> (KB * (j1 % per))) & msk) ^ flip;
+      const uint32_t b0 = ((w2[j0 / per] >> (KB * (j0 % per))) & msk) ^ flip;
+      const uint32_t b1 = ((w2[j1 / per] >> (KB * (j1 % per))) & msk) ^ flip;
+      X1[k] = f2_mul(f2_sub(f2_pack(__uint_as_float(0x4B000000u | a0),
+                                    __uint_as_float(0x4B000000u | a1)), OFF), S1);
+      X2[k] = f2_mul(f2_sub(f2_pack(__uint_as_float(0x4B000000u | b0),
+                                    __uint_as_float(0x4B000000u | b1)), OFF), S2);
     }
   }
-  // un-RoPE at the old index, re-RoPE at the new one (fp32, no contraction), cast to fp16
-  const float4* co4 = reinterpret_cast<const float4*>(a.table + (size_t)(n_sink + i) * a.half + 32 * gp);
-  const float4* cn4 = reinterpret_cast<const float4*>(a.table + (size_t)(n_sink + nv) * a.half + 32 * gp);
+  // un-RoPE at the old index, re-RoPE at the new one with scalar IEEE intrinsics (never merged
+  // into a fused multiply-add, so every product and sum is rounded separately, as specified;
+  // packed fp32x2 products feeding packed sums may be fused by the assembler), then the cast
+  // through fp16
+  {
+    const float4* to = reinterpret_cast<const float4*>(a.table) +
+                       (size_t)(n_sink + i) * (a.half / 2) + 16 * gp;
+    const float4* tn = reinterpret_cast<const float4*>(a.table) +
+                       (size_t)(n_sink + nv) * (a.half / 2) + 16 * gp;
 #pragma unroll
-  for (int j2 = 0; j2 < 16; ++j2) {
-    const float4 co = __ldg(co4 + j2), cn = __ldg(cn4 + j2);  // pairs 2*j2 and 2*j2+1
+    for (int k = 0; k < 16; ++k) {
+      const float4 co = __ldg(to + k), cn = __ldg(tn + k);  // (cos, cos, sin, sin) of 2 pairs
+      float a1[2], a2[2];
+      f2_unpack(X1[k], a1[0], a1[1]);
+      f2_unpack(X2[k], a2[0], a2[1]);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int j = 2 * j2 + h;
-      const float c_o = h ? co.z : co.x, s_o = h ? co.w : co.y;
-      const float c_n = h ? cn.z : cn.x, s_n = h ? cn.w : cn.y;
-      float t1, t2, y1, y2;
-      rotate_pair(x1[j], x2[j], c_o, -s_o, t1, t2);
-      rotate_pair(t1, t2, c_n, s_n, y1, y2);
-      x1[j] = __half2float(__float2half_rn(y1));
-      x2[j] = __half2float(__float2half_rn(y2));
+      for (int e = 0; e < 2; ++e) {
+        float t1, t2, y1, y2;
+        rotate_pair(a1[e], a2[e], e ? co.y : co.x, -(e ? co.w : co.z), t1, t2);
+        rotate_pair(t1, t2, e ? cn.y : cn.x, e ? cn.w : cn.z, y1, y2);
+        a1[e] = y1;
+        a2[e] = y2;
+      }
+      X1[k] = f2_round_f16(f2_pack(a1[0], a1[1]));
+      X2[k] = f2_round_f16(f2_pack(a2[0], a2[1]));
     }
   }
   uint32_t o1[KG / 4], o2[KG / 4];
-  mks_d[di * SROW + g1] = quant_group_thread<KB>(x1, o1);
-  mks_d[di * SROW + g2] = quant_group_thread<KB>(x2, o2);
+  mks_d[di * SROW + g1] = quant_group_packed<KB>(X1, o1);
+  mks_d[di * SROW + g2] = quant_group_packed<KB>(X2, o2);
 #pragma unroll
   for (int w = 0; w < KG / 4; ++w) {
     reinterpret_cast<uint32_t*>(krow_d + g1 * KG)[w] = o1[w];

@@ -35,8 +35,8 @@ struct RowLens {
   int32_t v[FADE_MAX_BATCH];
 };
 
-// Tensor-core attention over the middle tier (INT4 K / INT2 V); writes partial splits
-// 1..nsplit-1 (split 0 holds the FP16 tiers). Defined in attention_mma.cu.
+// Decode attention for INT4 K / INT2 V: split 0 covers the FP16 tiers on the CUDA cores,
+// splits 1..nsplit-1 the middle tier on the tensor cores. Defined in attention_mma.cu.
 bool mid_mma_supported(const fade_config_t* c);
 fade_status_t launch_mid_mma(const fade_config_t* c, const fade_layer_t* L, const uint16_t* q,
                              float* logits, float* part_ml, float* part_acc, int chunk,
@@ -103,15 +103,23 @@ __device__ __forceinline__ void rotate_pair(float x1, float x2, float c, float s
   y2 = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s));
 }
 
-// Re-position one pair: un-rotate at `pold`, rotate at `pnew` (table = float2 [pos][d/2]).
-__device__ __forceinline__ void reposition_pair(const float2* __restrict__ table, int half,
+// RoPE table layout: per position, d/2 rotation pairs grouped two by two; block b holds
+// (cos_{2b}, cos_{2b+1}, sin_{2b}, sin_{2b+1}) as one float4, so a 16-byte load gives the
+// cosines and sines of two adjacent pairs as ready-made fp32x2 operands.
+__device__ __forceinline__ float rope_cos(const float* table, int half, int pos, int i) {
+  return table[(size_t)pos * 2 * half + (i >> 1) * 4 + (i & 1)];
+}
+__device__ __forceinline__ float rope_sin(const float* table, int half, int pos, int i) {
+  return table[(size_t)pos * 2 * half + (i >> 1) * 4 + 2 + (i & 1)];
+}
+
+// Re-position one pair: un-rotate at `pold`, rotate at `pnew`.
+__device__ __forceinline__ void reposition_pair(const float* __restrict__ table, int half,
                                                 int i, int pold, int pnew, float x1, float x2,
                                                 float& y1, float& y2) {
-  const float2 co = table[(size_t)pold * half + i];
-  const float2 cn = table[(size_t)pnew * half + i];
   float t1, t2;
-  rotate_pair(x1, x2, co.x, -co.y, t1, t2);
-  rotate_pair(t1, t2, cn.x, cn.y, y1, y2);
+  rotate_pair(x1, x2, rope_cos(table, half, pold, i), -rope_sin(table, half, pold, i), t1, t2);
+  rotate_pair(t1, t2, rope_cos(table, half, pnew, i), rope_sin(table, half, pnew, i), y1, y2);
 }
 
 // Re-position a whole fp32 key held as pairs by a warp and write it quantised (middle tier)
@@ -141,6 +149,48 @@ __device__ __forceinline__ void warp_store_quantized(const WarpKey<D>& k, uint8_
     pack_group_store<BITS>(q, codes_row + (gp + D / 64) * bytes_per_group);
     if (lane == 0) scales_row[gp + D / 64] = sb;
   }
+}
+
+// ---- packed fp32 pairs (Blackwell f32x2 arithmetic). Each instruction rounds each element to
+// nearest like its scalar form, but the assembler may fuse a packed product into a following
+// packed sum even with an explicit rounding mode: use these only where such a fusion cannot
+// change a result (exact steps, or steps whose error analysis covers it). Separately rounded
+// products and sums use the scalar __fmul_rn / __fadd_rn intrinsics.
+typedef unsigned long long f2x;  // low 32 bits = first element
+__device__ __forceinline__ f2x f2_pack(float lo, float hi) {
+  f2x r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(f2x v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2x f2_mul(f2x a, f2x b) {
+  f2x d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2x f2_add(f2x a, f2x b) {
+  f2x d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2x f2_sub(f2x a, f2x b) {
+  f2x d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2x f2_fma(f2x a, f2x b, f2x c) {  // a*b + c, one rounding
+  f2x d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// Round both elements to fp16 and back (the cast through the model dtype).
+__device__ __forceinline__ f2x f2_round_f16(f2x v) {
+  float lo, hi;
+  f2_unpack(v, lo, hi);
+  const float2 f = __half22float2(__floats2half2_rn(lo, hi));
+  return f2_pack(f.x, f.y);
 }
 
 // round_half_even(x / s) for fp16-valued x and s > 0, exactly (equal to rint of the IEEE fp32
@@ -183,6 +233,69 @@ __device__ __forceinline__ uint16_t quant_group_thread(const float (&x)[32], uin
       v |= (uint32_t((int)q) & ((1u << BITS) - 1u)) << (BITS * e);
     }
     words[w] = v;
+  }
+  return __half_as_ushort(__float2half_rn(s));
+}
+
+// Quantise one 32-value group held as 16 packed pairs by one thread (values are fp16-valued
+// fp32). Same result as quant_group_thread: s = fp16(absmax/qmax) (2^-24 if that underflows),
+// codes round_half_even(x/s) clamped to +-qmax. Fast path: x * (1/s) rounded to an integer by
+// adding 1.5 * 2^23 (whose low bits then hold the code in two's complement); the exact residual
+// x - q*s flags the rare exact ties (|residual| = s/2), which are redone exactly. The candidate
+// is within 2^-22 of x/s whether or not the product is rounded before the addition (a fused
+// multiply-add is allowed here), while x/s lies at least 2^-13 from any half-integer unless it
+// is one, so only ties can round wrongly. A subnormal scale (where the clamp can bind) takes
+// the exact path for the whole group.
+template <int BITS>
+__device__ __forceinline__ uint16_t quant_group_packed(const f2x (&X)[16], uint32_t* words) {
+  constexpr int qmax = (1 << (BITS - 1)) - 1;
+  constexpr int per = 32 / BITS;             // codes per word
+  constexpr uint32_t mask = (1u << BITS) - 1u;
+  float a = 0.f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    float lo, hi;
+    f2_unpack(X[k], lo, hi);
+    a = fmaxf(a, fmaxf(fabsf(lo), fabsf(hi)));
+  }
+  float s = __half2float(__float2half_rn(__fdiv_rn(a, (float)qmax)));
+  if (a > 0.f && s == 0.f) s = kSubnormalMin;
+#pragma unroll
+  for (int w = 0; w < 32 / per; ++w) words[w] = 0u;
+  if (s == 0.f) return 0;
+  if (s < 6.103515625e-05f) {  // subnormal scale: exact path with clamping
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      float v[2];
+      f2_unpack(X[k], v[0], v[1]);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float q = fminf(fmaxf(rint_div_exact(v[e], s), (float)-qmax), (float)qmax);
+        const int idx = 2 * k + e;
+        words[idx / per] |= (uint32_t((int)q) & mask) << (BITS * (idx % per));
+      }
+    }
+    return __half_as_ushort(__float2half_rn(s));
+  }
+  const float r = __frcp_rn(s);
+  const float h = 0.5f * s;
+  const f2x R = f2_pack(r, r), M = f2_pack(12582912.f, 12582912.f), NS = f2_pack(-s, -s);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const f2x QM = f2_add(f2_mul(X[k], R), M);   // bits 0x4B400000 + q
+    const f2x E = f2_fma(f2_sub(QM, M), NS, X[k]);
+    float e0, e1, qm0, qm1;
+    f2_unpack(E, e0, e1);
+    f2_unpack(QM, qm0, qm1);
+    uint32_t c0 = __float_as_uint(qm0) & mask, c1 = __float_as_uint(qm1) & mask;
+    if (fabsf(e0) >= h || fabsf(e1) >= h) {  // an exact tie: resolve to the even code
+      float v0, v1;
+      f2_unpack(X[k], v0, v1);
+      c0 = uint32_t((int)rint_div_exact(v0, s)) & mask;
+      c1 = uint32_t((int)rint_div_exact(v1, s)) & mask;
+    }
+    const int idx = 2 * k;
+    words[idx / per] |= (c0 << (BITS * (idx % per))) | (c1 << (BITS * (idx % per + 1)));
   }
   return __half_as_ushort(__float2half_rn(s));
 }

@@ -41,17 +41,19 @@ InvFreq host_inv_freq(const fade_config_t* c) {
   return f;
 }
 
-__global__ void rope_table_kernel(InvFreq inv, int half, int max_pos, float2* __restrict__ table) {
+__global__ void rope_table_kernel(InvFreq inv, int half, int max_pos, float* __restrict__ table) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)max_pos * half) return;
   const int pos = (int)(i / half);
   const int k = (int)(i % half);
   const float ang = __fmul_rn((float)pos, inv.v[k]);
   const double a = (double)ang;
-  table[i] = make_float2((float)cos(a), (float)sin(a));
+  const size_t base = (size_t)pos * 2 * half + (k >> 1) * 4 + (k & 1);
+  table[base] = (float)cos(a);
+  table[base + 2] = (float)sin(a);
 }
 
-__global__ void rope_apply_kernel(const float2* __restrict__ table, int max_pos, int half,
+__global__ void rope_apply_kernel(const float* __restrict__ table, int max_pos, int half,
                                   const uint16_t* __restrict__ x, uint16_t* __restrict__ y,
                                   long long n_pairs, int group_len,
                                   const int32_t* __restrict__ pos_start, int pos_step) {
@@ -63,11 +65,10 @@ __global__ void rope_apply_kernel(const float2* __restrict__ table, int max_pos,
   const int j = (int)(vec % group_len);
   int pos = (pos_start ? pos_start[g] : 0) + j * pos_step;
   pos = min(max(pos, 0), max_pos - 1);  // out-of-range positions are clamped (memory safety)
-  const float2 cs = table[(long long)pos * half + k];
   const long long base = vec * (2LL * half);
   const float x1 = h2f(x[base + k]), x2 = h2f(x[base + k + half]);
   float y1, y2;
-  rotate_pair(x1, x2, cs.x, cs.y, y1, y2);
+  rotate_pair(x1, x2, rope_cos(table, half, pos, k), rope_sin(table, half, pos, k), y1, y2);
   y[base + k] = f2h(y1);
   y[base + k + half] = f2h(y2);
 }
@@ -86,12 +87,12 @@ extern "C" fade_status_t fade_rope_table_init(const fade_config_t* cfg, float* t
     return set_error(FADE_ERR_INVALID_ARGUMENT, "no RoPE table for FADE_ROPE_NONE");
   if (!table || max_pos < 1)
     return set_error(FADE_ERR_INVALID_ARGUMENT, "NULL table or max_pos < 1");
-  if (reinterpret_cast<uintptr_t>(table) & 7)
-    return set_error(FADE_ERR_INVALID_ARGUMENT, "table must be 8-byte aligned");
+  if (reinterpret_cast<uintptr_t>(table) & 15)
+    return set_error(FADE_ERR_INVALID_ARGUMENT, "table must be 16-byte aligned");
   const int half = cfg->head_dim / 2;
   const long long n = (long long)max_pos * half;
   rope_table_kernel<<<ceil_div(n, 256), 256, 0, as_stream(stream)>>>(
-      host_inv_freq(cfg), half, max_pos, reinterpret_cast<float2*>(table));
+      host_inv_freq(cfg), half, max_pos, table);
   return launch_status("fade_rope_table_init");
 }
 
@@ -123,7 +124,7 @@ extern "C" fade_status_t fade_rope_apply(const fade_config_t* cfg, const float* 
   const int half = cfg->head_dim / 2;
   const long long n_pairs = n_vec * half;
   rope_apply_kernel<<<ceil_div(n_pairs, 256), 256, 0, as_stream(stream)>>>(
-      reinterpret_cast<const float2*>(table), max_pos, half, x, y, n_pairs, group_len,
+      table, max_pos, half, x, y, n_pairs, group_len,
       pos_start, pos_step);
   return launch_status("fade_rope_apply");
 }

@@ -342,3 +342,4 @@ def fade_next_position(layer: TieredLayer, row: int) -> int:
 
 def fade_compressed_bytes(layer: TieredLayer) -> int:
     return int(lib().fade_compressed_bytes(ctypes.byref(layer.cfg.c()), ctypes.byref(layer.c)))
+

@@ -8,10 +8,34 @@ CUDA library on the caller's stream; this module only allocates buffers and pass
 
 from __future__ import annotations
 
+import ctypes
+
 import numpy as np
 import torch
 
 from . import fade as F
+
+_cudart = None
+
+
+def _record_event(ev):
+    """Record a timing event on the current stream; inside a CUDA-graph capture it becomes an
+    external event node (cudaEventRecordExternal), whose timestamps the host can read after
+    each replay."""
+    if not torch.cuda.is_current_stream_capturing():
+        ev.record()
+        return
+    global _cudart
+    if _cudart is None:
+        _cudart = ctypes.CDLL("libcudart.so.13", mode=ctypes.RTLD_GLOBAL)
+        _cudart.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
+                                                      ctypes.c_uint]
+        _cudart.cudaEventRecordWithFlags.restype = ctypes.c_int
+    rc = _cudart.cudaEventRecordWithFlags(ctypes.c_void_p(ev.cuda_event),
+                                          ctypes.c_void_p(torch.cuda.current_stream().cuda_stream),
+                                          1)  # cudaEventRecordExternal
+    if rc != 0:
+        raise RuntimeError(f"cudaEventRecordWithFlags failed ({rc})")
 
 
 class FadeCache:
@@ -106,18 +130,50 @@ class FadeCache:
             n += 1
         self.launches += n
 
+    def mirror(self):
+        """Host mirror of the tier counts of every layer (for steady-state checks)."""
+        return [(L.h_n_sink.copy(), L.h_n_mid.copy(), L.h_n_recent.copy()) for L in self.layers]
+
+    def step_all(self, q, k, v, out):
+        """One decode step of every layer: q [L][B][Hq][d], k/v [L][B][Hkv][d], out like q."""
+        self.set_positions(self.next_positions())
+        for layer in range(len(self.layers)):
+            self.step_layer(layer, q[layer], k[layer], v[layer], out[layer])
+
+    def capture_step(self, q, k, v, out):
+        """Capture step_all on fixed input/output buffers as a CUDA graph.
+
+        Valid only in steady state, where a step leaves every tier count unchanged (the cache
+        holds its budget; each step demotes one token, evicts one and appends one): the
+        launch shapes are then the same every step and the kernels follow the device-side
+        metadata (ring head, live buffer). Raises if a step would change the counts."""
+        before = self.mirror()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step_all(q, k, v, out)
+        after = self.mirror()
+        for a, b in zip(before, after):
+            if any((x != y).any() for x, y in zip(a, b)):
+                raise RuntimeError("capture_step needs a steady-state cache (tier counts changed)")
+        return g
+
     def _tick(self, name):
         if self.timers is None:
             return None
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
+        if torch.cuda.is_current_stream_capturing():
+            # create the events outside the capture (they are created on first record)
+            side = torch.cuda.Stream()
+            e0.record(side)
+            e1.record(side)
+        _record_event(e0)
         self.timers.setdefault(name, []).append((e0, e1))
         return e1
 
     @staticmethod
     def _tock(e1):
         if e1 is not None:
-            e1.record()
+            _record_event(e1)
 
     def attention_only(self, layer: int, q_rot: torch.Tensor, out: torch.Tensor):
         F.fade_decode_attention(self.layers[layer], q_rot, out,
