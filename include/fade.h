@@ -90,6 +90,7 @@ typedef struct {
 
 #define FADE_MAX_BATCH 256
 #define FADE_STATUS_WORDS 4
+#define FADE_NOALLOC_SCRATCH_BYTES (8u << 20) /* see fade_decode_attention_noalloc */
 #define FADE_GROUP 32
 
 /* Per-unit device metadata: int32 [batch][num_kv_heads][FADE_META_FIELDS]. */
@@ -258,6 +259,26 @@ fade_status_t fade_cache_append(const fade_config_t* cfg, fade_layer_t* layer,
 fade_status_t fade_decode_attention(const fade_config_t* cfg, const fade_layer_t* layer,
                                     const uint16_t* q_rot, uint16_t* out, float* logits_ws,
                                     float* ml_ws, void* ws, size_t ws_bytes, void* stream);
+
+/* Decode attention for callers that cannot allocate device memory. The pages have no
+ * counterpart to this call; it exists for code that may not call cudaMalloc (or any
+ * allocator) where attention runs: an allocator-free region of a serving loop, a plugin that
+ * is handed only its inputs and outputs, or code that must not touch a memory pool it does not
+ * own. It computes exactly what fade_decode_attention computes, with the same arguments except
+ * the workspace: the split-KV partials go to a fixed array inside the library, of
+ * FADE_NOALLOC_SCRATCH_BYTES (8 MiB) per GPU, which every GPU that loads the library holds
+ * until the process exits.
+ *   - The first call on a device looks up the array's device address with that device current
+ *     (cudaGetSymbolAddress); make the first call on each device before any stream capture.
+ *   - All calls on a device share the one array, which keeps the last call's contents. Calls
+ *     that overlap on the GPU (unordered streams) race; order them, e.g. on one stream. No part
+ *     of the array needs to start at zero: each call writes every partial before reading it.
+ *   - A shape whose partials (B * Hq * splits * (d + 2) * 4 bytes) exceed the array is
+ *     rejected on the host with FADE_ERR_CAPACITY and a message naming the limit.
+ *   - It allocates nothing: no cudaMalloc, cudaFree or allocating library routine. */
+fade_status_t fade_decode_attention_noalloc(const fade_config_t* cfg, const fade_layer_t* layer,
+                                            const uint16_t* q_rot, uint16_t* out,
+                                            float* logits_ws, float* ml_ws, void* stream);
 
 /* Accumulate attention mass (FADE-zh §四种驱逐策略详解 1 H2O, 2 EMA; KVLong §1.3.1 H2O: the
  * score of a token sums its attention). With p[h][j] = exp(s[h][j] - M[h]) / L[h] from the

@@ -343,3 +343,12 @@ def fade_next_position(layer: TieredLayer, row: int) -> int:
 def fade_compressed_bytes(layer: TieredLayer) -> int:
     return int(lib().fade_compressed_bytes(ctypes.byref(layer.cfg.c()), ctypes.byref(layer.c)))
 
+
+def fade_decode_attention_noalloc(layer: TieredLayer, q_rot, out, logits_ws, ml_ws, stream=None):
+    """Decode attention with the split scratch inside the library (no workspace argument), for
+    callers that cannot allocate device memory; see include/fade.h for its limits."""
+    fn = lib().fade_decode_attention_noalloc
+    fn.restype = c_i32
+    fn.argtypes = [ctypes.POINTER(ConfigT), ctypes.POINTER(LayerT), c_vp, c_vp, c_vp, c_vp, c_vp]
+    _check(fn(ctypes.byref(layer.cfg.c()), ctypes.byref(layer.c), _ptr(q_rot), _ptr(out),
+              _ptr(logits_ws), _ptr(ml_ws), _stream(stream)))
