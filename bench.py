@@ -225,12 +225,11 @@ def run_ours(args, rank, world):
     nsteps = 3 * K + W + 8   # timed, e2e, a possible eager timing pass, probe and warm-up
     max_pos = maxP + nsteps + 16
     fc = FadeCache(cfg, wl.layers, maxP, max_pos, dev)
-    mass = None
+    h2o = wl.policy == "h2o" and wl.int4_budget >= 0
     for layer in range(wl.layers):
-        pr = draw_prompt(wl, layer, maxP, backend="torch", device=dev)
-        if wl.policy == "h2o" and wl.int4_budget >= 0:
-            mass = torch.ones((wl.batch, wl.num_kv_heads, maxP), dtype=torch.float32, device=dev)
-        fc.prefill(layer, pr["k"], pr["v"], lens, mass)
+        # H2O: the prefill attention mass is computed on the GPU from the prompt's queries
+        pr = draw_prompt(wl, layer, maxP, with_q=h2o, backend="torch", device=dev)
+        fc.prefill(layer, pr["k"], pr["v"], lens, None, q_raw=pr.get("q"))
         del pr
     torch.cuda.synchronize()
     torch.cuda.empty_cache()   # drop the prompt draws: only the cache stays resident
