@@ -34,6 +34,13 @@ constexpr int kF = FADE_META_FIELDS;
 constexpr int kTileTok = 256;            // tokens per TMA tile
 constexpr int kConsumers = 4;            // consumer warps, 64 tokens each
 constexpr int kThreadsMma = 32 * (kConsumers + 1);
+// Pipeline depth for head_dim 128 and the resident-CTA hint given to the register allocator.
+#ifndef FADE_MMA_STAGES_128
+#define FADE_MMA_STAGES_128 3
+#endif
+#ifndef FADE_MMA_MIN_CTAS
+#define FADE_MMA_MIN_CTAS 1
+#endif
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz: a wait that never ends
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -59,7 +66,7 @@ struct MmaCfg {
   static constexpr int VROW = D / 4;        // INT2 codes per token (bytes)
   static constexpr int SROW = D / kGroup;   // scales per token
   static constexpr int STAGE = kTileTok * (KROW + VROW + 2 * SROW * 2);
-  static constexpr int NSTAGE = D == 128 ? 3 : 4;
+  static constexpr int NSTAGE = D == 128 ? FADE_MMA_STAGES_128 : 4;
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = kTileTok * KROW;
   static constexpr int KS_OFF = V_OFF + kTileTok * VROW;
@@ -185,7 +192,7 @@ __device__ __forceinline__ uint32_t v_crumb(uint32_t x, uint32_t x10) {
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kThreadsMma, 1)
+__global__ void __launch_bounds__(kThreadsMma, FADE_MMA_MIN_CTAS)
 attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_constant__ CUtensorMap tk1,
                     const __grid_constant__ CUtensorMap tv0, const __grid_constant__ CUtensorMap tv1,
                     MmaArgs a) {

@@ -137,6 +137,7 @@ struct LayerArgs {
   int victim_words, chunk_slots;
   int H, S, W, C, budget, policy;
   bool evicts;
+  bool positional;  // position policy: the victims are the oldest middle slots (no selection)
   const float* table;   // nullptr: RoPE kind NONE (re-positioning is the identity)
   int half;
 };
@@ -168,6 +169,7 @@ LayerArgs make_args(const fade_config_t* c, const fade_layer_t* L, const float* 
   a.budget = c->int4_budget;
   a.policy = c->policy;
   a.evicts = c->policy != FADE_EVICT_NONE && c->int4_budget >= 0;
+  a.positional = c->policy == FADE_EVICT_POSITION;
   a.table = (c->rope.kind == FADE_ROPE_NONE) ? nullptr : table;
   a.half = c->head_dim / 2;
   return a;
@@ -347,24 +349,26 @@ __global__ void __launch_bounds__(kSelThreads) evict_select_kernel(LayerArgs a) 
 
 // Compact survivors of the live middle buffer into the other one, re-positioning keys whose
 // index drops; the last x-block re-positions the recent ring in place.
-// grid = (ceil(max_mid / kCompactTok) + 1, H, B), 256 threads. Middle tokens: one thread per
-// (token, group pair gp): groups gp and gp + D/64 hold the two halves of the rotation pairs
-// (channel 32gp + j pairs with channel D/2 + 32gp + j), so dequantise -> un-RoPE -> re-RoPE ->
-// requantise of a moved key needs no communication between threads.
+// grid = (ceil(max_mid / compact_tok<D>()) + 1, H, B), 256 threads. Middle tokens: D/32 threads
+// per token; thread (gp, hf) owns rotation pairs 32gp + 16hf .. +15, i.e. half of group gp
+// (channels 32gp + 16hf + j) and the matching half of its partner group gp + D/64 (channels
+// D/2 + 32gp + 16hf + j). A moved key is dequantised, un-RoPE'd / re-RoPE'd and re-quantised;
+// each group's absmax is completed with the neighbouring thread (lane ^ 1).
 template <int D>
-__host__ __device__ constexpr int compact_tok() { return 256 / (D / 64); }
+__host__ __device__ constexpr int compact_tok() { return 256 / (D / 32); }
 
 template <int D, int KB, int VB>
 __global__ void __launch_bounds__(256) evict_compact_kernel(LayerArgs a) {
-  constexpr int NGP = D / 64;            // threads per token
+  constexpr int TPT = D / 32;            // threads per token
   constexpr int TOK = compact_tok<D>();  // tokens per CTA
-  constexpr int KG = kGroup * KB / 8;    // bytes of one group's K codes
+  constexpr int HB = 16 * KB / 8;        // bytes of half a group's K codes
   constexpr int VROW = D * VB / 8, SROW = D / kGroup, KROW = D * KB / 8;
   const int unit = blockIdx.z * a.H + blockIdx.y;
   const int32_t* m = a.meta + unit * kF;
-  const int n_ev = m[FADE_META_N_EV];
-  if (n_ev == 0) return;
   const int n_mid = m[FADE_META_N_MID], cur = m[FADE_META_CUR];
+  // the position policy evicts the oldest slots: no selection pass, no victim bitmap
+  const int n_ev = a.positional ? max(0, n_mid - a.budget) : m[FADE_META_N_EV];
+  if (n_ev == 0) return;
   const int n_sink = m[FADE_META_N_SINK], n_rec = m[FADE_META_N_RECENT];
   const int head = m[FADE_META_HEAD];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -384,12 +388,12 @@ __global__ void __launch_bounds__(256) evict_compact_kernel(LayerArgs a) {
   }
 
   const int lo = blockIdx.x * TOK;
-  if (lo >= n_mid) return;
+  if (lo >= n_mid) return;  // uniform per CTA
   const int hi = min(lo + TOK, n_mid);
   const uint32_t* bm = a.victims + (size_t)unit * a.victim_words;
-  __shared__ int wpre[TOK / 32];
+  __shared__ int wpre[TOK / 32 + 1];
   __shared__ int s_base;
-  if (warp == 0) {
+  if (warp == 0 && !a.positional) {
     // victims before `lo`: chunk prefix plus the words of lo's chunk that precede it
     const int w_lo = lo >> 5, w0 = (lo / kChunk) * (kChunk / 32);
     int c = (w0 + lane < w_lo) ? __popc(bm[w0 + lane]) : 0;
@@ -403,15 +407,28 @@ __global__ void __launch_bounds__(256) evict_compact_kernel(LayerArgs a) {
       const int tt = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += tt;
     }
-    if (lane < TOK / 32) wpre[lane] = incl - wc;
+    if (lane <= TOK / 32) wpre[lane] = incl - wc;
     if (lane == 0) s_base = a.chunk_base[(size_t)unit * a.chunk_slots + lo / kChunk] + c;
   }
   __syncthreads();
-  const int i = lo + threadIdx.x / NGP, gp = threadIdx.x % NGP;
-  if (i >= hi) return;
-  const uint32_t word = bm[i >> 5];
-  if ((word >> (i & 31)) & 1u) return;  // evicted
-  const int nv = i - (s_base + wpre[(i - lo) >> 5] + __popc(word & ((1u << (i & 31)) - 1u)));
+  const int i = lo + threadIdx.x / TPT, t_ = threadIdx.x % TPT;
+  const int gp = t_ >> 1, hf = t_ & 1;
+  // The lanes of one token are adjacent (TPT divides 32) and share every flag below, so the
+  // warp-wide ballot and the absmax exchange see whole tokens; nothing exits before them.
+  const bool in_range = i < hi;
+  bool keep = in_range;
+  int nv = 0;
+  if (in_range) {
+    if (a.positional) {
+      keep = i >= n_ev;
+      nv = i - n_ev;
+    } else {
+      const uint32_t word = bm[i >> 5];
+      keep = !((word >> (i & 31)) & 1u);
+      nv = i - (s_base + wpre[(i - lo) >> 5] + __popc(word & ((1u << (i & 31)) - 1u)));
+    }
+  }
+  const bool moved = keep && nv != i && a.table != nullptr;
 
   const uint8_t* mk_s = cur ? a.mk[1] : a.mk[0];
   uint8_t* mk_d = cur ? a.mk[0] : a.mk[1];
@@ -424,94 +441,115 @@ __global__ void __launch_bounds__(256) evict_compact_kernel(LayerArgs a) {
   const float* sc_s = cur ? a.mid_sc[1] : a.mid_sc[0];
   float* sc_d = cur ? a.mid_sc[0] : a.mid_sc[1];
   const size_t si = (size_t)unit * a.C + i, di = (size_t)unit * a.C + nv;
-
-  // V codes (this thread's share of the row), V and K scales of its groups, the score
-  constexpr int VSH = VROW / NGP;
-  copy_row<VSH>(mv_s + si * VROW + gp * VSH, mv_d + di * VROW + gp * VSH);
   const int g1 = gp, g2 = gp + D / 64;
-  mvs_d[di * SROW + g1] = mvs_s[si * SROW + g1];
-  mvs_d[di * SROW + g2] = mvs_s[si * SROW + g2];
-  if (gp == 0) sc_d[di] = sc_s[si];
-
   const uint8_t* krow_s = mk_s + si * KROW;
   uint8_t* krow_d = mk_d + di * KROW;
-  if (nv == i || !a.table) {
-    copy_row<KG>(krow_s + g1 * KG, krow_d + g1 * KG);
-    copy_row<KG>(krow_s + g2 * KG, krow_d + g2 * KG);
-    mks_d[di * SROW + g1] = mks_s[si * SROW + g1];
-    mks_d[di * SROW + g2] = mks_s[si * SROW + g2];
-    return;
+
+  if (keep) {
+    // V codes (this thread's share of the row), the V scales and the score
+    constexpr int VSH = VROW / TPT;
+    copy_row<VSH>(mv_s + si * VROW + t_ * VSH, mv_d + di * VROW + t_ * VSH);
+    if (hf == 0) {
+      mvs_d[di * SROW + g1] = mvs_s[si * SROW + g1];
+      mvs_d[di * SROW + g2] = mvs_s[si * SROW + g2];
+    }
+    if (t_ == 0) sc_d[di] = sc_s[si];
+    if (!moved) {
+      copy_row<HB>(krow_s + g1 * 2 * HB + hf * HB, krow_d + g1 * 2 * HB + hf * HB);
+      copy_row<HB>(krow_s + g2 * 2 * HB + hf * HB, krow_d + g2 * 2 * HB + hf * HB);
+      if (hf == 0) {
+        mks_d[di * SROW + g1] = mks_s[si * SROW + g1];
+        mks_d[di * SROW + g2] = mks_s[si * SROW + g2];
+      }
+    }
   }
-  // dequantise the two groups into packed pairs (exact in fp32): the code's offset-binary
-  // value is placed in the mantissa of 2^23, the offset removed, then the scale applied
-  f2x X1[16], X2[16];
-  {
+  if (__ballot_sync(0xffffffffu, moved) == 0u) return;  // warp-uniform
+  f2x X1[8], X2[8];
+  float a1m = 0.f, a2m = 0.f;
+  if (moved) {
     const float s1 = h2f(mks_s[si * SROW + g1]), s2 = h2f(mks_s[si * SROW + g2]);
-    uint32_t w1[KG / 4], w2[KG / 4];
+    uint32_t w1[HB / 4], w2[HB / 4];
 #pragma unroll
-    for (int w = 0; w < KG / 4; ++w) {
-      w1[w] = reinterpret_cast<const uint32_t*>(krow_s + g1 * KG)[w];
-      w2[w] = reinterpret_cast<const uint32_t*>(krow_s + g2 * KG)[w];
+    for (int w = 0; w < HB / 4; ++w) {
+      w1[w] = reinterpret_cast<const uint32_t*>(krow_s + g1 * 2 * HB + hf * HB)[w];
+      w2[w] = reinterpret_cast<const uint32_t*>(krow_s + g2 * 2 * HB + hf * HB)[w];
     }
     constexpr int per = 32 / KB;
     constexpr uint32_t msk = (1u << KB) - 1u, flip = 1u << (KB - 1);
     const float off = 8388608.f + (float)flip;   // 2^23 + 2^(bits-1)
     const f2x OFF = f2_pack(off, off), S1 = f2_pack(s1, s1), S2 = f2_pack(s2, s2);
+    // dequantise (exact): the offset-binary code sits in the mantissa of 2^23
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
+    for (int k = 0; k < 8; ++k) {
       const int j0 = 2 * k, j1 = 2 * k + 1;
-      const uint32_t a0 = ((w1[j0 / per] >> (KB * (j0 % per))) & msk) ^ flip;
-      const uint32_t a1 = ((w1[j1 / per] >> (KB * (j1 % per))) & msk) ^ flip;
-      const uint32_t b0 = ((w2[j0 / per] >> (KB * (j0 % per))) & msk) ^ flip;
-      const uint32_t b1 = ((w2[j1 / per] >> (KB * (j1 % per))) & msk) ^ flip;
-      X1[k] = f2_mul(f2_sub(f2_pack(__uint_as_float(0x4B000000u | a0),
-                                    __uint_as_float(0x4B000000u | a1)), OFF), S1);
-      X2[k] = f2_mul(f2_sub(f2_pack(__uint_as_float(0x4B000000u | b0),
-                                    __uint_as_float(0x4B000000u | b1)), OFF), S2);
+      const uint32_t c10 = ((w1[j0 / per] >> (KB * (j0 % per))) & msk) ^ flip;
+      const uint32_t c11 = ((w1[j1 / per] >> (KB * (j1 % per))) & msk) ^ flip;
+      const uint32_t c20 = ((w2[j0 / per] >> (KB * (j0 % per))) & msk) ^ flip;
+      const uint32_t c21 = ((w2[j1 / per] >> (KB * (j1 % per))) & msk) ^ flip;
+      X1[k] = f2_mul(f2_sub(f2_pack(__uint_as_float(0x4B000000u | c10),
+                                    __uint_as_float(0x4B000000u | c11)), OFF), S1);
+      X2[k] = f2_mul(f2_sub(f2_pack(__uint_as_float(0x4B000000u | c20),
+                                    __uint_as_float(0x4B000000u | c21)), OFF), S2);
     }
-  }
-  // un-RoPE at the old index, re-RoPE at the new one with scalar IEEE intrinsics (never merged
-  // into a fused multiply-add, so every product and sum is rounded separately, as specified;
-  // packed fp32x2 products feeding packed sums may be fused by the assembler), then the cast
-  // through fp16
-  {
+    // un-RoPE at the old index, re-RoPE at the new one with scalar IEEE intrinsics (never
+    // merged into a fused multiply-add: every product and sum rounded separately; packed
+    // fp32x2 products feeding packed sums may be fused by the assembler), then the fp16 cast
     const float4* to = reinterpret_cast<const float4*>(a.table) +
-                       (size_t)(n_sink + i) * (a.half / 2) + 16 * gp;
+                       (size_t)(n_sink + i) * (a.half / 2) + 16 * gp + 8 * hf;
     const float4* tn = reinterpret_cast<const float4*>(a.table) +
-                       (size_t)(n_sink + nv) * (a.half / 2) + 16 * gp;
+                       (size_t)(n_sink + nv) * (a.half / 2) + 16 * gp + 8 * hf;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
+    for (int k = 0; k < 8; ++k) {
       const float4 co = __ldg(to + k), cn = __ldg(tn + k);  // (cos, cos, sin, sin) of 2 pairs
-      float a1[2], a2[2];
-      f2_unpack(X1[k], a1[0], a1[1]);
-      f2_unpack(X2[k], a2[0], a2[1]);
+      float p1[2], p2[2];
+      f2_unpack(X1[k], p1[0], p1[1]);
+      f2_unpack(X2[k], p2[0], p2[1]);
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         float t1, t2, y1, y2;
-        rotate_pair(a1[e], a2[e], e ? co.y : co.x, -(e ? co.w : co.z), t1, t2);
+        rotate_pair(p1[e], p2[e], e ? co.y : co.x, -(e ? co.w : co.z), t1, t2);
         rotate_pair(t1, t2, e ? cn.y : cn.x, e ? cn.w : cn.z, y1, y2);
-        a1[e] = y1;
-        a2[e] = y2;
+        p1[e] = y1;
+        p2[e] = y2;
       }
-      X1[k] = f2_round_f16(f2_pack(a1[0], a1[1]));
-      X2[k] = f2_round_f16(f2_pack(a2[0], a2[1]));
+      X1[k] = f2_round_f16(f2_pack(p1[0], p1[1]));
+      X2[k] = f2_round_f16(f2_pack(p2[0], p2[1]));
+      f2_unpack(X1[k], p1[0], p1[1]);
+      f2_unpack(X2[k], p2[0], p2[1]);
+      a1m = fmaxf(a1m, fmaxf(fabsf(p1[0]), fabsf(p1[1])));
+      a2m = fmaxf(a2m, fmaxf(fabsf(p2[0]), fabsf(p2[1])));
     }
   }
-  uint32_t o1[KG / 4], o2[KG / 4];
-  mks_d[di * SROW + g1] = quant_group_packed<KB>(X1, o1);
-  mks_d[di * SROW + g2] = quant_group_packed<KB>(X2, o2);
+  // absmax of each group over the token's two half-threads (adjacent lanes)
+  a1m = fmaxf(a1m, __shfl_xor_sync(0xffffffffu, a1m, 1));
+  a2m = fmaxf(a2m, __shfl_xor_sync(0xffffffffu, a2m, 1));
+  if (!moved) return;
+  constexpr int qmax = (1 << (KB - 1)) - 1;
+  float s1 = __half2float(__float2half_rn(__fdiv_rn(a1m, (float)qmax)));
+  float s2 = __half2float(__float2half_rn(__fdiv_rn(a2m, (float)qmax)));
+  if (a1m > 0.f && s1 == 0.f) s1 = kSubnormalMin;
+  if (a2m > 0.f && s2 == 0.f) s2 = kSubnormalMin;
+  uint32_t o1[HB / 4], o2[HB / 4];
 #pragma unroll
-  for (int w = 0; w < KG / 4; ++w) {
-    reinterpret_cast<uint32_t*>(krow_d + g1 * KG)[w] = o1[w];
-    reinterpret_cast<uint32_t*>(krow_d + g2 * KG)[w] = o2[w];
+  for (int w = 0; w < HB / 4; ++w) o1[w] = o2[w] = 0u;
+  if (s1 > 0.f) codes_half_group<KB>(X1, s1, o1);
+  if (s2 > 0.f) codes_half_group<KB>(X2, s2, o2);
+#pragma unroll
+  for (int w = 0; w < HB / 4; ++w) {
+    reinterpret_cast<uint32_t*>(krow_d + g1 * 2 * HB + hf * HB)[w] = o1[w];
+    reinterpret_cast<uint32_t*>(krow_d + g2 * 2 * HB + hf * HB)[w] = o2[w];
+  }
+  if (hf == 0) {
+    mks_d[di * SROW + g1] = __half_as_ushort(__float2half_rn(s1));
+    mks_d[di * SROW + g2] = __half_as_ushort(__float2half_rn(s2));
   }
 }
 
-__global__ void evict_commit_kernel(int32_t* meta, int units) {
+__global__ void evict_commit_kernel(int32_t* meta, int units, bool positional, int budget) {
   const int u = blockIdx.x * blockDim.x + threadIdx.x;
   if (u >= units) return;
   int32_t* m = meta + u * kF;
-  const int n_ev = m[FADE_META_N_EV];
+  const int n_ev = positional ? max(0, m[FADE_META_N_MID] - budget) : m[FADE_META_N_EV];
   if (n_ev > 0) {
     m[FADE_META_N_MID] -= n_ev;
     m[FADE_META_CUR] ^= 1;
@@ -827,12 +865,15 @@ extern "C" fade_status_t fade_evict_rerope(const fade_config_t* c, fade_layer_t*
     return st;
   const LayerArgs a = make_args(c, L, table);
   cudaStream_t s = as_stream(stream);
-  evict_select_kernel<<<dim3(c->num_kv_heads, c->batch), kSelThreads, 0, s>>>(a);
-  if ((st = launch_status("fade_evict_rerope select"))) return st;
+  if (!a.positional) {  // the position policy needs no selection pass
+    evict_select_kernel<<<dim3(c->num_kv_heads, c->batch), kSelThreads, 0, s>>>(a);
+    if ((st = launch_status("fade_evict_rerope select"))) return st;
+  }
   const int ctok = c->head_dim == 128 ? compact_tok<128>() : compact_tok<64>();
   if ((st = dispatch_dkv<CompactLaunch>(c, a, c->batch, ceil_div(max_mid, ctok), s))) return st;
   const int units = c->batch * c->num_kv_heads;
-  evict_commit_kernel<<<ceil_div(units, 128), 128, 0, s>>>(L->meta, units);
+  evict_commit_kernel<<<ceil_div(units, 128), 128, 0, s>>>(L->meta, units, a.positional,
+                                                            c->int4_budget);
   if ((st = launch_status("fade_evict_rerope commit"))) return st;
   for (int b = 0; b < c->batch; ++b)
     if (L->h_n_mid[b] > c->int4_budget) L->h_n_mid[b] = c->int4_budget;

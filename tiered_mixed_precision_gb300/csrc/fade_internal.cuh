@@ -300,4 +300,38 @@ __device__ __forceinline__ uint16_t quant_group_packed(const f2x (&X)[16], uint3
   return __half_as_ushort(__float2half_rn(s));
 }
 
+// Codes of 16 fp16-valued values (8 packed pairs) of one group whose scale s (> 0) is already
+// known, packed little-endian from bit 0 of out[0] (INT4: two words, INT2: one). Exact
+// round_half_even(x/s) by the same fast path as quant_group_packed; a subnormal scale (where
+// the clamp can bind) and exact ties take the exact scalar path.
+template <int BITS>
+__device__ __forceinline__ void codes_half_group(const f2x (&X)[8], float s, uint32_t* out) {
+  constexpr int per = 32 / BITS;
+  constexpr uint32_t mask = (1u << BITS) - 1u;
+  constexpr int qmax = (1 << (BITS - 1)) - 1;
+#pragma unroll
+  for (int w = 0; w < 16 / per; ++w) out[w] = 0u;
+  const bool subnormal = s < 6.103515625e-05f;
+  const float r = __frcp_rn(s);
+  const float h = 0.5f * s;
+  const f2x R = f2_pack(r, r), M = f2_pack(12582912.f, 12582912.f), NS = f2_pack(-s, -s);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const f2x QM = f2_add(f2_mul(X[k], R), M);
+    const f2x E = f2_fma(f2_sub(QM, M), NS, X[k]);
+    float e0, e1, qm0, qm1;
+    f2_unpack(E, e0, e1);
+    f2_unpack(QM, qm0, qm1);
+    uint32_t c0 = __float_as_uint(qm0) & mask, c1 = __float_as_uint(qm1) & mask;
+    if (subnormal || fabsf(e0) >= h || fabsf(e1) >= h) {
+      float v0, v1;
+      f2_unpack(X[k], v0, v1);
+      c0 = uint32_t((int)fminf(fmaxf(rint_div_exact(v0, s), (float)-qmax), (float)qmax)) & mask;
+      c1 = uint32_t((int)fminf(fmaxf(rint_div_exact(v1, s), (float)-qmax), (float)qmax)) & mask;
+    }
+    const int idx = 2 * k;
+    out[idx / per] |= (c0 << (BITS * (idx % per))) | (c1 << (BITS * (idx % per + 1)));
+  }
+}
+
 }  // namespace fade

@@ -118,7 +118,7 @@ class FadeCache:
         t = self._tick("evict") if evicting else None
         F.fade_evict_rerope(L, self.table, self.max_pos)
         self._tock(t)
-        n += 3 if evicting else 0
+        n += (2 if c.policy == "position" else 3) if evicting else 0
         F.fade_cache_append(L, self.k_rot, v)
         t = self._tick("attention")
         F.fade_decode_attention(L, self.q_rot, out, self.logits if self.needs_logits else None,
