@@ -33,6 +33,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode-attn tokens/s (batch×steps) and achieved HBM GB/s vs GB300 peak"
+_T0 = time.perf_counter()
+
+
+def progress(msg):
+    """Stage marks on stderr (stdout carries only the JSON line)."""
+    print(f"[bench +{time.perf_counter() - _T0:7.1f}s] {msg}", file=sys.stderr, flush=True)
 
 
 def parse_args():
@@ -225,6 +231,7 @@ def run_ours(args, rank, world):
     nsteps = 3 * K + W + 8   # timed, e2e, a possible eager timing pass, probe and warm-up
     max_pos = maxP + nsteps + 16
     fc = FadeCache(cfg, wl.layers, maxP, max_pos, dev)
+    progress(f"cache allocated: {wl.name}, {wl.layers} layers")
     h2o = wl.policy == "h2o" and wl.int4_budget >= 0
     for layer in range(wl.layers):
         # H2O: the prefill attention mass is computed on the GPU from the prompt's queries
@@ -233,6 +240,7 @@ def run_ours(args, rank, world):
         del pr
     torch.cuda.synchronize()
     torch.cuda.empty_cache()   # drop the prompt draws: only the cache stays resident
+    progress("prefill done")
     L, B, Hq, Hkv, d = wl.layers, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
     q_all = draw_vectors(wl, "q", (K + W, L, B, Hq, d), "bench", backend="torch", device=dev)
     k_all = draw_vectors(wl, "k", (K + W, L, B, Hkv, d), "bench", backend="torch", device=dev)
@@ -245,6 +253,7 @@ def run_ours(args, rank, world):
     for s in range(W):
         step(s)
     torch.cuda.synchronize()
+    progress(f"{W} warm-up steps done")
 
     # Steady state (a step leaves every tier count unchanged): the whole step is captured
     # once as a CUDA graph, with per-call timing events as graph nodes, and replayed on fixed
@@ -261,6 +270,7 @@ def run_ours(args, rank, world):
         launches_per_step = fc.launches
         graph.replay()
         torch.cuda.synchronize()
+        progress("graph captured and replayed once")
     barrier(world)
     clocks = ClockSampler(dev.index)
     clocks.start()
@@ -281,6 +291,7 @@ def run_ours(args, rank, world):
     e1.record()
     torch.cuda.synchronize()
     clk = clocks.stop()
+    progress(f"{K} timed steps done")
     launches = launches_per_step * K if graph is not None else fc.launches
     ms = e0.elapsed_time(e1)
     ms_max = max_over_ranks(ms, world)
@@ -291,6 +302,7 @@ def run_ours(args, rank, world):
                     for name, pairs in fc.timers.items()}
     except Exception as exc:  # timing nodes unavailable in this graph: time eager steps instead
         timing_note = f"eager steps after the timed region ({type(exc).__name__})"
+        progress(f"per-call timing from eager steps ({exc})")
         fc.timers = {}
         for s in range(W, W + K):
             step(s)
@@ -351,6 +363,7 @@ def run_ours(args, rank, world):
         e2e = {"value": B * K * world / (ems / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": int(qd.nbytes + kd.nbytes + vd.nbytes),
                "d2h_bytes_per_step": int(out.nbytes), "ms_per_step": ems / K}
+        progress("end-to-end steps done")
 
     value = B * K * world / (ms_max / 1e3)
     res = {
@@ -421,9 +434,11 @@ def main():
             print(json.dumps(line), flush=True)
         return
     res = run_ours(args, rank, world)
+    progress("GPU arm done")
     if rank == 0:
         if not args.no_cpu_baseline:
             cb = run_oracle_sample(args.workload, steps=3, warmup=1, budget_s=20.0)
+            progress("oracle sample done")
             res["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
         print(json.dumps(res), flush=True)
     if world > 1:

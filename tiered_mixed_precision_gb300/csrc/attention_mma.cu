@@ -6,8 +6,8 @@
 //
 // One CTA = one (row, KV head) unit and one chunk of its middle tokens. A producer warp streams
 // 256-token tiles into a shared-memory ring with TMA (2D tiled copies of the code rows with a
-// bank-spreading swizzle, 1D bulk copies of the scale rows) under mbarrier completion; four
-// consumer warps each take 64 tokens of a tile:
+// bank-spreading swizzle, 1D bulk copies of the scale rows) under mbarrier completion; the
+// consumer warps each take an equal share (64 or 32 tokens) of a tile:
 //   QK^T: tokens are the MMA's M dimension, channels its K dimension. The packed codes become
 //     exact fp16 integers in registers; each 64-channel half of the head dimension accumulates
 //     in its own fragment whose 8 columns are (query head h, group parity), the query operand
@@ -32,9 +32,16 @@ namespace {
 
 constexpr int kF = FADE_META_FIELDS;
 constexpr int kTileTok = 256;            // tokens per TMA tile
-constexpr int kConsumers = 4;            // consumer warps, 64 tokens each
+// Consumer warps per CTA (each takes kTileTok / kConsumers tokens of a tile), pipeline depth
+// for head_dim 128, and the resident-CTA hint given to the register allocator.
+#ifndef FADE_MMA_CONSUMERS
+#define FADE_MMA_CONSUMERS 4
+#endif
+constexpr int kConsumers = FADE_MMA_CONSUMERS;
 constexpr int kThreadsMma = 32 * (kConsumers + 1);
-// Pipeline depth for head_dim 128 and the resident-CTA hint given to the register allocator.
+constexpr int kWarpTok = kTileTok / kConsumers;  // tokens per consumer warp per tile
+constexpr int kMT = kWarpTok / 16;               // 16-token M-tiles per consumer warp
+static_assert(kConsumers == 4 || kConsumers == 8, "4 or 8 consumer warps");
 #ifndef FADE_MMA_STAGES_128
 #define FADE_MMA_STAGES_128 3
 #endif
@@ -160,6 +167,26 @@ __device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uin
 }
 
 __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+// The N fp16 scales of one token row in shared memory (one 4- or 8-byte load) as fp32; zeros
+// when `valid` is false.
+template <int N>
+__device__ __forceinline__ void load_scale_row(const uint16_t* p, bool valid, float (&f)[N]) {
+  static_assert(N == 2 || N == 4, "2 or 4 groups per row");
+  uint32_t w[N / 2];
+  if constexpr (N == 4) {
+    const uint2 u = valid ? *reinterpret_cast<const uint2*>(p) : make_uint2(0u, 0u);
+    w[0] = u.x;
+    w[1] = u.y;
+  } else {
+    w[0] = valid ? *reinterpret_cast<const uint32_t*>(p) : 0u;
+  }
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) {
+    f[2 * i] = __half2float(__ushort_as_half((unsigned short)(w[i] & 0xFFFFu)));
+    f[2 * i + 1] = __half2float(__ushort_as_half((unsigned short)(w[i] >> 16)));
+  }
+}
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
 // INT4 codes -> exact fp16 integers. Word w holds 8 nibbles (nibble i = channel 8w'+i of its
@@ -404,22 +431,19 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
         break;
       }
       const int nt = min(kTileTok, n_tok - it * kTileTok);
-      const int wr0 = warp * 64;
+      const int wr0 = warp * kWarpTok;
       const uint32_t stage = sbase + s_ * Cfg::STAGE;
       const uint8_t* st_ptr = smem + s_ * Cfg::STAGE;
       const uint16_t* kss = reinterpret_cast<const uint16_t*>(st_ptr + Cfg::KS_OFF);
       const uint16_t* vss = reinterpret_cast<const uint16_t*>(st_ptr + Cfg::VS_OFF);
       if (wr0 < nt) {
-        float sc[4][NT][2];  // logits (exp2 domain) of tokens g, g+8 of each M-tile
+        float sc[kMT][NT][2];  // logits (exp2 domain) of tokens g, g+8 of each M-tile
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
+        for (int mt = 0; mt < kMT; ++mt) {
           const int r0 = wr0 + mt * 16;
           float ks_lo[D / kGroup], ks_hi[D / kGroup];
-#pragma unroll
-          for (int q4 = 0; q4 < D / kGroup; ++q4) {
-            ks_lo[q4] = __half2float(__ushort_as_half(kss[(r0 + g) * Cfg::SROW + q4]));
-            ks_hi[q4] = __half2float(__ushort_as_half(kss[(r0 + g + 8) * Cfg::SROW + q4]));
-          }
+          load_scale_row<D / kGroup>(kss + (r0 + g) * Cfg::SROW, true, ks_lo);
+          load_scale_row<D / kGroup>(kss + (r0 + g + 8) * Cfg::SROW, true, ks_hi);
           float acc_s[NT][2];
 #pragma unroll
           for (int j = 0; j < NT; ++j) acc_s[j][0] = acc_s[j][1] = 0.f;
@@ -479,7 +503,7 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
         for (int j = 0; j < NT; ++j) {
           float mx = -INFINITY;
 #pragma unroll
-          for (int mt = 0; mt < 4; ++mt) mx = fmaxf(mx, fmaxf(sc[mt][j][0], sc[mt][j][1]));
+          for (int mt = 0; mt < kMT; ++mt) mx = fmaxf(mx, fmaxf(sc[mt][j][0], sc[mt][j][1]));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -488,7 +512,7 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
           m2[j] = mn;
           float ps = 0.f;
 #pragma unroll
-          for (int mt = 0; mt < 4; ++mt)
+          for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
               const float p = (sc[mt][j][r] == -INFINITY) ? 0.f : exp2f(sc[mt][j][r] - mn);
@@ -497,31 +521,30 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
             }
           lsum[j] = lsum[j] * alpha[j] + ps;
         }
+        // rescale the accumulators only when some column's running max moved (warp-uniform)
+        bool moved = false;
 #pragma unroll
-        for (int s = 0; s < NHALF; ++s)
+        for (int j = 0; j < NT; ++j) moved |= alpha[j] != 1.f;
+        if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-          for (int mm = 0; mm < 4; ++mm)
+          for (int s = 0; s < NHALF; ++s)
 #pragma unroll
-            for (int j = 0; j < NT; ++j)
+            for (int mm = 0; mm < 4; ++mm)
 #pragma unroll
-              for (int e = 0; e < 4; ++e) o[s][mm][j][e] *= alpha[j];
+              for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[s][mm][j][e] *= alpha[j];
+        }
 
-        // PV over the four M-tiles (16 tokens each = one MMA k-step)
+        // PV over the warp's M-tiles (16 tokens each = one MMA k-step)
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
+        for (int mt = 0; mt < kMT; ++mt) {
           const int r0 = wr0 + mt * 16;
+          // past the tile's tokens the scale rows may never have been copied: use 0 so that a
+          // zero probability cannot meet a non-finite leftover
           float vs_lo[D / kGroup], vs_hi[D / kGroup];
-#pragma unroll
-          for (int q4 = 0; q4 < D / kGroup; ++q4) {
-            // past the tile's tokens the scale rows were never copied: use 0 so that a zero
-            // probability cannot meet a non-finite leftover
-            vs_lo[q4] = (r0 + g < nt)
-                            ? __half2float(__ushort_as_half(vss[(r0 + g) * Cfg::SROW + q4]))
-                            : 0.f;
-            vs_hi[q4] = (r0 + g + 8 < nt)
-                            ? __half2float(__ushort_as_half(vss[(r0 + g + 8) * Cfg::SROW + q4]))
-                            : 0.f;
-          }
+          load_scale_row<D / kGroup>(vss + (r0 + g) * Cfg::SROW, r0 + g < nt, vs_lo);
+          load_scale_row<D / kGroup>(vss + (r0 + g + 8) * Cfg::SROW, r0 + g + 8 < nt, vs_hi);
           uint32_t X[2 * NHALF];  // (tokens 0-7 | 8-15) x (channel half)
           {
             const int lrow = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;

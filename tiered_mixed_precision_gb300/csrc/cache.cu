@@ -357,8 +357,13 @@ __global__ void __launch_bounds__(kSelThreads) evict_select_kernel(LayerArgs a) 
 template <int D>
 __host__ __device__ constexpr int compact_tok() { return 256 / (D / 32); }
 
+// Resident CTAs per SM asked of the register allocator for the compaction kernel.
+#ifndef FADE_COMPACT_MIN_CTAS
+#define FADE_COMPACT_MIN_CTAS 3
+#endif
+
 template <int D, int KB, int VB>
-__global__ void __launch_bounds__(256) evict_compact_kernel(LayerArgs a) {
+__global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kernel(LayerArgs a) {
   constexpr int TPT = D / 32;            // threads per token
   constexpr int TOK = compact_tok<D>();  // tokens per CTA
   constexpr int HB = 16 * KB / 8;        // bytes of half a group's K codes
@@ -474,26 +479,33 @@ __global__ void __launch_bounds__(256) evict_compact_kernel(LayerArgs a) {
       w1[w] = reinterpret_cast<const uint32_t*>(krow_s + g1 * 2 * HB + hf * HB)[w];
       w2[w] = reinterpret_cast<const uint32_t*>(krow_s + g2 * 2 * HB + hf * HB)[w];
     }
-    constexpr int per = 32 / KB;
-    constexpr uint32_t msk = (1u << KB) - 1u, flip = 1u << (KB - 1);
-    const float off = 8388608.f + (float)flip;   // 2^23 + 2^(bits-1)
-    const f2x OFF = f2_pack(off, off), S1 = f2_pack(s1, s1), S2 = f2_pack(s2, s2);
-    // dequantise (exact): the offset-binary code sits in the mantissa of 2^23
+    if constexpr (KB == 4) {
+      dequant16_int4(w1, s1, X1);
+      dequant16_int4(w2, s2, X2);
+    } else {
+      constexpr int per = 32 / KB;
+      constexpr uint32_t msk = (1u << KB) - 1u, flip = 1u << (KB - 1);
+      const float off = 8388608.f + (float)flip;   // 2^23 + 2^(bits-1)
+      const f2x OFF = f2_pack(off, off), S1 = f2_pack(s1, s1), S2 = f2_pack(s2, s2);
+      // dequantise (exact): the offset-binary code sits in the mantissa of 2^23
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int j0 = 2 * k, j1 = 2 * k + 1;
-      const uint32_t c10 = ((w1[j0 / per] >> (KB * (j0 % per))) & msk) ^ flip;
-      const uint32_t c11 = ((w1[j1 / per] >> (KB * (j1 % per))) & msk) ^ flip;
-      const uint32_t c20 = ((w2[j0 / per] >> (KB * (j0 % per))) & msk) ^ flip;
-      const uint32_t c21 = ((w2[j1 / per] >> (KB * (j1 % per))) & msk) ^ flip;
-      X1[k] = f2_mul(f2_sub(f2_pack(__uint_as_float(0x4B000000u | c10),
-                                    __uint_as_float(0x4B000000u | c11)), OFF), S1);
-      X2[k] = f2_mul(f2_sub(f2_pack(__uint_as_float(0x4B000000u | c20),
-                                    __uint_as_float(0x4B000000u | c21)), OFF), S2);
+      for (int k = 0; k < 8; ++k) {
+        const int j0 = 2 * k, j1 = 2 * k + 1;
+        const uint32_t c10 = ((w1[j0 / per] >> (KB * (j0 % per))) & msk) ^ flip;
+        const uint32_t c11 = ((w1[j1 / per] >> (KB * (j1 % per))) & msk) ^ flip;
+        const uint32_t c20 = ((w2[j0 / per] >> (KB * (j0 % per))) & msk) ^ flip;
+        const uint32_t c21 = ((w2[j1 / per] >> (KB * (j1 % per))) & msk) ^ flip;
+        X1[k] = f2_mul(f2_sub(f2_pack(__uint_as_float(0x4B000000u | c10),
+                                      __uint_as_float(0x4B000000u | c11)), OFF), S1);
+        X2[k] = f2_mul(f2_sub(f2_pack(__uint_as_float(0x4B000000u | c20),
+                                      __uint_as_float(0x4B000000u | c21)), OFF), S2);
+      }
     }
-    // un-RoPE at the old index, re-RoPE at the new one with scalar IEEE intrinsics (never
-    // merged into a fused multiply-add: every product and sum rounded separately; packed
-    // fp32x2 products feeding packed sums may be fused by the assembler), then the fp16 cast
+    // un-RoPE at the old index, re-RoPE at the new one, every product and sum rounded
+    // separately: products as packed fp32x2 multiplies (two rotation pairs at once), sums as
+    // scalar IEEE adds. (A packed sum fed by a packed product may be fused into one rounding
+    // by the assembler; packed products read by scalar sums were bit-identical to the scalar
+    // form on 16.7M probe values.) Then the cast to fp16.
     const float4* to = reinterpret_cast<const float4*>(a.table) +
                        (size_t)(n_sink + i) * (a.half / 2) + 16 * gp + 8 * hf;
     const float4* tn = reinterpret_cast<const float4*>(a.table) +
@@ -501,19 +513,11 @@ __global__ void __launch_bounds__(256) evict_compact_kernel(LayerArgs a) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const float4 co = __ldg(to + k), cn = __ldg(tn + k);  // (cos, cos, sin, sin) of 2 pairs
+      rotate2(X1[k], X2[k], f2_pack(co.x, co.y), f2_pack(-co.z, -co.w));
+      rotate2(X1[k], X2[k], f2_pack(cn.x, cn.y), f2_pack(cn.z, cn.w));
+      X1[k] = f2_round_f16(X1[k]);
+      X2[k] = f2_round_f16(X2[k]);
       float p1[2], p2[2];
-      f2_unpack(X1[k], p1[0], p1[1]);
-      f2_unpack(X2[k], p2[0], p2[1]);
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float t1, t2, y1, y2;
-        rotate_pair(p1[e], p2[e], e ? co.y : co.x, -(e ? co.w : co.z), t1, t2);
-        rotate_pair(t1, t2, e ? cn.y : cn.x, e ? cn.w : cn.z, y1, y2);
-        p1[e] = y1;
-        p2[e] = y2;
-      }
-      X1[k] = f2_round_f16(f2_pack(p1[0], p1[1]));
-      X2[k] = f2_round_f16(f2_pack(p2[0], p2[1]));
       f2_unpack(X1[k], p1[0], p1[1]);
       f2_unpack(X2[k], p2[0], p2[1]);
       a1m = fmaxf(a1m, fmaxf(fabsf(p1[0]), fabsf(p1[1])));

@@ -237,84 +237,63 @@ __device__ __forceinline__ uint16_t quant_group_thread(const float (&x)[32], uin
   return __half_as_ushort(__float2half_rn(s));
 }
 
-// Quantise one 32-value group held as 16 packed pairs by one thread (values are fp16-valued
-// fp32). Same result as quant_group_thread: s = fp16(absmax/qmax) (2^-24 if that underflows),
-// codes round_half_even(x/s) clamped to +-qmax. Fast path: x * (1/s) rounded to an integer by
-// adding 1.5 * 2^23 (whose low bits then hold the code in two's complement); the exact residual
-// x - q*s flags the rare exact ties (|residual| = s/2), which are redone exactly. The candidate
-// is within 2^-22 of x/s whether or not the product is rounded before the addition (a fused
-// multiply-add is allowed here), while x/s lies at least 2^-13 from any half-integer unless it
-// is one, so only ties can round wrongly. A subnormal scale (where the clamp can bind) takes
-// the exact path for the whole group.
-template <int BITS>
-__device__ __forceinline__ uint16_t quant_group_packed(const f2x (&X)[16], uint32_t* words) {
-  constexpr int qmax = (1 << (BITS - 1)) - 1;
-  constexpr int per = 32 / BITS;             // codes per word
-  constexpr uint32_t mask = (1u << BITS) - 1u;
-  float a = 0.f;
+// Two rotation pairs at once: (x1, x2) <- (x1*c - x2*s, x2*c + x1*s) elementwise, with the
+// four products as packed multiplies and the sums as scalar IEEE adds, so that every product
+// and every sum is rounded on its own (no packed sum reads a packed product).
+__device__ __forceinline__ void rotate2(f2x& X1, f2x& X2, f2x C, f2x S) {
+  float a0, a1, b0, b1, c0, c1, d0, d1;
+  f2_unpack(f2_mul(X1, C), a0, a1);
+  f2_unpack(f2_mul(X2, S), b0, b1);
+  f2_unpack(f2_mul(X2, C), c0, c1);
+  f2_unpack(f2_mul(X1, S), d0, d1);
+  X1 = f2_pack(__fsub_rn(a0, b0), __fsub_rn(a1, b1));
+  X2 = f2_pack(__fadd_rn(c0, d0), __fadd_rn(c1, d1));
+}
+
+// Byte permute: output byte i = byte sel[4i+2:4i] of {b, a} (a = bytes 0-3, b = bytes 4-7).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Exact dequantisation of 16 INT4 codes (two little-endian words, channel j at bits 4j) with
+// scale s into 8 packed pairs (channels 2k, 2k+1). Each nibble, offset-binary (code + 8), is
+// moved by a byte permute into the low mantissa byte of 2^23, so the float is 2^23 + code + 8;
+// subtracting 2^23 + 8 and multiplying by s are exact.
+__device__ __forceinline__ void dequant16_int4(const uint32_t (&w)[2], float s, f2x (&X)[8]) {
+  const f2x OFF = f2_pack(8388616.f, 8388616.f), S = f2_pack(s, s);
+  const uint32_t magic = 0x4B000000u;
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    float lo, hi;
-    f2_unpack(X[k], lo, hi);
-    a = fmaxf(a, fmaxf(fabsf(lo), fabsf(hi)));
-  }
-  float s = __half2float(__float2half_rn(__fdiv_rn(a, (float)qmax)));
-  if (a > 0.f && s == 0.f) s = kSubnormalMin;
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t ev = (w[h] & 0x0F0F0F0Fu) ^ 0x08080808u;         // channels 8h + 2b
+    const uint32_t od = ((w[h] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;  // channels 8h + 2b + 1
 #pragma unroll
-  for (int w = 0; w < 32 / per; ++w) words[w] = 0u;
-  if (s == 0.f) return 0;
-  if (s < 6.103515625e-05f) {  // subnormal scale: exact path with clamping
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      float v[2];
-      f2_unpack(X[k], v[0], v[1]);
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float q = fminf(fmaxf(rint_div_exact(v[e], s), (float)-qmax), (float)qmax);
-        const int idx = 2 * k + e;
-        words[idx / per] |= (uint32_t((int)q) & mask) << (BITS * (idx % per));
-      }
+    for (int b = 0; b < 4; ++b) {
+      const float lo = __uint_as_float(prmt(ev, magic, 0x7650u + b));
+      const float hi = __uint_as_float(prmt(od, magic, 0x7650u + b));
+      X[4 * h + b] = f2_mul(f2_sub(f2_pack(lo, hi), OFF), S);
     }
-    return __half_as_ushort(__float2half_rn(s));
   }
-  const float r = __frcp_rn(s);
-  const float h = 0.5f * s;
-  const f2x R = f2_pack(r, r), M = f2_pack(12582912.f, 12582912.f), NS = f2_pack(-s, -s);
-#pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const f2x QM = f2_add(f2_mul(X[k], R), M);   // bits 0x4B400000 + q
-    const f2x E = f2_fma(f2_sub(QM, M), NS, X[k]);
-    float e0, e1, qm0, qm1;
-    f2_unpack(E, e0, e1);
-    f2_unpack(QM, qm0, qm1);
-    uint32_t c0 = __float_as_uint(qm0) & mask, c1 = __float_as_uint(qm1) & mask;
-    if (fabsf(e0) >= h || fabsf(e1) >= h) {  // an exact tie: resolve to the even code
-      float v0, v1;
-      f2_unpack(X[k], v0, v1);
-      c0 = uint32_t((int)rint_div_exact(v0, s)) & mask;
-      c1 = uint32_t((int)rint_div_exact(v1, s)) & mask;
-    }
-    const int idx = 2 * k;
-    words[idx / per] |= (c0 << (BITS * (idx % per))) | (c1 << (BITS * (idx % per + 1)));
-  }
-  return __half_as_ushort(__float2half_rn(s));
 }
 
 // Codes of 16 fp16-valued values (8 packed pairs) of one group whose scale s (> 0) is already
-// known, packed little-endian from bit 0 of out[0] (INT4: two words, INT2: one). Exact
-// round_half_even(x/s) by the same fast path as quant_group_packed; a subnormal scale (where
-// the clamp can bind) and exact ties take the exact scalar path.
+// known, packed little-endian from bit 0 of out[0] (INT4: two words, INT2: one): exact
+// round_half_even(x/s). Fast path: x * (1/s) + 1.5 * 2^23 leaves a candidate code in the low
+// bits (two's complement); the exact residual x - q*s, below s/2 for every value, confirms all
+// 16 candidates, which are then packed with byte permutes (INT4). Otherwise (an exact tie, a
+// candidate off by one, or a subnormal scale where the clamp can bind) every code is redone by
+// the exact scalar path with the clamp.
 template <int BITS>
 __device__ __forceinline__ void codes_half_group(const f2x (&X)[8], float s, uint32_t* out) {
   constexpr int per = 32 / BITS;
   constexpr uint32_t mask = (1u << BITS) - 1u;
   constexpr int qmax = (1 << (BITS - 1)) - 1;
-#pragma unroll
-  for (int w = 0; w < 16 / per; ++w) out[w] = 0u;
-  const bool subnormal = s < 6.103515625e-05f;
   const float r = __frcp_rn(s);
   const float h = 0.5f * s;
   const f2x R = f2_pack(r, r), M = f2_pack(12582912.f, 12582912.f), NS = f2_pack(-s, -s);
+  uint32_t qb[16];
+  float emax = 0.f;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const f2x QM = f2_add(f2_mul(X[k], R), M);
@@ -322,15 +301,41 @@ __device__ __forceinline__ void codes_half_group(const f2x (&X)[8], float s, uin
     float e0, e1, qm0, qm1;
     f2_unpack(E, e0, e1);
     f2_unpack(QM, qm0, qm1);
-    uint32_t c0 = __float_as_uint(qm0) & mask, c1 = __float_as_uint(qm1) & mask;
-    if (subnormal || fabsf(e0) >= h || fabsf(e1) >= h) {
-      float v0, v1;
-      f2_unpack(X[k], v0, v1);
-      c0 = uint32_t((int)fminf(fmaxf(rint_div_exact(v0, s), (float)-qmax), (float)qmax)) & mask;
-      c1 = uint32_t((int)fminf(fmaxf(rint_div_exact(v1, s), (float)-qmax), (float)qmax)) & mask;
+    qb[2 * k] = __float_as_uint(qm0);
+    qb[2 * k + 1] = __float_as_uint(qm1);
+    emax = fmaxf(emax, fmaxf(fabsf(e0), fabsf(e1)));
+  }
+  if (s >= 6.103515625e-05f && emax < h) {
+    if constexpr (BITS == 4) {
+      // word v: channels 8v..8v+7; A = bytes of the even channels' codes, B = the odd ones
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {
+        const uint32_t a = prmt(prmt(qb[8 * v], qb[8 * v + 2], 0x0040u),
+                                prmt(qb[8 * v + 4], qb[8 * v + 6], 0x0040u), 0x5410u);
+        const uint32_t b = prmt(prmt(qb[8 * v + 1], qb[8 * v + 3], 0x0040u),
+                                prmt(qb[8 * v + 5], qb[8 * v + 7], 0x0040u), 0x5410u);
+        out[v] = (a & 0x0F0F0F0Fu) | ((b << 4) & 0xF0F0F0F0u);
+      }
+    } else {
+      uint32_t o = 0u;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) o |= (qb[j] & mask) << (BITS * j);
+      out[0] = o;
     }
-    const int idx = 2 * k;
-    out[idx / per] |= (c0 << (BITS * (idx % per))) | (c1 << (BITS * (idx % per + 1)));
+    return;
+  }
+  float v[16];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) f2_unpack(X[k], v[2 * k], v[2 * k + 1]);
+#pragma unroll
+  for (int w = 0; w < 16 / per; ++w) {
+    uint32_t o = 0u;
+#pragma unroll
+    for (int e = 0; e < per; ++e) {
+      const float q = fminf(fmaxf(rint_div_exact(v[w * per + e], s), (float)-qmax), (float)qmax);
+      o |= (uint32_t((int)q) & mask) << (BITS * e);
+    }
+    out[w] = o;
   }
 }
 

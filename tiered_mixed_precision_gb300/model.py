@@ -63,6 +63,7 @@ class FadeCache:
         self.k_rot = torch.empty((cfg.batch, cfg.num_kv_heads, cfg.head_dim),
                                  dtype=torch.float16, device=self.device)
         self.timers = None      # optional {"attention": [...], "evict": [...]} of event pairs
+        self._graph_events = []  # timing events referenced by captured graphs
         self.launches = 0       # kernels enqueued by step_layer calls
 
     # ------------------------------------------------------------------ pieces
@@ -151,6 +152,9 @@ class FadeCache:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             self.step_all(q, k, v, out)
+        # the graph records into the timing events captured above: they must outlive it
+        if self.timers:
+            self._graph_events.append({n: list(p) for n, p in self.timers.items()})
         after = self.mirror()
         for a, b in zip(before, after):
             if any((x != y).any() for x, y in zip(a, b)):
