@@ -145,6 +145,58 @@ def evict_bytes(cfg, layer, n_ev=1):
     return read + write + rec
 
 
+# DRAM bytes per launch from an ncu capture (profiles/dram_traffic.json), keyed by the SHA-256
+# of the kernel sources they were taken on: a figure whose sources changed is reported as null.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+CSRC = os.path.join(ROOT, "tiered_mixed_precision_gb300", "csrc")
+TRAFFIC_SOURCES = {
+    "attention": ["attention_mma.cu", "attention.cu", "fade_internal.cuh"],
+    "evict_rerope": ["cache.cu", "fade_internal.cuh"],
+}
+
+
+def sources_sha256(call):
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES[call]:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(call, workload_name):
+    try:
+        rec = json.load(open(TRAFFIC_FILE))[call]
+    except (OSError, ValueError, KeyError):
+        return None
+    if rec.get("workload") != workload_name or rec.get("sources_sha256") != sources_sha256(call):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# fp32 operations the method performs per re-positioned key (head_dim d): dequantise d codes
+# (one multiply each), un-RoPE and re-RoPE (d/2 pairs x 2 rotations x 4 multiplies + 2 adds),
+# the fp16 cast (d), the group absmax (d comparisons), the requantising division and rounding
+# (2 d). Recent-ring keys are fp16 (no dequantisation or requantisation): rotations and cast.
+def evict_alu_ops(cfg, layer):
+    d = cfg.head_dim
+    mid_key = d + 2 * (d // 2) * 6 + d + d + 2 * d
+    rec_key = 2 * (d // 2) * 6 + d
+    H = cfg.num_kv_heads
+    n_mid = int(layer.h_n_mid.sum()) * H
+    n_rec = int(layer.h_n_recent.sum()) * H
+    return n_mid * mid_key + n_rec * rec_key
+
+
+def alu_peak_tops(dev, peaks):
+    import torch
+
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = (peaks or {}).get("sm_max_mhz", 2070.0)
+    return sms * 128 * mhz * 1e6 / 1e12
+
+
 def load_peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -224,11 +276,15 @@ def run_ours(args, rank, world):
         wl = wl.scaled(seed=wl.seed + 1000 * rank)   # weak scaling: each rank its own batch
     if args.layers:
         wl = wl.scaled(layers=args.layers)
-    cfg = Config.from_workload(wl)
     lens = ragged_context_lengths(wl)
     maxP = int(lens.max())
     K, W = args.steps, args.warmup
     nsteps = 3 * K + W + 8   # timed, e2e, a possible eager timing pass, probe and warm-up
+    if wl.policy != "none" and wl.int4_budget >= 0:
+        cfg = Config.from_workload(wl)
+    else:  # without eviction the middle tier grows by one token per step
+        cfg = Config.from_workload(
+            wl, mid_capacity=max(1, maxP + nsteps - wl.n_sink - wl.recent_window))
     max_pos = maxP + nsteps + 16
     fc = FadeCache(cfg, wl.layers, maxP, max_pos, dev)
     progress(f"cache allocated: {wl.name}, {wl.layers} layers")
@@ -321,16 +377,31 @@ def run_ours(args, rank, world):
     if "attention" in per_call:
         t = float(np.mean(per_call["attention"])) / 1e3
         rl["attention"] = {"bound": "hbm", "achieved": attn_b / t / 1e9, "peak": peak,
-                           "unit": "GB/s", "frac": attn_b / t / 1e9 / peak, "traffic": None,
+                           "unit": "GB/s", "frac": attn_b / t / 1e9 / peak,
+                           "traffic": measured_traffic("attention", wl.name),
                            "bytes_per_launch": attn_b, "ms_per_launch": t * 1e3,
                            "peak_source": peak_src, "time_share": sum(per_call["attention"]) / ms}
     if "evict" in per_call:
         eb = evict_bytes(cfg, lay0)
         t = float(np.mean(per_call["evict"])) / 1e3
-        rl["evict_rerope"] = {"bound": "hbm", "achieved": eb / t / 1e9, "peak": peak,
-                              "unit": "GB/s", "frac": eb / t / 1e9 / peak, "traffic": None,
-                              "bytes_per_launch": eb, "ms_per_launch": t * 1e3,
-                              "peak_source": peak_src, "time_share": sum(per_call["evict"]) / ms}
+        hbm = {"bound": "hbm", "achieved": eb / t / 1e9, "peak": peak,
+               "unit": "GB/s", "frac": eb / t / 1e9 / peak,
+               "traffic": measured_traffic("evict_rerope", wl.name),
+               "bytes_per_launch": eb, "ms_per_launch": t * 1e3,
+               "peak_source": peak_src, "time_share": sum(per_call["evict"]) / ms}
+        if wl.policy == "position":
+            # every survivor (middle and recent) is re-positioned: the method's fp32 arithmetic
+            # per key against the FP32 lanes of the device at the maximum SM clock
+            ops = evict_alu_ops(cfg, lay0)
+            apeak = alu_peak_tops(dev, peaks)
+            rl["evict_rerope"] = {"bound": "alu", "achieved": ops / t / 1e12, "peak": apeak,
+                                  "unit": "TOP/s", "frac": ops / t / 1e12 / apeak,
+                                  "traffic": hbm["traffic"], "ops_per_launch": ops,
+                                  "ms_per_launch": t * 1e3,
+                                  "peak_source": "derived: SMs x 128 FP32 lanes x max SM clock",
+                                  "time_share": hbm["time_share"], "hbm_view": hbm}
+        else:
+            rl["evict_rerope"] = hbm
     dominant = max(rl, key=lambda n: rl[n]["time_share"]) if rl else None
 
     # end to end: inputs copied from pinned host memory and outputs read back every step
@@ -381,8 +452,9 @@ def run_ours(args, rank, world):
                    "per_call_timing": timing_note},
         "roofline": dict(rl[dominant], kernel=dominant) if dominant else None,
         "roofline_by_call": rl,
+        # decode-attention calls alone: B tokens per step over L attention launches
         "attention_only": {
-            "value": B * K * world / (sum(per_call.get("attention", [np.nan])) / 1e3),
+            "value": B * world / (float(np.mean(per_call.get("attention", [np.nan]))) * L / 1e3),
             "unit": "tokens/s", "gbs": rl.get("attention", {}).get("achieved")},
         "e2e": e2e, "gpu_launches": launches, "clocks": clk,
     }

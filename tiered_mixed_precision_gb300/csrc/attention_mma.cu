@@ -23,6 +23,7 @@
 #include <cuda.h>
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "fade_internal.cuh"
@@ -32,22 +33,26 @@ namespace {
 
 constexpr int kF = FADE_META_FIELDS;
 constexpr int kTileTok = 256;            // tokens per TMA tile
-// Consumer warps per CTA (each takes kTileTok / kConsumers tokens of a tile), pipeline depth
-// for head_dim 128, and the resident-CTA hint given to the register allocator.
-#ifndef FADE_MMA_CONSUMERS
-#define FADE_MMA_CONSUMERS 4
+// Warp layout per (head_dim, query heads per KV head): consumer warps per CTA, each taking an
+// equal share of a tile (32 or 64 tokens), one producer warp, and the resident-CTA hint given to
+// the register allocator. Eight consumers (two CTAs per SM) when the accumulators are small
+// (G <= 4); four (one CTA) for G = 8, whose accumulators would not fit the smaller budget.
+// FADE_MMA_WIDE=0 forces four consumers everywhere; FADE_MMA_STAGES_128 sets the pipeline
+// depth for head_dim 128.
+#ifndef FADE_MMA_WIDE
+#define FADE_MMA_WIDE 1
 #endif
-constexpr int kConsumers = FADE_MMA_CONSUMERS;
-constexpr int kThreadsMma = 32 * (kConsumers + 1);
-constexpr int kWarpTok = kTileTok / kConsumers;  // tokens per consumer warp per tile
-constexpr int kMT = kWarpTok / 16;               // 16-token M-tiles per consumer warp
-static_assert(kConsumers == 4 || kConsumers == 8, "4 or 8 consumer warps");
 #ifndef FADE_MMA_STAGES_128
 #define FADE_MMA_STAGES_128 3
 #endif
-#ifndef FADE_MMA_MIN_CTAS
-#define FADE_MMA_MIN_CTAS 1
-#endif
+template <int D, int G>
+struct MmaShape {
+  static constexpr int CONS = (FADE_MMA_WIDE && G <= 4) ? 8 : 4;
+  static constexpr int THREADS = 32 * (CONS + 1);
+  static constexpr int WARP_TOK = kTileTok / CONS;  // tokens per consumer warp per tile
+  static constexpr int MT = WARP_TOK / 16;          // 16-token M-tiles per consumer warp
+  static constexpr int MINB = CONS == 8 ? 2 : 1;
+};
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz: a wait that never ends
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -63,7 +68,7 @@ struct MmaArgs {
   float* part_ml;                    // [B][Hq][nsplit][2]
   float* part_acc;                   // [B][Hq][nsplit][D]
   int32_t* status;
-  int Hq, H, S, W, C, NS, chunk, nsplit;
+  int B, Hq, H, S, W, C, NS, chunk, nsplit;
   float inv_sqrt_d;
 };
 
@@ -72,16 +77,26 @@ struct MmaCfg {
   static constexpr int KROW = D / 2;        // INT4 codes per token (bytes)
   static constexpr int VROW = D / 4;        // INT2 codes per token (bytes)
   static constexpr int SROW = D / kGroup;   // scales per token
-  static constexpr int STAGE = kTileTok * (KROW + VROW + 2 * SROW * 2);
+  static constexpr int Q_BYTES = 8 * D * 2; // the item's query rows (up to 8 heads), fp16
+  static constexpr int STAGE = kTileTok * (KROW + VROW + 2 * SROW * 2) + Q_BYTES;
   static constexpr int NSTAGE = D == 128 ? FADE_MMA_STAGES_128 : 4;
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = kTileTok * KROW;
   static constexpr int KS_OFF = V_OFF + kTileTok * VROW;
   static constexpr int VS_OFF = KS_OFF + kTileTok * SROW * 2;
-  static constexpr int BAR_OFF = NSTAGE * STAGE;
+  static constexpr int Q_OFF = VS_OFF + kTileTok * SROW * 2;
+  // per-item merge of the consumer warps' partials: m, l [8][8], acc [8][8][D], weights [8][8]
+  static constexpr int MERGE_OFF = NSTAGE * STAGE;
+  static constexpr int MERGE_BYTES = (64 + 64 + 8 * 8 * D / 2 + 64) * 4;
+  static constexpr int INFO_OFF = MERGE_OFF + MERGE_BYTES;  // per stage: kInfo ints
+  static constexpr int BAR_OFF = INFO_OFF + NSTAGE * 8 * 4;
   static constexpr int SMEM = BAR_OFF + 2 * NSTAGE * 8 + 1024;  // + alignment slack
+  static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned (TMA swizzle)");
 };
 
+// Stage info written by the producer before it arms a stage: what the consumers find there.
+enum StageInfo { kInfoUnit, kInfoSplit, kInfoNt, kInfoLast, kInfoTok0, kInfoSink, kInfoRec,
+                 kInfoHead, kInfo };
 // ------------------------------------------------------------------ PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -189,18 +204,115 @@ __device__ __forceinline__ void load_scale_row(const uint16_t* p, bool valid, fl
 }
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
+// 2^x by the hardware approximation (relative error ~2^-22; 2^-inf = +0; results below 2^-126
+// flush to zero, which is far below anything that reaches an fp16 output).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Sums over the warp of N per-lane values, every lane receiving all N sums: a reduce-scatter
+// (each step halves the values a lane carries and sends the other half across), a plain
+// reduction of the last value, and a broadcast from the lanes that own each sum.
+template <int N>
+__device__ __forceinline__ void warp_allreduce(float (&v)[N], int lane) {
+  if constexpr (N == 1) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+  } else {
+    constexpr int LOG = N == 2 ? 1 : N == 4 ? 2 : 3;
+    float w[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) w[i] = v[i];
+#pragma unroll
+    for (int st = 0; st < LOG; ++st) {
+      const int half = N >> (st + 1), off = 16 >> st;
+      const bool up = lane & off;
+#pragma unroll
+      for (int i = 0; i < half; ++i) {
+        const float send = up ? w[i] : w[i + half];
+        const float keep = up ? w[i + half] : w[i];
+        w[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+      }
+    }
+#pragma unroll
+    for (int o = 16 >> LOG; o; o >>= 1) w[0] += __shfl_xor_sync(0xffffffffu, w[0], o);
+#pragma unroll
+    for (int h = 0; h < N; ++h) {
+      int src = 0;
+#pragma unroll
+      for (int st = 0; st < LOG; ++st) src += ((h >> (LOG - 1 - st)) & 1) * (16 >> st);
+      v[h] = __shfl_sync(0xffffffffu, w[0], src);
+    }
+  }
+}
+
+// CPL consecutive fp16 values (CPL = 2 or 4, 4- or 8-byte aligned) as fp32.
+template <int CPL>
+__device__ __forceinline__ void load_f16_lane(const uint16_t* p, float (&f)[CPL]) {
+  if constexpr (CPL == 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    f[0] = a.x;
+    f[1] = a.y;
+    f[2] = b.x;
+    f[3] = b.y;
+  } else {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u));
+    f[0] = a.x;
+    f[1] = a.y;
+  }
+}
+
+// v[i] for a runtime index i < N, without indexing a register array dynamically.
+template <int N>
+__device__ __forceinline__ float pick(const float (&v)[N], int i) {
+  float r = v[0];
+#pragma unroll
+  for (int k = 1; k < N; ++k) r = (i == k) ? v[k] : r;
+  return r;
+}
+
+// Barrier among the NC consumer warps only (named barrier 1; the producer warp never joins).
+template <int NC>
+__device__ __forceinline__ void consumer_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NC * 32) : "memory");
+}
+
+// (x & m) ^ c in one logic instruction.
+__device__ __forceinline__ uint32_t and_xor(uint32_t x, uint32_t m, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(d) : "r"(x), "r"(m), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float h_lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu))); }
+__device__ __forceinline__ float h_hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
+
 // INT4 codes -> exact fp16 integers. Word w holds 8 nibbles (nibble i = channel 8w'+i of its
 // row). Pair kappa of a word is (nibble kappa', nibble kappa'+4) with kappa' = {0,1,2,3}: the
 // nibble is placed in an fp16 mantissa above 1024 (offset-binary), then the offset is removed
-// exactly.
+// exactly. x8 = w >> 8.
 template <int KAPPA>
-__device__ __forceinline__ uint32_t k_pair(uint32_t w) {
-  const uint32_t x = (KAPPA >= 2) ? (w >> 8) : w;
+__device__ __forceinline__ uint32_t k_pair(uint32_t w, uint32_t x8) {
+  const uint32_t x = (KAPPA >= 2) ? x8 : w;
   if constexpr (KAPPA % 2 == 0) {
-    const __half2 h = u32_as_h2((x & 0x000F000Fu) ^ 0x64086408u);       // 1024 + (n ^ 8)
+    const __half2 h = u32_as_h2(and_xor(x, 0x000F000Fu, 0x64086408u));   // 1024 + (n ^ 8)
     return h2_as_u32(__hsub2(h, __float2half2_rn(1032.f)));
   } else {
-    const __half2 h = u32_as_h2((x & 0x00F000F0u) ^ 0x64806480u);       // 1024 + 16 (n ^ 8)
+    const __half2 h = u32_as_h2(and_xor(x, 0x00F000F0u, 0x64806480u));   // 1024 + 16 (n ^ 8)
     return h2_as_u32(__hfma2(h, __float2half2_rn(0.0625f), __float2half2_rn(-72.f)));
   }
 }
@@ -212,136 +324,436 @@ __device__ __forceinline__ uint32_t v_crumb(uint32_t x, uint32_t x10) {
   const uint32_t src = C <= 4 ? x : x10;
   constexpr uint32_t mask = (0x3u << (2 * cc)) * 0x00010001u;
   constexpr uint32_t magic = (0x6400u | (2u << (2 * cc))) * 0x00010001u;
-  const __half2 h = u32_as_h2((src & mask) ^ magic);                       // 1024 + (u^2)*4^cc
+  const __half2 h = u32_as_h2(and_xor(src, mask, magic));                  // 1024 + (u^2)*4^cc
   constexpr float sc = 1.f / float(1 << (2 * cc));
   constexpr float off = -(1024.f / float(1 << (2 * cc)) + 2.f);
   return h2_as_u32(__hfma2(h, __float2half2_rn(sc), __float2half2_rn(off)));
 }
 
+// Per-lane shared-memory byte offsets inside a stage, for M-tile 0 of the warp (M-tile mt adds
+// mt * 16 rows). With the 64-/32-byte swizzles the XOR pattern depends only on the lane.
+template <int D>
+struct LaneOffsets {
+  uint32_t k[D / 64];  // ldmatrix address of the K codes, per 64-channel half
+  uint32_t v;          // ldmatrix.trans address of the V codes
+  uint32_t ks, vs;     // K / V scale row of token g
+};
+
+template <int D>
+__device__ __forceinline__ LaneOffsets<D> lane_offsets(int wr0, int lane) {
+  using Cfg = MmaCfg<D>;
+  LaneOffsets<D> o;
+  const int lr = (lane & 7) + ((lane >> 3) & 1) * 8, hi = lane >> 4, g = lane >> 2;
+  if constexpr (D == 128) {
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+      o.k[s] = Cfg::K_OFF + (wr0 + lr) * Cfg::KROW + (((2 * s + hi) ^ ((lr >> 1) & 3)) * 16);
+    o.v = Cfg::V_OFF + (wr0 + lr) * Cfg::VROW + ((hi ^ ((lr >> 2) & 1)) * 16);
+  } else {
+    o.k[0] = Cfg::K_OFF + (wr0 + lr) * Cfg::KROW + ((hi ^ ((lr >> 2) & 1)) * 16);
+    o.v = Cfg::V_OFF + (wr0 + lr) * Cfg::VROW;
+  }
+  o.ks = Cfg::KS_OFF + (wr0 + g) * Cfg::SROW * 2;
+  o.vs = Cfg::VS_OFF + (wr0 + g) * Cfg::SROW * 2;
+  return o;
+}
+
+// Scale words of one token row: D/32 fp16 scales as D/64 half2 words.
+template <int D>
+__device__ __forceinline__ void scale_words(uint32_t addr, uint32_t (&w)[D / 64]) {
+  if constexpr (D == 128) {
+    const uint2 v = lds64(addr);
+    w[0] = v.x;
+    w[1] = v.y;
+  } else {
+    w[0] = lds32(addr);
+  }
+}
+
+// One consumer warp's share of one tile: QK^T on the tensor cores with the K scales applied per
+// group in fp32, the online-softmax update, and PV. FULL: every token of the warp's share is
+// valid (no masking). Invalid head columns (G < 4) carry logit 0 and are discarded later.
+template <int D, int G, bool FULL, bool LOGITS>
+__device__ __forceinline__ void consume_tile(
+    const MmaArgs& a, uint32_t stage, const LaneOffsets<D>& lo_, int nt, int wr0, int lane,
+    const uint32_t (&qb)[D / 64][4][(2 * G + 7) / 8][2], float (&m2)[(2 * G + 7) / 8],
+    float (&lsum)[(2 * G + 7) / 8], float (&o)[D / 64][4][(2 * G + 7) / 8][4], float c2,
+    float* logit_row) {
+  using Cfg = MmaCfg<D>;
+  constexpr int NT = (2 * G + 7) / 8;
+  constexpr int NHALF = D / 64;
+  const int g = lane >> 2, t = lane & 3;
+  float sc[MmaShape<D, G>::MT][NT][2];  // logits (exp2 domain) of tokens g, g+8 of each M-tile
+#pragma unroll
+  for (int mt = 0; mt < MmaShape<D, G>::MT; ++mt) {
+    const int r0 = wr0 + mt * 16;
+    uint32_t kw_lo[NHALF], kw_hi[NHALF];
+    scale_words<D>(stage + lo_.ks + mt * 16 * Cfg::SROW * 2, kw_lo);
+    scale_words<D>(stage + lo_.ks + (mt * 16 + 8) * Cfg::SROW * 2, kw_hi);
+    float acc_s[NT][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) acc_s[j][0] = acc_s[j][1] = 0.f;
+#pragma unroll
+    for (int s = 0; s < NHALF; ++s) {
+      uint32_t k0, k1, k2, k3;  // (rows g, chunk 2s) (g+8, 2s) (g, 2s+1) (g+8, 2s+1)
+      ldsm_x4(stage + lo_.k[s] + mt * 16 * Cfg::KROW, k0, k1, k2, k3);
+      const uint32_t k0s = k0 >> 8, k1s = k1 >> 8, k2s = k2 >> 8, k3s = k3 >> 8;
+      float cacc[NT][4];
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) cacc[j][e] = 0.f;
+#define FADE_KSTEP(KP)                                                                        \
+  {                                                                                           \
+    const uint32_t a0 = k_pair<KP>(k0, k0s), a1 = k_pair<KP>(k1, k1s),                        \
+                   a2 = k_pair<KP>(k2, k2s), a3 = k_pair<KP>(k3, k3s);                        \
+    _Pragma("unroll") for (int j = 0; j < NT; ++j)                                            \
+        mma16816(cacc[j], a0, a1, a2, a3, qb[s][KP][j][0], qb[s][KP][j][1]);                  \
+  }
+      FADE_KSTEP(0) FADE_KSTEP(1) FADE_KSTEP(2) FADE_KSTEP(3)
+#undef FADE_KSTEP
+      // column 2t = (head 4j+t, group 2s), column 2t+1 = (head 4j+t, group 2s+1)
+      const float kl0 = h_lo(kw_lo[s]), kl1 = h_hi(kw_lo[s]);
+      const float kh0 = h_lo(kw_hi[s]), kh1 = h_hi(kw_hi[s]);
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        acc_s[j][0] = fmaf(cacc[j][0], kl0, acc_s[j][0]);
+        acc_s[j][0] = fmaf(cacc[j][1], kl1, acc_s[j][0]);
+        acc_s[j][1] = fmaf(cacc[j][2], kh0, acc_s[j][1]);
+        acc_s[j][1] = fmaf(cacc[j][3], kh1, acc_s[j][1]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int h = 4 * j + t;
+      const bool hv = h < G;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int tok = r0 + g + 8 * r;
+        const bool tv = FULL || tok < nt;
+        if (LOGITS && hv && tv) logit_row[(size_t)h * a.NS + tok] = acc_s[j][r] * a.inv_sqrt_d;
+        const float v = hv ? acc_s[j][r] * c2 : 0.f;
+        sc[mt][j][r] = tv ? v : -INFINITY;
+      }
+    }
+  }
+  // online softmax per head column; the warp holds at least one valid token, so the running
+  // max is finite after this tile and masked tokens get probability exp2(-inf) = 0
+  float alpha[NT];
+  bool moved = false;
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    float mx = sc[0][j][0];
+#pragma unroll
+    for (int mt = 0; mt < MmaShape<D, G>::MT; ++mt) mx = fmaxf(mx, fmaxf(sc[mt][j][0], sc[mt][j][1]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float mn = fmaxf(m2[j], mx);
+    alpha[j] = ex2(m2[j] - mn);   // 0 on the first tile (old max -inf)
+    moved |= mn != m2[j];
+    m2[j] = mn;
+    float ps = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < MmaShape<D, G>::MT; ++mt)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float pr = ex2(sc[mt][j][r] - mn);
+        sc[mt][j][r] = pr;
+        ps += pr;
+      }
+    lsum[j] = lsum[j] * alpha[j] + ps;
+  }
+  // rescale the accumulators only when some column's running max moved (warp-uniform)
+  if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+    for (int s = 0; s < NHALF; ++s)
+#pragma unroll
+      for (int mm = 0; mm < 4; ++mm)
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[s][mm][j][e] *= alpha[j];
+  }
+  // PV over the warp's M-tiles (16 tokens each = one MMA k-step). B operand: the probability
+  // (fp16) times the V scale of the column's group (fp16 multiply), transposed into place.
+#pragma unroll
+  for (int mt = 0; mt < MmaShape<D, G>::MT; ++mt) {
+    const int r0 = wr0 + mt * 16;
+    uint32_t vw_lo[NHALF], vw_hi[NHALF];
+    scale_words<D>(stage + lo_.vs + mt * 16 * Cfg::SROW * 2, vw_lo);
+    scale_words<D>(stage + lo_.vs + (mt * 16 + 8) * Cfg::SROW * 2, vw_hi);
+    if (!FULL) {
+      // past the tile's tokens the scale rows may never have been copied: use 0 so that a
+      // zero probability cannot meet a non-finite leftover
+#pragma unroll
+      for (int s = 0; s < NHALF; ++s) {
+        vw_lo[s] = (r0 + g < nt) ? vw_lo[s] : 0u;
+        vw_hi[s] = (r0 + g + 8 < nt) ? vw_hi[s] : 0u;
+      }
+    }
+    uint32_t X[2 * NHALF];  // (tokens 0-7 | 8-15) x (channel half)
+    if constexpr (D == 128)
+      ldsm_x4_t(stage + lo_.v + mt * 16 * Cfg::VROW, X[0], X[1], X[2], X[3]);
+    else
+      ldsm_x2_t(stage + lo_.v + mt * 16 * Cfg::VROW, X[0], X[1]);
+    __half2 pg[NT], pg8[NT];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      pg[j] = __float2half2_rn(sc[mt][j][0]);
+      pg8[j] = __float2half2_rn(sc[mt][j][1]);
+    }
+#pragma unroll
+    for (int s = 0; s < NHALF; ++s) {
+      uint32_t pb[NT][2];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        pb[j][0] = movm_t(h2_as_u32(__hmul2(pg[j], u32_as_h2(vw_lo[s]))));
+        pb[j][1] = movm_t(h2_as_u32(__hmul2(pg8[j], u32_as_h2(vw_hi[s]))));
+      }
+      const uint32_t xa = X[2 * s], xb = X[2 * s + 1];
+      const uint32_t xa10 = xa >> 10, xb10 = xb >> 10;
+#define FADE_PV(MM)                                                                         \
+  {                                                                                         \
+    const uint32_t a0 = v_crumb<2 * MM>(xa, xa10), a1 = v_crumb<2 * MM + 1>(xa, xa10);      \
+    const uint32_t a2 = v_crumb<2 * MM>(xb, xb10), a3 = v_crumb<2 * MM + 1>(xb, xb10);      \
+    _Pragma("unroll") for (int j = 0; j < NT; ++j)                                          \
+        mma16816(o[s][MM][j], a0, a1, a2, a3, pb[j][0], pb[j][1]);                          \
+  }
+      FADE_PV(0) FADE_PV(1) FADE_PV(2) FADE_PV(3)
+#undef FADE_PV
+    }
+  }
+}
+
+// Bounded wait that also gives up as soon as another warp of the CTA has raised `abort`.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, int32_t* status,
+                                                   int code, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      atomicCAS(status, 0, code);
+      *abort = 1;
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
+// Persistent decode attention: CTA c takes the work items c, c + gridDim.x, ... of the list
+// (split, unit) = (item / units, item % units), where split 0 is a unit's FP16 tiers and split
+// s >= 1 its middle tokens [(s-1)*chunk, s*chunk). Every item occupies one or more stages of the
+// ring: the producer warp copies each stage's code and scale rows (TMA) and, with the item's
+// first stage, the item's query rows (bulk copy); it writes what the stage holds into the stage
+// info before arming it. The producer therefore runs ahead across item boundaries and the
+// consumers never wait on global memory for metadata or queries. Consumer warps merge their
+// partials in shared memory at the end of each item (named barrier 1, consumers only) and
+// write the item's split partial.
 template <int D, int G>
-__global__ void __launch_bounds__(kThreadsMma, FADE_MMA_MIN_CTAS)
+__global__ void __launch_bounds__(MmaShape<D, G>::THREADS, MmaShape<D, G>::MINB)
 attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_constant__ CUtensorMap tk1,
                     const __grid_constant__ CUtensorMap tv0, const __grid_constant__ CUtensorMap tv1,
                     MmaArgs a) {
   using Cfg = MmaCfg<D>;
+  constexpr int kConsumers = MmaShape<D, G>::CONS;
   constexpr int NT = (2 * G + 7) / 8;    // 8-column n-tiles of (head, group parity)
   constexpr int NHALF = D / 64;          // 64-channel halves (accumulator sets)
   constexpr int NSTAGE = Cfg::NSTAGE;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // 1024-byte aligned base, kept as an offset into the __shared__ array so that every access
+  // through it compiles to a shared-memory (not a generic) load or store
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_full = sbase + Cfg::BAR_OFF;          // NSTAGE x 8 bytes
   const uint32_t bar_empty = bar_full + NSTAGE * 8;
+  int* info = reinterpret_cast<int*>(smem + Cfg::INFO_OFF);  // [NSTAGE][kInfo]
+  float* wm = reinterpret_cast<float*>(smem + Cfg::MERGE_OFF);  // [kConsumers][8]
+  float* wl = wm + 64;                                          // [kConsumers][8]
+  float* wf = wl + 64;                                          // [G][kConsumers]
+  float* wo = wf + 64;                                          // [kConsumers][G][D]
+  __shared__ int s_abort;
 
-  const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
-  const int unit = b * a.H + hk;
-  const int32_t* m = a.meta + unit * kF;
-  const int n_mid = m[FADE_META_N_MID], cur = m[FADE_META_CUR];
-  const int n_sink = m[FADE_META_N_SINK], n_rec = m[FADE_META_N_RECENT];
-  const int head_slot = m[FADE_META_HEAD];
-  const int lo = split > 0 ? (split - 1) * a.chunk : 0;
-  const int hi = split > 0 ? min(n_mid, lo + a.chunk) : 0;
-  const int n_tok = split > 0 ? max(0, hi - lo) : n_sink + n_rec;
-  const int n_tiles = (n_tok + kTileTok - 1) / kTileTok;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int hq0 = hk * G;
-  const size_t pbase = ((size_t)(b * a.Hq + hq0)) * a.nsplit + split;
+  const int units = a.B * a.H;
+  const int n_items = units * a.nsplit;
 
-  if (n_tok == 0) {  // an empty split still publishes an empty partial
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-      const int h = i / D, c = i % D;
-      a.part_acc[(pbase + (size_t)h * a.nsplit) * D + c] = 0.f;
-    }
-    if (threadIdx.x < G) {
-      a.part_ml[(pbase + (size_t)threadIdx.x * a.nsplit) * 2] = -INFINITY;
-      a.part_ml[(pbase + (size_t)threadIdx.x * a.nsplit) * 2 + 1] = 0.f;
-    }
-    return;
-  }
-
-  if (split > 0 && threadIdx.x == 0) {
+  if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, kConsumers);
     }
+    s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  volatile int* abort = &s_abort;
 
-  const size_t row0 = (size_t)unit * a.C + lo;  // first global code row of this chunk
-  bool failed = false;
-
-  // per-warp online-softmax state (consumer warps): running max (exp2 domain), mass, and
-  // the P.V accumulators
-  float m2[NT], lsum[NT];
-  float o[NHALF][4][NT][4];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    m2[j] = -INFINITY;
-    lsum[j] = 0.f;
+  if (warp == kConsumers) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
+        const int split = item / units, unit = item % units;
+        const int b = unit / a.H, hk = unit % a.H;
+        const int32_t* m = a.meta + unit * kF;
+        const int n_mid = m[FADE_META_N_MID], cur = m[FADE_META_CUR];
+        const int lo = split > 0 ? (split - 1) * a.chunk : 0;
+        const int hi = split > 0 ? min(n_mid, lo + a.chunk) : 0;
+        const int n_tok = max(0, hi - lo);
+        const int n_stage = max(1, (n_tok + kTileTok - 1) / kTileTok);  // q rides the first
+        const CUtensorMap* mk = cur ? &tk1 : &tk0;
+        const CUtensorMap* mv = cur ? &tv1 : &tv0;
+        const uint16_t* ksg = cur ? a.ks[1] : a.ks[0];
+        const uint16_t* vsg = cur ? a.vs[1] : a.vs[0];
+        const size_t row0 = (size_t)unit * a.C + lo;
+        for (int it = 0; it < n_stage; ++it) {
+          const int s = issued % NSTAGE;
+          if (issued >= NSTAGE &&
+              !mbar_wait_or_abort(bar_empty + 8 * s, ((issued / NSTAGE) & 1) ^ 1, a.status, 2,
+                                  abort))
+            break;
+          const int nt = min(kTileTok, n_tok - it * kTileTok);  // may be <= 0 (q only)
+          int* inf = info + s * kInfo;
+          inf[kInfoUnit] = unit;
+          inf[kInfoSplit] = split;
+          inf[kInfoNt] = max(nt, 0);
+          inf[kInfoLast] = it == n_stage - 1;
+          inf[kInfoTok0] = lo + it * kTileTok;
+          inf[kInfoSink] = m[FADE_META_N_SINK];
+          inf[kInfoRec] = m[FADE_META_N_RECENT];
+          inf[kInfoHead] = m[FADE_META_HEAD];
+          const uint32_t stage = sbase + s * Cfg::STAGE;
+          uint32_t bytes = 0;
+          if (nt > 0) {
+            // scale rows copied: rounded up so the copy is a multiple of 16 bytes (it stays
+            // inside the unit: rows start at multiples of 4 and the slot stride is a multiple
+            // of 64)
+            constexpr int kAlign = 16 / (Cfg::SROW * 2);
+            const int ns = (nt + kAlign - 1) / kAlign * kAlign;
+            bytes += kTileTok * (Cfg::KROW + Cfg::VROW) + 2u * ns * Cfg::SROW * 2;
+          }
+          if (it == 0) bytes += G * D * 2;
+          mbar_expect_tx(bar_full + 8 * s, bytes);
+          if (nt > 0) {
+            constexpr int kAlign = 16 / (Cfg::SROW * 2);
+            const int ns = (nt + kAlign - 1) / kAlign * kAlign;
+            const size_t r = row0 + (size_t)it * kTileTok;
+            tma_load_2d(stage + Cfg::K_OFF, mk, 0, (int)r, bar_full + 8 * s);
+            tma_load_2d(stage + Cfg::V_OFF, mv, 0, (int)r, bar_full + 8 * s);
+            bulk_load_1d(stage + Cfg::KS_OFF, ksg + r * Cfg::SROW, ns * Cfg::SROW * 2,
+                         bar_full + 8 * s);
+            bulk_load_1d(stage + Cfg::VS_OFF, vsg + r * Cfg::SROW, ns * Cfg::SROW * 2,
+                         bar_full + 8 * s);
+          }
+          if (it == 0)
+            bulk_load_1d(stage + Cfg::Q_OFF, a.q + (size_t)(b * a.Hq + hk * G) * D, G * D * 2,
+                         bar_full + 8 * s);
+          ++issued;
+        }
+      }
+      // never leave the CTA with copies in flight: wait (bounded) for the last issued stages
+      for (int k = max(0, issued - NSTAGE); k < issued; ++k)
+        mbar_wait(bar_full + 8 * (k % NSTAGE), (k / NSTAGE) & 1, a.status, 3);
+    }
+    // the producer warp takes part in no further barrier
+    return;
   }
-#pragma unroll
-  for (int s = 0; s < NHALF; ++s)
-#pragma unroll
-    for (int mm = 0; mm < 4; ++mm)
-#pragma unroll
-      for (int j = 0; j < NT; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[s][mm][j][e] = 0.f;
 
-  float* wm = reinterpret_cast<float*>(smem);                  // [kConsumers][8]
-  float* wl = wm + kConsumers * 8;                             // [kConsumers][8]
-  float* wo = wl + kConsumers * 8;                             // [kConsumers][G][D]
+  // ------------------------------------------------------------ consumers
+  const float c2 = a.inv_sqrt_d * kLog2e;
+  const int wr0 = warp * MmaShape<D, G>::WARP_TOK;
+  const LaneOffsets<D> lo_ = lane_offsets<D>(wr0, lane);
+  const bool want_logits = a.logits != nullptr;
+  int used = 0;  // stages consumed so far (the producer's `issued` sequence)
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    int s_ = used % NSTAGE;
+    bool ok = !*abort && mbar_wait_or_abort(bar_full + 8 * s_, (used / NSTAGE) & 1, a.status, 1,
+                                            abort);
+    const int* inf = info + s_ * kInfo;
+    const int unit = item % units, split = item / units;
+    const int b = unit / a.H, hk = unit % a.H, hq0 = hk * G;
+    const uint16_t* qs = reinterpret_cast<const uint16_t*>(smem + s_ * Cfg::STAGE + Cfg::Q_OFF);
+    float m2[NT], lsum[NT];
+    float o[NHALF][4][NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      m2[j] = -INFINITY;
+      lsum[j] = 0.f;
+    }
+#pragma unroll
+    for (int s = 0; s < NHALF; ++s)
+#pragma unroll
+      for (int mm = 0; mm < 4; ++mm)
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[s][mm][j][e] = 0.f;
 
-  if (split == 0) {
-    // ------------------------------------------------------------ FP16 tiers (CUDA cores)
-    // Warp w takes tokens w, w+4, ...; lane l holds channels l*CPL .. l*CPL+CPL-1.
-    if (warp < kConsumers) {
+    if (split == 0) {
+      // ---------------------------------------------------------- FP16 tiers (CUDA cores)
+      // warp w takes tokens w, w + kConsumers, ...; lane l holds channels l*CPL .. +CPL-1
       constexpr int CPL = D / 32;
       float qr[G][CPL], acc[G][CPL], mm_[G], ll[G];
-      const uint16_t* qrow = a.q + (size_t)(b * a.Hq + hq0) * D;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         mm_[h] = -INFINITY;
         ll[h] = 0.f;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
-          qr[h][c] = __half2float(__ushort_as_half(qrow[(size_t)h * D + lane * CPL + c]));
+          qr[h][c] = ok ? __half2float(__ushort_as_half(qs[h * D + lane * CPL + c])) : 0.f;
           acc[h][c] = 0.f;
         }
       }
-      const float c2 = a.inv_sqrt_d * kLog2e;
-      for (int u = warp; u < n_tok; u += kConsumers) {
-        const bool is_sink = u < n_sink;
-        const int slot = is_sink ? u : (head_slot + u - n_sink) % a.W;
-        const size_t row = is_sink ? ((size_t)unit * a.S + u) * D : ((size_t)unit * a.W + slot) * D;
-        const uint16_t* kr = (is_sink ? a.sink_k : a.rec_k) + row + lane * CPL;
-        const uint16_t* vr = (is_sink ? a.sink_v : a.rec_v) + row + lane * CPL;
-        float kv[CPL], vv[CPL];
+      const int n_sink = ok ? inf[kInfoSink] : 0, n_rec = ok ? inf[kInfoRec] : 0;
+      const int head_slot = ok ? inf[kInfoHead] : 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * s_);  // q is in registers: release the stage
+      ++used;
+      const int n_tok = n_sink + n_rec;
+      // two tokens per pass (u and u + kConsumers): both rows are loaded before either is used
+      for (int u0 = warp; u0 < n_tok; u0 += 2 * kConsumers) {
+        float kv[2][CPL], vv[2][CPL];
+        int lidx[2];
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-          kv[c] = __half2float(__ushort_as_half(kr[c]));
-          vv[c] = __half2float(__ushort_as_half(vr[c]));
+        for (int e = 0; e < 2; ++e) {
+          const int u = min(u0 + e * kConsumers, n_tok - 1);  // a duplicate is masked below
+          const bool is_sink = u < n_sink;
+          const int slot = is_sink ? u : (head_slot + u - n_sink) % a.W;
+          const size_t row =
+              is_sink ? ((size_t)unit * a.S + u) * D : ((size_t)unit * a.W + slot) * D;
+          load_f16_lane<CPL>((is_sink ? a.sink_k : a.rec_k) + row + lane * CPL, kv[e]);
+          load_f16_lane<CPL>((is_sink ? a.sink_v : a.rec_v) + row + lane * CPL, vv[e]);
+          lidx[e] = is_sink ? u : a.S + a.C + slot;
         }
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float d = 0.f;
+        for (int e = 0; e < 2; ++e) {
+          if (u0 + e * kConsumers >= n_tok) break;  // warp-uniform
+          float d[G];
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) d = fmaf(qr[h][c], kv[c], d);
-          d = warp_sum(d);
-          if (a.logits && lane == 0)
-            a.logits[(size_t)(b * a.Hq + hq0 + h) * a.NS + (is_sink ? u : a.S + a.C + slot)] =
-                d * a.inv_sqrt_d;
-          const float s2 = d * c2;
-          const float mn = fmaxf(mm_[h], s2);
-          const float al = exp2f(mm_[h] - mn);   // 0 when the old max is -inf
-          const float p = exp2f(s2 - mn);
-          ll[h] = ll[h] * al + p;
+          for (int h = 0; h < G; ++h) {
+            d[h] = 0.f;
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) acc[h][c] = fmaf(p, vv[c], acc[h][c] * al);
-          mm_[h] = mn;
+            for (int c = 0; c < CPL; ++c) d[h] = fmaf(qr[h][c], kv[e][c], d[h]);
+          }
+          warp_allreduce<G>(d, lane);
+          if (want_logits && lane < G)
+            a.logits[(size_t)(b * a.Hq + hq0 + lane) * a.NS + lidx[e]] =
+                pick(d, lane) * a.inv_sqrt_d;
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float s2 = d[h] * c2;
+            const float mn = fmaxf(mm_[h], s2);
+            const float al = ex2(mm_[h] - mn);   // 0 when the old max is -inf
+            const float p = ex2(s2 - mn);
+            ll[h] = ll[h] * al + p;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) acc[h][c] = fmaf(p, vv[e][c], acc[h][c] * al);
+            mm_[h] = mn;
+          }
         }
       }
 #pragma unroll
@@ -353,55 +765,15 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
 #pragma unroll
         for (int c = 0; c < CPL; ++c) wo[(warp * G + h) * D + lane * CPL + c] = acc[h][c];
       }
-    }
-    __syncthreads();
-  } else if (warp == kConsumers) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const CUtensorMap* mk = cur ? &tk1 : &tk0;
-      const CUtensorMap* mv = cur ? &tv1 : &tv0;
-      const uint16_t* ksg = cur ? a.ks[1] : a.ks[0];
-      const uint16_t* vsg = cur ? a.vs[1] : a.vs[0];
-      int issued = 0;
-      for (int it = 0; it < n_tiles; ++it) {
-        const int s = it % NSTAGE;
-        if (it >= NSTAGE &&
-            !mbar_wait(bar_empty + 8 * s, ((it / NSTAGE) & 1) ^ 1, a.status, 2)) {
-          failed = true;
-          break;
-        }
-        const int nt = min(kTileTok, n_tok - it * kTileTok);
-        // scale rows copied: rounded up so the copy is a multiple of 16 bytes (it stays inside
-        // the unit: rows start at multiples of 4 and the slot stride is a multiple of 64)
-        constexpr int kAlign = 16 / (Cfg::SROW * 2);
-        const int ns = (nt + kAlign - 1) / kAlign * kAlign;
-        const size_t r = row0 + (size_t)it * kTileTok;
-        const uint32_t stage = sbase + s * Cfg::STAGE;
-        const uint32_t bytes = kTileTok * (Cfg::KROW + Cfg::VROW) + 2u * ns * Cfg::SROW * 2;
-        mbar_expect_tx(bar_full + 8 * s, bytes);
-        tma_load_2d(stage + Cfg::K_OFF, mk, 0, (int)r, bar_full + 8 * s);
-        tma_load_2d(stage + Cfg::V_OFF, mv, 0, (int)r, bar_full + 8 * s);
-        bulk_load_1d(stage + Cfg::KS_OFF, ksg + r * Cfg::SROW, ns * Cfg::SROW * 2,
-                     bar_full + 8 * s);
-        bulk_load_1d(stage + Cfg::VS_OFF, vsg + r * Cfg::SROW, ns * Cfg::SROW * 2,
-                     bar_full + 8 * s);
-        ++issued;
-      }
-      // never leave the CTA with copies in flight: wait (bounded) for every issued tile
-      for (int it = max(0, issued - NSTAGE); it < issued; ++it)
-        mbar_wait(bar_full + 8 * (it % NSTAGE), (it / NSTAGE) & 1, a.status, 3);
-    }
-  } else {
-    // ------------------------------------------------------------ consumers
-    // query B operand: column n of n-tile j = (head 4j + n/2, parity n%2); thread (g, t)
-    // holds column g, k-slots {2t, 2t+1} (group 2s of half s) and {2t+8, 2t+9} (group 2s+1)
-    uint32_t qb[NHALF][4][NT][2];
-    {
-      const uint16_t* qrow = a.q + (size_t)(b * a.Hq + hq0) * D;
+    } else {
+      // ---------------------------------------------------------- packed middle tier (MMA)
+      // query B operand: column n of n-tile j = (head 4j + n/2, parity n%2); thread (g, t)
+      // holds column g, k-slots {2t, 2t+1} (group 2s of half s) and {2t+8, 2t+9} (group 2s+1)
+      uint32_t qb[NHALF][4][NT][2];
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         const int h = 4 * j + g / 2, par = g & 1;
-        const bool valid = h < G;
+        const bool valid = ok && h < G;
 #pragma unroll
         for (int s = 0; s < NHALF; ++s)
 #pragma unroll
@@ -410,233 +782,106 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
             const int c_hi = c_lo + 32;                  // group 2s+1
             uint16_t v0 = 0, v1 = 0, v2 = 0, v3 = 0;
             if (valid && par == 0) {
-              v0 = qrow[(size_t)h * D + c_lo];
-              v1 = qrow[(size_t)h * D + c_lo + 4];
+              v0 = qs[h * D + c_lo];
+              v1 = qs[h * D + c_lo + 4];
             }
             if (valid && par == 1) {
-              v2 = qrow[(size_t)h * D + c_hi];
-              v3 = qrow[(size_t)h * D + c_hi + 4];
+              v2 = qs[h * D + c_hi];
+              v3 = qs[h * D + c_hi + 4];
             }
             qb[s][kp][j][0] = uint32_t(v0) | (uint32_t(v1) << 16);
             qb[s][kp][j][1] = uint32_t(v2) | (uint32_t(v3) << 16);
           }
       }
-    }
-    const float c2 = a.inv_sqrt_d * kLog2e;
-
-    for (int it = 0; it < n_tiles; ++it) {
-      const int s_ = it % NSTAGE;
-      if (!mbar_wait(bar_full + 8 * s_, (it / NSTAGE) & 1, a.status, 1)) {
-        failed = true;
-        break;
+      float* logit_base =
+          want_logits ? a.logits + (size_t)(b * a.Hq + hq0) * a.NS + a.S : nullptr;
+      while (true) {
+        const int nt = ok ? inf[kInfoNt] : 0;
+        const bool last = ok ? inf[kInfoLast] != 0 : true;
+        const uint32_t stage = sbase + s_ * Cfg::STAGE;
+        float* logit_row = want_logits ? logit_base + (ok ? inf[kInfoTok0] : 0) : nullptr;
+        if (ok) {
+          if (want_logits) {
+            if (nt == kTileTok)
+              consume_tile<D, G, true, true>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o, c2,
+                                             logit_row);
+            else if (wr0 < nt)
+              consume_tile<D, G, false, true>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o, c2,
+                                              logit_row);
+          } else {
+            if (nt == kTileTok)
+              consume_tile<D, G, true, false>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o, c2,
+                                              logit_row);
+            else if (wr0 < nt)
+              consume_tile<D, G, false, false>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o, c2,
+                                               logit_row);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_empty + 8 * s_);
+          ++used;
+        }
+        if (last) break;
+        s_ = used % NSTAGE;
+        ok = !*abort && mbar_wait_or_abort(bar_full + 8 * s_, (used / NSTAGE) & 1, a.status, 1,
+                                           abort);
+        inf = info + s_ * kInfo;
       }
-      const int nt = min(kTileTok, n_tok - it * kTileTok);
-      const int wr0 = warp * kWarpTok;
-      const uint32_t stage = sbase + s_ * Cfg::STAGE;
-      const uint8_t* st_ptr = smem + s_ * Cfg::STAGE;
-      const uint16_t* kss = reinterpret_cast<const uint16_t*>(st_ptr + Cfg::KS_OFF);
-      const uint16_t* vss = reinterpret_cast<const uint16_t*>(st_ptr + Cfg::VS_OFF);
-      if (wr0 < nt) {
-        float sc[kMT][NT][2];  // logits (exp2 domain) of tokens g, g+8 of each M-tile
+      // total probability mass of each head over the warp's tokens (lanes sharing t)
 #pragma unroll
-        for (int mt = 0; mt < kMT; ++mt) {
-          const int r0 = wr0 + mt * 16;
-          float ks_lo[D / kGroup], ks_hi[D / kGroup];
-          load_scale_row<D / kGroup>(kss + (r0 + g) * Cfg::SROW, true, ks_lo);
-          load_scale_row<D / kGroup>(kss + (r0 + g + 8) * Cfg::SROW, true, ks_hi);
-          float acc_s[NT][2];
+      for (int j = 0; j < NT; ++j) {
+        lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], 4);
+        lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], 8);
+        lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], 16);
+      }
+      const int gsel = g >= 4 ? 1 : 0;  // the column parity that matches row g's group
 #pragma unroll
-          for (int j = 0; j < NT; ++j) acc_s[j][0] = acc_s[j][1] = 0.f;
-#pragma unroll
-          for (int s = 0; s < NHALF; ++s) {
-            // K rows r0..r0+15, 16-byte chunks 2s and 2s+1 (one 32-channel group each)
-            const int lrow = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-            const int chunk = 2 * s + (lane >> 4);
-            int sw;
-            if constexpr (D == 128)
-              sw = (chunk ^ ((lrow >> 1) & 3));            // 64-byte swizzle
-            else
-              sw = (chunk ^ ((lrow >> 2) & 1));            // 32-byte swizzle
-            uint32_t k0, k1, k2, k3;  // (rows g, chunk 2s) (g+8, 2s) (g, 2s+1) (g+8, 2s+1)
-            ldsm_x4(stage + Cfg::K_OFF + lrow * Cfg::KROW + sw * 16, k0, k1, k2, k3);
-            float cacc[NT][4];
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) cacc[j][e] = 0.f;
-#define FADE_KSTEP(KP)                                                                    \
-  {                                                                                       \
-    const uint32_t a0 = k_pair<KP>(k0), a1 = k_pair<KP>(k1), a2 = k_pair<KP>(k2),         \
-                   a3 = k_pair<KP>(k3);                                                   \
-    _Pragma("unroll") for (int j = 0; j < NT; ++j)                                        \
-        mma16816(cacc[j], a0, a1, a2, a3, qb[s][KP][j][0], qb[s][KP][j][1]);              \
-  }
-            FADE_KSTEP(0) FADE_KSTEP(1) FADE_KSTEP(2) FADE_KSTEP(3)
-#undef FADE_KSTEP
-            // column 2t = (head 4j+t, group 2s), column 2t+1 = (head 4j+t, group 2s+1)
-#pragma unroll
-            for (int j = 0; j < NT; ++j) {
-              acc_s[j][0] = fmaf(cacc[j][0], ks_lo[2 * s], acc_s[j][0]);
-              acc_s[j][0] = fmaf(cacc[j][1], ks_lo[2 * s + 1], acc_s[j][0]);
-              acc_s[j][1] = fmaf(cacc[j][2], ks_hi[2 * s], acc_s[j][1]);
-              acc_s[j][1] = fmaf(cacc[j][3], ks_hi[2 * s + 1], acc_s[j][1]);
-            }
+      for (int j = 0; j < NT; ++j) {
+        const int h = 4 * j + t;
+        if (h < G) {
+          if (g == 0) {
+            wm[warp * 8 + h] = m2[j];
+            wl[warp * 8 + h] = lsum[j];
           }
-#pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            const int h = 4 * j + t;
-            const bool hv = h < G;
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const int tok = r0 + g + 8 * r;
-              const bool tv = tok < nt;
-              if (a.logits && hv && tv)
-                a.logits[(size_t)(b * a.Hq + hq0 + h) * a.NS + a.S + lo + it * kTileTok + tok] =
-                    acc_s[j][r] * a.inv_sqrt_d;
-              sc[mt][j][r] = (hv && tv) ? acc_s[j][r] * c2 : -INFINITY;
-            }
-          }
-        }
-        // online softmax (per head column t of each n-tile; warp-uniform running max)
-        float alpha[NT];
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          float mx = -INFINITY;
-#pragma unroll
-          for (int mt = 0; mt < kMT; ++mt) mx = fmaxf(mx, fmaxf(sc[mt][j][0], sc[mt][j][1]));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float mn = fmaxf(m2[j], mx);
-          alpha[j] = (mn == -INFINITY) ? 1.f : exp2f(m2[j] - mn);
-          m2[j] = mn;
-          float ps = 0.f;
-#pragma unroll
-          for (int mt = 0; mt < kMT; ++mt)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const float p = (sc[mt][j][r] == -INFINITY) ? 0.f : exp2f(sc[mt][j][r] - mn);
-              sc[mt][j][r] = p;
-              ps += p;
-            }
-          lsum[j] = lsum[j] * alpha[j] + ps;
-        }
-        // rescale the accumulators only when some column's running max moved (warp-uniform)
-        bool moved = false;
-#pragma unroll
-        for (int j = 0; j < NT; ++j) moved |= alpha[j] != 1.f;
-        if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
           for (int s = 0; s < NHALF; ++s)
 #pragma unroll
-            for (int mm = 0; mm < 4; ++mm)
-#pragma unroll
-              for (int j = 0; j < NT; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) o[s][mm][j][e] *= alpha[j];
-        }
-
-        // PV over the warp's M-tiles (16 tokens each = one MMA k-step)
-#pragma unroll
-        for (int mt = 0; mt < kMT; ++mt) {
-          const int r0 = wr0 + mt * 16;
-          // past the tile's tokens the scale rows may never have been copied: use 0 so that a
-          // zero probability cannot meet a non-finite leftover
-          float vs_lo[D / kGroup], vs_hi[D / kGroup];
-          load_scale_row<D / kGroup>(vss + (r0 + g) * Cfg::SROW, r0 + g < nt, vs_lo);
-          load_scale_row<D / kGroup>(vss + (r0 + g + 8) * Cfg::SROW, r0 + g + 8 < nt, vs_hi);
-          uint32_t X[2 * NHALF];  // (tokens 0-7 | 8-15) x (channel half)
-          {
-            const int lrow = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-            if constexpr (D == 128) {
-              const int chunk = lane >> 4;
-              const int sw = chunk ^ ((lrow >> 2) & 1);    // 32-byte swizzle
-              ldsm_x4_t(stage + Cfg::V_OFF + lrow * Cfg::VROW + sw * 16, X[0], X[1], X[2], X[3]);
-            } else {
-              ldsm_x2_t(stage + Cfg::V_OFF + lrow * Cfg::VROW, X[0], X[1]);
+            for (int mm = 0; mm < 4; ++mm) {
+              const int c = 64 * s + 8 * g + 2 * mm;
+              wo[(warp * G + h) * D + c] = gsel ? o[s][mm][j][1] : o[s][mm][j][0];
+              wo[(warp * G + h) * D + c + 1] = gsel ? o[s][mm][j][3] : o[s][mm][j][2];
             }
-          }
-#pragma unroll
-          for (int s = 0; s < NHALF; ++s) {
-            uint32_t pb[NT][2];
-#pragma unroll
-            for (int j = 0; j < NT; ++j) {
-              const float p0 = sc[mt][j][0], p1 = sc[mt][j][1];
-              const uint32_t lo_ = h2_as_u32(__floats2half2_rn(p0 * vs_lo[2 * s], p0 * vs_lo[2 * s + 1]));
-              const uint32_t hi_ = h2_as_u32(__floats2half2_rn(p1 * vs_hi[2 * s], p1 * vs_hi[2 * s + 1]));
-              pb[j][0] = movm_t(lo_);
-              pb[j][1] = movm_t(hi_);
-            }
-            const uint32_t xa = X[2 * s], xb = X[2 * s + 1];
-            const uint32_t xa10 = xa >> 10, xb10 = xb >> 10;
-#define FADE_PV(MM)                                                                         \
-  {                                                                                         \
-    const uint32_t a0 = v_crumb<2 * MM>(xa, xa10), a1 = v_crumb<2 * MM + 1>(xa, xa10);      \
-    const uint32_t a2 = v_crumb<2 * MM>(xb, xb10), a3 = v_crumb<2 * MM + 1>(xb, xb10);      \
-    _Pragma("unroll") for (int j = 0; j < NT; ++j)                                          \
-        mma16816(o[s][MM][j], a0, a1, a2, a3, pb[j][0], pb[j][1]);                          \
-  }
-            FADE_PV(0) FADE_PV(1) FADE_PV(2) FADE_PV(3)
-#undef FADE_PV
-          }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + 8 * s_);
     }
-
-    // total probability mass of each head over the warp's tokens (lanes sharing t)
+    // ------------------------------------------------------------ merge the consumer warps
+    consumer_bar<kConsumers>();
+    const size_t pbase = ((size_t)(b * a.Hq + hq0)) * a.nsplit + split;
+    if (threadIdx.x < G) {
+      const int h = threadIdx.x;
+      float M = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], 4);
-      lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], 8);
-      lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], 16);
-    }
-  }
-  // Past this barrier every tile is consumed and the producer has drained its copies, so
-  // the stage memory can hold the per-warp results.
-  if (split > 0) __syncthreads();
-  if (split > 0 && warp < kConsumers) {
-    const int gsel = g >= 4 ? 1 : 0;  // the column parity that matches row g's group
+      for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, wm[w * 8 + h]);
+      float L = 0.f;
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      const int h = 4 * j + t;
-      if (h < G) {
-        if (g == 0) {
-          wm[warp * 8 + h] = m2[j];
-          wl[warp * 8 + h] = lsum[j];
-        }
-#pragma unroll
-        for (int s = 0; s < NHALF; ++s)
-#pragma unroll
-          for (int mm = 0; mm < 4; ++mm) {
-            const int c = 64 * s + 8 * g + 2 * mm;
-            wo[(warp * G + h) * D + c] = gsel ? o[s][mm][j][1] : o[s][mm][j][0];
-            wo[(warp * G + h) * D + c + 1] = gsel ? o[s][mm][j][3] : o[s][mm][j][2];
-          }
+      for (int w = 0; w < kConsumers; ++w) {
+        const float f = (wm[w * 8 + h] == -INFINITY) ? 0.f : ex2(wm[w * 8 + h] - M);
+        wf[h * kConsumers + w] = f;
+        L = fmaf(wl[w * 8 + h], f, L);
       }
-    }
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    const int h = i / D, c = i % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, wm[w * 8 + h]);
-    float L = 0.f, O = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConsumers; ++w) {
-      const float f = (wm[w * 8 + h] == -INFINITY) ? 0.f : exp2f(wm[w * 8 + h] - M);
-      L = fmaf(wl[w * 8 + h], f, L);
-      O = fmaf(wo[(w * G + h) * D + c], f, O);
-    }
-    a.part_acc[(pbase + (size_t)h * a.nsplit) * D + c] = O;
-    if (c == 0) {
       a.part_ml[(pbase + (size_t)h * a.nsplit) * 2] = M * kLn2;  // natural-log units
       a.part_ml[(pbase + (size_t)h * a.nsplit) * 2 + 1] = L;
     }
+    consumer_bar<kConsumers>();
+    for (int i = threadIdx.x; i < G * D; i += kConsumers * 32) {
+      const int h = i / D, c = i % D;
+      float O = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumers; ++w)
+        O = fmaf(wo[(w * G + h) * D + c], wf[h * kConsumers + w], O);
+      a.part_acc[(pbase + (size_t)h * a.nsplit) * D + c] = O;
+    }
+    consumer_bar<kConsumers>();  // the merge area is rewritten by the next item
   }
-  (void)failed;
 }
 
 // ------------------------------------------------------------------ host side
@@ -694,8 +939,14 @@ fade_status_t launch_mma(const fade_config_t* c, const fade_layer_t* L, const Mm
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
       cudaSuccess)
     return launch_status("fade_decode_attention (middle tier) shared-memory opt-in");
-  kern<<<dim3(n_splits, c->num_kv_heads, c->batch), kThreadsMma, Cfg::SMEM, st>>>(
-      tk[0], tk[1], tv[0], tv[1], a);
+  // persistent grid: as many CTAs as fit on the device at once (never more than the items)
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return launch_status("fade_decode_attention (middle tier) device query");
+  const long long items = (long long)c->batch * c->num_kv_heads * n_splits;
+  const int grid = (int)std::min<long long>(items, (long long)sms * MmaShape<D, G>::MINB);
+  kern<<<grid, MmaShape<D, G>::THREADS, Cfg::SMEM, st>>>(tk[0], tk[1], tv[0], tv[1], a);
   return launch_status("fade_decode_attention (middle tier)");
 }
 
@@ -724,6 +975,7 @@ fade_status_t launch_mid_mma(const fade_config_t* c, const fade_layer_t* L, cons
   a.part_ml = part_ml;
   a.part_acc = part_acc;
   a.status = L->status;
+  a.B = c->batch;
   a.Hq = c->num_q_heads;
   a.H = c->num_kv_heads;
   a.S = c->n_sink;

@@ -347,16 +347,102 @@ __global__ void __launch_bounds__(kSelThreads) evict_select_kernel(LayerArgs a) 
                a.chunk_base + (size_t)unit * a.chunk_slots);
 }
 
-// Compact survivors of the live middle buffer into the other one, re-positioning keys whose
-// index drops; the last x-block re-positions the recent ring in place.
-// grid = (ceil(max_mid / compact_tok<D>()) + 1, H, B), 256 threads. Middle tokens: D/32 threads
-// per token; thread (gp, hf) owns rotation pairs 32gp + 16hf .. +15, i.e. half of group gp
-// (channels 32gp + 16hf + j) and the matching half of its partner group gp + D/64 (channels
-// D/2 + 32gp + 16hf + j). A moved key is dequantised, un-RoPE'd / re-RoPE'd and re-quantised;
-// each group's absmax is completed with the neighbouring thread (lane ^ 1).
-template <int D>
-__host__ __device__ constexpr int compact_tok() { return 256 / (D / 32); }
+// 8 consecutive fp16 values (16-byte aligned) as 4 packed fp32 pairs, and back (RN to fp16).
+__device__ __forceinline__ void load_f16x8(const uint16_t* p, f2x (&X)[4]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+    X[k] = f2_pack(f.x, f.y);
+  }
+}
+__device__ __forceinline__ void store_f16x8(const f2x (&X)[4], uint16_t* p) {
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float lo, hi;
+    f2_unpack(X[k], lo, hi);
+    const __half2 h = __floats2half2_rn(lo, hi);
+    w[k] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
 
+// Asynchronous global -> shared copies of N bytes (4, 8 or 16; both addresses N-aligned).
+template <int N>
+__device__ __forceinline__ void cp_async(void* smem_dst, const void* gmem_src) {
+  static_assert(N == 4 || N == 8 || N == 16, "cp.async copies 4, 8 or 16 bytes");
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(d), "l"(gmem_src), "n"(N)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// One unit's middle-tier rows for compaction: source (live) and destination buffers, each at
+// the unit's slot 0.
+struct HeadPtrs {
+  const uint8_t* ks;
+  uint8_t* kd;
+  const uint8_t* vs;
+  uint8_t* vd;
+  const uint16_t* kss;
+  uint16_t* ksd;
+  const uint16_t* vss;
+  uint16_t* vsd;
+  const float* scs;
+  float* scd;
+};
+
+template <int D>
+struct CompactCfg {
+  static constexpr int TPT = D / 32;        // threads per middle token
+  static constexpr int TOK = 256 / TPT;     // middle indices per CTA
+  static constexpr int ROWF4 = D / 4;       // float4 per RoPE row: d/2 pairs x (cos, sin)
+  static constexpr int NROWS = TOK + 32;    // staged RoPE rows (blocks with n_ev <= 32)
+  static constexpr int PRE = TOK / 32 + 2;  // per-head ints: victim prefix words + base
+  // prefetch buffers: per thread its K code share (two buffers) and V code share (one); per
+  // token its K scale row (two buffers), V scale row and score (one)
+  static constexpr int KSH = 2 * 16 * 4 / 8;     // bytes of K codes per thread (INT4 worst case)
+  static constexpr int VSH = 16;                 // bytes of V codes per thread (INT4 worst case)
+  static constexpr int SRB = D / 32 * 2;         // bytes of one scale row
+  static constexpr int PF_BYTES = 2 * 256 * KSH + 256 * VSH + TOK * (3 * SRB + 4);
+  // staged rows, prefetch buffers, then per head: row pointers, 4 counts, the victim prefixes
+  static size_t smem(int H) {
+    return (size_t)NROWS * ROWF4 * 16 + PF_BYTES +
+           (size_t)H * (sizeof(HeadPtrs) + (PRE + 4) * 4);
+  }
+};
+
+// Swizzled float4 slot of (row, j) in the staged table: the 8 threads of a quarter warp (two or
+// four consecutive tokens, each reading float4 j = 8*t_ + k) land in 8 different bank quads.
+template <int D>
+__device__ __forceinline__ int tab_slot(int row, int j) {
+  if constexpr (D == 128)
+    return row * 32 + (j ^ (((j >> 3) & 3) | ((row & 1) << 2)));
+  else
+    return row * 16 + (j ^ (((j >> 3) & 1) | ((row & 3) << 1)));
+}
+
+template <int D>
+__host__ __device__ constexpr int compact_tok() { return CompactCfg<D>::TOK; }
+
+// Compact survivors of the live middle buffer into the other one, re-positioning keys whose
+// index drops (the recent rings follow in evict_recent_commit_kernel).
+// grid = (ceil(max_mid / TOK), B), 256 threads; one CTA takes one block of TOK middle indices
+// of one batch row and loops over the row's KV heads. Middle tokens: D/32 threads per token;
+// thread (gp, hf) owns rotation pairs 32gp + 16hf .. +15, i.e. half of group gp (channels
+// 32gp + 16hf + j) and the matching half of its partner group gp + D/64 (channels
+// D/2 + 32gp + 16hf + j). A moved key is dequantised, un-RoPE'd / re-RoPE'd and re-quantised;
+// each group's absmax is completed with the neighbouring thread (lane ^ 1). The RoPE rows the
+// block needs (its old positions and the new ones, at most 64 below) are staged once per CTA in
+// shared memory and serve every head.
 // Resident CTAs per SM asked of the register allocator for the compaction kernel.
 #ifndef FADE_COMPACT_MIN_CTAS
 #define FADE_COMPACT_MIN_CTAS 3
@@ -364,202 +450,392 @@ __host__ __device__ constexpr int compact_tok() { return 256 / (D / 32); }
 
 template <int D, int KB, int VB>
 __global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kernel(LayerArgs a) {
-  constexpr int TPT = D / 32;            // threads per token
-  constexpr int TOK = compact_tok<D>();  // tokens per CTA
+  using CC = CompactCfg<D>;
+  constexpr int TPT = CC::TPT, TOK = CC::TOK;
   constexpr int HB = 16 * KB / 8;        // bytes of half a group's K codes
   constexpr int VROW = D * VB / 8, SROW = D / kGroup, KROW = D * KB / 8;
-  const int unit = blockIdx.z * a.H + blockIdx.y;
-  const int32_t* m = a.meta + unit * kF;
-  const int n_mid = m[FADE_META_N_MID], cur = m[FADE_META_CUR];
-  // the position policy evicts the oldest slots: no selection pass, no victim bitmap
-  const int n_ev = a.positional ? max(0, n_mid - a.budget) : m[FADE_META_N_EV];
-  if (n_ev == 0) return;
-  const int n_sink = m[FADE_META_N_SINK], n_rec = m[FADE_META_N_RECENT];
-  const int head = m[FADE_META_HEAD];
+  extern __shared__ float4 tab[];        // [NROWS][ROWF4] swizzled, then the buffers below
+  uint8_t* pf = reinterpret_cast<uint8_t*>(tab + CC::NROWS * CC::ROWF4);
+  uint8_t* kbuf = pf;                                   // [2][256][KSH]
+  uint8_t* vbuf = kbuf + 2 * 256 * CC::KSH;             // [256][VSH]
+  uint8_t* ksbuf = vbuf + 256 * CC::VSH;                // [2][TOK][SRB]
+  uint8_t* vsbuf = ksbuf + 2 * TOK * CC::SRB;           // [TOK][SRB]
+  float* scbuf = reinterpret_cast<float*>(vsbuf + TOK * CC::SRB);  // [TOK]
+  HeadPtrs* hptr = reinterpret_cast<HeadPtrs*>(pf + CC::PF_BYTES);  // [H]
+  int* hinfo = reinterpret_cast<int*>(hptr + a.H);  // [H][4]: n_mid n_ev n_sink cur
+  int* hpre = hinfo + a.H * 4;                       // [H][PRE]
+  __shared__ int s_rlo, s_rhi;
+  const int b = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nblk = gridDim.x - 1;
-
-  if ((int)blockIdx.x == nblk) {
-    // recent ring: every token's index drops by n_ev; rewrite keys in place
-    for (int t = warp; t < n_rec; t += 8) {
-      const int slot = (head + t) % a.W;
-      uint16_t* row = a.rec_k + ((size_t)unit * a.W + slot) * D;
-      WarpKey<D> k = load_fp16_key<D>(row);
-      const int pold = n_sink + n_mid + t;
-      reposition_key<D>(a, k, pold, pold - n_ev);
-      store_fp16_key<D>(k, row);
-    }
-    return;
-  }
 
   const int lo = blockIdx.x * TOK;
-  if (lo >= n_mid) return;  // uniform per CTA
-  const int hi = min(lo + TOK, n_mid);
-  const uint32_t* bm = a.victims + (size_t)unit * a.victim_words;
-  __shared__ int wpre[TOK / 32 + 1];
-  __shared__ int s_base;
-  if (warp == 0 && !a.positional) {
-    // victims before `lo`: chunk prefix plus the words of lo's chunk that precede it
-    const int w_lo = lo >> 5, w0 = (lo / kChunk) * (kChunk / 32);
-    int c = (w0 + lane < w_lo) ? __popc(bm[w0 + lane]) : 0;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-    const int nw = (hi - lo + 31) / 32;
-    const int wc = lane < nw ? __popc(bm[w_lo + lane]) : 0;
-    int incl = wc;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int tt = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += tt;
-    }
-    if (lane <= TOK / 32) wpre[lane] = incl - wc;
-    if (lane == 0) s_base = a.chunk_base[(size_t)unit * a.chunk_slots + lo / kChunk] + c;
+  if (threadIdx.x == 0) {
+    s_rlo = 0x7fffffff;
+    s_rhi = -1;
   }
   __syncthreads();
-  const int i = lo + threadIdx.x / TPT, t_ = threadIdx.x % TPT;
-  const int gp = t_ >> 1, hf = t_ & 1;
-  // The lanes of one token are adjacent (TPT divides 32) and share every flag below, so the
-  // warp-wide ballot and the absmax exchange see whole tokens; nothing exits before them.
-  const bool in_range = i < hi;
-  bool keep = in_range;
-  int nv = 0;
-  if (in_range) {
-    if (a.positional) {
-      keep = i >= n_ev;
-      nv = i - n_ev;
-    } else {
-      const uint32_t word = bm[i >> 5];
-      keep = !((word >> (i & 31)) & 1u);
-      nv = i - (s_base + wpre[(i - lo) >> 5] + __popc(word & ((1u << (i & 31)) - 1u)));
+  // per-head bookkeeping (warp w takes heads w, w+8, ...): counts, the victims before each
+  // 32-token word of the block, and the block's range of RoPE rows
+  for (int h = warp; h < a.H; h += 8) {
+    const int unit = b * a.H + h;
+    const int32_t* m = a.meta + unit * kF;
+    const int n_mid = m[FADE_META_N_MID];
+    const int n_ev = a.positional ? max(0, n_mid - a.budget) : m[FADE_META_N_EV];
+    const int n_sink = m[FADE_META_N_SINK];
+    if (lane == 0) {
+      const int cur = m[FADE_META_CUR];
+      hinfo[4 * h + 0] = n_mid;
+      hinfo[4 * h + 1] = n_ev;
+      hinfo[4 * h + 2] = n_sink;
+      hinfo[4 * h + 3] = cur;
+      const size_t u0 = (size_t)unit * a.C;  // the unit's slot 0
+      HeadPtrs P;  // (selects, not a runtime index into the parameter arrays)
+      P.ks = (cur ? a.mk[1] : a.mk[0]) + u0 * KROW;
+      P.kd = (cur ? a.mk[0] : a.mk[1]) + u0 * KROW;
+      P.vs = (cur ? a.mv[1] : a.mv[0]) + u0 * VROW;
+      P.vd = (cur ? a.mv[0] : a.mv[1]) + u0 * VROW;
+      P.kss = (cur ? a.mks[1] : a.mks[0]) + u0 * SROW;
+      P.ksd = (cur ? a.mks[0] : a.mks[1]) + u0 * SROW;
+      P.vss = (cur ? a.mvs[1] : a.mvs[0]) + u0 * SROW;
+      P.vsd = (cur ? a.mvs[0] : a.mvs[1]) + u0 * SROW;
+      P.scs = (cur ? a.mid_sc[1] : a.mid_sc[0]) + u0;
+      P.scd = (cur ? a.mid_sc[0] : a.mid_sc[1]) + u0;
+      hptr[h] = P;
+    }
+    if (n_ev == 0 || lo >= n_mid) continue;
+    const int hi = min(lo + TOK, n_mid);
+    if (!a.positional) {
+      const uint32_t* bm = a.victims + (size_t)unit * a.victim_words;
+      // victims before `lo`: chunk prefix plus the words of lo's chunk that precede it
+      const int w_lo = lo >> 5, w0 = (lo / kChunk) * (kChunk / 32);
+      int c = (w0 + lane < w_lo) ? __popc(bm[w0 + lane]) : 0;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+      const int nw = (hi - lo + 31) / 32;
+      const int wc = lane < nw ? __popc(bm[w_lo + lane]) : 0;
+      int incl = wc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int tt = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += tt;
+      }
+      if (lane <= TOK / 32) hpre[h * CC::PRE + lane] = incl - wc;
+      if (lane == 0)
+        hpre[h * CC::PRE + TOK / 32 + 1] =
+            a.chunk_base[(size_t)unit * a.chunk_slots + lo / kChunk] + c;
+    }
+    if (lane == 0) {
+      atomicMin(&s_rlo, n_sink + max(0, lo - n_ev));  // lowest new position of the block
+      atomicMax(&s_rhi, n_sink + hi);                  // one past the highest old position
     }
   }
-  const bool moved = keep && nv != i && a.table != nullptr;
-
-  const uint8_t* mk_s = cur ? a.mk[1] : a.mk[0];
-  uint8_t* mk_d = cur ? a.mk[0] : a.mk[1];
-  const uint8_t* mv_s = cur ? a.mv[1] : a.mv[0];
-  uint8_t* mv_d = cur ? a.mv[0] : a.mv[1];
-  const uint16_t* mks_s = cur ? a.mks[1] : a.mks[0];
-  uint16_t* mks_d = cur ? a.mks[0] : a.mks[1];
-  const uint16_t* mvs_s = cur ? a.mvs[1] : a.mvs[0];
-  uint16_t* mvs_d = cur ? a.mvs[0] : a.mvs[1];
-  const float* sc_s = cur ? a.mid_sc[1] : a.mid_sc[0];
-  float* sc_d = cur ? a.mid_sc[0] : a.mid_sc[1];
-  const size_t si = (size_t)unit * a.C + i, di = (size_t)unit * a.C + nv;
-  const int g1 = gp, g2 = gp + D / 64;
-  const uint8_t* krow_s = mk_s + si * KROW;
-  uint8_t* krow_d = mk_d + di * KROW;
-
-  if (keep) {
-    // V codes (this thread's share of the row), the V scales and the score
-    constexpr int VSH = VROW / TPT;
-    copy_row<VSH>(mv_s + si * VROW + t_ * VSH, mv_d + di * VROW + t_ * VSH);
-    if (hf == 0) {
-      mvs_d[di * SROW + g1] = mvs_s[si * SROW + g1];
-      mvs_d[di * SROW + g2] = mvs_s[si * SROW + g2];
+  __syncthreads();
+  const int rlo = s_rlo, rhi = s_rhi;
+  if (rhi < 0) return;  // no head has work in this block (uniform per CTA)
+  const bool staged = a.table != nullptr && rhi - rlo <= CC::NROWS;
+  if (staged) {
+    const float4* src = reinterpret_cast<const float4*>(a.table) + (size_t)rlo * CC::ROWF4;
+    for (int e = threadIdx.x; e < (rhi - rlo) * CC::ROWF4; e += 256) {
+      const int r = e / CC::ROWF4, j = e % CC::ROWF4;
+      tab[tab_slot<D>(r, j)] = __ldg(src + e);
     }
-    if (t_ == 0) sc_d[di] = sc_s[si];
-    if (!moved) {
-      copy_row<HB>(krow_s + g1 * 2 * HB + hf * HB, krow_d + g1 * 2 * HB + hf * HB);
-      copy_row<HB>(krow_s + g2 * 2 * HB + hf * HB, krow_d + g2 * 2 * HB + hf * HB);
-      if (hf == 0) {
-        mks_d[di * SROW + g1] = mks_s[si * SROW + g1];
-        mks_d[di * SROW + g2] = mks_s[si * SROW + g2];
+  }
+  __syncthreads();
+
+  const int it = threadIdx.x / TPT, t_ = threadIdx.x % TPT;
+  const int gp = t_ >> 1, hf = t_ & 1;
+  const int i = lo + it;
+  const int g1 = gp, g2 = gp + D / 64;
+  constexpr int VSH = VROW / TPT;  // this thread's bytes of a V code row
+  // K codes and scales of a head's token for this thread, and its V share, score and V scales,
+  // fetched ahead with cp.async (K one processed head ahead, V during the head itself)
+  auto has_work = [&](int hh) { return hinfo[4 * hh + 1] != 0 && lo < hinfo[4 * hh + 0]; };
+  auto prefetch_k = [&](int hh, int buf) {
+    if (i >= min(lo + TOK, hinfo[4 * hh + 0])) return;
+    const HeadPtrs& Q = hptr[hh];
+    const uint8_t* kr = Q.ks + (size_t)i * KROW + hf * HB;
+    uint8_t* kd = kbuf + (buf * 256 + threadIdx.x) * CC::KSH;
+    cp_async<HB>(kd, kr + g1 * 2 * HB);
+    cp_async<HB>(kd + HB, kr + g2 * 2 * HB);
+    if (t_ == 0) cp_async<SROW * 2>(ksbuf + (buf * TOK + it) * CC::SRB, Q.kss + (size_t)i * SROW);
+  };
+  auto prefetch_v = [&](int hh) {
+    if (i >= min(lo + TOK, hinfo[4 * hh + 0])) return;
+    const HeadPtrs& Q = hptr[hh];
+    cp_async<VSH>(vbuf + threadIdx.x * CC::VSH, Q.vs + (size_t)i * VROW + t_ * VSH);
+    if (t_ == 0) {
+      cp_async<SROW * 2>(vsbuf + it * CC::SRB, Q.vss + (size_t)i * SROW);
+      cp_async<4>(scbuf + it, Q.scs + i);
+    }
+  };
+  int kb = 0;  // K buffer of the head being processed
+  {
+    int h0 = 0;
+    while (h0 < a.H && !has_work(h0)) ++h0;
+    if (h0 < a.H) prefetch_k(h0, 0);
+    cp_async_commit();
+  }
+  for (int h = 0; h < a.H; ++h) {
+    const int n_mid = hinfo[4 * h + 0], n_ev = hinfo[4 * h + 1];
+    if (n_ev == 0 || lo >= n_mid) continue;  // uniform per CTA
+    const int n_sink = hinfo[4 * h + 2];
+    const int unit = b * a.H + h;
+    const int hi = min(lo + TOK, n_mid);
+    cp_async_wait<0>();  // this head's K data has landed
+    __syncwarp();        // ... for every lane of the token; earlier reads of the buffers are done
+    prefetch_v(h);
+    cp_async_commit();
+    {
+      int hn = h + 1;
+      while (hn < a.H && !has_work(hn)) ++hn;
+      if (hn < a.H) prefetch_k(hn, kb ^ 1);
+      cp_async_commit();
+    }
+    // The lanes of one token are adjacent (TPT divides 32) and share every flag below, so the
+    // warp-wide ballot and the absmax exchange see whole tokens; nothing exits before them.
+    const bool in_range = i < hi;
+    bool keep = in_range;
+    int nv = 0;
+    if (in_range) {
+      if (a.positional) {
+        keep = i >= n_ev;
+        nv = i - n_ev;
+      } else {
+        const uint32_t* bm = a.victims + (size_t)unit * a.victim_words;
+        const uint32_t word = bm[i >> 5];
+        keep = !((word >> (i & 31)) & 1u);
+        nv = i - (hpre[h * CC::PRE + TOK / 32 + 1] + hpre[h * CC::PRE + ((i - lo) >> 5)] +
+                  __popc(word & ((1u << (i & 31)) - 1u)));
       }
     }
-  }
-  if (__ballot_sync(0xffffffffu, moved) == 0u) return;  // warp-uniform
-  f2x X1[8], X2[8];
-  float a1m = 0.f, a2m = 0.f;
-  if (moved) {
-    const float s1 = h2f(mks_s[si * SROW + g1]), s2 = h2f(mks_s[si * SROW + g2]);
-    uint32_t w1[HB / 4], w2[HB / 4];
-#pragma unroll
-    for (int w = 0; w < HB / 4; ++w) {
-      w1[w] = reinterpret_cast<const uint32_t*>(krow_s + g1 * 2 * HB + hf * HB)[w];
-      w2[w] = reinterpret_cast<const uint32_t*>(krow_s + g2 * 2 * HB + hf * HB)[w];
+    const bool moved = keep && nv != i && a.table != nullptr;
+
+    const HeadPtrs P = hptr[h];
+    uint16_t* mks_d = P.ksd;
+    const int di = nv;  // destination slot within the unit
+    uint8_t* krow_d = P.kd + (size_t)di * KROW;
+    const uint8_t* kpf = kbuf + (kb * 256 + threadIdx.x) * CC::KSH;
+    const uint16_t* kspf = reinterpret_cast<const uint16_t*>(ksbuf + (kb * TOK + it) * CC::SRB);
+    kb ^= 1;
+
+    if (keep && !moved) {  // survivor at its own index (or no RoPE): K codes and scales as they are
+      copy_row<HB>(kpf, krow_d + g1 * 2 * HB + hf * HB);
+      copy_row<HB>(kpf + HB, krow_d + g2 * 2 * HB + hf * HB);
+      if (hf == 0) {
+        mks_d[di * SROW + g1] = kspf[g1];
+        mks_d[di * SROW + g2] = kspf[g2];
+      }
     }
-    if constexpr (KB == 4) {
-      dequant16_int4(w1, s1, X1);
-      dequant16_int4(w2, s2, X2);
-    } else {
-      constexpr int per = 32 / KB;
-      constexpr uint32_t msk = (1u << KB) - 1u, flip = 1u << (KB - 1);
-      const float off = 8388608.f + (float)flip;   // 2^23 + 2^(bits-1)
-      const f2x OFF = f2_pack(off, off), S1 = f2_pack(s1, s1), S2 = f2_pack(s2, s2);
-      // dequantise (exact): the offset-binary code sits in the mantissa of 2^23
+    if (__ballot_sync(0xffffffffu, moved) != 0u) {  // warp-uniform
+    f2x X1[8], X2[8];
+    float a1m = 0.f, a2m = 0.f;
+    if (moved) {
+      const float s1 = h2f(kspf[g1]), s2 = h2f(kspf[g2]);
+      uint32_t w1[HB / 4], w2[HB / 4];
+#pragma unroll
+      for (int w = 0; w < HB / 4; ++w) {
+        w1[w] = reinterpret_cast<const uint32_t*>(kpf)[w];
+        w2[w] = reinterpret_cast<const uint32_t*>(kpf + HB)[w];
+      }
+      if constexpr (KB == 4) {
+        dequant16_int4(w1, s1, X1);
+        dequant16_int4(w2, s2, X2);
+      } else {
+        constexpr int per = 32 / KB;
+        constexpr uint32_t msk = (1u << KB) - 1u, flip = 1u << (KB - 1);
+        const float off = 8388608.f + (float)flip;   // 2^23 + 2^(bits-1)
+        const f2x OFF = f2_pack(off, off), S1 = f2_pack(s1, s1), S2 = f2_pack(s2, s2);
+        // dequantise (exact): the offset-binary code sits in the mantissa of 2^23
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int j0 = 2 * k, j1 = 2 * k + 1;
+          const uint32_t c10 = ((w1[j0 / per] >> (KB * (j0 % per))) & msk) ^ flip;
+          const uint32_t c11 = ((w1[j1 / per] >> (KB * (j1 % per))) & msk) ^ flip;
+          const uint32_t c20 = ((w2[j0 / per] >> (KB * (j0 % per))) & msk) ^ flip;
+          const uint32_t c21 = ((w2[j1 / per] >> (KB * (j1 % per))) & msk) ^ flip;
+          X1[k] = f2_mul(f2_sub(f2_pack(__uint_as_float(0x4B000000u | c10),
+                                        __uint_as_float(0x4B000000u | c11)), OFF), S1);
+          X2[k] = f2_mul(f2_sub(f2_pack(__uint_as_float(0x4B000000u | c20),
+                                        __uint_as_float(0x4B000000u | c21)), OFF), S2);
+        }
+      }
+      // un-RoPE at the old index, re-RoPE at the new one, every product and sum rounded
+      // separately: products as packed fp32x2 multiplies (two rotation pairs at once), sums
+      // as scalar IEEE adds (rotate2). Then the cast to fp16.
+      // staged rows of the old and new positions (inside [0, NROWS) whenever staged is set)
+      const int ro = staged ? n_sink + i - rlo : 0, rn = staged ? n_sink + nv - rlo : 0;
+      const float4* to = reinterpret_cast<const float4*>(a.table) +
+                         (size_t)(n_sink + i) * (a.half / 2) + 16 * gp + 8 * hf;
+      const float4* tn = reinterpret_cast<const float4*>(a.table) +
+                         (size_t)(n_sink + nv) * (a.half / 2) + 16 * gp + 8 * hf;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const int j0 = 2 * k, j1 = 2 * k + 1;
-        const uint32_t c10 = ((w1[j0 / per] >> (KB * (j0 % per))) & msk) ^ flip;
-        const uint32_t c11 = ((w1[j1 / per] >> (KB * (j1 % per))) & msk) ^ flip;
-        const uint32_t c20 = ((w2[j0 / per] >> (KB * (j0 % per))) & msk) ^ flip;
-        const uint32_t c21 = ((w2[j1 / per] >> (KB * (j1 % per))) & msk) ^ flip;
-        X1[k] = f2_mul(f2_sub(f2_pack(__uint_as_float(0x4B000000u | c10),
-                                      __uint_as_float(0x4B000000u | c11)), OFF), S1);
-        X2[k] = f2_mul(f2_sub(f2_pack(__uint_as_float(0x4B000000u | c20),
-                                      __uint_as_float(0x4B000000u | c21)), OFF), S2);
+        const int j = 8 * t_ + k;  // = 16 gp + 8 hf + k
+        // (cos, cos, sin, sin) of 2 pairs at the old and at the new position
+        float4 co, cn;
+        if (staged) {
+          co = tab[tab_slot<D>(ro, j)];
+          cn = tab[tab_slot<D>(rn, j)];
+        } else {
+          co = __ldg(to + k);
+          cn = __ldg(tn + k);
+        }
+        rotate2(X1[k], X2[k], f2_pack(co.x, co.y), f2_pack(-co.z, -co.w));
+        rotate2(X1[k], X2[k], f2_pack(cn.x, cn.y), f2_pack(cn.z, cn.w));
+        X1[k] = f2_round_f16(X1[k]);
+        X2[k] = f2_round_f16(X2[k]);
+        float p1[2], p2[2];
+        f2_unpack(X1[k], p1[0], p1[1]);
+        f2_unpack(X2[k], p2[0], p2[1]);
+        a1m = fmaxf(a1m, fmaxf(fabsf(p1[0]), fabsf(p1[1])));
+        a2m = fmaxf(a2m, fmaxf(fabsf(p2[0]), fabsf(p2[1])));
       }
     }
-    // un-RoPE at the old index, re-RoPE at the new one, every product and sum rounded
-    // separately: products as packed fp32x2 multiplies (two rotation pairs at once), sums as
-    // scalar IEEE adds. (A packed sum fed by a packed product may be fused into one rounding
-    // by the assembler; packed products read by scalar sums were bit-identical to the scalar
-    // form on 16.7M probe values.) Then the cast to fp16.
-    const float4* to = reinterpret_cast<const float4*>(a.table) +
-                       (size_t)(n_sink + i) * (a.half / 2) + 16 * gp + 8 * hf;
-    const float4* tn = reinterpret_cast<const float4*>(a.table) +
-                       (size_t)(n_sink + nv) * (a.half / 2) + 16 * gp + 8 * hf;
+    // absmax of each group over the token's two half-threads (adjacent lanes)
+    a1m = fmaxf(a1m, __shfl_xor_sync(0xffffffffu, a1m, 1));
+    a2m = fmaxf(a2m, __shfl_xor_sync(0xffffffffu, a2m, 1));
+    if (moved) {
+    constexpr int qmax = (1 << (KB - 1)) - 1;
+    float s1 = __half2float(__float2half_rn(__fdiv_rn(a1m, (float)qmax)));
+    float s2 = __half2float(__float2half_rn(__fdiv_rn(a2m, (float)qmax)));
+    if (a1m > 0.f && s1 == 0.f) s1 = kSubnormalMin;
+    if (a2m > 0.f && s2 == 0.f) s2 = kSubnormalMin;
+    uint32_t o1[HB / 4], o2[HB / 4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float4 co = __ldg(to + k), cn = __ldg(tn + k);  // (cos, cos, sin, sin) of 2 pairs
-      rotate2(X1[k], X2[k], f2_pack(co.x, co.y), f2_pack(-co.z, -co.w));
-      rotate2(X1[k], X2[k], f2_pack(cn.x, cn.y), f2_pack(cn.z, cn.w));
-      X1[k] = f2_round_f16(X1[k]);
-      X2[k] = f2_round_f16(X2[k]);
-      float p1[2], p2[2];
-      f2_unpack(X1[k], p1[0], p1[1]);
-      f2_unpack(X2[k], p2[0], p2[1]);
-      a1m = fmaxf(a1m, fmaxf(fabsf(p1[0]), fabsf(p1[1])));
-      a2m = fmaxf(a2m, fmaxf(fabsf(p2[0]), fabsf(p2[1])));
+    for (int w = 0; w < HB / 4; ++w) o1[w] = o2[w] = 0u;
+    if (s1 > 0.f) codes_half_group<KB>(X1, s1, o1);
+    if (s2 > 0.f) codes_half_group<KB>(X2, s2, o2);
+#pragma unroll
+    for (int w = 0; w < HB / 4; ++w) {
+      reinterpret_cast<uint32_t*>(krow_d + g1 * 2 * HB + hf * HB)[w] = o1[w];
+      reinterpret_cast<uint32_t*>(krow_d + g2 * 2 * HB + hf * HB)[w] = o2[w];
+    }
+    if (hf == 0) {
+      mks_d[di * SROW + g1] = __half_as_ushort(__float2half_rn(s1));
+      mks_d[di * SROW + g2] = __half_as_ushort(__float2half_rn(s2));
+    }
+    }  // moved
+    }  // some lane of the warp moved
+    // V codes (this thread's share of the row), the V scales and the score of every survivor
+    cp_async_wait<1>();  // this head's V data (the newer group is the next head's K data)
+    __syncwarp();
+    if (keep) {
+      copy_row<VSH>(vbuf + threadIdx.x * CC::VSH, P.vd + (size_t)di * VROW + t_ * VSH);
+      const uint16_t* vspf = reinterpret_cast<const uint16_t*>(vsbuf + it * CC::SRB);
+      if (hf == 0) {
+        P.vsd[di * SROW + g1] = vspf[g1];
+        P.vsd[di * SROW + g2] = vspf[g2];
+      }
+      if (t_ == 0) P.scd[di] = scbuf[it];
     }
   }
-  // absmax of each group over the token's two half-threads (adjacent lanes)
-  a1m = fmaxf(a1m, __shfl_xor_sync(0xffffffffu, a1m, 1));
-  a2m = fmaxf(a2m, __shfl_xor_sync(0xffffffffu, a2m, 1));
-  if (!moved) return;
-  constexpr int qmax = (1 << (KB - 1)) - 1;
-  float s1 = __half2float(__float2half_rn(__fdiv_rn(a1m, (float)qmax)));
-  float s2 = __half2float(__float2half_rn(__fdiv_rn(a2m, (float)qmax)));
-  if (a1m > 0.f && s1 == 0.f) s1 = kSubnormalMin;
-  if (a2m > 0.f && s2 == 0.f) s2 = kSubnormalMin;
-  uint32_t o1[HB / 4], o2[HB / 4];
-#pragma unroll
-  for (int w = 0; w < HB / 4; ++w) o1[w] = o2[w] = 0u;
-  if (s1 > 0.f) codes_half_group<KB>(X1, s1, o1);
-  if (s2 > 0.f) codes_half_group<KB>(X2, s2, o2);
-#pragma unroll
-  for (int w = 0; w < HB / 4; ++w) {
-    reinterpret_cast<uint32_t*>(krow_d + g1 * 2 * HB + hf * HB)[w] = o1[w];
-    reinterpret_cast<uint32_t*>(krow_d + g2 * 2 * HB + hf * HB)[w] = o2[w];
+  cp_async_wait<0>();  // nothing in flight when the CTA exits
+}
+
+// Recent rings after compaction: every ring token's index drops by its unit's n_ev, so its key
+// is re-positioned in place; then the unit's counts are committed (middle count, live buffer).
+// grid = (B), 256 threads: one CTA per batch row loops over the row's KV heads. Thread
+// (token t, t_) owns the same rotation pairs as in the middle tier; the RoPE rows of the ring's
+// old and new positions are staged once for all heads.
+template <int D>
+__global__ void __launch_bounds__(256) evict_recent_commit_kernel(LayerArgs a) {
+  using CC = CompactCfg<D>;
+  constexpr int TPT = CC::TPT, TOK = CC::TOK;
+  extern __shared__ float4 tab[];
+  int* hinfo = reinterpret_cast<int*>(tab + CC::NROWS * CC::ROWF4);  // [H][4]
+  __shared__ int s_rlo, s_rhi;
+  const int b = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // recent rings of this row: every token's index drops by its unit's n_ev; keys rewritten
+  // in place. Thread (token t, t_) owns the same rotation pairs as in the middle tier; the
+  // RoPE rows of the ring's old and new positions are staged once for all heads.
+  if (threadIdx.x == 0) {
+    s_rlo = 0x7fffffff;
+    s_rhi = -1;
   }
-  if (hf == 0) {
-    mks_d[di * SROW + g1] = __half_as_ushort(__float2half_rn(s1));
-    mks_d[di * SROW + g2] = __half_as_ushort(__float2half_rn(s2));
+  __syncthreads();
+  for (int h = warp; h < a.H; h += 8) {
+    const int32_t* m = a.meta + (b * a.H + h) * kF;
+    const int n_mid = m[FADE_META_N_MID];
+    const int n_ev = a.positional ? max(0, n_mid - a.budget) : m[FADE_META_N_EV];
+    const int n_rec = m[FADE_META_N_RECENT];
+    if (lane == 0) {
+      hinfo[4 * h + 0] = n_mid;
+      hinfo[4 * h + 1] = n_ev;
+      hinfo[4 * h + 2] = m[FADE_META_N_SINK];
+      hinfo[4 * h + 3] = n_rec | (m[FADE_META_HEAD] << 16);
+      if (n_ev > 0 && n_rec > 0) {
+        const int p0 = m[FADE_META_N_SINK] + n_mid;  // old position of ring token 0
+        atomicMin(&s_rlo, p0 - n_ev);
+        atomicMax(&s_rhi, p0 + n_rec);
+      }
+    }
+  }
+  __syncthreads();
+  const int rlo = s_rlo, rhi = s_rhi;
+  const bool rotate = rhi >= 0 && a.table != nullptr;  // uniform per CTA
+  const bool staged = rotate && rhi - rlo <= CC::NROWS;
+  if (staged) {
+    const float4* src = reinterpret_cast<const float4*>(a.table) + (size_t)rlo * CC::ROWF4;
+    for (int e = threadIdx.x; e < (rhi - rlo) * CC::ROWF4; e += 256) {
+      const int r = e / CC::ROWF4, j = e % CC::ROWF4;
+      tab[tab_slot<D>(r, j)] = __ldg(src + e);
+    }
+  }
+  __syncthreads();
+  const int tt = threadIdx.x / TPT, t_ = threadIdx.x % TPT;
+  const int gp = t_ >> 1, hf = t_ & 1;
+  for (int h = 0; h < a.H && rotate; ++h) {
+    const int n_mid = hinfo[4 * h + 0], n_ev = hinfo[4 * h + 1];
+    const int n_rec = hinfo[4 * h + 3] & 0xFFFF, head = hinfo[4 * h + 3] >> 16;
+    if (n_ev == 0) continue;
+    const int unit = b * a.H + h;
+    for (int t = tt; t < n_rec; t += TOK) {
+      const int slot = (head + t) % a.W;
+      uint16_t* row = a.rec_k + ((size_t)unit * a.W + slot) * D;
+      const int pold = hinfo[4 * h + 2] + n_mid + t, pnew = pold - n_ev;
+      const float4* to = reinterpret_cast<const float4*>(a.table) + (size_t)pold * (a.half / 2) +
+                         8 * t_;
+      const float4* tn = reinterpret_cast<const float4*>(a.table) + (size_t)pnew * (a.half / 2) +
+                         8 * t_;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {  // 8 channels of the first half and their partners
+        uint16_t* p1 = row + 32 * gp + 16 * hf + 8 * q;
+        uint16_t* p2 = p1 + D / 2;
+        f2x X1[4], X2[4];
+        load_f16x8(p1, X1);
+        load_f16x8(p2, X2);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int j = 8 * t_ + 4 * q + k;
+          float4 co, cn;
+          if (staged) {
+            co = tab[tab_slot<D>(pold - rlo, j)];
+            cn = tab[tab_slot<D>(pnew - rlo, j)];
+          } else {
+            co = __ldg(to + 4 * q + k);
+            cn = __ldg(tn + 4 * q + k);
+          }
+          rotate2(X1[k], X2[k], f2_pack(co.x, co.y), f2_pack(-co.z, -co.w));
+          rotate2(X1[k], X2[k], f2_pack(cn.x, cn.y), f2_pack(cn.z, cn.w));
+        }
+        store_f16x8(X1, p1);
+        store_f16x8(X2, p2);
+      }
+    }
+  }
+  __syncthreads();  // every thread is done with the counts read above
+  for (int h = threadIdx.x; h < a.H; h += 256) {
+    int32_t* m = a.meta + (b * a.H + h) * kF;
+    const int n_ev = a.positional ? max(0, m[FADE_META_N_MID] - a.budget) : m[FADE_META_N_EV];
+    if (n_ev > 0) {
+      m[FADE_META_N_MID] -= n_ev;
+      m[FADE_META_CUR] ^= 1;
+      m[FADE_META_N_EV] = 0;
+    }
   }
 }
 
-__global__ void evict_commit_kernel(int32_t* meta, int units, bool positional, int budget) {
-  const int u = blockIdx.x * blockDim.x + threadIdx.x;
-  if (u >= units) return;
-  int32_t* m = meta + u * kF;
-  const int n_ev = positional ? max(0, m[FADE_META_N_MID] - budget) : m[FADE_META_N_EV];
-  if (n_ev > 0) {
-    m[FADE_META_N_MID] -= n_ev;
-    m[FADE_META_CUR] ^= 1;
-    m[FADE_META_N_EV] = 0;
-  }
-}
 
 // ----------------------------------------------------------------- prefill
 struct PrefillArgs {
@@ -695,10 +971,30 @@ struct DemoteLaunch {
 template <int D, int KB, int VB>
 struct CompactLaunch {
   static fade_status_t run(const LayerArgs& a, int B, int chunks, cudaStream_t st) {
-    evict_compact_kernel<D, KB, VB><<<dim3(chunks + 1, a.H, B), 256, 0, st>>>(a);  // chunks of compact_tok<D>() tokens
+    // chunks of compact_tok<D>() middle indices per batch row
+    const size_t smem = CompactCfg<D>::smem(a.H);
+    auto kern = evict_compact_kernel<D, KB, VB>;
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+      return launch_status("fade_evict_rerope compact shared-memory opt-in");
+    kern<<<dim3(chunks, B), 256, smem, st>>>(a);
     return launch_status("fade_evict_rerope compact");
   }
 };
+
+template <int D>
+fade_status_t launch_recent_commit(const LayerArgs& a, int B, cudaStream_t st) {
+  using CC = CompactCfg<D>;
+  const size_t smem = (size_t)CC::NROWS * CC::ROWF4 * 16 + (size_t)a.H * 4 * 4;
+  auto kern = evict_recent_commit_kernel<D>;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess)
+    return launch_status("fade_evict_rerope recent shared-memory opt-in");
+  kern<<<B, 256, smem, st>>>(a);
+  return launch_status("fade_evict_rerope recent + commit");
+}
 
 template <int D, int KB, int VB>
 struct PlaceLaunch {
@@ -875,10 +1171,9 @@ extern "C" fade_status_t fade_evict_rerope(const fade_config_t* c, fade_layer_t*
   }
   const int ctok = c->head_dim == 128 ? compact_tok<128>() : compact_tok<64>();
   if ((st = dispatch_dkv<CompactLaunch>(c, a, c->batch, ceil_div(max_mid, ctok), s))) return st;
-  const int units = c->batch * c->num_kv_heads;
-  evict_commit_kernel<<<ceil_div(units, 128), 128, 0, s>>>(L->meta, units, a.positional,
-                                                            c->int4_budget);
-  if ((st = launch_status("fade_evict_rerope commit"))) return st;
+  st = c->head_dim == 128 ? launch_recent_commit<128>(a, c->batch, s)
+                          : launch_recent_commit<64>(a, c->batch, s);
+  if (st) return st;
   for (int b = 0; b < c->batch; ++b)
     if (L->h_n_mid[b] > c->int4_budget) L->h_n_mid[b] = c->int4_budget;
   return FADE_OK;
