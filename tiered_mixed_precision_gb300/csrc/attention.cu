@@ -309,16 +309,20 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(AttnArgs a) {
     }
 }
 
-// One CTA of D threads per (row, query head): merge the split partials.
-template <int D>
+// One CTA of D threads per (row, query head): merge the split partials. SK: the splits follow
+// the stream-K schedule of the tensor-core kernel (split 0 + one per unit segment); otherwise
+// split 0 + one per chunk of the middle tier.
+template <int D, bool SK>
 __global__ void __launch_bounds__(D) attn_combine_kernel(AttnArgs a, uint16_t* __restrict__ out,
-                                                         float* __restrict__ ml) {
+                                                         float* __restrict__ ml,
+                                                         const __grid_constant__ StreamK sk) {
   const int bh = blockIdx.x;
   const int b = bh / a.Hq, hq = bh % a.Hq;
   const int G = a.Hq / a.H;
   const int unit = b * a.H + hq / G;
   const int n_mid = a.meta[unit * kF + FADE_META_N_MID];
-  const int ns = min(a.nsplit, 1 + (n_mid + a.chunk - 1) / a.chunk);
+  const int ns = SK ? min(a.nsplit, 1 + sk_segments(sk, b, hq / G))
+                    : min(a.nsplit, 1 + (n_mid + a.chunk - 1) / a.chunk);
   const float* pm = a.part_ml + (size_t)bh * a.nsplit * 2;
   const float* pa = a.part_acc + (size_t)bh * a.nsplit * D;
   float M = -INFINITY;
@@ -469,9 +473,16 @@ extern "C" fade_status_t fade_decode_attention(const fade_config_t* c, const fad
   a.C = mid_stride(c);
   a.NS = a.S + a.C + a.W;
   const bool mma = mid_mma_supported(c);
-  a.chunk = mma ? choose_chunk(max_mid, units, 256, 6LL * 304)
-                : choose_chunk(max_mid, units, kTile, 8LL * 152);
-  a.nsplit = 1 + (max_mid + a.chunk - 1) / a.chunk;
+  StreamK sk{};  // the tensor-core kernel's stream-K schedule (unused by the CUDA-core kernel)
+  if (mma) {
+    build_stream_k(c, L, mid_mma_ctas(c), &sk);
+    a.chunk = kTileTokens;
+    a.nsplit = 1 + sk.smax;
+  } else {
+    sk.P = 0;
+    a.chunk = choose_chunk(max_mid, units, kTile, 8LL * 152);
+    a.nsplit = 1 + (max_mid + a.chunk - 1) / a.chunk;
+  }
   a.scale = 1.0f / sqrtf((float)c->head_dim);
   const size_t need = (size_t)c->batch * c->num_q_heads * a.nsplit * (c->head_dim + 2) * 4;
   if (ws_bytes < need)
@@ -482,17 +493,23 @@ extern "C" fade_status_t fade_decode_attention(const fade_config_t* c, const fad
   cudaStream_t s = as_stream(stream);
   if (mma) {
     // one launch: FP16 tiers (split 0) and the packed middle tier (tensor cores)
-    if ((st = launch_mid_mma(c, L, q_rot, logits_ws, a.part_ml, a.part_acc, a.chunk, a.nsplit,
-                             s)))
+    if ((st = launch_mid_mma(c, L, q_rot, logits_ws, a.part_ml, a.part_acc, sk, a.nsplit, s)))
       return st;
   } else if ((st = launch_split_any(c, a, s, a.nsplit))) {
     return st;
   }
   const int bh = c->batch * c->num_q_heads;
-  if (c->head_dim == 64)
-    attn_combine_kernel<64><<<bh, 64, 0, s>>>(a, out, ml_ws);
-  else
-    attn_combine_kernel<128><<<bh, 128, 0, s>>>(a, out, ml_ws);
+  if (c->head_dim == 64) {
+    if (mma)
+      attn_combine_kernel<64, true><<<bh, 64, 0, s>>>(a, out, ml_ws, sk);
+    else
+      attn_combine_kernel<64, false><<<bh, 64, 0, s>>>(a, out, ml_ws, sk);
+  } else {
+    if (mma)
+      attn_combine_kernel<128, true><<<bh, 128, 0, s>>>(a, out, ml_ws, sk);
+    else
+      attn_combine_kernel<128, false><<<bh, 128, 0, s>>>(a, out, ml_ws, sk);
+  }
   return launch_status("fade_decode_attention combine");
 }
 

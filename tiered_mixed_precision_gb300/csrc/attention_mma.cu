@@ -87,7 +87,9 @@ struct MmaCfg {
   static constexpr int Q_OFF = VS_OFF + kTileTok * SROW * 2;
   // per-item merge of the consumer warps' partials: m, l [8][8], acc [8][8][D], weights [8][8]
   static constexpr int MERGE_OFF = NSTAGE * STAGE;
-  static constexpr int MERGE_BYTES = (64 + 64 + 8 * 8 * D / 2 + 64) * 4;
+  // (acc rows padded by one float: the fragment-layout writes then hit 16 banks, not 4)
+  static constexpr int WO_ROW = D + 1;
+  static constexpr int MERGE_BYTES = (64 + 64 + 32 * WO_ROW + 64) * 4;
   static constexpr int INFO_OFF = MERGE_OFF + MERGE_BYTES;  // per stage: kInfo ints
   static constexpr int BAR_OFF = INFO_OFF + NSTAGE * 8 * 4;
   static constexpr int SMEM = BAR_OFF + 2 * NSTAGE * 8 + 1024;  // + alignment slack
@@ -267,6 +269,10 @@ __device__ __forceinline__ void load_f16_lane(const uint16_t* p, float (&f)[CPL]
   }
 }
 
+// CPL consecutive fp16 values from shared memory (32-bit shared address) as fp32.
+template <int CPL>
+__device__ __forceinline__ void lds_f16_lane(uint32_t addr, float (&f)[CPL]);
+
 // v[i] for a runtime index i < N, without indexing a register array dynamically.
 template <int N>
 __device__ __forceinline__ float pick(const float (&v)[N], int i) {
@@ -293,10 +299,34 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
   return v;
 }
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
+}
+template <int CPL>
+__device__ __forceinline__ void lds_f16_lane(uint32_t addr, float (&f)[CPL]) {
+  if constexpr (CPL == 4) {
+    const uint2 u = lds64(addr);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    f[0] = a.x;
+    f[1] = a.y;
+    f[2] = b.x;
+    f[3] = b.y;
+  } else {
+    const uint32_t u = lds32(addr);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u));
+    f[0] = a.x;
+    f[1] = a.y;
+  }
 }
 __device__ __forceinline__ float h_lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu))); }
 __device__ __forceinline__ float h_hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
@@ -526,6 +556,41 @@ __device__ __forceinline__ void consume_tile(
   }
 }
 
+// Position of a global middle tile in the schedule: row b, KV head h, tile within the unit.
+struct SkPos {
+  int b, h, tile;
+};
+__device__ __forceinline__ SkPos sk_locate(const StreamK& k, int g) {
+  int base = 0;
+  for (int b = 0; b < k.B; ++b) {
+    const int rt = k.row_tiles[b], n = k.H * rt;
+    if (g < base + n) return SkPos{b, (g - base) / rt, (g - base) % rt};
+    base += n;
+  }
+  return SkPos{k.B, 0, 0};
+}
+// Move `run` tiles forward, where the run ends at or before the end of the current unit.
+__device__ __forceinline__ void sk_advance(const StreamK& k, SkPos& p, int run) {
+  p.tile += run;
+  if (p.tile < k.row_tiles[p.b]) return;
+  p.tile = 0;
+  if (++p.h < k.H) return;
+  p.h = 0;
+  ++p.b;
+  while (p.b < k.B && k.row_tiles[p.b] == 0) ++p.b;
+}
+// Segments (maximal runs inside one unit) among n tiles starting at p.
+__device__ __forceinline__ int sk_count_segments(const StreamK& k, SkPos p, int n) {
+  int count = 0;
+  while (n > 0) {
+    const int run = min(n, (int)k.row_tiles[p.b] - p.tile);
+    ++count;
+    n -= run;
+    sk_advance(k, p, run);
+  }
+  return count;
+}
+
 // Bounded wait that also gives up as soon as another warp of the CTA has raised `abort`.
 __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, int32_t* status,
                                                    int code, volatile int* abort) {
@@ -543,20 +608,21 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity
   return true;
 }
 
-// Persistent decode attention: CTA c takes the work items c, c + gridDim.x, ... of the list
-// (split, unit) = (item / units, item % units), where split 0 is a unit's FP16 tiers and split
-// s >= 1 its middle tokens [(s-1)*chunk, s*chunk). Every item occupies one or more stages of the
-// ring: the producer warp copies each stage's code and scale rows (TMA) and, with the item's
-// first stage, the item's query rows (bulk copy); it writes what the stage holds into the stage
-// info before arming it. The producer therefore runs ahead across item boundaries and the
-// consumers never wait on global memory for metadata or queries. Consumer warps merge their
-// partials in shared memory at the end of each item (named barrier 1, consumers only) and
-// write the item's split partial.
+// Persistent decode attention under a stream-K schedule: CTA c first takes the FP16-tier items
+// of units c, c + P, ... (split 0), then its contiguous run of middle tiles [cta_start[c],
+// cta_start[c+1]) in global tile order, which may cross unit boundaries: every maximal run
+// inside one unit is a segment whose partial goes to split 1 + k (k = the CTA's rank among the
+// CTAs touching that unit). Every item occupies one or more stages of the ring: the producer
+// warp copies each stage's code and scale rows (TMA) and, with the item's first stage, the
+// item's query rows (bulk copy); it writes what the stage holds into the stage info before
+// arming it. The producer therefore runs ahead across item boundaries and the consumers never
+// wait on global memory for metadata or queries. Consumer warps merge their partials in shared
+// memory at the end of each item (named barrier 1, consumers only) and write its partial.
 template <int D, int G>
 __global__ void __launch_bounds__(MmaShape<D, G>::THREADS, MmaShape<D, G>::MINB)
 attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_constant__ CUtensorMap tk1,
                     const __grid_constant__ CUtensorMap tv0, const __grid_constant__ CUtensorMap tv1,
-                    MmaArgs a) {
+                    MmaArgs a, const __grid_constant__ StreamK sk) {
   using Cfg = MmaCfg<D>;
   constexpr int kConsumers = MmaShape<D, G>::CONS;
   constexpr int NT = (2 * G + 7) / 8;    // 8-column n-tiles of (head, group parity)
@@ -573,13 +639,20 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
   float* wm = reinterpret_cast<float*>(smem + Cfg::MERGE_OFF);  // [kConsumers][8]
   float* wl = wm + 64;                                          // [kConsumers][8]
   float* wf = wl + 64;                                          // [G][kConsumers]
-  float* wo = wf + 64;                                          // [kConsumers][G][D]
+  float* wo = wf + 64;                                  // [kConsumers][G][WO_ROW]
+  constexpr int WR = Cfg::WO_ROW;
   __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int units = a.B * a.H;
-  const int n_items = units * a.nsplit;
+  const bool f16_staged = (a.S + a.W) * D * 2 <= Cfg::Q_OFF;  // FP16 tiers through the ring
+  // this CTA's work: FP16 items of units c, c + P, ..., then middle tiles [g0, g1)
+  const int cta = blockIdx.x, P = gridDim.x;
+  const int n16 = cta < units ? (units - cta + P - 1) / P : 0;
+  const int g0 = sk.cta_start[cta], g1 = sk.cta_start[cta + 1];
+  const SkPos p0 = sk_locate(sk, g0);
+  const int nseg = sk_count_segments(sk, p0, g1 - g0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
@@ -596,52 +669,52 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int issued = 0;
-      for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
-        const int split = item / units, unit = item % units;
+      // one item: n_stage stages of unit `unit`; middle tiles tile0 .. tile0 + n_stage - 1
+      auto issue_item = [&](int unit, int split, int tile0, int n_stage) {
         const int b = unit / a.H, hk = unit % a.H;
         const int32_t* m = a.meta + unit * kF;
         const int n_mid = m[FADE_META_N_MID], cur = m[FADE_META_CUR];
-        const int lo = split > 0 ? (split - 1) * a.chunk : 0;
-        const int hi = split > 0 ? min(n_mid, lo + a.chunk) : 0;
-        const int n_tok = max(0, hi - lo);
-        const int n_stage = max(1, (n_tok + kTileTok - 1) / kTileTok);  // q rides the first
         const CUtensorMap* mk = cur ? &tk1 : &tk0;
         const CUtensorMap* mv = cur ? &tv1 : &tv0;
         const uint16_t* ksg = cur ? a.ks[1] : a.ks[0];
         const uint16_t* vsg = cur ? a.vs[1] : a.vs[0];
-        const size_t row0 = (size_t)unit * a.C + lo;
         for (int it = 0; it < n_stage; ++it) {
           const int s = issued % NSTAGE;
           if (issued >= NSTAGE &&
               !mbar_wait_or_abort(bar_empty + 8 * s, ((issued / NSTAGE) & 1) ^ 1, a.status, 2,
                                   abort))
-            break;
-          const int nt = min(kTileTok, n_tok - it * kTileTok);  // may be <= 0 (q only)
+            return false;
+          const int tile = tile0 + it;
+          const int nt = split > 0 ? min(kTileTok, n_mid - tile * kTileTok) : 0;  // <= 0: q only
           int* inf = info + s * kInfo;
           inf[kInfoUnit] = unit;
           inf[kInfoSplit] = split;
           inf[kInfoNt] = max(nt, 0);
           inf[kInfoLast] = it == n_stage - 1;
-          inf[kInfoTok0] = lo + it * kTileTok;
+          inf[kInfoTok0] = tile * kTileTok;
           inf[kInfoSink] = m[FADE_META_N_SINK];
           inf[kInfoRec] = m[FADE_META_N_RECENT];
           inf[kInfoHead] = m[FADE_META_HEAD];
           const uint32_t stage = sbase + s * Cfg::STAGE;
+          // scale rows copied: rounded up so the copy is a multiple of 16 bytes (it stays inside
+          // the unit: rows start at multiples of 4 and the slot stride is a multiple of 64)
+          constexpr int kAlign = 16 / (Cfg::SROW * 2);
+          const int ns = (max(nt, 0) + kAlign - 1) / kAlign * kAlign;
           uint32_t bytes = 0;
-          if (nt > 0) {
-            // scale rows copied: rounded up so the copy is a multiple of 16 bytes (it stays
-            // inside the unit: rows start at multiples of 4 and the slot stride is a multiple
-            // of 64)
-            constexpr int kAlign = 16 / (Cfg::SROW * 2);
-            const int ns = (nt + kAlign - 1) / kAlign * kAlign;
-            bytes += kTileTok * (Cfg::KROW + Cfg::VROW) + 2u * ns * Cfg::SROW * 2;
-          }
+          if (nt > 0) bytes += kTileTok * (Cfg::KROW + Cfg::VROW) + 2u * ns * Cfg::SROW * 2;
           if (it == 0) bytes += G * D * 2;
+          if (split == 0 && f16_staged) bytes += (a.S + a.W) * D * 2;
           mbar_expect_tx(bar_full + 8 * s, bytes);
+          if (split == 0 && f16_staged) {  // sinks then the whole ring, K (first) or V rows
+            const uint16_t* sink = it == 0 ? a.sink_k : a.sink_v;
+            const uint16_t* ring = it == 0 ? a.rec_k : a.rec_v;
+            if (a.S > 0)
+              bulk_load_1d(stage, sink + (size_t)unit * a.S * D, a.S * D * 2, bar_full + 8 * s);
+            bulk_load_1d(stage + a.S * D * 2, ring + (size_t)unit * a.W * D, a.W * D * 2,
+                         bar_full + 8 * s);
+          }
           if (nt > 0) {
-            constexpr int kAlign = 16 / (Cfg::SROW * 2);
-            const int ns = (nt + kAlign - 1) / kAlign * kAlign;
-            const size_t r = row0 + (size_t)it * kTileTok;
+            const size_t r = (size_t)unit * a.C + (size_t)tile * kTileTok;
             tma_load_2d(stage + Cfg::K_OFF, mk, 0, (int)r, bar_full + 8 * s);
             tma_load_2d(stage + Cfg::V_OFF, mv, 0, (int)r, bar_full + 8 * s);
             bulk_load_1d(stage + Cfg::KS_OFF, ksg + r * Cfg::SROW, ns * Cfg::SROW * 2,
@@ -654,6 +727,19 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
                          bar_full + 8 * s);
           ++issued;
         }
+        return true;
+      };
+      bool go = true;
+      for (int u = cta; u < units && go; u += P) go = issue_item(u, 0, 0, f16_staged ? 2 : 1);
+      SkPos pos = p0;
+      for (int g = g0; g < g1 && go;) {
+        const int rt = sk.row_tiles[pos.b];
+        const int run = min(g1 - g, rt - pos.tile);
+        // this CTA's rank among the CTAs holding tiles of the unit
+        const int k = sk_nonempty(sk, sk_cta_of(sk, g - pos.tile), cta - 1);
+        go = issue_item(pos.b * a.H + pos.h, 1 + k, pos.tile, run);
+        g += run;
+        sk_advance(sk, pos, run);
       }
       // never leave the CTA with copies in flight: wait (bounded) for the last issued stages
       for (int k = max(0, issued - NSTAGE); k < issued; ++k)
@@ -669,12 +755,15 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
   const LaneOffsets<D> lo_ = lane_offsets<D>(wr0, lane);
   const bool want_logits = a.logits != nullptr;
   int used = 0;  // stages consumed so far (the producer's `issued` sequence)
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+  // the same number of items in every consumer warp (and so the same barriers), whatever waits
+  // may fail: the count comes from the schedule, the rest from the stage info
+  for (int item = 0; item < n16 + nseg; ++item) {
     int s_ = used % NSTAGE;
     bool ok = !*abort && mbar_wait_or_abort(bar_full + 8 * s_, (used / NSTAGE) & 1, a.status, 1,
                                             abort);
     const int* inf = info + s_ * kInfo;
-    const int unit = item % units, split = item / units;
+    const int unit = ok ? inf[kInfoUnit] : 0, split = ok ? inf[kInfoSplit] : 0;
+    const bool write_ok = ok;
     const int b = unit / a.H, hk = unit % a.H, hq0 = hk * G;
     const uint16_t* qs = reinterpret_cast<const uint16_t*>(smem + s_ * Cfg::STAGE + Cfg::Q_OFF);
     float m2[NT], lsum[NT];
@@ -710,10 +799,22 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
       }
       const int n_sink = ok ? inf[kInfoSink] : 0, n_rec = ok ? inf[kInfoRec] : 0;
       const int head_slot = ok ? inf[kInfoHead] : 0;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + 8 * s_);  // q is in registers: release the stage
-      ++used;
-      const int n_tok = n_sink + n_rec;
+      const uint32_t st_k = sbase + s_ * Cfg::STAGE;  // K rows (staged case)
+      uint32_t st_v = 0;
+      int s_v = 0;
+      bool ok_v = false;
+      if (f16_staged) {  // the V rows arrive in the item's second stage
+        s_v = (used + 1) % NSTAGE;
+        ok_v = ok && !*abort &&
+               mbar_wait_or_abort(bar_full + 8 * s_v, ((used + 1) / NSTAGE) & 1, a.status, 1,
+                                  abort);
+        st_v = sbase + s_v * Cfg::STAGE;
+      } else {
+        __syncwarp();
+        if (lane == 0 && ok) mbar_arrive(bar_empty + 8 * s_);  // q is in registers
+        ++used;
+      }
+      const int n_tok = (!f16_staged || ok_v) ? n_sink + n_rec : 0;
       // two tokens per pass (u and u + kConsumers): both rows are loaded before either is used
       for (int u0 = warp; u0 < n_tok; u0 += 2 * kConsumers) {
         float kv[2][CPL], vv[2][CPL];
@@ -723,10 +824,16 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
           const int u = min(u0 + e * kConsumers, n_tok - 1);  // a duplicate is masked below
           const bool is_sink = u < n_sink;
           const int slot = is_sink ? u : (head_slot + u - n_sink) % a.W;
-          const size_t row =
-              is_sink ? ((size_t)unit * a.S + u) * D : ((size_t)unit * a.W + slot) * D;
-          load_f16_lane<CPL>((is_sink ? a.sink_k : a.rec_k) + row + lane * CPL, kv[e]);
-          load_f16_lane<CPL>((is_sink ? a.sink_v : a.rec_v) + row + lane * CPL, vv[e]);
+          if (f16_staged) {
+            const uint32_t off = (is_sink ? u : a.S + slot) * D * 2 + lane * CPL * 2;
+            lds_f16_lane<CPL>(st_k + off, kv[e]);
+            lds_f16_lane<CPL>(st_v + off, vv[e]);
+          } else {
+            const size_t row =
+                is_sink ? ((size_t)unit * a.S + u) * D : ((size_t)unit * a.W + slot) * D;
+            load_f16_lane<CPL>((is_sink ? a.sink_k : a.rec_k) + row + lane * CPL, kv[e]);
+            load_f16_lane<CPL>((is_sink ? a.sink_v : a.rec_v) + row + lane * CPL, vv[e]);
+          }
           lidx[e] = is_sink ? u : a.S + a.C + slot;
         }
 #pragma unroll
@@ -756,6 +863,14 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
           }
         }
       }
+      if (f16_staged) {  // both stages of the item are read: release them
+        __syncwarp();
+        if (lane == 0) {
+          if (ok) mbar_arrive(bar_empty + 8 * s_);
+          if (ok_v) mbar_arrive(bar_empty + 8 * s_v);
+        }
+        used += 2;
+      }
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         if (lane == 0) {
@@ -763,35 +878,32 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
           wl[warp * 8 + h] = ll[h];
         }
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) wo[(warp * G + h) * D + lane * CPL + c] = acc[h][c];
+        for (int c = 0; c < CPL; ++c) wo[(warp * G + h) * WR + lane * CPL + c] = acc[h][c];
       }
     } else {
       // ---------------------------------------------------------- packed middle tier (MMA)
       // query B operand: column n of n-tile j = (head 4j + n/2, parity n%2); thread (g, t)
       // holds column g, k-slots {2t, 2t+1} (group 2s of half s) and {2t+8, 2t+9} (group 2s+1)
+      // one 16-byte load gives channels 8t .. 8t+7 of the lane's group; byte permutes pair
+      // them as (c, c+4) for the four k-steps
       uint32_t qb[NHALF][4][NT][2];
+      const uint32_t qs_addr = sbase + s_ * Cfg::STAGE + Cfg::Q_OFF;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         const int h = 4 * j + g / 2, par = g & 1;
         const bool valid = ok && h < G;
 #pragma unroll
-        for (int s = 0; s < NHALF; ++s)
+        for (int s = 0; s < NHALF; ++s) {
+          const uint4 v = valid ? lds128(qs_addr + (h * D + 64 * s + 32 * par + 8 * t) * 2)
+                                : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t pk[4] = {prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u),
+                                  prmt(v.y, v.w, 0x5410u), prmt(v.y, v.w, 0x7632u)};
 #pragma unroll
           for (int kp = 0; kp < 4; ++kp) {
-            const int c_lo = 64 * s + 8 * t + kp;        // group 2s
-            const int c_hi = c_lo + 32;                  // group 2s+1
-            uint16_t v0 = 0, v1 = 0, v2 = 0, v3 = 0;
-            if (valid && par == 0) {
-              v0 = qs[h * D + c_lo];
-              v1 = qs[h * D + c_lo + 4];
-            }
-            if (valid && par == 1) {
-              v2 = qs[h * D + c_hi];
-              v3 = qs[h * D + c_hi + 4];
-            }
-            qb[s][kp][j][0] = uint32_t(v0) | (uint32_t(v1) << 16);
-            qb[s][kp][j][1] = uint32_t(v2) | (uint32_t(v3) << 16);
+            qb[s][kp][j][0] = par == 0 ? pk[kp] : 0u;   // group 2s
+            qb[s][kp][j][1] = par == 1 ? pk[kp] : 0u;   // group 2s+1
           }
+        }
       }
       float* logit_base =
           want_logits ? a.logits + (size_t)(b * a.Hq + hq0) * a.NS + a.S : nullptr;
@@ -847,8 +959,8 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
 #pragma unroll
             for (int mm = 0; mm < 4; ++mm) {
               const int c = 64 * s + 8 * g + 2 * mm;
-              wo[(warp * G + h) * D + c] = gsel ? o[s][mm][j][1] : o[s][mm][j][0];
-              wo[(warp * G + h) * D + c + 1] = gsel ? o[s][mm][j][3] : o[s][mm][j][2];
+              wo[(warp * G + h) * WR + c] = gsel ? o[s][mm][j][1] : o[s][mm][j][0];
+              wo[(warp * G + h) * WR + c + 1] = gsel ? o[s][mm][j][3] : o[s][mm][j][2];
             }
         }
       }
@@ -856,20 +968,25 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
     // ------------------------------------------------------------ merge the consumer warps
     consumer_bar<kConsumers>();
     const size_t pbase = ((size_t)(b * a.Hq + hq0)) * a.nsplit + split;
-    if (threadIdx.x < G) {
-      const int h = threadIdx.x;
-      float M = -INFINITY;
+    if (warp == 0) {
+      // lane (h, w) = (lane / kConsumers, lane % kConsumers): head h's max over the warps, the
+      // weight 2^(m_w - M) of warp w, and the weighted mass, reduced across the w lanes
+      static_assert(G * kConsumers <= 32, "one lane per (head, warp)");
+      const int h = lane / kConsumers, w = lane % kConsumers;
+      const bool act = lane < G * kConsumers;
+      const float mw = act ? wm[w * 8 + h] : -INFINITY;
+      float M = mw;
 #pragma unroll
-      for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, wm[w * 8 + h]);
-      float L = 0.f;
+      for (int o = kConsumers / 2; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+      float L = act ? wl[w * 8 + h] * f : 0.f;
 #pragma unroll
-      for (int w = 0; w < kConsumers; ++w) {
-        const float f = (wm[w * 8 + h] == -INFINITY) ? 0.f : ex2(wm[w * 8 + h] - M);
-        wf[h * kConsumers + w] = f;
-        L = fmaf(wl[w * 8 + h], f, L);
+      for (int o = kConsumers / 2; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      if (act) wf[h * kConsumers + w] = f;
+      if (act && w == 0 && write_ok) {
+        a.part_ml[(pbase + (size_t)h * a.nsplit) * 2] = M * kLn2;  // natural-log units
+        a.part_ml[(pbase + (size_t)h * a.nsplit) * 2 + 1] = L;
       }
-      a.part_ml[(pbase + (size_t)h * a.nsplit) * 2] = M * kLn2;  // natural-log units
-      a.part_ml[(pbase + (size_t)h * a.nsplit) * 2 + 1] = L;
     }
     consumer_bar<kConsumers>();
     for (int i = threadIdx.x; i < G * D; i += kConsumers * 32) {
@@ -877,8 +994,8 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
       float O = 0.f;
 #pragma unroll
       for (int w = 0; w < kConsumers; ++w)
-        O = fmaf(wo[(w * G + h) * D + c], wf[h * kConsumers + w], O);
-      a.part_acc[(pbase + (size_t)h * a.nsplit) * D + c] = O;
+        O = fmaf(wo[(w * G + h) * WR + c], wf[h * kConsumers + w], O);
+      if (write_ok) a.part_acc[(pbase + (size_t)h * a.nsplit) * D + c] = O;
     }
     consumer_bar<kConsumers>();  // the merge area is rewritten by the next item
   }
@@ -926,7 +1043,7 @@ fade_status_t encode_rows(CUtensorMap* m, const void* base, unsigned long long r
 
 template <int D, int G>
 fade_status_t launch_mma(const fade_config_t* c, const fade_layer_t* L, const MmaArgs& a,
-                         int n_splits, cudaStream_t st) {
+                         const StreamK& sk, cudaStream_t st) {
   using Cfg = MmaCfg<D>;
   const unsigned long long rows = (unsigned long long)c->batch * c->num_kv_heads * a.C;
   CUtensorMap tk[2], tv[2];
@@ -939,14 +1056,8 @@ fade_status_t launch_mma(const fade_config_t* c, const fade_layer_t* L, const Mm
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
       cudaSuccess)
     return launch_status("fade_decode_attention (middle tier) shared-memory opt-in");
-  // persistent grid: as many CTAs as fit on the device at once (never more than the items)
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return launch_status("fade_decode_attention (middle tier) device query");
-  const long long items = (long long)c->batch * c->num_kv_heads * n_splits;
-  const int grid = (int)std::min<long long>(items, (long long)sms * MmaShape<D, G>::MINB);
-  kern<<<grid, MmaShape<D, G>::THREADS, Cfg::SMEM, st>>>(tk[0], tk[1], tv[0], tv[1], a);
+  // persistent grid: the schedule's CTAs (as many as fit on the device at once)
+  kern<<<sk.P, MmaShape<D, G>::THREADS, Cfg::SMEM, st>>>(tk[0], tk[1], tv[0], tv[1], a, sk);
   return launch_status("fade_decode_attention (middle tier)");
 }
 
@@ -956,8 +1067,50 @@ bool mid_mma_supported(const fade_config_t* c) {
   return c->middle_k_bits == 4 && c->middle_v_bits == 2;
 }
 
+int mid_mma_ctas(const fade_config_t* c) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 1;
+  const int G = c->num_q_heads / c->num_kv_heads;
+  const int minb = (FADE_MMA_WIDE && G <= 4) ? 2 : 1;  // MmaShape<D, G>::MINB
+  return std::max(1, std::min(kMaxCtaSK, sms * minb));
+}
+
+void build_stream_k(const fade_config_t* c, const fade_layer_t* L, int ctas, StreamK* k) {
+  k->P = ctas;
+  k->B = c->batch;
+  k->H = c->num_kv_heads;
+  long long T = 0;
+  for (int b = 0; b < c->batch; ++b) {
+    const int rt = (L->h_n_mid[b] + kTileTok - 1) / kTileTok;
+    k->row_tiles[b] = (uint16_t)rt;
+    T += (long long)k->H * rt;
+  }
+  for (int b = c->batch; b < FADE_MAX_BATCH; ++b) k->row_tiles[b] = 0;
+  // an FP16-tier item (sinks + recent window on the CUDA cores) costs about kFp16Weight tiles
+  constexpr long long kFp16Weight = 3;
+  const long long F = (long long)c->batch * c->num_kv_heads, P = ctas;
+  const long long Wtot = T + kFp16Weight * F;
+  long long f16_before = 0, prev = 0;
+  k->cta_start[0] = 0;
+  for (long long cc = 1; cc <= P; ++cc) {
+    const long long n16 = (cc - 1) < F ? (F - (cc - 1) + P - 1) / P : 0;
+    f16_before += n16;
+    long long v = cc * Wtot / P - kFp16Weight * f16_before;
+    v = std::max(prev, std::min(T, v));
+    k->cta_start[cc] = (int)v;
+    prev = v;
+  }
+  k->cta_start[P] = (int)T;
+  int smax = 0;
+  for (int b = 0; b < c->batch; ++b)
+    for (int h = 0; h < k->H; ++h) smax = std::max(smax, sk_segments(*k, b, h));
+  k->smax = smax;
+}
+
 fade_status_t launch_mid_mma(const fade_config_t* c, const fade_layer_t* L, const uint16_t* q,
-                             float* logits, float* part_ml, float* part_acc, int chunk,
+                             float* logits, float* part_ml, float* part_acc, const StreamK& sk,
                              int nsplit, cudaStream_t st) {
   MmaArgs a;
   a.q = q;
@@ -981,12 +1134,12 @@ fade_status_t launch_mid_mma(const fade_config_t* c, const fade_layer_t* L, cons
   a.S = c->n_sink;
   a.C = mid_stride(c);
   a.NS = c->n_sink + a.C + c->recent_window;
-  a.chunk = chunk;
+  a.chunk = kTileTok;
   a.nsplit = nsplit;
   a.inv_sqrt_d = 1.0f / sqrtf((float)c->head_dim);
   const int G = c->num_q_heads / c->num_kv_heads;
 #define FADE_CASE(D_, G_) \
-  if (c->head_dim == D_ && G == G_) return launch_mma<D_, G_>(c, L, a, nsplit, st);
+  if (c->head_dim == D_ && G == G_) return launch_mma<D_, G_>(c, L, a, sk, st);
   FADE_CASE(64, 1) FADE_CASE(64, 2) FADE_CASE(64, 4) FADE_CASE(64, 8)
   FADE_CASE(128, 1) FADE_CASE(128, 2) FADE_CASE(128, 4) FADE_CASE(128, 8)
 #undef FADE_CASE

@@ -385,27 +385,14 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// One unit's middle-tier rows for compaction: source (live) and destination buffers, each at
-// the unit's slot 0.
-struct HeadPtrs {
-  const uint8_t* ks;
-  uint8_t* kd;
-  const uint8_t* vs;
-  uint8_t* vd;
-  const uint16_t* kss;
-  uint16_t* ksd;
-  const uint16_t* vss;
-  uint16_t* vsd;
-  const float* scs;
-  float* scd;
-};
-
 template <int D>
 struct CompactCfg {
   static constexpr int TPT = D / 32;        // threads per middle token
   static constexpr int TOK = 256 / TPT;     // middle indices per CTA
   static constexpr int ROWF4 = D / 4;       // float4 per RoPE row: d/2 pairs x (cos, sin)
   static constexpr int NROWS = TOK + 32;    // staged RoPE rows (blocks with n_ev <= 32)
+  static constexpr int TPW = 32 / TPT;      // tokens per warp
+  static constexpr int TABF4 = NROWS * (ROWF4 + 1);  // staged rows padded by one float4
   static constexpr int PRE = TOK / 32 + 2;  // per-head ints: victim prefix words + base
   // prefetch buffers: per thread its K code share (two buffers) and V code share (one); per
   // token its K scale row (two buffers), V scale row and score (one)
@@ -413,21 +400,19 @@ struct CompactCfg {
   static constexpr int VSH = 16;                 // bytes of V codes per thread (INT4 worst case)
   static constexpr int SRB = D / 32 * 2;         // bytes of one scale row
   static constexpr int PF_BYTES = 2 * 256 * KSH + 256 * VSH + TOK * (3 * SRB + 4);
-  // staged rows, prefetch buffers, then per head: row pointers, 4 counts, the victim prefixes
+  // staged rows, prefetch buffers, then per head: 4 counts and the victim prefixes
   static size_t smem(int H) {
-    return (size_t)NROWS * ROWF4 * 16 + PF_BYTES +
-           (size_t)H * (sizeof(HeadPtrs) + (PRE + 4) * 4);
+    return (size_t)TABF4 * 16 + PF_BYTES +
+           (size_t)H * (PRE + 4) * 4;
   }
 };
 
-// Swizzled float4 slot of (row, j) in the staged table: the 8 threads of a quarter warp (two or
-// four consecutive tokens, each reading float4 j = 8*t_ + k) land in 8 different bank quads.
+// Float4 slot of (row, j) in the staged table: rows padded by one float4, so the eight
+// threads of a quarter warp (eight consecutive tokens with the same t_, reading the same j of
+// eight consecutive rows) hit eight different bank quads.
 template <int D>
 __device__ __forceinline__ int tab_slot(int row, int j) {
-  if constexpr (D == 128)
-    return row * 32 + (j ^ (((j >> 3) & 3) | ((row & 1) << 2)));
-  else
-    return row * 16 + (j ^ (((j >> 3) & 1) | ((row & 3) << 1)));
+  return row * (D / 4 + 1) + j;
 }
 
 template <int D>
@@ -455,14 +440,13 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kern
   constexpr int HB = 16 * KB / 8;        // bytes of half a group's K codes
   constexpr int VROW = D * VB / 8, SROW = D / kGroup, KROW = D * KB / 8;
   extern __shared__ float4 tab[];        // [NROWS][ROWF4] swizzled, then the buffers below
-  uint8_t* pf = reinterpret_cast<uint8_t*>(tab + CC::NROWS * CC::ROWF4);
+  uint8_t* pf = reinterpret_cast<uint8_t*>(tab + CC::TABF4);
   uint8_t* kbuf = pf;                                   // [2][256][KSH]
   uint8_t* vbuf = kbuf + 2 * 256 * CC::KSH;             // [256][VSH]
   uint8_t* ksbuf = vbuf + 256 * CC::VSH;                // [2][TOK][SRB]
   uint8_t* vsbuf = ksbuf + 2 * TOK * CC::SRB;           // [TOK][SRB]
   float* scbuf = reinterpret_cast<float*>(vsbuf + TOK * CC::SRB);  // [TOK]
-  HeadPtrs* hptr = reinterpret_cast<HeadPtrs*>(pf + CC::PF_BYTES);  // [H]
-  int* hinfo = reinterpret_cast<int*>(hptr + a.H);  // [H][4]: n_mid n_ev n_sink cur
+  int* hinfo = reinterpret_cast<int*>(pf + CC::PF_BYTES);  // [H][4]: n_mid n_ev n_sink cur
   int* hpre = hinfo + a.H * 4;                       // [H][PRE]
   __shared__ int s_rlo, s_rhi;
   const int b = blockIdx.y;
@@ -488,19 +472,6 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kern
       hinfo[4 * h + 1] = n_ev;
       hinfo[4 * h + 2] = n_sink;
       hinfo[4 * h + 3] = cur;
-      const size_t u0 = (size_t)unit * a.C;  // the unit's slot 0
-      HeadPtrs P;  // (selects, not a runtime index into the parameter arrays)
-      P.ks = (cur ? a.mk[1] : a.mk[0]) + u0 * KROW;
-      P.kd = (cur ? a.mk[0] : a.mk[1]) + u0 * KROW;
-      P.vs = (cur ? a.mv[1] : a.mv[0]) + u0 * VROW;
-      P.vd = (cur ? a.mv[0] : a.mv[1]) + u0 * VROW;
-      P.kss = (cur ? a.mks[1] : a.mks[0]) + u0 * SROW;
-      P.ksd = (cur ? a.mks[0] : a.mks[1]) + u0 * SROW;
-      P.vss = (cur ? a.mvs[1] : a.mvs[0]) + u0 * SROW;
-      P.vsd = (cur ? a.mvs[0] : a.mvs[1]) + u0 * SROW;
-      P.scs = (cur ? a.mid_sc[1] : a.mid_sc[0]) + u0;
-      P.scd = (cur ? a.mid_sc[0] : a.mid_sc[1]) + u0;
-      hptr[h] = P;
     }
     if (n_ev == 0 || lo >= n_mid) continue;
     const int hi = min(lo + TOK, n_mid);
@@ -542,7 +513,10 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kern
   }
   __syncthreads();
 
-  const int it = threadIdx.x / TPT, t_ = threadIdx.x % TPT;
+  // lanes: token-minor (eight or sixteen consecutive tokens per t_), so a quarter warp reads
+  // one j of consecutive RoPE rows; the partner half-group thread is lane ^ TPW
+  const int tid = threadIdx.x;
+  const int it = warp * CC::TPW + lane % CC::TPW, t_ = lane / CC::TPW;
   const int gp = t_ >> 1, hf = t_ & 1;
   const int i = lo + it;
   const int g1 = gp, g2 = gp + D / 64;
@@ -550,22 +524,28 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kern
   // K codes and scales of a head's token for this thread, and its V share, score and V scales,
   // fetched ahead with cp.async (K one processed head ahead, V during the head itself)
   auto has_work = [&](int hh) { return hinfo[4 * hh + 1] != 0 && lo < hinfo[4 * hh + 0]; };
+  // a unit's row `slot` in its live (src) or other (dst) buffer; the buffer is a select between
+  // two kernel parameters, so no per-thread register holds the row pointers between uses
+  auto slot0 = [&](int hh) { return (size_t)(b * a.H + hh) * a.C; };
+  auto live = [&](int hh) { return hinfo[4 * hh + 3] != 0; };
   auto prefetch_k = [&](int hh, int buf) {
     if (i >= min(lo + TOK, hinfo[4 * hh + 0])) return;
-    const HeadPtrs& Q = hptr[hh];
-    const uint8_t* kr = Q.ks + (size_t)i * KROW + hf * HB;
-    uint8_t* kd = kbuf + (buf * 256 + threadIdx.x) * CC::KSH;
+    const size_t r = slot0(hh) + i;
+    const uint8_t* kr = (live(hh) ? a.mk[1] : a.mk[0]) + r * KROW + hf * HB;
+    uint8_t* kd = kbuf + (buf * 256 + tid) * CC::KSH;
     cp_async<HB>(kd, kr + g1 * 2 * HB);
     cp_async<HB>(kd + HB, kr + g2 * 2 * HB);
-    if (t_ == 0) cp_async<SROW * 2>(ksbuf + (buf * TOK + it) * CC::SRB, Q.kss + (size_t)i * SROW);
+    if (t_ == 0)
+      cp_async<SROW * 2>(ksbuf + (buf * TOK + it) * CC::SRB, (live(hh) ? a.mks[1] : a.mks[0]) + r * SROW);
   };
   auto prefetch_v = [&](int hh) {
     if (i >= min(lo + TOK, hinfo[4 * hh + 0])) return;
-    const HeadPtrs& Q = hptr[hh];
-    cp_async<VSH>(vbuf + threadIdx.x * CC::VSH, Q.vs + (size_t)i * VROW + t_ * VSH);
+    const size_t r = slot0(hh) + i;
+    const bool c = live(hh);
+    cp_async<VSH>(vbuf + tid * CC::VSH, (c ? a.mv[1] : a.mv[0]) + r * VROW + t_ * VSH);
     if (t_ == 0) {
-      cp_async<SROW * 2>(vsbuf + it * CC::SRB, Q.vss + (size_t)i * SROW);
-      cp_async<4>(scbuf + it, Q.scs + i);
+      cp_async<SROW * 2>(vsbuf + it * CC::SRB, (c ? a.mvs[1] : a.mvs[0]) + r * SROW);
+      cp_async<4>(scbuf + it, (c ? a.mid_sc[1] : a.mid_sc[0]) + r);
     }
   };
   int kb = 0;  // K buffer of the head being processed
@@ -591,8 +571,8 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kern
       if (hn < a.H) prefetch_k(hn, kb ^ 1);
       cp_async_commit();
     }
-    // The lanes of one token are adjacent (TPT divides 32) and share every flag below, so the
-    // warp-wide ballot and the absmax exchange see whole tokens; nothing exits before them.
+    // The TPT lanes of one token lie in one warp and share every flag below, so the warp-wide
+    // ballot and the absmax exchange see whole tokens; nothing exits before them.
     const bool in_range = i < hi;
     bool keep = in_range;
     int nv = 0;
@@ -610,109 +590,112 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kern
     }
     const bool moved = keep && nv != i && a.table != nullptr;
 
-    const HeadPtrs P = hptr[h];
-    uint16_t* mks_d = P.ksd;
-    const int di = nv;  // destination slot within the unit
-    uint8_t* krow_d = P.kd + (size_t)di * KROW;
-    const uint8_t* kpf = kbuf + (kb * 256 + threadIdx.x) * CC::KSH;
+    const bool cur = live(h);
+    const int di = nv;                             // destination slot within the unit
+    const size_t dr = slot0(h) + di;               // destination row
+    uint16_t* mks_d = (cur ? a.mks[0] : a.mks[1]) + slot0(h) * SROW;
+    uint8_t* krow_d = (cur ? a.mk[0] : a.mk[1]) + dr * KROW;
+    const uint8_t* kpf = kbuf + (kb * 256 + tid) * CC::KSH;
     const uint16_t* kspf = reinterpret_cast<const uint16_t*>(ksbuf + (kb * TOK + it) * CC::SRB);
     kb ^= 1;
 
     if (keep && !moved) {  // survivor at its own index (or no RoPE): K codes and scales as they are
       copy_row<HB>(kpf, krow_d + g1 * 2 * HB + hf * HB);
       copy_row<HB>(kpf + HB, krow_d + g2 * 2 * HB + hf * HB);
-      if (hf == 0) {
-        mks_d[di * SROW + g1] = kspf[g1];
-        mks_d[di * SROW + g2] = kspf[g2];
-      }
+      if (t_ == 0) copy_row<SROW * 2>(kspf, mks_d + di * SROW);
     }
     if (__ballot_sync(0xffffffffu, moved) != 0u) {  // warp-uniform
-    f2x X1[8], X2[8];
+    uint32_t H1[8], H2[8];  // the re-positioned key half groups, rounded to fp16 (half2 pairs)
     float a1m = 0.f, a2m = 0.f;
     if (moved) {
-      const float s1 = h2f(kspf[g1]), s2 = h2f(kspf[g2]);
+      const f2x S1 = f2_pack(h2f(kspf[g1]), h2f(kspf[g1])), S2 = f2_pack(h2f(kspf[g2]), h2f(kspf[g2]));
       uint32_t w1[HB / 4], w2[HB / 4];
 #pragma unroll
       for (int w = 0; w < HB / 4; ++w) {
         w1[w] = reinterpret_cast<const uint32_t*>(kpf)[w];
         w2[w] = reinterpret_cast<const uint32_t*>(kpf + HB)[w];
       }
+      uint32_t ev1[2], od1[2], ev2[2], od2[2];
       if constexpr (KB == 4) {
-        dequant16_int4(w1, s1, X1);
-        dequant16_int4(w2, s2, X2);
-      } else {
-        constexpr int per = 32 / KB;
-        constexpr uint32_t msk = (1u << KB) - 1u, flip = 1u << (KB - 1);
-        const float off = 8388608.f + (float)flip;   // 2^23 + 2^(bits-1)
-        const f2x OFF = f2_pack(off, off), S1 = f2_pack(s1, s1), S2 = f2_pack(s2, s2);
-        // dequantise (exact): the offset-binary code sits in the mantissa of 2^23
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int j0 = 2 * k, j1 = 2 * k + 1;
-          const uint32_t c10 = ((w1[j0 / per] >> (KB * (j0 % per))) & msk) ^ flip;
-          const uint32_t c11 = ((w1[j1 / per] >> (KB * (j1 % per))) & msk) ^ flip;
-          const uint32_t c20 = ((w2[j0 / per] >> (KB * (j0 % per))) & msk) ^ flip;
-          const uint32_t c21 = ((w2[j1 / per] >> (KB * (j1 % per))) & msk) ^ flip;
-          X1[k] = f2_mul(f2_sub(f2_pack(__uint_as_float(0x4B000000u | c10),
-                                        __uint_as_float(0x4B000000u | c11)), OFF), S1);
-          X2[k] = f2_mul(f2_sub(f2_pack(__uint_as_float(0x4B000000u | c20),
-                                        __uint_as_float(0x4B000000u | c21)), OFF), S2);
-        }
+        split_int4(w1, ev1, od1);
+        split_int4(w2, ev2, od2);
       }
-      // un-RoPE at the old index, re-RoPE at the new one, every product and sum rounded
-      // separately: products as packed fp32x2 multiplies (two rotation pairs at once), sums
-      // as scalar IEEE adds (rotate2). Then the cast to fp16.
-      // staged rows of the old and new positions (inside [0, NROWS) whenever staged is set)
-      const int ro = staged ? n_sink + i - rlo : 0, rn = staged ? n_sink + nv - rlo : 0;
+      // this thread's 8 float4 (pairs 16 t_ .. 16 t_ + 15) of the old and the new position's
+      // RoPE row: staged rows when the block's range fit, else the table in global memory
+      const int bo = staged ? tab_slot<D>(n_sink + i - rlo, 8 * t_) : 0;
+      const int bn = staged ? tab_slot<D>(n_sink + nv - rlo, 8 * t_) : 0;
       const float4* to = reinterpret_cast<const float4*>(a.table) +
-                         (size_t)(n_sink + i) * (a.half / 2) + 16 * gp + 8 * hf;
+                         (size_t)(n_sink + i) * (a.half / 2) + 8 * t_;
       const float4* tn = reinterpret_cast<const float4*>(a.table) +
-                         (size_t)(n_sink + nv) * (a.half / 2) + 16 * gp + 8 * hf;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int j = 8 * t_ + k;  // = 16 gp + 8 hf + k
-        // (cos, cos, sin, sin) of 2 pairs at the old and at the new position
-        float4 co, cn;
-        if (staged) {
-          co = tab[tab_slot<D>(ro, j)];
-          cn = tab[tab_slot<D>(rn, j)];
-        } else {
-          co = __ldg(to + k);
-          cn = __ldg(tn + k);
-        }
-        rotate2(X1[k], X2[k], f2_pack(co.x, co.y), f2_pack(-co.z, -co.w));
-        rotate2(X1[k], X2[k], f2_pack(cn.x, cn.y), f2_pack(cn.z, cn.w));
-        X1[k] = f2_round_f16(X1[k]);
-        X2[k] = f2_round_f16(X2[k]);
-        float p1[2], p2[2];
-        f2_unpack(X1[k], p1[0], p1[1]);
-        f2_unpack(X2[k], p2[0], p2[1]);
-        a1m = fmaxf(a1m, fmaxf(fabsf(p1[0]), fabsf(p1[1])));
-        a2m = fmaxf(a2m, fmaxf(fabsf(p2[0]), fabsf(p2[1])));
-      }
+                         (size_t)(n_sink + nv) * (a.half / 2) + 8 * t_;
+      // per pair block: dequantise (exact), un-RoPE at the old index, re-RoPE at the new one
+      // (every product and sum rounded on its own: packed products, scalar sums), cast to fp16
+#define FADE_ROT_K(K)                                                                        \
+  {                                                                                          \
+    f2x X1, X2;                                                                              \
+    if constexpr (KB == 4) {                                                                 \
+      X1 = dequant_pair_int4<K>(ev1, od1, S1);                                               \
+      X2 = dequant_pair_int4<K>(ev2, od2, S2);                                               \
+    } else {                                                                                 \
+      X1 = dequant_pair_bits<KB, K>(w1, S1);                                                 \
+      X2 = dequant_pair_bits<KB, K>(w2, S2);                                                 \
+    }                                                                                        \
+    float4 co, cn;                                                                           \
+    if (staged) {                                                                            \
+      co = tab[bo + K];                                                                      \
+      cn = tab[bn + K];                                                                      \
+    } else {                                                                                 \
+      co = __ldg(to + K);                                                                    \
+      cn = __ldg(tn + K);                                                                    \
+    }                                                                                        \
+    rotate2(X1, X2, f2_pack(co.x, co.y), f2_pack(-co.z, -co.w));                              \
+    rotate2(X1, X2, f2_pack(cn.x, cn.y), f2_pack(cn.z, cn.w));                                \
+    float p10, p11, p20, p21;                                                                \
+    f2_unpack(X1, p10, p11);                                                                 \
+    f2_unpack(X2, p20, p21);                                                                 \
+    a1m = fmaxf(a1m, fmaxf(fabsf(p10), fabsf(p11)));                                         \
+    a2m = fmaxf(a2m, fmaxf(fabsf(p20), fabsf(p21)));                                         \
+    const __half2 r1 = __floats2half2_rn(p10, p11), r2 = __floats2half2_rn(p20, p21);        \
+    H1[K] = *reinterpret_cast<const uint32_t*>(&r1);                                         \
+    H2[K] = *reinterpret_cast<const uint32_t*>(&r2);                                         \
+  }
+      FADE_ROT_K(0) FADE_ROT_K(1) FADE_ROT_K(2) FADE_ROT_K(3)
+      FADE_ROT_K(4) FADE_ROT_K(5) FADE_ROT_K(6) FADE_ROT_K(7)
+#undef FADE_ROT_K
     }
     // absmax of each group over the token's two half-threads (adjacent lanes)
-    a1m = fmaxf(a1m, __shfl_xor_sync(0xffffffffu, a1m, 1));
-    a2m = fmaxf(a2m, __shfl_xor_sync(0xffffffffu, a2m, 1));
-    if (moved) {
+    // group absmax over the token's two half-threads; the absmax of the fp16 values is the fp16
+    // rounding of the fp32 absmax (round-to-nearest is monotone and odd)
+    a1m = __half2float(__float2half_rn(fmaxf(a1m, __shfl_xor_sync(0xffffffffu, a1m, CC::TPW))));
+    a2m = __half2float(__float2half_rn(fmaxf(a2m, __shfl_xor_sync(0xffffffffu, a2m, CC::TPW))));
     constexpr int qmax = (1 << (KB - 1)) - 1;
-    float s1 = __half2float(__float2half_rn(__fdiv_rn(a1m, (float)qmax)));
-    float s2 = __half2float(__float2half_rn(__fdiv_rn(a2m, (float)qmax)));
+    // scales (the division is exact for qmax = 1)
+    float s1 = __half2float(__float2half_rn(qmax == 1 ? a1m : __fdiv_rn(a1m, (float)qmax)));
+    float s2 = __half2float(__float2half_rn(qmax == 1 ? a2m : __fdiv_rn(a2m, (float)qmax)));
     if (a1m > 0.f && s1 == 0.f) s1 = kSubnormalMin;
     if (a2m > 0.f && s2 == 0.f) s2 = kSubnormalMin;
+    // the token's scale row goes out in one store by t_ = 0: its own groups gp and gp + d/64,
+    // and (d = 128) groups 1 and 3 from the thread with t_ = 2
+    const uint32_t my = __half_as_ushort(__float2half_rn(s1)) |
+                        ((uint32_t)__half_as_ushort(__float2half_rn(s2)) << 16);
+    const uint32_t other = __shfl_down_sync(0xffffffffu, my, 2 * CC::TPW);
+    if (moved) {
     uint32_t o1[HB / 4], o2[HB / 4];
 #pragma unroll
     for (int w = 0; w < HB / 4; ++w) o1[w] = o2[w] = 0u;
-    if (s1 > 0.f) codes_half_group<KB>(X1, s1, o1);
-    if (s2 > 0.f) codes_half_group<KB>(X2, s2, o2);
+    if (s1 > 0.f) codes_half_group<KB>(H1, s1, o1);
+    if (s2 > 0.f) codes_half_group<KB>(H2, s2, o2);
 #pragma unroll
     for (int w = 0; w < HB / 4; ++w) {
       reinterpret_cast<uint32_t*>(krow_d + g1 * 2 * HB + hf * HB)[w] = o1[w];
       reinterpret_cast<uint32_t*>(krow_d + g2 * 2 * HB + hf * HB)[w] = o2[w];
     }
-    if (hf == 0) {
-      mks_d[di * SROW + g1] = __half_as_ushort(__float2half_rn(s1));
-      mks_d[di * SROW + g2] = __half_as_ushort(__float2half_rn(s2));
+    if (t_ == 0) {
+      if constexpr (SROW == 4)
+        *reinterpret_cast<uint2*>(mks_d + di * SROW) =
+            make_uint2((my & 0xFFFFu) | (other << 16), (my >> 16) | (other & 0xFFFF0000u));
+      else
+        *reinterpret_cast<uint32_t*>(mks_d + di * SROW) = my;
     }
     }  // moved
     }  // some lane of the warp moved
@@ -720,13 +703,11 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kern
     cp_async_wait<1>();  // this head's V data (the newer group is the next head's K data)
     __syncwarp();
     if (keep) {
-      copy_row<VSH>(vbuf + threadIdx.x * CC::VSH, P.vd + (size_t)di * VROW + t_ * VSH);
-      const uint16_t* vspf = reinterpret_cast<const uint16_t*>(vsbuf + it * CC::SRB);
-      if (hf == 0) {
-        P.vsd[di * SROW + g1] = vspf[g1];
-        P.vsd[di * SROW + g2] = vspf[g2];
+      copy_row<VSH>(vbuf + tid * CC::VSH, (cur ? a.mv[0] : a.mv[1]) + dr * VROW + t_ * VSH);
+      if (t_ == 0) {
+        copy_row<SROW * 2>(vsbuf + it * CC::SRB, (cur ? a.mvs[0] : a.mvs[1]) + dr * SROW);
+        (cur ? a.mid_sc[0] : a.mid_sc[1])[dr] = scbuf[it];
       }
-      if (t_ == 0) P.scd[di] = scbuf[it];
     }
   }
   cp_async_wait<0>();  // nothing in flight when the CTA exits
@@ -734,27 +715,26 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kern
 
 // Recent rings after compaction: every ring token's index drops by its unit's n_ev, so its key
 // is re-positioned in place; then the unit's counts are committed (middle count, live buffer).
-// grid = (B), 256 threads: one CTA per batch row loops over the row's KV heads. Thread
-// (token t, t_) owns the same rotation pairs as in the middle tier; the RoPE rows of the ring's
-// old and new positions are staged once for all heads.
+// grid = (H, B), 256 threads: one CTA per unit. Thread (token t, t_) owns the same rotation
+// pairs as in the middle tier; the RoPE rows of the ring's old and new positions are staged.
 template <int D>
 __global__ void __launch_bounds__(256) evict_recent_commit_kernel(LayerArgs a) {
   using CC = CompactCfg<D>;
   constexpr int TPT = CC::TPT, TOK = CC::TOK;
   extern __shared__ float4 tab[];
-  int* hinfo = reinterpret_cast<int*>(tab + CC::NROWS * CC::ROWF4);  // [H][4]
+  int* hinfo = reinterpret_cast<int*>(tab + CC::TABF4);  // [H][4]
   __shared__ int s_rlo, s_rhi;
-  const int b = blockIdx.x;
+  const int b = blockIdx.y, hb = blockIdx.x;  // one unit per CTA: (row b, KV head hb)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // recent rings of this row: every token's index drops by its unit's n_ev; keys rewritten
-  // in place. Thread (token t, t_) owns the same rotation pairs as in the middle tier; the
-  // RoPE rows of the ring's old and new positions are staged once for all heads.
+  // the unit's recent ring: every token's index drops by the unit's n_ev; keys rewritten in
+  // place. Thread (token t, t_) owns the same rotation pairs as in the middle tier; the RoPE
+  // rows of the ring's old and new positions are staged first.
   if (threadIdx.x == 0) {
     s_rlo = 0x7fffffff;
     s_rhi = -1;
   }
   __syncthreads();
-  for (int h = warp; h < a.H; h += 8) {
+  for (int h = hb + warp; h < hb + 1; h += 8) {
     const int32_t* m = a.meta + (b * a.H + h) * kF;
     const int n_mid = m[FADE_META_N_MID];
     const int n_ev = a.positional ? max(0, n_mid - a.budget) : m[FADE_META_N_EV];
@@ -783,9 +763,9 @@ __global__ void __launch_bounds__(256) evict_recent_commit_kernel(LayerArgs a) {
     }
   }
   __syncthreads();
-  const int tt = threadIdx.x / TPT, t_ = threadIdx.x % TPT;
+  const int tt = warp * CC::TPW + lane % CC::TPW, t_ = lane / CC::TPW;
   const int gp = t_ >> 1, hf = t_ & 1;
-  for (int h = 0; h < a.H && rotate; ++h) {
+  for (int h = hb; h < hb + 1 && rotate; ++h) {
     const int n_mid = hinfo[4 * h + 0], n_ev = hinfo[4 * h + 1];
     const int n_rec = hinfo[4 * h + 3] & 0xFFFF, head = hinfo[4 * h + 3] >> 16;
     if (n_ev == 0) continue;
@@ -825,7 +805,7 @@ __global__ void __launch_bounds__(256) evict_recent_commit_kernel(LayerArgs a) {
     }
   }
   __syncthreads();  // every thread is done with the counts read above
-  for (int h = threadIdx.x; h < a.H; h += 256) {
+  for (int h = hb + threadIdx.x; h < hb + 1; h += 256) {
     int32_t* m = a.meta + (b * a.H + h) * kF;
     const int n_ev = a.positional ? max(0, m[FADE_META_N_MID] - a.budget) : m[FADE_META_N_EV];
     if (n_ev > 0) {
@@ -986,13 +966,13 @@ struct CompactLaunch {
 template <int D>
 fade_status_t launch_recent_commit(const LayerArgs& a, int B, cudaStream_t st) {
   using CC = CompactCfg<D>;
-  const size_t smem = (size_t)CC::NROWS * CC::ROWF4 * 16 + (size_t)a.H * 4 * 4;
+  const size_t smem = (size_t)CC::TABF4 * 16 + (size_t)a.H * 4 * 4;
   auto kern = evict_recent_commit_kernel<D>;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
           cudaSuccess)
     return launch_status("fade_evict_rerope recent shared-memory opt-in");
-  kern<<<B, 256, smem, st>>>(a);
+  kern<<<dim3(a.H, B), 256, smem, st>>>(a);
   return launch_status("fade_evict_rerope recent + commit");
 }
 

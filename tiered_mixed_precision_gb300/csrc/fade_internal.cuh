@@ -35,11 +35,60 @@ struct RowLens {
   int32_t v[FADE_MAX_BATCH];
 };
 
+// Stream-K schedule of the persistent tensor-core attention (INT4 K / INT2 V). The middle tier
+// of every unit is cut into 256-token tiles; tiles are numbered unit by unit (row-major over
+// (row, KV head)); CTA c takes global tiles [cta_start[c], cta_start[c+1]) plus the FP16-tier
+// items of units c, c + P, ... . A unit's tiles may span several CTAs: each CTA writes one
+// partial per unit segment it covers (split 1 + k for the k-th CTA of the unit; split 0 is the
+// FP16 tiers). The boundaries are weighted so that every CTA gets about the same work.
+constexpr int kMaxCtaSK = 320;   // persistent CTAs at most
+constexpr int kTileTokens = 256;
+struct StreamK {
+  int P;                               // persistent CTAs
+  int B, H;
+  int smax;                            // most middle segments of any unit
+  uint16_t row_tiles[FADE_MAX_BATCH];  // middle tiles of every unit of row b
+  int cta_start[kMaxCtaSK + 1];
+};
+// First global tile of row b's first unit.
+__host__ __device__ inline int sk_row_start(const StreamK& k, int b) {
+  int s = 0;
+  for (int r = 0; r < b; ++r) s += k.H * (int)k.row_tiles[r];
+  return s;
+}
+// The CTA whose range holds global tile g: the largest c < P with cta_start[c] <= g.
+__host__ __device__ inline int sk_cta_of(const StreamK& k, int g) {
+  int lo = 0, hi = k.P - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    if (k.cta_start[mid] <= g) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+// CTAs c in [c_lo, c_hi] whose middle range is not empty.
+__host__ __device__ inline int sk_nonempty(const StreamK& k, int c_lo, int c_hi) {
+  int n = 0;
+  for (int c = c_lo; c <= c_hi; ++c) n += k.cta_start[c + 1] > k.cta_start[c];
+  return n;
+}
+// Number of middle segments (partials after split 0) of unit (b, h): the CTAs with tiles of
+// the unit. The k-th of them (k = sk_nonempty(first, c - 1)) writes split 1 + k.
+__host__ __device__ inline int sk_segments(const StreamK& k, int b, int h) {
+  const int rt = k.row_tiles[b];
+  if (rt == 0) return 0;
+  const int g0 = sk_row_start(k, b) + h * rt;
+  return sk_nonempty(k, sk_cta_of(k, g0), sk_cta_of(k, g0 + rt - 1));
+}
+
 // Decode attention for INT4 K / INT2 V: split 0 covers the FP16 tiers on the CUDA cores,
-// splits 1..nsplit-1 the middle tier on the tensor cores. Defined in attention_mma.cu.
+// splits 1.. the middle tier on the tensor cores. Defined in attention_mma.cu.
 bool mid_mma_supported(const fade_config_t* c);
+// Persistent CTAs the kernel runs with on the current device.
+int mid_mma_ctas(const fade_config_t* c);
+// The schedule for the layer's current middle-tier counts (host mirrors).
+void build_stream_k(const fade_config_t* c, const fade_layer_t* L, int ctas, StreamK* k);
 fade_status_t launch_mid_mma(const fade_config_t* c, const fade_layer_t* L, const uint16_t* q,
-                             float* logits, float* part_ml, float* part_acc, int chunk,
+                             float* logits, float* part_ml, float* part_acc, const StreamK& sk,
                              int nsplit, cudaStream_t st);
 
 // ---------------------------------------------------------------- device side
@@ -257,27 +306,42 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-// Exact dequantisation of 16 INT4 codes (two little-endian words, channel j at bits 4j) with
-// scale s into 8 packed pairs (channels 2k, 2k+1). Each nibble, offset-binary (code + 8), is
-// moved by a byte permute into the low mantissa byte of 2^23, so the float is 2^23 + code + 8;
-// subtracting 2^23 + 8 and multiplying by s are exact.
-__device__ __forceinline__ void dequant16_int4(const uint32_t (&w)[2], float s, f2x (&X)[8]) {
-  const f2x OFF = f2_pack(8388616.f, 8388616.f), S = f2_pack(s, s);
-  const uint32_t magic = 0x4B000000u;
+// Exact dequantisation of INT4 codes, one packed pair at a time. The two little-endian words
+// of a half group (channel j at bits 4j) are first split into offset-binary nibbles, even
+// channels in ev[w] and odd ones in od[w] (byte b of word w = channel 8w + 2b (+1)); a byte
+// permute then moves a nibble into the low mantissa byte of 2^23, so the float is
+// 2^23 + code + 8, and subtracting 2^23 + 8 and multiplying by s are exact.
+__device__ __forceinline__ void split_int4(const uint32_t (&w)[2], uint32_t (&ev)[2],
+                                           uint32_t (&od)[2]) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const uint32_t ev = (w[h] & 0x0F0F0F0Fu) ^ 0x08080808u;         // channels 8h + 2b
-    const uint32_t od = ((w[h] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;  // channels 8h + 2b + 1
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const float lo = __uint_as_float(prmt(ev, magic, 0x7650u + b));
-      const float hi = __uint_as_float(prmt(od, magic, 0x7650u + b));
-      X[4 * h + b] = f2_mul(f2_sub(f2_pack(lo, hi), OFF), S);
-    }
+    ev[h] = (w[h] & 0x0F0F0F0Fu) ^ 0x08080808u;
+    od[h] = ((w[h] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
   }
 }
+template <int K>  // pair K = channels 2K, 2K+1 of the half group
+__device__ __forceinline__ f2x dequant_pair_int4(const uint32_t (&ev)[2], const uint32_t (&od)[2],
+                                                 f2x S) {
+  const uint32_t magic = 0x4B000000u;
+  const float lo = __uint_as_float(prmt(ev[K / 4], magic, 0x7650u + (K % 4)));
+  const float hi = __uint_as_float(prmt(od[K / 4], magic, 0x7650u + (K % 4)));
+  return f2_mul(f2_sub(f2_pack(lo, hi), f2_pack(8388616.f, 8388616.f)), S);
+}
+// Same for BITS-bit codes in general (here used for INT2: one word per half group).
+template <int BITS, int K>
+__device__ __forceinline__ f2x dequant_pair_bits(const uint32_t* w, f2x S) {
+  constexpr int per = 32 / BITS;
+  constexpr uint32_t msk = (1u << BITS) - 1u, flip = 1u << (BITS - 1);
+  constexpr int j0 = 2 * K, j1 = 2 * K + 1;
+  const uint32_t c0 = ((w[j0 / per] >> (BITS * (j0 % per))) & msk) ^ flip;
+  const uint32_t c1 = ((w[j1 / per] >> (BITS * (j1 % per))) & msk) ^ flip;
+  const float off = 8388608.f + (float)flip;   // 2^23 + 2^(bits-1)
+  return f2_mul(f2_sub(f2_pack(__uint_as_float(0x4B000000u | c0), __uint_as_float(0x4B000000u | c1)),
+                       f2_pack(off, off)),
+                S);
+}
 
-// Codes of 16 fp16-valued values (8 packed pairs) of one group whose scale s (> 0) is already
+// Codes of 16 fp16 values (8 half2 words) of one group whose scale s (> 0) is already
 // known, packed little-endian from bit 0 of out[0] (INT4: two words, INT2: one): exact
 // round_half_even(x/s). Fast path: x * (1/s) + 1.5 * 2^23 leaves a candidate code in the low
 // bits (two's complement); the exact residual x - q*s, below s/2 for every value, confirms all
@@ -285,7 +349,7 @@ __device__ __forceinline__ void dequant16_int4(const uint32_t (&w)[2], float s, 
 // candidate off by one, or a subnormal scale where the clamp can bind) every code is redone by
 // the exact scalar path with the clamp.
 template <int BITS>
-__device__ __forceinline__ void codes_half_group(const f2x (&X)[8], float s, uint32_t* out) {
+__device__ __forceinline__ void codes_half_group(const uint32_t (&H)[8], float s, uint32_t* out) {
   constexpr int per = 32 / BITS;
   constexpr uint32_t mask = (1u << BITS) - 1u;
   constexpr int qmax = (1 << (BITS - 1)) - 1;
@@ -296,8 +360,10 @@ __device__ __forceinline__ void codes_half_group(const f2x (&X)[8], float s, uin
   float emax = 0.f;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const f2x QM = f2_add(f2_mul(X[k], R), M);
-    const f2x E = f2_fma(f2_sub(QM, M), NS, X[k]);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&H[k]));
+    const f2x X = f2_pack(f.x, f.y);
+    const f2x QM = f2_add(f2_mul(X, R), M);
+    const f2x E = f2_fma(f2_sub(QM, M), NS, X);
     float e0, e1, qm0, qm1;
     f2_unpack(E, e0, e1);
     f2_unpack(QM, qm0, qm1);
@@ -326,7 +392,11 @@ __device__ __forceinline__ void codes_half_group(const f2x (&X)[8], float s, uin
   }
   float v[16];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) f2_unpack(X[k], v[2 * k], v[2 * k + 1]);
+  for (int k = 0; k < 8; ++k) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&H[k]));
+    v[2 * k] = f.x;
+    v[2 * k + 1] = f.y;
+  }
 #pragma unroll
   for (int w = 0; w < 16 / per; ++w) {
     uint32_t o = 0u;
