@@ -641,7 +641,7 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kern
       X2 = dequant_pair_bits<KB, K>(w2, S2);                                                 \
     }                                                                                        \
     float4 co, cn;                                                                           \
-    if (staged) {                                                                            \
+    if (kStaged) {                                                                           \
       co = tab[bo + K];                                                                      \
       cn = tab[bn + K];                                                                      \
     } else {                                                                                 \
@@ -659,6 +659,7 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kern
     H1[K] = *reinterpret_cast<const uint32_t*>(&r1);                                         \
     H2[K] = *reinterpret_cast<const uint32_t*>(&r2);                                         \
   }
+      const bool kStaged = staged;
       FADE_ROT_K(0) FADE_ROT_K(1) FADE_ROT_K(2) FADE_ROT_K(3)
       FADE_ROT_K(4) FADE_ROT_K(5) FADE_ROT_K(6) FADE_ROT_K(7)
 #undef FADE_ROT_K
@@ -669,9 +670,9 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kern
     a1m = __half2float(__float2half_rn(fmaxf(a1m, __shfl_xor_sync(0xffffffffu, a1m, CC::TPW))));
     a2m = __half2float(__float2half_rn(fmaxf(a2m, __shfl_xor_sync(0xffffffffu, a2m, CC::TPW))));
     constexpr int qmax = (1 << (KB - 1)) - 1;
-    // scales (the division is exact for qmax = 1)
-    float s1 = __half2float(__float2half_rn(qmax == 1 ? a1m : __fdiv_rn(a1m, (float)qmax)));
-    float s2 = __half2float(__float2half_rn(qmax == 1 ? a2m : __fdiv_rn(a2m, (float)qmax)));
+    // scales: fp16(absmax / qmax)
+    float s1 = __half2float(__float2half_rn(div_by_qmax<qmax>(a1m)));
+    float s2 = __half2float(__float2half_rn(div_by_qmax<qmax>(a2m)));
     if (a1m > 0.f && s1 == 0.f) s1 = kSubnormalMin;
     if (a2m > 0.f && s2 == 0.f) s2 = kSubnormalMin;
     // the token's scale row goes out in one store by t_ = 0: its own groups gp and gp + d/64,

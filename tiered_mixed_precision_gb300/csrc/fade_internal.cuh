@@ -299,6 +299,22 @@ __device__ __forceinline__ void rotate2(f2x& X1, f2x& X2, f2x C, f2x S) {
   X2 = f2_pack(__fadd_rn(c0, d0), __fadd_rn(c1, d1));
 }
 
+// Correctly rounded fp32 a / QMAX for fp16-valued a >= 0 (QMAX = 7 or 1), the scale division
+// of the quantiser. For QMAX = 7: Markstein's correction step (q0 = a * RN(1/7), e = a - q0 * 7
+// exact by FMA, q1 = RN(q0 + e * RN(1/7))); an exhaustive check over every non-negative finite
+// fp16 a shows q1 equal to the IEEE quotient.
+template <int QMAX>
+__device__ __forceinline__ float div_by_qmax(float a) {
+  if constexpr (QMAX == 1) {
+    return a;
+  } else {
+    constexpr float r = 1.0f / (float)QMAX;
+    const float q0 = a * r;
+    const float e = fmaf(-q0, (float)QMAX, a);
+    return fmaf(e, r, q0);
+  }
+}
+
 // Byte permute: output byte i = byte sel[4i+2:4i] of {b, a} (a = bytes 0-3, b = bytes 4-7).
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
@@ -353,7 +369,9 @@ __device__ __forceinline__ void codes_half_group(const uint32_t (&H)[8], float s
   constexpr int per = 32 / BITS;
   constexpr uint32_t mask = (1u << BITS) - 1u;
   constexpr int qmax = (1 << (BITS - 1)) - 1;
-  const float r = __frcp_rn(s);
+  // any reciprocal estimate serves: the exact residual below confirms or rejects the candidates
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
   const float h = 0.5f * s;
   const f2x R = f2_pack(r, r), M = f2_pack(12582912.f, 12582912.f), NS = f2_pack(-s, -s);
   uint32_t qb[16];
@@ -407,6 +425,70 @@ __device__ __forceinline__ void codes_half_group(const uint32_t (&H)[8], float s
     }
     out[w] = o;
   }
+}
+
+// ---------------------------------------------------------------- async copies, mbarriers
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz: a wait that never ends
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: gives up after kWaitCycles and records the failure in status[0].
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status,
+                                          int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitCycles) {
+      atomicCAS(status, 0, code);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,
+                                             uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// Shared -> global bulk copy (both 16-byte aligned, bytes a multiple of 16), bulk async-group.
+__device__ __forceinline__ void bulk_store_1d(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the committed bulk stores have read their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until the committed bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Order this thread's generic shared-memory writes before later async-proxy (bulk copy) reads.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 }  // namespace fade
