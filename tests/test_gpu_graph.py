@@ -87,3 +87,48 @@ def test_graph_replay_matches_eager_steps(policy):
                         assert np.array_equal(a_[key], b_[key]), (layer, b, h, key)
                     else:
                         assert a_[key] == b_[key], (layer, b, h, key)
+
+
+@pytest.mark.parametrize("policy", ["position", "h2o"])
+def test_pipelined_graph_matches_eager_steps(policy):
+    """Pipelined steps (each layer's maintenance for the next step on a side stream, right
+    after its attention) give the same outputs as the method's step order, and after one more
+    maintenance pass the same cache."""
+    import torch
+
+    wl = get_workload(4).scaled(layers=3, batch=2, num_q_heads=8, num_kv_heads=2,
+                                prompt_len=1200, int4_budget=500, policy=policy)
+    if policy == "h2o":
+        wl = wl.scaled(rope=get_workload(3).rope)
+    masses = _masses(wl)
+    eager, piped = _make(wl, masses), _make(wl, masses)
+    L, B, Hq, Hkv, d = wl.layers, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+    steps = 4
+    q = torch.from_numpy(draw_vectors(wl, "q", (steps, L, B, Hq, d), "pipe")).cuda()
+    k = torch.from_numpy(draw_vectors(wl, "k", (steps, L, B, Hkv, d), "pipe")).cuda()
+    v = torch.from_numpy(draw_vectors(wl, "v", (steps, L, B, Hkv, d), "pipe")).cuda()
+    out_e = torch.empty((L, B, Hq, d), dtype=torch.float16, device="cuda")
+    out_p = torch.empty_like(out_e)
+    side = torch.cuda.Stream()
+    piped.maintain_all()
+    qb, kb, vb = q[0].clone(), k[0].clone(), v[0].clone()
+    g = piped.capture_step(qb, kb, vb, out_p, side)
+    for s in range(steps):
+        eager.step_all(q[s], k[s], v[s], out_e)
+        qb.copy_(q[s])
+        kb.copy_(k[s])
+        vb.copy_(v[s])
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out_e.view(torch.int16), out_p.view(torch.int16)), f"step {s}"
+    eager.maintain_all()
+    torch.cuda.synchronize()
+    for layer in range(L):
+        for b in range(B):
+            for h in range(Hkv):
+                a_, b_ = eager.unit_state(layer, b, h), piped.unit_state(layer, b, h)
+                for key in a_:
+                    if isinstance(a_[key], np.ndarray):
+                        assert np.array_equal(a_[key], b_[key]), (layer, b, h, key)
+                    else:
+                        assert a_[key] == b_[key], (layer, b, h, key)

@@ -516,29 +516,30 @@ struct SkPos {
   int b, h, tile;
 };
 __device__ __forceinline__ SkPos sk_locate(const StreamK& k, int g) {
-  int base = 0;
-  for (int b = 0; b < k.B; ++b) {
-    const int rt = k.row_tiles[b], n = k.H * rt;
-    if (g < base + n) return SkPos{b, (g - base) / rt, (g - base) % rt};
-    base += n;
+  if (g >= k.row_start[k.B]) return SkPos{k.B, 0, 0};
+  int lo = 0, hi = k.B - 1;  // the last row whose start is <= g (rows without tiles are skipped)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    if (k.row_start[mid] <= g) lo = mid; else hi = mid - 1;
   }
-  return SkPos{k.B, 0, 0};
+  const int rt = sk_row_tiles(k, lo), off = g - k.row_start[lo];
+  return SkPos{lo, off / rt, off % rt};
 }
 // Move `run` tiles forward, where the run ends at or before the end of the current unit.
 __device__ __forceinline__ void sk_advance(const StreamK& k, SkPos& p, int run) {
   p.tile += run;
-  if (p.tile < k.row_tiles[p.b]) return;
+  if (p.tile < sk_row_tiles(k, p.b)) return;
   p.tile = 0;
   if (++p.h < k.H) return;
   p.h = 0;
   ++p.b;
-  while (p.b < k.B && k.row_tiles[p.b] == 0) ++p.b;
+  while (p.b < k.B && sk_row_tiles(k, p.b) == 0) ++p.b;
 }
 // Segments (maximal runs inside one unit) among n tiles starting at p.
 __device__ __forceinline__ int sk_count_segments(const StreamK& k, SkPos p, int n) {
   int count = 0;
   while (n > 0) {
-    const int run = min(n, (int)k.row_tiles[p.b] - p.tile);
+    const int run = min(n, sk_row_tiles(k, p.b) - p.tile);
     ++count;
     n -= run;
     sk_advance(k, p, run);
@@ -688,7 +689,7 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
       for (int u = cta; u < units && go; u += P) go = issue_item(u, 0, 0, f16_staged ? 2 : 1);
       SkPos pos = p0;
       for (int g = g0; g < g1 && go;) {
-        const int rt = sk.row_tiles[pos.b];
+        const int rt = sk_row_tiles(sk, pos.b);
         const int run = min(g1 - g, rt - pos.tile);
         // this CTA's rank among the CTAs holding tiles of the unit
         const int k = sk_nonempty(sk, sk_cta_of(sk, g - pos.tile), cta - 1);
@@ -1038,11 +1039,10 @@ void build_stream_k(const fade_config_t* c, const fade_layer_t* L, int ctas, Str
   k->H = c->num_kv_heads;
   long long T = 0;
   for (int b = 0; b < c->batch; ++b) {
-    const int rt = (L->h_n_mid[b] + kTileTok - 1) / kTileTok;
-    k->row_tiles[b] = (uint16_t)rt;
-    T += (long long)k->H * rt;
+    k->row_start[b] = (int)T;
+    T += (long long)k->H * ((L->h_n_mid[b] + kTileTok - 1) / kTileTok);
   }
-  for (int b = c->batch; b < FADE_MAX_BATCH; ++b) k->row_tiles[b] = 0;
+  for (int b = c->batch; b <= FADE_MAX_BATCH; ++b) k->row_start[b] = (int)T;
   // an FP16-tier item (sinks + recent window on the CUDA cores) costs about kFp16Weight tiles
   constexpr long long kFp16Weight = 3;
   const long long F = (long long)c->batch * c->num_kv_heads, P = ctas;

@@ -47,14 +47,13 @@ struct StreamK {
   int P;                               // persistent CTAs
   int B, H;
   int smax;                            // most middle segments of any unit
-  uint16_t row_tiles[FADE_MAX_BATCH];  // middle tiles of every unit of row b
+  int row_start[FADE_MAX_BATCH + 1];   // first global tile of row b's first unit
   int cta_start[kMaxCtaSK + 1];
 };
-// First global tile of row b's first unit.
-__host__ __device__ inline int sk_row_start(const StreamK& k, int b) {
-  int s = 0;
-  for (int r = 0; r < b; ++r) s += k.H * (int)k.row_tiles[r];
-  return s;
+// First global tile of row b's first unit, and the middle tiles of each unit of row b.
+__host__ __device__ inline int sk_row_start(const StreamK& k, int b) { return k.row_start[b]; }
+__host__ __device__ inline int sk_row_tiles(const StreamK& k, int b) {
+  return (k.row_start[b + 1] - k.row_start[b]) / k.H;
 }
 // The CTA whose range holds global tile g: the largest c < P with cta_start[c] <= g.
 __host__ __device__ inline int sk_cta_of(const StreamK& k, int g) {
@@ -74,7 +73,7 @@ __host__ __device__ inline int sk_nonempty(const StreamK& k, int c_lo, int c_hi)
 // Number of middle segments (partials after split 0) of unit (b, h): the CTAs with tiles of
 // the unit. The k-th of them (k = sk_nonempty(first, c - 1)) writes split 1 + k.
 __host__ __device__ inline int sk_segments(const StreamK& k, int b, int h) {
-  const int rt = k.row_tiles[b];
+  const int rt = sk_row_tiles(k, b);
   if (rt == 0) return 0;
   const int g0 = sk_row_start(k, b) + h * rt;
   return sk_nonempty(k, sk_cta_of(k, g0), sk_cta_of(k, g0 + rt - 1));

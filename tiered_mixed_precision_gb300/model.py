@@ -100,11 +100,25 @@ class FadeCache:
         self._pos_host.copy_(torch.from_numpy(np.ascontiguousarray(pos, np.int32)))
         self.pos.copy_(self._pos_host, non_blocking=True)
 
-    def step_layer(self, layer: int, q_raw: torch.Tensor, k_raw: torch.Tensor, v: torch.Tensor,
-                   out: torch.Tensor):
-        """One decode step of one layer. q_raw [B][Hq][d], k_raw/v [B][Hkv][d] fp16, pre-RoPE
-        (rotated into work buffers at the positions last set by ``set_positions``);
-        out [B][Hq][d] fp16."""
+    def maintain_layer(self, layer: int):
+        """The part of a layer's decode step that precedes the append: demote (quantise-pack the
+        token leaving the recent window) and evict + re-position."""
+        c = self.cfg
+        L = self.layers[layer]
+        ring_full = bool((L.h_n_recent == c.recent_window).any())
+        F.fade_cache_demote(L)
+        n = 1 if ring_full else 0
+        evicting = c.evicts and bool((L.h_n_mid > c.int4_budget).any())
+        t = self._tick("evict") if evicting else None
+        F.fade_evict_rerope(L, self.table, self.max_pos)
+        self._tock(t)
+        n += (2 if c.policy == "position" else 3) if evicting else 0
+        self.launches += n
+
+    def attend_layer(self, layer: int, q_raw: torch.Tensor, k_raw: torch.Tensor,
+                     v: torch.Tensor, out: torch.Tensor):
+        """The rest of a layer's decode step: RoPE of the new q and k (into work buffers, at the
+        positions last set by ``set_positions``), append, attention, H2O / EMA accumulation."""
         c = self.cfg
         L = self.layers[layer]
         F.fade_rope_apply(c, self.table, self.max_pos, q_raw, self.q_rot, c.batch,
@@ -112,14 +126,6 @@ class FadeCache:
         F.fade_rope_apply(c, self.table, self.max_pos, k_raw, self.k_rot, c.batch,
                           c.num_kv_heads, self.pos, 0)
         n = 2 if c.rope_kind != "none" else 0
-        ring_full = bool((L.h_n_recent == c.recent_window).any())
-        F.fade_cache_demote(L)
-        n += 1 if ring_full else 0
-        evicting = c.evicts and bool((L.h_n_mid > c.int4_budget).any())
-        t = self._tick("evict") if evicting else None
-        F.fade_evict_rerope(L, self.table, self.max_pos)
-        self._tock(t)
-        n += (2 if c.policy == "position" else 3) if evicting else 0
         F.fade_cache_append(L, self.k_rot, v)
         t = self._tick("attention")
         F.fade_decode_attention(L, self.q_rot, out, self.logits if self.needs_logits else None,
@@ -131,6 +137,14 @@ class FadeCache:
             n += 1
         self.launches += n
 
+    def step_layer(self, layer: int, q_raw: torch.Tensor, k_raw: torch.Tensor, v: torch.Tensor,
+                   out: torch.Tensor):
+        """One decode step of one layer in the method's order: demote, evict + re-position,
+        append, attention, accumulation. q_raw [B][Hq][d], k_raw/v [B][Hkv][d] fp16, pre-RoPE;
+        out [B][Hq][d] fp16."""
+        self.maintain_layer(layer)
+        self.attend_layer(layer, q_raw, k_raw, v, out)
+
     def mirror(self):
         """Host mirror of the tier counts of every layer (for steady-state checks)."""
         return [(L.h_n_sink.copy(), L.h_n_mid.copy(), L.h_n_recent.copy()) for L in self.layers]
@@ -141,8 +155,38 @@ class FadeCache:
         for layer in range(len(self.layers)):
             self.step_layer(layer, q[layer], k[layer], v[layer], out[layer])
 
-    def capture_step(self, q, k, v, out):
-        """Capture step_all on fixed input/output buffers as a CUDA graph.
+    def maintain_all(self):
+        """Every layer's maintenance for the coming step (the prologue of pipelined steps)."""
+        for layer in range(len(self.layers)):
+            self.maintain_layer(layer)
+
+    def step_all_pipelined(self, q, k, v, out, side: torch.cuda.Stream | None):
+        """One decode step of every layer whose maintenance was already done (by
+        ``maintain_all`` or the previous pipelined step): each layer attends on the current
+        stream, then its maintenance for the NEXT step is issued on ``side`` and overlaps the
+        following layers (``side`` None: issued inline, no overlap). Per layer the operations
+        run in the same order as ``step_all``; the step ends when ``side`` has finished."""
+        self.set_positions(self.next_positions())
+        main = torch.cuda.current_stream()
+        for layer in range(len(self.layers)):
+            self.attend_layer(layer, q[layer], k[layer], v[layer], out[layer])
+            if side is None:
+                self.maintain_layer(layer)
+                continue
+            ev = torch.cuda.Event()
+            ev.record(main)
+            side.wait_event(ev)
+            with torch.cuda.stream(side):
+                self.maintain_layer(layer)
+        if side is not None:
+            done = torch.cuda.Event()
+            done.record(side)
+            main.wait_event(done)
+
+    def capture_step(self, q, k, v, out, side: torch.cuda.Stream | None = None,
+                     pipelined: bool = False):
+        """Capture step_all (or step_all_pipelined, with ``pipelined`` or a side stream) on fixed
+        input/output buffers as a CUDA graph.
 
         Valid only in steady state, where a step leaves every tier count unchanged (the cache
         holds its budget; each step demotes one token, evicts one and appends one): the
@@ -151,7 +195,10 @@ class FadeCache:
         before = self.mirror()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.step_all(q, k, v, out)
+            if side is None and not pipelined:
+                self.step_all(q, k, v, out)
+            else:
+                self.step_all_pipelined(q, k, v, out, side)
         # the graph records into the timing events captured above: they must outlive it
         if self.timers:
             self._graph_events.append({n: list(p) for n, p in self.timers.items()})
