@@ -82,7 +82,9 @@ typedef struct {
   int32_t int4_budget;    /* middle tokens kept per unit when evicting; < 0: unbounded */
   int32_t middle_k_bits;  /* 4 (2 is accepted too) */
   int32_t middle_v_bits;  /* 2 or 4 */
-  int32_t mid_capacity;   /* middle slots allocated per unit (>= budget + 1 when evicting) */
+  int32_t mid_capacity;   /* middle slots allocated per unit (>= budget + 1 when evicting);
+                             batch x num_kv_heads x mid_stride must stay below 2^31
+                             (FADE_ERR_UNSUPPORTED otherwise) */
   int32_t policy;         /* fade_policy_t */
   float ema_decay;        /* EMA decay delta in [0, 1) */
   fade_rope_t rope;

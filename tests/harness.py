@@ -88,14 +88,23 @@ class Lockstep:
                           mass=None if mass is None else mass[b, h, :P].astype(np.float64))
 
     # -------------------------------------------------------------------- decode
-    def step(self, check_state=True):
-        """One decode step of every layer; returns the max attention error seen."""
+    def step(self, check_state=True, evict=True):
+        """One decode step of every layer; returns the max attention error seen. evict=False
+        leaves out the eviction call on both sides (the middle tier then grows past its budget
+        and a later step evicts every pending token at once)."""
         torch = self.torch
         wl, G = self.wl, self.wl.group
-        pos = self.fc.next_positions()
-        for b in range(wl.batch):
-            want = self.units[0][b][0].next_position()
-            assert pos[b] == want, f"row {b}: next position {pos[b]} != oracle {want}"
+        if evict:
+            pos = self.fc.next_positions()
+            for b in range(wl.batch):
+                want = self.units[0][b][0].next_position()
+                assert pos[b] == want, f"row {b}: next position {pos[b]} != oracle {want}"
+        else:  # no eviction: the new token's position is the number of tokens held
+            L0 = self.fc.layers[0]
+            pos = (L0.h_n_sink + L0.h_n_mid + L0.h_n_recent).astype(np.int32)
+            for b in range(wl.batch):
+                want = self.units[0][b][0].n_held
+                assert pos[b] == want, f"row {b}: held {pos[b]} != oracle {want}"
         self.fc.set_positions(pos)
         worst = 0.0
         for layer in range(self.L):
@@ -105,14 +114,19 @@ class Lockstep:
             k = torch.from_numpy(t["k"].copy()).to(dev)
             v = torch.from_numpy(t["v"].copy()).to(dev)
             out = torch.empty_like(q)
-            self.fc.step_layer(layer, q, k, v, out)
+            if evict:
+                self.fc.step_layer(layer, q, k, v, out)
+            else:
+                from tiered_mixed_precision_gb300 import fade as F
+                F.fade_cache_demote(self.fc.layers[layer])
+                self.fc.attend_layer(layer, q, k, v, out)
             victims_gpu = self._gpu_victims(layer)
             out_h = out.float().cpu().numpy()
             for b in range(wl.batch):
                 for h in range(wl.num_kv_heads):
                     key = (layer, b, h)
                     u = self.units[layer][b][h]
-                    o_ref, tie = self._oracle_step(u, t, b, h, victims_gpu, key)
+                    o_ref, tie = self._oracle_step(u, t, b, h, victims_gpu, key, evict)
                     if key in self.diverged:
                         continue
                     ok, err, nbad = allclose_report(out_h[b, h * G:(h + 1) * G], o_ref)
@@ -129,11 +143,11 @@ class Lockstep:
         its selection bitmap, or None for units without an eviction."""
         return self.fc.layers[layer].victims.cpu().numpy().view(np.uint32)
 
-    def _oracle_step(self, u, t, b, h, bm, key):
+    def _oracle_step(self, u, t, b, h, bm, key, evict=True):
         G = self.wl.group
         u.demote()
         n_mid = u.n_mid
-        vic = u.choose_victims()
+        vic = u.choose_victims() if evict else np.zeros(0, np.int64)
         tie = False
         if vic.size and self.wl.policy in ("h2o", "ema") and key not in self.diverged:
             words = bm[b, h, :(n_mid + 31) // 32]
@@ -149,7 +163,8 @@ class Lockstep:
                 self.diverged.add(key)
                 self.near_ties += 1
                 tie = True
-        u.evict(vic)
+        if evict:
+            u.evict(vic)
         pos = u.n_held
         u.append(u.rope.apply(t["k"][b, h][None], pos), t["v"][b, h])
         out, p, _ = u.attend(u.rope.apply(t["q"][b, h * G:(h + 1) * G], pos))

@@ -130,6 +130,27 @@ def test_lockstep_small_workloads(T, key):
     assert ls.near_ties <= max(1, wl.batch * wl.num_kv_heads * ls.L // 20)
 
 
+@pytest.mark.parametrize("policy,skip", [("position", 40), ("h2o", 40), ("position", 3)])
+def test_deferred_eviction_many_victims(T, policy, skip):
+    """Eviction left out for `skip` steps, then steps that evict every pending token at once:
+    with 40 pending victims a compaction block needs more RoPE rows than it stages in shared
+    memory, so its re-positioning reads the table from global memory."""
+    if policy == "position":
+        wl = get_workload(4).scaled(layers=1, batch=2, num_q_heads=4, num_kv_heads=2,
+                                    prompt_len=1000, int4_budget=300, steps=skip + 2)
+    else:
+        wl = get_workload(3).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                    prompt_len=900, int4_budget=500, steps=skip + 2)
+    ls = Lockstep(wl, mid_capacity=wl.int4_budget + skip + 8)
+    ls.prefill(0)
+    ls.check_layer_state(0)
+    for _ in range(skip):
+        ls.step(evict=False)
+    for _ in range(2):
+        ls.step()
+    assert ls.near_ties <= 1
+
+
 @pytest.mark.parametrize("key,P", [(3, 700), (3, 130)])
 def test_prefill_mass_matches_oracle(T, key, P):
     """GPU prefill attention mass vs the oracle's fp64 causal column sums."""

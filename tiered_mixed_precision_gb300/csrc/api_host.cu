@@ -54,6 +54,10 @@ fade_status_t validate_config(const fade_config_t* c) {
     return set_error(FADE_ERR_INVALID_ARGUMENT, "ema_decay must lie in [0, 1)");
   if (c->mid_capacity < 1)
     return set_error(FADE_ERR_INVALID_ARGUMENT, "mid_capacity %d < 1", c->mid_capacity);
+  if ((long long)c->batch * c->num_kv_heads * (((long long)c->mid_capacity + 63) / 64 * 64) >
+      0x7fffffffLL)
+    return set_error(FADE_ERR_UNSUPPORTED,
+                     "batch x num_kv_heads x mid_capacity exceeds 2^31 middle slots");
   const bool evicts = c->policy != FADE_EVICT_NONE && c->int4_budget >= 0;
   if (evicts && c->mid_capacity < c->int4_budget + 1)
     return set_error(FADE_ERR_CAPACITY,

@@ -385,26 +385,16 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Recent-ring re-positioning: geometry. D/32 threads per ring token; thread t_ owns the rotation
+// pairs 16 t_ .. 16 t_ + 15.
 template <int D>
-struct CompactCfg {
-  static constexpr int TPT = D / 32;        // threads per middle token
-  static constexpr int TOK = 256 / TPT;     // middle indices per CTA
+struct RecentCfg {
+  static constexpr int TPT = D / 32;        // threads per ring token
+  static constexpr int TOK = 256 / TPT;     // ring tokens per pass of the CTA
   static constexpr int ROWF4 = D / 4;       // float4 per RoPE row: d/2 pairs x (cos, sin)
-  static constexpr int NROWS = TOK + 32;    // staged RoPE rows (blocks with n_ev <= 32)
+  static constexpr int NROWS = TOK + 32;    // staged RoPE rows
   static constexpr int TPW = 32 / TPT;      // tokens per warp
   static constexpr int TABF4 = NROWS * (ROWF4 + 1);  // staged rows padded by one float4
-  static constexpr int PRE = TOK / 32 + 2;  // per-head ints: victim prefix words + base
-  // prefetch buffers: per thread its K code share (two buffers) and V code share (one); per
-  // token its K scale row (two buffers), V scale row and score (one)
-  static constexpr int KSH = 2 * 16 * 4 / 8;     // bytes of K codes per thread (INT4 worst case)
-  static constexpr int VSH = 16;                 // bytes of V codes per thread (INT4 worst case)
-  static constexpr int SRB = D / 32 * 2;         // bytes of one scale row
-  static constexpr int PF_BYTES = 2 * 256 * KSH + 256 * VSH + TOK * (3 * SRB + 4);
-  // staged rows, prefetch buffers, then per head: 4 counts and the victim prefixes
-  static size_t smem(int H) {
-    return (size_t)TABF4 * 16 + PF_BYTES +
-           (size_t)H * (PRE + 4) * 4;
-  }
 };
 
 // Float4 slot of (row, j) in the staged table: rows padded by one float4, so the eight
@@ -415,39 +405,129 @@ __device__ __forceinline__ int tab_slot(int row, int j) {
   return row * (D / 4 + 1) + j;
 }
 
+// Middle-tier compaction: geometry. D/64 threads per middle token; thread t_ of a token owns
+// the rotation pairs 32 t_ .. 32 t_ + 31, i.e. the whole quantisation groups t_ (channels
+// 32 t_ + j) and t_ + D/64 (their partners D/2 + 32 t_ + j), so a group's absmax, scale and
+// codes stay in one thread.
 template <int D>
-__host__ __device__ constexpr int compact_tok() { return CompactCfg<D>::TOK; }
+struct MidCfg {
+  static constexpr int TPT = D / 64;        // threads per middle token
+  static constexpr int TOK = 256 / TPT;     // middle indices per CTA
+  static constexpr int TPW = 32 / TPT;      // tokens per warp
+  static constexpr int ROWF4 = D / 4;       // float4 per RoPE row: d/2 pairs x (cos, sin)
+  static constexpr int NROWS = TOK + 16;    // staged RoPE rows (blocks with n_ev <= 16)
+  static constexpr int TABF4 = NROWS * (ROWF4 + 1);  // staged rows padded by one float4
+  static constexpr int PRE = TOK / 32 + 2;  // per-head ints: victim prefix words + base
+  static constexpr int SRB = D / 32 * 2;    // bytes of one scale row
+};
+// Per-thread prefetch slots after the staged rows (every thread reads only its own slots).
+template <int D, int KB, int VB>
+struct MidBuf {
+  static constexpr int GB = 32 * KB / 8;                  // bytes of one group's K codes
+  static constexpr int KSH = 2 * GB;                      // K codes of a thread (two groups)
+  static constexpr int SRB = MidCfg<D>::SRB;
+  static constexpr int VSH = D * VB / 8 / MidCfg<D>::TPT;  // V codes of a thread
+  static constexpr int K_OFF = 0;                         // [2][256][KSH]
+  static constexpr int KS_OFF = K_OFF + 2 * 256 * KSH;    // [2][256][SRB]: the whole K scale row
+  static constexpr int V_OFF = KS_OFF + 2 * 256 * SRB;    // [256][VSH]
+  static constexpr int VS_OFF = V_OFF + 256 * VSH;        // [256][4]: this thread's 4 bytes
+  static constexpr int SC_OFF = VS_OFF + 256 * 4;         // [256]: score (first thread of a token)
+  static constexpr int BYTES = SC_OFF + 256 * 4;
+  static size_t smem(int H) {
+    return (size_t)MidCfg<D>::TABF4 * 16 + BYTES + (size_t)H * (MidCfg<D>::PRE + 4) * 4;
+  }
+};
+
+// cp.async of N bytes issued only where `p` holds (no branch).
+template <int N>
+__device__ __forceinline__ void cp_async_if(bool p, void* smem_dst, const void* gmem_src) {
+  static_assert(N == 4 || N == 8 || N == 16, "cp.async copies 4, 8 or 16 bytes");
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  if constexpr (N == 16)
+    asm volatile(
+        "{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n"
+        " @q cp.async.cg.shared.global [%0], [%1], 16;\n}\n" ::"r"(d),
+        "l"(gmem_src), "r"((int)p)
+        : "memory");
+  else
+    asm volatile(
+        "{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n"
+        " @q cp.async.ca.shared.global [%0], [%1], %3;\n}\n" ::"r"(d),
+        "l"(gmem_src), "r"((int)p), "n"(N)
+        : "memory");
+}
+
+template <int D>
+__host__ __device__ constexpr int compact_tok() { return MidCfg<D>::TOK; }
+
+// One thread's two key groups of a moved middle token (codes kp: group g1 then g2, GB bytes
+// each; scales S1, S2 as packed pairs): dequantise (exact), un-RoPE with the old position's row
+// `to`, re-RoPE with the new one's `tn` (16 float4 each: pairs 2k, 2k+1 in float4 k), every
+// product and sum rounded on its own (packed products, scalar sums), cast to fp16 (H1, H2: half2
+// words, pair k in word k) and the fp32 absmax of each group (a1m, a2m).
+template <int KB>
+__device__ __forceinline__ void reposition_groups(const uint8_t* kp, f2x S1, f2x S2,
+                                                  const float4* to, const float4* tn,
+                                                  uint32_t (&H1)[16], uint32_t (&H2)[16],
+                                                  float& a1m, float& a2m) {
+  constexpr int GB = 32 * KB / 8;
+  uint32_t w1[GB / 4], w2[GB / 4];
+#pragma unroll
+  for (int w = 0; w < GB / 4; ++w) {
+    w1[w] = reinterpret_cast<const uint32_t*>(kp)[w];
+    w2[w] = reinterpret_cast<const uint32_t*>(kp + GB)[w];
+  }
+  uint32_t ev1[2], od1[2], ev2[2], od2[2];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    f2x X1, X2;
+    if constexpr (KB == 4) {
+      if (k % 8 == 0) {  // words 2(k/8), 2(k/8)+1 hold channels 16(k/8) .. +15
+        const uint32_t p1[2] = {w1[2 * (k / 8)], w1[2 * (k / 8) + 1]};
+        const uint32_t p2[2] = {w2[2 * (k / 8)], w2[2 * (k / 8) + 1]};
+        split_int4(p1, ev1, od1);
+        split_int4(p2, ev2, od2);
+      }
+      X1 = dequant_pair_int4(ev1, od1, k % 8, S1);
+      X2 = dequant_pair_int4(ev2, od2, k % 8, S2);
+    } else {
+      X1 = dequant_pair_bits<KB>(w1, k, S1);
+      X2 = dequant_pair_bits<KB>(w2, k, S2);
+    }
+    const float4 co = to[k], cn = tn[k];
+    rotate2_inv(X1, X2, f2_pack(co.x, co.y), f2_pack(co.z, co.w));
+    rotate2(X1, X2, f2_pack(cn.x, cn.y), f2_pack(cn.z, cn.w));
+    float p10, p11, p20, p21;
+    f2_unpack(X1, p10, p11);
+    f2_unpack(X2, p20, p21);
+    a1m = fmaxf(a1m, fmaxf(fabsf(p10), fabsf(p11)));
+    a2m = fmaxf(a2m, fmaxf(fabsf(p20), fabsf(p21)));
+    const __half2 r1 = __floats2half2_rn(p10, p11), r2 = __floats2half2_rn(p20, p21);
+    H1[k] = *reinterpret_cast<const uint32_t*>(&r1);
+    H2[k] = *reinterpret_cast<const uint32_t*>(&r2);
+  }
+}
 
 // Compact survivors of the live middle buffer into the other one, re-positioning keys whose
 // index drops (the recent rings follow in evict_recent_commit_kernel).
 // grid = (ceil(max_mid / TOK), B), 256 threads; one CTA takes one block of TOK middle indices
-// of one batch row and loops over the row's KV heads. Middle tokens: D/32 threads per token;
-// thread (gp, hf) owns rotation pairs 32gp + 16hf .. +15, i.e. half of group gp (channels
-// 32gp + 16hf + j) and the matching half of its partner group gp + D/64 (channels
-// D/2 + 32gp + 16hf + j). A moved key is dequantised, un-RoPE'd / re-RoPE'd and re-quantised;
-// each group's absmax is completed with the neighbouring thread (lane ^ 1). The RoPE rows the
-// block needs (its old positions and the new ones, at most 64 below) are staged once per CTA in
-// shared memory and serve every head.
-// Resident CTAs per SM asked of the register allocator for the compaction kernel.
-#ifndef FADE_COMPACT_MIN_CTAS
-#define FADE_COMPACT_MIN_CTAS 3
-#endif
-
+// of one batch row and loops over the row's KV heads. A moved key is dequantised, un-RoPE'd at
+// its old position and re-RoPE'd at its new one, rounded to fp16 and re-quantised, all in the
+// owning thread (see MidCfg). The RoPE rows the block needs (its old positions and the new ones,
+// at most 16 below) are staged once per CTA in shared memory and serve every head; each head's
+// codes, scales and scores are fetched ahead with cp.async (K one processed head ahead, V during
+// the head itself) into slots private to the thread.
 template <int D, int KB, int VB>
-__global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kernel(LayerArgs a) {
-  using CC = CompactCfg<D>;
-  constexpr int TPT = CC::TPT, TOK = CC::TOK;
-  constexpr int HB = 16 * KB / 8;        // bytes of half a group's K codes
+__global__ void __launch_bounds__(256, 2) evict_compact_kernel(LayerArgs a) {
+  using CC = MidCfg<D>;
+  using MB = MidBuf<D, KB, VB>;
+  constexpr int TOK = CC::TOK, TPW = CC::TPW, SRB = CC::SRB;
+  constexpr int GB = MB::GB, KSH = MB::KSH, VSH = MB::VSH;
   constexpr int VROW = D * VB / 8, SROW = D / kGroup, KROW = D * KB / 8;
-  extern __shared__ float4 tab[];        // [NROWS][ROWF4] swizzled, then the buffers below
+  extern __shared__ float4 tab[];        // [NROWS][ROWF4 + 1], then the slots of MidBuf
   uint8_t* pf = reinterpret_cast<uint8_t*>(tab + CC::TABF4);
-  uint8_t* kbuf = pf;                                   // [2][256][KSH]
-  uint8_t* vbuf = kbuf + 2 * 256 * CC::KSH;             // [256][VSH]
-  uint8_t* ksbuf = vbuf + 256 * CC::VSH;                // [2][TOK][SRB]
-  uint8_t* vsbuf = ksbuf + 2 * TOK * CC::SRB;           // [TOK][SRB]
-  float* scbuf = reinterpret_cast<float*>(vsbuf + TOK * CC::SRB);  // [TOK]
-  int* hinfo = reinterpret_cast<int*>(pf + CC::PF_BYTES);  // [H][4]: n_mid n_ev n_sink cur
-  int* hpre = hinfo + a.H * 4;                       // [H][PRE]
+  int* hinfo = reinterpret_cast<int*>(pf + MB::BYTES);  // [H][4]: n_mid n_ev n_sink cur
+  int* hpre = hinfo + a.H * 4;                          // [H][PRE]
   __shared__ int s_rlo, s_rhi;
   const int b = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -513,40 +593,45 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kern
   }
   __syncthreads();
 
-  // lanes: token-minor (eight or sixteen consecutive tokens per t_), so a quarter warp reads
-  // one j of consecutive RoPE rows; the partner half-group thread is lane ^ TPW
+  // lanes: token-minor (TPW consecutive tokens per t_), so a quarter warp reads one float4 of
+  // eight consecutive RoPE rows (the padding puts them in eight different bank quads)
   const int tid = threadIdx.x;
-  const int it = warp * CC::TPW + lane % CC::TPW, t_ = lane / CC::TPW;
-  const int gp = t_ >> 1, hf = t_ & 1;
+  const int it = warp * TPW + lane % TPW, t_ = lane / TPW;
   const int i = lo + it;
-  const int g1 = gp, g2 = gp + D / 64;
-  constexpr int VSH = VROW / TPT;  // this thread's bytes of a V code row
-  // K codes and scales of a head's token for this thread, and its V share, score and V scales,
-  // fetched ahead with cp.async (K one processed head ahead, V during the head itself)
-  auto has_work = [&](int hh) { return hinfo[4 * hh + 1] != 0 && lo < hinfo[4 * hh + 0]; };
-  // a unit's row `slot` in its live (src) or other (dst) buffer; the buffer is a select between
-  // two kernel parameters, so no per-thread register holds the row pointers between uses
-  auto slot0 = [&](int hh) { return (size_t)(b * a.H + hh) * a.C; };
-  auto live = [&](int hh) { return hinfo[4 * hh + 3] != 0; };
+  const int g1 = t_, g2 = t_ + D / 64;
+  const int4* hinfo4 = reinterpret_cast<const int4*>(hinfo);
+  uint8_t* kslot = pf + MB::K_OFF + tid * KSH;    // + buffer * 256 * KSH
+  uint8_t* ksslot = pf + MB::KS_OFF + tid * SRB;  // + buffer * 256 * SRB
+  uint8_t* vslot = pf + MB::V_OFF + tid * VSH;
+  uint8_t* vsslot = pf + MB::VS_OFF + tid * 4;
+  float* scslot = reinterpret_cast<float*>(pf + MB::SC_OFF) + tid;
+  const uint32_t row0 = (uint32_t)(b * a.H) * (uint32_t)a.C;  // slot 0 of the row's first unit
+  // a head's K codes and scale row for this thread (into K buffer `buf`)
   auto prefetch_k = [&](int hh, int buf) {
-    if (i >= min(lo + TOK, hinfo[4 * hh + 0])) return;
-    const size_t r = slot0(hh) + i;
-    const uint8_t* kr = (live(hh) ? a.mk[1] : a.mk[0]) + r * KROW + hf * HB;
-    uint8_t* kd = kbuf + (buf * 256 + tid) * CC::KSH;
-    cp_async<HB>(kd, kr + g1 * 2 * HB);
-    cp_async<HB>(kd + HB, kr + g2 * 2 * HB);
-    if (t_ == 0)
-      cp_async<SROW * 2>(ksbuf + (buf * TOK + it) * CC::SRB, (live(hh) ? a.mks[1] : a.mks[0]) + r * SROW);
+    const int4 m = hinfo4[hh];
+    const bool p = i < m.x;
+    const uint32_t r = row0 + (uint32_t)hh * (uint32_t)a.C + (uint32_t)i;
+    const uint8_t* kr = (m.w ? a.mk[1] : a.mk[0]) + (size_t)r * KROW;
+    uint8_t* kd = kslot + buf * 256 * KSH;
+    cp_async_if<GB>(p, kd, kr + g1 * GB);
+    cp_async_if<GB>(p, kd + GB, kr + g2 * GB);
+    cp_async_if<SRB>(p, ksslot + buf * 256 * SRB, (m.w ? a.mks[1] : a.mks[0]) + (size_t)r * SROW);
   };
+  // a head's V codes (this thread's share), V scales (its 4 bytes) and score
   auto prefetch_v = [&](int hh) {
-    if (i >= min(lo + TOK, hinfo[4 * hh + 0])) return;
-    const size_t r = slot0(hh) + i;
-    const bool c = live(hh);
-    cp_async<VSH>(vbuf + tid * CC::VSH, (c ? a.mv[1] : a.mv[0]) + r * VROW + t_ * VSH);
-    if (t_ == 0) {
-      cp_async<SROW * 2>(vsbuf + it * CC::SRB, (c ? a.mvs[1] : a.mvs[0]) + r * SROW);
-      cp_async<4>(scbuf + it, (c ? a.mid_sc[1] : a.mid_sc[0]) + r);
-    }
+    const int4 m = hinfo4[hh];
+    const bool p = i < m.x;
+    const uint32_t r = row0 + (uint32_t)hh * (uint32_t)a.C + (uint32_t)i;
+    const bool c = m.w != 0;
+    const uint8_t* vr = (c ? a.mv[1] : a.mv[0]) + (size_t)r * VROW + t_ * VSH;
+#pragma unroll
+    for (int q = 0; q < VSH / 16; ++q) cp_async_if<16>(p, vslot + 16 * q, vr + 16 * q);
+    cp_async_if<4>(p, vsslot, (c ? a.mvs[1] : a.mvs[0]) + (size_t)r * SROW + 2 * t_);
+    cp_async_if<4>(p && t_ == 0, scslot, (c ? a.mid_sc[1] : a.mid_sc[0]) + r);
+  };
+  auto has_work = [&](int hh) {
+    const int4 m = hinfo4[hh];
+    return m.y != 0 && lo < m.x;
   };
   int kb = 0;  // K buffer of the head being processed
   {
@@ -556,13 +641,12 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kern
     cp_async_commit();
   }
   for (int h = 0; h < a.H; ++h) {
-    const int n_mid = hinfo[4 * h + 0], n_ev = hinfo[4 * h + 1];
+    const int4 m = hinfo4[h];
+    const int n_mid = m.x, n_ev = m.y, n_sink = m.z;
+    const bool cur = m.w != 0;
     if (n_ev == 0 || lo >= n_mid) continue;  // uniform per CTA
-    const int n_sink = hinfo[4 * h + 2];
-    const int unit = b * a.H + h;
-    const int hi = min(lo + TOK, n_mid);
     cp_async_wait<0>();  // this head's K data has landed
-    __syncwarp();        // ... for every lane of the token; earlier reads of the buffers are done
+    __syncwarp();
     prefetch_v(h);
     cp_async_commit();
     {
@@ -572,8 +656,8 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kern
       cp_async_commit();
     }
     // The TPT lanes of one token lie in one warp and share every flag below, so the warp-wide
-    // ballot and the absmax exchange see whole tokens; nothing exits before them.
-    const bool in_range = i < hi;
+    // ballot and the scale exchange see whole tokens; nothing exits before them.
+    const bool in_range = i < n_mid;
     bool keep = in_range;
     int nv = 0;
     if (in_range) {
@@ -581,7 +665,7 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kern
         keep = i >= n_ev;
         nv = i - n_ev;
       } else {
-        const uint32_t* bm = a.victims + (size_t)unit * a.victim_words;
+        const uint32_t* bm = a.victims + (size_t)(b * a.H + h) * a.victim_words;
         const uint32_t word = bm[i >> 5];
         keep = !((word >> (i & 31)) & 1u);
         nv = i - (hpre[h * CC::PRE + TOK / 32 + 1] + hpre[h * CC::PRE + ((i - lo) >> 5)] +
@@ -589,126 +673,86 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kern
       }
     }
     const bool moved = keep && nv != i && a.table != nullptr;
-
-    const bool cur = live(h);
-    const int di = nv;                             // destination slot within the unit
-    const size_t dr = slot0(h) + di;               // destination row
-    uint16_t* mks_d = (cur ? a.mks[0] : a.mks[1]) + slot0(h) * SROW;
-    uint8_t* krow_d = (cur ? a.mk[0] : a.mk[1]) + dr * KROW;
-    const uint8_t* kpf = kbuf + (kb * 256 + tid) * CC::KSH;
-    const uint16_t* kspf = reinterpret_cast<const uint16_t*>(ksbuf + (kb * TOK + it) * CC::SRB);
+    const uint32_t dr = row0 + (uint32_t)h * (uint32_t)a.C + (uint32_t)nv;  // destination row
+    uint8_t* krow_d = (cur ? a.mk[0] : a.mk[1]) + (size_t)dr * KROW;
+    uint16_t* ks_d = (cur ? a.mks[0] : a.mks[1]) + (size_t)dr * SROW + 2 * t_;  // 4 bytes
+    const uint8_t* kp = kslot + kb * 256 * KSH;
+    const uint8_t* ksp = ksslot + kb * 256 * SRB;
     kb ^= 1;
 
     if (keep && !moved) {  // survivor at its own index (or no RoPE): K codes and scales as they are
-      copy_row<HB>(kpf, krow_d + g1 * 2 * HB + hf * HB);
-      copy_row<HB>(kpf + HB, krow_d + g2 * 2 * HB + hf * HB);
-      if (t_ == 0) copy_row<SROW * 2>(kspf, mks_d + di * SROW);
+      copy_row<GB>(kp, krow_d + g1 * GB);
+      copy_row<GB>(kp + GB, krow_d + g2 * GB);
+      *reinterpret_cast<uint32_t*>(ks_d) = reinterpret_cast<const uint32_t*>(ksp)[t_];
     }
     if (__ballot_sync(0xffffffffu, moved) != 0u) {  // warp-uniform
-    uint32_t H1[8], H2[8];  // the re-positioned key half groups, rounded to fp16 (half2 pairs)
-    float a1m = 0.f, a2m = 0.f;
-    if (moved) {
-      const f2x S1 = f2_pack(h2f(kspf[g1]), h2f(kspf[g1])), S2 = f2_pack(h2f(kspf[g2]), h2f(kspf[g2]));
-      uint32_t w1[HB / 4], w2[HB / 4];
-#pragma unroll
-      for (int w = 0; w < HB / 4; ++w) {
-        w1[w] = reinterpret_cast<const uint32_t*>(kpf)[w];
-        w2[w] = reinterpret_cast<const uint32_t*>(kpf + HB)[w];
+      uint32_t H1[16], H2[16];  // the re-positioned groups g1, g2, rounded to fp16 (half2 pairs)
+      float a1m = 0.f, a2m = 0.f;
+      if (moved) {
+        const uint16_t* ksrow = reinterpret_cast<const uint16_t*>(ksp);
+        const float sc1 = h2f(ksrow[g1]), sc2 = h2f(ksrow[g2]);
+        const f2x S1 = f2_pack(sc1, sc1), S2 = f2_pack(sc2, sc2);
+        // this thread's 16 float4 (pairs 32 t_ .. 32 t_ + 31) of the old and the new position's
+        // RoPE row: the staged rows when the block's range fit (shared-memory loads), else the
+        // table in global memory
+        if (staged)
+          reposition_groups<KB>(kp, S1, S2, tab + tab_slot<D>(n_sink + i - rlo, 16 * t_),
+                                tab + tab_slot<D>(n_sink + nv - rlo, 16 * t_), H1, H2, a1m, a2m);
+        else
+          reposition_groups<KB>(
+              kp, S1, S2,
+              reinterpret_cast<const float4*>(a.table) + (size_t)(n_sink + i) * CC::ROWF4 + 16 * t_,
+              reinterpret_cast<const float4*>(a.table) + (size_t)(n_sink + nv) * CC::ROWF4 + 16 * t_,
+              H1, H2, a1m, a2m);
       }
-      uint32_t ev1[2], od1[2], ev2[2], od2[2];
-      if constexpr (KB == 4) {
-        split_int4(w1, ev1, od1);
-        split_int4(w2, ev2, od2);
+      // group absmax of the fp16 values = fp16 rounding of the fp32 absmax (round-to-nearest is
+      // monotone and odd); scale = fp16(absmax / qmax)
+      a1m = __half2float(__float2half_rn(a1m));
+      a2m = __half2float(__float2half_rn(a2m));
+      constexpr int qmax = (1 << (KB - 1)) - 1;
+      float s1 = __half2float(__float2half_rn(div_by_qmax<qmax>(a1m)));
+      float s2 = __half2float(__float2half_rn(div_by_qmax<qmax>(a2m)));
+      if (a1m > 0.f && s1 == 0.f) s1 = kSubnormalMin;
+      if (a2m > 0.f && s2 == 0.f) s2 = kSubnormalMin;
+      // the scale row [g0, g1, ...]: thread t_ stores its 4 bytes (groups 2 t_, 2 t_ + 1); with
+      // two threads per token those come from (g1, g2) of both threads
+      const uint32_t my = __half_as_ushort(__float2half_rn(s1)) |
+                          ((uint32_t)__half_as_ushort(__float2half_rn(s2)) << 16);
+      uint32_t srow = my;
+      if constexpr (CC::TPT == 2) {
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, my, TPW);
+        srow = t_ == 0 ? prmt(my, other, 0x5410u) : prmt(other, my, 0x7632u);
       }
-      // this thread's 8 float4 (pairs 16 t_ .. 16 t_ + 15) of the old and the new position's
-      // RoPE row: staged rows when the block's range fit, else the table in global memory
-      const int bo = staged ? tab_slot<D>(n_sink + i - rlo, 8 * t_) : 0;
-      const int bn = staged ? tab_slot<D>(n_sink + nv - rlo, 8 * t_) : 0;
-      const float4* to = reinterpret_cast<const float4*>(a.table) +
-                         (size_t)(n_sink + i) * (a.half / 2) + 8 * t_;
-      const float4* tn = reinterpret_cast<const float4*>(a.table) +
-                         (size_t)(n_sink + nv) * (a.half / 2) + 8 * t_;
-      // per pair block: dequantise (exact), un-RoPE at the old index, re-RoPE at the new one
-      // (every product and sum rounded on its own: packed products, scalar sums), cast to fp16
-#define FADE_ROT_K(K)                                                                        \
-  {                                                                                          \
-    f2x X1, X2;                                                                              \
-    if constexpr (KB == 4) {                                                                 \
-      X1 = dequant_pair_int4<K>(ev1, od1, S1);                                               \
-      X2 = dequant_pair_int4<K>(ev2, od2, S2);                                               \
-    } else {                                                                                 \
-      X1 = dequant_pair_bits<KB, K>(w1, S1);                                                 \
-      X2 = dequant_pair_bits<KB, K>(w2, S2);                                                 \
-    }                                                                                        \
-    float4 co, cn;                                                                           \
-    if (kStaged) {                                                                           \
-      co = tab[bo + K];                                                                      \
-      cn = tab[bn + K];                                                                      \
-    } else {                                                                                 \
-      co = __ldg(to + K);                                                                    \
-      cn = __ldg(tn + K);                                                                    \
-    }                                                                                        \
-    rotate2(X1, X2, f2_pack(co.x, co.y), f2_pack(-co.z, -co.w));                              \
-    rotate2(X1, X2, f2_pack(cn.x, cn.y), f2_pack(cn.z, cn.w));                                \
-    float p10, p11, p20, p21;                                                                \
-    f2_unpack(X1, p10, p11);                                                                 \
-    f2_unpack(X2, p20, p21);                                                                 \
-    a1m = fmaxf(a1m, fmaxf(fabsf(p10), fabsf(p11)));                                         \
-    a2m = fmaxf(a2m, fmaxf(fabsf(p20), fabsf(p21)));                                         \
-    const __half2 r1 = __floats2half2_rn(p10, p11), r2 = __floats2half2_rn(p20, p21);        \
-    H1[K] = *reinterpret_cast<const uint32_t*>(&r1);                                         \
-    H2[K] = *reinterpret_cast<const uint32_t*>(&r2);                                         \
-  }
-      const bool kStaged = staged;
-      FADE_ROT_K(0) FADE_ROT_K(1) FADE_ROT_K(2) FADE_ROT_K(3)
-      FADE_ROT_K(4) FADE_ROT_K(5) FADE_ROT_K(6) FADE_ROT_K(7)
-#undef FADE_ROT_K
-    }
-    // absmax of each group over the token's two half-threads (adjacent lanes)
-    // group absmax over the token's two half-threads; the absmax of the fp16 values is the fp16
-    // rounding of the fp32 absmax (round-to-nearest is monotone and odd)
-    a1m = __half2float(__float2half_rn(fmaxf(a1m, __shfl_xor_sync(0xffffffffu, a1m, CC::TPW))));
-    a2m = __half2float(__float2half_rn(fmaxf(a2m, __shfl_xor_sync(0xffffffffu, a2m, CC::TPW))));
-    constexpr int qmax = (1 << (KB - 1)) - 1;
-    // scales: fp16(absmax / qmax)
-    float s1 = __half2float(__float2half_rn(div_by_qmax<qmax>(a1m)));
-    float s2 = __half2float(__float2half_rn(div_by_qmax<qmax>(a2m)));
-    if (a1m > 0.f && s1 == 0.f) s1 = kSubnormalMin;
-    if (a2m > 0.f && s2 == 0.f) s2 = kSubnormalMin;
-    // the token's scale row goes out in one store by t_ = 0: its own groups gp and gp + d/64,
-    // and (d = 128) groups 1 and 3 from the thread with t_ = 2
-    const uint32_t my = __half_as_ushort(__float2half_rn(s1)) |
-                        ((uint32_t)__half_as_ushort(__float2half_rn(s2)) << 16);
-    const uint32_t other = __shfl_down_sync(0xffffffffu, my, 2 * CC::TPW);
-    if (moved) {
-    uint32_t o1[HB / 4], o2[HB / 4];
+      if (moved) {
+        constexpr int HW = GB / 8;  // words of codes per half group
+        uint32_t o1[GB / 4], o2[GB / 4];
 #pragma unroll
-    for (int w = 0; w < HB / 4; ++w) o1[w] = o2[w] = 0u;
-    if (s1 > 0.f) codes_half_group<KB>(H1, s1, o1);
-    if (s2 > 0.f) codes_half_group<KB>(H2, s2, o2);
-#pragma unroll
-    for (int w = 0; w < HB / 4; ++w) {
-      reinterpret_cast<uint32_t*>(krow_d + g1 * 2 * HB + hf * HB)[w] = o1[w];
-      reinterpret_cast<uint32_t*>(krow_d + g2 * 2 * HB + hf * HB)[w] = o2[w];
+        for (int w = 0; w < GB / 4; ++w) o1[w] = o2[w] = 0u;
+        if (s1 > 0.f) {
+          codes_half_group<KB>(*reinterpret_cast<const uint32_t(*)[8]>(&H1[0]), s1, o1);
+          codes_half_group<KB>(*reinterpret_cast<const uint32_t(*)[8]>(&H1[8]), s1, o1 + HW);
+        }
+        if (s2 > 0.f) {
+          codes_half_group<KB>(*reinterpret_cast<const uint32_t(*)[8]>(&H2[0]), s2, o2);
+          codes_half_group<KB>(*reinterpret_cast<const uint32_t(*)[8]>(&H2[8]), s2, o2 + HW);
+        }
+        if constexpr (GB == 16) {
+          *reinterpret_cast<uint4*>(krow_d + g1 * GB) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+          *reinterpret_cast<uint4*>(krow_d + g2 * GB) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+        } else {
+          *reinterpret_cast<uint2*>(krow_d + g1 * GB) = make_uint2(o1[0], o1[1]);
+          *reinterpret_cast<uint2*>(krow_d + g2 * GB) = make_uint2(o2[0], o2[1]);
+        }
+        *reinterpret_cast<uint32_t*>(ks_d) = srow;
+      }
     }
-    if (t_ == 0) {
-      if constexpr (SROW == 4)
-        *reinterpret_cast<uint2*>(mks_d + di * SROW) =
-            make_uint2((my & 0xFFFFu) | (other << 16), (my >> 16) | (other & 0xFFFF0000u));
-      else
-        *reinterpret_cast<uint32_t*>(mks_d + di * SROW) = my;
-    }
-    }  // moved
-    }  // some lane of the warp moved
     // V codes (this thread's share of the row), the V scales and the score of every survivor
     cp_async_wait<1>();  // this head's V data (the newer group is the next head's K data)
-    __syncwarp();
     if (keep) {
-      copy_row<VSH>(vbuf + tid * CC::VSH, (cur ? a.mv[0] : a.mv[1]) + dr * VROW + t_ * VSH);
-      if (t_ == 0) {
-        copy_row<SROW * 2>(vsbuf + it * CC::SRB, (cur ? a.mvs[0] : a.mvs[1]) + dr * SROW);
-        (cur ? a.mid_sc[0] : a.mid_sc[1])[dr] = scbuf[it];
-      }
+      copy_row<VSH>(vslot, (cur ? a.mv[0] : a.mv[1]) + (size_t)dr * VROW + t_ * VSH);
+      *reinterpret_cast<uint32_t*>((cur ? a.mvs[0] : a.mvs[1]) + (size_t)dr * SROW + 2 * t_) =
+          *reinterpret_cast<const uint32_t*>(vsslot);
+      if (t_ == 0) (cur ? a.mid_sc[0] : a.mid_sc[1])[dr] = *scslot;
     }
   }
   cp_async_wait<0>();  // nothing in flight when the CTA exits
@@ -720,7 +764,7 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MIN_CTAS) evict_compact_kern
 // pairs as in the middle tier; the RoPE rows of the ring's old and new positions are staged.
 template <int D>
 __global__ void __launch_bounds__(256) evict_recent_commit_kernel(LayerArgs a) {
-  using CC = CompactCfg<D>;
+  using CC = RecentCfg<D>;
   constexpr int TPT = CC::TPT, TOK = CC::TOK;
   extern __shared__ float4 tab[];
   int* hinfo = reinterpret_cast<int*>(tab + CC::TABF4);  // [H][4]
@@ -797,7 +841,7 @@ __global__ void __launch_bounds__(256) evict_recent_commit_kernel(LayerArgs a) {
             co = __ldg(to + 4 * q + k);
             cn = __ldg(tn + 4 * q + k);
           }
-          rotate2(X1[k], X2[k], f2_pack(co.x, co.y), f2_pack(-co.z, -co.w));
+          rotate2_inv(X1[k], X2[k], f2_pack(co.x, co.y), f2_pack(co.z, co.w));
           rotate2(X1[k], X2[k], f2_pack(cn.x, cn.y), f2_pack(cn.z, cn.w));
         }
         store_f16x8(X1, p1);
@@ -953,7 +997,7 @@ template <int D, int KB, int VB>
 struct CompactLaunch {
   static fade_status_t run(const LayerArgs& a, int B, int chunks, cudaStream_t st) {
     // chunks of compact_tok<D>() middle indices per batch row
-    const size_t smem = CompactCfg<D>::smem(a.H);
+    const size_t smem = MidBuf<D, KB, VB>::smem(a.H);
     auto kern = evict_compact_kernel<D, KB, VB>;
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -966,7 +1010,7 @@ struct CompactLaunch {
 
 template <int D>
 fade_status_t launch_recent_commit(const LayerArgs& a, int B, cudaStream_t st) {
-  using CC = CompactCfg<D>;
+  using CC = RecentCfg<D>;
   const size_t smem = (size_t)CC::TABF4 * 16 + (size_t)a.H * 4 * 4;
   auto kern = evict_recent_commit_kernel<D>;
   if (smem > 48 * 1024 &&

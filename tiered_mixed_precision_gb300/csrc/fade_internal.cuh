@@ -255,7 +255,7 @@ __device__ __forceinline__ float rint_div_exact(float x, float s) {
     q += copysignf(1.f, e);
   } else if (ae == h) {
     const float q2 = q + copysignf(1.f, e);
-    if (fmodf(q, 2.f) != 0.f) q = q2;  // exact tie: keep the even neighbour
+    if ((int)q & 1) q = q2;  // exact tie: keep the even neighbour (q is a small integer)
   }
   return q;
 }
@@ -298,6 +298,19 @@ __device__ __forceinline__ void rotate2(f2x& X1, f2x& X2, f2x C, f2x S) {
   X2 = f2_pack(__fadd_rn(c0, d0), __fadd_rn(c1, d1));
 }
 
+// The inverse rotation of rotate2 with the same (c, s): (x1*c + x2*s, x2*c - x1*s). Equal bit
+// for bit to rotate2 with the sines negated (a product with -s is the negated product, and
+// subtracting a negated value is adding it), without the negations.
+__device__ __forceinline__ void rotate2_inv(f2x& X1, f2x& X2, f2x C, f2x S) {
+  float a0, a1, b0, b1, c0, c1, d0, d1;
+  f2_unpack(f2_mul(X1, C), a0, a1);
+  f2_unpack(f2_mul(X2, S), b0, b1);
+  f2_unpack(f2_mul(X2, C), c0, c1);
+  f2_unpack(f2_mul(X1, S), d0, d1);
+  X1 = f2_pack(__fadd_rn(a0, b0), __fadd_rn(a1, b1));
+  X2 = f2_pack(__fsub_rn(c0, d0), __fsub_rn(c1, d1));
+}
+
 // Correctly rounded fp32 a / QMAX for fp16-valued a >= 0 (QMAX = 7 or 1), the scale division
 // of the quantiser. For QMAX = 7: Markstein's correction step (q0 = a * RN(1/7), e = a - q0 * 7
 // exact by FMA, q1 = RN(q0 + e * RN(1/7))); an exhaustive check over every non-negative finite
@@ -334,26 +347,52 @@ __device__ __forceinline__ void split_int4(const uint32_t (&w)[2], uint32_t (&ev
     od[h] = ((w[h] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
   }
 }
-template <int K>  // pair K = channels 2K, 2K+1 of the half group
+// Pair k (channels 2k, 2k+1 of the half group; k a constant once the caller's loop is unrolled).
 __device__ __forceinline__ f2x dequant_pair_int4(const uint32_t (&ev)[2], const uint32_t (&od)[2],
-                                                 f2x S) {
+                                                 int k, f2x S) {
   const uint32_t magic = 0x4B000000u;
-  const float lo = __uint_as_float(prmt(ev[K / 4], magic, 0x7650u + (K % 4)));
-  const float hi = __uint_as_float(prmt(od[K / 4], magic, 0x7650u + (K % 4)));
+  const float lo = __uint_as_float(prmt(ev[k >> 2], magic, 0x7650u + (k & 3)));
+  const float hi = __uint_as_float(prmt(od[k >> 2], magic, 0x7650u + (k & 3)));
   return f2_mul(f2_sub(f2_pack(lo, hi), f2_pack(8388616.f, 8388616.f)), S);
 }
-// Same for BITS-bit codes in general (here used for INT2: one word per half group).
-template <int BITS, int K>
-__device__ __forceinline__ f2x dequant_pair_bits(const uint32_t* w, f2x S) {
+// Same for BITS-bit codes in general (here used for INT2), pair k of the little-endian words w.
+template <int BITS>
+__device__ __forceinline__ f2x dequant_pair_bits(const uint32_t* w, int k, f2x S) {
   constexpr int per = 32 / BITS;
   constexpr uint32_t msk = (1u << BITS) - 1u, flip = 1u << (BITS - 1);
-  constexpr int j0 = 2 * K, j1 = 2 * K + 1;
+  const int j0 = 2 * k, j1 = 2 * k + 1;
   const uint32_t c0 = ((w[j0 / per] >> (BITS * (j0 % per))) & msk) ^ flip;
   const uint32_t c1 = ((w[j1 / per] >> (BITS * (j1 % per))) & msk) ^ flip;
   const float off = 8388608.f + (float)flip;   // 2^23 + 2^(bits-1)
   return f2_mul(f2_sub(f2_pack(__uint_as_float(0x4B000000u | c0), __uint_as_float(0x4B000000u | c1)),
                        f2_pack(off, off)),
                 S);
+}
+
+// The exact scalar path of codes_half_group (rare: exact ties, a candidate off by one, subnormal
+// scales), kept out of line so that the callers' unrolled code stays small; the 16 values come
+// in registers (two uint4 of half2 words) and the packed codes go back in registers.
+template <int BITS>
+__device__ __noinline__ uint2 codes_half_group_exact(uint4 lo, uint4 hi, float s) {
+  constexpr int per = 32 / BITS;
+  constexpr uint32_t mask = (1u << BITS) - 1u;
+  constexpr int qmax = (1 << (BITS - 1)) - 1;
+  const uint32_t H[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  uint32_t out[2] = {0u, 0u};
+#pragma unroll
+  for (int w = 0; w < 16 / per; ++w) {
+    uint32_t o = 0u;
+#pragma unroll
+    for (int e = 0; e < per; ++e) {
+      const int j = w * per + e;
+      const __half2 hp = *reinterpret_cast<const __half2*>(&H[j >> 1]);
+      const float x = (j & 1) ? __high2float(hp) : __low2float(hp);
+      const float q = fminf(fmaxf(rint_div_exact(x, s), (float)-qmax), (float)qmax);
+      o |= (uint32_t((int)q) & mask) << (BITS * e);
+    }
+    out[w] = o;
+  }
+  return make_uint2(out[0], out[1]);
 }
 
 // Codes of 16 fp16 values (8 half2 words) of one group whose scale s (> 0) is already
@@ -407,23 +446,10 @@ __device__ __forceinline__ void codes_half_group(const uint32_t (&H)[8], float s
     }
     return;
   }
-  float v[16];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&H[k]));
-    v[2 * k] = f.x;
-    v[2 * k + 1] = f.y;
-  }
-#pragma unroll
-  for (int w = 0; w < 16 / per; ++w) {
-    uint32_t o = 0u;
-#pragma unroll
-    for (int e = 0; e < per; ++e) {
-      const float q = fminf(fmaxf(rint_div_exact(v[w * per + e], s), (float)-qmax), (float)qmax);
-      o |= (uint32_t((int)q) & mask) << (BITS * e);
-    }
-    out[w] = o;
-  }
+  const uint2 ex = codes_half_group_exact<BITS>(make_uint4(H[0], H[1], H[2], H[3]),
+                                                make_uint4(H[4], H[5], H[6], H[7]), s);
+  out[0] = ex.x;
+  if constexpr (BITS == 4) out[1] = ex.y;
 }
 
 // ---------------------------------------------------------------- async copies, mbarriers
