@@ -309,20 +309,17 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(AttnArgs a) {
     }
 }
 
-// One CTA of D threads per (row, query head): merge the split partials. SK: the splits follow
-// the stream-K schedule of the tensor-core kernel (split 0 + one per unit segment); otherwise
-// split 0 + one per chunk of the middle tier.
-template <int D, bool SK>
+// One CTA of D threads per (row, query head): merge the split partials of the CUDA-core
+// kernel (split 0 + one per chunk of the middle tier).
+template <int D>
 __global__ void __launch_bounds__(D) attn_combine_kernel(AttnArgs a, uint16_t* __restrict__ out,
-                                                         float* __restrict__ ml,
-                                                         const __grid_constant__ StreamK sk) {
+                                                         float* __restrict__ ml) {
   const int bh = blockIdx.x;
   const int b = bh / a.Hq, hq = bh % a.Hq;
   const int G = a.Hq / a.H;
   const int unit = b * a.H + hq / G;
   const int n_mid = a.meta[unit * kF + FADE_META_N_MID];
-  const int ns = SK ? min(a.nsplit, 1 + sk_segments(sk, b, hq / G))
-                    : min(a.nsplit, 1 + (n_mid + a.chunk - 1) / a.chunk);
+  const int ns = min(a.nsplit, 1 + (n_mid + a.chunk - 1) / a.chunk);
   const float* pm = a.part_ml + (size_t)bh * a.nsplit * 2;
   const float* pa = a.part_acc + (size_t)bh * a.nsplit * D;
   float M = -INFINITY;
@@ -335,6 +332,40 @@ __global__ void __launch_bounds__(D) attn_combine_kernel(AttnArgs a, uint16_t* _
   }
   out[(size_t)bh * D + threadIdx.x] = f2h(o / Lsum);
   if (threadIdx.x == 0) {
+    ml[2 * bh] = M;
+    ml[2 * bh + 1] = Lsum;
+  }
+}
+
+// The tensor-core kernel's partials (split 0 + one per stream-K segment of the unit): one CTA of
+// G x D threads per unit (row, KV head), thread (h, c) merges channel c of query head h; the
+// unit's segment count is taken once from the schedule.
+template <int D>
+__global__ void __launch_bounds__(1024) attn_combine_sk_kernel(AttnArgs a,
+                                                               uint16_t* __restrict__ out,
+                                                               float* __restrict__ ml,
+                                                               const __grid_constant__ StreamK sk) {
+  const int unit = blockIdx.x;
+  const int b = unit / a.H, hk = unit % a.H;
+  const int G = a.Hq / a.H;
+  __shared__ int s_ns;
+  if (threadIdx.x == 0) s_ns = min(a.nsplit, 1 + sk_segments(sk, b, hk));
+  __syncthreads();
+  const int ns = s_ns;
+  const int h = threadIdx.x / D, c = threadIdx.x % D;
+  const size_t bh = (size_t)b * a.Hq + hk * G + h;
+  const float* pm = a.part_ml + bh * a.nsplit * 2;
+  const float* pa = a.part_acc + bh * a.nsplit * D + c;
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, pm[2 * s]);
+  float Lsum = 0.f, o = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float w = (pm[2 * s] == -INFINITY) ? 0.f : __expf(pm[2 * s] - M);
+    Lsum = fmaf(pm[2 * s + 1], w, Lsum);
+    o = fmaf(pa[(size_t)s * D], w, o);
+  }
+  out[bh * D + c] = f2h(o / Lsum);
+  if (c == 0) {
     ml[2 * bh] = M;
     ml[2 * bh + 1] = Lsum;
   }
@@ -501,14 +532,14 @@ extern "C" fade_status_t fade_decode_attention(const fade_config_t* c, const fad
   const int bh = c->batch * c->num_q_heads;
   if (c->head_dim == 64) {
     if (mma)
-      attn_combine_kernel<64, true><<<bh, 64, 0, s>>>(a, out, ml_ws, sk);
+      attn_combine_sk_kernel<64><<<units, 64 * (a.Hq / a.H), 0, s>>>(a, out, ml_ws, sk);
     else
-      attn_combine_kernel<64, false><<<bh, 64, 0, s>>>(a, out, ml_ws, sk);
+      attn_combine_kernel<64><<<bh, 64, 0, s>>>(a, out, ml_ws);
   } else {
     if (mma)
-      attn_combine_kernel<128, true><<<bh, 128, 0, s>>>(a, out, ml_ws, sk);
+      attn_combine_sk_kernel<128><<<units, 128 * (a.Hq / a.H), 0, s>>>(a, out, ml_ws, sk);
     else
-      attn_combine_kernel<128, false><<<bh, 128, 0, s>>>(a, out, ml_ws, sk);
+      attn_combine_kernel<128><<<bh, 128, 0, s>>>(a, out, ml_ws);
   }
   return launch_status("fade_decode_attention combine");
 }

@@ -765,7 +765,7 @@ __global__ void __launch_bounds__(256, 2) evict_compact_kernel(LayerArgs a) {
 template <int D>
 __global__ void __launch_bounds__(256) evict_recent_commit_kernel(LayerArgs a) {
   using CC = RecentCfg<D>;
-  constexpr int TPT = CC::TPT, TOK = CC::TOK;
+  constexpr int TOK = CC::TOK;
   extern __shared__ float4 tab[];
   int* hinfo = reinterpret_cast<int*>(tab + CC::TABF4);  // [H][4]
   __shared__ int s_rlo, s_rhi;

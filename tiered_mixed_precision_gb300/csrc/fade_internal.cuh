@@ -404,9 +404,7 @@ __device__ __noinline__ uint2 codes_half_group_exact(uint4 lo, uint4 hi, float s
 // the exact scalar path with the clamp.
 template <int BITS>
 __device__ __forceinline__ void codes_half_group(const uint32_t (&H)[8], float s, uint32_t* out) {
-  constexpr int per = 32 / BITS;
   constexpr uint32_t mask = (1u << BITS) - 1u;
-  constexpr int qmax = (1 << (BITS - 1)) - 1;
   // any reciprocal estimate serves: the exact residual below confirms or rejects the candidates
   float r;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
