@@ -342,7 +342,7 @@ def run_ours(args, rank, world):
     clocks = ClockSampler(dev.index)
     clocks.start()
     if graph is None:
-        fc.timers = {}
+        fc.timers = None  # no per-call events inside the timed region (they cost host time)
         fc.launches = 0
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -367,6 +367,8 @@ def run_ours(args, rank, world):
     per_call_overlapped = None
     ms_iso = None
     try:
+        if graph is None:  # eager launches: per-call events come from extra steps below
+            raise RuntimeError("eager launches")
         per_call = {name: [a.elapsed_time(b) for a, b in pairs]
                     for name, pairs in fc.timers.items()}
         if pipelined:
@@ -389,8 +391,9 @@ def run_ours(args, rank, world):
             timing_note = ("events of a replay after the timed region with each layer's "
                            f"maintenance inline (not overlapped; {ms_iso:.3f} ms per step)")
             del iso
-    except Exception as exc:  # timing nodes unavailable in this graph: time eager steps instead
-        timing_note = f"eager steps after the timed region ({type(exc).__name__})"
+    except Exception as exc:  # eager run, or timing nodes unavailable: time eager steps instead
+        timing_note = ("events of eager steps after the timed region" if graph is None else
+                       f"eager steps after the timed region ({type(exc).__name__})")
         progress(f"per-call timing from eager steps ({exc})")
         fc.timers = {}
         for s in range(W, W + K):
