@@ -53,6 +53,10 @@ def parse_args():
                         "line always runs every layer of the workload)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="launch every kernel (no CUDA graph)")
+    p.add_argument("--side-streams", type=int, default=0,
+                   help="streams that take the layers' maintenance in turn (pipelined schedule); "
+                        "0 = one when a layer's middle tier fills the GPU (at least 2^20 "
+                        "token-heads), else two")
     p.add_argument("--no-pipeline", action="store_true",
                    help="in the graph, run each layer's maintenance before its attention instead "
                         "of overlapping it with the following layers")
@@ -325,7 +329,10 @@ def run_ours(args, rank, world):
     fc.timers = {}
     fc.launches = 0
     pipelined = steady and not args.no_graph and not args.no_pipeline
-    side = torch.cuda.Stream() if pipelined else None
+    n_side = args.side_streams
+    if n_side <= 0:  # concurrent compactions of large layers compete; short ones fill gaps
+        n_side = 1 if B * Hkv * max(wl.int4_budget, 0) >= (1 << 20) else 2
+    side = [torch.cuda.Stream() for _ in range(n_side)] if pipelined else None
     if steady and not args.no_graph:
         if pipelined:
             # prologue: the coming step's maintenance of every layer; from here on each step
@@ -492,7 +499,8 @@ def run_ours(args, rank, world):
                    "l2": "no flush: the compressed cache read per step is far larger than L2",
                    "parallelism": f"replicas x{world} (rows independent, no collective)",
                    "launch": ("cuda graph per step" if graph is not None else "eager launches") +
-                             ("; each layer's maintenance overlaps the next layers" if pipelined else ""),
+                             (f"; each layer's maintenance overlaps the next layers "
+                              f"({len(side)} side streams taken in turn)" if pipelined else ""),
                    "per_call_timing": timing_note},
         "roofline": dict(rl[dominant], kernel=dominant) if dominant else None,
         "roofline_by_call": rl,

@@ -89,11 +89,11 @@ def test_graph_replay_matches_eager_steps(policy):
                         assert a_[key] == b_[key], (layer, b, h, key)
 
 
-@pytest.mark.parametrize("policy", ["position", "h2o"])
-def test_pipelined_graph_matches_eager_steps(policy):
+@pytest.mark.parametrize("policy,n_side", [("position", 1), ("position", 2), ("h2o", 2)])
+def test_pipelined_graph_matches_eager_steps(policy, n_side):
     """Pipelined steps (each layer's maintenance for the next step on a side stream, right
-    after its attention) give the same outputs as the method's step order, and after one more
-    maintenance pass the same cache."""
+    after its attention; with two side streams the layers take them in turn) give the same
+    outputs as the method's step order, and after one more maintenance pass the same cache."""
     import torch
 
     wl = get_workload(4).scaled(layers=3, batch=2, num_q_heads=8, num_kv_heads=2,
@@ -109,7 +109,7 @@ def test_pipelined_graph_matches_eager_steps(policy):
     v = torch.from_numpy(draw_vectors(wl, "v", (steps, L, B, Hkv, d), "pipe")).cuda()
     out_e = torch.empty((L, B, Hq, d), dtype=torch.float16, device="cuda")
     out_p = torch.empty_like(out_e)
-    side = torch.cuda.Stream()
+    side = [torch.cuda.Stream() for _ in range(n_side)]
     piped.maintain_all()
     qb, kb, vb = q[0].clone(), k[0].clone(), v[0].clone()
     g = piped.capture_step(qb, kb, vb, out_p, side)

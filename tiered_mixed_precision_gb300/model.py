@@ -160,31 +160,34 @@ class FadeCache:
         for layer in range(len(self.layers)):
             self.maintain_layer(layer)
 
-    def step_all_pipelined(self, q, k, v, out, side: torch.cuda.Stream | None):
+    def step_all_pipelined(self, q, k, v, out, side):
         """One decode step of every layer whose maintenance was already done (by
         ``maintain_all`` or the previous pipelined step): each layer attends on the current
-        stream, then its maintenance for the NEXT step is issued on ``side`` and overlaps the
-        following layers (``side`` None: issued inline, no overlap). Per layer the operations
-        run in the same order as ``step_all``; the step ends when ``side`` has finished."""
+        stream, then its maintenance for the NEXT step is issued on a side stream and overlaps
+        the following layers. ``side``: one stream, or several taken in turn by layer (so that
+        one layer's short maintenance launches overlap the next layer's), or None (issued
+        inline, no overlap). Per layer the operations run in the same order as ``step_all``;
+        the step ends when every side stream has finished."""
         self.set_positions(self.next_positions())
         main = torch.cuda.current_stream()
+        sides = [] if side is None else (list(side) if isinstance(side, (list, tuple)) else [side])
         for layer in range(len(self.layers)):
             self.attend_layer(layer, q[layer], k[layer], v[layer], out[layer])
-            if side is None:
+            if not sides:
                 self.maintain_layer(layer)
                 continue
+            st = sides[layer % len(sides)]
             ev = torch.cuda.Event()
             ev.record(main)
-            side.wait_event(ev)
-            with torch.cuda.stream(side):
+            st.wait_event(ev)
+            with torch.cuda.stream(st):
                 self.maintain_layer(layer)
-        if side is not None:
+        for st in sides:
             done = torch.cuda.Event()
-            done.record(side)
+            done.record(st)
             main.wait_event(done)
 
-    def capture_step(self, q, k, v, out, side: torch.cuda.Stream | None = None,
-                     pipelined: bool = False):
+    def capture_step(self, q, k, v, out, side=None, pipelined: bool = False):
         """Capture step_all (or step_all_pipelined, with ``pipelined`` or a side stream) on fixed
         input/output buffers as a CUDA graph.
 
