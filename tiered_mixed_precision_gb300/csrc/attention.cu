@@ -338,37 +338,64 @@ __global__ void __launch_bounds__(D) attn_combine_kernel(AttnArgs a, uint16_t* _
 }
 
 // The tensor-core kernel's partials (split 0 + one per stream-K segment of the unit): one CTA of
-// G x D threads per unit (row, KV head), thread (h, c) merges channel c of query head h; the
-// unit's segment count is taken once from the schedule.
+// G x D threads per unit (row, KV head). The unit's segment count comes once from the schedule;
+// every segment's (m, l) is loaded at once into shared memory, warp h reduces head h's
+// M = max m_s, its weights e^(m_s - M) and L = sum l_s e^(m_s - M), then thread (h, c) sums
+// channel c of the weighted partial outputs: out = sum acc_s e^(m_s - M) / L.
 template <int D>
 __global__ void __launch_bounds__(1024) attn_combine_sk_kernel(AttnArgs a,
                                                                uint16_t* __restrict__ out,
                                                                float* __restrict__ ml,
                                                                const __grid_constant__ StreamK sk) {
+  constexpr int kMaxSeg = kMaxCtaSK + 1;
+  __shared__ float s_w[8][kMaxSeg];  // m_s, then the weight e^(m_s - M)
+  __shared__ float s_l[8][kMaxSeg];
+  __shared__ float s_L[8];
+  __shared__ int s_ns;
   const int unit = blockIdx.x;
   const int b = unit / a.H, hk = unit % a.H;
   const int G = a.Hq / a.H;
-  __shared__ int s_ns;
-  if (threadIdx.x == 0) s_ns = min(a.nsplit, 1 + sk_segments(sk, b, hk));
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  if (tid == 0) s_ns = min(a.nsplit, min(kMaxSeg, 1 + sk_segments(sk, b, hk)));
   __syncthreads();
   const int ns = s_ns;
-  const int h = threadIdx.x / D, c = threadIdx.x % D;
-  const size_t bh = (size_t)b * a.Hq + hk * G + h;
-  const float* pm = a.part_ml + bh * a.nsplit * 2;
-  const float* pa = a.part_acc + bh * a.nsplit * D + c;
-  float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, pm[2 * s]);
-  float Lsum = 0.f, o = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float w = (pm[2 * s] == -INFINITY) ? 0.f : __expf(pm[2 * s] - M);
-    Lsum = fmaf(pm[2 * s + 1], w, Lsum);
-    o = fmaf(pa[(size_t)s * D], w, o);
+  const size_t bh0 = (size_t)b * a.Hq + hk * G;
+  for (int i = tid; i < G * ns; i += nthr) {
+    const int h = i / ns, sg = i % ns;
+    const float* pm = a.part_ml + ((bh0 + h) * a.nsplit + sg) * 2;
+    s_w[h][sg] = pm[0];
+    s_l[h][sg] = pm[1];
   }
-  out[bh * D + c] = f2h(o / Lsum);
-  if (c == 0) {
-    ml[2 * bh] = M;
-    ml[2 * bh + 1] = Lsum;
+  __syncthreads();
+  const int warp = tid >> 5, lane = tid & 31;
+  if (warp < G) {
+    const int h = warp;
+    float M = -INFINITY;
+    for (int sg = lane; sg < ns; sg += 32) M = fmaxf(M, s_w[h][sg]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float Lp = 0.f;
+    for (int sg = lane; sg < ns; sg += 32) {
+      const float m = s_w[h][sg];
+      const float w = (m == -INFINITY) ? 0.f : __expf(m - M);
+      s_w[h][sg] = w;
+      Lp = fmaf(s_l[h][sg], w, Lp);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) Lp += __shfl_xor_sync(0xffffffffu, Lp, o);
+    if (lane == 0) {
+      s_L[h] = Lp;
+      ml[2 * (bh0 + h)] = M;
+      ml[2 * (bh0 + h) + 1] = Lp;
+    }
   }
+  __syncthreads();
+  const int h = tid / D, c = tid % D;
+  const float* pa = a.part_acc + (bh0 + h) * a.nsplit * D + c;
+  float o = 0.f;
+#pragma unroll 4
+  for (int sg = 0; sg < ns; ++sg) o = fmaf(pa[(size_t)sg * D], s_w[h][sg], o);
+  out[(bh0 + h) * D + c] = f2h(o / s_L[h]);
 }
 
 struct AccArgs {
@@ -380,11 +407,24 @@ struct AccArgs {
   float decay;
 };
 
-// One thread per storage slot of a unit: score update from the G heads' probabilities.
-__global__ void h2o_accumulate_kernel(AccArgs a) {
+// One thread per storage slot of a unit: score update from the G heads' probabilities. The
+// G logits of the slot and the heads' (M, L) do not depend on the unit's counts, so they are
+// loaded first (for slots the unit does not hold they are read and dropped).
+__global__ void __launch_bounds__(256) h2o_accumulate_kernel(AccArgs a) {
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= a.NS) return;
   const int hk = blockIdx.y, b = blockIdx.z, unit = b * a.H + hk;
+  const int G = a.Hq / a.H;
+  float lg[8], mh[8], lh[8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    if (h < G) {
+      const size_t bh = (size_t)b * a.Hq + hk * G + h;
+      lg[h] = a.logits[bh * a.NS + j];
+      mh[h] = a.ml[2 * bh];
+      lh[h] = a.ml[2 * bh + 1];
+    }
+  }
   const int32_t* m = a.meta + unit * kF;
   float* sc;
   if (j < a.S) {
@@ -400,12 +440,10 @@ __global__ void h2o_accumulate_kernel(AccArgs a) {
     if (age >= m[FADE_META_N_RECENT]) return;
     sc = a.rec_sc + (size_t)unit * a.W + r;
   }
-  const int G = a.Hq / a.H;
   float psum = 0.f;
-  for (int h = 0; h < G; ++h) {
-    const size_t bh = (size_t)b * a.Hq + hk * G + h;
-    psum += __expf(a.logits[bh * a.NS + j] - a.ml[2 * bh]) / a.ml[2 * bh + 1];
-  }
+#pragma unroll
+  for (int h = 0; h < 8; ++h)
+    if (h < G) psum += __expf(lg[h] - mh[h]) / lh[h];
   if (a.policy == FADE_EVICT_H2O)
     *sc += psum;
   else
