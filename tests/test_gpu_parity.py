@@ -114,11 +114,34 @@ def _small(key):
     if key == "d128_g8":
         return get_workload(4).scaled(layers=1, batch=2, num_q_heads=16, num_kv_heads=2,
                                       prompt_len=1300, int4_budget=700, steps=5), None
+    # the remaining (head_dim, K bits, V bits) combinations of the eviction kernels
+    if key == "d64_k2v4_h2o":
+        return get_workload(3).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                      middle_k_bits=2, middle_v_bits=4, prompt_len=800,
+                                      int4_budget=300, steps=6), None
+    if key == "d128_k4v4_pos":
+        return get_workload(4).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                      middle_v_bits=4, prompt_len=1100, int4_budget=400,
+                                      steps=5), None
+    if key == "d64_k2v2_ema":
+        return get_workload(5).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                      head_dim=64, middle_k_bits=2, middle_v_bits=2,
+                                      ragged=(700, 1200), prompt_len=1200, int4_budget=500,
+                                      steps=5), None
+    if key == "d128_k2v2_pos":
+        return get_workload(4).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                      middle_k_bits=2, middle_v_bits=2, prompt_len=900,
+                                      int4_budget=350, steps=5), None
+    if key == "d64_k4v4_pos":
+        return get_workload(4).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                      head_dim=64, middle_v_bits=4, prompt_len=900,
+                                      int4_budget=350, steps=5), None
     raise KeyError(key)
 
 
 @pytest.mark.parametrize("key", ["1", "2s", "3s", "4s", "5s", "5bs", "g2_k2v4", "g1_h2o_d128",
-                                 "d64_g8", "d128_g8"])
+                                 "d64_g8", "d128_g8", "d64_k2v4_h2o", "d128_k4v4_pos",
+                                 "d64_k2v2_ema", "d128_k2v2_pos", "d64_k4v4_pos"])
 def test_lockstep_small_workloads(T, key):
     wl, cap = _small(key)
     ls = Lockstep(wl, mid_capacity=cap)
