@@ -45,13 +45,18 @@ constexpr int kTileTok = 256;            // tokens per TMA tile
 #ifndef FADE_MMA_STAGES_128
 #define FADE_MMA_STAGES_128 3
 #endif
+// Resident CTAs per SM of the eight-consumer shape (two: 96 registers a thread; one: more
+// registers and a deeper ring per CTA).
+#ifndef FADE_MMA_CTAS_PER_SM
+#define FADE_MMA_CTAS_PER_SM 2
+#endif
 template <int D, int G>
 struct MmaShape {
   static constexpr int CONS = (FADE_MMA_WIDE && G <= 4) ? 8 : 4;
   static constexpr int THREADS = 32 * (CONS + 1);
   static constexpr int WARP_TOK = kTileTok / CONS;  // tokens per consumer warp per tile
   static constexpr int MT = WARP_TOK / 16;          // 16-token M-tiles per consumer warp
-  static constexpr int MINB = CONS == 8 ? 2 : 1;
+  static constexpr int MINB = CONS == 8 ? FADE_MMA_CTAS_PER_SM : 1;
 };
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -1029,7 +1034,7 @@ int mid_mma_ctas(const fade_config_t* c) {
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 1;
   const int G = c->num_q_heads / c->num_kv_heads;
-  const int minb = (FADE_MMA_WIDE && G <= 4) ? 2 : 1;  // MmaShape<D, G>::MINB
+  const int minb = (FADE_MMA_WIDE && G <= 4) ? FADE_MMA_CTAS_PER_SM : 1;  // MmaShape::MINB
   return std::max(1, std::min(kMaxCtaSK, sms * minb));
 }
 
