@@ -112,6 +112,47 @@ __device__ void block_select(const float* __restrict__ keys, int n, int k,
   if (tid == 0) chunk_base[(n + kChunk - 1) / kChunk] = carry;
 }
 
+// block_select for k = 1 (one victim: the steady state of a decode step) in one pass: the
+// smallest (key, index) pair, i.e. the lowest index among the smallest keys, by a block-wide
+// minimum over 64-bit (ordered key, index) words; then the bitmap and the chunk prefixes.
+__device__ void block_select_one(const float* __restrict__ keys, int n,
+                                 uint32_t* __restrict__ bitmap, int32_t* __restrict__ chunk_base) {
+  __shared__ unsigned long long s_best[kSelThreads / 32];
+  __shared__ int s_victim;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned long long best = ~0ull;
+  if (keys) {
+    for (int i = tid; i < n; i += kSelThreads) {
+      const unsigned long long c = ((unsigned long long)ord_key(keys[i]) << 32) | (uint32_t)i;
+      best = c < best ? c : best;
+    }
+  } else if (tid == 0) {
+    best = 0ull;  // all keys equal: the oldest
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const unsigned long long t = __shfl_xor_sync(0xffffffffu, best, o);
+    best = t < best ? t : best;
+  }
+  if (lane == 0) s_best[warp] = best;
+  __syncthreads();
+  if (warp == 0) {
+    best = lane < kSelThreads / 32 ? s_best[lane] : ~0ull;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const unsigned long long t = __shfl_xor_sync(0xffffffffu, best, o);
+      best = t < best ? t : best;
+    }
+    if (lane == 0) s_victim = (int)(uint32_t)(best & 0xffffffffull);
+  }
+  __syncthreads();
+  const int vic = s_victim;
+  for (int w = tid; w < (n + 31) / 32; w += kSelThreads)
+    bitmap[w] = (w == (vic >> 5)) ? (1u << (vic & 31)) : 0u;
+  const int nc = (n + kChunk - 1) / kChunk;
+  for (int c = tid; c <= nc; c += kSelThreads) chunk_base[c] = (vic < c * kChunk) ? 1 : 0;
+}
+
 // Victims before candidate `ci`, from the chunk prefix plus the bitmap words of its chunk
 // (warp-cooperative; all lanes get the result).
 __device__ __forceinline__ int victims_before(const uint32_t* __restrict__ bitmap,
@@ -343,8 +384,12 @@ __global__ void __launch_bounds__(kSelThreads) evict_select_kernel(LayerArgs a) 
   const float* keys = (a.policy == FADE_EVICT_POSITION)
                           ? nullptr
                           : (cur ? a.mid_sc[1] : a.mid_sc[0]) + (size_t)unit * a.C;
-  block_select(keys, n_mid, k, a.victims + (size_t)unit * a.victim_words,
-               a.chunk_base + (size_t)unit * a.chunk_slots);
+  if (k == 1)
+    block_select_one(keys, n_mid, a.victims + (size_t)unit * a.victim_words,
+                     a.chunk_base + (size_t)unit * a.chunk_slots);
+  else
+    block_select(keys, n_mid, k, a.victims + (size_t)unit * a.victim_words,
+                 a.chunk_base + (size_t)unit * a.chunk_slots);
 }
 
 // 8 consecutive fp16 values (16-byte aligned) as 4 packed fp32 pairs, and back (RN to fp16).
