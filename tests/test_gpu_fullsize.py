@@ -76,3 +76,71 @@ def test_full_size_layer_sampled_units(key):
             _compare_unit(fc, u, b, h, f"after step {step}, unit {(b, h)}")
     torch.cuda.synchronize()
     assert int(fc.layers[0].status.abs().sum()) == 0
+
+
+@pytest.mark.parametrize("key", [4, 5])
+def test_full_size_pipelined_graph_sampled_units(key):
+    """The benchmark's own launch configuration at full layer size: the pipelined step (each
+    layer's maintenance for the next step on side streams) captured once as a CUDA graph and
+    replayed. The oracle follows the same order: maintenance first (demote, evict), then per
+    step append, attention, accumulation and the next step's maintenance."""
+    import torch
+
+    import tiered_mixed_precision_gb300 as T
+    from tiered_mixed_precision_gb300.model import FadeCache
+
+    wl = get_workload(key)
+    steps = 2
+    cfg = T.Config.from_workload(wl)
+    lens = ragged_context_lengths(wl)
+    maxP = int(lens.max())
+    max_pos = maxP + steps + 16
+    dev = torch.device("cuda")
+    fc = FadeCache(cfg, 1, maxP, max_pos, dev)
+    pr = draw_prompt(wl, 0, maxP, backend="torch", device=dev)
+    rng = np.random.default_rng(100 + key)
+    sample = sorted({(int(rng.integers(wl.batch)), int(rng.integers(wl.num_kv_heads)))
+                     for _ in range(4)} | {(0, 0)})
+    raw = {(b, h): (pr["k"][b, h, :lens[b]].cpu().numpy(), pr["v"][b, h, :lens[b]].cpu().numpy())
+           for b, h in sample}
+    fc.prefill(0, pr["k"], pr["v"], lens, None)
+    del pr
+    rope = RopeTable.from_workload(wl, max_pos)
+    units = {}
+    for (b, h), (k, v) in raw.items():
+        u = UnitCache(Params.from_workload(wl), rope)
+        u.prefill(k, v)
+        u.demote()                      # the prologue's maintenance
+        u.evict(u.choose_victims())
+        units[(b, h)] = u
+    G, d = wl.group, wl.head_dim
+    q = [draw_vectors(wl, "q", (1, wl.batch, wl.num_q_heads, d), "pipe", s, backend="torch",
+                      device=dev) for s in range(steps)]
+    k = [draw_vectors(wl, "k", (1, wl.batch, wl.num_kv_heads, d), "pipe", s, backend="torch",
+                      device=dev) for s in range(steps)]
+    v = [draw_vectors(wl, "v", (1, wl.batch, wl.num_kv_heads, d), "pipe", s, backend="torch",
+                      device=dev) for s in range(steps)]
+    out = torch.empty((1, wl.batch, wl.num_q_heads, d), dtype=torch.float16, device=dev)
+    side = [torch.cuda.Stream(), torch.cuda.Stream()]
+    fc.maintain_all()
+    qb, kb, vb = q[0].clone(), k[0].clone(), v[0].clone()
+    graph = fc.capture_step(qb, kb, vb, out, side)
+    for step in range(steps):
+        qb.copy_(q[step])
+        kb.copy_(k[step])
+        vb.copy_(v[step])
+        graph.replay()
+        torch.cuda.synchronize()
+        oh = out[0].float().cpu().numpy()
+        qh, kh, vh = q[step][0].cpu().numpy(), k[step][0].cpu().numpy(), v[step][0].cpu().numpy()
+        for (b, h), u in units.items():
+            pos = u.n_held
+            u.append(rope.apply(kh[b, h][None], pos), vh[b, h])
+            o_ref, p, _ = u.attend(rope.apply(qh[b, h * G:(h + 1) * G], pos))
+            u.accumulate(p)
+            ok, err, nbad = allclose_report(oh[b, h * G:(h + 1) * G], o_ref)
+            assert ok, f"step {step} unit {(b, h)}: max err {err}, {nbad} bad"
+            u.demote()                  # the next step's maintenance, as the graph did
+            u.evict(u.choose_victims())
+            _compare_unit(fc, u, b, h, f"after pipelined step {step}, unit {(b, h)}")
+    assert int(fc.layers[0].status.abs().sum()) == 0

@@ -182,7 +182,7 @@ class FadeCache:
             st.wait_event(ev)
             with torch.cuda.stream(st):
                 self.maintain_layer(layer)
-        for st in sides:
+        for st in sides[:len(self.layers)]:  # the streams some layer used (joined back)
             done = torch.cuda.Event()
             done.record(st)
             main.wait_event(done)
