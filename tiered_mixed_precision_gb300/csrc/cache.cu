@@ -463,6 +463,8 @@ struct MidCfg {
   static constexpr int NROWS = TOK + 16;    // staged RoPE rows (blocks with n_ev <= 16)
   static constexpr int TABF4 = NROWS * (ROWF4 + 1);  // staged rows padded by one float4
   static constexpr int PRE = TOK / 32 + 2;  // per-head ints: victim prefix words + base
+  // with the block's TOK/32 bitmap words after them (selection policies, staged bitmap)
+  static constexpr int PRE_SEL = PRE + TOK / 32;
   static constexpr int SRB = D / 32 * 2;    // bytes of one scale row
 };
 // Per-thread prefetch slots after the staged rows (every thread reads only its own slots).
@@ -479,7 +481,7 @@ struct MidBuf {
   static constexpr int SC_OFF = VS_OFF + 256 * 4;         // [256]: score (first thread of a token)
   static constexpr int BYTES = SC_OFF + 256 * 4;
   static size_t smem(int H) {
-    return (size_t)MidCfg<D>::TABF4 * 16 + BYTES + (size_t)H * (MidCfg<D>::PRE + 4) * 4;
+    return (size_t)MidCfg<D>::TABF4 * 16 + BYTES + (size_t)H * (MidCfg<D>::PRE_SEL + 4) * 4;
   }
 };
 
@@ -562,9 +564,13 @@ __device__ __forceinline__ void reposition_groups(const uint8_t* kp, f2x S1, f2x
 // at most 16 below) are staged once per CTA in shared memory and serve every head; each head's
 // codes, scales and scores are fetched ahead with cp.async (K one processed head ahead, V during
 // the head itself) into slots private to the thread.
-template <int D, int KB, int VB>
+// SEL: a selection policy (victims from the bitmap of evict_select_kernel) whose block's bitmap
+// words are staged in shared memory with their prefix counts; false: the code for every policy,
+// with the victims' prefix read from the bitmap per token (the position policy's instantiation).
+template <int D, int KB, int VB, bool SEL>
 __global__ void __launch_bounds__(256, 2) evict_compact_kernel(LayerArgs a) {
   using CC = MidCfg<D>;
+  constexpr int PRE = SEL ? CC::PRE_SEL : CC::PRE;
   using MB = MidBuf<D, KB, VB>;
   constexpr int TOK = CC::TOK, TPW = CC::TPW, SRB = CC::SRB;
   constexpr int GB = MB::GB, KSH = MB::KSH, VSH = MB::VSH;
@@ -608,16 +614,23 @@ __global__ void __launch_bounds__(256, 2) evict_compact_kernel(LayerArgs a) {
 #pragma unroll
       for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
       const int nw = (hi - lo + 31) / 32;
-      const int wc = lane < nw ? __popc(bm[w_lo + lane]) : 0;
+      int wc;
+      if constexpr (SEL) {
+        const uint32_t wv = lane < nw ? bm[w_lo + lane] : 0u;
+        wc = __popc(wv);
+        if (lane < TOK / 32) hpre[h * PRE + TOK / 32 + 2 + lane] = (int)wv;
+      } else {
+        wc = lane < nw ? __popc(bm[w_lo + lane]) : 0;
+      }
       int incl = wc;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int tt = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += tt;
       }
-      if (lane <= TOK / 32) hpre[h * CC::PRE + lane] = incl - wc;
+      if (lane <= TOK / 32) hpre[h * PRE + lane] = incl - wc;
       if (lane == 0)
-        hpre[h * CC::PRE + TOK / 32 + 1] =
+        hpre[h * PRE + TOK / 32 + 1] =
             a.chunk_base[(size_t)unit * a.chunk_slots + lo / kChunk] + c;
     }
     if (lane == 0) {
@@ -710,10 +723,15 @@ __global__ void __launch_bounds__(256, 2) evict_compact_kernel(LayerArgs a) {
         keep = i >= n_ev;
         nv = i - n_ev;
       } else {
-        const uint32_t* bm = a.victims + (size_t)(b * a.H + h) * a.victim_words;
-        const uint32_t word = bm[i >> 5];
+        uint32_t word;
+        if constexpr (SEL) {  // the block's bitmap word from shared memory (lo % 32 == 0)
+          word = (uint32_t)hpre[h * PRE + TOK / 32 + 2 + ((i - lo) >> 5)];
+        } else {
+          const uint32_t* bm = a.victims + (size_t)(b * a.H + h) * a.victim_words;
+          word = bm[i >> 5];
+        }
         keep = !((word >> (i & 31)) & 1u);
-        nv = i - (hpre[h * CC::PRE + TOK / 32 + 1] + hpre[h * CC::PRE + ((i - lo) >> 5)] +
+        nv = i - (hpre[h * PRE + TOK / 32 + 1] + hpre[h * PRE + ((i - lo) >> 5)] +
                   __popc(word & ((1u << (i & 31)) - 1u)));
       }
     }
@@ -1043,7 +1061,8 @@ struct CompactLaunch {
   static fade_status_t run(const LayerArgs& a, int B, int chunks, cudaStream_t st) {
     // chunks of compact_tok<D>() middle indices per batch row
     const size_t smem = MidBuf<D, KB, VB>::smem(a.H);
-    auto kern = evict_compact_kernel<D, KB, VB>;
+    auto kern = a.positional ? evict_compact_kernel<D, KB, VB, false>
+                             : evict_compact_kernel<D, KB, VB, true>;
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
