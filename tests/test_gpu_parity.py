@@ -7,6 +7,7 @@ from harness import Lockstep, allclose_report
 from oracle import quant
 from oracle.rope import RopeTable
 from synth import draw_codec_cases, get_workload
+from synth.workloads import Rope
 
 pytestmark = pytest.mark.gpu
 
@@ -136,12 +137,34 @@ def _small(key):
         return get_workload(4).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
                                       head_dim=64, middle_v_bits=4, prompt_len=900,
                                       int4_budget=350, steps=5), None
+    # degenerate cases of the method
+    if key == "deg_nosink":  # no sinks: the recent ring and the middle tier only
+        return get_workload(4).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                      head_dim=64, n_sink=0, recent_window=16, prompt_len=300,
+                                      int4_budget=120, steps=6), None
+    if key == "deg_w1_h2o":  # a one-token recent window: every step demotes the previous token
+        return get_workload(3).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                      n_sink=2, recent_window=1, prompt_len=200,
+                                      int4_budget=60, steps=8), None
+    if key == "deg_budget0":  # budget 0: every demoted token is evicted in the same step
+        return get_workload(4).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                      prompt_len=200, int4_budget=0, steps=5), None
+    if key == "deg_short_ragged":  # rows whose prompts do not reach the middle tier at first
+        return get_workload(5).scaled(layers=1, batch=4, num_q_heads=8, num_kv_heads=2,
+                                      recent_window=16, ragged=(2, 60), prompt_len=60,
+                                      int4_budget=30, steps=10), None
+    if key == "deg_norope_ema":  # no positional encoding: re-positioning is the identity
+        return get_workload(5).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                      rope=Rope("none"), ragged=None, prompt_len=400,
+                                      int4_budget=150, steps=6), None
     raise KeyError(key)
 
 
 @pytest.mark.parametrize("key", ["1", "2s", "3s", "4s", "5s", "5bs", "g2_k2v4", "g1_h2o_d128",
                                  "d64_g8", "d128_g8", "d64_k2v4_h2o", "d128_k4v4_pos",
-                                 "d64_k2v2_ema", "d128_k2v2_pos", "d64_k4v4_pos"])
+                                 "d64_k2v2_ema", "d128_k2v2_pos", "d64_k4v4_pos",
+                                 "deg_nosink", "deg_w1_h2o", "deg_budget0", "deg_short_ragged",
+                                 "deg_norope_ema"])
 def test_lockstep_small_workloads(T, key):
     wl, cap = _small(key)
     ls = Lockstep(wl, mid_capacity=cap)
