@@ -51,7 +51,27 @@ typedef enum {
 
 /* RoPE schemes (FADE-zh §RoPE方案兼容性). NONE: positions are not encoded in K (ALiBi
  * models), so re-positioning is the identity. */
-typedef enum { FADE_ROPE_NONE = 0, FADE_ROPE_DEFAULT = 1, FADE_ROPE_LLAMA3 = 2 } fade_rope_kind_t;
+/* RoPE schemes (FADE-zh §RoPE方案兼容性: standard RoPE and the scaling types llama3, linear,
+ * ntk, yarn; ALiBi models make re-positioning a no-op: FADE_ROPE_NONE). Every scheme is a set
+ * of inverse frequencies inv_i (rotate-half pairs i, i + d/2); base_i = base^(-2i/d):
+ *   DEFAULT  inv_i = base_i
+ *   LLAMA3   base_i blended by the number of rotations r_i = L / (2 pi / base_i) over the
+ *            original context L = original_max_position: r_i > high_freq_factor keeps base_i,
+ *            r_i < low_freq_factor uses base_i / factor, otherwise
+ *            (1 - t) base_i / factor + t base_i with t = (r_i - low) / (high - low)
+ *   LINEAR   inv_i = base_i / factor (position interpolation: positions divided by factor)
+ *   NTK      inv_i = (base * factor^(d / (d - 2)))^(-2i/d) (NTK-aware base scaling)
+ *   YARN     the LLAMA3 blend with low_freq_factor = alpha and high_freq_factor = beta of the
+ *            YaRN ramp (1 and 32 in its paper); YaRN's attention temperature is not part of
+ *            the table (it would scale every rotation, and un-RoPE / re-RoPE with it) */
+typedef enum {
+  FADE_ROPE_NONE = 0,
+  FADE_ROPE_DEFAULT = 1,
+  FADE_ROPE_LLAMA3 = 2,
+  FADE_ROPE_LINEAR = 3,
+  FADE_ROPE_NTK = 4,
+  FADE_ROPE_YARN = 5
+} fade_rope_kind_t;
 
 /* Eviction policies (FADE-zh §四种驱逐策略详解 1-3). NONE = safe mode (no eviction). */
 typedef enum {
@@ -63,11 +83,11 @@ typedef enum {
 
 typedef struct {
   int32_t kind;                  /* fade_rope_kind_t */
-  int32_t original_max_position; /* llama3 only */
+  int32_t original_max_position; /* llama3, yarn: the original context L */
   double base;                   /* theta base, e.g. 10000, 500000 */
-  double factor;                 /* llama3 only */
-  double low_freq_factor;        /* llama3 only */
-  double high_freq_factor;       /* llama3 only */
+  double factor;                 /* llama3, linear, ntk, yarn: the scaling factor (> 0) */
+  double low_freq_factor;        /* llama3; yarn: alpha */
+  double high_freq_factor;       /* llama3; yarn: beta (> low_freq_factor) */
 } fade_rope_t;
 
 /* One layer's cache configuration (FADE-zh §自定义配置: n_sink, recent_window, int4_budget,

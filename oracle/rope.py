@@ -37,11 +37,28 @@ F32 = np.float32
 
 def inv_freq(kind: str, base: float, head_dim: int, factor=1.0, low_freq_factor=1.0,
              high_freq_factor=4.0, original_max_position=8192) -> np.ndarray:
-    """fp32 inverse frequencies [d/2] for the rotation pairs."""
+    """fp32 inverse frequencies [d/2] for the rotation pairs.
+
+    FADE-zh §RoPE方案兼容性 names the scaling types; each follows its published definition:
+      * "linear" (position interpolation): every frequency divided by ``factor``, i.e. the
+        positions divided by it;
+      * "ntk" (NTK-aware scaling): the base raised to base * factor^(d/(d-2)), which keeps
+        the highest frequency and divides the lowest by ``factor``;
+      * "yarn": YaRN's ramp gamma(r) = clamp((r - alpha)/(beta - alpha), 0, 1) over the
+        number of rotations r = L/lambda a pair makes over the original context L, blending
+        theta/factor (gamma = 0) with theta (gamma = 1); alpha and beta come in
+        ``low_freq_factor`` and ``high_freq_factor``. It is the llama3 rule with those
+        boundaries. YaRN's attention temperature is left out: the table holds pure rotations.
+    """
     half = head_dim // 2
     i = np.arange(half, dtype=np.float64)
-    f = np.power(np.float64(base), -(2.0 * i) / head_dim)
-    if kind == "llama3":
+    b = np.float64(base)
+    if kind == "ntk":
+        b = b * np.power(np.float64(factor), head_dim / (head_dim - 2.0))
+    f = np.power(b, -(2.0 * i) / head_dim)
+    if kind == "linear":
+        f = f / factor
+    elif kind in ("llama3", "yarn"):
         lam = 2.0 * math.pi / f
         L = float(original_max_position)
         low_wl = L / low_freq_factor      # wavelengths above this: fully scaled
@@ -49,7 +66,7 @@ def inv_freq(kind: str, base: float, head_dim: int, factor=1.0, low_freq_factor=
         t = (L / lam - low_freq_factor) / (high_freq_factor - low_freq_factor)
         mixed = (1.0 - t) * f / factor + t * f
         f = np.where(lam < high_wl, f, np.where(lam > low_wl, f / factor, mixed))
-    elif kind not in ("default",):
+    elif kind not in ("default", "ntk"):
         raise ValueError(f"unsupported rope kind {kind!r}")
     return f.astype(F32)
 

@@ -16,11 +16,11 @@ from typing import Optional
 
 @dataclass(frozen=True)
 class Rope:
-    kind: str = "default"          # "none" | "default" | "llama3"
+    kind: str = "default"          # "none" | "default" | "llama3" | "linear" | "ntk" | "yarn"
     base: float = 10000.0
-    factor: float = 1.0            # llama3 only
-    low_freq_factor: float = 1.0   # llama3 only
-    high_freq_factor: float = 4.0  # llama3 only
+    factor: float = 1.0            # llama3, linear, ntk, yarn
+    low_freq_factor: float = 1.0   # llama3; yarn: alpha
+    high_freq_factor: float = 4.0  # llama3; yarn: beta
     original_max_position: int = 8192
 
 

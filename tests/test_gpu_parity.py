@@ -53,11 +53,20 @@ def test_codec_empty_input_is_a_no_op(T):
     assert int(c.sum()) == 7 * 32
 
 
-@pytest.mark.parametrize("key", [1, 3, 4])
+_SCALED_ROPES = {
+    "linear": Rope("linear", 1e4, factor=4.0),
+    "ntk": Rope("ntk", 1e4, factor=8.0),
+    "yarn": Rope("yarn", 1e4, factor=8.0, low_freq_factor=1.0, high_freq_factor=32.0,
+                 original_max_position=4096),
+}
+
+
+@pytest.mark.parametrize("key", [1, 3, 4, "linear", "ntk", "yarn"])
 def test_rope_table_and_apply(T, key):
     import torch
 
-    wl = get_workload(key)
+    wl = get_workload(key) if isinstance(key, int) else get_workload(4).scaled(
+        rope=_SCALED_ROPES[key])
     cfg = T.Config.from_workload(wl)
     max_pos = 40000
     table = torch.empty(max_pos * wl.head_dim, dtype=torch.float32, device="cuda")
@@ -71,7 +80,7 @@ def test_rope_table_and_apply(T, key):
         ulps = np.abs(got.view(np.int32).astype(np.int64) - want.view(np.int32).astype(np.int64))
         assert ulps.max() <= 1, "table entry more than 1 fp32 ulp from the oracle"
         assert (ulps != 0).mean() < 1e-4
-    rng = np.random.default_rng(key)
+    rng = np.random.default_rng(key if isinstance(key, int) else 10 + list(_SCALED_ROPES).index(key))
     x = rng.standard_normal((300, wl.head_dim)).astype(np.float16)
     pos = rng.integers(0, max_pos, 300).astype(np.int32)
     xd = torch.from_numpy(x).cuda()
@@ -157,6 +166,19 @@ def _small(key):
         return get_workload(5).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
                                       rope=Rope("none"), ragged=None, prompt_len=400,
                                       int4_budget=150, steps=6), None
+    # the scaled RoPE schemes under each eviction policy (re-positioning uses their tables)
+    if key == "rope_linear_pos":
+        return get_workload(4).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                      rope=_SCALED_ROPES["linear"], prompt_len=900,
+                                      int4_budget=300, steps=5), None
+    if key == "rope_ntk_h2o":
+        return get_workload(3).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                      rope=_SCALED_ROPES["ntk"], prompt_len=700,
+                                      int4_budget=250, steps=6), None
+    if key == "rope_yarn_ema":
+        return get_workload(5).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                      rope=_SCALED_ROPES["yarn"], ragged=(900, 1300),
+                                      prompt_len=1300, int4_budget=500, steps=5), None
     raise KeyError(key)
 
 
@@ -164,7 +186,8 @@ def _small(key):
                                  "d64_g8", "d128_g8", "d64_k2v4_h2o", "d128_k4v4_pos",
                                  "d64_k2v2_ema", "d128_k2v2_pos", "d64_k4v4_pos",
                                  "deg_nosink", "deg_w1_h2o", "deg_budget0", "deg_short_ragged",
-                                 "deg_norope_ema"])
+                                 "deg_norope_ema", "rope_linear_pos", "rope_ntk_h2o",
+                                 "rope_yarn_ema"])
 def test_lockstep_small_workloads(T, key):
     wl, cap = _small(key)
     ls = Lockstep(wl, mid_capacity=cap)

@@ -81,6 +81,43 @@ def test_llama3_bands_closed_form():
     assert np.all(np.diff(l3.astype(np.float64)) < 0)
 
 
+def test_linear_scaling_is_position_interpolation():
+    """Linear scaling rotates position p by the unscaled angle of position p / factor."""
+    d, base, factor = 128, 1e4, 4.0
+    lin = rope.inv_freq("linear", base, d, factor).astype(np.float64)
+    ref = rope.inv_freq("default", base, d).astype(np.float64)
+    for p in (4, 400, 40000):
+        assert np.allclose(p * lin, (p / factor) * ref, rtol=2 ** -22, atol=0)
+
+
+def test_ntk_keeps_the_highest_and_divides_the_lowest_frequency():
+    """NTK-aware scaling: pair 0 keeps frequency 1; the last pair's frequency is divided by
+    exactly the factor (closed form of base * factor^(d/(d-2)) at exponent -(d-2)/d)."""
+    for d, base, factor in [(64, 1e4, 8.0), (128, 5e5, 2.0)]:
+        ntk = rope.inv_freq("ntk", base, d, factor).astype(np.float64)
+        ref = rope.inv_freq("default", base, d).astype(np.float64)
+        assert ntk[0] == 1.0 == ref[0]
+        assert math.isclose(ref[-1] / ntk[-1], factor, rel_tol=2 ** -21)
+        assert np.all(ntk[1:-1] < ref[1:-1]) and np.all(ntk[1:-1] > ref[1:-1] / factor)
+
+
+def test_yarn_bands_over_rotations_per_context():
+    """YaRN (alpha = 1, beta = 32): pairs making more than beta rotations over the original
+    context keep their frequency, pairs making fewer than alpha are interpolated by the factor,
+    the ones between are blended (between the two values, monotone)."""
+    d, base, L, factor, alpha, beta = 128, 1e4, 4096, 8.0, 1.0, 32.0
+    yarn = rope.inv_freq("yarn", base, d, factor, alpha, beta, L)
+    ref = rope.inv_freq("default", base, d)
+    rot = L * ref.astype(np.float64) / (2 * math.pi)   # rotations over the original context
+    keep, interp = rot > beta, rot < alpha
+    assert keep.any() and interp.any() and (~keep & ~interp).any()
+    assert np.array_equal(yarn[keep], ref[keep])
+    assert np.allclose(ref[interp].astype(np.float64) / yarn[interp], factor, rtol=2 ** -22)
+    mid = ~keep & ~interp
+    assert np.all(yarn[mid] < ref[mid]) and np.all(yarn[mid] > ref[mid] / factor)
+    assert np.all(np.diff(yarn.astype(np.float64)) < 0)
+
+
 def test_scores_depend_only_on_relative_distance():
     rng = np.random.default_rng(4)
     q, k = rng.standard_normal(128), rng.standard_normal(128)

@@ -65,14 +65,16 @@ fade_status_t validate_config(const fade_config_t* c) {
                      "precedes eviction)",
                      c->mid_capacity, c->int4_budget + 1);
   const fade_rope_t& r = c->rope;
-  if (r.kind < FADE_ROPE_NONE || r.kind > FADE_ROPE_LLAMA3)
+  if (r.kind < FADE_ROPE_NONE || r.kind > FADE_ROPE_YARN)
     return set_error(FADE_ERR_UNSUPPORTED, "unknown rope kind %d", r.kind);
   if (r.kind != FADE_ROPE_NONE && !(r.base > 1.0))
     return set_error(FADE_ERR_INVALID_ARGUMENT, "rope base must exceed 1");
-  if (r.kind == FADE_ROPE_LLAMA3 &&
+  if ((r.kind == FADE_ROPE_LLAMA3 || r.kind == FADE_ROPE_YARN) &&
       !(r.factor > 0.0 && r.low_freq_factor > 0.0 && r.high_freq_factor > r.low_freq_factor &&
         r.original_max_position > 0))
-    return set_error(FADE_ERR_INVALID_ARGUMENT, "bad llama3 rope scaling parameters");
+    return set_error(FADE_ERR_INVALID_ARGUMENT, "bad llama3 / yarn rope scaling parameters");
+  if ((r.kind == FADE_ROPE_LINEAR || r.kind == FADE_ROPE_NTK) && !(r.factor > 0.0))
+    return set_error(FADE_ERR_INVALID_ARGUMENT, "rope scaling factor must be positive");
   return FADE_OK;
 }
 

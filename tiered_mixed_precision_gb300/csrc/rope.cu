@@ -1,6 +1,8 @@
 // RoPE table and rotation of q/k to cache positions.
 // Sources: page "FADE：面向LLM推理的注意力感知分层KV缓存压缩技术", §RoPE重计算 (float32 RoPE math,
-// cast through the model dtype) and §RoPE方案兼容性 (standard RoPE and llama3 scaling); page
+// cast through the model dtype) and §RoPE方案兼容性 (standard RoPE; llama3, linear, ntk and yarn
+// scaling, as their published definitions: position interpolation, NTK-aware base scaling and
+// YaRN's ramp over rotations per original context); page
 // "探秘Transformer系列之（25）--- KV Cache优化之处理长文本序列", §1.2.2 StreamingLLM (positions are
 // indices inside the cache).
 #include <math.h>
@@ -14,15 +16,20 @@ struct InvFreq {
   float v[64];  // d/2 <= 64
 };
 
-// inv_freq_i = base^(-2i/d) in fp64, llama3-adjusted in fp64, rounded once to fp32.
-// Host code: compiled without floating-point contraction so every step rounds as written.
+// inv_freq_i in fp64 per the scheme (fade_rope_kind_t), rounded once to fp32. Host code:
+// compiled without floating-point contraction so every step rounds as written.
 InvFreq host_inv_freq(const fade_config_t* c) {
   InvFreq f{};
   const int half = c->head_dim / 2;
   const fade_rope_t& r = c->rope;
+  // NTK-aware scaling raises the base so that the lowest frequency is divided by the factor
+  const double base = r.kind == FADE_ROPE_NTK
+                          ? r.base * pow(r.factor, (double)c->head_dim / (c->head_dim - 2))
+                          : r.base;
   for (int i = 0; i < half; ++i) {
-    double x = pow(r.base, -(2.0 * i) / c->head_dim);
-    if (r.kind == FADE_ROPE_LLAMA3) {
+    double x = pow(base, -(2.0 * i) / c->head_dim);
+    if (r.kind == FADE_ROPE_LINEAR) x = x / r.factor;
+    if (r.kind == FADE_ROPE_LLAMA3 || r.kind == FADE_ROPE_YARN) {
       const double lam = 2.0 * M_PI / x;
       const double L = (double)r.original_max_position;
       const double low_wl = L / r.low_freq_factor;
