@@ -66,6 +66,57 @@ class FadeCache:
         self._graph_events = []  # timing events referenced by captured graphs
         self.launches = 0       # kernels enqueued by step_layer calls
 
+    # ------------------------------------------------------------------ session persistence
+    # Page "FADE：面向LLM推理的注意力感知分层KV缓存压缩技术", §会话持久化: the compressed cache is
+    # saved and restored (cache_state_dict / load_cache_state_dict, then torch.save / torch.load).
+    _STATE_BUFFERS = ("sink_k", "sink_v", "recent_k", "recent_v", "mid_k_codes", "mid_k_scales",
+                      "mid_v_codes", "mid_v_scales", "sink_scores", "mid_scores", "recent_scores",
+                      "meta")
+    _CONFIG_FIELDS = ("batch", "num_q_heads", "num_kv_heads", "head_dim", "n_sink",
+                      "recent_window", "int4_budget", "middle_k_bits", "middle_v_bits",
+                      "mid_capacity", "policy", "ema_decay", "rope_kind", "rope_base",
+                      "rope_factor", "rope_low_freq_factor", "rope_high_freq_factor",
+                      "rope_original_max_position")
+
+    def cache_state_dict(self) -> dict:
+        """Every layer's tier buffers (both middle buffers and the device metadata, which says
+        which one is live) and host tier counts, copied to host memory, with the configuration
+        and sizes; only tensors, numbers and strings, so torch.load(weights_only=True) reads
+        it. Pending work on the current stream is finished first."""
+        layers = []
+        for L in self.layers:
+            d = {}
+            for name in self._STATE_BUFFERS:
+                v = getattr(L, name)
+                d[name] = [t.cpu() for t in v] if isinstance(v, list) else v.cpu()
+            for name in ("h_n_sink", "h_n_mid", "h_n_recent"):
+                d[name] = torch.from_numpy(getattr(L, name).copy())
+            layers.append(d)
+        return {"config": {f: getattr(self.cfg, f) for f in self._CONFIG_FIELDS},
+                "num_layers": len(self.layers), "max_prompt": self.max_prompt,
+                "max_pos": self.max_pos, "layers": layers}
+
+    def load_cache_state_dict(self, sd: dict):
+        """Restore a state saved by cache_state_dict into this cache, which must have been made
+        with the same configuration, layer count and sizes (ValueError otherwise)."""
+        mine = {f: getattr(self.cfg, f) for f in self._CONFIG_FIELDS}
+        if sd["config"] != mine:
+            raise ValueError(f"configuration differs: saved {sd['config']}, this cache {mine}")
+        if (sd["num_layers"], sd["max_prompt"], sd["max_pos"]) != (
+                len(self.layers), self.max_prompt, self.max_pos):
+            raise ValueError("layer count, max_prompt or max_pos differs from the saved cache")
+        for L, d in zip(self.layers, sd["layers"]):
+            for name in self._STATE_BUFFERS:
+                dst, src = getattr(L, name), d[name]
+                for t, u in (zip(dst, src) if isinstance(dst, list) else [(dst, src)]):
+                    if t.shape != u.shape or t.dtype != u.dtype:
+                        raise ValueError(f"buffer {name}: saved {tuple(u.shape)} {u.dtype}, "
+                                         f"this cache {tuple(t.shape)} {t.dtype}")
+                    t.copy_(u)
+            for name in ("h_n_sink", "h_n_mid", "h_n_recent"):
+                getattr(L, name)[:] = d[name].numpy()  # in place: the C struct points at them
+        torch.cuda.synchronize(self.device)
+
     # ------------------------------------------------------------------ pieces
     def rope_(self, x: torch.Tensor, n_groups: int, group_len: int, pos_start=None, pos_step=1):
         """Rotate x in place (fp16 [n_groups][group_len][d])."""
