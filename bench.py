@@ -57,6 +57,9 @@ def parse_args():
                    help="streams that take the layers' maintenance in turn (pipelined schedule); "
                         "0 = one when a layer's middle tier fills the GPU (at least 2^20 "
                         "token-heads), else two")
+    p.add_argument("--shared-rows", action="store_true",
+                   help="the rows share their tier decisions (row-summed scores; rows of equal "
+                        "length)")
     p.add_argument("--no-pipeline", action="store_true",
                    help="in the graph, run each layer's maintenance before its attention instead "
                         "of overlapping it with the following layers")
@@ -292,6 +295,10 @@ def run_ours(args, rank, world):
     else:  # without eviction the middle tier grows by one token per step
         cfg = Config.from_workload(
             wl, mid_capacity=max(1, maxP + nsteps - wl.n_sink - wl.recent_window))
+    if args.shared_rows:
+        import dataclasses
+
+        cfg = dataclasses.replace(cfg, shared_rows=True)
     max_pos = maxP + nsteps + 16
     fc = FadeCache(cfg, wl.layers, maxP, max_pos, dev)
     progress(f"cache allocated: {wl.name}, {wl.layers} layers")
@@ -495,6 +502,7 @@ def run_ours(args, rank, world):
                    "num_kv_heads": Hkv, "head_dim": d, "context": maxP, "n_sink": wl.n_sink,
                    "recent_window": wl.recent_window, "int4_budget": wl.int4_budget,
                    "policy": wl.policy, "k_bits": wl.middle_k_bits, "v_bits": wl.middle_v_bits,
+                   "shared_rows": bool(args.shared_rows),
                    "storage": "fp16 sinks/recent, packed INT4 K / INT2 V middle",
                    "l2": "no flush: the compressed cache read per step is far larger than L2",
                    "parallelism": f"replicas x{world} (rows independent, no collective)",

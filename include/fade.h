@@ -107,6 +107,12 @@ typedef struct {
                              (FADE_ERR_UNSUPPORTED otherwise) */
   int32_t policy;         /* fade_policy_t */
   float ema_decay;        /* EMA decay delta in [0, 1) */
+  int32_t shared_rows;    /* 0: tier decisions per (row, KV head); 1: the rows share them
+                             (FADE-zh §批处理支持: one allocation for all rows). Victims are
+                             then chosen per KV head by the row-summed scores (H2O, EMA; the
+                             prefill mass for H2O) and applied to every row; every row must hold
+                             equal tier counts (equal prompt lengths at prefill), otherwise
+                             FADE_ERR_INVALID_ARGUMENT. Each row keeps its own scores. */
   fade_rope_t rope;
 } fade_config_t;
 

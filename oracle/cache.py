@@ -236,11 +236,13 @@ class UnitCache:
         return out, p, logits, pos
 
     # -- prefill -----------------------------------------------------------------------
-    def prefill(self, k_raw16, v16, mass=None):
+    def prefill(self, k_raw16, v16, mass=None, select_mass=None):
         """Build the tiers from a raw prompt: k, v [P, d] fp16 (k pre-RoPE).
 
         ``mass`` [P] is the prefill attention mass (H2O key and initial score); it is
-        required for H2O and ignored otherwise. Returns the evicted prompt positions."""
+        required for H2O and ignored otherwise. ``select_mass`` [P], if given, is the key H2O
+        selects by instead (rows sharing their decisions: the mass summed over the rows); the
+        scores still start at ``mass``. Returns the evicted prompt positions."""
         if self.n_held:
             raise RuntimeError("prefill needs an empty cache")
         k_raw16 = np.asarray(k_raw16, np.float16)
@@ -260,7 +262,8 @@ class UnitCache:
             elif self.p.policy == "h2o":
                 if mass is None:
                     raise ValueError("H2O prefill needs the prefill attention mass")
-                victims = cand[pol.select_victims(np.asarray(mass)[cand], k)]
+                key = mass if select_mass is None else select_mass
+                victims = cand[pol.select_victims(np.asarray(key)[cand], k)]
             else:  # EMA: every score starts at zero
                 victims = cand[pol.select_victims(np.zeros(n_m), k)]
         keep = np.ones(P, bool)
@@ -287,6 +290,25 @@ class UnitCache:
         self.orig_pos = old.astype(np.int64)
         self.seen = P
         return victims
+
+
+def choose_shared_victims(units) -> np.ndarray:
+    """Batch-shared tier decisions (FADE-zh §批处理支持: all rows share their positions and tier
+    decisions): the victims of every row of one (layer, KV head), chosen once among the middle
+    candidates by the sum over the rows of each candidate's score (position policy: the oldest).
+    The rows must hold equal tier counts."""
+    u0 = units[0]
+    counts = (u0.n_sink, u0.n_mid, u0.n_recent)
+    if any((u.n_sink, u.n_mid, u.n_recent) != counts for u in units):
+        raise ValueError("rows sharing their decisions must hold equal tier counts")
+    if not u0.p.evicts or u0.n_mid <= u0.p.int4_budget:
+        return np.zeros(0, np.int64)
+    k = u0.n_mid - u0.p.int4_budget
+    if u0.p.policy == "position":
+        return pol.select_victims_position(u0.n_mid, k)
+    s0 = u0.n_sink
+    keys = np.sum([u.sigma[s0:s0 + u0.n_mid] for u in units], axis=0)
+    return pol.select_victims(keys, k)
 
 
 def packed_state(u: UnitCache) -> dict:

@@ -31,7 +31,10 @@ def allclose_report(got, ref, atol=ATOL, rtol=RTOL):
 class Lockstep:
     """Drives ``FadeCache`` and per-unit oracle caches over a workload."""
 
-    def __init__(self, wl, layers=None, steps=None, device="cuda", mid_capacity=None):
+    def __init__(self, wl, layers=None, steps=None, device="cuda", mid_capacity=None,
+                 shared_rows=False):
+        import dataclasses
+
         import torch
 
         from tiered_mixed_precision_gb300 import Config
@@ -44,7 +47,9 @@ class Lockstep:
         self.lens = ragged_context_lengths(wl)
         self.maxP = int(self.lens.max())
         self.max_pos = self.maxP + self.steps + 8
-        self.cfg = Config.from_workload(wl, mid_capacity=mid_capacity)
+        self.shared = shared_rows   # the rows share their tier decisions (row-summed scores)
+        self.cfg = dataclasses.replace(Config.from_workload(wl, mid_capacity=mid_capacity),
+                                       shared_rows=shared_rows)
         self.fc = FadeCache(self.cfg, self.L, self.maxP, self.max_pos, device)
         self.params = Params.from_workload(wl)
         self.rope = RopeTable.from_workload(wl, self.max_pos)
@@ -80,12 +85,16 @@ class Lockstep:
         v = torch.from_numpy(pr["v"]).to(dev)
         md = torch.from_numpy(mass).to(dev) if mass is not None else None
         self.fc.prefill(layer, k, v, self.lens, md)
+        sel = None
+        if mass is not None and self.shared:  # rows sharing decisions select by the row sum
+            sel = mass.astype(np.float64).sum(axis=0)
         for b in range(wl.batch):
             P = int(self.lens[b])
             for h in range(wl.num_kv_heads):
                 u = self.units[layer][b][h]
                 u.prefill(pr["k"][b, h, :P], pr["v"][b, h, :P],
-                          mass=None if mass is None else mass[b, h, :P].astype(np.float64))
+                          mass=None if mass is None else mass[b, h, :P].astype(np.float64),
+                          select_mass=None if sel is None else sel[h, :P])
 
     # -------------------------------------------------------------------- decode
     def step(self, check_state=True, evict=True):
@@ -122,11 +131,16 @@ class Lockstep:
                 self.fc.attend_layer(layer, q, k, v, out)
             victims_gpu = self._gpu_victims(layer)
             out_h = out.float().cpu().numpy()
+            shared_vic = {}
+            if self.shared and evict:
+                for h in range(wl.num_kv_heads):
+                    shared_vic[h] = self._shared_victims(layer, h, victims_gpu)
             for b in range(wl.batch):
                 for h in range(wl.num_kv_heads):
                     key = (layer, b, h)
                     u = self.units[layer][b][h]
-                    o_ref, tie = self._oracle_step(u, t, b, h, victims_gpu, key, evict)
+                    o_ref, tie = self._oracle_step(u, t, b, h, victims_gpu, key, evict,
+                                                   shared_vic.get(h))
                     if key in self.diverged:
                         continue
                     ok, err, nbad = allclose_report(out_h[b, h * G:(h + 1) * G], o_ref)
@@ -143,8 +157,42 @@ class Lockstep:
         its selection bitmap, or None for units without an eviction."""
         return self.fc.layers[layer].victims.cpu().numpy().view(np.uint32)
 
-    def _oracle_step(self, u, t, b, h, bm, key, evict=True):
+    def _shared_victims(self, layer, h, bm):
+        """Rows sharing their decisions: demote every row of (layer, h), choose the victims
+        once by the row-summed scores, check that the GPU gave every row the same set and that
+        it equals this one (up to an fp32-vs-fp64 near-tie, which the oracle then adopts)."""
+        from oracle.cache import choose_shared_victims
+
+        units = [self.units[layer][b][h] for b in range(self.wl.batch)]
+        for u in units:
+            u.demote()
+        vic = choose_shared_victims(units)
+        n_mid = units[0].n_mid
+        if vic.size == 0 or self.wl.policy == "position":  # no bitmap: the oldest go
+            return vic
+        words = [bm[b, h, :(n_mid + 31) // 32] for b in range(self.wl.batch)]
+        assert all(np.array_equal(w, words[0]) for w in words), "rows got different victims"
+        bits = np.unpackbits(words[0].view(np.uint8), bitorder="little")[:n_mid]
+        gpu_vic = np.nonzero(bits)[0]
+        if not np.array_equal(np.sort(gpu_vic), np.sort(vic)):
+            s0 = units[0].n_sink
+            keys = np.sum([u.sigma[s0:s0 + n_mid] for u in units], axis=0)
+            a, g = np.sort(keys[vic]), np.sort(keys[gpu_vic])
+            assert gpu_vic.size == vic.size and np.allclose(a, g, rtol=TIE_RTOL, atol=1e-7), (
+                f"shared selection differs beyond a near-tie at layer {layer} head {h}")
+            self.near_ties += 1
+            vic = gpu_vic
+        return vic
+
+    def _oracle_step(self, u, t, b, h, bm, key, evict=True, shared_vic=None):
         G = self.wl.group
+        if shared_vic is not None:  # demoted and chosen for all rows by _shared_victims
+            u.evict(shared_vic)
+            pos = u.n_held
+            u.append(u.rope.apply(t["k"][b, h][None], pos), t["v"][b, h])
+            out, p, _ = u.attend(u.rope.apply(t["q"][b, h * G:(h + 1) * G], pos))
+            u.accumulate(p)
+            return out, False
         u.demote()
         n_mid = u.n_mid
         vic = u.choose_victims() if evict else np.zeros(0, np.int64)

@@ -220,6 +220,21 @@ def test_deferred_eviction_many_victims(T, policy, skip):
     assert ls.near_ties <= 1
 
 
+@pytest.mark.parametrize("policy", ["h2o", "ema", "position"])
+def test_shared_row_decisions_lockstep(T, policy):
+    """Rows sharing their tier decisions (FADE-zh §批处理支持): the victims of every row of a
+    KV head come from the row-summed scores (H2O: the row-summed prefill mass at prefill)."""
+    base = {"h2o": 3, "ema": 5, "position": 4}[policy]
+    wl = get_workload(base).scaled(layers=1, batch=3, num_q_heads=8, num_kv_heads=2,
+                                   ragged=None, prompt_len=700, int4_budget=250, steps=8)
+    ls = Lockstep(wl, shared_rows=True)
+    ls.prefill(0)
+    ls.check_layer_state(0)
+    for _ in range(ls.steps):
+        ls.step()
+    assert ls.near_ties <= 1
+
+
 @pytest.mark.parametrize("key,P", [(3, 700), (3, 130)])
 def test_prefill_mass_matches_oracle(T, key, P):
     """GPU prefill attention mass vs the oracle's fp64 causal column sums."""

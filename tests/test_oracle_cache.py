@@ -219,3 +219,48 @@ def test_demoted_token_keeps_its_index_and_codes_are_its_quantisation():
     q, s = quant.quantize(oldest[None], 4)
     assert np.array_equal(u.mid_kq[0], q[0]) and np.array_equal(u.mid_ks[0], s[0])
     assert u.orig_pos[2] == 2
+
+
+def _units_with_scores(rows_sigma, S=2, W=4, budget=3, policy="h2o"):
+    """Units of one (layer, KV head) whose middle tiers hold len(sigma) tokens with the given
+    scores (one unit per row)."""
+    from oracle.cache import choose_shared_victims  # noqa: F401  (imported by the tests)
+    units = []
+    wl = _tiny_wl(n_sink=S, recent_window=W)
+    n_mid = len(rows_sigma[0])
+    pr = draw_prompt(wl, 0, S + n_mid + W)
+    for sig in rows_sigma:
+        u = _unit(S=S, W=W, budget=-1, policy="none")
+        u.prefill(pr["k"][0, 0], pr["v"][0, 0])
+        u.p = Params(64, 4, S, W, budget, policy, 4, 2, 0.9)
+        u.sigma = np.concatenate([np.zeros(S), np.asarray(sig, np.float64), np.zeros(W)])
+        units.append(u)
+    return units
+
+
+def test_shared_victims_reduce_to_one_row_and_to_identical_rows():
+    from oracle.cache import choose_shared_victims
+
+    rng = np.random.default_rng(11)
+    sig = rng.random(9)
+    one = _units_with_scores([sig])
+    assert np.array_equal(choose_shared_victims(one), one[0].choose_victims())
+    same = _units_with_scores([sig] * 4)           # identical rows: the same choice
+    assert np.array_equal(choose_shared_victims(same), one[0].choose_victims())
+
+
+def test_shared_victims_follow_the_row_sum_not_any_row():
+    from oracle.cache import choose_shared_victims
+
+    # row 0 alone would drop index 0, row 1 alone index 2; their sums [10, 6, 10, ...] drop 1
+    rows = [[1.0, 3.0, 9.0, 20.0, 20.0], [9.0, 3.0, 1.0, 20.0, 20.0]]
+    units = _units_with_scores(rows, budget=4)
+    assert list(units[0].choose_victims()) == [0] and list(units[1].choose_victims()) == [2]
+    assert list(choose_shared_victims(units)) == [1]
+    # equal sums: the lower index goes first, as for one row
+    tie = _units_with_scores([[1.0, 5.0, 9.0], [9.0, 5.0, 1.0]], budget=2)
+    assert list(choose_shared_victims(tie)) == [0]
+    # rows with different tier counts cannot share decisions
+    bad = _units_with_scores([[1.0, 2.0, 3.0]]) + _units_with_scores([[1.0, 2.0, 3.0, 4.0]])
+    with pytest.raises(ValueError):
+        choose_shared_victims(bad)

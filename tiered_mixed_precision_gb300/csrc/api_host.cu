@@ -50,6 +50,8 @@ fade_status_t validate_config(const fade_config_t* c) {
                      c->middle_k_bits, c->middle_v_bits);
   if (c->policy < FADE_EVICT_NONE || c->policy > FADE_EVICT_POSITION)
     return set_error(FADE_ERR_INVALID_ARGUMENT, "unknown eviction policy %d", c->policy);
+  if (c->shared_rows != 0 && c->shared_rows != 1)
+    return set_error(FADE_ERR_INVALID_ARGUMENT, "shared_rows must be 0 or 1");
   if (!(c->ema_decay >= 0.f && c->ema_decay < 1.f))
     return set_error(FADE_ERR_INVALID_ARGUMENT, "ema_decay must lie in [0, 1)");
   if (c->mid_capacity < 1)

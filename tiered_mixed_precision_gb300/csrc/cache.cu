@@ -46,13 +46,32 @@ __device__ __forceinline__ int block_excl_count(bool f, int* sh /*[33]*/, int& t
   return r;
 }
 
+// Selection keys: one unit's scores, or (rows sharing their tier decisions) the sum over the
+// batch rows of the same candidate's scores, added in ascending row order in fp32. `p` null:
+// every key equal (the oldest go first).
+struct KeysOne {
+  const float* p;
+  __device__ float operator()(int i) const { return p[i]; }
+};
+struct KeysRows {
+  const float* p;   // row 0's scores of the unit
+  size_t stride;    // floats from one row's unit to the next row's
+  int rows;
+  __device__ float operator()(int i) const {
+    float s = p[i];
+    for (int r = 1; r < rows; ++r) s += p[(size_t)r * stride + i];
+    return s;
+  }
+};
+
 // Selects the k smallest (key, index) among n candidates with one CTA of kSelThreads
 // threads: an exact 4-pass radix select finds the k-th smallest key T, then one pass in index
 // order marks keys < T and the first (k - #below) keys equal to T. keys == nullptr means all
 // keys are equal (the oldest k go first). Writes bitmap words [0, ceil(n/32)) and
 // chunk_base[c] = victims among candidates [0, c*kChunk), c = 0..ceil(n/kChunk).
-__device__ void block_select(const float* __restrict__ keys, int n, int k,
-                             uint32_t* __restrict__ bitmap, int32_t* __restrict__ chunk_base) {
+template <class Keys>
+__device__ void block_select(Keys keys, int n, int k, uint32_t* __restrict__ bitmap,
+                             int32_t* __restrict__ chunk_base) {
   __shared__ uint32_t hist[256];
   __shared__ uint32_t s_prefix;
   __shared__ int s_rem;
@@ -60,14 +79,14 @@ __device__ void block_select(const float* __restrict__ keys, int n, int k,
   const int tid = threadIdx.x;
   uint32_t T = ord_key(0.f);
   int remaining = k;
-  if (keys && k > 0) {
+  if (keys.p && k > 0) {
     uint32_t prefix = 0, mask = 0;
     int rem = k;
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
       __syncthreads();
       for (int i = tid; i < n; i += blockDim.x) {
-        const uint32_t u = ord_key(keys[i]);
+        const uint32_t u = ord_key(keys(i));
         if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
       }
       __syncthreads();
@@ -96,7 +115,7 @@ __device__ void block_select(const float* __restrict__ keys, int n, int k,
   for (int base = 0; base < n; base += kSelThreads) {
     const int i = base + tid;
     const bool valid = i < n;
-    const uint32_t u = valid ? (keys ? ord_key(keys[i]) : T) : 0u;
+    const uint32_t u = valid ? (keys.p ? ord_key(keys(i)) : T) : 0u;
     const bool eq = valid && k > 0 && u == T;
     int eq_tot;
     const int eq_rank = block_excl_count(eq, sh, eq_tot) + eq_carry;
@@ -115,15 +134,16 @@ __device__ void block_select(const float* __restrict__ keys, int n, int k,
 // block_select for k = 1 (one victim: the steady state of a decode step) in one pass: the
 // smallest (key, index) pair, i.e. the lowest index among the smallest keys, by a block-wide
 // minimum over 64-bit (ordered key, index) words; then the bitmap and the chunk prefixes.
-__device__ void block_select_one(const float* __restrict__ keys, int n,
-                                 uint32_t* __restrict__ bitmap, int32_t* __restrict__ chunk_base) {
+template <class Keys>
+__device__ void block_select_one(Keys keys, int n, uint32_t* __restrict__ bitmap,
+                                 int32_t* __restrict__ chunk_base) {
   __shared__ unsigned long long s_best[kSelThreads / 32];
   __shared__ int s_victim;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   unsigned long long best = ~0ull;
-  if (keys) {
+  if (keys.p) {
     for (int i = tid; i < n; i += kSelThreads) {
-      const unsigned long long c = ((unsigned long long)ord_key(keys[i]) << 32) | (uint32_t)i;
+      const unsigned long long c = ((unsigned long long)ord_key(keys(i)) << 32) | (uint32_t)i;
       best = c < best ? c : best;
     }
   } else if (tid == 0) {
@@ -179,6 +199,8 @@ struct LayerArgs {
   int H, S, W, C, budget, policy;
   bool evicts;
   bool positional;  // position policy: the victims are the oldest middle slots (no selection)
+  bool shared;      // the rows share their tier decisions (row-summed selection keys)
+  int B;            // batch rows
   const float* table;   // nullptr: RoPE kind NONE (re-positioning is the identity)
   int half;
 };
@@ -211,6 +233,8 @@ LayerArgs make_args(const fade_config_t* c, const fade_layer_t* L, const float* 
   a.policy = c->policy;
   a.evicts = c->policy != FADE_EVICT_NONE && c->int4_budget >= 0;
   a.positional = c->policy == FADE_EVICT_POSITION;
+  a.shared = c->shared_rows != 0;
+  a.B = c->batch;
   a.table = (c->rope.kind == FADE_ROPE_NONE) ? nullptr : table;
   a.half = c->head_dim / 2;
   return a;
@@ -373,23 +397,51 @@ __global__ void __launch_bounds__(32) append_kernel(LayerArgs a, const uint16_t*
 
 // ----------------------------------------------------------------- eviction (decode)
 // One CTA per unit: choose N_MID - budget victims among the live middle tier.
+// Copies unit `from`'s victim bitmap (n candidates) and chunk prefixes to unit `to`.
+__device__ void copy_selection(const LayerArgs& a, int from, int to, int n) {
+  const uint32_t* bs = a.victims + (size_t)from * a.victim_words;
+  uint32_t* bd = a.victims + (size_t)to * a.victim_words;
+  for (int w = threadIdx.x; w < (n + 31) / 32; w += blockDim.x) bd[w] = bs[w];
+  const int32_t* cs = a.chunk_base + (size_t)from * a.chunk_slots;
+  int32_t* cd = a.chunk_base + (size_t)to * a.chunk_slots;
+  for (int c = threadIdx.x; c <= (n + kChunk - 1) / kChunk; c += blockDim.x) cd[c] = cs[c];
+}
+
+// grid = (H, B) with one CTA per unit; rows sharing their decisions: grid = (H, 1), the CTA
+// selects by the row-summed scores of head h and gives every row the same victims (the rows
+// hold equal counts and evolve alike, so their live buffers agree).
 __global__ void __launch_bounds__(kSelThreads) evict_select_kernel(LayerArgs a) {
   const int unit = blockIdx.y * a.H + blockIdx.x;
   int32_t* m = a.meta + unit * kF;
   const int n_mid = m[FADE_META_N_MID], cur = m[FADE_META_CUR];
   const int k = (a.evicts && n_mid > a.budget) ? n_mid - a.budget : 0;
   __syncthreads();
-  if (threadIdx.x == 0) m[FADE_META_N_EV] = k;
+  if (threadIdx.x == 0) {
+    m[FADE_META_N_EV] = k;
+    if (a.shared)
+      for (int r = 1; r < a.B; ++r) a.meta[(r * a.H + blockIdx.x) * kF + FADE_META_N_EV] = k;
+  }
   if (k == 0) return;
-  const float* keys = (a.policy == FADE_EVICT_POSITION)
-                          ? nullptr
-                          : (cur ? a.mid_sc[1] : a.mid_sc[0]) + (size_t)unit * a.C;
-  if (k == 1)
-    block_select_one(keys, n_mid, a.victims + (size_t)unit * a.victim_words,
-                     a.chunk_base + (size_t)unit * a.chunk_slots);
-  else
-    block_select(keys, n_mid, k, a.victims + (size_t)unit * a.victim_words,
-                 a.chunk_base + (size_t)unit * a.chunk_slots);
+  const float* sc = (a.policy == FADE_EVICT_POSITION)
+                        ? nullptr
+                        : (cur ? a.mid_sc[1] : a.mid_sc[0]) + (size_t)unit * a.C;
+  uint32_t* bm = a.victims + (size_t)unit * a.victim_words;
+  int32_t* cb = a.chunk_base + (size_t)unit * a.chunk_slots;
+  if (a.shared) {
+    const KeysRows keys{sc, (size_t)a.H * a.C, a.B};
+    if (k == 1)
+      block_select_one(keys, n_mid, bm, cb);
+    else
+      block_select(keys, n_mid, k, bm, cb);
+    __syncthreads();
+    for (int r = 1; r < a.B; ++r) copy_selection(a, unit, r * a.H + blockIdx.x, n_mid);
+  } else {
+    const KeysOne keys{sc};
+    if (k == 1)
+      block_select_one(keys, n_mid, bm, cb);
+    else
+      block_select(keys, n_mid, k, bm, cb);
+  }
 }
 
 // 8 consecutive fp16 values (16-byte aligned) as 4 packed fp32 pairs, and back (RN to fp16).
@@ -946,15 +998,24 @@ __device__ __forceinline__ PrefillSplit prefill_split(const LayerArgs& a, int P)
   return s;
 }
 
+// grid = (H, B); rows sharing their decisions (equal prompt lengths): grid = (H, 1), the
+// row-summed prefill mass decides and every row gets the same victims.
 __global__ void __launch_bounds__(kSelThreads) prefill_select_kernel(LayerArgs a, PrefillArgs p,
                                                                      RowLens lens) {
   const int unit = blockIdx.y * a.H + blockIdx.x;
   const PrefillSplit s = prefill_split(a, lens.v[blockIdx.y]);
   if (s.k == 0) return;
-  const float* keys = (a.policy == FADE_EVICT_H2O) ? p.mass + (size_t)unit * p.maxP + s.n_s
+  const float* mass = (a.policy == FADE_EVICT_H2O) ? p.mass + (size_t)unit * p.maxP + s.n_s
                                                    : nullptr;  // EMA: all 0; position: index
-  block_select(keys, s.n_m0, s.k, a.victims + (size_t)unit * a.victim_words,
-               a.chunk_base + (size_t)unit * a.chunk_slots);
+  uint32_t* bm = a.victims + (size_t)unit * a.victim_words;
+  int32_t* cb = a.chunk_base + (size_t)unit * a.chunk_slots;
+  if (a.shared) {
+    block_select(KeysRows{mass, (size_t)a.H * p.maxP, a.B}, s.n_m0, s.k, bm, cb);
+    __syncthreads();
+    for (int r = 1; r < a.B; ++r) copy_selection(a, unit, r * a.H + blockIdx.x, s.n_m0);
+  } else {
+    block_select(KeysOne{mass}, s.n_m0, s.k, bm, cb);
+  }
 }
 
 // grid = (ceil(maxP / kChunk), H, B), 8 warps; one warp per prompt token.
@@ -1158,10 +1219,17 @@ extern "C" fade_status_t fade_cache_prefill(const fade_config_t* c, fade_layer_t
       return set_error(FADE_ERR_CAPACITY, "row %d needs %d middle slots, capacity %d", b, n_m,
                        c->mid_capacity);
   }
+  if (c->shared_rows)
+    for (int b = 1; b < c->batch; ++b)
+      if (lens.v[b] != lens.v[0])
+        return set_error(FADE_ERR_INVALID_ARGUMENT,
+                         "rows sharing their tier decisions need equal prompt lengths "
+                         "(row %d: %d, row 0: %d)", b, lens.v[b], lens.v[0]);
   const LayerArgs a = make_args(c, L, table);
   const PrefillArgs p{k_rot, v, mass, max_prompt};
   cudaStream_t s = as_stream(stream);
-  prefill_select_kernel<<<dim3(c->num_kv_heads, c->batch), kSelThreads, 0, s>>>(a, p, lens);
+  prefill_select_kernel<<<dim3(c->num_kv_heads, c->shared_rows ? 1 : c->batch), kSelThreads, 0,
+                          s>>>(a, p, lens);
   if ((st = launch_status("fade_cache_prefill select"))) return st;
   if ((st = dispatch_dkv<PlaceLaunch>(c, a, p, lens, c->batch, s))) return st;
   const int units = c->batch * c->num_kv_heads;
@@ -1247,6 +1315,12 @@ extern "C" fade_status_t fade_evict_rerope(const fade_config_t* c, fade_layer_t*
     if (L->h_n_mid[b] > c->int4_budget) any = true;
   }
   if (!any) return FADE_OK;
+  if (c->shared_rows)
+    for (int b = 1; b < c->batch; ++b)
+      if (L->h_n_sink[b] != L->h_n_sink[0] || L->h_n_mid[b] != L->h_n_mid[0] ||
+          L->h_n_recent[b] != L->h_n_recent[0])
+        return set_error(FADE_ERR_INVALID_ARGUMENT,
+                         "rows sharing their tier decisions need equal tier counts (row %d)", b);
   if ((long long)L->victim_words < (c->mid_capacity + 31) / 32 + 1 ||
       (long long)L->chunk_slots < (c->mid_capacity + kChunk - 1) / kChunk + 1)
     return set_error(FADE_ERR_CAPACITY, "scratch buffers are smaller than the middle tier");
@@ -1255,7 +1329,8 @@ extern "C" fade_status_t fade_evict_rerope(const fade_config_t* c, fade_layer_t*
   const LayerArgs a = make_args(c, L, table);
   cudaStream_t s = as_stream(stream);
   if (!a.positional) {  // the position policy needs no selection pass
-    evict_select_kernel<<<dim3(c->num_kv_heads, c->batch), kSelThreads, 0, s>>>(a);
+    evict_select_kernel<<<dim3(c->num_kv_heads, c->shared_rows ? 1 : c->batch), kSelThreads, 0,
+                          s>>>(a);
     if ((st = launch_status("fade_evict_rerope select"))) return st;
   }
   const int ctok = c->head_dim == 128 ? compact_tok<128>() : compact_tok<64>();

@@ -46,7 +46,7 @@ class ConfigT(ctypes.Structure):
                 ("head_dim", c_i32), ("n_sink", c_i32), ("recent_window", c_i32),
                 ("int4_budget", c_i32), ("middle_k_bits", c_i32), ("middle_v_bits", c_i32),
                 ("mid_capacity", c_i32), ("policy", c_i32), ("ema_decay", c_f32),
-                ("rope", RopeT)]
+                ("shared_rows", c_i32), ("rope", RopeT)]
 
 
 class LayerT(ctypes.Structure):
@@ -152,6 +152,7 @@ class Config:
     rope_low_freq_factor: float = 1.0
     rope_high_freq_factor: float = 4.0
     rope_original_max_position: int = 8192
+    shared_rows: bool = False  # the rows share their tier decisions (row-summed scores)
     _c: ConfigT = field(default=None, repr=False, compare=False)
 
     def c(self) -> ConfigT:
@@ -160,7 +161,7 @@ class Config:
         self._c = ConfigT(self.batch, self.num_q_heads, self.num_kv_heads, self.head_dim,
                           self.n_sink, self.recent_window, self.int4_budget,
                           self.middle_k_bits, self.middle_v_bits, self.mid_capacity,
-                          POLICIES[self.policy], self.ema_decay, r)
+                          POLICIES[self.policy], self.ema_decay, int(self.shared_rows), r)
         return self._c
 
     @property
