@@ -24,4 +24,4 @@ pages pin only by model-quality figures (greedy match, coherence) have no parity
 "parity unpinned".
 """
 
-from . import accounting, attention, cache, policy, quant, rope  # noqa: F401
+from . import accounting, attention, cache, policy, pq, quant, rope  # noqa: F401

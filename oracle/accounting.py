@@ -8,7 +8,9 @@ compression; §性能基准 gives two measured KV sizes (Qwen2.5-3B 12.2 -> 4.0 
 
 Layout being counted (the spec's): FP16 tokens store K and V at 2 bytes per channel; a middle
 token stores d*k_bits/8 + d*v_bits/8 code bytes plus one fp16 scale per 32 channels for K and
-for V. The FP16 baseline stores every token ever seen at 4*d bytes.
+for V. With product-quantised V (FADE-zh §产品量化) a middle token's V is d/4 code bytes and
+no scale (the per-layer codebook, 256*d fp16 values, is a fixed cost counted apart). The FP16
+baseline stores every token ever seen at 4*d bytes.
 """
 
 from __future__ import annotations
@@ -18,9 +20,17 @@ def fp16_token_bytes(head_dim: int) -> int:
     return 4 * head_dim
 
 
-def middle_token_bytes(head_dim: int, k_bits: int, v_bits: int, group: int = 32) -> int:
+def middle_token_bytes(head_dim: int, k_bits: int, v_bits: int, group: int = 32,
+                       v_codec: str = "int") -> int:
     scales = 2 * (head_dim // group)
+    if v_codec == "pq":
+        return head_dim * k_bits // 8 + scales + head_dim // 4
     return head_dim * k_bits // 8 + scales + head_dim * v_bits // 8 + scales
+
+
+def pq_codebook_bytes(head_dim: int) -> int:
+    """One layer's PQ codebook: 256 centroids of every 4-channel sub-space, fp16."""
+    return 256 * head_dim * 2
 
 
 def unit_bytes(head_dim, n_fp16, n_mid, k_bits, v_bits) -> int:

@@ -24,6 +24,8 @@ Step order per decode step (reading; the pages do not order the steps):
      the new one included;
   5. accumulate: H2O or EMA scores take the step's probabilities.
 ``int4_budget`` counts middle tokens only; evicted tokens are dropped, not demoted further.
+With ``v_codec="pq"`` (FADE-zh §产品量化, the alternative to INT2) the middle tier's V is
+product-quantised with a per-layer codebook (pq.py) instead of INT{v_bits}.
 Prefill (reading): the prompt's keys are RoPE'd at 0..P-1; sinks are the first n_sink, the
 recent window the last recent_window, the rest are middle candidates; the excess over the
 budget is evicted by the policy key (H2O: prefill attention mass, EMA: all zero, so the
@@ -40,7 +42,7 @@ from dataclasses import dataclass
 
 import numpy as np
 
-from . import attention, policy as pol, quant
+from . import attention, policy as pol, pq, quant
 from .rope import RopeTable
 
 
@@ -55,11 +57,13 @@ class Params:
     k_bits: int
     v_bits: int
     ema_decay: float = 0.9
+    v_codec: str = "int"    # "int": INT{v_bits} V; "pq": product-quantised V (pq.py)
 
     @classmethod
     def from_workload(cls, wl) -> "Params":
         return cls(wl.head_dim, wl.group, wl.n_sink, wl.recent_window, wl.int4_budget,
-                   wl.policy, wl.middle_k_bits, wl.middle_v_bits, wl.ema_decay)
+                   wl.policy, wl.middle_k_bits, wl.middle_v_bits, wl.ema_decay,
+                   getattr(wl, "v_codec", "int"))
 
     @property
     def evicts(self) -> bool:
@@ -72,15 +76,21 @@ class UnitCache:
     Arrays are kept in cache-index (logical) order: sinks, then middle, then recent, oldest
     first. ``orig_pos`` records each held token's position in the original sequence."""
 
-    def __init__(self, params: Params, rope: RopeTable):
+    def __init__(self, params: Params, rope: RopeTable, codebook=None):
         p = self.p = params
         d = p.head_dim
         self.rope = rope
+        if p.v_codec not in ("int", "pq"):
+            raise ValueError("v_codec must be 'int' or 'pq'")
+        if p.v_codec == "pq" and codebook is None:
+            raise ValueError("PQ-coded V needs a codebook")
+        self.codebook = None if codebook is None else np.asarray(codebook, np.float16)
         self.sink_k = np.zeros((0, d), np.float16)
         self.sink_v = np.zeros((0, d), np.float16)
         self.mid_kq = np.zeros((0, d), np.int8)
         self.mid_ks = np.zeros((0, d // quant.GROUP), np.float16)
-        self.mid_vq = np.zeros((0, d), np.int8)
+        self.mid_vq = (np.zeros((0, d // pq.SUB), np.uint8) if p.v_codec == "pq"
+                       else np.zeros((0, d), np.int8))
         self.mid_vs = np.zeros((0, d // quant.GROUP), np.float16)
         self.rec_k = np.zeros((0, d), np.float16)
         self.rec_v = np.zeros((0, d), np.float16)
@@ -128,9 +138,21 @@ class UnitCache:
                                self.rec_k.astype(np.float64)])
 
     def values(self) -> np.ndarray:
-        return np.concatenate([self.sink_v.astype(np.float64),
-                               quant.dequantize(self.mid_vq, self.mid_vs),
+        if self.p.v_codec == "pq":
+            mid = pq.decode(self.mid_vq, self.codebook).astype(np.float64)
+        else:
+            mid = quant.dequantize(self.mid_vq, self.mid_vs)
+        return np.concatenate([self.sink_v.astype(np.float64), mid,
                                self.rec_v.astype(np.float64)])
+
+    def _code_v(self, v16: np.ndarray):
+        """Middle-tier V: INT codes and scales, or PQ codes and all-zero scales (a PQ row
+        carries no scale; the scale slots are kept so both codecs share one layout)."""
+        if self.p.v_codec == "pq":
+            v16 = np.asarray(v16, np.float16)
+            return (pq.encode(v16, self.codebook),
+                    np.zeros((v16.shape[0], self.p.head_dim // quant.GROUP), np.float16))
+        return quant.quantize(v16, self.p.v_bits)
 
     # -- step pieces -------------------------------------------------------------------
     def demote(self) -> bool:
@@ -138,7 +160,7 @@ class UnitCache:
         if not self._ring_full():
             return False
         kq, ks = quant.quantize(self.rec_k[:1], self.p.k_bits)
-        vq, vs = quant.quantize(self.rec_v[:1], self.p.v_bits)
+        vq, vs = self._code_v(self.rec_v[:1])
         self.mid_kq = np.concatenate([self.mid_kq, kq])
         self.mid_ks = np.concatenate([self.mid_ks, ks])
         self.mid_vq = np.concatenate([self.mid_vq, vq])
@@ -280,7 +302,7 @@ class UnitCache:
         self.sink_k, self.sink_v = k_new[:n_s].copy(), v_new[:n_s].copy()
         mk, mv = k_new[n_s:n_s + m_keep], v_new[n_s:n_s + m_keep]
         self.mid_kq, self.mid_ks = quant.quantize(mk, self.p.k_bits)
-        self.mid_vq, self.mid_vs = quant.quantize(mv, self.p.v_bits)
+        self.mid_vq, self.mid_vs = self._code_v(mv)
         self.rec_k = k_new[n_s + m_keep:].copy()
         self.rec_v = v_new[n_s + m_keep:].copy()
         if self.p.policy == "h2o":
@@ -316,6 +338,7 @@ def packed_state(u: UnitCache) -> dict:
     return {
         "sink_k": u.sink_k, "sink_v": u.sink_v,
         "mid_k_codes": quant.pack(u.mid_kq, u.p.k_bits), "mid_k_scales": u.mid_ks,
-        "mid_v_codes": quant.pack(u.mid_vq, u.p.v_bits), "mid_v_scales": u.mid_vs,
+        "mid_v_codes": (u.mid_vq if u.p.v_codec == "pq" else quant.pack(u.mid_vq, u.p.v_bits)),
+        "mid_v_scales": u.mid_vs,
         "recent_k": u.rec_k, "recent_v": u.rec_v, "sigma": u.sigma,
     }

@@ -25,7 +25,7 @@ import numpy as np
 
 from .workloads import Workload
 
-_KINDS = {"q": 1, "k": 2, "v": 3, "scores": 4, "ctx": 5, "mass": 6, "x": 7}
+_KINDS = {"q": 1, "k": 2, "v": 3, "scores": 4, "ctx": 5, "mass": 6, "x": 7, "pq": 8}
 
 
 def _seed(wl_seed: int, *parts) -> int:
@@ -172,3 +172,24 @@ def draw_codec_cases(n_vec: int, dim: int, seed: int) -> np.ndarray:
         if i < n_vec:
             x[(i * 7919) % n_vec] = s
     return x
+
+
+def pq_calibration(wl: Workload, n: int, *, backend="numpy", device=None):
+    """Calibration V rows for a PQ codebook: ``n`` fp16 [n][d] draws of the workload's V
+    recipe, from a stream of their own."""
+    return draw_vectors(wl, "v", (n, wl.head_dim), "pq_calibration", backend=backend,
+                        device=device)
+
+
+def pq_init_indices(n: int, seed: int) -> np.ndarray:
+    """The random draw that seeds k-means: 256 distinct row indices in [0, n) (n >= 256),
+    or 256 indices with repeats when n < 256."""
+    rng = np.random.Generator(np.random.PCG64(_seed(seed, _KINDS["pq"], n)))
+    return rng.choice(n, size=256, replace=n < 256).astype(np.int32)
+
+
+def pq_codebook(rng: np.random.Generator, head_dim: int, scale: float = 1.0) -> np.ndarray:
+    """A codebook-shaped draw, fp16 [head_dim/4][256][4] from N(0, scale^2): a stand-in for a
+    trained codebook where only its shape and value range matter."""
+    x = rng.standard_normal((head_dim // 4, 256, 4), dtype=np.float32) * np.float32(scale)
+    return x.astype(np.float16)
