@@ -33,6 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode-attn tokens/s (batch×steps) and achieved HBM GB/s vs GB300 peak"
+PQ_CALIB_ROWS, PQ_ITERS = 4096, 8   # --v-codec pq: calibration rows and k-means rounds
 _T0 = time.perf_counter()
 
 
@@ -60,6 +61,9 @@ def parse_args():
     p.add_argument("--shared-rows", action="store_true",
                    help="the rows share their tier decisions (row-summed scores; rows of equal "
                         "length)")
+    p.add_argument("--v-codec", default="int", choices=["int", "pq"],
+                   help="middle-tier V: INT codes with scales, or product-quantised (a codebook "
+                        "trained on the GPU from synthetic calibration rows before timing)")
     p.add_argument("--no-pipeline", action="store_true",
                    help="in the graph, run each layer's maintenance before its attention instead "
                         "of overlapping it with the following layers")
@@ -131,11 +135,20 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- bytes
+def mid_token_bytes(cfg):
+    """Bytes of one middle token: packed K with its scales, and V as INT codes with scales or
+    as d/4 PQ code bytes (the per-layer codebook comes from L2, not counted per token)."""
+    d = cfg.head_dim
+    if cfg.v_codec == "pq":
+        return d * cfg.middle_k_bits // 8 + 2 * (d // 32) + d // 4
+    return d * (cfg.middle_k_bits + cfg.middle_v_bits) // 8 + 2 * 2 * (d // 32)
+
+
 def attention_bytes(cfg, layer):
     """Algorithmic bytes of one fade_decode_attention call: every held token once (middle at
     its packed size with scales, FP16 tiers at 4d) plus q read and out written."""
     d = cfg.head_dim
-    mid_tok = d * (cfg.middle_k_bits + cfg.middle_v_bits) // 8 + 2 * 2 * (d // 32)
+    mid_tok = mid_token_bytes(cfg)
     units_fp16 = int((layer.h_n_sink + layer.h_n_recent).sum()) * cfg.num_kv_heads
     units_mid = int(layer.h_n_mid.sum()) * cfg.num_kv_heads
     return units_mid * mid_tok + units_fp16 * 4 * d + 2 * cfg.batch * cfg.num_q_heads * d * 2
@@ -146,7 +159,7 @@ def evict_bytes(cfg, layer, n_ev=1):
     scales, scores) read once and its survivors written once to the other buffer, plus the
     recent keys read and rewritten in place."""
     d = cfg.head_dim
-    mid_tok = d * (cfg.middle_k_bits + cfg.middle_v_bits) // 8 + 2 * 2 * (d // 32) + 4
+    mid_tok = mid_token_bytes(cfg) + 4
     H = cfg.num_kv_heads
     n_mid_after = int(layer.h_n_mid.sum())
     read = (n_mid_after + n_ev * cfg.batch) * mid_tok * H
@@ -277,6 +290,7 @@ def run_ours(args, rank, world):
     from tiered_mixed_precision_gb300 import Config, build
     from tiered_mixed_precision_gb300.model import FadeCache
     from synth import draw_prompt, draw_vectors, ragged_context_lengths
+    from synth.draws import pq_calibration, pq_init_indices
 
     build.build()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
@@ -299,9 +313,18 @@ def run_ours(args, rank, world):
         import dataclasses
 
         cfg = dataclasses.replace(cfg, shared_rows=True)
+    if args.v_codec == "pq":
+        import dataclasses
+
+        cfg = dataclasses.replace(cfg, v_codec="pq")
     max_pos = maxP + nsteps + 16
     fc = FadeCache(cfg, wl.layers, maxP, max_pos, dev)
     progress(f"cache allocated: {wl.name}, {wl.layers} layers")
+    if args.v_codec == "pq":   # one codebook, trained on the GPU, shared by every layer
+        calib = pq_calibration(wl, PQ_CALIB_ROWS, backend="torch", device=dev)
+        fc.train_pq_codebook(calib, pq_init_indices(PQ_CALIB_ROWS, wl.seed), PQ_ITERS)
+        del calib
+        progress("PQ codebook trained")
     h2o = wl.policy == "h2o" and wl.int4_budget >= 0
     for layer in range(wl.layers):
         # H2O: the prefill attention mass is computed on the GPU from the prompt's queries
@@ -427,13 +450,14 @@ def run_ours(args, rank, world):
     peak = peaks["hbm_gbs"] if peaks else 6800.0
     peak_src = "measured" if peaks else "fallback"
     lay0 = fc.layers[0]
+    traffic_key = wl.name if args.v_codec == "int" else wl.name + "+pq"
     rl = {}
     attn_b = attention_bytes(cfg, lay0)
     if "attention" in per_call:
         t = float(np.mean(per_call["attention"])) / 1e3
         rl["attention"] = {"bound": "hbm", "achieved": attn_b / t / 1e9, "peak": peak,
                            "unit": "GB/s", "frac": attn_b / t / 1e9 / peak,
-                           "traffic": measured_traffic("attention", wl.name),
+                           "traffic": measured_traffic("attention", traffic_key),
                            "bytes_per_launch": attn_b, "ms_per_launch": t * 1e3,
                            "peak_source": peak_src,
                            "time_share": float(np.mean(per_call["attention"])) * L / step_ms_for_share}
@@ -442,7 +466,7 @@ def run_ours(args, rank, world):
         t = float(np.mean(per_call["evict"])) / 1e3
         hbm = {"bound": "hbm", "achieved": eb / t / 1e9, "peak": peak,
                "unit": "GB/s", "frac": eb / t / 1e9 / peak,
-               "traffic": measured_traffic("evict_rerope", wl.name),
+               "traffic": measured_traffic("evict_rerope", traffic_key),
                "bytes_per_launch": eb, "ms_per_launch": t * 1e3,
                "peak_source": peak_src,
                "time_share": float(np.mean(per_call["evict"])) * L / step_ms_for_share}
@@ -502,8 +526,12 @@ def run_ours(args, rank, world):
                    "num_kv_heads": Hkv, "head_dim": d, "context": maxP, "n_sink": wl.n_sink,
                    "recent_window": wl.recent_window, "int4_budget": wl.int4_budget,
                    "policy": wl.policy, "k_bits": wl.middle_k_bits, "v_bits": wl.middle_v_bits,
-                   "shared_rows": bool(args.shared_rows),
-                   "storage": "fp16 sinks/recent, packed INT4 K / INT2 V middle",
+                   "shared_rows": bool(args.shared_rows), "v_codec": args.v_codec,
+                   "storage": ("fp16 sinks/recent, packed INT4 K / INT2 V middle"
+                               if args.v_codec == "int" else
+                               f"fp16 sinks/recent, packed INT{wl.middle_k_bits} K / PQ V middle "
+                               f"(256 centroids per 4-channel sub-space, codebook trained on "
+                               f"{PQ_CALIB_ROWS} synthetic rows, {PQ_ITERS} rounds)"),
                    "l2": "no flush: the compressed cache read per step is far larger than L2",
                    "parallelism": f"replicas x{world} (rows independent, no collective)",
                    "launch": ("cuda graph per step" if graph is not None else "eager launches") +

@@ -113,8 +113,17 @@ typedef struct {
                              prefill mass for H2O) and applied to every row; every row must hold
                              equal tier counts (equal prompt lengths at prefill), otherwise
                              FADE_ERR_INVALID_ARGUMENT. Each row keeps its own scores. */
+  int32_t v_codec;        /* fade_v_codec_t: how the middle tier stores V. FADE_V_PQ needs
+                             middle_v_bits = 2 (a PQ row has the INT2 row's d/4 bytes) and
+                             fade_layer_t.pq_codebook */
   fade_rope_t rope;
 } fade_config_t;
+
+/* Middle-tier V codec. FADE_V_PQ (FADE-zh §产品量化, the alternative to INT2 at about 2 bits
+ * per element): each 4-channel sub-vector of V is stored as the uint8 index of its nearest
+ * centroid in a per-layer codebook (see fade_pq_encode); the V scale slots are then written
+ * as zeros and carry nothing. */
+typedef enum { FADE_V_INT = 0, FADE_V_PQ = 1 } fade_v_codec_t;
 
 #define FADE_MAX_BATCH 256
 #define FADE_STATUS_WORDS 4
@@ -162,6 +171,8 @@ typedef struct {
   int32_t* h_n_sink;         /* HOST i32 [B]: mirror of N_SINK (same for every head) */
   int32_t* h_n_mid;          /* HOST i32 [B]: mirror of N_MID */
   int32_t* h_n_recent;       /* HOST i32 [B]: mirror of N_RECENT */
+  const uint16_t* pq_codebook; /* FADE_V_PQ only: fp16 [d/4][256][4], this layer's codebook
+                                  (shared by every row and KV head); NULL otherwise */
 } fade_layer_t;
 
 /* Byte sizes of every buffer of a layer and of the per-call workspaces. */
@@ -217,6 +228,41 @@ fade_status_t fade_quantize_pack(const uint16_t* x, int64_t n_vec, int32_t dim, 
 /* Inverse codec: out[n][c] = q * s as f32 (exact). Same layouts as fade_quantize_pack. */
 fade_status_t fade_dequantize(const uint8_t* codes, const uint16_t* scales, int64_t n_vec,
                               int32_t dim, int32_t bits, float* out, void* stream);
+
+/* Product quantisation of V (FADE-zh §产品量化: a codebook trained from calibration vectors
+ * with 256 centroids; vectors encoded to uint8 codes and decoded back). A vector of `dim`
+ * channels (a multiple of 4, at most 1024) is cut into dim/4 sub-vectors of 4 consecutive
+ * channels; sub-space s has its own 256 centroids. codebook: fp16 [dim/4][256][4].
+ *
+ * fade_pq_encode: codes[n][s] = the centroid c of sub-space s with the smallest squared
+ * distance to x[n][4s..4s+3], the distance taken in fp32 as ((e0^2 + e1^2) + e2^2) + e3^2
+ * with e_j = x_j - c_j and every difference, square and sum rounded on its own (no fused
+ * operations); the lowest index wins a tie. x: fp16 [n_vec][dim], finite; codes: u8
+ * [n_vec][dim/4]. */
+fade_status_t fade_pq_encode(const uint16_t* codebook, const uint16_t* x, int64_t n_vec,
+                             int32_t dim, uint8_t* codes, void* stream);
+
+/* out[n][4s + j] = codebook[s][codes[n][s]][j]: fp16 [n_vec][dim], exact. */
+fade_status_t fade_pq_decode(const uint16_t* codebook, const uint8_t* codes, int64_t n_vec,
+                             int32_t dim, uint16_t* out, void* stream);
+
+#define FADE_PQ_SUB 4
+#define FADE_PQ_CENTROIDS 256
+#define FADE_PQ_MAX_CALIB 8192
+/* Workspace of fade_pq_train: i64 member sums, i32 member counts and the copied indices. */
+#define FADE_PQ_TRAIN_WS_BYTES(dim) ((size_t)(dim) * 2304u + 1024u)
+
+/* Train a codebook by Lloyd's k-means in every sub-space. Centroid c starts at the
+ * sub-vectors of calibration row h_init_idx[c] (HOST i32 [256], each in [0, n_vec): the
+ * caller's random draw); each of `iters` rounds assigns every calibration sub-vector by the
+ * fade_pq_encode rule and sets each centroid to the mean of its members: the member sum is
+ * exact (taken in integers of 2^-24), divided once in fp64 and rounded to fp16 (nearest
+ * even); a centroid without members keeps its value. calib: fp16 [n_vec][dim], finite,
+ * 1 <= n_vec <= FADE_PQ_MAX_CALIB. codebook (out): fp16 [dim/4][256][4]. ws: device,
+ * FADE_PQ_TRAIN_WS_BYTES(dim) bytes, 16-byte aligned. */
+fade_status_t fade_pq_train(const uint16_t* calib, int64_t n_vec, int32_t dim,
+                            const int32_t* h_init_idx, int32_t iters, uint16_t* codebook,
+                            void* ws, size_t ws_bytes, void* stream);
 
 /* Empty the cache: zero the device metadata and the host mirror. */
 fade_status_t fade_cache_reset(const fade_config_t* cfg, fade_layer_t* layer, void* stream);

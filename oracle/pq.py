@@ -29,8 +29,8 @@ Readings (the pages give the API and the rate only):
   * decoded value = the centroid's fp16 channels, exactly.
 Pinned by: brute-force nearest search against fp64 distances on separated centroids, tie
 order, decode(encode(centroid)) identity, Lloyd rounds on hand-built clusters with known
-means, the empty-cluster rule, the rate, and attention over PQ values equal to attention
-over the decoded values.
+means, the empty-cluster rule, the rate, and the unit cache's middle values after demotion
+equal to decode(encode(v)) of the demoted tokens.
 """
 
 from __future__ import annotations
@@ -67,9 +67,11 @@ def distances(x16: np.ndarray, codebook: np.ndarray) -> np.ndarray:
 
 def encode(x16: np.ndarray, codebook: np.ndarray) -> np.ndarray:
     """fp16 [n, d] -> uint8 codes [n, d/4] (nearest centroid, lowest index on ties)."""
-    if np.asarray(x16).shape[0] == 0:
-        return np.zeros((0, np.asarray(x16).shape[1] // SUB), np.uint8)
-    return np.argmin(distances(x16, codebook), axis=-1).astype(np.uint8)  # first minimum
+    x16 = np.asarray(x16, np.float16)
+    out = np.zeros((x16.shape[0], x16.shape[1] // SUB), np.uint8)
+    for r in range(0, x16.shape[0], 128):       # rows in blocks, to bound the memory
+        out[r:r + 128] = np.argmin(distances(x16[r:r + 128], codebook), axis=-1)  # first min
+    return out
 
 
 def decode(codes: np.ndarray, codebook: np.ndarray) -> np.ndarray:

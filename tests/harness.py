@@ -15,6 +15,7 @@ from oracle import attention, quant
 from oracle.cache import Params, UnitCache
 from oracle.rope import RopeTable
 from synth import draw_decode_tokens, draw_prompt, ragged_context_lengths
+from synth.draws import pq_calibration
 
 ATOL, RTOL = 2e-3, 1e-2          # the spec's attention / score tolerance (allclose form)
 TIE_RTOL = 1e-5                  # fp32-vs-fp64 score noise that may flip a near-tie
@@ -32,7 +33,7 @@ class Lockstep:
     """Drives ``FadeCache`` and per-unit oracle caches over a workload."""
 
     def __init__(self, wl, layers=None, steps=None, device="cuda", mid_capacity=None,
-                 shared_rows=False):
+                 shared_rows=False, v_codec="int"):
         import dataclasses
 
         import torch
@@ -49,13 +50,21 @@ class Lockstep:
         self.max_pos = self.maxP + self.steps + 8
         self.shared = shared_rows   # the rows share their tier decisions (row-summed scores)
         self.cfg = dataclasses.replace(Config.from_workload(wl, mid_capacity=mid_capacity),
-                                       shared_rows=shared_rows)
+                                       shared_rows=shared_rows, v_codec=v_codec)
         self.fc = FadeCache(self.cfg, self.L, self.maxP, self.max_pos, device)
-        self.params = Params.from_workload(wl)
+        self.params = dataclasses.replace(Params.from_workload(wl), v_codec=v_codec)
+        self.codebook = None
+        if v_codec == "pq":
+            # a codebook made of 256 V-like draws (centroid c of sub-space s = channels
+            # 4s..4s+3 of draw c), the same array on both sides
+            d = wl.head_dim
+            rows = pq_calibration(wl, 256)
+            self.codebook = np.ascontiguousarray(rows.reshape(256, d // 4, 4).transpose(1, 0, 2))
+            self.fc.set_pq_codebook(torch.from_numpy(self.codebook).to(self.fc.device))
         self.rope = RopeTable.from_workload(wl, self.max_pos)
         B, H = wl.batch, wl.num_kv_heads
-        self.units = [[[UnitCache(self.params, self.rope) for _ in range(H)] for _ in range(B)]
-                      for _ in range(self.L)]
+        self.units = [[[UnitCache(self.params, self.rope, codebook=self.codebook)
+                        for _ in range(H)] for _ in range(B)] for _ in range(self.L)]
         self.diverged = set()            # (layer, row, head) after a near-tie selection flip
         self.near_ties = 0
         self.step_index = 0
@@ -242,7 +251,7 @@ class Lockstep:
             d = np.nonzero(g["recent_k"].view(np.uint16) != u.rec_k.view(np.uint16))
             raise AssertionError(f"recent K differs at {where}: {len(d[0])} entries, first {d[0][:5]}")
         kc = quant.pack(u.mid_kq, u.p.k_bits)
-        vc = quant.pack(u.mid_vq, u.p.v_bits)
+        vc = u.mid_vq if u.p.v_codec == "pq" else quant.pack(u.mid_vq, u.p.v_bits)
         for name, got, ref in (("mid K codes", g["mid_k_codes"], kc),
                                ("mid V codes", g["mid_v_codes"], vc)):
             if not np.array_equal(got, ref):

@@ -59,6 +59,7 @@ def _cfg(T, **kw):
     (dict(batch=257), 1),
     (dict(rope_base=1.0), 1),
     (dict(rope_kind="llama3", rope_low_freq_factor=4.0, rope_high_freq_factor=1.0), 1),
+    (dict(v_codec="pq", middle_v_bits=4), 1),
 ])
 def test_invalid_configs_are_rejected_on_the_host(T, kw, status):
     with pytest.raises(T.FadeError) as e:
@@ -115,6 +116,20 @@ def test_next_position_and_compressed_bytes_follow_the_oracle(T):
         u.step(t["q"][0], t["k"][0, 0], t["v"][0, 0])
     with pytest.raises(T.FadeError):
         T.fade_next_position(layer, 5)
+
+
+def test_pq_compressed_bytes_follow_the_oracle(T):
+    """A PQ middle token stores K codes and scales plus d/4 code bytes, no V scale."""
+    from oracle import accounting
+
+    for d in (64, 128):
+        cfg = _cfg(T, head_dim=d, v_codec="pq", batch=1, num_q_heads=4, num_kv_heads=1)
+        layer = T.TieredLayer(cfg, 16, device="cpu")
+        layer.h_n_sink[0], layer.h_n_mid[0], layer.h_n_recent[0] = 4, 300, 64
+        want = accounting.unit_bytes(d, 68, 0, 4, 2) + 300 * accounting.middle_token_bytes(
+            d, 4, 2, v_codec="pq")
+        assert T.fade_compressed_bytes(layer) == want
+        assert layer.pq_codebook.shape == (d // 4, 256, 4)
 
 
 def test_missing_library_fails_loudly(monkeypatch):

@@ -107,3 +107,28 @@ def test_layer_with_missing_buffers_is_rejected(T):
     L = _layer(T)
     L.c.status = None
     _expect(T, 1, T.fade_cache_demote, L)
+
+
+def test_pq_argument_errors(T):
+    import torch
+
+    cb = torch.zeros((32, 256, 4), dtype=torch.float16)
+    x = torch.zeros((8, 128), dtype=torch.float16)
+    codes = torch.zeros((8, 32), dtype=torch.uint8)
+    ws = torch.zeros(T.fade.pq_train_ws_bytes(128), dtype=torch.uint8)
+    _expect(T, 1, T.fade_pq_encode, cb, x, 8, 126, codes)          # dim not a multiple of 4
+    _expect(T, 1, T.fade_pq_encode, None, x, 8, 128, codes)
+    _expect(T, 1, T.fade_pq_decode, cb, None, 8, 128, x)
+    idx = np.arange(256)
+    _expect(T, 1, T.fade_pq_train, x, 8, 128, idx, 3, cb, ws)       # indices beyond 8 rows
+    _expect(T, 1, T.fade_pq_train, x, 0, 128, np.zeros(256), 3, cb, ws)
+    _expect(T, 1, T.fade_pq_train, x, 9000, 128, np.zeros(256), 3, cb, ws)
+    _expect(T, 3, T.fade_pq_train, x, 8, 128, np.zeros(256), 3, cb, ws[:100])
+    with pytest.raises(ValueError):
+        T.fade_pq_train(x, 8, 128, np.zeros(255), 3, cb, ws, stream=_S())
+
+
+def test_pq_layer_without_codebook_is_rejected(T):
+    L = _layer(T, v_codec="pq")
+    L.c.pq_codebook = None
+    _expect(T, 1, T.fade_cache_demote, L)

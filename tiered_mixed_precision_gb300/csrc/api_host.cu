@@ -50,6 +50,11 @@ fade_status_t validate_config(const fade_config_t* c) {
                      c->middle_k_bits, c->middle_v_bits);
   if (c->policy < FADE_EVICT_NONE || c->policy > FADE_EVICT_POSITION)
     return set_error(FADE_ERR_INVALID_ARGUMENT, "unknown eviction policy %d", c->policy);
+  if (c->v_codec != FADE_V_INT && c->v_codec != FADE_V_PQ)
+    return set_error(FADE_ERR_INVALID_ARGUMENT, "unknown v_codec %d", c->v_codec);
+  if (c->v_codec == FADE_V_PQ && c->middle_v_bits != 2)
+    return set_error(FADE_ERR_INVALID_ARGUMENT,
+                     "PQ-coded V uses the INT2 row layout: middle_v_bits must be 2");
   if (c->shared_rows != 0 && c->shared_rows != 1)
     return set_error(FADE_ERR_INVALID_ARGUMENT, "shared_rows must be 0 or 1");
   if (!(c->ema_decay >= 0.f && c->ema_decay < 1.f))
@@ -94,6 +99,9 @@ fade_status_t validate_layer(const fade_config_t* c, const fade_layer_t* L) {
     return set_error(FADE_ERR_INVALID_ARGUMENT, "meta, status or scratch buffers are NULL");
   if (!L->h_n_sink || !L->h_n_mid || !L->h_n_recent)
     return set_error(FADE_ERR_INVALID_ARGUMENT, "host mirror arrays are NULL");
+  if (c->v_codec == FADE_V_PQ &&
+      (!L->pq_codebook || (reinterpret_cast<uintptr_t>(L->pq_codebook) & 15)))
+    return set_error(FADE_ERR_INVALID_ARGUMENT, "PQ-coded V needs a 16-byte aligned codebook");
   return FADE_OK;
 }
 
@@ -161,8 +169,11 @@ extern "C" uint64_t fade_compressed_bytes(const fade_config_t* c, const fade_lay
   }
   const uint64_t d = c->head_dim;
   const uint64_t fp16_tok = 4 * d;
-  const uint64_t mid_tok =
-      d * (c->middle_k_bits + c->middle_v_bits) / 8 + 2 * 2 * (d / kGroup);
+  // a PQ middle token's V is d/4 code bytes without scales (the codebook is counted apart)
+  const uint64_t mid_tok = c->v_codec == FADE_V_PQ
+                               ? d * c->middle_k_bits / 8 + 2 * (d / kGroup) + d / 4
+                               : d * (c->middle_k_bits + c->middle_v_bits) / 8 +
+                                     2 * 2 * (d / kGroup);
   uint64_t total = 0;
   for (int b = 0; b < c->batch; ++b)
     total += (uint64_t)c->num_kv_heads *

@@ -28,21 +28,25 @@ struct AttnArgs {
   float* part_acc;                      // [B][Hq][nsplit][D]
   int Hq, H, S, W, C, NS, chunk, nsplit;
   float scale;                          // 1/sqrt(D)
+  const uint16_t* pq_cb;                // PQ-coded V: the layer's codebook [D/4][256][4]
 };
 
-template <int D, int KB, int VB, int G>
+template <int D, int KB, int VB, int G, bool PQ>
 struct Smem {
   static constexpr int KROW = D * KB / 8, VROW = D * VB / 8, SROW = D / kGroup;
   static constexpr int KROWP = KROW + kPad, VROWP = VROW + kPad;
   static constexpr int FROWP = D * 2 + kPad;  // fp16 row, padded
   static constexpr int MID_BYTES = kTile * (KROWP + VROWP + 2 * SROW * 2);
+  static constexpr int CB_BYTES = PQ ? kPqCentroids * D * 2 : 0;  // PQ codebook (middle splits)
   static constexpr int F16_BYTES = kTile * 2 * FROWP;
-  static constexpr int TILE_BYTES = MID_BYTES > F16_BYTES ? MID_BYTES : F16_BYTES;
+  static constexpr int MIDCB_BYTES = MID_BYTES + CB_BYTES;
+  static constexpr int TILE_BYTES = MIDCB_BYTES > F16_BYTES ? MIDCB_BYTES : F16_BYTES;
   static constexpr int NSUB = kThreads / (D / 4);  // token subsets in the value phase
   static constexpr int Q_OFF = 0;                              // float [D][G]
   static constexpr int P_OFF = Q_OFF + D * G * 4;               // float [G][kTile]
   static constexpr int R_OFF = P_OFF + G * kTile * 4;           // float [4][G] + [G]*3
   static constexpr int T_OFF = R_OFF + (4 * G + 4 * G) * 4;     // tile buffers
+  static constexpr int CB_OFF = T_OFF + MID_BYTES;              // codebook after the mid tile
   static constexpr int A_OFF = T_OFF;                           // acc reduction (reuses tile)
   static constexpr int TOTAL = T_OFF + (TILE_BYTES > NSUB * G * D * 4 ? TILE_BYTES : NSUB * G * D * 4);
 };
@@ -60,9 +64,9 @@ __device__ __forceinline__ void stage_rows(uint8_t* dst, int dst_stride, int byt
   }
 }
 
-template <int D, int KB, int VB, int G>
+template <int D, int KB, int VB, int G, bool PQ>
 __global__ void __launch_bounds__(kThreads) attn_split_kernel(AttnArgs a) {
-  using L = Smem<D, KB, VB, G>;
+  using L = Smem<D, KB, VB, G, PQ>;
   extern __shared__ __align__(16) uint8_t smem[];
   float* qs = reinterpret_cast<float*>(smem + L::Q_OFF);    // [D][G]
   float* ps = reinterpret_cast<float*>(smem + L::P_OFF);    // [G][kTile]
@@ -102,6 +106,14 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(AttnArgs a) {
   for (int i = tid; i < G * D; i += kThreads) {
     const int h = i / D, c = i % D;
     qs[c * G + h] = h2f(a.q[((size_t)(b * a.Hq + hq0 + h)) * D + c]);
+  }
+  // PQ-coded V: the codebook sits in shared memory for the whole middle split (it stays
+  // clear of the tile, which the loop below refills)
+  const uint2* cbs = reinterpret_cast<const uint2*>(smem + L::CB_OFF);
+  if constexpr (PQ) {
+    if (split != 0)
+      for (int i = tid; i < L::CB_BYTES / 16; i += kThreads)
+        reinterpret_cast<uint4*>(smem + L::CB_OFF)[i] = reinterpret_cast<const uint4*>(a.pq_cb)[i];
   }
 
   constexpr int QUADS = D / 4, NSUB = L::NSUB;
@@ -158,7 +170,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(AttnArgs a) {
       const int words = nt * L::SROW / 2;
       for (int i = tid; i < words; i += kThreads) {
         reinterpret_cast<uint32_t*>(kst)[i] = ksg[i];
-        reinterpret_cast<uint32_t*>(vst)[i] = vsg[i];
+        if constexpr (!PQ) reinterpret_cast<uint32_t*>(vst)[i] = vsg[i];
       }
     }
     __syncthreads();
@@ -259,6 +271,16 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(AttnArgs a) {
         const __half2 h01 = *reinterpret_cast<const __half2*>(&raw.x);
         const __half2 h23 = *reinterpret_cast<const __half2*>(&raw.y);
         const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+        v4[0] = f01.x;
+        v4[1] = f01.y;
+        v4[2] = f23.x;
+        v4[3] = f23.y;
+      } else if constexpr (PQ) {
+        // channels 4cq..4cq+3 are sub-space cq: one code byte, one 8-byte centroid
+        const uint32_t code = vt[t * L::VROWP + cq];
+        const uint2 raw = cbs[cq * kPqCentroids + code];
+        const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+        const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
         v4[0] = f01.x;
         v4[1] = f01.y;
         v4[2] = f23.x;
@@ -450,25 +472,25 @@ __global__ void __launch_bounds__(256) h2o_accumulate_kernel(AccArgs a) {
     *sc = a.decay * *sc + (1.f - a.decay) * psum;
 }
 
-template <int D, int KB, int VB, int G>
+template <int D, int KB, int VB, int G, bool PQ>
 fade_status_t launch_split(const AttnArgs& a, int B, cudaStream_t st, int nx) {
-  using L = Smem<D, KB, VB, G>;
+  using L = Smem<D, KB, VB, G, PQ>;
   // opt in to more than 48 KB of dynamic shared memory (cheap; done on every launch so it
   // holds for whichever device is current)
-  if (cudaFuncSetAttribute(attn_split_kernel<D, KB, VB, G>,
+  if (cudaFuncSetAttribute(attn_split_kernel<D, KB, VB, G, PQ>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL) != cudaSuccess)
     return launch_status("fade_decode_attention shared-memory opt-in");
-  attn_split_kernel<D, KB, VB, G><<<dim3(nx, a.H, B), kThreads, L::TOTAL, st>>>(a);
+  attn_split_kernel<D, KB, VB, G, PQ><<<dim3(nx, a.H, B), kThreads, L::TOTAL, st>>>(a);
   return launch_status("fade_decode_attention split");
 }
 
-template <int D, int KB, int VB>
+template <int D, int KB, int VB, bool PQ = false>
 fade_status_t launch_split_g(const AttnArgs& a, int G, int B, cudaStream_t st, int nx) {
   switch (G) {
-    case 1: return launch_split<D, KB, VB, 1>(a, B, st, nx);
-    case 2: return launch_split<D, KB, VB, 2>(a, B, st, nx);
-    case 4: return launch_split<D, KB, VB, 4>(a, B, st, nx);
-    case 8: return launch_split<D, KB, VB, 8>(a, B, st, nx);
+    case 1: return launch_split<D, KB, VB, 1, PQ>(a, B, st, nx);
+    case 2: return launch_split<D, KB, VB, 2, PQ>(a, B, st, nx);
+    case 4: return launch_split<D, KB, VB, 4, PQ>(a, B, st, nx);
+    case 8: return launch_split<D, KB, VB, 8, PQ>(a, B, st, nx);
   }
   return set_error(FADE_ERR_UNSUPPORTED, "query heads per KV head %d", G);
 }
@@ -477,6 +499,12 @@ fade_status_t launch_split_g(const AttnArgs& a, int G, int B, cudaStream_t st, i
 fade_status_t launch_split_any(const fade_config_t* c, const AttnArgs& a, cudaStream_t st, int nx) {
   const int G = c->num_q_heads / c->num_kv_heads, B = c->batch;
   const int d = c->head_dim, kb = c->middle_k_bits, vb = c->middle_v_bits;
+  if (c->v_codec == FADE_V_PQ) {  // PQ codes occupy the INT2 rows (validated)
+    if (d == 64) return kb == 4 ? launch_split_g<64, 4, 2, true>(a, G, B, st, nx)
+                                : launch_split_g<64, 2, 2, true>(a, G, B, st, nx);
+    return kb == 4 ? launch_split_g<128, 4, 2, true>(a, G, B, st, nx)
+                   : launch_split_g<128, 2, 2, true>(a, G, B, st, nx);
+  }
 #define FADE_CASE(D_, KB_, VB_) \
   if (d == D_ && kb == KB_ && vb == VB_) return launch_split_g<D_, KB_, VB_>(a, G, B, st, nx);
   FADE_CASE(64, 4, 2) FADE_CASE(64, 4, 4) FADE_CASE(64, 2, 2) FADE_CASE(64, 2, 4)
@@ -549,10 +577,14 @@ extern "C" fade_status_t fade_decode_attention(const fade_config_t* c, const fad
     a.nsplit = 1 + sk.smax;
   } else {
     sk.P = 0;
-    a.chunk = choose_chunk(max_mid, units, kTile, 8LL * 152);
+    // PQ: fewer, longer middle splits, so that staging the codebook (256 x d fp16 from L2)
+    // stays small beside the split's own bytes
+    a.chunk = choose_chunk(max_mid, units, c->v_codec == FADE_V_PQ ? 16 * kTile : kTile,
+                           (c->v_codec == FADE_V_PQ ? 4LL : 8LL) * 152);
     a.nsplit = 1 + (max_mid + a.chunk - 1) / a.chunk;
   }
   a.scale = 1.0f / sqrtf((float)c->head_dim);
+  a.pq_cb = L->pq_codebook;
   const size_t need = (size_t)c->batch * c->num_q_heads * a.nsplit * (c->head_dim + 2) * 4;
   if (ws_bytes < need)
     return set_error(FADE_ERR_CAPACITY, "attention workspace %zu bytes, %zu needed", ws_bytes,

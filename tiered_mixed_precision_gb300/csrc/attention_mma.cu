@@ -1025,7 +1025,7 @@ fade_status_t launch_mma(const fade_config_t* c, const fade_layer_t* L, const Mm
 }  // namespace
 
 bool mid_mma_supported(const fade_config_t* c) {
-  return c->middle_k_bits == 4 && c->middle_v_bits == 2;
+  return c->middle_k_bits == 4 && c->middle_v_bits == 2 && c->v_codec == FADE_V_INT;
 }
 
 int mid_mma_ctas(const fade_config_t* c) {

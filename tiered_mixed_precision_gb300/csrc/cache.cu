@@ -203,6 +203,8 @@ struct LayerArgs {
   int B;            // batch rows
   const float* table;   // nullptr: RoPE kind NONE (re-positioning is the identity)
   int half;
+  bool pq;                    // middle-tier V is product-quantised (codes in the INT2 rows)
+  const uint16_t* pq_cb;      // the layer's PQ codebook, fp16 [d/4][256][4]
 };
 
 LayerArgs make_args(const fade_config_t* c, const fade_layer_t* L, const float* table) {
@@ -237,6 +239,8 @@ LayerArgs make_args(const fade_config_t* c, const fade_layer_t* L, const float* 
   a.B = c->batch;
   a.table = (c->rope.kind == FADE_ROPE_NONE) ? nullptr : table;
   a.half = c->head_dim / 2;
+  a.pq = c->v_codec == FADE_V_PQ;
+  a.pq_cb = L->pq_codebook;
   return a;
 }
 
@@ -345,8 +349,12 @@ __global__ void __launch_bounds__(32) demote_kernel(LayerArgs a) {
   const size_t mrow = (size_t)unit * a.C + n_mid;
   warp_quantize_row<D, KB>(a.rec_k + rrow, (cur ? a.mk[1] : a.mk[0]) + mrow * (D * KB / 8),
                            (cur ? a.mks[1] : a.mks[0]) + mrow * (D / kGroup));
-  warp_quantize_row<D, VB>(a.rec_v + rrow, (cur ? a.mv[1] : a.mv[0]) + mrow * (D * VB / 8),
-                           (cur ? a.mvs[1] : a.mvs[0]) + mrow * (D / kGroup));
+  if (a.pq)
+    warp_pq_encode_row<D>(a.rec_v + rrow, a.pq_cb, (cur ? a.mv[1] : a.mv[0]) + mrow * (D / 4),
+                          (cur ? a.mvs[1] : a.mvs[0]) + mrow * (D / kGroup));
+  else
+    warp_quantize_row<D, VB>(a.rec_v + rrow, (cur ? a.mv[1] : a.mv[0]) + mrow * (D * VB / 8),
+                             (cur ? a.mvs[1] : a.mvs[0]) + mrow * (D / kGroup));
   __syncwarp();
   if (threadIdx.x == 0) {
     (cur ? a.mid_sc[1] : a.mid_sc[0])[mrow] = a.rec_sc[(size_t)unit * a.W + head];
@@ -1058,7 +1066,10 @@ __global__ void __launch_bounds__(256) prefill_place_kernel(LayerArgs a, Prefill
     if (tier == 1) {
       const size_t row = (size_t)unit * a.C + (nv - s.n_s);
       warp_store_quantized<D, KB>(key, a.mk[0] + row * KROW, a.mks[0] + row * SROW);
-      warp_quantize_row<D, VB>(p.v + src, a.mv[0] + row * VROW, a.mvs[0] + row * SROW);
+      if (a.pq)
+        warp_pq_encode_row<D>(p.v + src, a.pq_cb, a.mv[0] + row * VROW, a.mvs[0] + row * SROW);
+      else
+        warp_quantize_row<D, VB>(p.v + src, a.mv[0] + row * VROW, a.mvs[0] + row * SROW);
       if (lane == 0) a.mid_sc[0][row] = score;
     } else {
       size_t row;

@@ -144,6 +144,56 @@ __device__ __forceinline__ int unpack_code(const uint8_t* row, int c) {
   return int(u) - (int(u >> (BITS - 1)) << BITS);
 }
 
+// ---- product quantisation of V (FADE-zh §产品量化): 256 centroids per 4-channel sub-space.
+constexpr int kPqSub = 4, kPqCentroids = 256;
+
+// Squared distance between a sub-vector x (fp16 values held as fp32) and the centroid whose
+// four fp16 channels are packed in `c`, in one fixed order: ((e0^2 + e1^2) + e2^2) + e3^2,
+// e_j = x_j - c_j, every operation rounded on its own (the intrinsics keep the compiler
+// from fusing them), so that every caller takes the same integer decision.
+__device__ __forceinline__ float pq_dist(const float x[4], uint2 c) {
+  const float2 c01 = __half22float2(*reinterpret_cast<const __half2*>(&c.x));
+  const float2 c23 = __half22float2(*reinterpret_cast<const __half2*>(&c.y));
+  const float e0 = __fsub_rn(x[0], c01.x), e1 = __fsub_rn(x[1], c01.y);
+  const float e2 = __fsub_rn(x[2], c23.x), e3 = __fsub_rn(x[3], c23.y);
+  float acc = __fadd_rn(__fmul_rn(e0, e0), __fmul_rn(e1, e1));
+  acc = __fadd_rn(acc, __fmul_rn(e2, e2));
+  return __fadd_rn(acc, __fmul_rn(e3, e3));
+}
+
+// Index of the nearest of the 256 centroids `cb` of one sub-space; a strict comparison in
+// increasing index order gives the lowest index on ties.
+__device__ __forceinline__ int pq_nearest(const float x[4], const uint2* cb) {
+  float best = __int_as_float(0x7f800000);  // +inf
+  int bi = 0;
+#pragma unroll 8
+  for (int c = 0; c < kPqCentroids; ++c) {
+    const float d = pq_dist(x, cb[c]);
+    if (d < best) {
+      best = d;
+      bi = c;
+    }
+  }
+  return bi;
+}
+
+// Encode one fp16 row of D channels with one warp: lane s < D/4 codes sub-space s. The V
+// scale slots of a PQ row are written as zeros.
+template <int D>
+__device__ __forceinline__ void warp_pq_encode_row(const uint16_t* x, const uint16_t* codebook,
+                                                   uint8_t* codes, uint16_t* scales) {
+  const int lane = threadIdx.x & 31;
+  if (lane < D / kPqSub) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(x + kPqSub * lane);
+    const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+    const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+    const float xv[4] = {x01.x, x01.y, x23.x, x23.y};
+    const uint2* cb = reinterpret_cast<const uint2*>(codebook) + (size_t)lane * kPqCentroids;
+    codes[lane] = (uint8_t)pq_nearest(xv, cb);
+  }
+  if (lane < D / kGroup) scales[lane] = 0;
+}
+
 // fp32 rotation of one pair with every product and sum rounded separately.
 __device__ __forceinline__ void rotate_pair(float x1, float x2, float c, float s, float& y1,
                                             float& y2) {

@@ -20,6 +20,13 @@ LIB_PATH = os.path.join(_PKG, "_build", "libfade.so")
 FADE_OK, FADE_ERR_INVALID_ARGUMENT, FADE_ERR_UNSUPPORTED, FADE_ERR_CAPACITY, FADE_ERR_CUDA = range(5)
 ROPE_KINDS = {"none": 0, "default": 1, "llama3": 2, "linear": 3, "ntk": 4, "yarn": 5}
 POLICIES = {"none": 0, "h2o": 1, "ema": 2, "position": 3}
+V_CODECS = {"int": 0, "pq": 1}
+PQ_SUB, PQ_CENTROIDS, PQ_MAX_CALIB = 4, 256, 8192
+
+
+def pq_train_ws_bytes(dim: int) -> int:
+    """FADE_PQ_TRAIN_WS_BYTES(dim)."""
+    return dim * 2304 + 1024
 META_FIELDS = 8
 META = {"n_sink": 0, "n_mid": 1, "n_recent": 2, "head": 3, "cur": 4, "n_ev": 5}
 MAX_BATCH = 256
@@ -46,7 +53,7 @@ class ConfigT(ctypes.Structure):
                 ("head_dim", c_i32), ("n_sink", c_i32), ("recent_window", c_i32),
                 ("int4_budget", c_i32), ("middle_k_bits", c_i32), ("middle_v_bits", c_i32),
                 ("mid_capacity", c_i32), ("policy", c_i32), ("ema_decay", c_f32),
-                ("shared_rows", c_i32), ("rope", RopeT)]
+                ("shared_rows", c_i32), ("v_codec", c_i32), ("rope", RopeT)]
 
 
 class LayerT(ctypes.Structure):
@@ -56,7 +63,8 @@ class LayerT(ctypes.Structure):
                 ("sink_scores", c_vp), ("mid_scores", c_vp * 2), ("recent_scores", c_vp),
                 ("meta", c_vp), ("victims", c_vp), ("chunk_base", c_vp),
                 ("victim_words", c_i32), ("chunk_slots", c_i32), ("status", c_vp),
-                ("h_n_sink", c_vp), ("h_n_mid", c_vp), ("h_n_recent", c_vp)]
+                ("h_n_sink", c_vp), ("h_n_mid", c_vp), ("h_n_recent", c_vp),
+                ("pq_codebook", c_vp)]
 
 
 class LayoutT(ctypes.Structure):
@@ -100,6 +108,9 @@ def lib():
             "fade_h2o_accumulate": (c_i32, [S(ConfigT), S(LayerT), c_vp, c_vp, c_vp]),
             "fade_next_position": (c_i32, [S(ConfigT), S(LayerT), c_i32]),
             "fade_compressed_bytes": (ctypes.c_uint64, [S(ConfigT), S(LayerT)]),
+            "fade_pq_encode": (c_i32, [c_vp, c_vp, c_i64, c_i32, c_vp, c_vp]),
+            "fade_pq_decode": (c_i32, [c_vp, c_vp, c_i64, c_i32, c_vp, c_vp]),
+            "fade_pq_train": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp]),
             "fade_last_error": (ctypes.c_char_p, []),
         }
         for name, (res, args) in sig.items():
@@ -153,6 +164,7 @@ class Config:
     rope_high_freq_factor: float = 4.0
     rope_original_max_position: int = 8192
     shared_rows: bool = False  # the rows share their tier decisions (row-summed scores)
+    v_codec: str = "int"       # "pq": product-quantised middle V (needs middle_v_bits = 2)
     _c: ConfigT = field(default=None, repr=False, compare=False)
 
     def c(self) -> ConfigT:
@@ -161,7 +173,8 @@ class Config:
         self._c = ConfigT(self.batch, self.num_q_heads, self.num_kv_heads, self.head_dim,
                           self.n_sink, self.recent_window, self.int4_budget,
                           self.middle_k_bits, self.middle_v_bits, self.mid_capacity,
-                          POLICIES[self.policy], self.ema_decay, int(self.shared_rows), r)
+                          POLICIES[self.policy], self.ema_decay, int(self.shared_rows),
+                          V_CODECS[self.v_codec], r)
         return self._c
 
     @property
@@ -247,6 +260,8 @@ class TieredLayer:
         self.h_n_sink = np.zeros(B, np.int32)
         self.h_n_mid = np.zeros(B, np.int32)
         self.h_n_recent = np.zeros(B, np.int32)
+        # the layer's PQ codebook (product-quantised V only): fp16 [d/4][256][4]
+        self.pq_codebook = z((d // PQ_SUB, PQ_CENTROIDS, PQ_SUB), f16) if cfg.v_codec == "pq" else None
         p = lambda t: t.data_ptr()
         self.c = LayerT(
             p(self.sink_k), p(self.sink_v), p(self.recent_k), p(self.recent_v),
@@ -255,7 +270,14 @@ class TieredLayer:
             p(self.sink_scores), (c_vp * 2)(*map(p, self.mid_scores)), p(self.recent_scores),
             p(self.meta), p(self.victims), p(self.chunk_base), lay.victim_words,
             lay.chunk_slots, p(self.status), self.h_n_sink.ctypes.data, self.h_n_mid.ctypes.data,
-            self.h_n_recent.ctypes.data)
+            self.h_n_recent.ctypes.data,
+            None if self.pq_codebook is None else p(self.pq_codebook))
+
+    def set_pq_codebook(self, codebook):
+        """Copy a codebook (fp16 [d/4][256][4], e.g. from fade_pq_train) into the layer."""
+        if self.pq_codebook is None:
+            raise ValueError("the layer does not use product-quantised V")
+        self.pq_codebook.copy_(codebook)
 
     def workspaces(self):
         """(logits_ws, ml_ws, attn_ws) tensors sized by the layout."""
@@ -353,3 +375,23 @@ def fade_decode_attention_noalloc(layer: TieredLayer, q_rot, out, logits_ws, ml_
     fn.argtypes = [ctypes.POINTER(ConfigT), ctypes.POINTER(LayerT), c_vp, c_vp, c_vp, c_vp, c_vp]
     _check(fn(ctypes.byref(layer.cfg.c()), ctypes.byref(layer.c), _ptr(q_rot), _ptr(out),
               _ptr(logits_ws), _ptr(ml_ws), _stream(stream)))
+
+
+def fade_pq_encode(codebook, x, n_vec, dim, codes, stream=None):
+    _check(lib().fade_pq_encode(_ptr(codebook), _ptr(x), n_vec, dim, _ptr(codes),
+                                _stream(stream)))
+
+
+def fade_pq_decode(codebook, codes, n_vec, dim, out, stream=None):
+    _check(lib().fade_pq_decode(_ptr(codebook), _ptr(codes), n_vec, dim, _ptr(out),
+                                _stream(stream)))
+
+
+def fade_pq_train(calib, n_vec, dim, init_idx, iters, codebook, ws, stream=None):
+    """``init_idx``: 256 host row indices (any int sequence); ``ws``: a device tensor of at
+    least pq_train_ws_bytes(dim) bytes."""
+    idx = np.ascontiguousarray(init_idx, np.int32)
+    if idx.shape != (PQ_CENTROIDS,):
+        raise ValueError("init_idx must hold 256 indices")
+    _check(lib().fade_pq_train(_ptr(calib), n_vec, dim, idx.ctypes.data, iters, _ptr(codebook),
+                               _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))

@@ -76,7 +76,7 @@ class FadeCache:
                       "recent_window", "int4_budget", "middle_k_bits", "middle_v_bits",
                       "mid_capacity", "policy", "ema_decay", "rope_kind", "rope_base",
                       "rope_factor", "rope_low_freq_factor", "rope_high_freq_factor",
-                      "rope_original_max_position", "shared_rows")
+                      "rope_original_max_position", "shared_rows", "v_codec")
 
     def cache_state_dict(self) -> dict:
         """Every layer's tier buffers (both middle buffers and the device metadata, which says
@@ -91,6 +91,8 @@ class FadeCache:
                 d[name] = [t.cpu() for t in v] if isinstance(v, list) else v.cpu()
             for name in ("h_n_sink", "h_n_mid", "h_n_recent"):
                 d[name] = torch.from_numpy(getattr(L, name).copy())
+            if L.pq_codebook is not None:
+                d["pq_codebook"] = L.pq_codebook.cpu()
             layers.append(d)
         return {"config": {f: getattr(self.cfg, f) for f in self._CONFIG_FIELDS},
                 "num_layers": len(self.layers), "max_prompt": self.max_prompt,
@@ -115,7 +117,29 @@ class FadeCache:
                     t.copy_(u)
             for name in ("h_n_sink", "h_n_mid", "h_n_recent"):
                 getattr(L, name)[:] = d[name].numpy()  # in place: the C struct points at them
+            if L.pq_codebook is not None:
+                L.set_pq_codebook(d["pq_codebook"])
         torch.cuda.synchronize(self.device)
+
+    # ------------------------------------------------------------------ PQ codebooks
+    # Page "FADE：面向LLM推理的注意力感知分层KV缓存压缩技术", §产品量化: V can be product-quantised
+    # with a codebook trained from calibration vectors (256 centroids, uint8 codes).
+    def set_pq_codebook(self, codebook: torch.Tensor, layer=None):
+        """Install a codebook (fp16 [d/4][256][4]) in one layer, or in every layer."""
+        for L in (self.layers if layer is None else [self.layers[layer]]):
+            L.set_pq_codebook(codebook)
+
+    def train_pq_codebook(self, calib: torch.Tensor, init_idx, iters: int, layer=None):
+        """Train a codebook on the GPU from calibration V rows (fp16 [n][d], n <= 8192; the
+        256 start rows ``init_idx`` are the caller's random draw) and install it in one layer
+        or every layer. Returns the codebook."""
+        d = self.cfg.head_dim
+        cb = torch.empty((d // F.PQ_SUB, F.PQ_CENTROIDS, F.PQ_SUB), dtype=torch.float16,
+                         device=self.device)
+        ws = torch.empty(F.pq_train_ws_bytes(d), dtype=torch.uint8, device=self.device)
+        F.fade_pq_train(calib, calib.shape[0], d, init_idx, iters, cb, ws)
+        self.set_pq_codebook(cb, layer)
+        return cb
 
     # ------------------------------------------------------------------ pieces
     def rope_(self, x: torch.Tensor, n_groups: int, group_len: int, pos_start=None, pos_step=1):
