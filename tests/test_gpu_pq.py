@@ -94,3 +94,18 @@ def test_pq_lockstep(T, key, policy, kbits):
     for _ in range(ls.steps):
         ls.step()
     assert ls.near_ties <= 1
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 8])
+def test_pq_lockstep_query_groups(T, d, G):
+    """PQ-coded V on the tensor-core kernel for every query-group size it is built for."""
+    wl = get_workload(4).scaled(layers=1, batch=2, num_q_heads=2 * G, num_kv_heads=2,
+                                head_dim=d, ragged=None, prompt_len=700, int4_budget=300,
+                                steps=4, policy="h2o" if G == 2 else "position")
+    ls = Lockstep(wl, v_codec="pq")
+    ls.prefill(0)
+    ls.check_layer_state(0)
+    for _ in range(ls.steps):
+        ls.step()
+    assert ls.near_ties <= 1

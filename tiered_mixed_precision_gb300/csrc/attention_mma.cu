@@ -50,13 +50,14 @@ constexpr int kTileTok = 256;            // tokens per TMA tile
 #ifndef FADE_MMA_CTAS_PER_SM
 #define FADE_MMA_CTAS_PER_SM 2
 #endif
-template <int D, int G>
+template <int D, int G, bool PQ = false>
 struct MmaShape {
   static constexpr int CONS = (FADE_MMA_WIDE && G <= 4) ? 8 : 4;
   static constexpr int THREADS = 32 * (CONS + 1);
   static constexpr int WARP_TOK = kTileTok / CONS;  // tokens per consumer warp per tile
   static constexpr int MT = WARP_TOK / 16;          // 16-token M-tiles per consumer warp
-  static constexpr int MINB = CONS == 8 ? FADE_MMA_CTAS_PER_SM : 1;
+  // PQ-coded V keeps the codebook and per-warp V tiles in shared memory: one CTA per SM
+  static constexpr int MINB = PQ ? 1 : (CONS == 8 ? FADE_MMA_CTAS_PER_SM : 1);
 };
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -74,6 +75,7 @@ struct MmaArgs {
   int32_t* status;
   int B, Hq, H, S, W, C, NS, chunk, nsplit;
   float inv_sqrt_d;
+  const uint16_t* pq_cb;             // PQ-coded V: the layer's codebook [D/4][256][4]
 };
 
 template <int D>
@@ -98,6 +100,24 @@ struct MmaCfg {
   static constexpr int BAR_OFF = INFO_OFF + NSTAGE * 8 * 4;
   static constexpr int SMEM = BAR_OFF + 2 * NSTAGE * 8 + 1024;  // + alignment slack
   static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned (TMA swizzle)");
+};
+
+// Shared memory added for PQ-coded V, after the layout above: the layer's codebook stored
+// centroid-major ([256][D/4] entries of 4 fp16 channels, so that the 32 lanes of a warp, one
+// per sub-space, gather 32 different entries in two wavefronts whatever the codes) and one
+// decoded 16-token V tile per consumer warp ([16][D] fp16, rows padded by 16 bytes so that the
+// transposing matrix loads touch 32 distinct banks).
+template <int D>
+struct PqCfg {
+  using C = MmaCfg<D>;
+  static constexpr int SUBS = D / kPqSub;
+  static constexpr int CB_OFF = (C::BAR_OFF + 2 * C::NSTAGE * 8 + 15) / 16 * 16;
+  static constexpr int CB_BYTES = kPqCentroids * D * 2;
+  static constexpr int VT_ROW = D * 2 + 16;
+  static constexpr int VT_OFF = CB_OFF + CB_BYTES;
+  static constexpr int VT_BYTES = 8 * 16 * VT_ROW;   // up to eight consumer warps
+  static constexpr int SMEM = VT_OFF + VT_BYTES + 1024;  // + alignment slack
+  static_assert(SMEM <= 227 * 1024, "PQ layout exceeds the shared memory of a CTA");
 };
 
 // Stage info written by the producer before it arms a stage: what the consumers find there.
@@ -271,6 +291,14 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts64(uint32_t addr, uint2 v) {
+  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
+}
 template <int CPL>
 __device__ __forceinline__ void lds_f16_lane(uint32_t addr, float (&f)[CPL]) {
   if constexpr (CPL == 4) {
@@ -363,12 +391,12 @@ __device__ __forceinline__ void scale_words(uint32_t addr, uint32_t (&w)[D / 64]
 // One consumer warp's share of one tile: QK^T on the tensor cores with the K scales applied per
 // group in fp32, the online-softmax update, and PV. FULL: every token of the warp's share is
 // valid (no masking). Invalid head columns (G < 4) carry logit 0 and are discarded later.
-template <int D, int G, bool FULL, bool LOGITS>
+template <int D, int G, bool FULL, bool LOGITS, bool PQ>
 __device__ __forceinline__ void consume_tile(
     const MmaArgs& a, uint32_t stage, const LaneOffsets<D>& lo_, int nt, int wr0, int lane,
     const uint32_t (&qb)[D / 64][4][(2 * G + 7) / 8][2], float (&m2)[(2 * G + 7) / 8],
     float (&lsum)[(2 * G + 7) / 8], float (&o)[D / 64][4][(2 * G + 7) / 8][4], float c2,
-    float* logit_row) {
+    float* logit_row, uint32_t vt, uint32_t cbs) {
   using Cfg = MmaCfg<D>;
   constexpr int NT = (2 * G + 7) / 8;
   constexpr int NHALF = D / 64;
@@ -464,6 +492,50 @@ __device__ __forceinline__ void consume_tile(
         for (int j = 0; j < NT; ++j)
 #pragma unroll
           for (int e = 0; e < 4; ++e) o[s][mm][j][e] *= alpha[j];
+  }
+  if constexpr (PQ) {
+    // PQ-coded V: per M-tile the warp decodes its 16 tokens into its fp16 tile (one code byte,
+    // one 8-byte centroid and one 8-byte store per (token, sub-space)), then reads the A
+    // operand transposed with ldmatrix: row g of block (s, mm) is channel 64s + 16mm + g, row
+    // g + 8 channel 64s + 16mm + g + 8. B operand: the probability, the same in both group
+    // parity columns (a PQ row has no scales). Codes past the tile's tokens index real
+    // centroids (finite) and meet probability 0.
+    using PC = PqCfg<D>;
+    constexpr int SUBS = PC::SUBS;
+    const uint32_t vt_ld = vt + ((lane & 7) + 8 * (lane >> 4)) * PC::VT_ROW + ((lane >> 3) & 1) * 16;
+#pragma unroll
+    for (int mt = 0; mt < MmaShape<D, G>::MT; ++mt) {
+      const int r0 = wr0 + mt * 16;
+#pragma unroll 4
+      for (int i = lane; i < 16 * SUBS; i += 32) {
+        const int tk = i / SUBS, sub = i % SUBS, r = r0 + tk;
+        uint32_t off;
+        if constexpr (D == 128)  // 32-byte rows under the 32-byte swizzle of the TMA copy
+          off = r * Cfg::VROW + ((((sub >> 4) ^ (r >> 2)) & 1) << 4) + (sub & 15);
+        else                     // 16-byte rows, no swizzle
+          off = r * Cfg::VROW + sub;
+        const uint32_t code = lds_u8(stage + Cfg::V_OFF + off);
+        sts64(vt + tk * PC::VT_ROW + sub * 8, lds64(cbs + (code * SUBS + sub) * 8));
+      }
+      __syncwarp();
+      uint32_t pb[NT][2];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        pb[j][0] = movm_t(h2_as_u32(__float2half2_rn(sc[mt][j][0])));
+        pb[j][1] = movm_t(h2_as_u32(__float2half2_rn(sc[mt][j][1])));
+      }
+#pragma unroll
+      for (int s = 0; s < NHALF; ++s)
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(vt_ld + (64 * s + 16 * mm) * 2, a0, a1, a2, a3);
+#pragma unroll
+          for (int j = 0; j < NT; ++j) mma16816(o[s][mm][j], a0, a1, a2, a3, pb[j][0], pb[j][1]);
+        }
+      __syncwarp();  // the tile is read before the next M-tile overwrites it
+    }
+    return;
   }
   // PV over the warp's M-tiles (16 tokens each = one MMA k-step). B operand: the probability
   // (fp16) times the V scale of the column's group (fp16 multiply), transposed into place.
@@ -579,8 +651,8 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity
 // arming it. The producer therefore runs ahead across item boundaries and the consumers never
 // wait on global memory for metadata or queries. Consumer warps merge their partials in shared
 // memory at the end of each item (named barrier 1, consumers only) and write its partial.
-template <int D, int G>
-__global__ void __launch_bounds__(MmaShape<D, G>::THREADS, MmaShape<D, G>::MINB)
+template <int D, int G, bool PQ>
+__global__ void __launch_bounds__(MmaShape<D, G, PQ>::THREADS, MmaShape<D, G, PQ>::MINB)
 attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_constant__ CUtensorMap tk1,
                     const __grid_constant__ CUtensorMap tv0, const __grid_constant__ CUtensorMap tv1,
                     MmaArgs a, const __grid_constant__ StreamK sk) {
@@ -623,6 +695,13 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if constexpr (PQ) {  // the layer's codebook, transposed to centroid-major, once per CTA
+    constexpr int SUBS = PqCfg<D>::SUBS;
+    const uint2* src = reinterpret_cast<const uint2*>(a.pq_cb);
+    uint2* dst = reinterpret_cast<uint2*>(smem + PqCfg<D>::CB_OFF);
+    for (int e = threadIdx.x; e < SUBS * kPqCentroids; e += blockDim.x)
+      dst[(e % kPqCentroids) * SUBS + e / kPqCentroids] = src[e];
+  }
   __syncthreads();
   volatile int* abort = &s_abort;
 
@@ -662,7 +741,8 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
           constexpr int kAlign = 16 / (Cfg::SROW * 2);
           const int ns = (max(nt, 0) + kAlign - 1) / kAlign * kAlign;
           uint32_t bytes = 0;
-          if (nt > 0) bytes += kTileTok * (Cfg::KROW + Cfg::VROW) + 2u * ns * Cfg::SROW * 2;
+          // (PQ-coded V has no scale rows: only the K scales are copied)
+          if (nt > 0) bytes += kTileTok * (Cfg::KROW + Cfg::VROW) + (PQ ? 1u : 2u) * ns * Cfg::SROW * 2;
           if (it == 0) bytes += G * D * 2;
           if (split == 0 && f16_staged) bytes += (a.S + a.W) * D * 2;
           mbar_expect_tx(bar_full + 8 * s, bytes);
@@ -680,8 +760,9 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
             tma_load_2d(stage + Cfg::V_OFF, mv, 0, (int)r, bar_full + 8 * s);
             bulk_load_1d(stage + Cfg::KS_OFF, ksg + r * Cfg::SROW, ns * Cfg::SROW * 2,
                          bar_full + 8 * s);
-            bulk_load_1d(stage + Cfg::VS_OFF, vsg + r * Cfg::SROW, ns * Cfg::SROW * 2,
-                         bar_full + 8 * s);
+            if (!PQ)
+              bulk_load_1d(stage + Cfg::VS_OFF, vsg + r * Cfg::SROW, ns * Cfg::SROW * 2,
+                           bar_full + 8 * s);
           }
           if (it == 0)
             bulk_load_1d(stage + Cfg::Q_OFF, a.q + (size_t)(b * a.Hq + hk * G) * D, G * D * 2,
@@ -715,6 +796,9 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
   const int wr0 = warp * MmaShape<D, G>::WARP_TOK;
   const LaneOffsets<D> lo_ = lane_offsets<D>(wr0, lane);
   const bool want_logits = a.logits != nullptr;
+  // PQ-coded V: this warp's decoded V tile and the codebook (unused otherwise)
+  const uint32_t vt = sbase + PqCfg<D>::VT_OFF + warp * 16 * PqCfg<D>::VT_ROW;
+  const uint32_t cbs = sbase + PqCfg<D>::CB_OFF;
   int used = 0;  // stages consumed so far (the producer's `issued` sequence)
   // the same number of items in every consumer warp (and so the same barriers), whatever waits
   // may fail: the count comes from the schedule, the rest from the stage info
@@ -876,18 +960,18 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
         if (ok) {
           if (want_logits) {
             if (nt == kTileTok)
-              consume_tile<D, G, true, true>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o, c2,
-                                             logit_row);
+              consume_tile<D, G, true, true, PQ>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o,
+                                             c2, logit_row, vt, cbs);
             else if (wr0 < nt)
-              consume_tile<D, G, false, true>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o, c2,
-                                              logit_row);
+              consume_tile<D, G, false, true, PQ>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o,
+                                              c2, logit_row, vt, cbs);
           } else {
             if (nt == kTileTok)
-              consume_tile<D, G, true, false>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o, c2,
-                                              logit_row);
+              consume_tile<D, G, true, false, PQ>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o,
+                                              c2, logit_row, vt, cbs);
             else if (wr0 < nt)
-              consume_tile<D, G, false, false>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o, c2,
-                                               logit_row);
+              consume_tile<D, G, false, false, PQ>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o,
+                                               c2, logit_row, vt, cbs);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_empty + 8 * s_);
@@ -919,9 +1003,16 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
           for (int s = 0; s < NHALF; ++s)
 #pragma unroll
             for (int mm = 0; mm < 4; ++mm) {
-              const int c = 64 * s + 8 * g + 2 * mm;
-              wo[(warp * G + h) * WR + c] = gsel ? o[s][mm][j][1] : o[s][mm][j][0];
-              wo[(warp * G + h) * WR + c + 1] = gsel ? o[s][mm][j][3] : o[s][mm][j][2];
+              if constexpr (PQ) {  // rows g, g + 8 = channels 64s + 16mm + g (+ 8); both
+                                   // parity columns carry the same probability
+                const int c = 64 * s + 16 * mm + g;
+                wo[(warp * G + h) * WR + c] = o[s][mm][j][0];
+                wo[(warp * G + h) * WR + c + 8] = o[s][mm][j][2];
+              } else {
+                const int c = 64 * s + 8 * g + 2 * mm;
+                wo[(warp * G + h) * WR + c] = gsel ? o[s][mm][j][1] : o[s][mm][j][0];
+                wo[(warp * G + h) * WR + c + 1] = gsel ? o[s][mm][j][3] : o[s][mm][j][2];
+              }
             }
         }
       }
@@ -1002,10 +1093,11 @@ fade_status_t encode_rows(CUtensorMap* m, const void* base, unsigned long long r
   return FADE_OK;
 }
 
-template <int D, int G>
+template <int D, int G, bool PQ>
 fade_status_t launch_mma(const fade_config_t* c, const fade_layer_t* L, const MmaArgs& a,
                          const StreamK& sk, cudaStream_t st) {
   using Cfg = MmaCfg<D>;
+  constexpr int kSmem = PQ ? PqCfg<D>::SMEM : Cfg::SMEM;
   const unsigned long long rows = (unsigned long long)c->batch * c->num_kv_heads * a.C;
   CUtensorMap tk[2], tv[2];
   fade_status_t s;
@@ -1013,19 +1105,20 @@ fade_status_t launch_mma(const fade_config_t* c, const fade_layer_t* L, const Mm
     if ((s = encode_rows(&tk[i], L->mid_k_codes[i], rows, Cfg::KROW))) return s;
     if ((s = encode_rows(&tv[i], L->mid_v_codes[i], rows, Cfg::VROW))) return s;
   }
-  auto kern = attn_mid_mma_kernel<D, G>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
+  auto kern = attn_mid_mma_kernel<D, G, PQ>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
       cudaSuccess)
     return launch_status("fade_decode_attention (middle tier) shared-memory opt-in");
   // persistent grid: the schedule's CTAs (as many as fit on the device at once)
-  kern<<<sk.P, MmaShape<D, G>::THREADS, Cfg::SMEM, st>>>(tk[0], tk[1], tv[0], tv[1], a, sk);
+  kern<<<sk.P, MmaShape<D, G, PQ>::THREADS, kSmem, st>>>(tk[0], tk[1], tv[0], tv[1], a, sk);
   return launch_status("fade_decode_attention (middle tier)");
 }
 
 }  // namespace
 
 bool mid_mma_supported(const fade_config_t* c) {
-  return c->middle_k_bits == 4 && c->middle_v_bits == 2 && c->v_codec == FADE_V_INT;
+  // INT4 K with INT2 V, or with PQ-coded V (whose codes fill the INT2 rows)
+  return c->middle_k_bits == 4 && c->middle_v_bits == 2;
 }
 
 int mid_mma_ctas(const fade_config_t* c) {
@@ -1034,7 +1127,8 @@ int mid_mma_ctas(const fade_config_t* c) {
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 1;
   const int G = c->num_q_heads / c->num_kv_heads;
-  const int minb = (FADE_MMA_WIDE && G <= 4) ? FADE_MMA_CTAS_PER_SM : 1;  // MmaShape::MINB
+  const int minb = c->v_codec == FADE_V_PQ ? 1                        // MmaShape::MINB
+                   : (FADE_MMA_WIDE && G <= 4) ? FADE_MMA_CTAS_PER_SM : 1;
   return std::max(1, std::min(kMaxCtaSK, sms * minb));
 }
 
@@ -1097,9 +1191,13 @@ fade_status_t launch_mid_mma(const fade_config_t* c, const fade_layer_t* L, cons
   a.chunk = kTileTok;
   a.nsplit = nsplit;
   a.inv_sqrt_d = 1.0f / sqrtf((float)c->head_dim);
+  a.pq_cb = L->pq_codebook;
   const int G = c->num_q_heads / c->num_kv_heads;
-#define FADE_CASE(D_, G_) \
-  if (c->head_dim == D_ && G == G_) return launch_mma<D_, G_>(c, L, a, sk, st);
+  const bool pq = c->v_codec == FADE_V_PQ;
+#define FADE_CASE(D_, G_)                                                     \
+  if (c->head_dim == D_ && G == G_)                                           \
+    return pq ? launch_mma<D_, G_, true>(c, L, a, sk, st)                     \
+              : launch_mma<D_, G_, false>(c, L, a, sk, st);
   FADE_CASE(64, 1) FADE_CASE(64, 2) FADE_CASE(64, 4) FADE_CASE(64, 8)
   FADE_CASE(128, 1) FADE_CASE(128, 2) FADE_CASE(128, 4) FADE_CASE(128, 8)
 #undef FADE_CASE
