@@ -50,6 +50,12 @@ constexpr int kTileTok = 256;            // tokens per TMA tile
 #ifndef FADE_MMA_CTAS_PER_SM
 #define FADE_MMA_CTAS_PER_SM 2
 #endif
+// Independent (code byte -> centroid -> store) chains a consumer lane keeps in flight when it
+// decodes a PQ-coded V tile (all of them: the measured best).
+#ifndef FADE_PQ_DECODE_UNROLL
+#define FADE_PQ_DECODE_UNROLL 16
+#endif
+constexpr int kPqDecodeUnroll = FADE_PQ_DECODE_UNROLL;
 template <int D, int G, bool PQ = false>
 struct MmaShape {
   static constexpr int CONS = (FADE_MMA_WIDE && G <= 4) ? 8 : 4;
@@ -506,7 +512,7 @@ __device__ __forceinline__ void consume_tile(
 #pragma unroll
     for (int mt = 0; mt < MmaShape<D, G>::MT; ++mt) {
       const int r0 = wr0 + mt * 16;
-#pragma unroll 4
+#pragma unroll kPqDecodeUnroll
       for (int i = lane; i < 16 * SUBS; i += 32) {
         const int tk = i / SUBS, sub = i % SUBS, r = r0 + tk;
         uint32_t off;
