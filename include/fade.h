@@ -63,14 +63,21 @@ typedef enum {
  *   NTK      inv_i = (base * factor^(d / (d - 2)))^(-2i/d) (NTK-aware base scaling)
  *   YARN     the LLAMA3 blend with low_freq_factor = alpha and high_freq_factor = beta of the
  *            YaRN ramp (1 and 32 in its paper); YaRN's attention temperature is not part of
- *            the table (it would scale every rotation, and un-RoPE / re-RoPE with it) */
+ *            the table (it would scale every rotation, and un-RoPE / re-RoPE with it)
+ *   DYNAMIC  dynamic NTK: the NTK rule with the factor taken from the sequence length L,
+ *            base' = base * (factor * L / original_max_position - (factor - 1))^(d / (d - 2))
+ *            when L > original_max_position, the default table otherwise. L is the length the
+ *            table is built for (max_pos of fade_rope_table_init), so every key is rotated and
+ *            re-positioned with one table; re-basing every step as the sequence grows is not
+ *            done (it would re-rotate every cached key). */
 typedef enum {
   FADE_ROPE_NONE = 0,
   FADE_ROPE_DEFAULT = 1,
   FADE_ROPE_LLAMA3 = 2,
   FADE_ROPE_LINEAR = 3,
   FADE_ROPE_NTK = 4,
-  FADE_ROPE_YARN = 5
+  FADE_ROPE_YARN = 5,
+  FADE_ROPE_DYNAMIC = 6
 } fade_rope_kind_t;
 
 /* Eviction policies (FADE-zh §四种驱逐策略详解 1-3). NONE = safe mode (no eviction). */

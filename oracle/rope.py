@@ -36,7 +36,7 @@ F32 = np.float32
 
 
 def inv_freq(kind: str, base: float, head_dim: int, factor=1.0, low_freq_factor=1.0,
-             high_freq_factor=4.0, original_max_position=8192) -> np.ndarray:
+             high_freq_factor=4.0, original_max_position=8192, seq_len=None) -> np.ndarray:
     """fp32 inverse frequencies [d/2] for the rotation pairs.
 
     FADE-zh §RoPE方案兼容性 names the scaling types; each follows its published definition:
@@ -48,13 +48,24 @@ def inv_freq(kind: str, base: float, head_dim: int, factor=1.0, low_freq_factor=
         number of rotations r = L/lambda a pair makes over the original context L, blending
         theta/factor (gamma = 0) with theta (gamma = 1); alpha and beta come in
         ``low_freq_factor`` and ``high_freq_factor``. It is the llama3 rule with those
-        boundaries. YaRN's attention temperature is left out: the table holds pure rotations.
+        boundaries. YaRN's attention temperature is left out: the table holds pure rotations;
+      * "dynamic" (dynamic NTK): the ntk rule with the factor taken from the sequence length
+        ``seq_len``, factor * seq_len / original_max_position - (factor - 1), once the
+        sequence is longer than the original context (default frequencies before). Reading:
+        ``seq_len`` is the length the table is built for, so one table serves every rotation
+        and re-positioning; the rule's re-basing at every decode step is not modelled.
     """
     half = head_dim // 2
     i = np.arange(half, dtype=np.float64)
     b = np.float64(base)
     if kind == "ntk":
         b = b * np.power(np.float64(factor), head_dim / (head_dim - 2.0))
+    if kind == "dynamic":
+        if seq_len is None:
+            raise ValueError("dynamic NTK needs the sequence length")
+        if seq_len > original_max_position:
+            f_dyn = factor * float(seq_len) / float(original_max_position) - (factor - 1.0)
+            b = b * np.power(np.float64(f_dyn), head_dim / (head_dim - 2.0))
     f = np.power(b, -(2.0 * i) / head_dim)
     if kind == "linear":
         f = f / factor
@@ -66,7 +77,7 @@ def inv_freq(kind: str, base: float, head_dim: int, factor=1.0, low_freq_factor=
         t = (L / lam - low_freq_factor) / (high_freq_factor - low_freq_factor)
         mixed = (1.0 - t) * f / factor + t * f
         f = np.where(lam < high_wl, f, np.where(lam > low_wl, f / factor, mixed))
-    elif kind not in ("default", "ntk"):
+    elif kind not in ("default", "ntk", "dynamic"):
         raise ValueError(f"unsupported rope kind {kind!r}")
     return f.astype(F32)
 
@@ -101,7 +112,7 @@ class RopeTable:
         self.max_pos = max_pos
         if kind != "none":
             self.inv_freq = inv_freq(kind, base, head_dim, factor, low_freq_factor,
-                                     high_freq_factor, original_max_position)
+                                     high_freq_factor, original_max_position, seq_len=max_pos)
             self.cos, self.sin = table(self.inv_freq, max_pos)
 
     @classmethod

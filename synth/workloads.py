@@ -17,11 +17,12 @@ from typing import Optional
 @dataclass(frozen=True)
 class Rope:
     kind: str = "default"          # "none" | "default" | "llama3" | "linear" | "ntk" | "yarn"
+                                   # | "dynamic"
     base: float = 10000.0
-    factor: float = 1.0            # llama3, linear, ntk, yarn
+    factor: float = 1.0            # llama3, linear, ntk, yarn, dynamic
     low_freq_factor: float = 1.0   # llama3; yarn: alpha
     high_freq_factor: float = 4.0  # llama3; yarn: beta
-    original_max_position: int = 8192
+    original_max_position: int = 8192   # llama3, yarn, dynamic
 
 
 @dataclass(frozen=True)

@@ -60,6 +60,7 @@ def _cfg(T, **kw):
     (dict(rope_base=1.0), 1),
     (dict(rope_kind="llama3", rope_low_freq_factor=4.0, rope_high_freq_factor=1.0), 1),
     (dict(v_codec="pq", middle_v_bits=4), 1),
+    (dict(rope_kind="dynamic", rope_factor=0.5), 1),
 ])
 def test_invalid_configs_are_rejected_on_the_host(T, kw, status):
     with pytest.raises(T.FadeError) as e:

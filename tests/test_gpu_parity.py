@@ -58,10 +58,14 @@ _SCALED_ROPES = {
     "ntk": Rope("ntk", 1e4, factor=8.0),
     "yarn": Rope("yarn", 1e4, factor=8.0, low_freq_factor=1.0, high_freq_factor=32.0,
                  original_max_position=4096),
+    # the table length (40 000 here; about 900 in the lockstep case) exceeds the original
+    # context, so the base is scaled by the length-derived factor
+    "dynamic": Rope("dynamic", 1e4, factor=2.0, original_max_position=4096),
+    "dynamic_short": Rope("dynamic", 1e4, factor=2.0, original_max_position=512),
 }
 
 
-@pytest.mark.parametrize("key", [1, 3, 4, "linear", "ntk", "yarn"])
+@pytest.mark.parametrize("key", [1, 3, 4, "linear", "ntk", "yarn", "dynamic"])
 def test_rope_table_and_apply(T, key):
     import torch
 
@@ -175,6 +179,10 @@ def _small(key):
         return get_workload(3).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
                                       rope=_SCALED_ROPES["ntk"], prompt_len=700,
                                       int4_budget=250, steps=6), None
+    if key == "rope_dynamic_pos":
+        return get_workload(4).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                      rope=_SCALED_ROPES["dynamic_short"], prompt_len=900,
+                                      int4_budget=300, steps=5), None
     if key == "rope_yarn_ema":
         return get_workload(5).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
                                       rope=_SCALED_ROPES["yarn"], ragged=(900, 1300),
@@ -187,7 +195,7 @@ def _small(key):
                                  "d64_k2v2_ema", "d128_k2v2_pos", "d64_k4v4_pos",
                                  "deg_nosink", "deg_w1_h2o", "deg_budget0", "deg_short_ragged",
                                  "deg_norope_ema", "rope_linear_pos", "rope_ntk_h2o",
-                                 "rope_yarn_ema"])
+                                 "rope_yarn_ema", "rope_dynamic_pos"])
 def test_lockstep_small_workloads(T, key):
     wl, cap = _small(key)
     ls = Lockstep(wl, mid_capacity=cap)

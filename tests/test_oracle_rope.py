@@ -101,6 +101,30 @@ def test_ntk_keeps_the_highest_and_divides_the_lowest_frequency():
         assert np.all(ntk[1:-1] < ref[1:-1]) and np.all(ntk[1:-1] > ref[1:-1] / factor)
 
 
+def test_dynamic_ntk_follows_the_sequence_length():
+    """Dynamic NTK: up to the original context the default frequencies; beyond it pair 0
+    keeps frequency 1 and the last pair's frequency is divided by exactly
+    factor * L / L0 - (factor - 1) (e.g. 2 * 16384 / 4096 - 1 = 7); longer sequences scale
+    more (monotone), and the table of length L is the one RopeTable builds."""
+    d, base, L0, factor = 128, 1e4, 4096, 2.0
+    ref = rope.inv_freq("default", base, d).astype(np.float64)
+    for L in (100, 4096):
+        dyn = rope.inv_freq("dynamic", base, d, factor, original_max_position=L0, seq_len=L)
+        assert np.array_equal(dyn, rope.inv_freq("default", base, d))
+    prev = ref
+    for L, want in ((8192, 3.0), (16384, 7.0), (40000, 2 * 40000 / 4096 - 1)):
+        dyn = rope.inv_freq("dynamic", base, d, factor, original_max_position=L0,
+                            seq_len=L).astype(np.float64)
+        assert dyn[0] == 1.0
+        assert math.isclose(ref[-1] / dyn[-1], want, rel_tol=2 ** -21)
+        assert np.all(dyn[1:] < prev[1:])   # a longer sequence lowers every frequency further
+        prev = dyn
+    t = rope.RopeTable("dynamic", d, 16384, base=base, factor=factor, original_max_position=L0)
+    assert math.isclose(ref[-1] / float(t.inv_freq[-1]), 7.0, rel_tol=2 ** -21)
+    with pytest.raises(ValueError):
+        rope.inv_freq("dynamic", base, d, factor, original_max_position=L0)
+
+
 def test_yarn_bands_over_rotations_per_context():
     """YaRN (alpha = 1, beta = 32): pairs making more than beta rotations over the original
     context keep their frequency, pairs making fewer than alpha are interpolated by the factor,

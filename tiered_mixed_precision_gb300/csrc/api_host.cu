@@ -72,7 +72,7 @@ fade_status_t validate_config(const fade_config_t* c) {
                      "precedes eviction)",
                      c->mid_capacity, c->int4_budget + 1);
   const fade_rope_t& r = c->rope;
-  if (r.kind < FADE_ROPE_NONE || r.kind > FADE_ROPE_YARN)
+  if (r.kind < FADE_ROPE_NONE || r.kind > FADE_ROPE_DYNAMIC)
     return set_error(FADE_ERR_UNSUPPORTED, "unknown rope kind %d", r.kind);
   if (r.kind != FADE_ROPE_NONE && !(r.base > 1.0))
     return set_error(FADE_ERR_INVALID_ARGUMENT, "rope base must exceed 1");
@@ -82,6 +82,9 @@ fade_status_t validate_config(const fade_config_t* c) {
     return set_error(FADE_ERR_INVALID_ARGUMENT, "bad llama3 / yarn rope scaling parameters");
   if ((r.kind == FADE_ROPE_LINEAR || r.kind == FADE_ROPE_NTK) && !(r.factor > 0.0))
     return set_error(FADE_ERR_INVALID_ARGUMENT, "rope scaling factor must be positive");
+  if (r.kind == FADE_ROPE_DYNAMIC && !(r.factor >= 1.0 && r.original_max_position > 0))
+    return set_error(FADE_ERR_INVALID_ARGUMENT,
+                     "dynamic NTK needs factor >= 1 and original_max_position > 0");
   return FADE_OK;
 }
 

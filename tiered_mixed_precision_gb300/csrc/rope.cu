@@ -1,8 +1,9 @@
 // RoPE table and rotation of q/k to cache positions.
 // Sources: page "FADE：面向LLM推理的注意力感知分层KV缓存压缩技术", §RoPE重计算 (float32 RoPE math,
-// cast through the model dtype) and §RoPE方案兼容性 (standard RoPE; llama3, linear, ntk and yarn
-// scaling, as their published definitions: position interpolation, NTK-aware base scaling and
-// YaRN's ramp over rotations per original context); page
+// cast through the model dtype) and §RoPE方案兼容性 (standard RoPE; llama3, linear, ntk, dynamic
+// and yarn scaling, as their published definitions: position interpolation, NTK-aware base
+// scaling, with the factor from the sequence length for dynamic, and YaRN's ramp over rotations
+// per original context); page
 // "探秘Transformer系列之（25）--- KV Cache优化之处理长文本序列", §1.2.2 StreamingLLM (positions are
 // indices inside the cache).
 #include <math.h>
@@ -18,14 +19,18 @@ struct InvFreq {
 
 // inv_freq_i in fp64 per the scheme (fade_rope_kind_t), rounded once to fp32. Host code:
 // compiled without floating-point contraction so every step rounds as written.
-InvFreq host_inv_freq(const fade_config_t* c) {
+InvFreq host_inv_freq(const fade_config_t* c, int max_pos) {
   InvFreq f{};
   const int half = c->head_dim / 2;
   const fade_rope_t& r = c->rope;
-  // NTK-aware scaling raises the base so that the lowest frequency is divided by the factor
-  const double base = r.kind == FADE_ROPE_NTK
-                          ? r.base * pow(r.factor, (double)c->head_dim / (c->head_dim - 2))
-                          : r.base;
+  // NTK-aware scaling raises the base so that the lowest frequency is divided by the factor;
+  // dynamic NTK takes that factor from the sequence length (the table's length)
+  double ntk = 0.0;
+  if (r.kind == FADE_ROPE_NTK) ntk = r.factor;
+  if (r.kind == FADE_ROPE_DYNAMIC && max_pos > r.original_max_position)
+    ntk = r.factor * (double)max_pos / (double)r.original_max_position - (r.factor - 1.0);
+  const double base =
+      ntk > 0.0 ? r.base * pow(ntk, (double)c->head_dim / (c->head_dim - 2)) : r.base;
   for (int i = 0; i < half; ++i) {
     double x = pow(base, -(2.0 * i) / c->head_dim);
     if (r.kind == FADE_ROPE_LINEAR) x = x / r.factor;
@@ -99,7 +104,7 @@ extern "C" fade_status_t fade_rope_table_init(const fade_config_t* cfg, float* t
   const int half = cfg->head_dim / 2;
   const long long n = (long long)max_pos * half;
   rope_table_kernel<<<ceil_div(n, 256), 256, 0, as_stream(stream)>>>(
-      host_inv_freq(cfg), half, max_pos, table);
+      host_inv_freq(cfg, max_pos), half, max_pos, table);
   return launch_status("fade_rope_table_init");
 }
 

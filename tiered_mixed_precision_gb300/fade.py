@@ -18,7 +18,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libfade.so")
 
 FADE_OK, FADE_ERR_INVALID_ARGUMENT, FADE_ERR_UNSUPPORTED, FADE_ERR_CAPACITY, FADE_ERR_CUDA = range(5)
-ROPE_KINDS = {"none": 0, "default": 1, "llama3": 2, "linear": 3, "ntk": 4, "yarn": 5}
+ROPE_KINDS = {"none": 0, "default": 1, "llama3": 2, "linear": 3, "ntk": 4, "yarn": 5,
+              "dynamic": 6}
 POLICIES = {"none": 0, "h2o": 1, "ema": 2, "position": 3}
 V_CODECS = {"int": 0, "pq": 1}
 PQ_SUB, PQ_CENTROIDS, PQ_MAX_CALIB = 4, 256, 8192
