@@ -140,3 +140,18 @@ def test_missing_library_fails_loudly(monkeypatch):
     monkeypatch.setattr(F, "LIB_PATH", "/nonexistent/libfade.so")
     with pytest.raises(ImportError):
         F.lib()
+
+
+def test_config_struct_is_cached_and_rebuilt_on_change(T):
+    """Config.c() builds the C struct once per set of field values (every entry point takes
+    it); setting a field, or dataclasses.replace, gives a fresh struct."""
+    import dataclasses
+
+    cfg = _cfg(T)
+    a = cfg.c()
+    assert cfg.c() is a
+    cfg.policy = "ema"
+    assert cfg.c() is not a and cfg.c().policy == 2
+    pq = dataclasses.replace(cfg, v_codec="pq")
+    assert pq.c().v_codec == 1 and cfg.c().v_codec == 0
+    assert dataclasses.replace(cfg) == cfg

@@ -166,16 +166,24 @@ class Config:
     rope_original_max_position: int = 8192
     shared_rows: bool = False  # the rows share their tier decisions (row-summed scores)
     v_codec: str = "int"       # "pq": product-quantised middle V (needs middle_v_bits = 2)
-    _c: ConfigT = field(default=None, repr=False, compare=False)
+    _c: ConfigT = field(default=None, init=False, repr=False, compare=False)
+
+    def __setattr__(self, name, value):
+        object.__setattr__(self, name, value)
+        if name != "_c":   # any change of a field invalidates the cached C struct
+            object.__setattr__(self, "_c", None)
 
     def c(self) -> ConfigT:
-        r = RopeT(ROPE_KINDS[self.rope_kind], self.rope_original_max_position, self.rope_base,
-                  self.rope_factor, self.rope_low_freq_factor, self.rope_high_freq_factor)
-        self._c = ConfigT(self.batch, self.num_q_heads, self.num_kv_heads, self.head_dim,
-                          self.n_sink, self.recent_window, self.int4_budget,
-                          self.middle_k_bits, self.middle_v_bits, self.mid_capacity,
-                          POLICIES[self.policy], self.ema_decay, int(self.shared_rows),
-                          V_CODECS[self.v_codec], r)
+        """The C struct (built once per set of field values: every entry point takes it)."""
+        if self._c is None:
+            r = RopeT(ROPE_KINDS[self.rope_kind], self.rope_original_max_position,
+                      self.rope_base, self.rope_factor, self.rope_low_freq_factor,
+                      self.rope_high_freq_factor)
+            object.__setattr__(self, "_c", ConfigT(
+                self.batch, self.num_q_heads, self.num_kv_heads, self.head_dim, self.n_sink,
+                self.recent_window, self.int4_budget, self.middle_k_bits, self.middle_v_bits,
+                self.mid_capacity, POLICIES[self.policy], self.ema_decay,
+                int(self.shared_rows), V_CODECS[self.v_codec], r))
         return self._c
 
     @property
