@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 
 from synth import draw_prompt, draw_vectors, get_workload
+from synth.draws import pq_calibration
 
 pytestmark = pytest.mark.gpu
 
@@ -36,14 +37,19 @@ def _masses(wl):
     return out
 
 
-def _make(wl, masses):
+def _make(wl, masses, v_codec="int"):
     import torch
 
     import tiered_mixed_precision_gb300 as T
     from tiered_mixed_precision_gb300.model import FadeCache
 
     cfg = T.Config.from_workload(wl)
+    cfg.v_codec = v_codec
     fc = FadeCache(cfg, wl.layers, wl.prompt_len, wl.prompt_len + 64, "cuda")
+    if v_codec == "pq":   # a codebook made of 256 V-like draws
+        rows = pq_calibration(wl, 256)
+        cb = rows.reshape(256, wl.head_dim // 4, 4).transpose(1, 0, 2).copy()
+        fc.set_pq_codebook(torch.from_numpy(cb).cuda())
     for layer in range(wl.layers):
         pr = draw_prompt(wl, layer)
         fc.prefill(layer, torch.from_numpy(pr["k"]).cuda(), torch.from_numpy(pr["v"]).cuda(),
@@ -89,8 +95,9 @@ def test_graph_replay_matches_eager_steps(policy):
                         assert a_[key] == b_[key], (layer, b, h, key)
 
 
-@pytest.mark.parametrize("policy,n_side", [("position", 1), ("position", 2), ("h2o", 2)])
-def test_pipelined_graph_matches_eager_steps(policy, n_side):
+@pytest.mark.parametrize("policy,n_side,v_codec", [("position", 1, "int"), ("position", 2, "int"),
+                                                   ("h2o", 2, "int"), ("position", 2, "pq")])
+def test_pipelined_graph_matches_eager_steps(policy, n_side, v_codec):
     """Pipelined steps (each layer's maintenance for the next step on a side stream, right
     after its attention; with two side streams the layers take them in turn) give the same
     outputs as the method's step order, and after one more maintenance pass the same cache."""
@@ -101,7 +108,7 @@ def test_pipelined_graph_matches_eager_steps(policy, n_side):
     if policy == "h2o":
         wl = wl.scaled(rope=get_workload(3).rope)
     masses = _masses(wl)
-    eager, piped = _make(wl, masses), _make(wl, masses)
+    eager, piped = _make(wl, masses, v_codec), _make(wl, masses, v_codec)
     L, B, Hq, Hkv, d = wl.layers, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
     steps = 4
     q = torch.from_numpy(draw_vectors(wl, "q", (steps, L, B, Hq, d), "pipe")).cuda()

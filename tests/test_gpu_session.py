@@ -8,12 +8,15 @@ import numpy as np
 import pytest
 
 from synth import draw_prompt, draw_vectors, get_workload, ragged_context_lengths
+from synth.draws import pq_calibration, pq_init_indices
 
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("policy", ["position", "h2o", "ema"])
-def test_state_dict_round_trip_continues_bit_identically(policy):
+@pytest.mark.parametrize("policy,v_codec", [("position", "int"), ("h2o", "int"), ("ema", "int"),
+                                            ("position", "pq")])
+def test_state_dict_round_trip_continues_bit_identically(policy, v_codec):
+    """With PQ-coded V the layers' codebooks travel in the state too."""
     import torch
 
     import tiered_mixed_precision_gb300 as T
@@ -23,10 +26,16 @@ def test_state_dict_round_trip_continues_bit_identically(policy):
     wl = get_workload(base).scaled(layers=2, batch=2, num_q_heads=8, num_kv_heads=2,
                                    prompt_len=700, int4_budget=200, ragged=None, steps=6)
     cfg = T.Config.from_workload(wl)
+    cfg.v_codec = v_codec
     lens = ragged_context_lengths(wl)
     maxP = int(lens.max())
     max_pos = maxP + 32
     a = FadeCache(cfg, wl.layers, maxP, max_pos)
+    if v_codec == "pq":   # a trained codebook per layer (different per layer)
+        for layer in range(wl.layers):
+            calib = pq_calibration(wl.scaled(seed=wl.seed + layer), 600, backend="torch",
+                                   device="cuda")
+            a.train_pq_codebook(calib, pq_init_indices(600, layer), 2, layer=layer)
     for layer in range(wl.layers):
         pr = draw_prompt(wl, layer, maxP, with_q=policy == "h2o", backend="torch", device="cuda")
         a.prefill(layer, pr["k"], pr["v"], lens, None, q_raw=pr.get("q"))

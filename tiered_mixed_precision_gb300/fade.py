@@ -135,11 +135,22 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+_raw_stream = None
+
+
 def _stream(stream):
+    """The handle of ``stream``, or of the current CUDA stream (the raw-handle query when
+    torch has it: it skips building a Stream object on every call)."""
+    global _raw_stream
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
     import torch
 
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    if _raw_stream is None:
+        fn = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        _raw_stream = ((lambda: fn(torch.cuda.current_device())) if fn is not None
+                       else (lambda: torch.cuda.current_stream().cuda_stream))
+    return ctypes.c_void_p(_raw_stream())
 
 
 # --------------------------------------------------------------------------- config
