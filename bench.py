@@ -363,6 +363,20 @@ def run_ours(args, rank, world):
     if n_side <= 0:  # concurrent compactions of large layers compete; short ones fill gaps
         n_side = 1 if B * Hkv * max(wl.int4_budget, 0) >= (1 << 20) else 2
     side = [torch.cuda.Stream() for _ in range(n_side)] if pipelined else None
+    # a cache that grows every step (no eviction) with CUDA-core attention: one captured
+    # step replayed with the positions copied in and the host mirror advanced
+    growing = not steady and not args.no_graph and fc.growing_graph_ok()
+    if growing:
+        fc.timers = None   # per-call events come from eager steps after the timed region
+        fc.launches = 0
+        graph = fc.capture_growing_step(qb, kb, vb, out)
+        launches_per_step = fc.launches
+        qb.copy_(q_all[W - 1 if W > 0 else 0])
+        kb.copy_(k_all[W - 1 if W > 0 else 0])
+        vb.copy_(v_all[W - 1 if W > 0 else 0])
+        fc.replay_growing(graph)
+        torch.cuda.synchronize()
+        progress("growing-cache graph captured and replayed once")
     if steady and not args.no_graph:
         if pipelined:
             # prologue: the coming step's maintenance of every layer; from here on each step
@@ -389,7 +403,7 @@ def run_ours(args, rank, world):
             qb.copy_(q_all[s], non_blocking=True)
             kb.copy_(k_all[s], non_blocking=True)
             vb.copy_(v_all[s], non_blocking=True)
-            graph.replay()
+            fc.replay_growing(graph) if growing else graph.replay()
         else:
             step(s)
     e1.record()
@@ -404,8 +418,8 @@ def run_ours(args, rank, world):
     per_call_overlapped = None
     ms_iso = None
     try:
-        if graph is None:  # eager launches: per-call events come from extra steps below
-            raise RuntimeError("eager launches")
+        if graph is None or growing:  # per-call events come from extra eager steps below
+            raise RuntimeError("eager launches" if graph is None else "growing-cache graph")
         per_call = {name: [a.elapsed_time(b) for a, b in pairs]
                     for name, pairs in fc.timers.items()}
         if pipelined:
@@ -502,7 +516,7 @@ def run_ours(args, rank, world):
                 qb.copy_(qh[s], non_blocking=True)
                 kb.copy_(kh[s], non_blocking=True)
                 vb.copy_(vh[s], non_blocking=True)
-                graph.replay()
+                fc.replay_growing(graph) if growing else graph.replay()
             else:
                 qd.copy_(qh[s], non_blocking=True)
                 kd.copy_(kh[s], non_blocking=True)
@@ -534,7 +548,9 @@ def run_ours(args, rank, world):
                                f"{PQ_CALIB_ROWS} synthetic rows, {PQ_ITERS} rounds)"),
                    "l2": "no flush: the compressed cache read per step is far larger than L2",
                    "parallelism": f"replicas x{world} (rows independent, no collective)",
-                   "launch": ("cuda graph per step" if graph is not None else "eager launches") +
+                   "launch": ("cuda graph per step (growing cache: positions copied in, host "
+                              "mirror advanced per replay)" if growing else
+                              "cuda graph per step" if graph is not None else "eager launches") +
                              (f"; each layer's maintenance overlaps the next layers "
                               f"({len(side)} side streams taken in turn)" if pipelined else ""),
                    "per_call_timing": timing_note},

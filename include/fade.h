@@ -271,6 +271,13 @@ fade_status_t fade_pq_train(const uint16_t* calib, int64_t n_vec, int32_t dim,
                             const int32_t* h_init_idx, int32_t iters, uint16_t* codebook,
                             void* ws, size_t ws_bytes, void* stream);
 
+/* Host mirror only: apply to h_n_sink / h_n_mid / h_n_recent the tier-count changes of one
+ * decode step (fade_cache_demote, fade_evict_rerope, fade_cache_append in that order), with
+ * their capacity checks, without enqueuing any work. For a caller that replays a captured
+ * step (a CUDA graph), whose kernels advance the device-side metadata themselves. On an error
+ * (FADE_ERR_CAPACITY: a full middle tier or recent window) the mirror is left unchanged. */
+fade_status_t fade_cache_advance_host(const fade_config_t* cfg, fade_layer_t* layer);
+
 /* Empty the cache: zero the device metadata and the host mirror. */
 fade_status_t fade_cache_reset(const fade_config_t* cfg, fade_layer_t* layer, void* stream);
 

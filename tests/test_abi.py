@@ -155,3 +155,37 @@ def test_config_struct_is_cached_and_rebuilt_on_change(T):
     pq = dataclasses.replace(cfg, v_codec="pq")
     assert pq.c().v_codec == 1 and cfg.c().v_codec == 0
     assert dataclasses.replace(cfg) == cfg
+
+
+@pytest.mark.parametrize("policy,budget", [("none", -1), ("position", 3), ("h2o", 5)])
+def test_advance_host_follows_the_oracle_counts(T, policy, budget):
+    """fade_cache_advance_host moves the host mirror exactly as one decode step moves the
+    oracle's tier counts (demote, evict, append), and a step that would overflow the middle
+    tier is refused with the mirror unchanged."""
+    from oracle.cache import Params, UnitCache
+    from oracle.rope import RopeTable
+    from synth import Workload, draw_decode_tokens, draw_prompt
+
+    wl = Workload(name="t", layers=1, batch=1, num_q_heads=4, num_kv_heads=1, head_dim=64,
+                  n_sink=2, recent_window=4, int4_budget=budget, policy=policy,
+                  middle_k_bits=4, middle_v_bits=2, prompt_len=3, steps=14, seed=5)
+    cfg = T.Config.from_workload(wl)
+    layer = T.TieredLayer(cfg, 16, device="cpu")
+    u = UnitCache(Params.from_workload(wl), RopeTable.from_workload(wl, 64))
+    pr = draw_prompt(wl, 0)
+    u.prefill(pr["k"][0, 0], pr["v"][0, 0], mass=np.ones(3) if policy == "h2o" else None)
+    layer.h_n_sink[0], layer.h_n_mid[0], layer.h_n_recent[0] = u.n_sink, u.n_mid, u.n_recent
+    for step in range(14):
+        t = draw_decode_tokens(wl, 0, step)
+        u.step(t["q"][0], t["k"][0, 0], t["v"][0, 0])
+        T.fade_cache_advance_host(layer)
+        assert (layer.h_n_sink[0], layer.h_n_mid[0], layer.h_n_recent[0]) == \
+            (u.n_sink, u.n_mid, u.n_recent), step
+    if policy == "none":   # the middle tier is at its capacity: the next demotion is refused
+        full = T.TieredLayer(T.Config.from_workload(wl, mid_capacity=layer.h_n_mid[0]), 16,
+                             device="cpu")
+        full.h_n_sink[0], full.h_n_mid[0], full.h_n_recent[0] = 2, layer.h_n_mid[0], 4
+        with pytest.raises(T.FadeError) as e:
+            T.fade_cache_advance_host(full)
+        assert e.value.status == 3
+        assert (full.h_n_sink[0], full.h_n_mid[0], full.h_n_recent[0]) == (2, layer.h_n_mid[0], 4)

@@ -139,3 +139,55 @@ def test_pipelined_graph_matches_eager_steps(policy, n_side, v_codec):
                         assert np.array_equal(a_[key], b_[key]), (layer, b, h, key)
                     else:
                         assert a_[key] == b_[key], (layer, b, h, key)
+
+
+@pytest.mark.parametrize("kb,vb", [(4, 4), (2, 2)])
+def test_growing_graph_matches_eager_steps(kb, vb):
+    """Without eviction the cache grows by one token a step; a step captured once (attention
+    on the CUDA-core kernel, sized by the middle capacity) and replayed with the positions
+    copied in and the host mirror advanced gives the same bytes as launching every call."""
+    import torch
+
+    wl = get_workload(2).scaled(layers=2, batch=2, num_q_heads=8, num_kv_heads=2,
+                                prompt_len=700, middle_k_bits=kb, middle_v_bits=vb, steps=6)
+    import tiered_mixed_precision_gb300 as T
+    from tiered_mixed_precision_gb300.model import FadeCache
+
+    def make():
+        cfg = T.Config.from_workload(wl, mid_capacity=700)
+        fc = FadeCache(cfg, wl.layers, wl.prompt_len, wl.prompt_len + 64, "cuda")
+        for layer in range(wl.layers):
+            pr = draw_prompt(wl, layer)
+            fc.prefill(layer, torch.from_numpy(pr["k"]).cuda(), torch.from_numpy(pr["v"]).cuda())
+        return fc
+
+    eager, grown = make(), make()
+    assert grown.growing_graph_ok()
+    L, B, Hq, Hkv, d = wl.layers, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+    steps = 6
+    q = torch.from_numpy(draw_vectors(wl, "q", (steps, L, B, Hq, d), "grow")).cuda()
+    k = torch.from_numpy(draw_vectors(wl, "k", (steps, L, B, Hkv, d), "grow")).cuda()
+    v = torch.from_numpy(draw_vectors(wl, "v", (steps, L, B, Hkv, d), "grow")).cuda()
+    out_e = torch.empty((L, B, Hq, d), dtype=torch.float16, device="cuda")
+    out_g = torch.empty_like(out_e)
+    qb, kb_, vb_ = q[0].clone(), k[0].clone(), v[0].clone()
+    g = grown.capture_growing_step(qb, kb_, vb_, out_g)
+    for s in range(steps):
+        eager.step_all(q[s], k[s], v[s], out_e)
+        qb.copy_(q[s])
+        kb_.copy_(k[s])
+        vb_.copy_(v[s])
+        grown.replay_growing(g)
+        torch.cuda.synchronize()
+        assert torch.equal(out_e.view(torch.int16), out_g.view(torch.int16)), f"step {s}"
+        assert all((a == b).all() for x, y in zip(eager.mirror(), grown.mirror())
+                   for a, b in zip(x, y))
+    for layer in range(L):
+        for b in range(B):
+            for h in range(Hkv):
+                a_, b_ = eager.unit_state(layer, b, h), grown.unit_state(layer, b, h)
+                for key in a_:
+                    if isinstance(a_[key], np.ndarray):
+                        assert np.array_equal(a_[key], b_[key]), (layer, b, h, key)
+                    else:
+                        assert a_[key] == b_[key], (layer, b, h, key)

@@ -577,11 +577,14 @@ extern "C" fade_status_t fade_decode_attention(const fade_config_t* c, const fad
     a.nsplit = 1 + sk.smax;
   } else {
     sk.P = 0;
-    // PQ: fewer, longer middle splits, so that staging the codebook (256 x d fp16 from L2)
-    // stays small beside the split's own bytes
-    a.chunk = choose_chunk(max_mid, units, c->v_codec == FADE_V_PQ ? 16 * kTile : kTile,
+    // splits sized by the middle capacity, not the current count: the launch is then the
+    // same at every step while the cache grows (a captured step can be replayed), and splits
+    // past a unit's tokens write empty partials. PQ: fewer, longer middle splits, so that
+    // staging the codebook (256 x d fp16 from L2) stays small beside the split's own bytes
+    a.chunk = choose_chunk(c->mid_capacity, units,
+                           c->v_codec == FADE_V_PQ ? 16 * kTile : kTile,
                            (c->v_codec == FADE_V_PQ ? 4LL : 8LL) * 152);
-    a.nsplit = 1 + (max_mid + a.chunk - 1) / a.chunk;
+    a.nsplit = 1 + (c->mid_capacity + a.chunk - 1) / a.chunk;
   }
   a.scale = 1.0f / sqrtf((float)c->head_dim);
   a.pq_cb = L->pq_codebook;

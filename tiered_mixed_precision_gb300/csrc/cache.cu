@@ -1311,6 +1311,40 @@ extern "C" fade_status_t fade_cache_append(const fade_config_t* c, fade_layer_t*
   return FADE_OK;
 }
 
+extern "C" fade_status_t fade_cache_advance_host(const fade_config_t* c, fade_layer_t* L) {
+  clear_error();
+  fade_status_t st = validate_config(c);
+  if (st) return st;
+  if (!L || !L->h_n_sink || !L->h_n_mid || !L->h_n_recent)
+    return set_error(FADE_ERR_INVALID_ARGUMENT, "host mirror arrays are NULL");
+  const bool evicts = c->policy != FADE_EVICT_NONE && c->int4_budget >= 0;
+  // every row's counts after the step, checked before any of them is stored
+  for (int pass = 0; pass < 2; ++pass)
+    for (int b = 0; b < c->batch; ++b) {
+      int s = L->h_n_sink[b], m = L->h_n_mid[b], r = L->h_n_recent[b];
+      if (r == c->recent_window) {  // demote
+        if (m + 1 > c->mid_capacity)
+          return set_error(FADE_ERR_CAPACITY, "row %d: middle tier full (%d slots)", b,
+                           c->mid_capacity);
+        m += 1;
+        r -= 1;
+      }
+      if (evicts && m > c->int4_budget) m = c->int4_budget;  // evict
+      if (s >= c->n_sink && r >= c->recent_window)             // append
+        return set_error(FADE_ERR_CAPACITY, "row %d: recent window full (demote first)", b);
+      if (s < c->n_sink)
+        s += 1;
+      else
+        r += 1;
+      if (pass == 1) {
+        L->h_n_sink[b] = s;
+        L->h_n_mid[b] = m;
+        L->h_n_recent[b] = r;
+      }
+    }
+  return FADE_OK;
+}
+
 extern "C" fade_status_t fade_evict_rerope(const fade_config_t* c, fade_layer_t* L,
                                            const float* table, int32_t max_pos, void* stream) {
   clear_error();

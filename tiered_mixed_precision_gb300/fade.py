@@ -109,6 +109,7 @@ def lib():
             "fade_h2o_accumulate": (c_i32, [S(ConfigT), S(LayerT), c_vp, c_vp, c_vp]),
             "fade_next_position": (c_i32, [S(ConfigT), S(LayerT), c_i32]),
             "fade_compressed_bytes": (ctypes.c_uint64, [S(ConfigT), S(LayerT)]),
+            "fade_cache_advance_host": (c_i32, [S(ConfigT), S(LayerT)]),
             "fade_pq_encode": (c_i32, [c_vp, c_vp, c_i64, c_i32, c_vp, c_vp]),
             "fade_pq_decode": (c_i32, [c_vp, c_vp, c_i64, c_i32, c_vp, c_vp]),
             "fade_pq_train": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp]),
@@ -381,6 +382,10 @@ def fade_next_position(layer: TieredLayer, row: int) -> int:
     if r < 0:
         raise FadeError(FADE_ERR_INVALID_ARGUMENT, fade_last_error())
     return r
+
+
+def fade_cache_advance_host(layer: TieredLayer):
+    _check(lib().fade_cache_advance_host(ctypes.byref(layer.cfg.c()), ctypes.byref(layer.c)))
 
 
 def fade_compressed_bytes(layer: TieredLayer) -> int:

@@ -65,6 +65,7 @@ class FadeCache:
         self.timers = None      # optional {"attention": [...], "evict": [...]} of event pairs
         self._graph_events = []  # timing events referenced by captured graphs
         self.launches = 0       # kernels enqueued by step_layer calls
+        self._pos_ring, self._pos_ring_ev, self._pos_ring_i = None, None, 0
 
     # ------------------------------------------------------------------ session persistence
     # Page "FADE：面向LLM推理的注意力感知分层KV缓存压缩技术", §会话持久化: the compressed cache is
@@ -285,6 +286,57 @@ class FadeCache:
             if any((x != y).any() for x, y in zip(a, b)):
                 raise RuntimeError("capture_step needs a steady-state cache (tier counts changed)")
         return g
+
+    # ------------------------------------------------------------------ growing caches
+    def growing_graph_ok(self) -> bool:
+        """A step of this cache can be captured once and replayed while the cache grows: no
+        eviction, attention on the CUDA-core kernel (whose launch is sized by the middle
+        capacity; the tensor-core kernel's schedule follows the current counts), and every
+        row with full sinks and a full recent window, so that each step demotes one token
+        and appends one in every row."""
+        c = self.cfg
+        if c.evicts or (c.middle_k_bits == 4 and c.middle_v_bits == 2):
+            return False
+        return all(bool((L.h_n_sink == c.n_sink).all() and (L.h_n_recent == c.recent_window).all())
+                   for L in self.layers)
+
+    def capture_growing_step(self, q, k, v, out):
+        """Capture every layer's step (positions excluded: ``replay_growing`` sets them) as a
+        CUDA graph for a cache that grows by one token a step (see ``growing_graph_ok``).
+        The host mirror is left as it was before the capture."""
+        if not self.growing_graph_ok():
+            raise RuntimeError("capture_growing_step needs a growing cache without eviction, "
+                               "full sinks and recent windows, and CUDA-core attention")
+        before = self.mirror()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for layer in range(len(self.layers)):
+                self.step_layer(layer, q[layer], k[layer], v[layer], out[layer])
+        for L, (s, m, r) in zip(self.layers, before):
+            L.h_n_sink[:], L.h_n_mid[:], L.h_n_recent[:] = s, m, r
+        return g
+
+    def replay_growing(self, graph):
+        """One step from a graph of ``capture_growing_step``: the positions (from the host
+        mirror) are copied in through a ring of pinned buffers, the graph is replayed, and the
+        host mirror advances by the step's count changes."""
+        if self._pos_ring is None:
+            self._pos_ring = [torch.zeros(self.cfg.batch, dtype=torch.int32).pin_memory()
+                              for _ in range(4)]
+            self._pos_ring_ev = [None] * 4
+        i = self._pos_ring_i
+        self._pos_ring_i = (i + 1) % len(self._pos_ring)
+        if self._pos_ring_ev[i] is not None:
+            self._pos_ring_ev[i].synchronize()   # the copy that last read this buffer is done
+        buf = self._pos_ring[i]
+        buf.copy_(torch.from_numpy(self.next_positions()))
+        self.pos.copy_(buf, non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record()
+        self._pos_ring_ev[i] = ev
+        graph.replay()
+        for L in self.layers:
+            F.fade_cache_advance_host(L)
 
     def _tick(self, name):
         if self.timers is None:
