@@ -56,6 +56,16 @@ constexpr int kTileTok = 256;            // tokens per TMA tile
 #define FADE_PQ_DECODE_UNROLL 16
 #endif
 constexpr int kPqDecodeUnroll = FADE_PQ_DECODE_UNROLL;
+// The FP16 tiers (sinks + recent ring) of an item on the tensor cores (1) or the CUDA cores (0;
+// also the path when they do not fit a ring stage).
+#ifndef FADE_F16_MMA
+#define FADE_F16_MMA 1
+#endif
+constexpr bool kF16Mma = FADE_F16_MMA != 0;
+// Weight of an FP16-tier item in the stream-K schedule, in middle tiles.
+#ifndef FADE_F16_ITEM_WEIGHT
+#define FADE_F16_ITEM_WEIGHT 3
+#endif
 template <int D, int G, bool PQ = false>
 struct MmaShape {
   static constexpr int CONS = (FADE_MMA_WIDE && G <= 4) ? 8 : 4;
@@ -833,7 +843,141 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
 #pragma unroll
           for (int e = 0; e < 4; ++e) o[s][mm][j][e] = 0.f;
 
-    if (split == 0) {
+    if (split == 0 && kF16Mma && f16_staged) {
+      // ---------------------------------------------------------- FP16 tiers (tensor cores)
+      // the item's two stages hold the K rows and the V rows: sinks (rows 0..S-1) then the
+      // ring slots (rows S..S+W-1), fp16. Warp w takes the 16-row M-tiles w, w + kConsumers,
+      // ...: QK^T with the K rows as A operand (ldmatrix) and the queries as B (column n =
+      // head n), softmax per head column, PV with V^T as A (ldmatrix.trans) and the
+      // probabilities as B (movmatrix). Rows that hold no token (unfilled sinks, empty ring
+      // slots, padding past the staged rows) get logit -inf; V past the staged rows is zeroed.
+      const int n_sink = ok ? inf[kInfoSink] : 0, n_rec = ok ? inf[kInfoRec] : 0;
+      const int head_slot = ok ? inf[kInfoHead] : 0;
+      const uint32_t st_k = sbase + s_ * Cfg::STAGE;
+      const int s_v = (used + 1) % NSTAGE;
+      const bool ok_v = ok && !*abort &&
+                        mbar_wait_or_abort(bar_full + 8 * s_v, ((used + 1) / NSTAGE) & 1,
+                                           a.status, 1, abort);
+      const uint32_t st_v = sbase + s_v * Cfg::STAGE;
+      const int R = a.S + a.W;
+      const int nmt = (ok && ok_v) ? (R + 15) / 16 : 0;
+      uint32_t qf[D / 16][2];  // B operand: (channels 16kk + 2t, +1 | +8, +9) of head g
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const bool hv = ok && g < G;
+        const uint32_t qa = st_k + Cfg::Q_OFF + (g * D + 16 * kk + 2 * t) * 2;
+        qf[kk][0] = hv ? lds32(qa) : 0u;
+        qf[kk][1] = hv ? lds32(qa + 16) : 0u;
+      }
+      float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
+      float of[NHALF][4][4];
+#pragma unroll
+      for (int s = 0; s < NHALF; ++s)
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) of[s][mm][e] = 0.f;
+      for (int mt = warp; mt < nmt; mt += kConsumers) {
+        const int r0 = mt * 16;
+        float cacc[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t k_ld =
+            st_k + (r0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * D * 2 + 8 * (lane >> 4) * 2;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(k_ld + 32 * kk, a0, a1, a2, a3);
+          mma16816(cacc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+        }
+        // logits of rows r0 + g + 8e for the head columns 2t + cc
+        float sc[2][2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int r = r0 + g + 8 * e;
+          const bool tv = r < a.S ? r < n_sink
+                                  : (r < R && (r - a.S - head_slot + a.W) % a.W < n_rec);
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int h = 2 * t + cc;
+            const bool v = tv && h < G;
+            if (want_logits && v)
+              a.logits[(size_t)(b * a.Hq + hq0 + h) * a.NS + (r < a.S ? r : a.C + r)] =
+                  cacc[2 * e + cc] * a.inv_sqrt_d;
+            sc[e][cc] = v ? cacc[2 * e + cc] * c2 : -INFINITY;
+          }
+        }
+        float al[2];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          float mx = fmaxf(sc[0][cc], sc[1][cc]);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float mn = fmaxf(mrun[cc], mx);
+          const float mref = mn == -INFINITY ? 0.f : mn;  // no valid token yet: all terms 0
+          al[cc] = ex2(mrun[cc] - mref);
+          mrun[cc] = mn;
+          sc[0][cc] = ex2(sc[0][cc] - mref);
+          sc[1][cc] = ex2(sc[1][cc] - mref);
+          lrun[cc] = lrun[cc] * al[cc] + sc[0][cc] + sc[1][cc];
+        }
+#pragma unroll
+        for (int s = 0; s < NHALF; ++s)
+#pragma unroll
+          for (int mm = 0; mm < 4; ++mm) {
+            of[s][mm][0] *= al[0];
+            of[s][mm][1] *= al[1];
+            of[s][mm][2] *= al[0];
+            of[s][mm][3] *= al[1];
+          }
+        const uint32_t pb0 = movm_t(h2_as_u32(__floats2half2_rn(sc[0][0], sc[0][1])));
+        const uint32_t pb1 = movm_t(h2_as_u32(__floats2half2_rn(sc[1][0], sc[1][1])));
+        // V^T halves of tokens past the staged rows are zeroed (the stage may hold anything
+        // there); masks for tokens (2t, 2t+1) and (2t+8, 2t+9) of the M-tile
+        const int tk = r0 + 2 * t;
+        const uint32_t mlo = (tk < R ? 0xFFFFu : 0u) | (tk + 1 < R ? 0xFFFF0000u : 0u);
+        const uint32_t mhi = (tk + 8 < R ? 0xFFFFu : 0u) | (tk + 9 < R ? 0xFFFF0000u : 0u);
+        const uint32_t v_ld =
+            st_v + (r0 + (lane & 7) + 8 * (lane >> 4)) * D * 2 + ((lane >> 3) & 1) * 16;
+#pragma unroll
+        for (int s = 0; s < NHALF; ++s)
+#pragma unroll
+          for (int mm = 0; mm < 4; ++mm) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(v_ld + (64 * s + 16 * mm) * 2, a0, a1, a2, a3);
+            mma16816(of[s][mm], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, pb0, pb1);
+          }
+      }
+      __syncwarp();
+      if (lane == 0) {  // both stages of the item are read: release them
+        if (ok) mbar_arrive(bar_empty + 8 * s_);
+        if (ok_v) mbar_arrive(bar_empty + 8 * s_v);
+      }
+      used += 2;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {  // the head columns' mass over the warp's rows
+        lrun[cc] += __shfl_xor_sync(0xffffffffu, lrun[cc], 4);
+        lrun[cc] += __shfl_xor_sync(0xffffffffu, lrun[cc], 8);
+        lrun[cc] += __shfl_xor_sync(0xffffffffu, lrun[cc], 16);
+      }
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int h = 2 * t + cc;
+        if (h < G) {
+          if (g == 0) {
+            wm[warp * 8 + h] = mrun[cc];
+            wl[warp * 8 + h] = lrun[cc];
+          }
+#pragma unroll
+          for (int s = 0; s < NHALF; ++s)
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) {
+              const int c = 64 * s + 16 * mm + g;
+              wo[(warp * G + h) * WR + c] = of[s][mm][cc];
+              wo[(warp * G + h) * WR + c + 8] = of[s][mm][2 + cc];
+            }
+        }
+      }
+    } else if (split == 0) {
       // ---------------------------------------------------------- FP16 tiers (CUDA cores)
       // warp w takes tokens w, w + kConsumers, ...; lane l holds channels l*CPL .. +CPL-1
       constexpr int CPL = D / 32;
@@ -1148,8 +1292,8 @@ void build_stream_k(const fade_config_t* c, const fade_layer_t* L, int ctas, Str
     T += (long long)k->H * ((L->h_n_mid[b] + kTileTok - 1) / kTileTok);
   }
   for (int b = c->batch; b <= FADE_MAX_BATCH; ++b) k->row_start[b] = (int)T;
-  // an FP16-tier item (sinks + recent window on the CUDA cores) costs about kFp16Weight tiles
-  constexpr long long kFp16Weight = 3;
+  // an FP16-tier item (sinks + recent window) costs about kFp16Weight middle tiles
+  constexpr long long kFp16Weight = FADE_F16_ITEM_WEIGHT;
   const long long F = (long long)c->batch * c->num_kv_heads, P = ctas;
   const long long Wtot = T + kFp16Weight * F;
   long long f16_before = 0, prev = 0;
