@@ -277,3 +277,23 @@ def test_prefill_mass_matches_oracle(T, key, P):
             ok, err, nbad = allclose_report(got[b, h, :n], ref, atol=1e-5, rtol=1e-4)
             assert ok, f"row {b} head {h}: max err {err}, {nbad} bad"
             assert np.all(got[b, h, n:] == 0.0)
+
+
+@pytest.mark.parametrize("key,kv", [(3, (4, 2)), (4, (4, 2)), (2, (4, 4))])
+def test_max_batch_ragged_lockstep(T, key, kv):
+    """The largest batch the ABI admits (256 rows), ragged prompt lengths: every per-row
+    schedule (stream-K row starts, selection grids, split partials) at its bound."""
+    from tiered_mixed_precision_gb300.fade import MAX_BATCH
+
+    kb, vb = kv
+    over = dict(layers=1, batch=MAX_BATCH, num_q_heads=4, num_kv_heads=1, ragged=(90, 160),
+                prompt_len=160, steps=3, middle_k_bits=kb, middle_v_bits=vb)
+    if key != 2:
+        over["int4_budget"] = 40
+    wl = get_workload(key).scaled(**over)
+    ls = Lockstep(wl)
+    ls.prefill(0)
+    ls.check_layer_state(0)
+    for _ in range(ls.steps):
+        ls.step()
+    assert ls.near_ties <= 2
