@@ -297,3 +297,21 @@ def test_max_batch_ragged_lockstep(T, key, kv):
     for _ in range(ls.steps):
         ls.step()
     assert ls.near_ties <= 2
+
+
+@pytest.mark.parametrize("d,window,policy", [(64, 100, "h2o"), (128, 96, "position"),
+                                             (128, 140, "ema")])
+def test_wide_fp16_tiers_lockstep(T, d, window, policy):
+    """Sink + recent windows around and past what one ring stage of the tensor-core kernel
+    holds (about 100 rows): the FP16 tiers then go through the stage (tensor cores) or are
+    read from global memory (CUDA cores); both against the oracle."""
+    base = {"h2o": 3, "position": 4, "ema": 5}[policy]
+    wl = get_workload(base).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                   head_dim=d, n_sink=8, recent_window=window, ragged=None,
+                                   prompt_len=window + 400, int4_budget=200, steps=4)
+    ls = Lockstep(wl)
+    ls.prefill(0)
+    ls.check_layer_state(0)
+    for _ in range(ls.steps):
+        ls.step()
+    assert ls.near_ties <= 1
