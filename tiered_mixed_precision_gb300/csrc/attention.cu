@@ -370,53 +370,59 @@ __global__ void __launch_bounds__(1024) attn_combine_sk_kernel(AttnArgs a,
                                                                float* __restrict__ ml,
                                                                const __grid_constant__ StreamK sk) {
   constexpr int kMaxSeg = kMaxCtaSK + 1;
+  constexpr int kPre = 8;            // partials a thread loads before the weights are known
   __shared__ float s_w[8][kMaxSeg];  // m_s, then the weight e^(m_s - M)
   __shared__ float s_l[8][kMaxSeg];
   __shared__ float s_L[8];
-  __shared__ int s_ns;
   const int unit = blockIdx.x;
   const int b = unit / a.H, hk = unit % a.H;
   const int G = a.Hq / a.H;
-  const int tid = threadIdx.x, nthr = blockDim.x;
-  if (tid == 0) s_ns = min(a.nsplit, min(kMaxSeg, 1 + sk_segments(sk, b, hk)));
-  __syncthreads();
-  const int ns = s_ns;
+  const int tid = threadIdx.x;
   const size_t bh0 = (size_t)b * a.Hq + hk * G;
-  for (int i = tid; i < G * ns; i += nthr) {
-    const int h = i / ns, sg = i % ns;
-    const float* pm = a.part_ml + ((bh0 + h) * a.nsplit + sg) * 2;
-    s_w[h][sg] = pm[0];
-    s_l[h][sg] = pm[1];
-  }
-  __syncthreads();
+  // this thread's channel of its head: the first partials are loaded at once, so that their
+  // latency overlaps the (m, l) loads and the weights below (slots below nsplit are in
+  // bounds; only the unit's first ns are used)
+  const int h = tid / D, c = tid % D;
+  const float* pa = a.part_acc + (bh0 + h) * a.nsplit * D + c;
+  float pre[kPre];
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) pre[i] = i < a.nsplit ? pa[(size_t)i * D] : 0.f;
+  const int ns = min(a.nsplit, min(kMaxSeg, 1 + sk_segments(sk, b, hk)));
   const int warp = tid >> 5, lane = tid & 31;
-  if (warp < G) {
-    const int h = warp;
+  if (warp < G) {  // warp hh: head hh's max over the segments, their weights and total mass
+    const int hh = warp;
+    const float* pm = a.part_ml + (bh0 + hh) * a.nsplit * 2;
     float M = -INFINITY;
-    for (int sg = lane; sg < ns; sg += 32) M = fmaxf(M, s_w[h][sg]);
+    for (int sg = lane; sg < ns; sg += 32) {
+      const float m = pm[2 * sg];
+      s_w[hh][sg] = m;
+      s_l[hh][sg] = pm[2 * sg + 1];
+      M = fmaxf(M, m);
+    }
 #pragma unroll
     for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float Lp = 0.f;
-    for (int sg = lane; sg < ns; sg += 32) {
-      const float m = s_w[h][sg];
+    for (int sg = lane; sg < ns; sg += 32) {  // entries this lane wrote itself
+      const float m = s_w[hh][sg];
       const float w = (m == -INFINITY) ? 0.f : __expf(m - M);
-      s_w[h][sg] = w;
-      Lp = fmaf(s_l[h][sg], w, Lp);
+      s_w[hh][sg] = w;
+      Lp = fmaf(s_l[hh][sg], w, Lp);
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) Lp += __shfl_xor_sync(0xffffffffu, Lp, o);
     if (lane == 0) {
-      s_L[h] = Lp;
-      ml[2 * (bh0 + h)] = M;
-      ml[2 * (bh0 + h) + 1] = Lp;
+      s_L[hh] = Lp;
+      ml[2 * (bh0 + hh)] = M;
+      ml[2 * (bh0 + hh) + 1] = Lp;
     }
   }
   __syncthreads();
-  const int h = tid / D, c = tid % D;
-  const float* pa = a.part_acc + (bh0 + h) * a.nsplit * D + c;
   float o = 0.f;
+#pragma unroll
+  for (int i = 0; i < kPre; ++i)
+    if (i < ns) o = fmaf(pre[i], s_w[h][i], o);
 #pragma unroll 4
-  for (int sg = 0; sg < ns; ++sg) o = fmaf(pa[(size_t)sg * D], s_w[h][sg], o);
+  for (int sg = kPre; sg < ns; ++sg) o = fmaf(pa[(size_t)sg * D], s_w[h][sg], o);
   out[(bh0 + h) * D + c] = f2h(o / s_L[h]);
 }
 
