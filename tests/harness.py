@@ -139,6 +139,8 @@ class Lockstep:
                 F.fade_cache_demote(self.fc.layers[layer])
                 self.fc.attend_layer(layer, q, k, v, out)
             victims_gpu = self._gpu_victims(layer)
+            if evict and wl.policy in ("h2o", "ema"):
+                self._replay_selection(layer, victims_gpu)
             out_h = out.float().cpu().numpy()
             shared_vic = {}
             if self.shared and evict:
@@ -160,6 +162,46 @@ class Lockstep:
                 self.check_layer_state(layer)
         self.step_index += 1
         return worst
+
+    def _replay_selection(self, layer, bm):
+        """Selection replay: the selection rule (smallest key, lower index first on ties; the
+        oracle's) applied to the very fp32 keys the GPU compared must give the GPU's victims
+        bit for bit. The keys are the middle scores in the buffer the step compacted from
+        (eviction writes the survivors to the other buffer); rows sharing their decisions
+        compare the fp32 sum over the rows in ascending row order."""
+        from oracle import policy as pol
+
+        L = self.fc.layers[layer]
+        meta = L.meta.cpu().numpy()
+        wl = self.wl
+        for h in range(wl.num_kv_heads):
+            rows = []
+            for b in range(wl.batch):
+                u = self.units[layer][b][h]   # oracle state before this step
+                n_mid = u.n_mid + (1 if u._ring_full() else 0)
+                k = n_mid - u.p.int4_budget if u.p.evicts else 0
+                if k <= 0:
+                    continue
+                prev = 1 - int(meta[b, h, 4])   # the buffer the selection read
+                keys = L.mid_scores[prev][b, h, :n_mid].cpu().numpy().astype(np.float32)
+                words = bm[b, h, :(n_mid + 31) // 32]
+                gpu = np.nonzero(np.unpackbits(words.view(np.uint8), bitorder="little")[:n_mid])[0]
+                rows.append((b, keys, k, gpu))
+            if not rows:
+                continue
+            if self.shared:
+                total = rows[0][1].copy()
+                for _, keys, _, _ in rows[1:]:
+                    total = (total + keys).astype(np.float32)
+                want = np.sort(pol.select_victims(total.astype(np.float64), rows[0][2]))
+                for b, _, _, gpu in rows:
+                    assert np.array_equal(gpu, want), f"shared selection replay at {layer, b, h}"
+            else:
+                for b, keys, k, gpu in rows:
+                    want = np.sort(pol.select_victims(keys.astype(np.float64), k))
+                    assert np.array_equal(gpu, want), (
+                        f"selection replay differs at layer {layer} row {b} head {h}: "
+                        f"gpu {gpu}, rule on the gpu keys {want}")
 
     def _gpu_victims(self, layer):
         """Victim middle indices chosen by the CUDA path in this step (per unit), read from
