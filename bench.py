@@ -238,8 +238,8 @@ from synth import draw_vectors, get_workload
 wl = get_workload({key!r})
 P = int({P})
 u = UnitCache(Params.from_workload(wl), RopeTable.from_workload(wl, P + 4096))
-k = draw_vectors(wl, "k", (P, wl.head_dim), "cpu_sample")
-v = draw_vectors(wl, "v", (P, wl.head_dim), "cpu_sample")
+k = draw_vectors(wl, "k", (P, wl.head_dim), "cpu_sample", {worker})
+v = draw_vectors(wl, "v", (P, wl.head_dim), "cpu_sample", {worker})
 u.prefill(k, v, mass=np.ones(P) if wl.policy == "h2o" else None)
 steps, warm, budget_s = {steps}, {warmup}, {budget_s}
 G = wl.group
@@ -247,9 +247,9 @@ times = []
 i = 0
 t_start = time.perf_counter()
 while True:
-    q = draw_vectors(wl, "q", (G, wl.head_dim), "cpu_step", i)
-    kk = draw_vectors(wl, "k", (wl.head_dim,), "cpu_step", i)
-    vv = draw_vectors(wl, "v", (wl.head_dim,), "cpu_step", i)
+    q = draw_vectors(wl, "q", (G, wl.head_dim), "cpu_step", {worker}, i)
+    kk = draw_vectors(wl, "k", (wl.head_dim,), "cpu_step", {worker}, i)
+    vv = draw_vectors(wl, "v", (wl.head_dim,), "cpu_step", {worker}, i)
     t0 = time.perf_counter()
     u.step(q, kk, vv)
     dt = time.perf_counter() - t0
@@ -262,23 +262,38 @@ print(json.dumps({{"unit_step_s": float(np.mean(times)), "n": len(times)}}))
 """
 
 
-def run_oracle_sample(key, steps, warmup, budget_s=25.0):
+def run_oracle_sample(key, steps, warmup, budget_s=25.0, workers=None):
+    """The oracle's decode step on the host cores: one single-threaded process per core, each
+    stepping its own full-size (layer, row, KV head) unit (units are independent), all at
+    once; the mean per-unit step time under that load, times the units of a whole step and
+    divided by the processes, gives the whole-step time."""
     wl = workload(key)
     P = wl.ragged[1] if wl.ragged else wl.prompt_len
+    if workers is None:
+        workers = max(1, int(os.environ.get("FADE_CPU_WORKERS", os.cpu_count() or 1)))
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    code = _CPU_SNIPPET.format(root=ROOT, key=key if not key.isdigit() else int(key), P=P,
-                               steps=steps, warmup=warmup, budget_s=budget_s)
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
-                       timeout=900)
-    if r.returncode != 0:
-        raise RuntimeError("oracle sample failed: " + r.stderr[-2000:])
-    res = json.loads(r.stdout.strip().splitlines()[-1])
+    procs = []
+    for w in range(workers):
+        code = _CPU_SNIPPET.format(root=ROOT, key=key if not key.isdigit() else int(key), P=P,
+                                   steps=steps, warmup=warmup, budget_s=budget_s, worker=w)
+        procs.append(subprocess.Popen([sys.executable, "-c", code], stdout=subprocess.PIPE,
+                                      stderr=subprocess.PIPE, text=True, env=env))
+    res = []
+    for pr in procs:
+        out, err = pr.communicate(timeout=900)
+        if pr.returncode != 0:
+            raise RuntimeError("oracle sample failed: " + err[-2000:])
+        res.append(json.loads(out.strip().splitlines()[-1]))
+    unit_step_s = float(np.mean([r["unit_step_s"] for r in res]))
+    n = min(r["n"] for r in res)
     units = wl.layers * wl.batch * wl.num_kv_heads
-    step_s = res["unit_step_s"] * units
+    step_s = unit_step_s * units / workers
     return {
-        "value": wl.batch / step_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-        "sample": (f"{res['n']} decode steps of one full-size (layer, row, KV head) unit "
-                   f"(prompt {P}); time x {units} units = one whole step"),
+        "value": wl.batch / step_s, "unit": "tokens/s", "cores": workers, "kind": "oracle",
+        "sample": (f"{n} decode steps of one full-size (layer, row, KV head) unit (prompt {P}) "
+                   f"in each of {workers} single-threaded processes running at once (one per "
+                   f"host core); mean unit-step time x {units} units / {workers} = one whole "
+                   f"step"),
         "ms_per_step": step_s * 1e3,
     }
 
@@ -303,7 +318,8 @@ def run_ours(args, rank, world):
     lens = ragged_context_lengths(wl)
     maxP = int(lens.max())
     K, W = args.steps, args.warmup
-    nsteps = 3 * K + W + 8   # timed, e2e, a possible eager timing pass, probe and warm-up
+    # timed, per-step spread, e2e, a possible eager timing pass, probe and warm-up
+    nsteps = 4 * K + W + 8
     if wl.policy != "none" and wl.int4_budget >= 0:
         cfg = Config.from_workload(wl)
     else:  # without eviction the middle tier grows by one token per step
@@ -411,6 +427,28 @@ def run_ours(args, rank, world):
     clk = clocks.stop()
     progress(f"{K} timed steps done")
     launches = launches_per_step * K if graph is not None else fc.launches
+    # spread of the step time: K more steps, each between its own events (outside the
+    # timed region, in the same launch mode)
+    fc.timers, saved_timers = None, fc.timers
+    spread = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+    for i, (sa, sb) in enumerate(spread):
+        s = W + i
+        sa.record()
+        if graph is not None:
+            qb.copy_(q_all[s], non_blocking=True)
+            kb.copy_(k_all[s], non_blocking=True)
+            vb.copy_(v_all[s], non_blocking=True)
+            fc.replay_growing(graph) if growing else graph.replay()
+        else:
+            step(s)
+        sb.record()
+    torch.cuda.synchronize()
+    fc.timers = saved_timers
+    per_step = sorted(sa.elapsed_time(sb) for sa, sb in spread)
+    per_step_ms = {"median": float(np.median(per_step)),
+                   "p90": float(np.percentile(per_step, 90)), "n": K,
+                   "note": "per-step events after the timed region"}
     ms = e0.elapsed_time(e1)
     ms_max = max_over_ranks(ms, world)
     # per-call durations: the events of the last replay (graph) or of every timed step
@@ -554,6 +592,7 @@ def run_ours(args, rank, world):
                              (f"; each layer's maintenance overlaps the next layers "
                               f"({len(side)} side streams taken in turn)" if pipelined else ""),
                    "per_call_timing": timing_note},
+        "per_step_ms": per_step_ms,
         "roofline": dict(rl[dominant], kernel=dominant) if dominant else None,
         "roofline_by_call": rl,
         # decode-attention calls alone: B tokens per step over L attention launches
