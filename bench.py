@@ -154,6 +154,14 @@ def attention_bytes(cfg, layer):
     return units_mid * mid_tok + units_fp16 * 4 * d + 2 * cfg.batch * cfg.num_q_heads * d * 2
 
 
+def accumulate_bytes(cfg, layer):
+    """Algorithmic bytes of one fade_h2o_accumulate call: each held token's G logits read and
+    its score read and written, plus the (M, L) of every query head."""
+    held = int((layer.h_n_sink + layer.h_n_mid + layer.h_n_recent).sum()) * cfg.num_kv_heads
+    G = cfg.num_q_heads // cfg.num_kv_heads
+    return held * (4 * G + 8) + cfg.batch * cfg.num_q_heads * 8
+
+
 def evict_bytes(cfg, layer, n_ev=1):
     """Algorithmic bytes of one steady-state fade_evict_rerope call: the middle tier (codes,
     scales, scores) read once and its survivors written once to the other buffer, plus the
@@ -365,14 +373,15 @@ def run_ours(args, rank, world):
     progress(f"{W} warm-up steps done")
 
     # Steady state (a step leaves every tier count unchanged): the whole step is captured
-    # once as a CUDA graph, with per-call timing events as graph nodes, and replayed on fixed
-    # input buffers (each step's inputs are copied in first, inside the timed region).
+    # once as a CUDA graph (without timing nodes: per-call times come from separately
+    # captured graphs after the timed region) and replayed on fixed input buffers (each
+    # step's inputs are copied in first, inside the timed region).
     before = fc.mirror()
     step(W - 1 if W > 0 else 0)
     steady = all((x == y).all() for a, b in zip(before, fc.mirror()) for x, y in zip(a, b))
     graph = None
     qb, kb, vb = q_all[0].clone(), k_all[0].clone(), v_all[0].clone()
-    fc.timers = {}
+    fc.timers = None
     fc.launches = 0
     pipelined = steady and not args.no_graph and not args.no_pipeline
     n_side = args.side_streams
@@ -451,15 +460,21 @@ def run_ours(args, rank, world):
                    "note": "per-step events after the timed region"}
     ms = e0.elapsed_time(e1)
     ms_max = max_over_ranks(ms, world)
-    # per-call durations: the events of the last replay (graph) or of every timed step
-    timing_note = "events inside the timed region"
+    # per-call durations: from graphs of the same step captured with timing events as nodes,
+    # replayed after the timed region (or from eager steps)
+    timing_note = "events of an instrumented replay after the timed region"
     per_call_overlapped = None
     ms_iso = None
     try:
         if graph is None or growing:  # per-call events come from extra eager steps below
             raise RuntimeError("eager launches" if graph is None else "growing-cache graph")
+        fc.timers = {}
+        inst = fc.capture_step(qb, kb, vb, out, side)   # same schedule, with timing nodes
+        inst.replay()
+        torch.cuda.synchronize()
         per_call = {name: [a.elapsed_time(b) for a, b in pairs]
                     for name, pairs in fc.timers.items()}
+        del inst
         if pipelined:
             # Overlapped calls share the GPU, so their events do not give a kernel's own
             # duration: replay the same step order with the maintenance inline (no overlap)
@@ -513,6 +528,18 @@ def run_ours(args, rank, world):
                            "bytes_per_launch": attn_b, "ms_per_launch": t * 1e3,
                            "peak_source": peak_src,
                            "time_share": float(np.mean(per_call["attention"])) * L / step_ms_for_share}
+    if "attention" in rl and fc.needs_logits:   # H2O / EMA: the call also writes its logits
+        held = int((lay0.h_n_sink + lay0.h_n_mid + lay0.h_n_recent).sum()) * Hkv
+        rl["attention"]["logits_written_bytes"] = held * 4 * (Hq // Hkv)
+    if "accumulate" in per_call:   # H2O / EMA: the score update reads the step's logits
+        ab = accumulate_bytes(cfg, lay0)
+        t = float(np.mean(per_call["accumulate"])) / 1e3
+        rl["accumulate"] = {"bound": "hbm", "achieved": ab / t / 1e9, "peak": peak,
+                            "unit": "GB/s", "frac": ab / t / 1e9 / peak, "traffic": None,
+                            "bytes_per_launch": ab, "ms_per_launch": t * 1e3,
+                            "peak_source": peak_src,
+                            "time_share": float(np.mean(per_call["accumulate"])) * L /
+                            step_ms_for_share}
     if "evict" in per_call:
         eb = evict_bytes(cfg, lay0)
         t = float(np.mean(per_call["evict"])) / 1e3

@@ -209,7 +209,9 @@ class FadeCache:
         self._tock(t)
         n += 3
         if self.needs_logits:
+            t = self._tick("accumulate")
             F.fade_h2o_accumulate(L, self.logits, self.ml)
+            self._tock(t)
             n += 1
         self.launches += n
 
