@@ -55,3 +55,31 @@ def test_reference_arm_prints_the_contract_line():
         assert key in line
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_bench_byte_accounting_follows_the_oracle():
+    """The bench's algorithmic bytes per middle token (INT and PQ V) and per accumulate call
+    agree with the oracle's accounting and the definition of the score update."""
+    import numpy as np
+
+    sys.path.insert(0, ROOT)
+    import bench
+    from oracle import accounting
+    import tiered_mixed_precision_gb300 as T
+
+    for d, kb, vb, codec in [(128, 4, 2, "int"), (64, 4, 4, "int"), (128, 2, 2, "int"),
+                             (128, 4, 2, "pq")]:
+        cfg = T.Config(batch=2, num_q_heads=8, num_kv_heads=2, head_dim=d, middle_k_bits=kb,
+                       middle_v_bits=vb, mid_capacity=64, v_codec=codec)
+        assert bench.mid_token_bytes(cfg) == accounting.middle_token_bytes(d, kb, vb,
+                                                                           v_codec=codec)
+
+    class _L:  # host mirrors only
+        h_n_sink = np.array([4, 4], np.int32)
+        h_n_mid = np.array([100, 50], np.int32)
+        h_n_recent = np.array([64, 10], np.int32)
+
+    cfg = T.Config(batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128, mid_capacity=128)
+    held = (4 + 100 + 64 + 4 + 50 + 10) * 2          # token-heads held
+    # G = 4 logits read, a score read and written, per held token; (M, L) per query head
+    assert bench.accumulate_bytes(cfg, _L) == held * (4 * 4 + 8) + 2 * 8 * 8
