@@ -428,7 +428,10 @@ def run_ours(args, rank, world):
             qb.copy_(q_all[s], non_blocking=True)
             kb.copy_(k_all[s], non_blocking=True)
             vb.copy_(v_all[s], non_blocking=True)
-            fc.replay_growing(graph) if growing else graph.replay()
+            if growing:
+                fc.replay_growing(graph)
+            else:
+                graph.replay()
         else:
             step(s)
     e1.record()
@@ -448,7 +451,10 @@ def run_ours(args, rank, world):
             qb.copy_(q_all[s], non_blocking=True)
             kb.copy_(k_all[s], non_blocking=True)
             vb.copy_(v_all[s], non_blocking=True)
-            fc.replay_growing(graph) if growing else graph.replay()
+            if growing:
+                fc.replay_growing(graph)
+            else:
+                graph.replay()
         else:
             step(s)
         sb.record()
@@ -581,7 +587,10 @@ def run_ours(args, rank, world):
                 qb.copy_(qh[s], non_blocking=True)
                 kb.copy_(kh[s], non_blocking=True)
                 vb.copy_(vh[s], non_blocking=True)
-                fc.replay_growing(graph) if growing else graph.replay()
+                if growing:
+                    fc.replay_growing(graph)
+                else:
+                    graph.replay()
             else:
                 qd.copy_(qh[s], non_blocking=True)
                 kd.copy_(kh[s], non_blocking=True)

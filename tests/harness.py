@@ -173,6 +173,7 @@ class Lockstep:
 
         L = self.fc.layers[layer]
         meta = L.meta.cpu().numpy()
+        scores = [t.cpu().numpy() for t in L.mid_scores]   # both ping-pong buffers
         wl = self.wl
         for h in range(wl.num_kv_heads):
             rows = []
@@ -183,7 +184,7 @@ class Lockstep:
                 if k <= 0:
                     continue
                 prev = 1 - int(meta[b, h, 4])   # the buffer the selection read
-                keys = L.mid_scores[prev][b, h, :n_mid].cpu().numpy().astype(np.float32)
+                keys = scores[prev][b, h, :n_mid].astype(np.float32)
                 words = bm[b, h, :(n_mid + 31) // 32]
                 gpu = np.nonzero(np.unpackbits(words.view(np.uint8), bitorder="little")[:n_mid])[0]
                 rows.append((b, keys, k, gpu))
