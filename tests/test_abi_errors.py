@@ -129,6 +129,23 @@ def test_pq_argument_errors(T):
 
 
 def test_pq_layer_without_codebook_is_rejected(T):
+    """The C side refuses a PQ layer whose codebook pointer is NULL."""
+    import torch
+
     L = _layer(T, v_codec="pq")
+    L.set_pq_codebook(torch.ones_like(L.pq_codebook))
     L.c.pq_codebook = None
+    msg = _expect(T, 1, T.fade_cache_demote, L)
+    assert "codebook" in msg
+
+
+def test_pq_layer_refuses_to_encode_before_its_codebook_is_set(T):
+    import torch
+
+    L = _layer(T, v_codec="pq")
+    with pytest.raises(ValueError):
+        T.fade_cache_demote(L, stream=_S())
+    L.set_pq_codebook(torch.ones_like(L.pq_codebook))
+    assert L.pq_codebook_set
+    L.c.status = None   # now the C side runs its own checks (and refuses this layer)
     _expect(T, 1, T.fade_cache_demote, L)

@@ -283,6 +283,7 @@ class TieredLayer:
         self.h_n_recent = np.zeros(B, np.int32)
         # the layer's PQ codebook (product-quantised V only): fp16 [d/4][256][4]
         self.pq_codebook = z((d // PQ_SUB, PQ_CENTROIDS, PQ_SUB), f16) if cfg.v_codec == "pq" else None
+        self.pq_codebook_set = False   # PQ: encoding needs a codebook installed first
         p = lambda t: t.data_ptr()
         self.c = LayerT(
             p(self.sink_k), p(self.sink_v), p(self.recent_k), p(self.recent_v),
@@ -299,6 +300,7 @@ class TieredLayer:
         if self.pq_codebook is None:
             raise ValueError("the layer does not use product-quantised V")
         self.pq_codebook.copy_(codebook)
+        self.pq_codebook_set = True
 
     def workspaces(self):
         """(logits_ws, ml_ws, attn_ws) tensors sized by the layout."""
@@ -337,8 +339,15 @@ def fade_cache_reset(layer: TieredLayer, stream=None):
                                   _stream(stream)))
 
 
+def _require_codebook(layer: TieredLayer):
+    if layer.pq_codebook is not None and not layer.pq_codebook_set:
+        raise ValueError("product-quantised V: install the layer's codebook first "
+                         "(set_pq_codebook, or FadeCache.train_pq_codebook)")
+
+
 def fade_cache_prefill(layer: TieredLayer, k_rot, v, max_prompt, prompt_len, mass, table,
                        max_pos, stream=None):
+    _require_codebook(layer)
     lens = np.ascontiguousarray(prompt_len, np.int32)
     _check(lib().fade_cache_prefill(ctypes.byref(layer.cfg.c()), ctypes.byref(layer.c),
                                     _ptr(k_rot), _ptr(v), max_prompt, lens.ctypes.data,
@@ -352,6 +361,7 @@ def fade_prefill_mass(cfg: Config, q_rot, k_rot, max_prompt, prompt_len, mass, s
 
 
 def fade_cache_demote(layer: TieredLayer, stream=None):
+    _require_codebook(layer)
     _check(lib().fade_cache_demote(ctypes.byref(layer.cfg.c()), ctypes.byref(layer.c),
                                    _stream(stream)))
 
