@@ -12,9 +12,17 @@ H2O/EMA accumulation for the policies that use it). ``value`` = batch x steps x 
 (max over ranks of the device time of the timed steps). The compressed cache (8 GB) is far
 larger than L2, so no L2 flush is needed between steps.
 
+Besides the contract keys, the line carries: ``roofline_by_call`` (attention and eviction,
+and score accumulation under H2O / EMA, each against its bound, with the recorded DRAM
+traffic of the current sources), ``attention_only`` (decode-attention tokens/s),
+``per_step_ms`` (median and p90 of separately timed steps), ``per_call_overlapped_ms``, and
+``cpu_baseline``. Options: ``--workload`` (1, 2, 3, 4, 5, 5b), ``--v-codec pq`` (product-
+quantised middle V), ``--shared-rows`` (batch-shared tier decisions), ``--no-graph``,
+``--no-pipeline``, ``--side-streams``.
+
 --impl reference runs the oracle (plain numpy CPU restatement of the method) on the same
-workload: each step is one full-size (layer, row, KV head) unit's decode step, scaled to a
-whole step by the number of units.
+workload: one single-threaded process per host core, each stepping one full-size (layer,
+row, KV head) unit, the unit time scaled to a whole step by the number of units.
 """
 
 from __future__ import annotations
