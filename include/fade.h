@@ -312,8 +312,10 @@ fade_status_t fade_prefill_mass(const fade_config_t* cfg, const uint16_t* q_rot,
 
 /* Demote (FADE-zh §第二层: mid-aged tokens go to the quantised tier): in every unit whose
  * recent window is full, the oldest recent token is quantise-packed (K at middle_k_bits, V
- * at middle_v_bits) into the next middle slot of the live buffer and its score moves with
- * it; its cache index is unchanged. FADE_ERR_CAPACITY if a middle slot would overflow. */
+ * at middle_v_bits, or with FADE_V_PQ V encoded by the fade_pq_encode rule against
+ * layer->pq_codebook, its scale slots set to 0) into the next middle slot of the live buffer
+ * and its score moves with it; its cache index is unchanged. FADE_ERR_CAPACITY if a middle
+ * slot would overflow. fade_cache_prefill codes its middle tier the same way. */
 fade_status_t fade_cache_demote(const fade_config_t* cfg, fade_layer_t* layer, void* stream);
 
 /* Evict and re-position (FADE-zh §驱逐策略: on reaching INT4_BUDGET tokens are evicted and
@@ -339,8 +341,9 @@ fade_status_t fade_cache_append(const fade_config_t* cfg, fade_layer_t* layer,
 /* Decode attention (FADE-zh §项目结构与代码质量, kernels/: fused INT4 dequant + SDPA; KVLong
  * §1.2: softmax-weighted average of V). q_rot: fp16 [B][Hq][d] RoPE'd at the new token's
  * position; out: fp16 [B][Hq][d]. Every query head h attends, with scale 1/sqrt(d), to
- * every token held by its KV head h / (Hq/Hkv): sinks, middle (dequantised in registers)
- * and recent. Split-KV over SMs: partials go to `ws` (ws_bytes >= fade_layout().attn_ws),
+ * every token held by its KV head h / (Hq/Hkv): sinks, middle (dequantised in registers;
+ * with FADE_V_PQ the middle V is each sub-space's centroid from layer->pq_codebook) and
+ * recent. Split-KV over SMs: partials go to `ws` (ws_bytes >= fade_layout().attn_ws),
  * then a combine writes out and ml_ws = f32 [B][Hq][2] (max logit M, sum L of exp(s - M)).
  * If logits_ws is not NULL (f32 [B][Hq][S + C + W]) the scaled logits s are stored at the
  * token's storage slot: sink i at i, middle slot m at S + m, ring slot r at S + C + r. */
