@@ -33,7 +33,12 @@ oldest go first; position: the index); survivors are re-positioned in fp16 and t
 tier is quantised once. H2O starts from the survivors' mass, EMA from zero.
 Pinned through the pins of the pieces (quant, rope, attention, policy) plus: safe mode with
 every token in FP16 equals textbook attention, the position-policy kept set equals the
-StreamingLLM closed form, the H2O mass sum, and relative-position invariance after eviction.
+StreamingLLM closed form, the H2O mass sum, relative-position invariance after eviction, and
+the re-positioning of keys against exact fp64 rotations: every middle key moved by an
+eviction equals the rotation of its previous value by its index change within s/2 plus the
+fp16 and fp32 roundings, logits at unchanged distance agree within the bound that follows,
+and every key held after a prefill with evictions is its raw key rotated to its cache index
+(mutations of the index, the rotation or the re-quantisation fail these pins).
 """
 
 from __future__ import annotations
