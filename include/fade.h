@@ -29,7 +29,9 @@
  *   - fp16 data is passed as raw IEEE binary16 (uint16 bits). Row-major layouts throughout.
  *   - The host keeps a mirror of per-row tier counts in the fade_layer_t (h_* arrays); each
  *     call updates it as it enqueues work, so the caller never synchronises to learn sizes.
- *   - Kernels never trap or spin: all waits in the library are stream order.
+ *   - Kernels never trap and never spin without a limit: a wait inside a kernel (an
+ *     mbarrier of a bulk-copy pipeline) gives up after about 2 s, records a code in the
+ *     layer's status words and returns; fade_check_status reports it.
  */
 #ifndef FADE_H_
 #define FADE_H_
@@ -46,11 +48,10 @@ typedef enum {
   FADE_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad shape, out-of-range value */
   FADE_ERR_UNSUPPORTED = 2,      /* a valid configuration this build does not implement */
   FADE_ERR_CAPACITY = 3,         /* a tier or workspace would overflow its buffer */
-  FADE_ERR_CUDA = 4              /* a CUDA call or kernel launch failed */
+  FADE_ERR_CUDA = 4,             /* a CUDA call or kernel launch failed */
+  FADE_ERR_TIMEOUT = 5           /* a kernel gave up a bounded wait (fade_check_status) */
 } fade_status_t;
 
-/* RoPE schemes (FADE-zh §RoPE方案兼容性). NONE: positions are not encoded in K (ALiBi
- * models), so re-positioning is the identity. */
 /* RoPE schemes (FADE-zh §RoPE方案兼容性: standard RoPE and the scaling types llama3, linear,
  * ntk, yarn; ALiBi models make re-positioning a no-op: FADE_ROPE_NONE). Every scheme is a set
  * of inverse frequencies inv_i (rotate-half pairs i, i + d/2); base_i = base^(-2i/d):
@@ -174,7 +175,8 @@ typedef struct {
   int32_t chunk_slots;       /* from fade_layout_t */
   int32_t* status;           /* i32 [FADE_STATUS_WORDS]: device-side error status, 0 = ok;
                                 zeroed by fade_cache_reset; nonzero after a kernel gave up a
-                                bounded wait (the call's results are then invalid) */
+                                bounded wait (the call's results are then invalid); read by
+                                fade_check_status */
   int32_t* h_n_sink;         /* HOST i32 [B]: mirror of N_SINK (same for every head) */
   int32_t* h_n_mid;          /* HOST i32 [B]: mirror of N_MID */
   int32_t* h_n_recent;       /* HOST i32 [B]: mirror of N_RECENT */
@@ -195,6 +197,7 @@ typedef struct {
   int32_t chunk_slots;   /* i32 entries per unit in `chunk_base` */
   int32_t max_prompt;    /* the prompt length the scratch sizes were computed for */
   int32_t max_splits;    /* split-KV partial slots per (row, query head) */
+  size_t prefill_mass_ws; /* workspace of fade_prefill_mass for prompts of max_prompt */
 } fade_layout_t;
 
 /* Validate `cfg` and return the sizes of a layer's buffers for prompts of up to
@@ -304,11 +307,14 @@ fade_status_t fade_cache_prefill(const fade_config_t* cfg, fade_layer_t* layer,
  * RoPE'd at positions 0..P-1; h_prompt_len: HOST i32 [B]. Writes mass: f32
  * [B][H][max_prompt], mass[b][h][j] = sum over the query heads of KV head h and over the
  * queries i >= j of softmax_j(q_i . k_j / sqrt(d)) (causal), 0 past a row's length. fp32
- * arithmetic with atomic column sums (the last bits may differ between runs). The result is
- * the `mass` argument of fade_cache_prefill. */
+ * arithmetic in one fixed order (no atomics): the result is identical on every run. ws:
+ * device workspace of fade_layout_t.prefill_mass_ws bytes (B * Hq * max_prompt * 8: each
+ * query row's softmax max and sum), 8-byte aligned; FADE_ERR_CAPACITY if ws_bytes is
+ * smaller. The result is the `mass` argument of fade_cache_prefill. */
 fade_status_t fade_prefill_mass(const fade_config_t* cfg, const uint16_t* q_rot,
                                 const uint16_t* k_rot, int32_t max_prompt,
-                                const int32_t* h_prompt_len, float* mass, void* stream);
+                                const int32_t* h_prompt_len, float* mass, void* ws,
+                                size_t ws_bytes, void* stream);
 
 /* Demote (FADE-zh §第二层: mid-aged tokens go to the quantised tier): in every unit whose
  * recent window is full, the oldest recent token is quantise-packed (K at middle_k_bits, V
@@ -387,6 +393,24 @@ int32_t fade_next_position(const fade_config_t* cfg, const fade_layer_t* layer, 
  * storage only): FP16 tokens at 4d bytes, middle tokens at d*(kb+vb)/8 code bytes plus two
  * fp16 scales per 32 channels. */
 uint64_t fade_compressed_bytes(const fade_config_t* cfg, const fade_layer_t* layer);
+
+/* Host, synchronising: wait for the work queued on `stream`, then read the layer's device
+ * status words. FADE_ERR_TIMEOUT if a kernel of this layer gave up a bounded wait since the
+ * last fade_cache_reset (every wait on an mbarrier or a bulk copy is bounded, about 2 s; the
+ * kernel then records a code in status[0] and returns instead of hanging; the results of
+ * the calls since are invalid); FADE_ERR_CUDA if the stream reports an error; FADE_OK
+ * otherwise. The asynchronous calls never read the status words: this is the call that
+ * turns them into an error. */
+fade_status_t fade_check_status(const fade_layer_t* layer, void* stream);
+
+/* Self-test of the bounded waits: one kernel in which a consumer waits on an mbarrier with
+ * the same bounded wait the attention kernel uses, for at most `limit_cycles` SM clock cycles
+ * (1 .. the kernels' own limit of 4e9), while a producer warp arrives on it only if
+ * `producer_arrives` is nonzero. On a timeout the kernel writes code 1 into status[0]
+ * (device i32, unless status[0] is already nonzero) and returns. Lets a test make a wait run
+ * out without a fault or a hang and check that fade_check_status reports it. */
+fade_status_t fade_selftest_bounded_wait(int32_t* status, int32_t producer_arrives,
+                                         int64_t limit_cycles, void* stream);
 
 /* The calling thread's last error message ("" if none). */
 const char* fade_last_error(void);

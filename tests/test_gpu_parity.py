@@ -91,9 +91,20 @@ def test_rope_table_and_apply(T, key):
     yd = torch.empty_like(xd)
     T.fade_rope_apply(cfg, table, max_pos, xd, yd, 300, 1, torch.from_numpy(pos).cuda(), 0)
     want = ref.apply(x, pos)
-    same = yd.cpu().numpy().view(np.uint16) == want.view(np.uint16)
-    # identical tables give identical bytes; a 1-ulp table entry may move one fp16 rounding
-    assert same.mean() > 0.999
+    got16 = yd.cpu().numpy().view(np.uint16)
+    want16 = want.view(np.uint16)
+    # where the two tables' rows agree the rotation must give identical bytes; a row with a
+    # 1-ulp table entry may move an fp16 rounding by at most one ulp
+    rows_agree = (np.all(cos[pos] == ref.cos[pos], axis=1)
+                  & np.all(sin[pos] == ref.sin[pos], axis=1))
+    assert rows_agree.mean() > 0.9
+    assert np.array_equal(got16[rows_agree], want16[rows_agree])
+
+    def ordered(u):  # fp16 bits -> integers in float order
+        u = u.astype(np.int32)
+        return np.where(u & 0x8000, -(u & 0x7FFF), u)
+
+    assert np.abs(ordered(got16) - ordered(want16)).max() <= 1
 
 
 def _small(key):
@@ -204,7 +215,7 @@ def test_lockstep_small_workloads(T, key):
         ls.check_layer_state(layer)
     for _ in range(ls.steps):
         ls.step()
-    assert ls.near_ties <= max(1, wl.batch * wl.num_kv_heads * ls.L // 20)
+    ls.check_near_ties()
 
 
 @pytest.mark.parametrize("policy,skip", [("position", 40), ("h2o", 40), ("position", 3)])
@@ -225,7 +236,7 @@ def test_deferred_eviction_many_victims(T, policy, skip):
         ls.step(evict=False)
     for _ in range(2):
         ls.step()
-    assert ls.near_ties <= 1
+    ls.check_near_ties()
 
 
 @pytest.mark.parametrize("policy", ["h2o", "ema", "position"])
@@ -240,12 +251,13 @@ def test_shared_row_decisions_lockstep(T, policy):
     ls.check_layer_state(0)
     for _ in range(ls.steps):
         ls.step()
-    assert ls.near_ties <= 1
+    ls.check_near_ties()
 
 
-@pytest.mark.parametrize("key,P", [(3, 700), (3, 130)])
+@pytest.mark.parametrize("key,P", [(3, 700), (3, 130), (4, 300)])
 def test_prefill_mass_matches_oracle(T, key, P):
-    """GPU prefill attention mass vs the oracle's fp64 causal column sums."""
+    """GPU prefill attention mass vs the oracle's fp64 causal column sums (d = 64 and 128),
+    and the same bits on a second run."""
     import torch
 
     from oracle import attention
@@ -267,6 +279,9 @@ def test_prefill_mass_matches_oracle(T, key, P):
     mass = torch.full((B, Hkv, P), 7.0, dtype=torch.float32, device="cuda")
     T.fade_prefill_mass(cfg, qd, kd, P, lens, mass)
     got = mass.cpu().numpy()
+    again = torch.full((B, Hkv, P), -1.0, dtype=torch.float32, device="cuda")
+    T.fade_prefill_mass(cfg, qd, kd, P, lens, again)
+    assert np.array_equal(again.cpu().numpy().view(np.uint32), got.view(np.uint32))
     G = wl.group
     for b in range(B):
         n = int(lens[b])
@@ -277,6 +292,24 @@ def test_prefill_mass_matches_oracle(T, key, P):
             ok, err, nbad = allclose_report(got[b, h, :n], ref, atol=1e-5, rtol=1e-4)
             assert ok, f"row {b} head {h}: max err {err}, {nbad} bad"
             assert np.all(got[b, h, n:] == 0.0)
+
+
+@pytest.mark.parametrize("key", ["3s", "g1_h2o_d128", "d64_g8"])
+def test_gpu_prefill_mass_lockstep(T, key):
+    """The product path of an H2O cache: the GPU computes the prefill mass and its prefill
+    evicts by it. The mass must be deterministic and within tolerance of the oracle's, the
+    selection rule replayed on the GPU's mass must give the GPU's victims (the prefilled state
+    is compared bit for bit), and the decode steps that follow stay in lockstep."""
+    wl, cap = _small(key)
+    ls = Lockstep(wl, mid_capacity=cap)
+    for layer in range(ls.L):
+        ls.prefill(layer, gpu_mass=True)
+        ls.check_layer_state(layer)
+    for _ in range(ls.steps):
+        ls.step()
+    print(f"prefill near-ties (fp64 mass vs the GPU's fp32 mass): {ls.prefill_near_ties}")
+    assert ls.prefill_near_ties <= max(1, wl.batch * wl.num_kv_heads * ls.L // 100)
+    ls.check_near_ties()
 
 
 @pytest.mark.parametrize("key,kv", [(3, (4, 2)), (4, (4, 2)), (2, (4, 4))])
@@ -296,7 +329,7 @@ def test_max_batch_ragged_lockstep(T, key, kv):
     ls.check_layer_state(0)
     for _ in range(ls.steps):
         ls.step()
-    assert ls.near_ties <= 2
+    ls.check_near_ties()
 
 
 @pytest.mark.parametrize("d,window,policy", [(64, 100, "h2o"), (128, 96, "position"),
@@ -314,4 +347,4 @@ def test_wide_fp16_tiers_lockstep(T, d, window, policy):
     ls.check_layer_state(0)
     for _ in range(ls.steps):
         ls.step()
-    assert ls.near_ties <= 1
+    ls.check_near_ties()

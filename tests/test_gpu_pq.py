@@ -93,7 +93,7 @@ def test_pq_lockstep(T, key, policy, kbits):
     ls.check_layer_state(0)
     for _ in range(ls.steps):
         ls.step()
-    assert ls.near_ties <= 1
+    ls.check_near_ties()
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -108,4 +108,4 @@ def test_pq_lockstep_query_groups(T, d, G):
     ls.check_layer_state(0)
     for _ in range(ls.steps):
         ls.step()
-    assert ls.near_ties <= 1
+    ls.check_near_ties()

@@ -146,6 +146,7 @@ extern "C" fade_status_t fade_layout(const fade_config_t* c, int32_t max_prompt,
   o->attn_ws = B * Hq * (size_t)o->max_splits * (d + 2) * 4;
   o->max_prompt = max_prompt;
   o->mid_stride = (int32_t)C;
+  o->prefill_mass_ws = B * Hq * (size_t)max_prompt * 8;
   return FADE_OK;
 }
 

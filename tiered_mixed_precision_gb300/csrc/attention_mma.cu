@@ -4,10 +4,14 @@
 // fp16 scale per 32 channels); page "探秘Transformer系列之（25）--- KV Cache优化之处理长文本序列"
 // §1.2 (softmax-weighted average of V).
 //
-// One CTA = one (row, KV head) unit and one chunk of its middle tokens. A producer warp streams
-// 256-token tiles into a shared-memory ring with TMA (2D tiled copies of the code rows with a
-// bank-spreading swizzle, 1D bulk copies of the scale rows) under mbarrier completion; the
-// consumer warps each take an equal share (64 or 32 tokens) of a tile:
+// A persistent grid (a fixed number of CTAs per SM) under a stream-K schedule: every unit's
+// middle tier is cut into 256-token tiles, and CTA c takes the FP16-tier items of units c,
+// c + P, ... and then a contiguous run of tiles in global order (which may cross units; each
+// run inside one unit is a segment with its own partial, merged by attn_combine_sk_kernel).
+// A producer warp streams the items' tiles into a shared-memory ring with TMA (2D tiled copies
+// of the code rows with a bank-spreading swizzle, 1D bulk copies of the scale rows) under
+// mbarrier completion; the consumer warps each take an equal share (64 or 32 tokens) of a
+// tile:
 //   QK^T: tokens are the MMA's M dimension, channels its K dimension. The packed codes become
 //     exact fp16 integers in registers; each 64-channel half of the head dimension accumulates
 //     in its own fragment whose 8 columns are (query head h, group parity), the query operand

@@ -525,19 +525,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: gives up after kWaitCycles and records the failure in status[0].
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status,
-                                          int code) {
+// Bounded wait: gives up after `limit` cycles and records the failure (`code`) in status[0]
+// unless an earlier failure is recorded there.
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, int32_t* status,
+                                                int code, long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       atomicCAS(status, 0, code);
       return false;
     }
     __nanosleep(64);
   }
   return true;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status,
+                                          int code) {
+  return mbar_wait_limit(bar, parity, status, code, kWaitCycles);
 }
 __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,
                                              uint32_t bar) {

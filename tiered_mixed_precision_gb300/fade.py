@@ -75,7 +75,7 @@ class LayoutT(ctypes.Structure):
         "victims", "chunk_base", "status", "logits_ws")] + [("mid_stride", c_i32)] + [
         (n, c_sz) for n in ("ml_ws", "attn_ws")] + [
         ("victim_words", c_i32), ("chunk_slots", c_i32), ("max_prompt", c_i32),
-        ("max_splits", c_i32)]
+        ("max_splits", c_i32), ("prefill_mass_ws", c_sz)]
 
 
 _lib = None
@@ -100,7 +100,8 @@ def lib():
             "fade_cache_reset": (c_i32, [S(ConfigT), S(LayerT), c_vp]),
             "fade_cache_prefill": (c_i32, [S(ConfigT), S(LayerT), c_vp, c_vp, c_i32, c_vp,
                                            c_vp, c_vp, c_i32, c_vp]),
-            "fade_prefill_mass": (c_i32, [S(ConfigT), c_vp, c_vp, c_i32, c_vp, c_vp, c_vp]),
+            "fade_prefill_mass": (c_i32, [S(ConfigT), c_vp, c_vp, c_i32, c_vp, c_vp, c_vp,
+                                          c_sz, c_vp]),
             "fade_cache_demote": (c_i32, [S(ConfigT), S(LayerT), c_vp]),
             "fade_evict_rerope": (c_i32, [S(ConfigT), S(LayerT), c_vp, c_i32, c_vp]),
             "fade_cache_append": (c_i32, [S(ConfigT), S(LayerT), c_vp, c_vp, c_vp]),
@@ -113,6 +114,8 @@ def lib():
             "fade_pq_encode": (c_i32, [c_vp, c_vp, c_i64, c_i32, c_vp, c_vp]),
             "fade_pq_decode": (c_i32, [c_vp, c_vp, c_i64, c_i32, c_vp, c_vp]),
             "fade_pq_train": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp]),
+            "fade_check_status": (c_i32, [S(LayerT), c_vp]),
+            "fade_selftest_bounded_wait": (c_i32, [c_vp, c_i32, c_i64, c_vp]),
             "fade_last_error": (ctypes.c_char_p, []),
         }
         for name, (res, args) in sig.items():
@@ -354,10 +357,20 @@ def fade_cache_prefill(layer: TieredLayer, k_rot, v, max_prompt, prompt_len, mas
                                     _ptr(mass), _ptr(table), max_pos, _stream(stream)))
 
 
-def fade_prefill_mass(cfg: Config, q_rot, k_rot, max_prompt, prompt_len, mass, stream=None):
+def fade_prefill_mass(cfg: Config, q_rot, k_rot, max_prompt, prompt_len, mass, ws=None,
+                      stream=None):
+    """ws: device workspace of at least layout(cfg, max_prompt).prefill_mass_ws bytes (made
+    here when not given)."""
     lens = np.ascontiguousarray(prompt_len, np.int32)
+    if ws is None:
+        import torch
+
+        ws = torch.empty(fade_layout(cfg, max_prompt).prefill_mass_ws, dtype=torch.uint8,
+                         device=q_rot.device)
+    nbytes = ws.numel() * ws.element_size()
     _check(lib().fade_prefill_mass(ctypes.byref(cfg.c()), _ptr(q_rot), _ptr(k_rot), max_prompt,
-                                   lens.ctypes.data, _ptr(mass), _stream(stream)))
+                                   lens.ctypes.data, _ptr(mass), _ptr(ws), nbytes,
+                                   _stream(stream)))
 
 
 def fade_cache_demote(layer: TieredLayer, stream=None):
@@ -430,3 +443,15 @@ def fade_pq_train(calib, n_vec, dim, init_idx, iters, codebook, ws, stream=None)
         raise ValueError("init_idx must hold 256 indices")
     _check(lib().fade_pq_train(_ptr(calib), n_vec, dim, idx.ctypes.data, iters, _ptr(codebook),
                                _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def fade_check_status(layer: TieredLayer, stream=None):
+    """Synchronise the stream and raise FadeError (status 5, FADE_ERR_TIMEOUT) if a kernel of
+    the layer gave up a bounded wait since the last reset."""
+    _check(lib().fade_check_status(ctypes.byref(layer.c), _stream(stream)))
+
+
+def fade_selftest_bounded_wait(status, producer_arrives: bool, limit_cycles: int, stream=None):
+    """Launch the bounded-wait self-test kernel (status: a device int32 tensor)."""
+    _check(lib().fade_selftest_bounded_wait(_ptr(status), int(bool(producer_arrives)),
+                                            int(limit_cycles), _stream(stream)))

@@ -154,7 +154,8 @@ class FadeCache:
         """k_raw, v: fp16 [B][Hkv][P][d] device tensors (k pre-RoPE; rotated in place).
 
         For H2O either ``mass`` (f32 [B][Hkv][P]) is given, or ``q_raw`` (fp16 [B][Hq][P][d],
-        pre-RoPE, rotated in place) and the prefill attention mass is computed on the GPU."""
+        pre-RoPE, rotated in place) and the prefill attention mass is computed on the GPU.
+        Returns the mass the prefill used (None when it used none)."""
         c = self.cfg
         B, H, P, d = k_raw.shape
         if prompt_len is None:
@@ -167,6 +168,7 @@ class FadeCache:
         L = self.layers[layer]
         F.fade_cache_reset(L)
         F.fade_cache_prefill(L, k_raw, v, P, prompt_len, mass, self.table, self.max_pos)
+        return mass
 
     def next_positions(self) -> np.ndarray:
         L = self.layers[0]
