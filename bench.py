@@ -60,6 +60,8 @@ def parse_args():
     p.add_argument("--layers", type=int, default=None,
                    help="override the layer count (profiling captures only; the headline "
                         "line always runs every layer of the workload)")
+    p.add_argument("--batch", type=int, default=None,
+                   help="override the batch (profiling captures of a reduced case only)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="launch every kernel (no CUDA graph)")
     p.add_argument("--side-streams", type=int, default=0,
@@ -331,6 +333,8 @@ def run_ours(args, rank, world):
         wl = wl.scaled(seed=wl.seed + 1000 * rank)   # weak scaling: each rank its own batch
     if args.layers:
         wl = wl.scaled(layers=args.layers)
+    if args.batch:
+        wl = wl.scaled(batch=args.batch)
     lens = ragged_context_lengths(wl)
     maxP = int(lens.max())
     K, W = args.steps, args.warmup

@@ -205,6 +205,7 @@ struct LayerArgs {
   int half;
   bool pq;                    // middle-tier V is product-quantised (codes in the INT2 rows)
   const uint16_t* pq_cb;      // the layer's PQ codebook, fp16 [d/4][256][4]
+  float one, neg_one;         // 1 and -1, opaque to the compiler (see PlusMinus)
 };
 
 LayerArgs make_args(const fade_config_t* c, const fade_layer_t* L, const float* table) {
@@ -241,6 +242,8 @@ LayerArgs make_args(const fade_config_t* c, const fade_layer_t* L, const float* 
   a.half = c->head_dim / 2;
   a.pq = c->v_codec == FADE_V_PQ;
   a.pq_cb = L->pq_codebook;
+  a.one = 1.0f;
+  a.neg_one = -1.0f;
   return a;
 }
 
@@ -527,118 +530,300 @@ struct MidCfg {
   static constexpr int PRE_SEL = PRE + TOK / 32;
   static constexpr int SRB = D / 32 * 2;    // bytes of one scale row
 };
-// Per-thread prefetch slots after the staged rows (every thread reads only its own slots).
-template <int D, int KB, int VB>
-struct MidBuf {
-  static constexpr int GB = 32 * KB / 8;                  // bytes of one group's K codes
-  static constexpr int KSH = 2 * GB;                      // K codes of a thread (two groups)
-  static constexpr int SRB = MidCfg<D>::SRB;
-  static constexpr int VSH = D * VB / 8 / MidCfg<D>::TPT;  // V codes of a thread
-  static constexpr int K_OFF = 0;                         // [2][256][KSH]
-  static constexpr int KS_OFF = K_OFF + 2 * 256 * KSH;    // [2][256][SRB]: the whole K scale row
-  static constexpr int V_OFF = KS_OFF + 2 * 256 * SRB;    // [256][VSH]
-  static constexpr int VS_OFF = V_OFF + 256 * VSH;        // [256][4]: this thread's 4 bytes
-  static constexpr int SC_OFF = VS_OFF + 256 * 4;         // [256]: score (first thread of a token)
-  static constexpr int BYTES = SC_OFF + 256 * 4;
-  static size_t smem(int H) {
-    return (size_t)MidCfg<D>::TABF4 * 16 + BYTES + (size_t)H * (MidCfg<D>::PRE_SEL + 4) * 4;
-  }
-};
-
-// cp.async of N bytes issued only where `p` holds (no branch).
-template <int N>
-__device__ __forceinline__ void cp_async_if(bool p, void* smem_dst, const void* gmem_src) {
-  static_assert(N == 4 || N == 8 || N == 16, "cp.async copies 4, 8 or 16 bytes");
-  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
-  if constexpr (N == 16)
-    asm volatile(
-        "{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n"
-        " @q cp.async.cg.shared.global [%0], [%1], 16;\n}\n" ::"r"(d),
-        "l"(gmem_src), "r"((int)p)
-        : "memory");
-  else
-    asm volatile(
-        "{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n"
-        " @q cp.async.ca.shared.global [%0], [%1], %3;\n}\n" ::"r"(d),
-        "l"(gmem_src), "r"((int)p), "n"(N)
-        : "memory");
+// Shared memory of the compaction kernel: the staged RoPE rows, then per head the counts and
+// the victim prefixes of the block.
+template <int D>
+size_t compact_smem(int H) {
+  return (size_t)MidCfg<D>::TABF4 * 16 + (size_t)H * (MidCfg<D>::PRE_SEL + 4) * 4;
 }
 
 template <int D>
 __host__ __device__ constexpr int compact_tok() { return MidCfg<D>::TOK; }
 
-// One thread's two key groups of a moved middle token (codes kp: group g1 then g2, GB bytes
-// each; scales S1, S2 as packed pairs): dequantise (exact), un-RoPE with the old position's row
-// `to`, re-RoPE with the new one's `tn` (16 float4 each: pairs 2k, 2k+1 in float4 k), every
-// product and sum rounded on its own (packed products, scalar sums), cast to fp16 (H1, H2: half2
-// words, pair k in word k) and the fp32 absmax of each group (a1m, a2m).
-template <int KB>
-__device__ __forceinline__ void reposition_groups(const uint8_t* kp, f2x S1, f2x S2,
-                                                  const float4* to, const float4* tn,
-                                                  uint32_t (&H1)[16], uint32_t (&H2)[16],
-                                                  float& a1m, float& a2m) {
-  constexpr int GB = 32 * KB / 8;
-  uint32_t w1[GB / 4], w2[GB / 4];
+// Packed (1, 1) and (-1, -1) whose values the compiler cannot see (they come from kernel
+// arguments). A sum or difference of two separately rounded products is taken as
+// fma(p, +-1, q): that rounds p +- q once, exactly like the scalar IEEE sum, and the product
+// that made p cannot be fused into it.
+struct PlusMinus {
+  f2x one, neg;
+};
+
+// Rotation of two pairs at once with every product and every sum rounded on its own:
+// X1 = (x_a, x_b) of the first half, X2 = their partners, C and S the pairs' cos and sin.
+__device__ __forceinline__ void rot2_inv_pm(f2x& X1, f2x& X2, f2x C, f2x S, const PlusMinus& u) {
+  const f2x p = f2_mul(X1, C), q = f2_mul(X2, S), r = f2_mul(X2, C), t = f2_mul(X1, S);
+  X1 = f2_fma(p, u.one, q);  // x1 c + x2 s
+  X2 = f2_fma(t, u.neg, r);  // x2 c - x1 s
+}
+__device__ __forceinline__ void rot2_fwd_pm(f2x& X1, f2x& X2, f2x C, f2x S, const PlusMinus& u) {
+  const f2x p = f2_mul(X1, C), q = f2_mul(X2, S), r = f2_mul(X2, C), t = f2_mul(X1, S);
+  X1 = f2_fma(q, u.neg, p);  // x1 c - x2 s
+  X2 = f2_fma(r, u.one, t);  // x2 c + x1 s
+}
+
+// Exact dequantisation of one INT4 group (4 little-endian words, channel j at bits 4j), pair k
+// = channels (2k, 2k+1) as one packed pair. The offset-binary nibble u = q + 8 of an even
+// channel (low nibble of its byte) goes to mantissa bits 8..11 of 2^15, giving 2^15 + u; an
+// odd channel's (high nibble) to bits 12..15, giving 2^15 + 16u. One fused multiply-add then
+// yields q s exactly: (2^15 + u) s - (2^15 + 8) s and (2^15 + 16u) (s/16) - (2^11 + 8) s. Its
+// exact result q s is representable, and so are the constants: (2^15 + 8) s = 8 s (2^12 + 1)
+// and (2^11 + 8) s = 8 s (2^8 + 1) need at most 11 + 13 significant bits, and s/16 is a
+// power-of-two scaling (no underflow for any fp16 s).
+struct Int4Group {
+  uint32_t ev[4], od[4];  // bytes: offset-binary even nibbles (low), odd nibbles (high)
+  f2x S, C;               // (s, s/16), (-(2^15 + 8) s, -(2^11 + 8) s)
+};
+__device__ __forceinline__ Int4Group int4_group(const uint32_t (&w)[4], float s) {
+  Int4Group g;
 #pragma unroll
-  for (int w = 0; w < GB / 4; ++w) {
-    w1[w] = reinterpret_cast<const uint32_t*>(kp)[w];
-    w2[w] = reinterpret_cast<const uint32_t*>(kp + GB)[w];
+  for (int i = 0; i < 4; ++i) {
+    g.ev[i] = (w[i] & 0x0F0F0F0Fu) ^ 0x08080808u;
+    g.od[i] = (w[i] & 0xF0F0F0F0u) ^ 0x80808080u;
   }
-  uint32_t ev1[2], od1[2], ev2[2], od2[2];
+  g.S = f2_pack(s, s * 0.0625f);
+  g.C = f2_pack(s * -32776.f, s * -2056.f);
+  return g;
+}
+template <int K>
+__device__ __forceinline__ f2x int4_pair(const Int4Group& g) {
+  constexpr uint32_t sel = 0x7504u | ((uint32_t)(K & 3) << 4);  // byte 1 <- byte K%4
+  const float lo = __uint_as_float(prmt(g.ev[K >> 2], 0x47000000u, sel));
+  const float hi = __uint_as_float(prmt(g.od[K >> 2], 0x47000000u, sel));
+  return f2_fma(f2_pack(lo, hi), g.S, g.C);
+}
+
+// Codes of 16 fp16 values (8 half2 words) for a scale s >= 2^-14 (normal), packed little-endian
+// from bit 0 of out[0] (INT4: two words, INT2: one): exact round_half_even(x / s). The candidate
+// rint(x * r) (r = an approximate 1/s; the product is exact inside the fused multiply-add that
+// adds 1.5 * 2^23) is within 8e-7 of x / s, while x / s is either exactly a half-integer or at
+// least 2^-13 from one (fp16 operands), so only exact ties can be mis-rounded; the exact
+// residual x - q s, equal to s/2 in magnitude exactly at a tie, confirms all 16 codes or sends
+// the half group to the exact scalar path (ties to even).
+template <int BITS>
+__device__ __forceinline__ void codes_half_group_fast(const uint32_t (&H)[8], float s,
+                                                      uint32_t* out) {
+  constexpr uint32_t mask = (1u << BITS) - 1u;
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+  const f2x R = f2_pack(r, r), M = f2_pack(12582912.f, 12582912.f), NS = f2_pack(-s, -s);
+  uint32_t qb[16];
+  float emax = 0.f;
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    f2x X1, X2;
-    if constexpr (KB == 4) {
-      if (k % 8 == 0) {  // words 2(k/8), 2(k/8)+1 hold channels 16(k/8) .. +15
-        const uint32_t p1[2] = {w1[2 * (k / 8)], w1[2 * (k / 8) + 1]};
-        const uint32_t p2[2] = {w2[2 * (k / 8)], w2[2 * (k / 8) + 1]};
-        split_int4(p1, ev1, od1);
-        split_int4(p2, ev2, od2);
+  for (int k = 0; k < 8; ++k) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&H[k]));
+    const f2x X = f2_pack(f.x, f.y);
+    const f2x QM = f2_fma(X, R, M);
+    const f2x E = f2_fma(f2_sub(QM, M), NS, X);
+    float e0, e1, qm0, qm1;
+    f2_unpack(E, e0, e1);
+    f2_unpack(QM, qm0, qm1);
+    qb[2 * k] = __float_as_uint(qm0);
+    qb[2 * k + 1] = __float_as_uint(qm1);
+    emax = fmaxf(emax, fmaxf(fabsf(e0), fabsf(e1)));
+  }
+  if (emax < 0.5f * s) {
+    if constexpr (BITS == 4) {
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {
+        const uint32_t a = prmt(prmt(qb[8 * v], qb[8 * v + 2], 0x0040u),
+                                prmt(qb[8 * v + 4], qb[8 * v + 6], 0x0040u), 0x5410u);
+        const uint32_t b = prmt(prmt(qb[8 * v + 1], qb[8 * v + 3], 0x0040u),
+                                prmt(qb[8 * v + 5], qb[8 * v + 7], 0x0040u), 0x5410u);
+        out[v] = (a & 0x0F0F0F0Fu) | ((b << 4) & 0xF0F0F0F0u);
       }
-      X1 = dequant_pair_int4(ev1, od1, k % 8, S1);
-      X2 = dequant_pair_int4(ev2, od2, k % 8, S2);
     } else {
-      X1 = dequant_pair_bits<KB>(w1, k, S1);
-      X2 = dequant_pair_bits<KB>(w2, k, S2);
+      uint32_t o = 0u;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) o |= (qb[j] & mask) << (BITS * j);
+      out[0] = o;
     }
-    const float4 co = to[k], cn = tn[k];
-    rotate2_inv(X1, X2, f2_pack(co.x, co.y), f2_pack(co.z, co.w));
-    rotate2(X1, X2, f2_pack(cn.x, cn.y), f2_pack(cn.z, cn.w));
-    float p10, p11, p20, p21;
-    f2_unpack(X1, p10, p11);
-    f2_unpack(X2, p20, p21);
-    a1m = fmaxf(a1m, fmaxf(fabsf(p10), fabsf(p11)));
-    a2m = fmaxf(a2m, fmaxf(fabsf(p20), fabsf(p21)));
-    const __half2 r1 = __floats2half2_rn(p10, p11), r2 = __floats2half2_rn(p20, p21);
-    H1[k] = *reinterpret_cast<const uint32_t*>(&r1);
-    H2[k] = *reinterpret_cast<const uint32_t*>(&r2);
+    return;
+  }
+  const uint2 ex = codes_half_group_exact<BITS>(make_uint4(H[0], H[1], H[2], H[3]),
+                                                make_uint4(H[4], H[5], H[6], H[7]), s);
+  out[0] = ex.x;
+  if constexpr (BITS == 4) out[1] = ex.y;
+}
+
+// Quantise one group of 32 fp16 values (16 half2 words) whose fp32 absmax (before the fp16
+// cast) is a32: scale s = fp16(fp16(a32) / qmax) (the fp16 absmax equals the fp16 rounding of
+// the fp32 one: rounding is monotone and odd), 2^-24 if it underflows; codes into `o`.
+// Returns the scale's fp16 bits.
+template <int KB>
+__device__ __forceinline__ uint16_t quantize_group16(const uint32_t (&H)[16], float a32,
+                                                     uint32_t (&o)[KB]) {
+  constexpr int qmax = (1 << (KB - 1)) - 1;
+  const float ah = __half2float(__float2half_rn(a32));
+  float s = __half2float(__float2half_rn(div_by_qmax<qmax>(ah)));
+  if (ah > 0.f && s == 0.f) s = kSubnormalMin;
+#pragma unroll
+  for (int w = 0; w < KB; ++w) o[w] = 0u;
+  if (s >= 6.103515625e-05f) {
+    codes_half_group_fast<KB>(*reinterpret_cast<const uint32_t(*)[8]>(&H[0]), s, o);
+    codes_half_group_fast<KB>(*reinterpret_cast<const uint32_t(*)[8]>(&H[8]), s, o + KB / 2);
+  } else if (s > 0.f) {  // subnormal scale: the clamp can bind; the exact path
+    const uint2 lo = codes_half_group_exact<KB>(make_uint4(H[0], H[1], H[2], H[3]),
+                                                make_uint4(H[4], H[5], H[6], H[7]), s);
+    const uint2 hi = codes_half_group_exact<KB>(make_uint4(H[8], H[9], H[10], H[11]),
+                                                make_uint4(H[12], H[13], H[14], H[15]), s);
+    if constexpr (KB == 4) {
+      o[0] = lo.x; o[1] = lo.y; o[2] = hi.x; o[3] = hi.y;
+    } else {
+      o[0] = lo.x; o[1] = hi.x;
+    }
+  }
+  return __half_as_ushort(__float2half_rn(s));
+}
+
+// One thread's two key groups of a moved middle token: codes k1 (group g1) and k2 (group g2,
+// the rotation partners of g1), scales s1, s2. Dequantise (exact), un-RoPE with the old
+// position's row `to`, re-RoPE with the new one's `tn` (16 float4 each: pairs 2k, 2k+1 in
+// float4 k), every product and sum rounded on its own, cast to fp16 and requantise. Writes the
+// new codes and returns the two scales' fp16 bits in sb1, sb2.
+// RoPE rows of the table: staged in shared memory (a 32-bit shared address, read with
+// ld.shared) or in global memory.
+struct SharedRow {
+  uint32_t addr;
+  __device__ __forceinline__ float4 operator[](int k) const {
+    float4 v;
+    // not volatile: the rows are written before the CTA barrier that precedes every read
+    // (the address depends on values read after it), so the load may be scheduled freely
+    asm("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "r"(addr + 16u * (uint32_t)k));
+    return v;
+  }
+};
+struct GlobalRow {
+  const float4* p;
+  __device__ __forceinline__ float4 operator[](int k) const { return __ldg(p + k); }
+};
+
+template <int KB, class Row>
+__device__ __forceinline__ void requant_moved(const uint32_t (&k1)[KB], const uint32_t (&k2)[KB],
+                                              float s1, float s2, const Row to, const Row tn,
+                                              const PlusMinus& pm, uint32_t (&o1)[KB],
+                                              uint32_t (&o2)[KB], uint16_t& sb1,
+                                              uint16_t& sb2) {
+  uint32_t H1[16], H2[16];
+  float a1 = 0.f, a2 = 0.f;
+  if constexpr (KB == 4) {
+    const Int4Group G1 = int4_group(k1, s1), G2 = int4_group(k2, s2);
+#define FADE_REQ_PAIR(K)                                                                  \
+  {                                                                                       \
+    f2x X1 = int4_pair<K>(G1), X2 = int4_pair<K>(G2);                                     \
+    const float4 co = to[K], cn = tn[K];                                                  \
+    rot2_inv_pm(X1, X2, f2_pack(co.x, co.y), f2_pack(co.z, co.w), pm);                    \
+    rot2_fwd_pm(X1, X2, f2_pack(cn.x, cn.y), f2_pack(cn.z, cn.w), pm);                    \
+    float y10, y11, y20, y21;                                                             \
+    f2_unpack(X1, y10, y11);                                                              \
+    f2_unpack(X2, y20, y21);                                                              \
+    a1 = fmaxf(a1, fmaxf(fabsf(y10), fabsf(y11)));                                       \
+    a2 = fmaxf(a2, fmaxf(fabsf(y20), fabsf(y21)));                                        \
+    const __half2 r1 = __floats2half2_rn(y10, y11), r2 = __floats2half2_rn(y20, y21);     \
+    H1[K] = *reinterpret_cast<const uint32_t*>(&r1);                                      \
+    H2[K] = *reinterpret_cast<const uint32_t*>(&r2);                                      \
+  }
+    FADE_REQ_PAIR(0) FADE_REQ_PAIR(1) FADE_REQ_PAIR(2) FADE_REQ_PAIR(3)
+    FADE_REQ_PAIR(4) FADE_REQ_PAIR(5) FADE_REQ_PAIR(6) FADE_REQ_PAIR(7)
+    FADE_REQ_PAIR(8) FADE_REQ_PAIR(9) FADE_REQ_PAIR(10) FADE_REQ_PAIR(11)
+    FADE_REQ_PAIR(12) FADE_REQ_PAIR(13) FADE_REQ_PAIR(14) FADE_REQ_PAIR(15)
+#undef FADE_REQ_PAIR
+  } else {
+    const f2x S1 = f2_pack(s1, s1), S2 = f2_pack(s2, s2);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      f2x X1 = dequant_pair_bits<KB>(k1, k, S1), X2 = dequant_pair_bits<KB>(k2, k, S2);
+      const float4 co = to[k], cn = tn[k];
+      rot2_inv_pm(X1, X2, f2_pack(co.x, co.y), f2_pack(co.z, co.w), pm);
+      rot2_fwd_pm(X1, X2, f2_pack(cn.x, cn.y), f2_pack(cn.z, cn.w), pm);
+      float y10, y11, y20, y21;
+      f2_unpack(X1, y10, y11);
+      f2_unpack(X2, y20, y21);
+      a1 = fmaxf(a1, fmaxf(fabsf(y10), fabsf(y11)));
+      a2 = fmaxf(a2, fmaxf(fabsf(y20), fabsf(y21)));
+      const __half2 r1 = __floats2half2_rn(y10, y11), r2 = __floats2half2_rn(y20, y21);
+      H1[k] = *reinterpret_cast<const uint32_t*>(&r1);
+      H2[k] = *reinterpret_cast<const uint32_t*>(&r2);
+    }
+  }
+  sb1 = quantize_group16<KB>(H1, a1, o1);
+  sb2 = quantize_group16<KB>(H2, a2, o2);
+}
+
+// One head's data of one middle token for one thread, loaded ahead of its use: the K codes
+// of the thread's two groups, the token's K scale row, the thread's share of the V codes, its
+// share of the V scale row and the score.
+template <int D, int KB, int VB>
+struct MidToken {
+  static constexpr int KW = KB;                        // words of one group's codes
+  static constexpr int SW = D / kGroup / 2;            // words of the scale row (1 or 2)
+  static constexpr int VW = D * VB / 8 / MidCfg<D>::TPT / 4;  // words of V (4 or 8)
+  uint32_t k1[KW], k2[KW];
+  uint32_t ks[SW];
+  uint32_t v[VW];
+  uint32_t vs;     // the thread's 4 bytes of the V scale row
+  float sc;
+};
+
+template <int W>
+__device__ __forceinline__ void ldg_words(const void* p, uint32_t (&w)[W]) {
+  static_assert(W == 1 || W == 2 || W % 4 == 0, "1, 2 or a multiple of 4 words");
+  if constexpr (W == 1) {
+    w[0] = __ldg(reinterpret_cast<const uint32_t*>(p));
+  } else if constexpr (W == 2) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+    w[0] = u.x;
+    w[1] = u.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < W / 4; ++i) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(p) + i);
+      w[4 * i] = u.x;
+      w[4 * i + 1] = u.y;
+      w[4 * i + 2] = u.z;
+      w[4 * i + 3] = u.w;
+    }
+  }
+}
+template <int W>
+__device__ __forceinline__ void stg_words(void* p, const uint32_t (&w)[W]) {
+  if constexpr (W == 1) {
+    *reinterpret_cast<uint32_t*>(p) = w[0];
+  } else if constexpr (W == 2) {
+    *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < W / 4; ++i)
+      reinterpret_cast<uint4*>(p)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
   }
 }
 
 // Compact survivors of the live middle buffer into the other one, re-positioning keys whose
 // index drops (the recent rings follow in evict_recent_commit_kernel).
 // grid = (ceil(max_mid / TOK), B), 256 threads; one CTA takes one block of TOK middle indices
-// of one batch row and loops over the row's KV heads. A moved key is dequantised, un-RoPE'd at
-// its old position and re-RoPE'd at its new one, rounded to fp16 and re-quantised, all in the
-// owning thread (see MidCfg). The RoPE rows the block needs (its old positions and the new ones,
-// at most 16 below) are staged once per CTA in shared memory and serve every head; each head's
-// codes, scales and scores are fetched ahead with cp.async (K one processed head ahead, V during
-// the head itself) into slots private to the thread.
+// of one batch row and loops over the row's KV heads. A middle token is handled by D/64
+// adjacent threads (MidCfg); thread t_ of a token owns its quantisation groups g1 = t_ and
+// g2 = t_ + D/64, whose channels are each other's rotation partners. A moved key is
+// dequantised, un-RoPE'd at its old position and re-RoPE'd at its new one, rounded to fp16 and
+// re-quantised, all in the owning thread. The RoPE rows the block needs (its old positions
+// and the new ones, at most 16 below) are staged once per CTA in shared memory and serve
+// every head; each head's codes, scales and score are loaded into registers one head ahead.
 // SEL: a selection policy (victims from the bitmap of evict_select_kernel) whose block's bitmap
 // words are staged in shared memory with their prefix counts; false: the code for every policy,
 // with the victims' prefix read from the bitmap per token (the position policy's instantiation).
 template <int D, int KB, int VB, bool SEL>
 __global__ void __launch_bounds__(256, 2) evict_compact_kernel(LayerArgs a) {
   using CC = MidCfg<D>;
+  using TD = MidToken<D, KB, VB>;
   constexpr int PRE = SEL ? CC::PRE_SEL : CC::PRE;
-  using MB = MidBuf<D, KB, VB>;
-  constexpr int TOK = CC::TOK, TPW = CC::TPW, SRB = CC::SRB;
-  constexpr int GB = MB::GB, KSH = MB::KSH, VSH = MB::VSH;
+  constexpr int TOK = CC::TOK, TPW = CC::TPW;
+  constexpr int GB = 32 * KB / 8;              // bytes of one group's codes
   constexpr int VROW = D * VB / 8, SROW = D / kGroup, KROW = D * KB / 8;
-  extern __shared__ float4 tab[];        // [NROWS][ROWF4 + 1], then the slots of MidBuf
-  uint8_t* pf = reinterpret_cast<uint8_t*>(tab + CC::TABF4);
-  int* hinfo = reinterpret_cast<int*>(pf + MB::BYTES);  // [H][4]: n_mid n_ev n_sink cur
-  int* hpre = hinfo + a.H * 4;                          // [H][PRE]
+  constexpr int VSH = VROW / CC::TPT;          // bytes of V per thread
+  extern __shared__ float4 tab[];              // [NROWS][ROWF4 + 1], then hinfo, hpre
+  int* hinfo = reinterpret_cast<int*>(tab + CC::TABF4);  // [H][4]: n_mid n_ev n_sink cur
+  int* hpre = hinfo + a.H * 4;                           // [H][PRE]
   __shared__ int s_rlo, s_rhi;
   const int b = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -711,70 +896,47 @@ __global__ void __launch_bounds__(256, 2) evict_compact_kernel(LayerArgs a) {
   }
   __syncthreads();
 
+  const PlusMinus pm{f2_pack(a.one, a.one), f2_pack(a.neg_one, a.neg_one)};
   // lanes: token-minor (TPW consecutive tokens per t_), so a quarter warp reads one float4 of
   // eight consecutive RoPE rows (the padding puts them in eight different bank quads)
-  const int tid = threadIdx.x;
   const int it = warp * TPW + lane % TPW, t_ = lane / TPW;
   const int i = lo + it;
   const int g1 = t_, g2 = t_ + D / 64;
   const int4* hinfo4 = reinterpret_cast<const int4*>(hinfo);
-  uint8_t* kslot = pf + MB::K_OFF + tid * KSH;    // + buffer * 256 * KSH
-  uint8_t* ksslot = pf + MB::KS_OFF + tid * SRB;  // + buffer * 256 * SRB
-  uint8_t* vslot = pf + MB::V_OFF + tid * VSH;
-  uint8_t* vsslot = pf + MB::VS_OFF + tid * 4;
-  float* scslot = reinterpret_cast<float*>(pf + MB::SC_OFF) + tid;
   const uint32_t row0 = (uint32_t)(b * a.H) * (uint32_t)a.C;  // slot 0 of the row's first unit
-  // a head's K codes and scale row for this thread (into K buffer `buf`)
-  auto prefetch_k = [&](int hh, int buf) {
-    const int4 m = hinfo4[hh];
-    const bool p = i < m.x;
-    const uint32_t r = row0 + (uint32_t)hh * (uint32_t)a.C + (uint32_t)i;
-    const uint8_t* kr = (m.w ? a.mk[1] : a.mk[0]) + (size_t)r * KROW;
-    uint8_t* kd = kslot + buf * 256 * KSH;
-    cp_async_if<GB>(p, kd, kr + g1 * GB);
-    cp_async_if<GB>(p, kd + GB, kr + g2 * GB);
-    cp_async_if<SRB>(p, ksslot + buf * 256 * SRB, (m.w ? a.mks[1] : a.mks[0]) + (size_t)r * SROW);
-  };
-  // a head's V codes (this thread's share), V scales (its 4 bytes) and score
-  auto prefetch_v = [&](int hh) {
-    const int4 m = hinfo4[hh];
-    const bool p = i < m.x;
-    const uint32_t r = row0 + (uint32_t)hh * (uint32_t)a.C + (uint32_t)i;
-    const bool c = m.w != 0;
-    const uint8_t* vr = (c ? a.mv[1] : a.mv[0]) + (size_t)r * VROW + t_ * VSH;
-#pragma unroll
-    for (int q = 0; q < VSH / 16; ++q) cp_async_if<16>(p, vslot + 16 * q, vr + 16 * q);
-    cp_async_if<4>(p, vsslot, (c ? a.mvs[1] : a.mvs[0]) + (size_t)r * SROW + 2 * t_);
-    cp_async_if<4>(p && t_ == 0, scslot, (c ? a.mid_sc[1] : a.mid_sc[0]) + r);
-  };
   auto has_work = [&](int hh) {
     const int4 m = hinfo4[hh];
     return m.y != 0 && lo < m.x;
   };
-  int kb = 0;  // K buffer of the head being processed
-  {
-    int h0 = 0;
-    while (h0 < a.H && !has_work(h0)) ++h0;
-    if (h0 < a.H) prefetch_k(h0, 0);
-    cp_async_commit();
-  }
-  for (int h = 0; h < a.H; ++h) {
+  // a head's data for this thread (zeros past the unit's middle tier)
+  auto load = [&](int hh, TD& d) {
+    const int4 m = hinfo4[hh];
+    if (i < m.x) {
+      const uint32_t r = row0 + (uint32_t)hh * (uint32_t)a.C + (uint32_t)i;
+      const uint8_t* kr = (m.w ? a.mk[1] : a.mk[0]) + (size_t)r * KROW;
+      ldg_words(kr + g1 * GB, d.k1);
+      ldg_words(kr + g2 * GB, d.k2);
+      ldg_words((m.w ? a.mks[1] : a.mks[0]) + (size_t)r * SROW, d.ks);
+      ldg_words((m.w ? a.mv[1] : a.mv[0]) + (size_t)r * VROW + t_ * VSH, d.v);
+      d.vs = __ldg(reinterpret_cast<const uint32_t*>((m.w ? a.mvs[1] : a.mvs[0]) +
+                                                     (size_t)r * SROW) + t_);
+      d.sc = __ldg((m.w ? a.mid_sc[1] : a.mid_sc[0]) + r);
+    }
+  };
+  int h = 0;
+  while (h < a.H && !has_work(h)) ++h;
+  TD cur;
+  if (h < a.H) load(h, cur);
+  while (h < a.H) {  // uniform per CTA
+    int hn = h + 1;
+    while (hn < a.H && !has_work(hn)) ++hn;
+    TD nxt;
+    if (hn < a.H) load(hn, nxt);
     const int4 m = hinfo4[h];
     const int n_mid = m.x, n_ev = m.y, n_sink = m.z;
-    const bool cur = m.w != 0;
-    if (n_ev == 0 || lo >= n_mid) continue;  // uniform per CTA
-    cp_async_wait<0>();  // this head's K data has landed
-    __syncwarp();
-    prefetch_v(h);
-    cp_async_commit();
-    {
-      int hn = h + 1;
-      while (hn < a.H && !has_work(hn)) ++hn;
-      if (hn < a.H) prefetch_k(hn, kb ^ 1);
-      cp_async_commit();
-    }
+    const bool cbuf = m.w != 0;
     // The TPT lanes of one token lie in one warp and share every flag below, so the warp-wide
-    // ballot and the scale exchange see whole tokens; nothing exits before them.
+    // ballot sees whole tokens; nothing exits before it.
     const bool in_range = i < n_mid;
     bool keep = in_range;
     int nv = 0;
@@ -797,88 +959,45 @@ __global__ void __launch_bounds__(256, 2) evict_compact_kernel(LayerArgs a) {
     }
     const bool moved = keep && nv != i && a.table != nullptr;
     const uint32_t dr = row0 + (uint32_t)h * (uint32_t)a.C + (uint32_t)nv;  // destination row
-    uint8_t* krow_d = (cur ? a.mk[0] : a.mk[1]) + (size_t)dr * KROW;
-    uint16_t* ks_d = (cur ? a.mks[0] : a.mks[1]) + (size_t)dr * SROW + 2 * t_;  // 4 bytes
-    const uint8_t* kp = kslot + kb * 256 * KSH;
-    const uint8_t* ksp = ksslot + kb * 256 * SRB;
-    kb ^= 1;
-
-    if (keep && !moved) {  // survivor at its own index (or no RoPE): K codes and scales as they are
-      copy_row<GB>(kp, krow_d + g1 * GB);
-      copy_row<GB>(kp + GB, krow_d + g2 * GB);
-      *reinterpret_cast<uint32_t*>(ks_d) = reinterpret_cast<const uint32_t*>(ksp)[t_];
+    uint8_t* krow_d = (cbuf ? a.mk[0] : a.mk[1]) + (size_t)dr * KROW;
+    uint16_t* ks_d = (cbuf ? a.mks[0] : a.mks[1]) + (size_t)dr * SROW;
+    const uint16_t* ksrc = reinterpret_cast<const uint16_t*>(cur.ks);
+    if (keep && !moved) {  // survivor at its own index (or no RoPE): K as it is
+      stg_words(krow_d + g1 * GB, cur.k1);
+      stg_words(krow_d + g2 * GB, cur.k2);
+      ks_d[g1] = ksrc[g1];
+      ks_d[g2] = ksrc[g2];
     }
-    if (__ballot_sync(0xffffffffu, moved) != 0u) {  // warp-uniform
-      uint32_t H1[16], H2[16];  // the re-positioned groups g1, g2, rounded to fp16 (half2 pairs)
-      float a1m = 0.f, a2m = 0.f;
-      if (moved) {
-        const uint16_t* ksrow = reinterpret_cast<const uint16_t*>(ksp);
-        const float sc1 = h2f(ksrow[g1]), sc2 = h2f(ksrow[g2]);
-        const f2x S1 = f2_pack(sc1, sc1), S2 = f2_pack(sc2, sc2);
-        // this thread's 16 float4 (pairs 32 t_ .. 32 t_ + 31) of the old and the new position's
-        // RoPE row: the staged rows when the block's range fit (shared-memory loads), else the
-        // table in global memory
-        if (staged)
-          reposition_groups<KB>(kp, S1, S2, tab + tab_slot<D>(n_sink + i - rlo, 16 * t_),
-                                tab + tab_slot<D>(n_sink + nv - rlo, 16 * t_), H1, H2, a1m, a2m);
-        else
-          reposition_groups<KB>(
-              kp, S1, S2,
-              reinterpret_cast<const float4*>(a.table) + (size_t)(n_sink + i) * CC::ROWF4 + 16 * t_,
-              reinterpret_cast<const float4*>(a.table) + (size_t)(n_sink + nv) * CC::ROWF4 + 16 * t_,
-              H1, H2, a1m, a2m);
-      }
-      // group absmax of the fp16 values = fp16 rounding of the fp32 absmax (round-to-nearest is
-      // monotone and odd); scale = fp16(absmax / qmax)
-      a1m = __half2float(__float2half_rn(a1m));
-      a2m = __half2float(__float2half_rn(a2m));
-      constexpr int qmax = (1 << (KB - 1)) - 1;
-      float s1 = __half2float(__float2half_rn(div_by_qmax<qmax>(a1m)));
-      float s2 = __half2float(__float2half_rn(div_by_qmax<qmax>(a2m)));
-      if (a1m > 0.f && s1 == 0.f) s1 = kSubnormalMin;
-      if (a2m > 0.f && s2 == 0.f) s2 = kSubnormalMin;
-      // the scale row [g0, g1, ...]: thread t_ stores its 4 bytes (groups 2 t_, 2 t_ + 1); with
-      // two threads per token those come from (g1, g2) of both threads
-      const uint32_t my = __half_as_ushort(__float2half_rn(s1)) |
-                          ((uint32_t)__half_as_ushort(__float2half_rn(s2)) << 16);
-      uint32_t srow = my;
-      if constexpr (CC::TPT == 2) {
-        const uint32_t other = __shfl_xor_sync(0xffffffffu, my, TPW);
-        srow = t_ == 0 ? prmt(my, other, 0x5410u) : prmt(other, my, 0x7632u);
-      }
-      if (moved) {
-        constexpr int HW = GB / 8;  // words of codes per half group
-        uint32_t o1[GB / 4], o2[GB / 4];
-#pragma unroll
-        for (int w = 0; w < GB / 4; ++w) o1[w] = o2[w] = 0u;
-        if (s1 > 0.f) {
-          codes_half_group<KB>(*reinterpret_cast<const uint32_t(*)[8]>(&H1[0]), s1, o1);
-          codes_half_group<KB>(*reinterpret_cast<const uint32_t(*)[8]>(&H1[8]), s1, o1 + HW);
-        }
-        if (s2 > 0.f) {
-          codes_half_group<KB>(*reinterpret_cast<const uint32_t(*)[8]>(&H2[0]), s2, o2);
-          codes_half_group<KB>(*reinterpret_cast<const uint32_t(*)[8]>(&H2[8]), s2, o2 + HW);
-        }
-        if constexpr (GB == 16) {
-          *reinterpret_cast<uint4*>(krow_d + g1 * GB) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-          *reinterpret_cast<uint4*>(krow_d + g2 * GB) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
-        } else {
-          *reinterpret_cast<uint2*>(krow_d + g1 * GB) = make_uint2(o1[0], o1[1]);
-          *reinterpret_cast<uint2*>(krow_d + g2 * GB) = make_uint2(o2[0], o2[1]);
-        }
-        *reinterpret_cast<uint32_t*>(ks_d) = srow;
-      }
+    if (__ballot_sync(0xffffffffu, moved) != 0u && moved) {
+      uint32_t o1[KB], o2[KB];
+      uint16_t sb1, sb2;
+      // this thread's 16 float4 (pairs 32 t_ .. 32 t_ + 31) of the old and the new RoPE row
+      if (staged)
+        requant_moved<KB>(cur.k1, cur.k2, h2f(ksrc[g1]), h2f(ksrc[g2]),
+                          SharedRow{smem_u32(tab + tab_slot<D>(n_sink + i - rlo, 16 * t_))},
+                          SharedRow{smem_u32(tab + tab_slot<D>(n_sink + nv - rlo, 16 * t_))}, pm,
+                          o1, o2, sb1, sb2);
+      else
+        requant_moved<KB>(
+            cur.k1, cur.k2, h2f(ksrc[g1]), h2f(ksrc[g2]),
+            GlobalRow{reinterpret_cast<const float4*>(a.table) + (size_t)(n_sink + i) * CC::ROWF4 +
+                      16 * t_},
+            GlobalRow{reinterpret_cast<const float4*>(a.table) + (size_t)(n_sink + nv) * CC::ROWF4 +
+                      16 * t_},
+            pm, o1, o2, sb1, sb2);
+      stg_words(krow_d + g1 * GB, o1);
+      stg_words(krow_d + g2 * GB, o2);
+      ks_d[g1] = sb1;
+      ks_d[g2] = sb2;
     }
-    // V codes (this thread's share of the row), the V scales and the score of every survivor
-    cp_async_wait<1>();  // this head's V data (the newer group is the next head's K data)
-    if (keep) {
-      copy_row<VSH>(vslot, (cur ? a.mv[0] : a.mv[1]) + (size_t)dr * VROW + t_ * VSH);
-      *reinterpret_cast<uint32_t*>((cur ? a.mvs[0] : a.mvs[1]) + (size_t)dr * SROW + 2 * t_) =
-          *reinterpret_cast<const uint32_t*>(vsslot);
-      if (t_ == 0) (cur ? a.mid_sc[0] : a.mid_sc[1])[dr] = *scslot;
+    if (keep) {  // V codes (this thread's share), its V scales and the score move unchanged
+      stg_words((cbuf ? a.mv[0] : a.mv[1]) + (size_t)dr * VROW + t_ * VSH, cur.v);
+      reinterpret_cast<uint32_t*>((cbuf ? a.mvs[0] : a.mvs[1]) + (size_t)dr * SROW)[t_] = cur.vs;
+      if (t_ == 0) (cbuf ? a.mid_sc[0] : a.mid_sc[1])[dr] = cur.sc;
     }
+    cur = nxt;
+    h = hn;
   }
-  cp_async_wait<0>();  // nothing in flight when the CTA exits
 }
 
 // Recent rings after compaction: every ring token's index drops by its unit's n_ev, so its key
@@ -1132,7 +1251,7 @@ template <int D, int KB, int VB>
 struct CompactLaunch {
   static fade_status_t run(const LayerArgs& a, int B, int chunks, cudaStream_t st) {
     // chunks of compact_tok<D>() middle indices per batch row
-    const size_t smem = MidBuf<D, KB, VB>::smem(a.H);
+    const size_t smem = compact_smem<D>(a.H);
     auto kern = a.positional ? evict_compact_kernel<D, KB, VB, false>
                              : evict_compact_kernel<D, KB, VB, true>;
     if (smem > 48 * 1024 &&
