@@ -53,8 +53,10 @@ typedef enum {
 } fade_status_t;
 
 /* RoPE schemes (FADE-zh §RoPE方案兼容性: standard RoPE and the scaling types llama3, linear,
- * ntk, yarn; ALiBi models make re-positioning a no-op: FADE_ROPE_NONE). Every scheme is a set
- * of inverse frequencies inv_i (rotate-half pairs i, i + d/2); base_i = base^(-2i/d):
+ * ntk, yarn, dynamic and proportional; ALiBi models make re-positioning a no-op:
+ * FADE_ROPE_NONE). Every scheme is a set of inverse frequencies inv_i (rotate-half pairs
+ * i, i + r/2 over the rotated width r = fade_rope_t.rotary_dim, d by default: proportional
+ * RoPE is any scheme with r < d); base_i = base^(-2i/r), and d below reads r:
  *   DEFAULT  inv_i = base_i
  *   LLAMA3   base_i blended by the number of rotations r_i = L / (2 pi / base_i) over the
  *            original context L = original_max_position: r_i > high_freq_factor keeps base_i,
@@ -96,6 +98,13 @@ typedef struct {
   double factor;                 /* llama3, linear, ntk, yarn: the scaling factor (> 0) */
   double low_freq_factor;        /* llama3; yarn: alpha */
   double high_freq_factor;       /* llama3; yarn: beta (> low_freq_factor) */
+  int32_t rotary_dim;            /* proportional RoPE (FADE-zh §RoPE方案兼容性: Gemma 4,
+                                    partial_rotary_factor): only channels 0..rotary_dim-1
+                                    rotate, paired (i, i + rotary_dim/2), with every
+                                    scheme's frequencies computed for a rotary_dim-wide head
+                                    (base^(-2i/rotary_dim)); channels rotary_dim..d-1 pass
+                                    through. 0 or d: every channel (standard RoPE). Otherwise
+                                    a multiple of 4 in [4, d). */
 } fade_rope_t;
 
 /* One layer's cache configuration (FADE-zh §自定义配置: n_sink, recent_window, int4_budget,
@@ -204,9 +213,10 @@ typedef struct {
  * `max_prompt` tokens per row. Host only, no CUDA calls. */
 fade_status_t fade_layout(const fade_config_t* cfg, int32_t max_prompt, fade_layout_t* out);
 
-/* RoPE table (FADE-zh §RoPE重计算: float32 RoPE math; FADE-zh §RoPE方案兼容性: default and
- * llama3 scaling). Writes f32 [max_pos][d/4][4]: block b of position pos holds (cos_{2b},
- * cos_{2b+1}, sin_{2b}, sin_{2b+1}) of rotation pairs 2b and 2b+1, for
+/* RoPE table (FADE-zh §RoPE重计算: float32 RoPE math; FADE-zh §RoPE方案兼容性: the schemes
+ * above). Writes f32 [max_pos][d/4][4]: block b < r/4 of position pos holds (cos_{2b},
+ * cos_{2b+1}, sin_{2b}, sin_{2b+1}) of rotation pairs 2b and 2b+1 (r = the rotated width;
+ * blocks r/4..d/4-1 are not written), for
  * angle = fp32(pos) * inv_freq_i (one fp32 multiply), inv_freq_i = base^(-2i/d) in fp64
  * (llama3-adjusted in fp64) rounded to fp32, cos/sin evaluated in fp64 and rounded to fp32.
  * `table` is device memory of max_pos*d*4 bytes, 16-byte aligned. Not valid for
@@ -218,7 +228,8 @@ fade_status_t fade_rope_table_init(const fade_config_t* cfg, float* table, int32
  * position of a token is its index in the cache). x, y: fp16 [n_groups][group_len][d]
  * (y may alias x). Vector j of group g is rotated to position
  * (pos_start ? pos_start[g] : 0) + j * pos_step, with pos_start a device i32 [n_groups].
- * Rotation pairs channel i with i + d/2; every product and sum is rounded to fp32 (no fused
+ * Rotation pairs channel i with i + r/2 for i < r/2 (r = the rotated width, d by default);
+ * channels r..d-1 are copied unchanged; every product and sum is rounded to fp32 (no fused
  * multiply-add); the result is rounded to fp16. Positions must lie in [0, max_pos). */
 fade_status_t fade_rope_apply(const fade_config_t* cfg, const float* table, int32_t max_pos,
                               const uint16_t* x, uint16_t* y, int64_t n_groups,

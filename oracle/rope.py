@@ -11,6 +11,10 @@ at cache index j carries rotation j.
 Readings:
   * rotate-half pairing: channel i pairs with channel i + d/2, i < d/2 (the pairing of the
     model families the pages list);
+  * proportional RoPE (FADE-zh §RoPE方案兼容性: Gemma 4, ``partial_rotary_factor``): only the
+    first ``rotary_dim`` = factor * d channels rotate, paired as (i, i + rotary_dim/2), with
+    the frequencies taken over rotary_dim (base ** (-2i/rotary_dim)); the other channels pass
+    through unchanged (the published partial-rotary convention). rotary_dim = d is full RoPE;
   * inv_freq_i = base ** (-2i/d) computed in fp64 and rounded once to fp32; the llama3 rule
     adjusts it in fp64 first: wavelength lam = 2*pi/inv_freq; lam < L/hf keeps inv_freq,
     lam > L/lf divides it by ``factor``, otherwise it is mixed with
@@ -21,6 +25,8 @@ Readings:
     product and sum rounded to fp32 separately (no fused multiply-add); inverse: s -> -s;
   * re-positioning: K' = fp16(forward(inverse(K, old), new)), no fp16 rounding in between.
 Pinned by: rotation equals complex multiplication by exp(i*angle) to fp32 rounding,
+pass-through channels bit-identical under proportional RoPE (and the full-width case equal to
+standard RoPE bit for bit),
 inverse-of-forward is the identity (exactly in the fp64 variant, within a few fp32 ulps in
 the table variant), position 0 is the identity, pair norms are preserved, the llama3 bands
 match their closed forms, and scores depend only on the relative distance.
@@ -37,7 +43,8 @@ F32 = np.float32
 
 def inv_freq(kind: str, base: float, head_dim: int, factor=1.0, low_freq_factor=1.0,
              high_freq_factor=4.0, original_max_position=8192, seq_len=None) -> np.ndarray:
-    """fp32 inverse frequencies [d/2] for the rotation pairs.
+    """fp32 inverse frequencies [head_dim/2] for the rotation pairs. ``head_dim`` is the
+    rotated width: the rotary dimension under proportional (partial) RoPE.
 
     FADE-zh §RoPE方案兼容性 names the scaling types; each follows its published definition:
       * "linear" (position interpolation): every frequency divided by ``factor``, i.e. the
@@ -91,27 +98,33 @@ def table(inv_freq32: np.ndarray, max_pos: int):
 
 
 def rotate(x32: np.ndarray, c: np.ndarray, s: np.ndarray, inverse=False) -> np.ndarray:
-    """Rotate fp32 vectors [..., d] by per-pair fp32 (cos, sin) [..., d/2]."""
+    """Rotate fp32 vectors [..., d] by per-pair fp32 (cos, sin) [..., r/2]: channel i pairs
+    with i + r/2 for i < r/2; channels r..d-1 pass through unchanged (r = d: full RoPE)."""
     x32 = np.asarray(x32, F32)
-    half = x32.shape[-1] // 2
-    x1, x2 = x32[..., :half], x32[..., half:]
+    half = np.shape(c)[-1]
+    x1, x2, rest = x32[..., :half], x32[..., half:2 * half], x32[..., 2 * half:]
     if inverse:
         s = -s
     y1 = (x1 * c).astype(F32) - (x2 * s).astype(F32)
     y2 = (x2 * c).astype(F32) + (x1 * s).astype(F32)
-    return np.concatenate([y1.astype(F32), y2.astype(F32)], axis=-1)
+    return np.concatenate([y1.astype(F32), y2.astype(F32), rest], axis=-1)
 
 
 class RopeTable:
     """A model's RoPE: kind "none" makes every operation the identity (ALiBi models)."""
 
     def __init__(self, kind: str, head_dim: int, max_pos: int, base=10000.0, factor=1.0,
-                 low_freq_factor=1.0, high_freq_factor=4.0, original_max_position=8192):
+                 low_freq_factor=1.0, high_freq_factor=4.0, original_max_position=8192,
+                 rotary_dim=0):
         self.kind = kind
         self.head_dim = head_dim
         self.max_pos = max_pos
+        # proportional (partial) RoPE: the rotated width; 0 = every channel
+        self.rotary_dim = head_dim if not rotary_dim else int(rotary_dim)
+        if not (0 < self.rotary_dim <= head_dim and self.rotary_dim % 2 == 0):
+            raise ValueError("rotary_dim must be even and within (0, head_dim]")
         if kind != "none":
-            self.inv_freq = inv_freq(kind, base, head_dim, factor, low_freq_factor,
+            self.inv_freq = inv_freq(kind, base, self.rotary_dim, factor, low_freq_factor,
                                      high_freq_factor, original_max_position, seq_len=max_pos)
             self.cos, self.sin = table(self.inv_freq, max_pos)
 
@@ -119,7 +132,8 @@ class RopeTable:
     def from_workload(cls, wl, max_pos: int) -> "RopeTable":
         r = wl.rope
         return cls(r.kind, wl.head_dim, max_pos, r.base, r.factor, r.low_freq_factor,
-                   r.high_freq_factor, r.original_max_position)
+                   r.high_freq_factor, r.original_max_position,
+                   getattr(r, "rotary_dim", 0))
 
     def _cs(self, pos):
         pos = np.asarray(pos, np.int64)
@@ -146,11 +160,13 @@ class RopeTable:
 
 
 def rotate64(x: np.ndarray, angle: np.ndarray, inverse=False) -> np.ndarray:
-    """fp64 rotate-half rotation by explicit angles [..., d/2] (used by the pins only)."""
+    """fp64 rotate-half rotation by explicit angles [..., r/2] (used by the pins only);
+    channels past r pass through."""
     x = np.asarray(x, np.float64)
-    half = x.shape[-1] // 2
+    half = np.shape(angle)[-1]
     c, s = np.cos(angle), np.sin(angle)
     if inverse:
         s = -s
-    x1, x2 = x[..., :half], x[..., half:]
-    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+    x1, x2, rest = x[..., :half], x[..., half:2 * half], x[..., 2 * half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s, np.broadcast_to(
+        rest, np.broadcast_shapes(rest.shape, x1.shape[:-1] + (rest.shape[-1],)))], axis=-1)

@@ -23,6 +23,7 @@ class Rope:
     low_freq_factor: float = 1.0   # llama3; yarn: alpha
     high_freq_factor: float = 4.0  # llama3; yarn: beta
     original_max_position: int = 8192   # llama3, yarn, dynamic
+    rotary_dim: int = 0            # proportional (partial) RoPE: rotated channels; 0 = all
 
 
 @dataclass(frozen=True)

@@ -58,6 +58,9 @@ def _cfg(T, **kw):
     (dict(batch=0), 1),
     (dict(batch=257), 1),
     (dict(rope_base=1.0), 1),
+    (dict(rope_rotary_dim=6), 1),
+    (dict(rope_rotary_dim=132), 1),
+    (dict(rope_rotary_dim=2), 1),
     (dict(rope_kind="llama3", rope_low_freq_factor=4.0, rope_high_freq_factor=1.0), 1),
     (dict(v_codec="pq", middle_v_bits=4), 1),
     (dict(rope_kind="dynamic", rope_factor=0.5), 1),

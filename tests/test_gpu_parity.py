@@ -62,15 +62,27 @@ _SCALED_ROPES = {
     # context, so the base is scaled by the length-derived factor
     "dynamic": Rope("dynamic", 1e4, factor=2.0, original_max_position=4096),
     "dynamic_short": Rope("dynamic", 1e4, factor=2.0, original_max_position=512),
+    # proportional RoPE (partial_rotary_factor): 64 of 128 channels rotate (whole groups),
+    # 80 of 128 (the third group half rotated), with llama3 frequencies over 48 of 64
+    "prop64": Rope("default", 1e4, rotary_dim=64),
+    "prop80": Rope("default", 5e5, rotary_dim=80),
+    "prop48_llama3": Rope("llama3", 5e5, factor=32.0, low_freq_factor=1.0, high_freq_factor=4.0,
+                          original_max_position=8192, rotary_dim=48),
 }
 
 
-@pytest.mark.parametrize("key", [1, 3, 4, "linear", "ntk", "yarn", "dynamic"])
+@pytest.mark.parametrize("key", [1, 3, 4, "linear", "ntk", "yarn", "dynamic", "prop64", "prop80",
+                                 "prop48_llama3"])
 def test_rope_table_and_apply(T, key):
     import torch
 
-    wl = get_workload(key) if isinstance(key, int) else get_workload(4).scaled(
-        rope=_SCALED_ROPES[key])
+    if isinstance(key, int):
+        wl = get_workload(key)
+    elif key == "prop48_llama3":
+        wl = get_workload(3).scaled(rope=_SCALED_ROPES[key])
+    else:
+        wl = get_workload(4).scaled(rope=_SCALED_ROPES[key])
+    rh = (wl.rope.rotary_dim or wl.head_dim) // 2   # rotation pairs in the table
     cfg = T.Config.from_workload(wl)
     max_pos = 40000
     table = torch.empty(max_pos * wl.head_dim, dtype=torch.float32, device="cuda")
@@ -78,8 +90,8 @@ def test_rope_table_and_apply(T, key):
     ref = RopeTable.from_workload(wl, max_pos)
     # layout: per position, blocks of two pairs (cos_2b, cos_2b+1, sin_2b, sin_2b+1)
     tab = table.view(max_pos, wl.head_dim // 4, 4).cpu().numpy()
-    cos = tab[..., 0:2].reshape(max_pos, wl.head_dim // 2)
-    sin = tab[..., 2:4].reshape(max_pos, wl.head_dim // 2)
+    cos = tab[..., 0:2].reshape(max_pos, wl.head_dim // 2)[:, :rh]
+    sin = tab[..., 2:4].reshape(max_pos, wl.head_dim // 2)[:, :rh]
     for got, want in ((cos, ref.cos), (sin, ref.sin)):
         ulps = np.abs(got.view(np.int32).astype(np.int64) - want.view(np.int32).astype(np.int64))
         assert ulps.max() <= 1, "table entry more than 1 fp32 ulp from the oracle"
@@ -194,6 +206,23 @@ def _small(key):
         return get_workload(4).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
                                       rope=_SCALED_ROPES["dynamic_short"], prompt_len=900,
                                       int4_budget=300, steps=5), None
+    # proportional RoPE under each eviction policy: whole groups rotated, a group split
+    if key == "prop_pos_r64":
+        return get_workload(4).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                      rope=_SCALED_ROPES["prop64"], prompt_len=900,
+                                      int4_budget=300, steps=5), None
+    if key == "prop_h2o_r48":
+        return get_workload(3).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                      rope=_SCALED_ROPES["prop48_llama3"], prompt_len=700,
+                                      int4_budget=250, steps=6), None
+    if key == "prop_pos_r80":
+        return get_workload(4).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                      rope=_SCALED_ROPES["prop80"], prompt_len=900,
+                                      int4_budget=300, steps=5), None
+    if key == "prop_ema_r80":
+        return get_workload(5).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
+                                      rope=_SCALED_ROPES["prop80"], ragged=(900, 1300),
+                                      prompt_len=1300, int4_budget=500, steps=5), None
     if key == "rope_yarn_ema":
         return get_workload(5).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
                                       rope=_SCALED_ROPES["yarn"], ragged=(900, 1300),
@@ -206,7 +235,8 @@ def _small(key):
                                  "d64_k2v2_ema", "d128_k2v2_pos", "d64_k4v4_pos",
                                  "deg_nosink", "deg_w1_h2o", "deg_budget0", "deg_short_ragged",
                                  "deg_norope_ema", "rope_linear_pos", "rope_ntk_h2o",
-                                 "rope_yarn_ema", "rope_dynamic_pos"])
+                                 "rope_yarn_ema", "rope_dynamic_pos", "prop_pos_r64",
+                                 "prop_h2o_r48", "prop_pos_r80", "prop_ema_r80"])
 def test_lockstep_small_workloads(T, key):
     wl, cap = _small(key)
     ls = Lockstep(wl, mid_capacity=cap)

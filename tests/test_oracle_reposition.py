@@ -25,33 +25,45 @@ BASE = 10000.0
 D = 64
 
 
-def _inv64(d=D, base=BASE):
-    i = np.arange(d // 2, dtype=np.float64)
-    return base ** (-2.0 * i / d)
+RD = {"r": D}   # rotated width (proportional RoPE); the tests set it
 
 
-def _rot64(x, pos, d=D):
-    """fp64 rotate-half rotation of x [..., d] to position(s) pos (exact angles)."""
+def _inv64(r=None, base=BASE):
+    r = RD["r"] if r is None else r
+    i = np.arange(r // 2, dtype=np.float64)
+    return base ** (-2.0 * i / r)
+
+
+def _rot64(x, pos):
+    """fp64 rotate-half rotation of the first r channels of x [..., D] to position(s) pos
+    (exact angles); the other channels pass through."""
     x = np.asarray(x, np.float64)
-    ang = np.asarray(pos, np.float64)[..., None] * _inv64(d)
+    r = RD["r"]
+    ang = np.asarray(pos, np.float64)[..., None] * _inv64()
     c, s = np.cos(ang), np.sin(ang)
-    h = d // 2
-    x1, x2 = x[..., :h], x[..., h:]
-    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+    h = r // 2
+    x1, x2, rest = x[..., :h], x[..., h:r], x[..., r:]
+    rest = np.broadcast_to(rest, x1.shape[:-1] + rest.shape[-1:]) if rest.ndim < x1.ndim else rest
+    y1, y2 = x1 * c - x2 * s, x2 * c + x1 * s
+    rest = np.broadcast_to(rest, y1.shape[:-1] + rest.shape[-1:])
+    return np.concatenate([y1, y2, rest], axis=-1)
 
 
-def _pair_norm(x, d=D):
-    h = d // 2
-    n = np.sqrt(x[..., :h] ** 2 + x[..., h:] ** 2)
-    return np.concatenate([n, n], axis=-1)
+def _pair_norm(x):
+    r = RD["r"]
+    h = r // 2
+    n = np.sqrt(x[..., :h] ** 2 + x[..., h:r] ** 2)
+    return np.concatenate([n, n, np.abs(x[..., r:])], axis=-1)
 
 
-def _angle_tol(x, positions, d=D):
+def _angle_tol(x, positions):
     """Rotation error allowance per channel: fp32 table angles at `positions` (summed) plus
-    fp32 rounding of the rotations, on the pair magnitude."""
-    inv = np.concatenate([_inv64(d), _inv64(d)])
+    fp32 rounding of the rotations, on the pair magnitude (none on pass-through channels)."""
+    r = RD["r"]
+    inv = np.concatenate([_inv64(), _inv64(), np.zeros(D - r)])
+    rot = np.concatenate([np.ones(r), np.zeros(D - r)])
     ptot = np.asarray(positions, np.float64)[..., None]
-    return _pair_norm(x, d) * (2.0 ** -22 * (ptot + 1.0) * inv + 2.0 ** -20)
+    return _pair_norm(x) * (2.0 ** -22 * (ptot + 1.0) * inv + 2.0 ** -20 * rot)
 
 
 def _scales_per_channel(ks):
@@ -67,7 +79,16 @@ def _wl(S, W):
 
 def _unit(S, W, budget, policy):
     p = Params(D, 4, S, W, budget, policy, 4, 2, 0.9)
-    return UnitCache(p, RopeTable("default", D, 8192, base=BASE))
+    return UnitCache(p, RopeTable("default", D, 8192, base=BASE, rotary_dim=RD["r"]))
+
+
+@pytest.fixture(params=[64, 32, 48], ids=["full", "rotary32", "rotary48"], autouse=True)
+def rotary(request):
+    """Every pin runs with full RoPE and with proportional RoPE over 32 channels (one whole
+    quantisation group rotates) and 48 (the rotated width splits the second group)."""
+    RD["r"] = request.param
+    yield request.param
+    RD["r"] = D
 
 
 def _prefilled(policy, S=4, W=8, budget=40, P=120, seed=5):

@@ -168,3 +168,77 @@ def test_reposition_matches_direct_rotation_to_fp16_rounding():
     tol = 3 * np.spacing(r.astype(np.float16)).astype(np.float64) + 2.0 ** -24
     tol = np.concatenate([tol, tol], axis=1)
     assert np.all(diff <= tol)
+
+
+# ---------------------------------------------------------------- proportional (partial) RoPE
+# FADE-zh §RoPE方案兼容性 lists proportional RoPE (Gemma 4, partial_rotary_factor): only the
+# first rotary_dim channels rotate, paired (i, i + rotary_dim/2), frequencies over rotary_dim.
+
+
+def test_proportional_full_width_equals_standard_rope():
+    full = rope.RopeTable("default", 128, 2048, base=1e4)
+    same = rope.RopeTable("default", 128, 2048, base=1e4, rotary_dim=128)
+    assert np.array_equal(full.cos, same.cos) and np.array_equal(full.sin, same.sin)
+    x = np.random.default_rng(20).standard_normal((40, 128)).astype(np.float16)
+    pos = np.arange(40) * 37
+    assert np.array_equal(full.apply(x, pos).view(np.uint16), same.apply(x, pos).view(np.uint16))
+
+
+@pytest.mark.parametrize("d,r", [(128, 64), (128, 96), (64, 32), (64, 48), (64, 16)])
+def test_proportional_pass_through_and_closed_form(d, r):
+    rt = rope.RopeTable("default", d, 5000, base=1e4, rotary_dim=r)
+    assert rt.cos.shape == (5000, r // 2)
+    # the frequencies are the standard ones of an r-dimensional RoPE (closed form, fp64)
+    i = np.arange(r // 2, dtype=np.float64)
+    assert np.array_equal(rt.inv_freq, (1e4 ** (-2.0 * i / r)).astype(F32))
+    rng = np.random.default_rng(d + r)
+    x = rng.standard_normal((64, d)).astype(np.float16)
+    pos = rng.integers(0, 5000, 64)
+    y = rt.apply(x, pos)
+    # channels past the rotary width are untouched, bit for bit
+    assert np.array_equal(y[:, r:].view(np.uint16), x[:, r:].view(np.uint16))
+    # the rotated ones are the complex rotation of pairs (i, i + r/2) by pos * inv_freq
+    ang = (pos.astype(F32)[:, None] * rt.inv_freq[None, :]).astype(F32).astype(np.float64)
+    z = (x[:, :r // 2].astype(np.complex128) + 1j * x[:, r // 2:r]) * np.exp(1j * ang)
+    want = np.concatenate([z.real, z.imag], axis=-1)
+    assert np.allclose(y[:, :r].astype(np.float64), want, atol=2e-3, rtol=2e-3)
+    # re-positioning back to the same position is the fp16 cast of the input
+    same = rt.reposition(x.astype(F32), pos, pos)
+    assert np.array_equal(same[:, r:].view(np.uint16), x[:, r:].view(np.uint16))
+
+
+@pytest.mark.parametrize("d,r", [(128, 64), (64, 48)])
+def test_proportional_scores_depend_only_on_relative_distance(d, r):
+    rt = rope.RopeTable("default", d, 6000, base=1e4, rotary_dim=r)
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal(d)
+    k = rng.standard_normal(d)
+    inv = rt.inv_freq.astype(np.float64)
+    s = []
+    for shift in (0, 100, 4000):
+        P, j = 1000 + shift, 900 + shift
+        qr = rope.rotate64(q, P * inv)
+        kr = rope.rotate64(k, j * inv)
+        s.append(float(qr @ kr))
+    assert np.allclose(s, s[0], atol=1e-9)
+    # and the pass-through channels contribute their plain dot product at any position
+    qr, kr = rope.rotate64(q, 5 * inv), rope.rotate64(k, 3 * inv)
+    assert math.isclose(float(qr[r:] @ kr[r:]), float(q[r:] @ k[r:]), abs_tol=1e-12)
+
+
+def test_proportional_inverse_of_forward():
+    rt = rope.RopeTable("llama3", 128, 9000, base=5e5, factor=8, low_freq_factor=1,
+                        high_freq_factor=4, original_max_position=8192, rotary_dim=64)
+    rng = np.random.default_rng(9)
+    x32 = rng.standard_normal((32, 128)).astype(F32)
+    pos = rng.integers(0, 9000, 32)
+    c, s = rt.cos[pos], rt.sin[pos]
+    back = rope.rotate(rope.rotate(x32, c, s), c, s, inverse=True)
+    assert np.array_equal(back[:, 64:], x32[:, 64:])
+    assert np.max(np.abs(back - x32)) <= 8 * np.spacing(np.abs(x32).max())
+
+
+def test_proportional_rejects_bad_widths():
+    for r in (3, 130, -2):
+        with pytest.raises(ValueError):
+            rope.RopeTable("default", 128, 16, rotary_dim=r)

@@ -85,6 +85,10 @@ fade_status_t validate_config(const fade_config_t* c) {
   if (r.kind == FADE_ROPE_DYNAMIC && !(r.factor >= 1.0 && r.original_max_position > 0))
     return set_error(FADE_ERR_INVALID_ARGUMENT,
                      "dynamic NTK needs factor >= 1 and original_max_position > 0");
+  if (r.rotary_dim != 0 && (r.rotary_dim < 4 || r.rotary_dim > c->head_dim || r.rotary_dim % 4))
+    return set_error(FADE_ERR_INVALID_ARGUMENT,
+                     "rotary_dim %d must be 0 or a multiple of 4 in [4, head_dim]",
+                     r.rotary_dim);
   return FADE_OK;
 }
 

@@ -206,6 +206,7 @@ struct LayerArgs {
   bool pq;                    // middle-tier V is product-quantised (codes in the INT2 rows)
   const uint16_t* pq_cb;      // the layer's PQ codebook, fp16 [d/4][256][4]
   float one, neg_one;         // 1 and -1, opaque to the compiler (see PlusMinus)
+  int rd;                     // rotated width (head_dim unless proportional RoPE)
 };
 
 LayerArgs make_args(const fade_config_t* c, const fade_layer_t* L, const float* table) {
@@ -244,6 +245,7 @@ LayerArgs make_args(const fade_config_t* c, const fade_layer_t* L, const float* 
   a.pq_cb = L->pq_codebook;
   a.one = 1.0f;
   a.neg_one = -1.0f;
+  a.rd = rotary_width(c);
   return a;
 }
 
@@ -477,22 +479,6 @@ __device__ __forceinline__ void store_f16x8(const f2x (&X)[4], uint16_t* p) {
   *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Asynchronous global -> shared copies of N bytes (4, 8 or 16; both addresses N-aligned).
-template <int N>
-__device__ __forceinline__ void cp_async(void* smem_dst, const void* gmem_src) {
-  static_assert(N == 4 || N == 8 || N == 16, "cp.async copies 4, 8 or 16 bytes");
-  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
-  asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(d), "l"(gmem_src), "n"(N)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // Recent-ring re-positioning: geometry. D/32 threads per ring token; thread t_ owns the rotation
 // pairs 16 t_ .. 16 t_ + 15.
 template <int D>
@@ -528,7 +514,6 @@ struct MidCfg {
   static constexpr int PRE = TOK / 32 + 2;  // per-head ints: victim prefix words + base
   // with the block's TOK/32 bitmap words after them (selection policies, staged bitmap)
   static constexpr int PRE_SEL = PRE + TOK / 32;
-  static constexpr int SRB = D / 32 * 2;    // bytes of one scale row
 };
 // Shared memory of the compaction kernel: the staged RoPE rows, then per head the counts and
 // the victim prefixes of the block.
@@ -1104,6 +1089,139 @@ __global__ void __launch_bounds__(256) evict_recent_commit_kernel(LayerArgs a) {
 }
 
 
+// ----------------------------------------------------------------- proportional RoPE
+// With a rotated width rd < D (proportional RoPE) the rotation pairs (i, i + rd/2) no longer
+// line up with the thread-per-group layout of the kernels above, so keys are re-positioned by
+// a warp through a row of fp32 values in shared memory (one row per warp). Every product and
+// sum is rounded on its own, exactly as in the full-width path; channels rd..D-1 only go
+// through the same fp16 cast and requantisation.
+
+// Re-position the fp32 key `row` [D] (shared memory, one warp): pairs i < rd/2.
+template <int D>
+__device__ __forceinline__ void warp_reposition_row(float* row, const LayerArgs& a, int pold,
+                                                    int pnew) {
+  const int lane = threadIdx.x & 31, rh = a.rd / 2;
+  __syncwarp();
+  if (a.table && pold != pnew)
+    for (int i = lane; i < rh; i += 32) {
+      float y1, y2;
+      reposition_pair(a.table, a.half, i, pold, pnew, row[i], row[i + rh], y1, y2);
+      row[i] = y1;
+      row[i + rh] = y2;
+    }
+  __syncwarp();
+}
+
+template <int D>
+__device__ __forceinline__ void warp_key_to_row(const WarpKey<D>& k, float* row) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int gp = 0; gp < D / 64; ++gp) {
+    row[32 * gp + lane] = k.lo[gp];
+    row[32 * gp + lane + D / 2] = k.hi[gp];
+  }
+}
+template <int D>
+__device__ __forceinline__ WarpKey<D> row_to_warp_key(const float* row) {
+  const int lane = threadIdx.x & 31;
+  WarpKey<D> k;
+#pragma unroll
+  for (int gp = 0; gp < D / 64; ++gp) {
+    k.lo[gp] = row[32 * gp + lane];
+    k.hi[gp] = row[32 * gp + lane + D / 2];
+  }
+  return k;
+}
+
+// Re-position a warp-held key (WarpKey layout) with any rotated width: the full-width pairing
+// in registers, otherwise through the warp's shared row.
+template <int D>
+__device__ __forceinline__ void reposition_key_any(const LayerArgs& a, WarpKey<D>& k, int pold,
+                                                   int pnew, float* row) {
+  if (a.rd == D) {
+    reposition_key<D>(a, k, pold, pnew);
+    return;
+  }
+  if (!a.table || pold == pnew) return;
+  warp_key_to_row<D>(k, row);
+  warp_reposition_row<D>(row, a, pold, pnew);
+  k = row_to_warp_key<D>(row);
+  __syncwarp();
+}
+
+// Compaction with proportional RoPE: one warp per middle index of one unit.
+// grid = (ceil(max_mid / 8), H, B), 256 threads.
+template <int D, int KB, int VB>
+__global__ void __launch_bounds__(256) evict_compact_rows_kernel(LayerArgs a) {
+  __shared__ float rows[8][D];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z, h = blockIdx.y, unit = b * a.H + h;
+  const int i = blockIdx.x * 8 + warp;
+  const int32_t* m = a.meta + unit * kF;
+  const int n_mid = m[FADE_META_N_MID], n_sink = m[FADE_META_N_SINK];
+  const int n_ev = a.positional ? max(0, n_mid - a.budget) : m[FADE_META_N_EV];
+  const bool cur = m[FADE_META_CUR] != 0;
+  if (n_ev == 0 || i >= n_mid) return;  // warp-uniform
+  int nv;
+  if (a.positional) {
+    if (i < n_ev) return;
+    nv = i - n_ev;
+  } else {
+    const uint32_t* bm = a.victims + (size_t)unit * a.victim_words;
+    const int32_t* cb = a.chunk_base + (size_t)unit * a.chunk_slots;
+    if ((bm[i >> 5] >> (i & 31)) & 1u) return;
+    nv = i - victims_before(bm, cb, i);
+  }
+  constexpr int KROW = D * KB / 8, VROW = D * VB / 8, SROW = D / kGroup;
+  const size_t r = (size_t)unit * a.C + i, dr = (size_t)unit * a.C + nv;
+  const uint8_t* ks = (cur ? a.mk[1] : a.mk[0]) + r * KROW;
+  const uint16_t* kss = (cur ? a.mks[1] : a.mks[0]) + r * SROW;
+  uint8_t* kd = (cur ? a.mk[0] : a.mk[1]) + dr * KROW;
+  uint16_t* ksd = (cur ? a.mks[0] : a.mks[1]) + dr * SROW;
+  if (nv == i || !a.table) {
+    for (int c = lane; c < KROW; c += 32) kd[c] = ks[c];
+    if (lane < SROW) ksd[lane] = kss[lane];
+  } else {
+    WarpKey<D> key = load_mid_key<D, KB>(ks, kss);
+    reposition_key_any<D>(a, key, n_sink + i, n_sink + nv, rows[warp]);
+    warp_store_quantized<D, KB>(key, kd, ksd);
+  }
+  const uint8_t* vs = (cur ? a.mv[1] : a.mv[0]) + r * VROW;
+  uint8_t* vd = (cur ? a.mv[0] : a.mv[1]) + dr * VROW;
+  for (int c = lane; c < VROW; c += 32) vd[c] = vs[c];
+  if (lane < SROW) (cur ? a.mvs[0] : a.mvs[1])[dr * SROW + lane] = (cur ? a.mvs[1] : a.mvs[0])[r * SROW + lane];
+  if (lane == 0) (cur ? a.mid_sc[0] : a.mid_sc[1])[dr] = (cur ? a.mid_sc[1] : a.mid_sc[0])[r];
+}
+
+// Recent rings after the compaction above, with proportional RoPE: every ring key's index
+// drops by the unit's n_ev (re-positioned in place, one warp per ring token); then the unit's
+// counts are committed. grid = (H, B), 256 threads.
+template <int D>
+__global__ void __launch_bounds__(256) evict_recent_commit_rows_kernel(LayerArgs a) {
+  __shared__ float rows[8][D];
+  const int warp = threadIdx.x >> 5;
+  const int b = blockIdx.y, h = blockIdx.x, unit = b * a.H + h;
+  int32_t* m = a.meta + unit * kF;
+  const int n_mid = m[FADE_META_N_MID], n_sink = m[FADE_META_N_SINK];
+  const int n_rec = m[FADE_META_N_RECENT], head = m[FADE_META_HEAD];
+  const int n_ev = a.positional ? max(0, n_mid - a.budget) : m[FADE_META_N_EV];
+  if (n_ev > 0 && a.table) {
+    for (int t = warp; t < n_rec; t += 8) {
+      uint16_t* row = a.rec_k + ((size_t)unit * a.W + (head + t) % a.W) * D;
+      WarpKey<D> key = load_fp16_key<D>(row);
+      const int pold = n_sink + n_mid + t;
+      reposition_key_any<D>(a, key, pold, pold - n_ev, rows[warp]);
+      store_fp16_key<D>(key, row);
+    }
+  }
+  __syncthreads();  // every warp has read the counts
+  if (threadIdx.x == 0 && n_ev > 0) {
+    m[FADE_META_N_MID] = n_mid - n_ev;
+    m[FADE_META_CUR] ^= 1;
+    m[FADE_META_N_EV] = 0;
+  }
+}
+
 // ----------------------------------------------------------------- prefill
 struct PrefillArgs {
   const uint16_t* k;    // [B][H][maxP][D], RoPE'd at 0..P-1
@@ -1154,6 +1272,7 @@ __global__ void __launch_bounds__(256) prefill_place_kernel(LayerArgs a, Prefill
   const PrefillSplit s = prefill_split(a, P);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int lo = blockIdx.x * kChunk, hi = min(lo + kChunk, P);
+  __shared__ float rows[8][D];  // proportional RoPE: each warp's key during re-positioning
   const uint32_t* bm = a.victims + (size_t)unit * a.victim_words;
   const int32_t* cb = a.chunk_base + (size_t)unit * a.chunk_slots;
   const int m_keep = s.n_m0 - s.k;
@@ -1179,7 +1298,7 @@ __global__ void __launch_bounds__(256) prefill_place_kernel(LayerArgs a, Prefill
     }
     const size_t src = ((size_t)unit * p.maxP + i) * D;
     WarpKey<D> key = load_fp16_key<D>(p.k + src);
-    reposition_key<D>(a, key, i, nv);
+    reposition_key_any<D>(a, key, i, nv, rows[warp]);
     const float score = (a.policy == FADE_EVICT_H2O && p.mass) ? p.mass[(size_t)unit * p.maxP + i]
                                                                : 0.f;
     if (tier == 1) {
@@ -1249,8 +1368,13 @@ struct DemoteLaunch {
 
 template <int D, int KB, int VB>
 struct CompactLaunch {
-  static fade_status_t run(const LayerArgs& a, int B, int chunks, cudaStream_t st) {
+  static fade_status_t run(const LayerArgs& a, int B, int max_mid, cudaStream_t st) {
+    if (a.rd < D) {  // proportional RoPE: one warp per middle index
+      evict_compact_rows_kernel<D, KB, VB><<<dim3(ceil_div(max_mid, 8), a.H, B), 256, 0, st>>>(a);
+      return launch_status("fade_evict_rerope compact (proportional RoPE)");
+    }
     // chunks of compact_tok<D>() middle indices per batch row
+    const int chunks = ceil_div(max_mid, compact_tok<D>());
     const size_t smem = compact_smem<D>(a.H);
     auto kern = a.positional ? evict_compact_kernel<D, KB, VB, false>
                              : evict_compact_kernel<D, KB, VB, true>;
@@ -1265,6 +1389,10 @@ struct CompactLaunch {
 
 template <int D>
 fade_status_t launch_recent_commit(const LayerArgs& a, int B, cudaStream_t st) {
+  if (a.rd < D) {
+    evict_recent_commit_rows_kernel<D><<<dim3(a.H, B), 256, 0, st>>>(a);
+    return launch_status("fade_evict_rerope recent + commit (proportional RoPE)");
+  }
   using CC = RecentCfg<D>;
   const size_t smem = (size_t)CC::TABF4 * 16 + (size_t)a.H * 4 * 4;
   auto kern = evict_recent_commit_kernel<D>;
@@ -1497,8 +1625,7 @@ extern "C" fade_status_t fade_evict_rerope(const fade_config_t* c, fade_layer_t*
                           s>>>(a);
     if ((st = launch_status("fade_evict_rerope select"))) return st;
   }
-  const int ctok = c->head_dim == 128 ? compact_tok<128>() : compact_tok<64>();
-  if ((st = dispatch_dkv<CompactLaunch>(c, a, c->batch, ceil_div(max_mid, ctok), s))) return st;
+  if ((st = dispatch_dkv<CompactLaunch>(c, a, c->batch, max_mid, s))) return st;
   st = c->head_dim == 128 ? launch_recent_commit<128>(a, c->batch, s)
                           : launch_recent_commit<64>(a, c->batch, s);
   if (st) return st;

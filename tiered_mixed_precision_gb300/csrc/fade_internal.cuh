@@ -27,6 +27,12 @@ constexpr int kGroup = FADE_GROUP;     // channels per quantisation group
 constexpr int kChunk = 1024;           // slots per selection chunk (bitmap prefix unit)
 constexpr float kSubnormalMin = 5.9604644775390625e-08f;  // 2^-24
 
+// Rotated width of the configuration's RoPE (proportional RoPE: rotary_dim < d).
+inline int rotary_width(const fade_config_t* c) {
+  return (c->rope.rotary_dim > 0 && c->rope.rotary_dim < c->head_dim) ? c->rope.rotary_dim
+                                                                       : c->head_dim;
+}
+
 // Middle slots per unit in every middle buffer: the capacity rounded up to 64 slots.
 inline int mid_stride(const fade_config_t* c) { return (c->mid_capacity + 63) / 64 * 64; }
 

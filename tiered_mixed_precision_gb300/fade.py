@@ -46,7 +46,8 @@ c_i32, c_i64, c_f32, c_f64, c_sz, c_vp = (ctypes.c_int32, ctypes.c_int64, ctypes
 
 class RopeT(ctypes.Structure):
     _fields_ = [("kind", c_i32), ("original_max_position", c_i32), ("base", c_f64),
-                ("factor", c_f64), ("low_freq_factor", c_f64), ("high_freq_factor", c_f64)]
+                ("factor", c_f64), ("low_freq_factor", c_f64), ("high_freq_factor", c_f64),
+                ("rotary_dim", c_i32)]
 
 
 class ConfigT(ctypes.Structure):
@@ -179,6 +180,7 @@ class Config:
     rope_low_freq_factor: float = 1.0
     rope_high_freq_factor: float = 4.0
     rope_original_max_position: int = 8192
+    rope_rotary_dim: int = 0   # proportional RoPE: rotated channels (0 = every channel)
     shared_rows: bool = False  # the rows share their tier decisions (row-summed scores)
     v_codec: str = "int"       # "pq": product-quantised middle V (needs middle_v_bits = 2)
     _c: ConfigT = field(default=None, init=False, repr=False, compare=False)
@@ -193,7 +195,7 @@ class Config:
         if self._c is None:
             r = RopeT(ROPE_KINDS[self.rope_kind], self.rope_original_max_position,
                       self.rope_base, self.rope_factor, self.rope_low_freq_factor,
-                      self.rope_high_freq_factor)
+                      self.rope_high_freq_factor, self.rope_rotary_dim)
             object.__setattr__(self, "_c", ConfigT(
                 self.batch, self.num_q_heads, self.num_kv_heads, self.head_dim, self.n_sink,
                 self.recent_window, self.int4_budget, self.middle_k_bits, self.middle_v_bits,
@@ -222,7 +224,8 @@ class Config:
         return cls(batch or wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.n_sink,
                    wl.recent_window, wl.int4_budget, wl.middle_k_bits, wl.middle_v_bits,
                    mid_capacity, wl.policy, wl.ema_decay, r.kind, r.base, r.factor,
-                   r.low_freq_factor, r.high_freq_factor, r.original_max_position)
+                   r.low_freq_factor, r.high_freq_factor, r.original_max_position,
+                   getattr(r, "rotary_dim", 0))
 
 
 def preset(name: str, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,

@@ -77,7 +77,7 @@ class FadeCache:
                       "recent_window", "int4_budget", "middle_k_bits", "middle_v_bits",
                       "mid_capacity", "policy", "ema_decay", "rope_kind", "rope_base",
                       "rope_factor", "rope_low_freq_factor", "rope_high_freq_factor",
-                      "rope_original_max_position", "shared_rows", "v_codec")
+                      "rope_original_max_position", "rope_rotary_dim", "shared_rows", "v_codec")
 
     def cache_state_dict(self) -> dict:
         """Every layer's tier buffers (both middle buffers and the device metadata, which says
