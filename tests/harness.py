@@ -29,6 +29,69 @@ def allclose_report(got, ref, atol=ATOL, rtol=RTOL):
     return (not bad.any()), float(err.max(initial=0.0)), int(bad.sum())
 
 
+def victims_from_bits(words, n_mid):
+    """Victim middle indices from a unit's selection bitmap words (bit i = index i)."""
+    words = np.ascontiguousarray(words[:(n_mid + 31) // 32], np.uint32)
+    bits = np.unpackbits(words.view(np.uint8), bitorder="little")[:n_mid]
+    return np.nonzero(bits)[0]
+
+
+def oracle_unit_step(u, t, b, h, G, policy, gpu_words=None, evict=True):
+    """One decode step of oracle unit ``u`` (layer row b, KV head h) on the raw draws ``t``
+    (q [B][Hq][d], k, v [B][Hkv][d]): demote, evict, append, attend, accumulate. Under H2O /
+    EMA the oracle's own fp64 selection is compared with the GPU's victims (``gpu_words``, the
+    unit's selection bitmap); where they differ they must be a near-tie, and the oracle then
+    adopts the GPU's victims (R10) and the unit stays under comparison.
+    Returns (attention output [G, d] fp64, whether a near-tie was adopted)."""
+    u.demote()
+    n_mid = u.n_mid
+    vic = u.choose_victims() if evict else np.zeros(0, np.int64)
+    tie = False
+    if vic.size and policy in ("h2o", "ema") and gpu_words is not None:
+        gpu_vic = victims_from_bits(gpu_words, n_mid)
+        if not np.array_equal(np.sort(gpu_vic), np.sort(vic)):
+            keys = u.sigma[u.n_sink:u.n_sink + n_mid]
+            a, g = np.sort(keys[vic]), np.sort(keys[gpu_vic])
+            assert gpu_vic.size == vic.size and np.allclose(a, g, rtol=TIE_RTOL, atol=1e-7), (
+                f"selection differs beyond a near-tie at row {b} head {h}: oracle {vic} {a}, "
+                f"gpu {gpu_vic} {g}")
+            vic = gpu_vic
+            tie = True
+    if evict:
+        u.evict(vic)
+    pos = u.n_held
+    u.append(u.rope.apply(t["k"][b, h][None], pos), t["v"][b, h])
+    out, p, _ = u.attend(u.rope.apply(t["q"][b, h * G:(h + 1) * G], pos))
+    u.accumulate(p)
+    return out, tie
+
+
+def compare_unit_state(g, u, where):
+    """A unit's GPU tiers (``g``, cache order) against the oracle unit: counts, FP16 tiers,
+    packed codes and scales bit for bit; scores within the tolerance."""
+    assert (g["n_sink"], g["n_mid"], g["n_recent"]) == (u.n_sink, u.n_mid, u.n_recent), \
+        f"tier counts differ at {where}: gpu {(g['n_sink'], g['n_mid'], g['n_recent'])} " \
+        f"oracle {(u.n_sink, u.n_mid, u.n_recent)}"
+    eq16 = lambda a, r: np.array_equal(np.asarray(a).view(np.uint16), np.asarray(r).view(np.uint16))
+    assert eq16(g["sink_k"], u.sink_k) and eq16(g["sink_v"], u.sink_v), f"sinks differ at {where}"
+    assert eq16(g["recent_v"], u.rec_v), f"recent V differs at {where}"
+    if not eq16(g["recent_k"], u.rec_k):
+        d = np.nonzero(np.asarray(g["recent_k"]).view(np.uint16) != u.rec_k.view(np.uint16))
+        raise AssertionError(f"recent K differs at {where}: {len(d[0])} entries, first {d[0][:5]}")
+    kc = quant.pack(u.mid_kq, u.p.k_bits)
+    vc = u.mid_vq if u.p.v_codec == "pq" else quant.pack(u.mid_vq, u.p.v_bits)
+    for name, got, ref in (("mid K codes", g["mid_k_codes"], kc),
+                           ("mid V codes", g["mid_v_codes"], vc)):
+        if not np.array_equal(got, ref):
+            rows = np.nonzero((got != ref).any(-1))[0]
+            raise AssertionError(f"{name} differ at {where}: rows {rows[:8]} of {len(rows)}")
+    assert eq16(g["mid_k_scales"], u.mid_ks), f"mid K scales differ at {where}"
+    assert eq16(g["mid_v_scales"], u.mid_vs), f"mid V scales differ at {where}"
+    if u.p.policy in ("h2o", "ema"):
+        ok, err, nbad = allclose_report(g["scores"], u.sigma)
+        assert ok, f"scores differ at {where}: max err {err}, {nbad} bad"
+
+
 class Lockstep:
     """Drives ``FadeCache`` and per-unit oracle caches over a workload."""
 
@@ -294,33 +357,8 @@ class Lockstep:
             out, p, _ = u.attend(u.rope.apply(t["q"][b, h * G:(h + 1) * G], pos))
             u.accumulate(p)
             return out, False
-        u.demote()
-        n_mid = u.n_mid
-        vic = u.choose_victims() if evict else np.zeros(0, np.int64)
-        tie = False
-        if vic.size and self.wl.policy in ("h2o", "ema"):
-            words = bm[b, h, :(n_mid + 31) // 32]
-            bits = np.unpackbits(words.view(np.uint8), bitorder="little")[:n_mid]
-            gpu_vic = np.nonzero(bits)[0]
-            if not np.array_equal(np.sort(gpu_vic), np.sort(vic)):
-                keys = u.sigma[u.n_sink:u.n_sink + n_mid]
-                a, g = np.sort(keys[vic]), np.sort(keys[gpu_vic])
-                assert gpu_vic.size == vic.size and np.allclose(
-                    a, g, rtol=TIE_RTOL, atol=1e-7), (
-                    f"selection differs beyond a near-tie at {key}: oracle {vic} {a}, "
-                    f"gpu {gpu_vic} {g}")
-                # R10: at an fp32-vs-fp64 near-tie the oracle adopts the GPU's victims (which
-                # the selection replay has shown to be the rule applied to the GPU's own
-                # keys) and the unit stays under comparison
-                self.near_ties += 1
-                vic = gpu_vic
-                tie = True
-        if evict:
-            u.evict(vic)
-        pos = u.n_held
-        u.append(u.rope.apply(t["k"][b, h][None], pos), t["v"][b, h])
-        out, p, _ = u.attend(u.rope.apply(t["q"][b, h * G:(h + 1) * G], pos))
-        u.accumulate(p)
+        out, tie = oracle_unit_step(u, t, b, h, G, self.wl.policy, bm[b, h], evict)
+        self.near_ties += tie
         return out, tie
 
     def check_near_ties(self, frac=0.01, floor=1):
@@ -339,27 +377,5 @@ class Lockstep:
                 self.check_unit_state(layer, b, h)
 
     def check_unit_state(self, layer, b, h):
-        g = self.fc.unit_state(layer, b, h)
-        u = self.units[layer][b][h]
-        where = f"layer {layer} row {b} head {h} step {self.step_index}"
-        assert (g["n_sink"], g["n_mid"], g["n_recent"]) == (u.n_sink, u.n_mid, u.n_recent), \
-            f"tier counts differ at {where}: gpu {(g['n_sink'], g['n_mid'], g['n_recent'])} " \
-            f"oracle {(u.n_sink, u.n_mid, u.n_recent)}"
-        eq16 = lambda a, r: np.array_equal(np.asarray(a).view(np.uint16), np.asarray(r).view(np.uint16))
-        assert eq16(g["sink_k"], u.sink_k) and eq16(g["sink_v"], u.sink_v), f"sinks differ at {where}"
-        assert eq16(g["recent_v"], u.rec_v), f"recent V differs at {where}"
-        if not eq16(g["recent_k"], u.rec_k):
-            d = np.nonzero(g["recent_k"].view(np.uint16) != u.rec_k.view(np.uint16))
-            raise AssertionError(f"recent K differs at {where}: {len(d[0])} entries, first {d[0][:5]}")
-        kc = quant.pack(u.mid_kq, u.p.k_bits)
-        vc = u.mid_vq if u.p.v_codec == "pq" else quant.pack(u.mid_vq, u.p.v_bits)
-        for name, got, ref in (("mid K codes", g["mid_k_codes"], kc),
-                               ("mid V codes", g["mid_v_codes"], vc)):
-            if not np.array_equal(got, ref):
-                rows = np.nonzero((got != ref).any(-1))[0]
-                raise AssertionError(f"{name} differ at {where}: rows {rows[:8]} of {len(rows)}")
-        assert eq16(g["mid_k_scales"], u.mid_ks), f"mid K scales differ at {where}"
-        assert eq16(g["mid_v_scales"], u.mid_vs), f"mid V scales differ at {where}"
-        if self.wl.policy in ("h2o", "ema"):
-            ok, err, nbad = allclose_report(g["scores"], u.sigma)
-            assert ok, f"scores differ at {where}: max err {err}, {nbad} bad"
+        compare_unit_state(self.fc.unit_state(layer, b, h), self.units[layer][b][h],
+                           f"layer {layer} row {b} head {h} step {self.step_index}")

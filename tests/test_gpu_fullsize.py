@@ -1,7 +1,7 @@
 """Parity at the full per-layer sizes of the throughput workloads, in the launch configuration
 the benchmark times (full batch, heads and context of one layer): sampled (row, KV head)
 units are replayed by the oracle from the same raw draws and compared after prefill and after
-each decode step."""
+each of 16 decode steps (every step evicts and re-positions the whole middle tier)."""
 
 import numpy as np
 import pytest
@@ -37,7 +37,7 @@ def test_full_size_layer_sampled_units(key):
     from tiered_mixed_precision_gb300.model import FadeCache
 
     wl = get_workload(key)
-    steps = 2
+    steps = 16
     cfg = T.Config.from_workload(wl)
     lens = ragged_context_lengths(wl)
     maxP = int(lens.max())
@@ -90,7 +90,7 @@ def test_full_size_pipelined_graph_sampled_units(key):
     from tiered_mixed_precision_gb300.model import FadeCache
 
     wl = get_workload(key)
-    steps = 2
+    steps = 16
     cfg = T.Config.from_workload(wl)
     lens = ragged_context_lengths(wl)
     maxP = int(lens.max())
