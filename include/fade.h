@@ -201,7 +201,8 @@ typedef struct {
   size_t logits_ws;   /* f32 [B][Hq][S + C + W]: per-token logits for H2O / EMA */
   int32_t mid_stride;  /* C: middle slots per unit in every middle buffer */
   size_t ml_ws;       /* f32 [B][Hq][2]: final (max, sum) of each query head's softmax */
-  size_t attn_ws;     /* split-KV partials for fade_decode_attention */
+  size_t attn_ws;     /* split-KV partials for fade_decode_attention (and one i32 partial
+                         count per unit) */
   int32_t victim_words;  /* u32 words per unit in `victims` */
   int32_t chunk_slots;   /* i32 entries per unit in `chunk_base` */
   int32_t max_prompt;    /* the prompt length the scratch sizes were computed for */
@@ -381,7 +382,8 @@ fade_status_t fade_decode_attention(const fade_config_t* cfg, const fade_layer_t
  *   - All calls on a device share the one array, which keeps the last call's contents. Calls
  *     that overlap on the GPU (unordered streams) race; order them, e.g. on one stream. No part
  *     of the array needs to start at zero: each call writes every partial before reading it.
- *   - A shape whose partials (B * Hq * splits * (d + 2) * 4 bytes) exceed the array is
+ *   - A shape whose partials (B * Hq * splits * (d + 2) * 4 bytes, plus 4 bytes per unit)
+ *     exceed the array is
  *     rejected on the host with FADE_ERR_CAPACITY and a message naming the limit.
  *   - It allocates nothing: no cudaMalloc, cudaFree or allocating library routine. */
 fade_status_t fade_decode_attention_noalloc(const fade_config_t* cfg, const fade_layer_t* layer,

@@ -147,7 +147,7 @@ extern "C" fade_status_t fade_layout(const fade_config_t* c, int32_t max_prompt,
   o->logits_ws = B * Hq * (S + C + W) * 4;
   o->ml_ws = B * Hq * 2 * 4;
   o->max_splits = 1 + ceil_div((long long)C, kMinSplitTokens);
-  o->attn_ws = B * Hq * (size_t)o->max_splits * (d + 2) * 4;
+  o->attn_ws = B * Hq * (size_t)o->max_splits * (d + 2) * 4 + units * 4;
   o->max_prompt = max_prompt;
   o->mid_stride = (int32_t)C;
   o->prefill_mass_ws = B * Hq * (size_t)max_prompt * 8;

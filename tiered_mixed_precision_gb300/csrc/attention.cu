@@ -26,6 +26,7 @@ struct AttnArgs {
   float* logits;                        // nullable, [B][Hq][NS]
   float* part_ml;                       // [B][Hq][nsplit][2]
   float* part_acc;                      // [B][Hq][nsplit][D]
+  const int32_t* seg_count;             // [B][H]: partials of each unit (stream-K combine)
   int Hq, H, S, W, C, NS, chunk, nsplit;
   float scale;                          // 1/sqrt(D)
   const uint16_t* pq_cb;                // PQ-coded V: the layer's codebook [D/4][256][4]
@@ -360,70 +361,82 @@ __global__ void __launch_bounds__(D) attn_combine_kernel(AttnArgs a, uint16_t* _
 }
 
 // The tensor-core kernel's partials (split 0 + one per stream-K segment of the unit): one CTA of
-// G x D threads per unit (row, KV head). The unit's segment count comes once from the schedule;
-// every segment's (m, l) is loaded at once into shared memory, warp h reduces head h's
-// M = max m_s, its weights e^(m_s - M) and L = sum l_s e^(m_s - M), then thread (h, c) sums
-// channel c of the weighted partial outputs: out = sum acc_s e^(m_s - M) / L.
+// One CTA per unit (row, KV head), one warp per query head, D/32 channels per lane. No
+// shared memory and no barrier: every lane reads the unit's partial count and the head's
+// (m, l) of every partial (the same addresses across the warp), forms M = max m_s, the
+// weights e^(m_s - M) and L = sum l_s e^(m_s - M) itself, and sums its channels of the
+// weighted partial outputs: out = sum acc_s e^(m_s - M) / L. The first kPre partials are
+// loaded before the count is known (slots below nsplit are in bounds).
 template <int D>
-__global__ void __launch_bounds__(1024) attn_combine_sk_kernel(AttnArgs a,
-                                                               uint16_t* __restrict__ out,
-                                                               float* __restrict__ ml,
-                                                               const __grid_constant__ StreamK sk) {
-  constexpr int kMaxSeg = kMaxCtaSK + 1;
-  constexpr int kPre = 8;            // partials a thread loads before the weights are known
-  __shared__ float s_w[8][kMaxSeg];  // m_s, then the weight e^(m_s - M)
-  __shared__ float s_l[8][kMaxSeg];
-  __shared__ float s_L[8];
+__global__ void __launch_bounds__(256) attn_combine_sk_kernel(AttnArgs a,
+                                                              uint16_t* __restrict__ out,
+                                                              float* __restrict__ ml) {
+  constexpr int CPL = D / 32;       // channels per lane
+  constexpr int kPre = 4;
   const int unit = blockIdx.x;
   const int b = unit / a.H, hk = unit % a.H;
   const int G = a.Hq / a.H;
-  const int tid = threadIdx.x;
-  const size_t bh0 = (size_t)b * a.Hq + hk * G;
-  // this thread's channel of its head: the first partials are loaded at once, so that their
-  // latency overlaps the (m, l) loads and the weights below (slots below nsplit are in
-  // bounds; only the unit's first ns are used)
-  const int h = tid / D, c = tid % D;
-  const float* pa = a.part_acc + (bh0 + h) * a.nsplit * D + c;
-  float pre[kPre];
+  const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t bh = (size_t)b * a.Hq + hk * G + h;
+  const float* pa = a.part_acc + bh * a.nsplit * D + CPL * lane;
+  const float* pm = a.part_ml + bh * a.nsplit * 2;
+  // launched as a programmatic dependent of the attention kernel: this CTA may start while
+  // the attention grid's last CTAs still run; wait here until that grid has completed and its
+  // partials are visible (a no-op when launched without the dependency)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int ns = max(1, min(a.nsplit, a.seg_count[unit]));
+  float acc[kPre][CPL], mv[kPre], lv[kPre];
 #pragma unroll
-  for (int i = 0; i < kPre; ++i) pre[i] = i < a.nsplit ? pa[(size_t)i * D] : 0.f;
-  const int ns = min(a.nsplit, min(kMaxSeg, 1 + sk_segments(sk, b, hk)));
-  const int warp = tid >> 5, lane = tid & 31;
-  if (warp < G) {  // warp hh: head hh's max over the segments, their weights and total mass
-    const int hh = warp;
-    const float* pm = a.part_ml + (bh0 + hh) * a.nsplit * 2;
-    float M = -INFINITY;
-    for (int sg = lane; sg < ns; sg += 32) {
-      const float m = pm[2 * sg];
-      s_w[hh][sg] = m;
-      s_l[hh][sg] = pm[2 * sg + 1];
-      M = fmaxf(M, m);
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float Lp = 0.f;
-    for (int sg = lane; sg < ns; sg += 32) {  // entries this lane wrote itself
-      const float m = s_w[hh][sg];
-      const float w = (m == -INFINITY) ? 0.f : __expf(m - M);
-      s_w[hh][sg] = w;
-      Lp = fmaf(s_l[hh][sg], w, Lp);
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) Lp += __shfl_xor_sync(0xffffffffu, Lp, o);
-    if (lane == 0) {
-      s_L[hh] = Lp;
-      ml[2 * (bh0 + hh)] = M;
-      ml[2 * (bh0 + hh) + 1] = Lp;
+  for (int i = 0; i < kPre; ++i) {
+    const bool in = i < a.nsplit;
+    mv[i] = in ? pm[2 * i] : -INFINITY;
+    lv[i] = in ? pm[2 * i + 1] : 0.f;
+    if constexpr (CPL == 4) {
+      const float4 v = in ? *reinterpret_cast<const float4*>(pa + (size_t)i * D)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+      acc[i][0] = v.x; acc[i][1] = v.y; acc[i][2] = v.z; acc[i][3] = v.w;
+    } else {
+      const float2 v = in ? *reinterpret_cast<const float2*>(pa + (size_t)i * D)
+                          : make_float2(0.f, 0.f);
+      acc[i][0] = v.x; acc[i][1] = v.y;
     }
   }
-  __syncthreads();
-  float o = 0.f;
+  float M = -INFINITY;
 #pragma unroll
   for (int i = 0; i < kPre; ++i)
-    if (i < ns) o = fmaf(pre[i], s_w[h][i], o);
-#pragma unroll 4
-  for (int sg = kPre; sg < ns; ++sg) o = fmaf(pa[(size_t)sg * D], s_w[h][sg], o);
-  out[(bh0 + h) * D + c] = f2h(o / s_L[h]);
+    if (i < ns) M = fmaxf(M, mv[i]);
+  for (int s = kPre; s < ns; ++s) M = fmaxf(M, pm[2 * s]);
+  float L = 0.f, o[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) o[c] = 0.f;
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) {
+    if (i < ns) {
+      const float w = (mv[i] == -INFINITY) ? 0.f : __expf(mv[i] - M);
+      L = fmaf(lv[i], w, L);
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) o[c] = fmaf(acc[i][c], w, o[c]);
+    }
+  }
+  for (int s = kPre; s < ns; ++s) {
+    const float m = pm[2 * s];
+    const float w = (m == -INFINITY) ? 0.f : __expf(m - M);
+    L = fmaf(pm[2 * s + 1], w, L);
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) o[c] = fmaf(pa[(size_t)s * D + c], w, o[c]);
+  }
+  if (lane == 0) {
+    ml[2 * bh] = M;
+    ml[2 * bh + 1] = L;
+  }
+  uint16_t r[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) r[c] = f2h(o[c] / L);
+  if constexpr (CPL == 4)
+    *reinterpret_cast<uint2*>(out + bh * D + CPL * lane) =
+        make_uint2(r[0] | ((uint32_t)r[1] << 16), r[2] | ((uint32_t)r[3] << 16));
+  else
+    *reinterpret_cast<uint32_t*>(out + bh * D + CPL * lane) = r[0] | ((uint32_t)r[1] << 16);
 }
 
 struct AccArgs {
@@ -594,31 +607,48 @@ extern "C" fade_status_t fade_decode_attention(const fade_config_t* c, const fad
   }
   a.scale = 1.0f / sqrtf((float)c->head_dim);
   a.pq_cb = L->pq_codebook;
-  const size_t need = (size_t)c->batch * c->num_q_heads * a.nsplit * (c->head_dim + 2) * 4;
+  const size_t part = (size_t)c->batch * c->num_q_heads * a.nsplit * (c->head_dim + 2) * 4;
+  const size_t need = part + (size_t)units * 4;
   if (ws_bytes < need)
     return set_error(FADE_ERR_CAPACITY, "attention workspace %zu bytes, %zu needed", ws_bytes,
                      need);
   a.part_ml = reinterpret_cast<float*>(ws);
   a.part_acc = a.part_ml + (size_t)c->batch * c->num_q_heads * a.nsplit * 2;
+  int32_t* seg_count = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + part);
+  a.seg_count = seg_count;
   cudaStream_t s = as_stream(stream);
   if (mma) {
     // one launch: FP16 tiers (split 0) and the packed middle tier (tensor cores)
-    if ((st = launch_mid_mma(c, L, q_rot, logits_ws, a.part_ml, a.part_acc, sk, a.nsplit, s)))
+    if ((st = launch_mid_mma(c, L, q_rot, logits_ws, a.part_ml, a.part_acc, seg_count, sk,
+                             a.nsplit, s)))
       return st;
   } else if ((st = launch_split_any(c, a, s, a.nsplit))) {
     return st;
   }
   const int bh = c->batch * c->num_q_heads;
-  if (c->head_dim == 64) {
-    if (mma)
-      attn_combine_sk_kernel<64><<<units, 64 * (a.Hq / a.H), 0, s>>>(a, out, ml_ws, sk);
-    else
-      attn_combine_kernel<64><<<bh, 64, 0, s>>>(a, out, ml_ws);
+  if (mma) {
+    // the combine launches as a programmatic dependent of the attention kernel (its CTAs are
+    // scheduled while the attention grid drains and wait on the device for its completion)
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(units);
+    lc.blockDim = dim3(32 * (a.Hq / a.H));
+    lc.dynamicSmemBytes = 0;
+    lc.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    const cudaError_t e =
+        c->head_dim == 64
+            ? cudaLaunchKernelEx(&lc, attn_combine_sk_kernel<64>, a, out, ml_ws)
+            : cudaLaunchKernelEx(&lc, attn_combine_sk_kernel<128>, a, out, ml_ws);
+    if (e != cudaSuccess)
+      return set_error(FADE_ERR_CUDA, "fade_decode_attention combine: %s", cudaGetErrorString(e));
+  } else if (c->head_dim == 64) {
+    attn_combine_kernel<64><<<bh, 64, 0, s>>>(a, out, ml_ws);
   } else {
-    if (mma)
-      attn_combine_sk_kernel<128><<<units, 128 * (a.Hq / a.H), 0, s>>>(a, out, ml_ws, sk);
-    else
-      attn_combine_kernel<128><<<bh, 128, 0, s>>>(a, out, ml_ws);
+    attn_combine_kernel<128><<<bh, 128, 0, s>>>(a, out, ml_ws);
   }
   return launch_status("fade_decode_attention combine");
 }

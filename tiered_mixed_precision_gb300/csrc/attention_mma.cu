@@ -93,6 +93,7 @@ struct MmaArgs {
   float* part_ml;                    // [B][Hq][nsplit][2]
   float* part_acc;                   // [B][Hq][nsplit][D]
   int32_t* status;
+  int32_t* seg_count;                // [B][H]: partials of each unit (split 0 + segments)
   int B, Hq, H, S, W, C, NS, chunk, nsplit;
   float inv_sqrt_d;
   const uint16_t* pq_cb;             // PQ-coded V: the layer's codebook [D/4][256][4]
@@ -724,6 +725,9 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
   }
   __syncthreads();
   volatile int* abort = &s_abort;
+  // the combine kernel that follows is a programmatic dependent: let it be scheduled now (its
+  // CTAs take SM slots as this grid's CTAs exit and wait on the device for this grid's end)
+  asm volatile("griddepcontrol.launch_dependents;");
 
   if (warp == kConsumers) {
     // ------------------------------------------------------------ producer
@@ -792,13 +796,20 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
         return true;
       };
       bool go = true;
-      for (int u = cta; u < units && go; u += P) go = issue_item(u, 0, 0, f16_staged ? 2 : 1);
+      // every unit's partial count for the combine: 1 (split 0) for a unit without middle
+      // tiles, written with its FP16 item; else 2 + k, written by the CTA (rank k) that holds
+      // the unit's last tile
+      for (int u = cta; u < units && go; u += P) {
+        if (sk_row_tiles(sk, u / a.H) == 0) a.seg_count[u] = 1;
+        go = issue_item(u, 0, 0, f16_staged ? 2 : 1);
+      }
       SkPos pos = p0;
       for (int g = g0; g < g1 && go;) {
         const int rt = sk_row_tiles(sk, pos.b);
         const int run = min(g1 - g, rt - pos.tile);
         // this CTA's rank among the CTAs holding tiles of the unit
         const int k = sk_nonempty(sk, sk_cta_of(sk, g - pos.tile), cta - 1);
+        if (pos.tile + run == rt) a.seg_count[pos.b * a.H + pos.h] = 2 + k;
         go = issue_item(pos.b * a.H + pos.h, 1 + k, pos.tile, run);
         g += run;
         sk_advance(sk, pos, run);
@@ -1318,8 +1329,8 @@ void build_stream_k(const fade_config_t* c, const fade_layer_t* L, int ctas, Str
 }
 
 fade_status_t launch_mid_mma(const fade_config_t* c, const fade_layer_t* L, const uint16_t* q,
-                             float* logits, float* part_ml, float* part_acc, const StreamK& sk,
-                             int nsplit, cudaStream_t st) {
+                             float* logits, float* part_ml, float* part_acc, int32_t* seg_count,
+                             const StreamK& sk, int nsplit, cudaStream_t st) {
   MmaArgs a;
   a.q = q;
   a.sink_k = L->sink_k;
@@ -1335,6 +1346,7 @@ fade_status_t launch_mid_mma(const fade_config_t* c, const fade_layer_t* L, cons
   a.logits = logits;
   a.part_ml = part_ml;
   a.part_acc = part_acc;
+  a.seg_count = seg_count;
   a.status = L->status;
   a.B = c->batch;
   a.Hq = c->num_q_heads;

@@ -93,8 +93,8 @@ int mid_mma_ctas(const fade_config_t* c);
 // The schedule for the layer's current middle-tier counts (host mirrors).
 void build_stream_k(const fade_config_t* c, const fade_layer_t* L, int ctas, StreamK* k);
 fade_status_t launch_mid_mma(const fade_config_t* c, const fade_layer_t* L, const uint16_t* q,
-                             float* logits, float* part_ml, float* part_acc, const StreamK& sk,
-                             int nsplit, cudaStream_t st);
+                             float* logits, float* part_ml, float* part_acc, int32_t* seg_count,
+                             const StreamK& sk, int nsplit, cudaStream_t st);
 
 // ---------------------------------------------------------------- device side
 __device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
