@@ -425,6 +425,16 @@ fade_status_t fade_check_status(const fade_layer_t* layer, void* stream);
 fade_status_t fade_selftest_bounded_wait(int32_t* status, int32_t producer_arrives,
                                          int64_t limit_cycles, void* stream);
 
+/* Measurement helper (no counterpart in the pages; it serves the roofline of
+ * fade_evict_rerope, whose cost is fp32 arithmetic): launches `blocks` CTAs of 256 threads in
+ * which every thread runs `iters` rounds of eight independent chains of packed fp32 multiplies
+ * (mul.rn.f32x2, two separately rounded fp32 operations per lane per instruction) on
+ * registers. *ops_out (host, may be NULL) receives the fp32 operations the launch performs;
+ * timed with events on `stream` this is the device's rate of separately rounded fp32
+ * operations. sink: device f32 [256], never written in practice (keeps the chains alive). */
+fade_status_t fade_measure_fp32_rate(int32_t blocks, int32_t iters, float* sink,
+                                     double* ops_out, void* stream);
+
 /* The calling thread's last error message ("" if none). */
 const char* fade_last_error(void);
 

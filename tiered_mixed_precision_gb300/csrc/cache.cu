@@ -12,6 +12,10 @@ namespace fade {
 namespace {
 
 constexpr int kSelThreads = kChunk;  // one selection CTA covers one chunk per pass
+// Resident CTAs per SM the compaction kernel is compiled for (its register budget).
+#ifndef FADE_COMPACT_MINB
+#define FADE_COMPACT_MINB 2
+#endif
 constexpr int kF = FADE_META_FIELDS;
 
 // Unsigned key whose order is the float order (-0 and +0 equal).
@@ -798,7 +802,7 @@ __device__ __forceinline__ void stg_words(void* p, const uint32_t (&w)[W]) {
 // words are staged in shared memory with their prefix counts; false: the code for every policy,
 // with the victims' prefix read from the bitmap per token (the position policy's instantiation).
 template <int D, int KB, int VB, bool SEL>
-__global__ void __launch_bounds__(256, 2) evict_compact_kernel(LayerArgs a) {
+__global__ void __launch_bounds__(256, FADE_COMPACT_MINB) evict_compact_kernel(LayerArgs a) {
   using CC = MidCfg<D>;
   using TD = MidToken<D, KB, VB>;
   constexpr int PRE = SEL ? CC::PRE_SEL : CC::PRE;

@@ -116,6 +116,7 @@ def lib():
             "fade_pq_decode": (c_i32, [c_vp, c_vp, c_i64, c_i32, c_vp, c_vp]),
             "fade_pq_train": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp]),
             "fade_check_status": (c_i32, [S(LayerT), c_vp]),
+            "fade_measure_fp32_rate": (c_i32, [c_i32, c_i32, c_vp, ctypes.POINTER(c_f64), c_vp]),
             "fade_selftest_bounded_wait": (c_i32, [c_vp, c_i32, c_i64, c_vp]),
             "fade_last_error": (ctypes.c_char_p, []),
         }
@@ -458,3 +459,11 @@ def fade_selftest_bounded_wait(status, producer_arrives: bool, limit_cycles: int
     """Launch the bounded-wait self-test kernel (status: a device int32 tensor)."""
     _check(lib().fade_selftest_bounded_wait(_ptr(status), int(bool(producer_arrives)),
                                             int(limit_cycles), _stream(stream)))
+
+
+def fade_measure_fp32_rate(blocks: int, iters: int, sink, stream=None) -> float:
+    """Launch the fp32-rate measurement kernel; returns the fp32 operations it performs."""
+    ops = c_f64(0.0)
+    _check(lib().fade_measure_fp32_rate(int(blocks), int(iters), _ptr(sink), ctypes.byref(ops),
+                                        _stream(stream)))
+    return ops.value
