@@ -49,7 +49,8 @@ typedef enum {
   FADE_ERR_UNSUPPORTED = 2,      /* a valid configuration this build does not implement */
   FADE_ERR_CAPACITY = 3,         /* a tier or workspace would overflow its buffer */
   FADE_ERR_CUDA = 4,             /* a CUDA call or kernel launch failed */
-  FADE_ERR_TIMEOUT = 5           /* a kernel gave up a bounded wait (fade_check_status) */
+  FADE_ERR_TIMEOUT = 5,          /* a kernel gave up a bounded wait (fade_check_status) */
+  FADE_ERR_DEVICE_CHECK = 6      /* a device-side index check failed (fade_check_status) */
 } fade_status_t;
 
 /* RoPE schemes (FADE-zh §RoPE方案兼容性: standard RoPE and the scaling types llama3, linear,
@@ -402,6 +403,11 @@ fade_status_t fade_h2o_accumulate(const fade_config_t* cfg, fade_layer_t* layer,
  * demotion and eviction (KVLong §1.2.2: positions inside the cache). -1 on bad arguments. */
 int32_t fade_next_position(const fade_config_t* cfg, const fade_layer_t* layer, int32_t row);
 
+/* Host: the layer's tier counts from the host mirror (FADE-zh §遥测与调试: tokens per tier):
+ * out = HOST i32 [B][3] = (sinks, middle, recent) of every row (the same for all KV heads). */
+fade_status_t fade_tier_counts(const fade_config_t* cfg, const fade_layer_t* layer,
+                               int32_t* out);
+
 /* Host: KV bytes held by the layer (FADE-zh §使用注意事项 3, compressed_storage_bytes: KV
  * storage only): FP16 tokens at 4d bytes, middle tokens at d*(kb+vb)/8 code bytes plus two
  * fp16 scales per 32 channels. */
@@ -410,10 +416,12 @@ uint64_t fade_compressed_bytes(const fade_config_t* cfg, const fade_layer_t* lay
 /* Host, synchronising: wait for the work queued on `stream`, then read the layer's device
  * status words. FADE_ERR_TIMEOUT if a kernel of this layer gave up a bounded wait since the
  * last fade_cache_reset (every wait on an mbarrier or a bulk copy is bounded, about 2 s; the
- * kernel then records a code in status[0] and returns instead of hanging; the results of
- * the calls since are invalid); FADE_ERR_CUDA if the stream reports an error; FADE_OK
- * otherwise. The asynchronous calls never read the status words: this is the call that
- * turns them into an error. */
+ * kernel then records a code in status[0] and returns instead of hanging);
+ * FADE_ERR_DEVICE_CHECK if a kernel's index guard failed (codes >= 16: the guard skips the
+ * access and records its code; a library built with FADE_DEBUG=1 adds such guards on every
+ * compacted row and attention tile); in both cases the results of the calls since are
+ * invalid. FADE_ERR_CUDA if the stream reports an error; FADE_OK otherwise. The asynchronous
+ * calls never read the status words: this is the call that turns them into an error. */
 fade_status_t fade_check_status(const fade_layer_t* layer, void* stream);
 
 /* Self-test of the bounded waits: one kernel in which a consumer waits on an mbarrier with

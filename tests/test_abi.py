@@ -192,3 +192,26 @@ def test_advance_host_follows_the_oracle_counts(T, policy, budget):
             T.fade_cache_advance_host(full)
         assert e.value.status == 3
         assert (full.h_n_sink[0], full.h_n_mid[0], full.h_n_recent[0]) == (2, layer.h_n_mid[0], 4)
+
+
+def test_tier_counts_query_reads_the_host_mirror(T):
+    cfg = _cfg(T, batch=3)
+    layer = T.TieredLayer(cfg, 16, device="cpu")
+    for b, (s, m, r) in enumerate([(4, 0, 10), (4, 350, 64), (2, 0, 0)]):
+        layer.h_n_sink[b], layer.h_n_mid[b], layer.h_n_recent[b] = s, m, r
+    got = T.fade.fade_tier_counts(layer)
+    assert got.tolist() == [[4, 0, 10], [4, 350, 64], [2, 0, 0]]
+
+
+def test_debug_build_compiles_and_exports_every_symbol():
+    """The FADE_DEBUG=1 variant (device index checks on the hot paths) builds in its own
+    directory and exports the same entry points."""
+    import torch  # noqa: F401
+
+    from tiered_mixed_precision_gb300 import build
+
+    path = build.build(debug=True)
+    assert path.endswith(os.path.join("_build_debug", "libfade.so"))
+    lib = ctypes.CDLL(path)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported by the debug build: {missing}"

@@ -17,6 +17,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")   # FADE_DEBUG=1: device checks on hot paths
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(BUILD, "libfade.so")
 
@@ -49,14 +50,20 @@ def _headers():
     return hs
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
-    """Compile every .cu under csrc/ and link libfade.so; returns the library path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile every .cu under csrc/ and link libfade.so; returns the library path. debug:
+    the FADE_DEBUG=1 variant (index checks on every compacted row and attention tile that
+    record a code in the layer's status word) in its own directory."""
+    out_dir = BUILD_DEBUG if debug else BUILD
+    lib_path = os.path.join(out_dir, "libfade.so")
+    if debug:
+        extra_flags = (*extra_flags, "-DFADE_DEBUG=1")
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     hdrs = _headers()
     objs, jobs = [], []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src, *hdrs, __file__]):
             cmd = [nvcc, *ARCH, *NVFLAGS, *extra_flags, "-c", src, "-o", obj]
@@ -74,10 +81,10 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
             list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        run([nvcc, *ARCH, "-shared", "-cudart", "shared", *objs, "-o", LIB])
-    return LIB
+    if force or jobs or _stale(lib_path, objs):
+        run([nvcc, *ARCH, "-shared", "-cudart", "shared", *objs, "-o", lib_path])
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv))
+    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv, debug="--debug" in sys.argv))

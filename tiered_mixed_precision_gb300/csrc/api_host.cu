@@ -5,6 +5,10 @@
 
 #include "fade_internal.cuh"
 
+#if FADE_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
+
 namespace fade {
 
 static thread_local char g_err[512] = "";
@@ -114,6 +118,11 @@ fade_status_t validate_layer(const fade_config_t* c, const fade_layer_t* L) {
 
 }  // namespace fade
 
+#if FADE_NVTX
+fade::NvtxRange::NvtxRange(const char* name) { nvtxRangePushA(name); }
+fade::NvtxRange::~NvtxRange() { nvtxRangePop(); }
+#endif
+
 using namespace fade;
 
 // Smallest split of the middle tier in fade_decode_attention; bounds the partial slots.
@@ -191,3 +200,16 @@ extern "C" uint64_t fade_compressed_bytes(const fade_config_t* c, const fade_lay
 }
 
 extern "C" const char* fade_last_error(void) { return g_err; }
+
+extern "C" fade_status_t fade_tier_counts(const fade_config_t* c, const fade_layer_t* L,
+                                          int32_t* out) {
+  clear_error();
+  if (validate_config(c) || !L || !L->h_n_sink || !L->h_n_mid || !L->h_n_recent || !out)
+    return set_error(FADE_ERR_INVALID_ARGUMENT, "fade_tier_counts: bad arguments");
+  for (int b = 0; b < c->batch; ++b) {
+    out[3 * b + 0] = L->h_n_sink[b];
+    out[3 * b + 1] = L->h_n_mid[b];
+    out[3 * b + 2] = L->h_n_recent[b];
+  }
+  return FADE_OK;
+}

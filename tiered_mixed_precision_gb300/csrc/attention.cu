@@ -554,6 +554,7 @@ extern "C" fade_status_t fade_decode_attention(const fade_config_t* c, const fad
                                                float* logits_ws, float* ml_ws, void* ws,
                                                size_t ws_bytes, void* stream) {
   clear_error();
+  FADE_RANGE("fade_decode_attention");
   fade_status_t st = validate_config(c);
   if (!st) st = validate_layer(c, L);
   if (st) return st;
@@ -657,6 +658,7 @@ extern "C" fade_status_t fade_h2o_accumulate(const fade_config_t* c, fade_layer_
                                              const float* logits_ws, const float* ml_ws,
                                              void* stream) {
   clear_error();
+  FADE_RANGE("fade_h2o_accumulate");
   fade_status_t st = validate_config(c);
   if (!st) st = validate_layer(c, L);
   if (st) return st;

@@ -749,7 +749,11 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
                                   abort))
             return false;
           const int tile = tile0 + it;
-          const int nt = split > 0 ? min(kTileTok, n_mid - tile * kTileTok) : 0;  // <= 0: q only
+          int nt = split > 0 ? min(kTileTok, n_mid - tile * kTileTok) : 0;  // <= 0: q only
+          if (FADE_DEBUG && nt > 0 && tile * kTileTok + nt > a.C) {  // past the unit's slots
+            record_status(a.status, kCheckAttnTile);
+            nt = 0;
+          }
           int* inf = info + s * kInfo;
           inf[kInfoUnit] = unit;
           inf[kInfoSplit] = split;

@@ -63,6 +63,7 @@ extern "C" fade_status_t fade_decode_attention_noalloc(const fade_config_t* cfg,
                                                        float* logits_ws, float* ml_ws,
                                                        void* stream) {
   clear_error();
+  FADE_RANGE("fade_decode_attention_noalloc");
   void* scratch = nullptr;
   fade_status_t st = scratch_on_current_device(&scratch);
   if (st) return st;

@@ -211,6 +211,7 @@ struct LayerArgs {
   const uint16_t* pq_cb;      // the layer's PQ codebook, fp16 [d/4][256][4]
   float one, neg_one;         // 1 and -1, opaque to the compiler (see PlusMinus)
   int rd;                     // rotated width (head_dim unless proportional RoPE)
+  int32_t* status;            // the layer's device status words (device-side checks)
 };
 
 LayerArgs make_args(const fade_config_t* c, const fade_layer_t* L, const float* table) {
@@ -250,6 +251,7 @@ LayerArgs make_args(const fade_config_t* c, const fade_layer_t* L, const float* 
   a.one = 1.0f;
   a.neg_one = -1.0f;
   a.rd = rotary_width(c);
+  a.status = L->status;
   return a;
 }
 
@@ -353,7 +355,10 @@ __global__ void __launch_bounds__(32) demote_kernel(LayerArgs a) {
   const int n_rec = m[FADE_META_N_RECENT];
   if (n_rec != a.W) return;
   const int n_mid = m[FADE_META_N_MID], cur = m[FADE_META_CUR], head = m[FADE_META_HEAD];
-  if (n_mid >= a.C || head < 0 || head >= a.W) return;  // host checks capacity; never overrun
+  if (n_mid >= a.C || head < 0 || head >= a.W) {  // the host checks capacity; never overrun
+    if (threadIdx.x == 0) record_status(a.status, kCheckDemoteSlot);
+    return;
+  }
   const size_t rrow = ((size_t)unit * a.W + head) * D;
   const size_t mrow = (size_t)unit * a.C + n_mid;
   warp_quantize_row<D, KB>(a.rec_k + rrow, (cur ? a.mk[1] : a.mk[0]) + mrow * (D * KB / 8),
@@ -383,7 +388,10 @@ __global__ void __launch_bounds__(32) append_kernel(LayerArgs a, const uint16_t*
   uint16_t *dk, *dv;
   float* dsc;
   const bool to_sink = n_sink < a.S;
-  if (!to_sink && n_rec >= a.W) return;  // host checks capacity; never overwrite the ring
+  if (!to_sink && n_rec >= a.W) {  // the host checks capacity; never overwrite the ring
+    if (threadIdx.x == 0) record_status(a.status, kCheckAppendSlot);
+    return;
+  }
   if (to_sink) {
     const size_t row = (size_t)unit * a.S + n_sink;
     dk = a.sink_k + row * D;
@@ -946,6 +954,10 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MINB) evict_compact_kernel(L
                   __popc(word & ((1u << (i & 31)) - 1u)));
       }
     }
+    if (FADE_DEBUG && keep && (nv < 0 || nv >= a.C)) {  // a destination outside the unit
+      record_status(a.status, kCheckCompactRow);
+      keep = false;
+    }
     const bool moved = keep && nv != i && a.table != nullptr;
     const uint32_t dr = row0 + (uint32_t)h * (uint32_t)a.C + (uint32_t)nv;  // destination row
     uint8_t* krow_d = (cbuf ? a.mk[0] : a.mk[1]) + (size_t)dr * KROW;
@@ -1434,6 +1446,7 @@ using namespace fade;
 
 extern "C" fade_status_t fade_cache_reset(const fade_config_t* c, fade_layer_t* L, void* stream) {
   clear_error();
+  FADE_RANGE("fade_cache_reset");
   fade_status_t st = validate_config(c);
   if (!st) st = validate_layer(c, L);
   if (st) return st;
@@ -1451,6 +1464,7 @@ extern "C" fade_status_t fade_cache_prefill(const fade_config_t* c, fade_layer_t
                                             const float* mass, const float* table,
                                             int32_t max_pos, void* stream) {
   clear_error();
+  FADE_RANGE("fade_cache_prefill");
   fade_status_t st = validate_config(c);
   if (!st) st = validate_layer(c, L);
   if (st) return st;
@@ -1513,6 +1527,7 @@ extern "C" fade_status_t fade_cache_prefill(const fade_config_t* c, fade_layer_t
 extern "C" fade_status_t fade_cache_demote(const fade_config_t* c, fade_layer_t* L,
                                            void* stream) {
   clear_error();
+  FADE_RANGE("fade_cache_demote");
   fade_status_t st = validate_config(c);
   if (!st) st = validate_layer(c, L);
   if (st) return st;
@@ -1539,6 +1554,7 @@ extern "C" fade_status_t fade_cache_append(const fade_config_t* c, fade_layer_t*
                                            const uint16_t* k_rot, const uint16_t* v,
                                            void* stream) {
   clear_error();
+  FADE_RANGE("fade_cache_append");
   fade_status_t st = validate_config(c);
   if (!st) st = validate_layer(c, L);
   if (st) return st;
@@ -1599,6 +1615,7 @@ extern "C" fade_status_t fade_cache_advance_host(const fade_config_t* c, fade_la
 extern "C" fade_status_t fade_evict_rerope(const fade_config_t* c, fade_layer_t* L,
                                            const float* table, int32_t max_pos, void* stream) {
   clear_error();
+  FADE_RANGE("fade_evict_rerope");
   fade_status_t st = validate_config(c);
   if (!st) st = validate_layer(c, L);
   if (st) return st;

@@ -63,6 +63,7 @@ extern "C" fade_status_t fade_quantize_pack(const uint16_t* x, int64_t n_vec, in
                                             int32_t bits, uint8_t* codes, uint16_t* scales,
                                             void* stream) {
   clear_error();
+  FADE_RANGE("fade_quantize_pack");
   fade_status_t st = check_codec_args(x, codes, scales, n_vec, dim, bits);
   if (st) return st;
   if (n_vec == 0) return FADE_OK;
@@ -78,6 +79,7 @@ extern "C" fade_status_t fade_dequantize(const uint8_t* codes, const uint16_t* s
                                          int64_t n_vec, int32_t dim, int32_t bits, float* out,
                                          void* stream) {
   clear_error();
+  FADE_RANGE("fade_dequantize");
   fade_status_t st = check_codec_args(codes, scales, out, n_vec, dim, bits);
   if (st) return st;
   if (n_vec == 0) return FADE_OK;

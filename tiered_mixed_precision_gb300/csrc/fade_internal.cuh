@@ -21,6 +21,37 @@ fade_status_t validate_config(const fade_config_t* cfg);
 fade_status_t validate_layer(const fade_config_t* cfg, const fade_layer_t* layer);
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// NVTX ranges around the entry points that enqueue device work (a profiler shows each C-ABI
+// call as a named range; without a profiler attached a range costs a function-pointer test).
+#ifndef FADE_NVTX
+#define FADE_NVTX 1
+#endif
+#if FADE_NVTX
+struct NvtxRange {
+  explicit NvtxRange(const char* name);
+  ~NvtxRange();
+};
+#define FADE_RANGE(name) ::fade::NvtxRange fade_nvtx_range_(name)
+#else
+#define FADE_RANGE(name)
+#endif
+
+// Device-side checks. Every kernel guards its indices against the device metadata; a guard
+// that fails (a state the host-side checks should have excluded) records its code in the
+// layer's status word (status[0], first failure wins) and skips the access; fade_check_status
+// reports codes >= kDevCheckBase as FADE_ERR_DEVICE_CHECK. FADE_DEBUG=1 builds add the checks
+// that cost instructions on the hot paths (every compacted row, every attention tile).
+#ifndef FADE_DEBUG
+#define FADE_DEBUG 0
+#endif
+constexpr int kDevCheckBase = 16;
+enum DevCheck {
+  kCheckDemoteSlot = kDevCheckBase,  // demote: no free middle slot or a bad ring head
+  kCheckAppendSlot,                  // append: the recent window is full
+  kCheckCompactRow,                  // compaction: a destination row outside the unit (debug)
+  kCheckAttnTile,                    // attention: a tile past the unit's capacity (debug)
+};
 inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
 constexpr int kGroup = FADE_GROUP;     // channels per quantisation group
@@ -531,6 +562,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+__device__ __forceinline__ void record_status(int32_t* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
 // Bounded wait: gives up after `limit` cycles and records the failure (`code`) in status[0]
 // unless an earlier failure is recorded there.
 __device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, int32_t* status,

@@ -41,6 +41,7 @@ using namespace fade;
 extern "C" fade_status_t fade_measure_fp32_rate(int32_t blocks, int32_t iters, float* sink,
                                                 double* ops_out, void* stream) {
   clear_error();
+  FADE_RANGE("fade_measure_fp32_rate");
   if (blocks < 1 || iters < 1 || !sink)
     return set_error(FADE_ERR_INVALID_ARGUMENT, "blocks and iters must be positive, sink set");
   fp32_rate_kernel<<<blocks, kRateThreads, 0, as_stream(stream)>>>(iters, 1.0f, sink);

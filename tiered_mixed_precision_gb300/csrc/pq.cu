@@ -102,6 +102,7 @@ extern "C" fade_status_t fade_pq_encode(const uint16_t* codebook, const uint16_t
                                         int64_t n_vec, int32_t dim, uint8_t* codes,
                                         void* stream) {
   clear_error();
+  FADE_RANGE("fade_pq_encode");
   fade_status_t st = check_dim(dim, n_vec);
   if (st) return st;
   if (n_vec == 0) return FADE_OK;
@@ -120,6 +121,7 @@ extern "C" fade_status_t fade_pq_decode(const uint16_t* codebook, const uint8_t*
                                         int64_t n_vec, int32_t dim, uint16_t* out,
                                         void* stream) {
   clear_error();
+  FADE_RANGE("fade_pq_decode");
   fade_status_t st = check_dim(dim, n_vec);
   if (st) return st;
   if (n_vec == 0) return FADE_OK;
@@ -139,6 +141,7 @@ extern "C" fade_status_t fade_pq_train(const uint16_t* calib, int64_t n_vec, int
                                        uint16_t* codebook, void* ws, size_t ws_bytes,
                                        void* stream) {
   clear_error();
+  FADE_RANGE("fade_pq_train");
   fade_status_t st = check_dim(dim, n_vec);
   if (st) return st;
   if (n_vec < 1 || n_vec > FADE_PQ_MAX_CALIB)

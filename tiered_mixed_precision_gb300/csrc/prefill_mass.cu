@@ -191,6 +191,7 @@ extern "C" fade_status_t fade_prefill_mass(const fade_config_t* c, const uint16_
                                            const int32_t* h_prompt_len, float* mass, void* ws,
                                            size_t ws_bytes, void* stream) {
   clear_error();
+  FADE_RANGE("fade_prefill_mass");
   fade_status_t st = validate_config(c);
   if (st) return st;
   if (!q_rot || !k_rot || !h_prompt_len || !mass)

@@ -104,6 +104,7 @@ using namespace fade;
 extern "C" fade_status_t fade_rope_table_init(const fade_config_t* cfg, float* table,
                                               int32_t max_pos, void* stream) {
   clear_error();
+  FADE_RANGE("fade_rope_table_init");
   fade_status_t st = validate_config(cfg);
   if (st) return st;
   if (cfg->rope.kind == FADE_ROPE_NONE)
@@ -125,6 +126,7 @@ extern "C" fade_status_t fade_rope_apply(const fade_config_t* cfg, const float* 
                                          const int32_t* pos_start, int32_t pos_step,
                                          void* stream) {
   clear_error();
+  FADE_RANGE("fade_rope_apply");
   fade_status_t st = validate_config(cfg);
   if (st) return st;
   if (!x || !y) return set_error(FADE_ERR_INVALID_ARGUMENT, "NULL x or y");

@@ -39,6 +39,11 @@ extern "C" fade_status_t fade_check_status(const fade_layer_t* L, void* stream) 
   e = cudaMemcpy(w, L->status, sizeof(w), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess)
     return set_error(FADE_ERR_CUDA, "fade_check_status: %s", cudaGetErrorString(e));
+  if (w[0] >= kDevCheckBase)
+    return set_error(FADE_ERR_DEVICE_CHECK,
+                     "a device-side check failed (code %d: 16 demote slot, 17 append slot, "
+                     "18 compaction row, 19 attention tile); results since the last reset are "
+                     "invalid", w[0]);
   if (w[0] != 0)
     return set_error(FADE_ERR_TIMEOUT,
                      "a kernel gave up a bounded wait (code %d: 1 consumer stage, 2 producer "
@@ -50,6 +55,7 @@ extern "C" fade_status_t fade_check_status(const fade_layer_t* L, void* stream) 
 extern "C" fade_status_t fade_selftest_bounded_wait(int32_t* status, int32_t producer_arrives,
                                                     int64_t limit_cycles, void* stream) {
   clear_error();
+  FADE_RANGE("fade_selftest_bounded_wait");
   if (!status || (reinterpret_cast<uintptr_t>(status) & 3))
     return set_error(FADE_ERR_INVALID_ARGUMENT, "status is NULL or not 4-byte aligned");
   if (limit_cycles < 1 || limit_cycles > kWaitCycles)

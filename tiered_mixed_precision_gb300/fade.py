@@ -15,7 +15,9 @@ from dataclasses import dataclass, field
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "_build", "libfade.so")
+# FADE_LIBRARY=debug loads the FADE_DEBUG=1 build (build.build(debug=True)) instead
+LIB_PATH = os.path.join(_PKG, "_build_debug" if os.environ.get("FADE_LIBRARY") == "debug"
+                        else "_build", "libfade.so")
 
 FADE_OK, FADE_ERR_INVALID_ARGUMENT, FADE_ERR_UNSUPPORTED, FADE_ERR_CAPACITY, FADE_ERR_CUDA = range(5)
 ROPE_KINDS = {"none": 0, "default": 1, "llama3": 2, "linear": 3, "ntk": 4, "yarn": 5,
@@ -116,6 +118,7 @@ def lib():
             "fade_pq_decode": (c_i32, [c_vp, c_vp, c_i64, c_i32, c_vp, c_vp]),
             "fade_pq_train": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp]),
             "fade_check_status": (c_i32, [S(LayerT), c_vp]),
+            "fade_tier_counts": (c_i32, [S(ConfigT), S(LayerT), c_vp]),
             "fade_measure_fp32_rate": (c_i32, [c_i32, c_i32, c_vp, ctypes.POINTER(c_f64), c_vp]),
             "fade_selftest_bounded_wait": (c_i32, [c_vp, c_i32, c_i64, c_vp]),
             "fade_last_error": (ctypes.c_char_p, []),
@@ -467,3 +470,11 @@ def fade_measure_fp32_rate(blocks: int, iters: int, sink, stream=None) -> float:
     _check(lib().fade_measure_fp32_rate(int(blocks), int(iters), _ptr(sink), ctypes.byref(ops),
                                         _stream(stream)))
     return ops.value
+
+
+def fade_tier_counts(layer: TieredLayer) -> np.ndarray:
+    """Per-row (sinks, middle, recent) token counts from the host mirror: i32 [B][3]."""
+    out = np.zeros((layer.cfg.batch, 3), np.int32)
+    _check(lib().fade_tier_counts(ctypes.byref(layer.cfg.c()), ctypes.byref(layer.c),
+                                  out.ctypes.data))
+    return out
