@@ -94,6 +94,8 @@ struct MmaArgs {
   float* part_acc;                   // [B][Hq][nsplit][D]
   int32_t* status;
   int32_t* seg_count;                // [B][H]: partials of each unit (split 0 + segments)
+  int f16_sreg, f16_rreg;            // staged FP16 tiers: bytes of a sink / ring region (one
+                                     // 64-channel half of the rows); f16_rreg 0: not staged
   int B, Hq, H, S, W, C, NS, chunk, nsplit;
   float inv_sqrt_d;
   const uint16_t* pq_cb;             // PQ-coded V: the layer's codebook [D/4][256][4]
@@ -676,6 +678,8 @@ template <int D, int G, bool PQ>
 __global__ void __launch_bounds__(MmaShape<D, G, PQ>::THREADS, MmaShape<D, G, PQ>::MINB)
 attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_constant__ CUtensorMap tk1,
                     const __grid_constant__ CUtensorMap tv0, const __grid_constant__ CUtensorMap tv1,
+                    const __grid_constant__ CUtensorMap tsk, const __grid_constant__ CUtensorMap tsv,
+                    const __grid_constant__ CUtensorMap trk, const __grid_constant__ CUtensorMap trv,
                     MmaArgs a, const __grid_constant__ StreamK sk) {
   using Cfg = MmaCfg<D>;
   constexpr int kConsumers = MmaShape<D, G>::CONS;
@@ -700,7 +704,7 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int units = a.B * a.H;
-  const bool f16_staged = (a.S + a.W) * D * 2 <= Cfg::Q_OFF;  // FP16 tiers through the ring
+  const bool f16_staged = a.f16_rreg > 0;  // FP16 tiers through the ring (the host decides)
   // this CTA's work: FP16 items of units c, c + P, ..., then middle tiles [g0, g1)
   const int cta = blockIdx.x, P = gridDim.x;
   const int n16 = cta < units ? (units - cta + P - 1) / P : 0;
@@ -774,13 +778,19 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
           if (it == 0) bytes += G * D * 2;
           if (split == 0 && f16_staged) bytes += (a.S + a.W) * D * 2;
           mbar_expect_tx(bar_full + 8 * s, bytes);
-          if (split == 0 && f16_staged) {  // sinks then the whole ring, K (first) or V rows
-            const uint16_t* sink = it == 0 ? a.sink_k : a.sink_v;
-            const uint16_t* ring = it == 0 ? a.rec_k : a.rec_v;
-            if (a.S > 0)
-              bulk_load_1d(stage, sink + (size_t)unit * a.S * D, a.S * D * 2, bar_full + 8 * s);
-            bulk_load_1d(stage + a.S * D * 2, ring + (size_t)unit * a.W * D, a.W * D * 2,
-                         bar_full + 8 * s);
+          if (split == 0 && f16_staged) {  // K (first stage) or V rows: sinks, then the ring
+            // each 64-channel half of the rows into its own region, 128-byte swizzled: the
+            // sink region of half h at h * sreg, the ring region of half h at
+            // NHALF * sreg + h * rreg (every region 1024-byte aligned)
+            const CUtensorMap* ms = it == 0 ? &tsk : &tsv;
+            const CUtensorMap* mr = it == 0 ? &trk : &trv;
+#pragma unroll
+            for (int hh = 0; hh < NHALF; ++hh) {
+              if (a.S > 0)
+                tma_load_2d(stage + hh * a.f16_sreg, ms, 64 * hh, unit * a.S, bar_full + 8 * s);
+              tma_load_2d(stage + NHALF * a.f16_sreg + hh * a.f16_rreg, mr, 64 * hh,
+                          unit * a.W, bar_full + 8 * s);
+            }
           }
           if (nt > 0) {
             const size_t r = (size_t)unit * a.C + (size_t)tile * kTileTok;
@@ -899,12 +909,21 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
       for (int mt = warp; mt < nmt; mt += kConsumers) {
         const int r0 = mt * 16;
         float cacc[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t k_ld =
-            st_k + (r0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * D * 2 + 8 * (lane >> 4) * 2;
+        // this lane's row in its region (sinks or ring) and the 128-byte swizzle of its
+        // 16-byte chunks: chunk c of row rr sits at chunk c ^ (rr & 7)
+        uint32_t k_row, k_reg, k_y;
+        {
+          const int r = r0 + (lane & 7) + 8 * ((lane >> 3) & 1);
+          const bool sink = r < a.S;
+          const int rr = sink ? r : r - a.S;
+          k_reg = sink ? a.f16_sreg : a.f16_rreg;
+          k_row = st_k + (sink ? 0u : NHALF * a.f16_sreg) + rr * 128;
+          k_y = (uint32_t)((lane >> 4) ^ (rr & 7));
+        }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           uint32_t a0, a1, a2, a3;
-          ldsm_x4(k_ld + 32 * kk, a0, a1, a2, a3);
+          ldsm_x4(k_row + (kk >> 2) * k_reg + ((((2 * kk) & 7) ^ k_y) << 4), a0, a1, a2, a3);
           mma16816(cacc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
         }
         // logits of rows r0 + g + 8e for the head columns 2t + cc
@@ -955,14 +974,21 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
         const int tk = r0 + 2 * t;
         const uint32_t mlo = (tk < R ? 0xFFFFu : 0u) | (tk + 1 < R ? 0xFFFF0000u : 0u);
         const uint32_t mhi = (tk + 8 < R ? 0xFFFFu : 0u) | (tk + 9 < R ? 0xFFFF0000u : 0u);
-        const uint32_t v_ld =
-            st_v + (r0 + (lane & 7) + 8 * (lane >> 4)) * D * 2 + ((lane >> 3) & 1) * 16;
+        uint32_t v_row, v_reg, v_y;
+        {
+          const int r = r0 + (lane & 7) + 8 * (lane >> 4);
+          const bool sink = r < a.S;
+          const int rr = sink ? r : r - a.S;
+          v_reg = sink ? a.f16_sreg : a.f16_rreg;
+          v_row = st_v + (sink ? 0u : NHALF * a.f16_sreg) + rr * 128;
+          v_y = (uint32_t)(((lane >> 3) & 1) ^ (rr & 7));
+        }
 #pragma unroll
         for (int s = 0; s < NHALF; ++s)
 #pragma unroll
           for (int mm = 0; mm < 4; ++mm) {
             uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(v_ld + (64 * s + 16 * mm) * 2, a0, a1, a2, a3);
+            ldsm_x4_t(v_row + s * v_reg + (((2 * mm) ^ v_y) << 4), a0, a1, a2, a3);
             mma16816(of[s][mm], a0 & mlo, a1 & mlo, a2 & mhi, a3 & mhi, pb0, pb1);
           }
       }
@@ -1262,24 +1288,69 @@ fade_status_t encode_rows(CUtensorMap* m, const void* base, unsigned long long r
   return FADE_OK;
 }
 
+// 2D map over fp16 rows of D channels ([rows][D]), boxes of 64 channels (128 bytes) x box_rows
+// rows under the 128-byte swizzle: one box fills one region of staged FP16-tier rows.
+fade_status_t encode_f16_rows(CUtensorMap* m, const void* base, unsigned long long rows, int D,
+                              int box_rows) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return set_error(FADE_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {(cuuint64_t)D, rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(FADE_ERR_CUDA, "cuTensorMapEncodeTiled (fp16 rows) failed (%d)", (int)r);
+  return FADE_OK;
+}
+
 template <int D, int G, bool PQ>
-fade_status_t launch_mma(const fade_config_t* c, const fade_layer_t* L, const MmaArgs& a,
+fade_status_t launch_mma(const fade_config_t* c, const fade_layer_t* L, MmaArgs a,
                          const StreamK& sk, cudaStream_t st) {
   using Cfg = MmaCfg<D>;
   constexpr int kSmem = PQ ? PqCfg<D>::SMEM : Cfg::SMEM;
-  const unsigned long long rows = (unsigned long long)c->batch * c->num_kv_heads * a.C;
+  constexpr int NH = D / 64;
+  const unsigned long long units = (unsigned long long)c->batch * c->num_kv_heads;
+  const unsigned long long rows = units * a.C;
   CUtensorMap tk[2], tv[2];
   fade_status_t s;
   for (int i = 0; i < 2; ++i) {
     if ((s = encode_rows(&tk[i], L->mid_k_codes[i], rows, Cfg::KROW))) return s;
     if ((s = encode_rows(&tv[i], L->mid_v_codes[i], rows, Cfg::VROW))) return s;
   }
+  // the FP16 tiers of an item go through the ring when their swizzled regions (1024-byte
+  // aligned, one per 64-channel half of the sinks and of the ring), plus 16 rows of reads
+  // past the last one (the padding of the last 16-row M-tile), fit before the query rows
+  const int S = c->n_sink, W = c->recent_window;
+  const int sreg = S > 0 ? (S * 128 + 1023) / 1024 * 1024 : 0;
+  const int rreg = (W * 128 + 1023) / 1024 * 1024;
+  const bool staged = kF16Mma && S <= 256 && W <= 256 && NH * (sreg + rreg) + 16 * 128 <= Cfg::Q_OFF;
+  a.f16_sreg = staged ? sreg : 0;
+  a.f16_rreg = staged ? rreg : 0;
+  CUtensorMap tsk, tsv, trk, trv;
+  if (staged) {
+    if ((s = encode_f16_rows(&trk, L->recent_k, units * W, D, W))) return s;
+    if ((s = encode_f16_rows(&trv, L->recent_v, units * W, D, W))) return s;
+    if (S > 0) {
+      if ((s = encode_f16_rows(&tsk, L->sink_k, units * S, D, S))) return s;
+      if ((s = encode_f16_rows(&tsv, L->sink_v, units * S, D, S))) return s;
+    } else {  // no sinks: never read
+      tsk = trk;
+      tsv = trv;
+    }
+  } else {  // not staged: never read
+    tsk = tsv = trk = trv = tk[0];
+  }
   auto kern = attn_mid_mma_kernel<D, G, PQ>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
       cudaSuccess)
     return launch_status("fade_decode_attention (middle tier) shared-memory opt-in");
   // persistent grid: the schedule's CTAs (as many as fit on the device at once)
-  kern<<<sk.P, MmaShape<D, G, PQ>::THREADS, kSmem, st>>>(tk[0], tk[1], tv[0], tv[1], a, sk);
+  kern<<<sk.P, MmaShape<D, G, PQ>::THREADS, kSmem, st>>>(tk[0], tk[1], tv[0], tv[1], tsk, tsv,
+                                                         trk, trv, a, sk);
   return launch_status("fade_decode_attention (middle tier)");
 }
 
