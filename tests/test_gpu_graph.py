@@ -12,8 +12,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _masses(wl):
-    """H2O prefill masses computed once on the GPU (their atomic sums may differ between runs
-    in the last bits, so both caches of a comparison take the same ones)."""
+    """H2O prefill masses computed once on the GPU and given to both caches of a comparison."""
     import torch
 
     import tiered_mixed_precision_gb300 as T
@@ -191,3 +190,42 @@ def test_growing_graph_matches_eager_steps(kb, vb):
                         assert np.array_equal(a_[key], b_[key]), (layer, b, h, key)
                     else:
                         assert a_[key] == b_[key], (layer, b, h, key)
+
+
+@pytest.mark.parametrize("policy", ["position", "h2o"])
+def test_host_fed_pipeline_matches_eager_steps(policy):
+    """run_from_host (two captured graphs taking the steps in turn, inputs copied in from
+    pinned host memory while the previous step runs, outputs copied out while the next one
+    runs, maintenance on side streams) gives every step's outputs, and the cache after the
+    last step, bit for bit as launching every call."""
+    import torch
+
+    wl = get_workload(4).scaled(layers=2, batch=2, num_q_heads=8, num_kv_heads=2,
+                                prompt_len=1200, int4_budget=500, policy=policy)
+    if policy == "h2o":
+        wl = wl.scaled(rope=get_workload(3).rope)
+    masses = _masses(wl)
+    eager, fed = _make(wl, masses), _make(wl, masses)
+    L, B, Hq, Hkv, d = wl.layers, wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim
+    steps = 5
+    qh = torch.from_numpy(draw_vectors(wl, "q", (steps, L, B, Hq, d), "host")).pin_memory()
+    kh = torch.from_numpy(draw_vectors(wl, "k", (steps, L, B, Hkv, d), "host")).pin_memory()
+    vh = torch.from_numpy(draw_vectors(wl, "v", (steps, L, B, Hkv, d), "host")).pin_memory()
+    oh = torch.full((steps, L, B, Hq, d), float("nan"), dtype=torch.float16).pin_memory()
+    side = [torch.cuda.Stream(), torch.cuda.Stream()]
+    fed.maintain_all()                    # the pipelined schedule's prologue
+    fed.run_from_host(qh, kh, vh, oh, side)
+    torch.cuda.synchronize()
+    out_e = torch.empty((L, B, Hq, d), dtype=torch.float16, device="cuda")
+    for s in range(steps):
+        eager.step_all(qh[s].cuda(), kh[s].cuda(), vh[s].cuda(), out_e)
+        torch.cuda.synchronize()
+        assert torch.equal(oh[s].view(torch.int16), out_e.cpu().view(torch.int16)), f"step {s}"
+    eager.maintain_all()                  # the fed cache already ran the next maintenance
+    torch.cuda.synchronize()
+    for a, b in zip(eager.layers, fed.layers):
+        assert torch.equal(a.meta, b.meta)
+        cur = int(a.meta[0, 0, 4])
+        assert torch.equal(a.mid_k_codes[cur], b.mid_k_codes[cur])
+        assert torch.equal(a.recent_k, b.recent_k)
+        assert np.array_equal(a.h_n_mid, b.h_n_mid)

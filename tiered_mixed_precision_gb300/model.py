@@ -291,6 +291,74 @@ class FadeCache:
                 raise RuntimeError("capture_step needs a steady-state cache (tier counts changed)")
         return g
 
+    # ------------------------------------------------------------------ host-fed steps
+    def prepare_host_pipeline(self, side=None):
+        """Capture the two step graphs ``run_from_host`` alternates between (steady state
+        only, see ``capture_step``): each reads its own q/k/v buffers and writes its own output
+        buffer, so one step's inputs can be copied in while the other graph runs."""
+        if getattr(self, "_host_pipe", None) is not None:
+            return
+        c, L, dev = self.cfg, len(self.layers), self.device
+        shp_q = (L, c.batch, c.num_q_heads, c.head_dim)
+        shp_kv = (L, c.batch, c.num_kv_heads, c.head_dim)
+        bufs = []
+        for _ in range(2):
+            qb = torch.zeros(shp_q, dtype=torch.float16, device=dev)
+            kb = torch.zeros(shp_kv, dtype=torch.float16, device=dev)
+            vb = torch.zeros(shp_kv, dtype=torch.float16, device=dev)
+            ob = torch.empty(shp_q, dtype=torch.float16, device=dev)
+            bufs.append((qb, kb, vb, ob))
+        graphs = [self.capture_step(qb, kb, vb, ob, side) for qb, kb, vb, ob in bufs]
+        ev = lambda: [torch.cuda.Event(), torch.cuda.Event()]
+        self._host_pipe = {"graphs": graphs, "bufs": bufs, "copy": torch.cuda.Stream(device=dev),
+                           "in_ready": ev(), "done": ev(), "out_copied": ev(),
+                           "out_used": [False, False]}
+
+    def run_from_host(self, qh, kh, vh, oh, side=None):
+        """K decode steps fed from host memory: qh [K][L][B][Hq][d], kh/vh [K][L][B][Hkv][d]
+        (pinned, fp16) in, oh like qh (pinned) out. Step s+1's inputs are copied to the device
+        on a copy stream while step s runs (the two captured graphs of
+        ``prepare_host_pipeline`` take the steps in turn), and step s's outputs are copied back
+        while step s+1 runs. Enqueued on the current stream, which waits for the last output
+        copy: synchronise it (or record an event on it) to know the outputs have arrived."""
+        self.prepare_host_pipeline(side)
+        P = self._host_pipe
+        main, cs = torch.cuda.current_stream(), P["copy"]
+        K = qh.shape[0]
+        if K == 0:
+            return
+
+        def copy_in(s, j):
+            qb, kb, vb, _ = P["bufs"][j]
+            qb.copy_(qh[s], non_blocking=True)
+            kb.copy_(kh[s], non_blocking=True)
+            vb.copy_(vh[s], non_blocking=True)
+            P["in_ready"][j].record(cs)
+
+        start = torch.cuda.Event()
+        start.record(main)
+        cs.wait_event(start)                   # nothing of this call starts before the caller's work
+        with torch.cuda.stream(cs):
+            copy_in(0, 0)
+        for s in range(K):
+            j, jn = s % 2, (s + 1) % 2
+            if s + 1 < K:
+                with torch.cuda.stream(cs):
+                    if s >= 1:                 # the other graph (step s-1) has read its inputs
+                        cs.wait_event(P["done"][jn])
+                    copy_in(s + 1, jn)
+            main.wait_event(P["in_ready"][j])
+            if P["out_used"][j]:               # step s-2's outputs have left the buffer
+                main.wait_event(P["out_copied"][j])
+            P["graphs"][j].replay()
+            P["done"][j].record(main)
+            with torch.cuda.stream(cs):
+                cs.wait_event(P["done"][j])
+                oh[s].copy_(P["bufs"][j][3], non_blocking=True)
+                P["out_copied"][j].record(cs)
+            P["out_used"][j] = True
+        main.wait_event(P["out_copied"][(K - 1) % 2])
+
     # ------------------------------------------------------------------ growing caches
     def growing_graph_ok(self) -> bool:
         """A step of this cache can be captured once and replayed while the cache grows: no
