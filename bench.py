@@ -429,20 +429,23 @@ def run_ours(args, rank, world):
     if n_side <= 0:  # concurrent compactions of large layers compete; short ones fill gaps
         n_side = 1 if B * Hkv * max(wl.int4_budget, 0) >= (1 << 20) else 2
     side = [torch.cuda.Stream() for _ in range(n_side)] if pipelined else None
-    # a cache that grows every step (no eviction) with CUDA-core attention: one captured
-    # step replayed with the positions copied in and the host mirror advanced
+    # a cache that grows every step (no eviction): a captured step replayed with the positions
+    # copied in and the host mirror advanced, captured again whenever the tensor-core
+    # attention kernel's schedule changes (a row's middle tier reaching a new tile); those
+    # captures inside the timed region are timed with it
     growing = not steady and not args.no_graph and fc.growing_graph_ok()
     if growing:
         fc.timers = None   # per-call events come from eager steps after the timed region
         fc.launches = 0
-        graph = fc.capture_growing_step(qb, kb, vb, out)
-        launches_per_step = fc.launches
         qb.copy_(q_all[W - 1 if W > 0 else 0])
         kb.copy_(k_all[W - 1 if W > 0 else 0])
         vb.copy_(v_all[W - 1 if W > 0 else 0])
-        fc.replay_growing(graph)
+        fc.growing_step(qb, kb, vb, out)
+        launches_per_step = fc.launches
+        graph = fc  # not None: the replays go through fc.growing_step
         torch.cuda.synchronize()
         progress("growing-cache graph captured and replayed once")
+    captures_before = fc.growing_captures
     if steady and not args.no_graph:
         if pipelined:
             # prologue: the coming step's maintenance of every layer; from here on each step
@@ -470,13 +473,14 @@ def run_ours(args, rank, world):
             kb.copy_(k_all[s], non_blocking=True)
             vb.copy_(v_all[s], non_blocking=True)
             if growing:
-                fc.replay_growing(graph)
+                fc.growing_step(qb, kb, vb, out)
             else:
                 graph.replay()
         else:
             step(s)
     e1.record()
     torch.cuda.synchronize()
+    timed_captures = fc.growing_captures - captures_before
     clk = clocks.stop()
     progress(f"{K} timed steps done")
     launches = launches_per_step * K if graph is not None else fc.launches
@@ -493,7 +497,7 @@ def run_ours(args, rank, world):
             kb.copy_(k_all[s], non_blocking=True)
             vb.copy_(v_all[s], non_blocking=True)
             if growing:
-                fc.replay_growing(graph)
+                fc.growing_step(qb, kb, vb, out)
             else:
                 graph.replay()
         else:
@@ -636,7 +640,7 @@ def run_ours(args, rank, world):
                 kb.copy_(kh[s], non_blocking=True)
                 vb.copy_(vh[s], non_blocking=True)
                 if growing:
-                    fc.replay_growing(graph)
+                    fc.growing_step(qb, kb, vb, out)
                 else:
                     graph.replay()
             else:
@@ -670,8 +674,9 @@ def run_ours(args, rank, world):
                                f"{PQ_CALIB_ROWS} synthetic rows, {PQ_ITERS} rounds)"),
                    "l2": "no flush: the compressed cache read per step is far larger than L2",
                    "parallelism": f"replicas x{world} (rows independent, no collective)",
-                   "launch": ("cuda graph per step (growing cache: positions copied in, host "
-                              "mirror advanced per replay)" if growing else
+                   "launch": (f"cuda graph per step (growing cache: positions copied in, host "
+                              f"mirror advanced per replay; {timed_captures} re-captures in the "
+                              f"timed region)" if growing else
                               "cuda graph per step" if graph is not None else "eager launches") +
                              (f"; each layer's maintenance overlaps the next layers "
                               f"({len(side)} side streams taken in turn)" if pipelined else ""),

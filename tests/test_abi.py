@@ -215,3 +215,27 @@ def test_debug_build_compiles_and_exports_every_symbol():
     lib = ctypes.CDLL(path)
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
     assert not missing, f"declared but not exported by the debug build: {missing}"
+
+
+@pytest.mark.parametrize("kw,tiled", [
+    (dict(), True),                                          # INT4 K, INT2 V
+    (dict(middle_v_bits=4), True),                           # INT4 V (safe preset)
+    (dict(v_codec="pq"), True),                              # PQ-coded V
+    (dict(head_dim=64, middle_v_bits=4, num_q_heads=16), True),
+    (dict(middle_k_bits=2, middle_v_bits=2), False),         # INT2 K: CUDA-core kernel
+    (dict(middle_k_bits=2, middle_v_bits=4), False),
+])
+def test_attention_tiled_query(T, kw, tiled):
+    """fade_attention_tiled names the configurations whose attention runs the tensor-core
+    kernel (scheduled by middle tiles); an invalid configuration is an error."""
+    assert T.fade.fade_attention_tiled(_cfg(T, **kw)) is tiled
+
+
+def test_attention_tiled_query_rejects_invalid_config(T):
+    with pytest.raises(T.FadeError):
+        T.fade.fade_attention_tiled(_cfg(T, head_dim=96))
+
+
+def test_tile_constant_matches_the_header(T):
+    m = re.search(r"#define\s+FADE_ATTN_TILE_TOKENS\s+(\d+)", open(HEADER).read())
+    assert m and int(m.group(1)) == T.fade.ATTN_TILE_TOKENS

@@ -173,6 +173,21 @@ def _small(key):
         return get_workload(4).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
                                       head_dim=64, middle_v_bits=4, prompt_len=900,
                                       int4_budget=350, steps=5), None
+    # INT4 V on the tensor-core kernel (INT4 K) at every query-group size and head dimension
+    if key == "v4_g1_h2o_d128":   # logits written for H2O, three tiles per unit
+        return get_workload(3).scaled(layers=1, batch=2, num_q_heads=4, num_kv_heads=4,
+                                      head_dim=128, middle_v_bits=4, prompt_len=900,
+                                      int4_budget=600, steps=6), None
+    if key == "v4_g2_ema_d64":    # ragged rows, EMA
+        return get_workload(5).scaled(layers=1, batch=3, num_q_heads=4, num_kv_heads=2,
+                                      head_dim=64, middle_v_bits=4, ragged=(700, 1300),
+                                      prompt_len=1300, int4_budget=800, steps=5), None
+    if key == "v4_g8_d64_h2o":
+        return get_workload(3).scaled(layers=1, batch=2, num_q_heads=16, num_kv_heads=2,
+                                      middle_v_bits=4, prompt_len=900, int4_budget=500,
+                                      steps=6), None
+    if key == "v4_g8_d128_grow":  # the safe preset's shape, six tiles per unit, no eviction
+        return get_workload(2).scaled(layers=1, batch=2, prompt_len=1400, steps=4), None
     # degenerate cases of the method
     if key == "deg_nosink":  # no sinks: the recent ring and the middle tier only
         return get_workload(4).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2,
@@ -233,6 +248,8 @@ def _small(key):
 @pytest.mark.parametrize("key", ["1", "2s", "3s", "4s", "5s", "5bs", "g2_k2v4", "g1_h2o_d128",
                                  "d64_g8", "d128_g8", "d64_k2v4_h2o", "d128_k4v4_pos",
                                  "d64_k2v2_ema", "d128_k2v2_pos", "d64_k4v4_pos",
+                                 "v4_g1_h2o_d128", "v4_g2_ema_d64", "v4_g8_d64_h2o",
+                                 "v4_g8_d128_grow",
                                  "deg_nosink", "deg_w1_h2o", "deg_budget0", "deg_short_ragged",
                                  "deg_norope_ema", "rope_linear_pos", "rope_ntk_h2o",
                                  "rope_yarn_ema", "rope_dynamic_pos", "prop_pos_r64",

@@ -163,6 +163,12 @@ extern "C" fade_status_t fade_layout(const fade_config_t* c, int32_t max_prompt,
   return FADE_OK;
 }
 
+extern "C" int32_t fade_attention_tiled(const fade_config_t* c) {
+  clear_error();
+  if (validate_config(c)) return -1;
+  return mid_mma_supported(c) ? 1 : 0;
+}
+
 extern "C" int32_t fade_next_position(const fade_config_t* c, const fade_layer_t* L,
                                       int32_t row) {
   clear_error();

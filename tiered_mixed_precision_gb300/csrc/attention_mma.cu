@@ -36,7 +36,7 @@ namespace fade {
 namespace {
 
 constexpr int kF = FADE_META_FIELDS;
-constexpr int kTileTok = 256;            // tokens per TMA tile
+constexpr int kTileTok = FADE_ATTN_TILE_TOKENS;  // tokens per TMA tile
 // Warp layout per (head_dim, query heads per KV head): consumer warps per CTA, each taking an
 // equal share of a tile (32 or 64 tokens), one producer warp, and the resident-CTA hint given to
 // the register allocator. Eight consumers (two CTAs per SM) when the accumulators are small
@@ -101,14 +101,16 @@ struct MmaArgs {
   const uint16_t* pq_cb;             // PQ-coded V: the layer's codebook [D/4][256][4]
 };
 
-template <int D>
+// Stage layout of the ring for V codes of VB bits (2, or 4: the safe preset) and NST stages (0:
+// the default for the head dimension).
+template <int D, int VB = 2, int NST = 0>
 struct MmaCfg {
   static constexpr int KROW = D / 2;        // INT4 codes per token (bytes)
-  static constexpr int VROW = D / 4;        // INT2 codes per token (bytes)
+  static constexpr int VROW = D * VB / 8;   // INT2 / INT4 V codes per token (bytes)
   static constexpr int SROW = D / kGroup;   // scales per token
   static constexpr int Q_BYTES = 8 * D * 2; // the item's query rows (up to 8 heads), fp16
   static constexpr int STAGE = kTileTok * (KROW + VROW + 2 * SROW * 2) + Q_BYTES;
-  static constexpr int NSTAGE = D == 128 ? FADE_MMA_STAGES_128 : 4;
+  static constexpr int NSTAGE = NST ? NST : (D == 128 ? FADE_MMA_STAGES_128 : 4);
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = kTileTok * KROW;
   static constexpr int KS_OFF = V_OFF + kTileTok * VROW;
@@ -124,6 +126,15 @@ struct MmaCfg {
   static constexpr int SMEM = BAR_OFF + 2 * NSTAGE * 8 + 1024;  // + alignment slack
   static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned (TMA swizzle)");
 };
+
+// Ring depth of one shape: the default, except INT4 V at d = 128 (38 KB stages): two stages
+// when two CTAs share an SM, four when one CTA holds it.
+template <int D, int G, bool PQ, int VB>
+__host__ __device__ constexpr int mma_stages() {
+  return (VB == 4 && D == 128) ? (MmaShape<D, G, PQ>::MINB > 1 ? 2 : 4) : 0;
+}
+template <int D, int G, bool PQ, int VB>
+using MmaCfgOf = MmaCfg<D, VB, mma_stages<D, G, PQ, VB>()>;
 
 // Shared memory added for PQ-coded V, after the layout above: the layer's codebook stored
 // centroid-major ([256][D/4] entries of 4 fp16 channels, so that the 32 lanes of a warp, one
@@ -373,26 +384,32 @@ __device__ __forceinline__ uint32_t v_crumb(uint32_t x, uint32_t x10) {
 
 // Per-lane shared-memory byte offsets inside a stage, for M-tile 0 of the warp (M-tile mt adds
 // mt * 16 rows). With the 64-/32-byte swizzles the XOR pattern depends only on the lane.
-template <int D>
+template <int D, int VB>
 struct LaneOffsets {
-  uint32_t k[D / 64];  // ldmatrix address of the K codes, per 64-channel half
-  uint32_t v;          // ldmatrix.trans address of the V codes
-  uint32_t ks, vs;     // K / V scale row of token g
+  uint32_t k[D / 64];               // ldmatrix address of the K codes, per 64-channel half
+  uint32_t v[VB == 4 ? D / 64 : 1]; // ldmatrix.trans address of the V codes (INT4: per half)
+  uint32_t ks, vs;                  // K / V scale row of token g
 };
 
-template <int D>
-__device__ __forceinline__ LaneOffsets<D> lane_offsets(int wr0, int lane) {
-  using Cfg = MmaCfg<D>;
-  LaneOffsets<D> o;
+// INT4 V rows have the K rows' width and swizzle, so they are addressed like the K rows (the
+// 16-byte chunks 2s and 2s + 1, i.e. the quantisation groups of half s, of tokens 0-15).
+template <int D, int VB>
+__device__ __forceinline__ LaneOffsets<D, VB> lane_offsets(int wr0, int lane) {
+  using Cfg = MmaCfg<D, VB>;
+  LaneOffsets<D, VB> o;
   const int lr = (lane & 7) + ((lane >> 3) & 1) * 8, hi = lane >> 4, g = lane >> 2;
   if constexpr (D == 128) {
 #pragma unroll
-    for (int s = 0; s < 2; ++s)
-      o.k[s] = Cfg::K_OFF + (wr0 + lr) * Cfg::KROW + (((2 * s + hi) ^ ((lr >> 1) & 3)) * 16);
-    o.v = Cfg::V_OFF + (wr0 + lr) * Cfg::VROW + ((hi ^ ((lr >> 2) & 1)) * 16);
+    for (int s = 0; s < 2; ++s) {
+      const int sw = ((2 * s + hi) ^ ((lr >> 1) & 3)) * 16;
+      o.k[s] = Cfg::K_OFF + (wr0 + lr) * Cfg::KROW + sw;
+      if constexpr (VB == 4) o.v[s] = Cfg::V_OFF + (wr0 + lr) * Cfg::VROW + sw;
+    }
+    if constexpr (VB == 2) o.v[0] = Cfg::V_OFF + (wr0 + lr) * Cfg::VROW + ((hi ^ ((lr >> 2) & 1)) * 16);
   } else {
-    o.k[0] = Cfg::K_OFF + (wr0 + lr) * Cfg::KROW + ((hi ^ ((lr >> 2) & 1)) * 16);
-    o.v = Cfg::V_OFF + (wr0 + lr) * Cfg::VROW;
+    const int sw = (hi ^ ((lr >> 2) & 1)) * 16;
+    o.k[0] = Cfg::K_OFF + (wr0 + lr) * Cfg::KROW + sw;
+    o.v[0] = Cfg::V_OFF + (wr0 + lr) * Cfg::VROW + (VB == 4 ? sw : 0);
   }
   o.ks = Cfg::KS_OFF + (wr0 + g) * Cfg::SROW * 2;
   o.vs = Cfg::VS_OFF + (wr0 + g) * Cfg::SROW * 2;
@@ -414,13 +431,13 @@ __device__ __forceinline__ void scale_words(uint32_t addr, uint32_t (&w)[D / 64]
 // One consumer warp's share of one tile: QK^T on the tensor cores with the K scales applied per
 // group in fp32, the online-softmax update, and PV. FULL: every token of the warp's share is
 // valid (no masking). Invalid head columns (G < 4) carry logit 0 and are discarded later.
-template <int D, int G, bool FULL, bool LOGITS, bool PQ>
+template <int D, int G, bool FULL, bool LOGITS, bool PQ, int VB>
 __device__ __forceinline__ void consume_tile(
-    const MmaArgs& a, uint32_t stage, const LaneOffsets<D>& lo_, int nt, int wr0, int lane,
+    const MmaArgs& a, uint32_t stage, const LaneOffsets<D, VB>& lo_, int nt, int wr0, int lane,
     const uint32_t (&qb)[D / 64][4][(2 * G + 7) / 8][2], float (&m2)[(2 * G + 7) / 8],
     float (&lsum)[(2 * G + 7) / 8], float (&o)[D / 64][4][(2 * G + 7) / 8][4], float c2,
     float* logit_row, uint32_t vt, uint32_t cbs) {
-  using Cfg = MmaCfg<D>;
+  using Cfg = MmaCfg<D, VB>;
   constexpr int NT = (2 * G + 7) / 8;
   constexpr int NHALF = D / 64;
   const int g = lane >> 2, t = lane & 3;
@@ -577,11 +594,13 @@ __device__ __forceinline__ void consume_tile(
         vw_hi[s] = (r0 + g + 8 < nt) ? vw_hi[s] : 0u;
       }
     }
-    uint32_t X[2 * NHALF];  // (tokens 0-7 | 8-15) x (channel half)
-    if constexpr (D == 128)
-      ldsm_x4_t(stage + lo_.v + mt * 16 * Cfg::VROW, X[0], X[1], X[2], X[3]);
-    else
-      ldsm_x2_t(stage + lo_.v + mt * 16 * Cfg::VROW, X[0], X[1]);
+    uint32_t X[2 * NHALF];  // INT2: (tokens 0-7 | 8-15) x (channel half)
+    if constexpr (VB == 2) {
+      if constexpr (D == 128)
+        ldsm_x4_t(stage + lo_.v[0] + mt * 16 * Cfg::VROW, X[0], X[1], X[2], X[3]);
+      else
+        ldsm_x2_t(stage + lo_.v[0] + mt * 16 * Cfg::VROW, X[0], X[1]);
+    }
     __half2 pg[NT], pg8[NT];
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
@@ -596,6 +615,25 @@ __device__ __forceinline__ void consume_tile(
         pb[j][0] = movm_t(h2_as_u32(__hmul2(pg[j], u32_as_h2(vw_lo[s]))));
         pb[j][1] = movm_t(h2_as_u32(__hmul2(pg8[j], u32_as_h2(vw_hi[s]))));
       }
+      if constexpr (VB == 4) {
+        // INT4: X4 = (chunk 2s | 2s+1) x (tokens 0-7 | 8-15), each register two tokens' 16-bit
+        // word g (channels 4g .. 4g+3 of the chunk's group). M-tile mm = chunk 2s + mm / 2,
+        // nibbles 2 (mm % 2) (rows g) and 2 (mm % 2) + 1 (rows g + 8): all 16 rows in one
+        // quantisation group, whose parity column is the one kept
+        uint32_t X4[4];
+        ldsm_x4_t(stage + lo_.v[s] + mt * 16 * Cfg::VROW, X4[0], X4[1], X4[2], X4[3]);
+        const uint32_t x08 = X4[0] >> 8, x18 = X4[1] >> 8, x28 = X4[2] >> 8, x38 = X4[3] >> 8;
+#define FADE_PV4(MM, XA, XA8, XB, XB8)                                                      \
+  {                                                                                         \
+    const uint32_t a0 = k_pair<2 * (MM % 2)>(XA, XA8), a1 = k_pair<2 * (MM % 2) + 1>(XA, XA8); \
+    const uint32_t a2 = k_pair<2 * (MM % 2)>(XB, XB8), a3 = k_pair<2 * (MM % 2) + 1>(XB, XB8); \
+    _Pragma("unroll") for (int j = 0; j < NT; ++j)                                          \
+        mma16816(o[s][MM][j], a0, a1, a2, a3, pb[j][0], pb[j][1]);                          \
+  }
+        FADE_PV4(0, X4[0], x08, X4[1], x18) FADE_PV4(1, X4[0], x08, X4[1], x18)
+        FADE_PV4(2, X4[2], x28, X4[3], x38) FADE_PV4(3, X4[2], x28, X4[3], x38)
+#undef FADE_PV4
+      } else {
       const uint32_t xa = X[2 * s], xb = X[2 * s + 1];
       const uint32_t xa10 = xa >> 10, xb10 = xb >> 10;
 #define FADE_PV(MM)                                                                         \
@@ -607,6 +645,7 @@ __device__ __forceinline__ void consume_tile(
   }
       FADE_PV(0) FADE_PV(1) FADE_PV(2) FADE_PV(3)
 #undef FADE_PV
+      }
     }
   }
 }
@@ -674,14 +713,14 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity
 // arming it. The producer therefore runs ahead across item boundaries and the consumers never
 // wait on global memory for metadata or queries. Consumer warps merge their partials in shared
 // memory at the end of each item (named barrier 1, consumers only) and write its partial.
-template <int D, int G, bool PQ>
+template <int D, int G, bool PQ, int VB>
 __global__ void __launch_bounds__(MmaShape<D, G, PQ>::THREADS, MmaShape<D, G, PQ>::MINB)
 attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_constant__ CUtensorMap tk1,
                     const __grid_constant__ CUtensorMap tv0, const __grid_constant__ CUtensorMap tv1,
                     const __grid_constant__ CUtensorMap tsk, const __grid_constant__ CUtensorMap tsv,
                     const __grid_constant__ CUtensorMap trk, const __grid_constant__ CUtensorMap trv,
                     MmaArgs a, const __grid_constant__ StreamK sk) {
-  using Cfg = MmaCfg<D>;
+  using Cfg = MmaCfgOf<D, G, PQ, VB>;
   constexpr int kConsumers = MmaShape<D, G>::CONS;
   constexpr int NT = (2 * G + 7) / 8;    // 8-column n-tiles of (head, group parity)
   constexpr int NHALF = D / 64;          // 64-channel halves (accumulator sets)
@@ -839,7 +878,7 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
   // ------------------------------------------------------------ consumers
   const float c2 = a.inv_sqrt_d * kLog2e;
   const int wr0 = warp * MmaShape<D, G>::WARP_TOK;
-  const LaneOffsets<D> lo_ = lane_offsets<D>(wr0, lane);
+  const LaneOffsets<D, VB> lo_ = lane_offsets<D, VB>(wr0, lane);
   const bool want_logits = a.logits != nullptr;
   // PQ-coded V: this warp's decoded V tile and the codebook (unused otherwise)
   const uint32_t vt = sbase + PqCfg<D>::VT_OFF + warp * 16 * PqCfg<D>::VT_ROW;
@@ -1155,17 +1194,17 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
         if (ok) {
           if (want_logits) {
             if (nt == kTileTok)
-              consume_tile<D, G, true, true, PQ>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o,
+              consume_tile<D, G, true, true, PQ, VB>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o,
                                              c2, logit_row, vt, cbs);
             else if (wr0 < nt)
-              consume_tile<D, G, false, true, PQ>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o,
+              consume_tile<D, G, false, true, PQ, VB>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o,
                                               c2, logit_row, vt, cbs);
           } else {
             if (nt == kTileTok)
-              consume_tile<D, G, true, false, PQ>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o,
+              consume_tile<D, G, true, false, PQ, VB>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o,
                                               c2, logit_row, vt, cbs);
             else if (wr0 < nt)
-              consume_tile<D, G, false, false, PQ>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o,
+              consume_tile<D, G, false, false, PQ, VB>(a, stage, lo_, nt, wr0, lane, qb, m2, lsum, o,
                                                c2, logit_row, vt, cbs);
           }
           __syncwarp();
@@ -1203,6 +1242,11 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
                 const int c = 64 * s + 16 * mm + g;
                 wo[(warp * G + h) * WR + c] = o[s][mm][j][0];
                 wo[(warp * G + h) * WR + c + 8] = o[s][mm][j][2];
+              } else if constexpr (VB == 4) {  // rows g, g + 8 = nibbles 2 (mm % 2) (+ 1) of
+                                                // word g of group 2s + mm / 2: its parity kept
+                const int c = 64 * s + 32 * (mm >> 1) + 4 * g + 2 * (mm & 1);
+                wo[(warp * G + h) * WR + c] = o[s][mm][j][mm >> 1];
+                wo[(warp * G + h) * WR + c + 1] = o[s][mm][j][2 + (mm >> 1)];
               } else {
                 const int c = 64 * s + 8 * g + 2 * mm;
                 wo[(warp * G + h) * WR + c] = gsel ? o[s][mm][j][1] : o[s][mm][j][0];
@@ -1307,11 +1351,15 @@ fade_status_t encode_f16_rows(CUtensorMap* m, const void* base, unsigned long lo
   return FADE_OK;
 }
 
-template <int D, int G, bool PQ>
+template <int D, int G, bool PQ, int VB>
 fade_status_t launch_mma(const fade_config_t* c, const fade_layer_t* L, MmaArgs a,
                          const StreamK& sk, cudaStream_t st) {
-  using Cfg = MmaCfg<D>;
+  using Cfg = MmaCfgOf<D, G, PQ, VB>;
   constexpr int kSmem = PQ ? PqCfg<D>::SMEM : Cfg::SMEM;
+  // the resident CTAs (each with 1 KB reserved by the system) fit the 228 KB of an SM
+  static_assert(kSmem <= 227 * 1024 &&
+                    MmaShape<D, G, PQ>::MINB * (kSmem + 1024) <= 228 * 1024,
+                "shared memory of the resident CTAs");
   constexpr int NH = D / 64;
   const unsigned long long units = (unsigned long long)c->batch * c->num_kv_heads;
   const unsigned long long rows = units * a.C;
@@ -1344,7 +1392,7 @@ fade_status_t launch_mma(const fade_config_t* c, const fade_layer_t* L, MmaArgs 
   } else {  // not staged: never read
     tsk = tsv = trk = trv = tk[0];
   }
-  auto kern = attn_mid_mma_kernel<D, G, PQ>;
+  auto kern = attn_mid_mma_kernel<D, G, PQ, VB>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
       cudaSuccess)
     return launch_status("fade_decode_attention (middle tier) shared-memory opt-in");
@@ -1357,8 +1405,9 @@ fade_status_t launch_mma(const fade_config_t* c, const fade_layer_t* L, MmaArgs 
 }  // namespace
 
 bool mid_mma_supported(const fade_config_t* c) {
-  // INT4 K with INT2 V, or with PQ-coded V (whose codes fill the INT2 rows)
-  return c->middle_k_bits == 4 && c->middle_v_bits == 2;
+  // INT4 K with INT2 V (or PQ-coded V, whose codes fill the INT2 rows) or with INT4 V
+  return c->middle_k_bits == 4 &&
+         (c->middle_v_bits == 2 || (c->middle_v_bits == 4 && c->v_codec != FADE_V_PQ));
 }
 
 int mid_mma_ctas(const fade_config_t* c) {
@@ -1435,10 +1484,12 @@ fade_status_t launch_mid_mma(const fade_config_t* c, const fade_layer_t* L, cons
   a.pq_cb = L->pq_codebook;
   const int G = c->num_q_heads / c->num_kv_heads;
   const bool pq = c->v_codec == FADE_V_PQ;
+  const bool v4 = c->middle_v_bits == 4;
 #define FADE_CASE(D_, G_)                                                     \
   if (c->head_dim == D_ && G == G_)                                           \
-    return pq ? launch_mma<D_, G_, true>(c, L, a, sk, st)                     \
-              : launch_mma<D_, G_, false>(c, L, a, sk, st);
+    return pq ? launch_mma<D_, G_, true, 2>(c, L, a, sk, st)                  \
+              : v4 ? launch_mma<D_, G_, false, 4>(c, L, a, sk, st)            \
+                   : launch_mma<D_, G_, false, 2>(c, L, a, sk, st);
   FADE_CASE(64, 1) FADE_CASE(64, 2) FADE_CASE(64, 4) FADE_CASE(64, 8)
   FADE_CASE(128, 1) FADE_CASE(128, 2) FADE_CASE(128, 4) FADE_CASE(128, 8)
 #undef FADE_CASE

@@ -79,7 +79,7 @@ struct RowLens {
 // partial per unit segment it covers (split 1 + k for the k-th CTA of the unit; split 0 is the
 // FP16 tiers). The boundaries are weighted so that every CTA gets about the same work.
 constexpr int kMaxCtaSK = 320;   // persistent CTAs at most
-constexpr int kTileTokens = 256;
+constexpr int kTileTokens = FADE_ATTN_TILE_TOKENS;
 struct StreamK {
   int P;                               // persistent CTAs
   int B, H;

@@ -34,6 +34,7 @@ META_FIELDS = 8
 META = {"n_sink": 0, "n_mid": 1, "n_recent": 2, "head": 3, "cur": 4, "n_ev": 5}
 MAX_BATCH = 256
 STATUS_WORDS = 4
+ATTN_TILE_TOKENS = 256   # FADE_ATTN_TILE_TOKENS
 
 
 class FadeError(RuntimeError):
@@ -119,6 +120,7 @@ def lib():
             "fade_pq_train": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp]),
             "fade_check_status": (c_i32, [S(LayerT), c_vp]),
             "fade_tier_counts": (c_i32, [S(ConfigT), S(LayerT), c_vp]),
+            "fade_attention_tiled": (c_i32, [S(ConfigT)]),
             "fade_measure_fp32_rate": (c_i32, [c_i32, c_i32, c_vp, ctypes.POINTER(c_f64), c_vp]),
             "fade_selftest_bounded_wait": (c_i32, [c_vp, c_i32, c_i64, c_vp]),
             "fade_last_error": (ctypes.c_char_p, []),
@@ -470,6 +472,16 @@ def fade_measure_fp32_rate(blocks: int, iters: int, sink, stream=None) -> float:
     _check(lib().fade_measure_fp32_rate(int(blocks), int(iters), _ptr(sink), ctypes.byref(ops),
                                         _stream(stream)))
     return ops.value
+
+
+def fade_attention_tiled(cfg: Config) -> bool:
+    """Whether decode attention for ``cfg`` runs the tensor-core kernel, whose launch is
+    scheduled from every row's count of ATTN_TILE_TOKENS-token middle tiles (the host mirror
+    at the call), so that a captured call stays valid only while those counts are unchanged."""
+    r = lib().fade_attention_tiled(ctypes.byref(cfg.c()))
+    if r < 0:
+        raise FadeError(FADE_ERR_INVALID_ARGUMENT, fade_last_error())
+    return bool(r)
 
 
 def fade_tier_counts(layer: TieredLayer) -> np.ndarray:

@@ -66,6 +66,8 @@ class FadeCache:
         self._graph_events = []  # timing events referenced by captured graphs
         self.launches = 0       # kernels enqueued by step_layer calls
         self._pos_ring, self._pos_ring_ev, self._pos_ring_i = None, None, 0
+        self._growing = None        # (key, graph) of growing_step
+        self.growing_captures = 0   # captures made by growing_step
 
     # ------------------------------------------------------------------ session persistence
     # Page "FADE：面向LLM推理的注意力感知分层KV缓存压缩技术", §会话持久化: the compressed cache is
@@ -361,24 +363,35 @@ class FadeCache:
 
     # ------------------------------------------------------------------ growing caches
     def growing_graph_ok(self) -> bool:
-        """A step of this cache can be captured once and replayed while the cache grows: no
-        eviction, attention on the CUDA-core kernel (whose launch is sized by the middle
-        capacity; the tensor-core kernel's schedule follows the current counts), and every
-        row with full sinks and a full recent window, so that each step demotes one token
-        and appends one in every row."""
+        """A step of this cache can be captured and replayed while the cache grows: no
+        eviction, and every row with full sinks and a full recent window, so that each step
+        demotes one token and appends one in every row (see ``growing_graph_key`` for when a
+        captured step has to be captured again)."""
         c = self.cfg
-        if c.evicts or (c.middle_k_bits == 4 and c.middle_v_bits == 2):
+        if c.evicts:
             return False
         return all(bool((L.h_n_sink == c.n_sink).all() and (L.h_n_recent == c.recent_window).all())
                    for L in self.layers)
+
+    def growing_graph_key(self) -> tuple:
+        """What a captured growing step depends on beyond the device-side counts: with the
+        tensor-core attention kernel, every layer's and row's number of middle tiles at the
+        coming step's attention call (after its demotion: one more middle token), from which
+        the launch's stream-K schedule is built; nothing with the CUDA-core kernel, whose
+        launch is sized by the middle capacity."""
+        if not F.fade_attention_tiled(self.cfg):
+            return ()
+        t = F.ATTN_TILE_TOKENS
+        return tuple(tuple(((L.h_n_mid.astype(np.int64) + 1 + t - 1) // t).tolist())
+                     for L in self.layers)
 
     def capture_growing_step(self, q, k, v, out):
         """Capture every layer's step (positions excluded: ``replay_growing`` sets them) as a
         CUDA graph for a cache that grows by one token a step (see ``growing_graph_ok``).
         The host mirror is left as it was before the capture."""
         if not self.growing_graph_ok():
-            raise RuntimeError("capture_growing_step needs a growing cache without eviction, "
-                               "full sinks and recent windows, and CUDA-core attention")
+            raise RuntimeError("capture_growing_step needs a growing cache without eviction "
+                               "and with full sinks and recent windows")
         before = self.mirror()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
@@ -387,6 +400,18 @@ class FadeCache:
         for L, (s, m, r) in zip(self.layers, before):
             L.h_n_sink[:], L.h_n_mid[:], L.h_n_recent[:] = s, m, r
         return g
+
+    def growing_step(self, q, k, v, out):
+        """One step of a growing cache (``growing_graph_ok``) on fixed buffers through a
+        captured graph: captured on the first call and again whenever the buffers or
+        ``growing_graph_key`` change (a row's middle tier reaching a new tile, with the
+        tensor-core kernel), replayed otherwise."""
+        key = (tuple(x.data_ptr() for x in (q, k, v, out)), self.growing_graph_key())
+        if self._growing is None or self._growing[0] != key:
+            self._growing = None  # the previous graph is released before the next capture
+            self._growing = (key, self.capture_growing_step(q, k, v, out))
+            self.growing_captures += 1
+        self.replay_growing(self._growing[1])
 
     def replay_growing(self, graph):
         """One step from a graph of ``capture_growing_step``: the positions (from the host
