@@ -156,7 +156,8 @@ enum {
   FADE_META_HEAD = 3,     /* ring slot of the oldest recent token */
   FADE_META_CUR = 4,      /* live middle buffer, 0 or 1 */
   FADE_META_N_EV = 5,     /* evictions chosen and not yet committed (internal) */
-  FADE_META_P0 = 6,       /* internal (prefill) */
+  FADE_META_SYNC = 6,     /* internal: middle slots below this index hold the same K/V codes
+                             and scales in both buffers (0 after prefill or reset) */
   FADE_META_P1 = 7,       /* internal (prefill) */
   FADE_META_FIELDS = 8
 };

@@ -360,19 +360,21 @@ __global__ void __launch_bounds__(D) attn_combine_kernel(AttnArgs a, uint16_t* _
   }
 }
 
-// The tensor-core kernel's partials (split 0 + one per stream-K segment of the unit): one CTA of
+// The tensor-core kernel's partials (split 0 + one per stream-K segment of the unit).
 // One CTA per unit (row, KV head), one warp per query head, D/32 channels per lane. No
 // shared memory and no barrier: every lane reads the unit's partial count and the head's
-// (m, l) of every partial (the same addresses across the warp), forms M = max m_s, the
-// weights e^(m_s - M) and L = sum l_s e^(m_s - M) itself, and sums its channels of the
-// weighted partial outputs: out = sum acc_s e^(m_s - M) / L. The first kPre partials are
-// loaded before the count is known (slots below nsplit are in bounds).
+// (m, l) of every partial (the same addresses across the warp) and merges the partials in
+// chunks of kChunk with a running maximum: per chunk M' = max(M, m_s), the running sums are
+// scaled by e^(M - M') and each partial adds l_s e^(m_s - M') and acc_s e^(m_s - M');
+// out = acc / L. A chunk's loads depend only on nsplit (every slot below it is in bounds), so
+// they are issued before the count is known and masked by it afterwards. With at most kChunk
+// partials this is one pass with no rescaling.
 template <int D>
 __global__ void __launch_bounds__(256) attn_combine_sk_kernel(AttnArgs a,
                                                               uint16_t* __restrict__ out,
                                                               float* __restrict__ ml) {
   constexpr int CPL = D / 32;       // channels per lane
-  constexpr int kPre = 4;
+  constexpr int kChunk = 8;
   const int unit = blockIdx.x;
   const int b = unit / a.H, hk = unit % a.H;
   const int G = a.Hq / a.H;
@@ -385,46 +387,50 @@ __global__ void __launch_bounds__(256) attn_combine_sk_kernel(AttnArgs a,
   // partials are visible (a no-op when launched without the dependency)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int ns = max(1, min(a.nsplit, a.seg_count[unit]));
-  float acc[kPre][CPL], mv[kPre], lv[kPre];
-#pragma unroll
-  for (int i = 0; i < kPre; ++i) {
-    const bool in = i < a.nsplit;
-    mv[i] = in ? pm[2 * i] : -INFINITY;
-    lv[i] = in ? pm[2 * i + 1] : 0.f;
-    if constexpr (CPL == 4) {
-      const float4 v = in ? *reinterpret_cast<const float4*>(pa + (size_t)i * D)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-      acc[i][0] = v.x; acc[i][1] = v.y; acc[i][2] = v.z; acc[i][3] = v.w;
-    } else {
-      const float2 v = in ? *reinterpret_cast<const float2*>(pa + (size_t)i * D)
-                          : make_float2(0.f, 0.f);
-      acc[i][0] = v.x; acc[i][1] = v.y;
-    }
-  }
-  float M = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < kPre; ++i)
-    if (i < ns) M = fmaxf(M, mv[i]);
-  for (int s = kPre; s < ns; ++s) M = fmaxf(M, pm[2 * s]);
-  float L = 0.f, o[CPL];
+  float M = -INFINITY, L = 0.f, o[CPL];
 #pragma unroll
   for (int c = 0; c < CPL; ++c) o[c] = 0.f;
+  int s0 = 0;
+  do {
+    float acc[kChunk][CPL], mv[kChunk], lv[kChunk];
 #pragma unroll
-  for (int i = 0; i < kPre; ++i) {
-    if (i < ns) {
-      const float w = (mv[i] == -INFINITY) ? 0.f : __expf(mv[i] - M);
-      L = fmaf(lv[i], w, L);
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) o[c] = fmaf(acc[i][c], w, o[c]);
+    for (int i = 0; i < kChunk; ++i) {
+      const int s = s0 + i;
+      const bool in = s < a.nsplit;
+      mv[i] = in ? pm[2 * s] : -INFINITY;
+      lv[i] = in ? pm[2 * s + 1] : 0.f;
+      if constexpr (CPL == 4) {
+        const float4 v = in ? *reinterpret_cast<const float4*>(pa + (size_t)s * D)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        acc[i][0] = v.x; acc[i][1] = v.y; acc[i][2] = v.z; acc[i][3] = v.w;
+      } else {
+        const float2 v = in ? *reinterpret_cast<const float2*>(pa + (size_t)s * D)
+                            : make_float2(0.f, 0.f);
+        acc[i][0] = v.x; acc[i][1] = v.y;
+      }
     }
-  }
-  for (int s = kPre; s < ns; ++s) {
-    const float m = pm[2 * s];
-    const float w = (m == -INFINITY) ? 0.f : __expf(m - M);
-    L = fmaf(pm[2 * s + 1], w, L);
+    float Mc = M;
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) o[c] = fmaf(pa[(size_t)s * D + c], w, o[c]);
-  }
+    for (int i = 0; i < kChunk; ++i)
+      if (s0 + i < ns) Mc = fmaxf(Mc, mv[i]);
+    if (s0 > 0) {  // rescale what the earlier chunks summed (M finite: a partial has m > -inf)
+      const float r = (M == -INFINITY) ? 0.f : __expf(M - Mc);
+      L *= r;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) o[c] *= r;
+    }
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      if (s0 + i < ns) {
+        const float w = (mv[i] == -INFINITY) ? 0.f : __expf(mv[i] - Mc);
+        L = fmaf(lv[i], w, L);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) o[c] = fmaf(acc[i][c], w, o[c]);
+      }
+    }
+    M = Mc;
+    s0 += kChunk;
+  } while (s0 < ns);
   if (lane == 0) {
     ml[2 * bh] = M;
     ml[2 * bh + 1] = L;
@@ -448,9 +454,12 @@ struct AccArgs {
   float decay;
 };
 
-// One thread per storage slot of a unit: score update from the G heads' probabilities. The
-// G logits of the slot and the heads' (M, L) do not depend on the unit's counts, so they are
-// loaded first (for slots the unit does not hold they are read and dropped).
+// One thread per storage slot of a unit: score update from the G heads' probabilities. Every
+// load is issued before any of them is used: the G logits of the slot and the heads' (M, L)
+// do not depend on the unit's counts, and neither does the score's address except for a
+// middle slot, whose score is read from both ping-pong buffers and the live one kept (for
+// slots the unit does not hold the values are read and dropped). One round trip to memory
+// per thread, then the update.
 __global__ void __launch_bounds__(256) h2o_accumulate_kernel(AccArgs a) {
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= a.NS) return;
@@ -466,29 +475,131 @@ __global__ void __launch_bounds__(256) h2o_accumulate_kernel(AccArgs a) {
       lh[h] = a.ml[2 * bh + 1];
     }
   }
-  const int32_t* m = a.meta + unit * kF;
+  const int32_t* mp = a.meta + unit * kF;
+  const int4 m = make_int4(mp[FADE_META_N_SINK], mp[FADE_META_N_MID], mp[FADE_META_N_RECENT],
+                           mp[FADE_META_HEAD]);
+  const int cur = mp[FADE_META_CUR];
   float* sc;
+  float old0, old1 = 0.f;
+  int region;  // 0 sink, 1 middle, 2 ring
+  int idx;
   if (j < a.S) {
-    if (j >= m[FADE_META_N_SINK]) return;
+    region = 0;
+    idx = j;
     sc = a.sink_sc + (size_t)unit * a.S + j;
+    old0 = *sc;
   } else if (j < a.S + a.C) {
-    const int s = j - a.S;
-    if (s >= m[FADE_META_N_MID]) return;
-    sc = (m[FADE_META_CUR] ? a.mid_sc[1] : a.mid_sc[0]) + (size_t)unit * a.C + s;
+    region = 1;
+    idx = j - a.S;
+    const size_t o = (size_t)unit * a.C + idx;
+    old0 = a.mid_sc[0][o];
+    old1 = a.mid_sc[1][o];
+    sc = nullptr;
   } else {
-    const int r = j - a.S - a.C;
-    const int age = (r - m[FADE_META_HEAD] + a.W) % a.W;
-    if (age >= m[FADE_META_N_RECENT]) return;
-    sc = a.rec_sc + (size_t)unit * a.W + r;
+    region = 2;
+    idx = j - a.S - a.C;
+    sc = a.rec_sc + (size_t)unit * a.W + idx;
+    old0 = *sc;
   }
+  bool held;
+  float old;
+  if (region == 0) {
+    held = idx < m.x;
+    old = old0;
+  } else if (region == 1) {
+    held = idx < m.y;
+    sc = (cur ? a.mid_sc[1] : a.mid_sc[0]) + (size_t)unit * a.C + idx;
+    old = cur ? old1 : old0;
+  } else {
+    const int age = (idx - m.w + a.W) % a.W;
+    held = age < m.z;
+    old = old0;
+  }
+  if (!held) return;
   float psum = 0.f;
 #pragma unroll
   for (int h = 0; h < 8; ++h)
     if (h < G) psum += __expf(lg[h] - mh[h]) / lh[h];
   if (a.policy == FADE_EVICT_H2O)
-    *sc += psum;
+    *sc = old + psum;
   else
-    *sc = a.decay * *sc + (1.f - a.decay) * psum;
+    *sc = a.decay * old + (1.f - a.decay) * psum;
+}
+
+// The same update for four consecutive slots per thread (when the sink count and the slot
+// count are multiples of 4, so that a group of four never straddles two tiers and every
+// vector access is 16-byte aligned): the G heads' (M, L) are loaded once per four slots, the
+// logits and the scores (both middle buffers) as float4. Per slot the arithmetic is the scalar
+// kernel's, term for term.
+template <int G>
+__global__ void __launch_bounds__(256) h2o_accumulate4_kernel(AccArgs a) {
+  const int j0 = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (j0 >= a.NS) return;
+  const int hk = blockIdx.y, b = blockIdx.z, unit = b * a.H + hk;
+  float4 lg[G];
+  float mh[G], lh[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const size_t bh = (size_t)b * a.Hq + hk * G + h;
+    lg[h] = *reinterpret_cast<const float4*>(a.logits + bh * a.NS + j0);
+    mh[h] = a.ml[2 * bh];
+    lh[h] = a.ml[2 * bh + 1];
+  }
+  const int32_t* mp = a.meta + unit * kF;
+  const int n_sink = mp[FADE_META_N_SINK], n_mid = mp[FADE_META_N_MID];
+  const int n_rec = mp[FADE_META_N_RECENT], head = mp[FADE_META_HEAD], cur = mp[FADE_META_CUR];
+  float* sc;
+  float4 o0, o1 = make_float4(0.f, 0.f, 0.f, 0.f);
+  int region, idx;
+  if (j0 < a.S) {
+    region = 0;
+    idx = j0;
+    sc = a.sink_sc + (size_t)unit * a.S + j0;
+    o0 = *reinterpret_cast<const float4*>(sc);
+  } else if (j0 < a.S + a.C) {
+    region = 1;
+    idx = j0 - a.S;
+    const size_t off = (size_t)unit * a.C + idx;
+    o0 = *reinterpret_cast<const float4*>(a.mid_sc[0] + off);
+    o1 = *reinterpret_cast<const float4*>(a.mid_sc[1] + off);
+    sc = (cur ? a.mid_sc[1] : a.mid_sc[0]) + off;
+  } else {
+    region = 2;
+    idx = j0 - a.S - a.C;
+    sc = a.rec_sc + (size_t)unit * a.W + idx;
+    o0 = *reinterpret_cast<const float4*>(sc);
+  }
+  const float4 ov = (region == 1 && cur) ? o1 : o0;
+  const float old[4] = {ov.x, ov.y, ov.z, ov.w};
+  float nv[4];
+  bool held[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    if (region == 0) {
+      held[e] = idx + e < n_sink;
+    } else if (region == 1) {
+      held[e] = idx + e < n_mid;
+    } else {
+      int age = idx + e - head;
+      if (age < 0) age += a.W;
+      held[e] = age < n_rec;
+    }
+    float psum = 0.f;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float l = e == 0 ? lg[h].x : e == 1 ? lg[h].y : e == 2 ? lg[h].z : lg[h].w;
+      psum += __expf(l - mh[h]) / lh[h];
+    }
+    nv[e] = a.policy == FADE_EVICT_H2O ? old[e] + psum
+                                       : a.decay * old[e] + (1.f - a.decay) * psum;
+  }
+  if (held[0] && held[1] && held[2] && held[3]) {
+    *reinterpret_cast<float4*>(sc) = make_float4(nv[0], nv[1], nv[2], nv[3]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (held[e]) sc[e] = nv[e];
+  }
 }
 
 template <int D, int KB, int VB, int G, bool PQ>
@@ -680,7 +791,20 @@ extern "C" fade_status_t fade_h2o_accumulate(const fade_config_t* c, fade_layer_
   a.NS = a.S + a.C + a.W;
   a.policy = c->policy;
   a.decay = c->ema_decay;
-  h2o_accumulate_kernel<<<dim3(ceil_div(a.NS, 256), c->num_kv_heads, c->batch), 256, 0,
-                          as_stream(stream)>>>(a);
+  const int G = c->num_q_heads / c->num_kv_heads;
+  cudaStream_t cs = as_stream(stream);
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (a.S % 4 == 0 && a.NS % 4 == 0 && al16(a.logits) && al16(a.sink_sc) && al16(a.mid_sc[0]) &&
+      al16(a.mid_sc[1]) && al16(a.rec_sc)) {
+    const dim3 grid(ceil_div(a.NS / 4, 256), c->num_kv_heads, c->batch);
+    switch (G) {
+      case 1: h2o_accumulate4_kernel<1><<<grid, 256, 0, cs>>>(a); break;
+      case 2: h2o_accumulate4_kernel<2><<<grid, 256, 0, cs>>>(a); break;
+      case 4: h2o_accumulate4_kernel<4><<<grid, 256, 0, cs>>>(a); break;
+      default: h2o_accumulate4_kernel<8><<<grid, 256, 0, cs>>>(a); break;
+    }
+  } else {
+    h2o_accumulate_kernel<<<dim3(ceil_div(a.NS, 256), c->num_kv_heads, c->batch), 256, 0, cs>>>(a);
+  }
   return launch_status("fade_h2o_accumulate");
 }

@@ -531,7 +531,7 @@ struct MidCfg {
 // the victim prefixes of the block.
 template <int D>
 size_t compact_smem(int H) {
-  return (size_t)MidCfg<D>::TABF4 * 16 + (size_t)H * (MidCfg<D>::PRE_SEL + 4) * 4;
+  return (size_t)MidCfg<D>::TABF4 * 16 + (size_t)H * (MidCfg<D>::PRE_SEL + 5) * 4;
 }
 
 template <int D>
@@ -798,12 +798,12 @@ __device__ __forceinline__ void stg_words(void* p, const uint32_t (&w)[W]) {
 
 // Compact survivors of the live middle buffer into the other one, re-positioning keys whose
 // index drops (the recent rings follow in evict_recent_commit_kernel).
-// grid = (ceil(max_mid / TOK), B), 256 threads; one CTA takes one block of TOK middle indices
-// of one batch row and loops over the row's KV heads. A middle token is handled by D/64
-// adjacent threads (MidCfg); thread t_ of a token owns its quantisation groups g1 = t_ and
-// g2 = t_ + D/64, whose channels are each other's rotation partners. A moved key is
-// dequantised, un-RoPE'd at its old position and re-RoPE'd at its new one, rounded to fp16 and
-// re-quantised, all in the owning thread. The RoPE rows the block needs (its old positions
+// grid = (B, ceil(max_mid / TOK)), 256 threads (a row's blocks in reverse order); one CTA
+// takes one block of TOK middle indices of one batch row and loops over the row's KV heads.
+// A middle token is handled by D/64 adjacent threads (MidCfg); thread t_ of a token owns its
+// quantisation groups g1 = t_ and g2 = t_ + D/64, whose channels are each other's rotation
+// partners. A moved key is dequantised, un-RoPE'd at its old position and re-RoPE'd at its new
+// one, rounded to fp16 and re-quantised, all in the owning thread. The RoPE rows the block needs (its old positions
 // and the new ones, at most 16 below) are staged once per CTA in shared memory and serve
 // every head; each head's codes, scales and score are loaded into registers one head ahead.
 // SEL: a selection policy (victims from the bitmap of evict_select_kernel) whose block's bitmap
@@ -821,14 +821,21 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MINB) evict_compact_kernel(L
   extern __shared__ float4 tab[];              // [NROWS][ROWF4 + 1], then hinfo, hpre
   int* hinfo = reinterpret_cast<int*>(tab + CC::TABF4);  // [H][4]: n_mid n_ev n_sink cur
   int* hpre = hinfo + a.H * 4;                           // [H][PRE]
-  __shared__ int s_rlo, s_rhi;
-  const int b = blockIdx.y;
+  // [H]: the head's block lies below both the agreement index of the two middle buffers and
+  // the first victim: its codes and scales are already in place, only its scores are copied
+  int* hlight = hpre + a.H * PRE;
+  __shared__ int s_rlo, s_rhi, s_any;
+  const int b = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-  const int lo = blockIdx.x * TOK;
+  // blocks in reverse index order, rows fastest: under a selection policy a block's work
+  // grows with its index (every key after a unit's victim is re-positioned, the ones before
+  // it are copied), so the heaviest blocks of every row are scheduled first
+  const int lo = (gridDim.y - 1 - blockIdx.y) * TOK;
   if (threadIdx.x == 0) {
     s_rlo = 0x7fffffff;
     s_rhi = -1;
+    s_any = 0;
   }
   __syncthreads();
   // per-head bookkeeping (warp w takes heads w, w+8, ...): counts, the victims before each
@@ -871,19 +878,28 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MINB) evict_compact_kernel(L
         if (lane >= o) incl += tt;
       }
       if (lane <= TOK / 32) hpre[h * PRE + lane] = incl - wc;
-      if (lane == 0)
-        hpre[h * PRE + TOK / 32 + 1] =
-            a.chunk_base[(size_t)unit * a.chunk_slots + lo / kChunk] + c;
+      const int before_lo = a.chunk_base[(size_t)unit * a.chunk_slots + lo / kChunk] + c;
+      if (lane == 0) hpre[h * PRE + TOK / 32 + 1] = before_lo;
+      if constexpr (SEL) {
+        const int in_block = __shfl_sync(0xffffffffu, incl, TOK / 32 - 1);
+        const bool light = hi <= m[FADE_META_SYNC] && before_lo + in_block == 0;
+        if (lane == 0) hlight[h] = light ? 1 : 0;
+        if (light) {
+          if (lane == 0) s_any = 1;
+          continue;
+        }
+      }
     }
     if (lane == 0) {
+      s_any = 1;
       atomicMin(&s_rlo, n_sink + max(0, lo - n_ev));  // lowest new position of the block
       atomicMax(&s_rhi, n_sink + hi);                  // one past the highest old position
     }
   }
   __syncthreads();
   const int rlo = s_rlo, rhi = s_rhi;
-  if (rhi < 0) return;  // no head has work in this block (uniform per CTA)
-  const bool staged = a.table != nullptr && rhi - rlo <= CC::NROWS;
+  if (!s_any) return;  // no head has work in this block (uniform per CTA)
+  const bool staged = a.table != nullptr && rhi >= 0 && rhi - rlo <= CC::NROWS;
   if (staged) {
     const float4* src = reinterpret_cast<const float4*>(a.table) + (size_t)rlo * CC::ROWF4;
     for (int e = threadIdx.x; e < (rhi - rlo) * CC::ROWF4; e += 256) {
@@ -910,6 +926,10 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MINB) evict_compact_kernel(L
     const int4 m = hinfo4[hh];
     if (i < m.x) {
       const uint32_t r = row0 + (uint32_t)hh * (uint32_t)a.C + (uint32_t)i;
+      if (SEL && hlight[hh]) {  // the score only
+        d.sc = __ldg((m.w ? a.mid_sc[1] : a.mid_sc[0]) + r);
+        return;
+      }
       const uint8_t* kr = (m.w ? a.mk[1] : a.mk[0]) + (size_t)r * KROW;
       ldg_words(kr + g1 * GB, d.k1);
       ldg_words(kr + g2 * GB, d.k2);
@@ -932,6 +952,14 @@ __global__ void __launch_bounds__(256, FADE_COMPACT_MINB) evict_compact_kernel(L
     const int4 m = hinfo4[h];
     const int n_mid = m.x, n_ev = m.y, n_sink = m.z;
     const bool cbuf = m.w != 0;
+    if (SEL && hlight[h]) {  // uniform per CTA: no victim before the block, codes in place
+      if (i < n_mid && t_ == 0)
+        (cbuf ? a.mid_sc[0] : a.mid_sc[1])[row0 + (uint32_t)h * (uint32_t)a.C + (uint32_t)i] =
+            cur.sc;
+      cur = nxt;
+      h = hn;
+      continue;
+    }
     // The TPT lanes of one token lie in one warp and share every flag below, so the warp-wide
     // ballot sees whole tokens; nothing exits before it.
     const bool in_range = i < n_mid;
@@ -1092,7 +1120,20 @@ __global__ void __launch_bounds__(256) evict_recent_commit_kernel(LayerArgs a) {
       }
     }
   }
+  // the first victim of the unit: both middle buffers now hold the same codes and scales
+  // below it (the compaction copied them or found them equal), which the next compaction
+  // uses to skip them. Position eviction drops the oldest tokens: 0.
+  __shared__ int s_first;
+  if (threadIdx.x == 0) s_first = 0x7fffffff;
   __syncthreads();  // every thread is done with the counts read above
+  if (!a.positional && hinfo[4 * hb + 1] > 0) {
+    const uint32_t* bm = a.victims + (size_t)(b * a.H + hb) * a.victim_words;
+    for (int w = threadIdx.x; w < (hinfo[4 * hb + 0] + 31) / 32; w += 256) {
+      const uint32_t x = bm[w];
+      if (x) atomicMin(&s_first, 32 * w + __ffs(x) - 1);
+    }
+  }
+  __syncthreads();
   for (int h = hb + threadIdx.x; h < hb + 1; h += 256) {
     int32_t* m = a.meta + (b * a.H + h) * kF;
     const int n_ev = a.positional ? max(0, m[FADE_META_N_MID] - a.budget) : m[FADE_META_N_EV];
@@ -1100,6 +1141,7 @@ __global__ void __launch_bounds__(256) evict_recent_commit_kernel(LayerArgs a) {
       m[FADE_META_N_MID] -= n_ev;
       m[FADE_META_CUR] ^= 1;
       m[FADE_META_N_EV] = 0;
+      m[FADE_META_SYNC] = (a.positional || s_first == 0x7fffffff) ? 0 : s_first;
     }
   }
 }
@@ -1235,6 +1277,7 @@ __global__ void __launch_bounds__(256) evict_recent_commit_rows_kernel(LayerArgs
     m[FADE_META_N_MID] = n_mid - n_ev;
     m[FADE_META_CUR] ^= 1;
     m[FADE_META_N_EV] = 0;
+    m[FADE_META_SYNC] = 0;  // (this path's compaction reads no agreement index)
   }
 }
 
@@ -1358,7 +1401,7 @@ __global__ void prefill_commit_kernel(LayerArgs a, RowLens lens, int units) {
   m[FADE_META_HEAD] = 0;
   m[FADE_META_CUR] = 0;
   m[FADE_META_N_EV] = 0;
-  m[FADE_META_P0] = 0;
+  m[FADE_META_SYNC] = 0;
   m[FADE_META_P1] = 0;
 }
 
@@ -1398,7 +1441,7 @@ struct CompactLaunch {
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
       return launch_status("fade_evict_rerope compact shared-memory opt-in");
-    kern<<<dim3(chunks, B), 256, smem, st>>>(a);
+    kern<<<dim3(B, chunks), 256, smem, st>>>(a);
     return launch_status("fade_evict_rerope compact");
   }
 };

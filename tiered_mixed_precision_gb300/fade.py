@@ -31,7 +31,7 @@ def pq_train_ws_bytes(dim: int) -> int:
     """FADE_PQ_TRAIN_WS_BYTES(dim)."""
     return dim * 2304 + 1024
 META_FIELDS = 8
-META = {"n_sink": 0, "n_mid": 1, "n_recent": 2, "head": 3, "cur": 4, "n_ev": 5}
+META = {"n_sink": 0, "n_mid": 1, "n_recent": 2, "head": 3, "cur": 4, "n_ev": 5, "sync": 6}
 MAX_BATCH = 256
 STATUS_WORDS = 4
 ATTN_TILE_TOKENS = 256   # FADE_ATTN_TILE_TOKENS
