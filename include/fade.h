@@ -358,6 +358,18 @@ fade_status_t fade_evict_rerope(const fade_config_t* cfg, fade_layer_t* layer,
 fade_status_t fade_cache_append(const fade_config_t* cfg, fade_layer_t* layer,
                                 const uint16_t* k_rot, const uint16_t* v, void* stream);
 
+/* A decode step's RoPE and append in one launch (FADE-zh §第一层 and §RoPE方案兼容性): the
+ * result of fade_rope_apply on q_raw (fp16 [B][Hq][d]) into q_rot and on k_raw (fp16
+ * [B][H][d]), every vector of row b at position pos[b] (pos: DEVICE i32 [B]; group_len Hq
+ * resp. H, pos_step 0), followed by fade_cache_append of the rotated key and v (fp16
+ * [B][H][d]), bit for bit; the rotated key goes straight into its slot (no k_rot buffer).
+ * table / max_pos as for fade_rope_apply (unused for FADE_ROPE_NONE: a copy). Errors as for
+ * the two calls it replaces: FADE_ERR_CAPACITY (recent window full) before any launch. */
+fade_status_t fade_rope_append(const fade_config_t* cfg, fade_layer_t* layer, const float* table,
+                               int32_t max_pos, const uint16_t* q_raw, const uint16_t* k_raw,
+                               const uint16_t* v, const int32_t* pos, uint16_t* q_rot,
+                               void* stream);
+
 /* Decode attention (FADE-zh §项目结构与代码质量, kernels/: fused INT4 dequant + SDPA; KVLong
  * §1.2: softmax-weighted average of V). q_rot: fp16 [B][Hq][d] RoPE'd at the new token's
  * position; out: fp16 [B][Hq][d]. Every query head h attends, with scale 1/sqrt(d), to

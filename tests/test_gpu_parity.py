@@ -119,6 +119,60 @@ def test_rope_table_and_apply(T, key):
     assert np.abs(ordered(got16) - ordered(want16)).max() <= 1
 
 
+@pytest.mark.parametrize("d,hq,hkv,rope,prompt", [
+    (128, 8, 2, "default", 30),       # ring slots
+    (128, 4, 4, "default", 2),        # sink slots (fewer than n_sink held)
+    (64, 16, 2, "prop48", 30),        # proportional RoPE, G = 8
+    (64, 8, 2, "none", 30),           # no positional encoding: copies
+])
+def test_rope_append_fused_matches_separate_calls(T, d, hq, hkv, rope, prompt):
+    """fade_rope_append gives q_rot and the appended key, value, score and counts bit for bit
+    as fade_rope_apply (q and k) followed by fade_cache_append, over several steps."""
+    import torch
+
+    from synth import draw_prompt, draw_vectors
+    from tiered_mixed_precision_gb300.model import FadeCache
+
+    r = {"default": Rope("default", 1e4), "none": Rope("none"),
+         "prop48": _SCALED_ROPES["prop48_llama3"]}[rope]
+    wl = get_workload(4).scaled(layers=1, batch=3, num_q_heads=hq, num_kv_heads=hkv,
+                                head_dim=d, prompt_len=prompt, int4_budget=200, rope=r, steps=3)
+
+    def make():
+        fc = FadeCache(T.Config.from_workload(wl), 1, prompt, prompt + 16, "cuda")
+        pr = draw_prompt(wl, 0)
+        fc.prefill(0, torch.from_numpy(pr["k"]).cuda(), torch.from_numpy(pr["v"]).cuda())
+        return fc
+
+    sep, fus = make(), make()
+    B = wl.batch
+    for step in range(3):
+        q = torch.from_numpy(draw_vectors(wl, "q", (B, hq, d), "fuse", step)).cuda()
+        k = torch.from_numpy(draw_vectors(wl, "k", (B, hkv, d), "fuse", step)).cuda()
+        v = torch.from_numpy(draw_vectors(wl, "v", (B, hkv, d), "fuse", step)).cuda()
+        for fc in (sep, fus):
+            fc.set_positions(fc.next_positions())
+        c, L = sep.cfg, sep.layers[0]
+        k_rot = torch.empty_like(k)
+        T.fade.fade_rope_apply(c, sep.table, sep.max_pos, q, sep.q_rot, B, hq, sep.pos, 0)
+        T.fade.fade_rope_apply(c, sep.table, sep.max_pos, k, k_rot, B, hkv, sep.pos, 0)
+        T.fade.fade_cache_append(L, k_rot, v)
+        T.fade.fade_rope_append(fus.layers[0], fus.table, fus.max_pos, q, k, v, fus.pos,
+                                fus.q_rot)
+        torch.cuda.synchronize()
+        assert torch.equal(sep.q_rot.view(torch.int16), fus.q_rot.view(torch.int16)), step
+        for b in range(B):
+            for h in range(hkv):
+                x, y = sep.unit_state(0, b, h), fus.unit_state(0, b, h)
+                for key in x:
+                    if isinstance(x[key], np.ndarray):
+                        assert np.array_equal(x[key], y[key]), (step, b, h, key)
+                    else:
+                        assert x[key] == y[key], (step, b, h, key)
+        assert (sep.layers[0].h_n_recent == fus.layers[0].h_n_recent).all()
+        assert (sep.layers[0].h_n_sink == fus.layers[0].h_n_sink).all()
+
+
 def _small(key):
     if key == "1":
         return get_workload(1).scaled(steps=6), None

@@ -420,6 +420,76 @@ __global__ void __launch_bounds__(32) append_kernel(LayerArgs a, const uint16_t*
   }
 }
 
+// One CTA per unit (row b, KV head h): a decode step's RoPE and append in one launch. The
+// unit's G query heads and its new key are rotated at the row's position exactly as
+// rope_apply_kernel rotates them (slot k < rh rotates the pair (k, k + rh) with the table's
+// cos and sin, the remaining slots copy their two pass-through channels; no table: a copy),
+// the queries into q_rot and the key straight into the slot append_kernel gives it (a sink
+// while fewer than n_sink are held, else the newest ring entry), with its value and score 0.
+template <int D>
+__global__ void __launch_bounds__(128)
+    rope_append_kernel(LayerArgs a, const float* __restrict__ table, int max_pos, int rh,
+                       const uint16_t* __restrict__ q_raw, const uint16_t* __restrict__ k_raw,
+                       const uint16_t* __restrict__ v, const int32_t* __restrict__ pos,
+                       uint16_t* __restrict__ q_rot, int Hq) {
+  constexpr int half = D / 2;
+  const int h = blockIdx.x, b = blockIdx.y, unit = b * a.H + h;
+  const int G = Hq / a.H;
+  const int p = table ? min(max(pos[b], 0), max_pos - 1) : 0;
+  // one slot of vector x (D channels) into y
+  auto rot = [&](const uint16_t* x, uint16_t* y, int k) {
+    if (!table) {
+      y[k] = x[k];
+      y[k + half] = x[k + half];
+    } else if (k >= rh) {
+      const int c = 2 * rh + 2 * (k - rh);
+      y[c] = x[c];
+      y[c + 1] = x[c + 1];
+    } else {
+      float y1, y2;
+      rotate_pair(h2f(x[k]), h2f(x[k + rh]), rope_cos(table, half, p, k),
+                  rope_sin(table, half, p, k), y1, y2);
+      y[k] = f2h(y1);
+      y[k + rh] = f2h(y2);
+    }
+  };
+  for (int i = threadIdx.x; i < G * half; i += blockDim.x) {
+    const size_t base = ((size_t)b * Hq + (size_t)h * G + i / half) * D;
+    rot(q_raw + base, q_rot + base, i % half);
+  }
+  int32_t* m = a.meta + unit * kF;
+  const int n_sink = m[FADE_META_N_SINK], n_rec = m[FADE_META_N_RECENT];
+  const bool to_sink = n_sink < a.S;
+  if (!to_sink && n_rec >= a.W) {  // the host checks capacity; never overwrite the ring
+    if (threadIdx.x == 0) record_status(a.status, kCheckAppendSlot);
+    return;
+  }
+  size_t row;
+  uint16_t *dk, *dv;
+  float* dsc;
+  if (to_sink) {
+    row = (size_t)unit * a.S + n_sink;
+    dk = a.sink_k + row * D;
+    dv = a.sink_v + row * D;
+    dsc = a.sink_sc + row;
+  } else {
+    row = (size_t)unit * a.W + (m[FADE_META_HEAD] + n_rec) % a.W;
+    dk = a.rec_k + row * D;
+    dv = a.rec_v + row * D;
+    dsc = a.rec_sc + row;
+  }
+  for (int k = threadIdx.x; k < half; k += blockDim.x) rot(k_raw + (size_t)unit * D, dk, k);
+  for (int c = threadIdx.x; c < D; c += blockDim.x) dv[c] = v[(size_t)unit * D + c];
+  __syncthreads();  // every thread has read the counts
+  if (threadIdx.x == 0) {
+    *dsc = 0.f;
+    if (to_sink)
+      m[FADE_META_N_SINK] = n_sink + 1;
+    else
+      m[FADE_META_N_RECENT] = n_rec + 1;
+  }
+}
+
 // ----------------------------------------------------------------- eviction (decode)
 // One CTA per unit: choose N_MID - budget victims among the live middle tier.
 // Copies unit `from`'s victim bitmap (n candidates) and chunk prefixes to unit `to`.
@@ -803,9 +873,10 @@ __device__ __forceinline__ void stg_words(void* p, const uint32_t (&w)[W]) {
 // A middle token is handled by D/64 adjacent threads (MidCfg); thread t_ of a token owns its
 // quantisation groups g1 = t_ and g2 = t_ + D/64, whose channels are each other's rotation
 // partners. A moved key is dequantised, un-RoPE'd at its old position and re-RoPE'd at its new
-// one, rounded to fp16 and re-quantised, all in the owning thread. The RoPE rows the block needs (its old positions
-// and the new ones, at most 16 below) are staged once per CTA in shared memory and serve
-// every head; each head's codes, scales and score are loaded into registers one head ahead.
+// one, rounded to fp16 and re-quantised, all in the owning thread. The RoPE rows the block
+// needs (its old positions and the new ones, at most 16 below) are staged once per CTA in
+// shared memory and serve every head; each head's codes, scales and score are loaded into
+// registers one head ahead.
 // SEL: a selection policy (victims from the bitmap of evict_select_kernel) whose block's bitmap
 // words are staged in shared memory with their prefix counts; false: the code for every policy,
 // with the victims' prefix read from the bitmap per token (the position policy's instantiation).
@@ -1612,6 +1683,45 @@ extern "C" fade_status_t fade_cache_append(const fade_config_t* c, fade_layer_t*
   else
     append_kernel<128><<<grid, 32, 0, as_stream(stream)>>>(a, k_rot, v);
   if ((st = launch_status("fade_cache_append"))) return st;
+  for (int b = 0; b < c->batch; ++b) {
+    if (L->h_n_sink[b] < c->n_sink)
+      L->h_n_sink[b] += 1;
+    else
+      L->h_n_recent[b] += 1;
+  }
+  return FADE_OK;
+}
+
+extern "C" fade_status_t fade_rope_append(const fade_config_t* c, fade_layer_t* L,
+                                          const float* table, int32_t max_pos,
+                                          const uint16_t* q_raw, const uint16_t* k_raw,
+                                          const uint16_t* v, const int32_t* pos,
+                                          uint16_t* q_rot, void* stream) {
+  clear_error();
+  FADE_RANGE("fade_rope_append");
+  fade_status_t st = validate_config(c);
+  if (!st) st = validate_layer(c, L);
+  if (st) return st;
+  if (!q_raw || !k_raw || !v || !pos || !q_rot)
+    return set_error(FADE_ERR_INVALID_ARGUMENT, "NULL q_raw, k_raw, v, pos or q_rot");
+  const bool rope = c->rope.kind != FADE_ROPE_NONE;
+  if (rope && (!table || max_pos < 1))
+    return set_error(FADE_ERR_INVALID_ARGUMENT, "NULL RoPE table");
+  for (int b = 0; b < c->batch; ++b)
+    if (L->h_n_sink[b] >= c->n_sink && L->h_n_recent[b] >= c->recent_window)
+      return set_error(FADE_ERR_CAPACITY, "row %d: recent window full (demote first)", b);
+  const LayerArgs a = make_args(c, L, nullptr);
+  const dim3 grid(c->num_kv_heads, c->batch);
+  const float* t = rope ? table : nullptr;
+  const int rh = rotary_width(c) / 2;
+  cudaStream_t s = as_stream(stream);
+  if (c->head_dim == 64)
+    rope_append_kernel<64><<<grid, 128, 0, s>>>(a, t, max_pos, rh, q_raw, k_raw, v, pos, q_rot,
+                                                c->num_q_heads);
+  else
+    rope_append_kernel<128><<<grid, 128, 0, s>>>(a, t, max_pos, rh, q_raw, k_raw, v, pos, q_rot,
+                                                 c->num_q_heads);
+  if ((st = launch_status("fade_rope_append"))) return st;
   for (int b = 0; b < c->batch; ++b) {
     if (L->h_n_sink[b] < c->n_sink)
       L->h_n_sink[b] += 1;

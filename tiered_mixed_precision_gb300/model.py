@@ -57,11 +57,10 @@ class FadeCache:
         self._pos_host = torch.zeros(cfg.batch, dtype=torch.int32).pin_memory() \
             if self.device.type == "cuda" else torch.zeros(cfg.batch, dtype=torch.int32)
         self.needs_logits = cfg.policy in ("h2o", "ema")
-        # rotated copies of the step's q and k (the caller's raw inputs stay intact)
+        # rotated copy of the step's q (the caller's raw inputs stay intact; the rotated key
+        # goes straight into its cache slot)
         self.q_rot = torch.empty((cfg.batch, cfg.num_q_heads, cfg.head_dim), dtype=torch.float16,
                                  device=self.device)
-        self.k_rot = torch.empty((cfg.batch, cfg.num_kv_heads, cfg.head_dim),
-                                 dtype=torch.float16, device=self.device)
         self.timers = None      # optional {"attention": [...], "evict": [...]} of event pairs
         self._graph_events = []  # timing events referenced by captured graphs
         self.launches = 0       # kernels enqueued by step_layer calls
@@ -197,16 +196,13 @@ class FadeCache:
 
     def attend_layer(self, layer: int, q_raw: torch.Tensor, k_raw: torch.Tensor,
                      v: torch.Tensor, out: torch.Tensor):
-        """The rest of a layer's decode step: RoPE of the new q and k (into work buffers, at the
-        positions last set by ``set_positions``), append, attention, H2O / EMA accumulation."""
+        """The rest of a layer's decode step: RoPE of the new q (into a work buffer) and k at
+        the positions last set by ``set_positions`` and the append of the new token, in one
+        launch (``fade_rope_append``); attention; H2O / EMA accumulation."""
         c = self.cfg
         L = self.layers[layer]
-        F.fade_rope_apply(c, self.table, self.max_pos, q_raw, self.q_rot, c.batch,
-                          c.num_q_heads, self.pos, 0)
-        F.fade_rope_apply(c, self.table, self.max_pos, k_raw, self.k_rot, c.batch,
-                          c.num_kv_heads, self.pos, 0)
-        n = 2 if c.rope_kind != "none" else 0
-        F.fade_cache_append(L, self.k_rot, v)
+        F.fade_rope_append(L, self.table, self.max_pos, q_raw, k_raw, v, self.pos, self.q_rot)
+        n = 1
         t = self._tick("attention")
         F.fade_decode_attention(L, self.q_rot, out, self.logits if self.needs_logits else None,
                                 self.ml, self.ws)
