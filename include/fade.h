@@ -363,12 +363,15 @@ fade_status_t fade_cache_append(const fade_config_t* cfg, fade_layer_t* layer,
  * [B][H][d]), every vector of row b at position pos[b] (pos: DEVICE i32 [B]; group_len Hq
  * resp. H, pos_step 0), followed by fade_cache_append of the rotated key and v (fp16
  * [B][H][d]), bit for bit; the rotated key goes straight into its slot (no k_rot buffer).
- * table / max_pos as for fade_rope_apply (unused for FADE_ROPE_NONE: a copy). Errors as for
- * the two calls it replaces: FADE_ERR_CAPACITY (recent window full) before any launch. */
+ * demote != 0: fade_cache_demote first, in the same launch (for a step in which no eviction
+ * separates the demotion from the append: a cache that does not evict, or whose middle tier
+ * stays within its budget). table / max_pos as for fade_rope_apply (unused for
+ * FADE_ROPE_NONE: a copy). Errors as for the calls it replaces (FADE_ERR_CAPACITY: the recent
+ * window full without demotion, or the middle tier full), before any launch. */
 fade_status_t fade_rope_append(const fade_config_t* cfg, fade_layer_t* layer, const float* table,
                                int32_t max_pos, const uint16_t* q_raw, const uint16_t* k_raw,
                                const uint16_t* v, const int32_t* pos, uint16_t* q_rot,
-                               void* stream);
+                               int32_t demote, void* stream);
 
 /* Decode attention (FADE-zh §项目结构与代码质量, kernels/: fused INT4 dequant + SDPA; KVLong
  * §1.2: softmax-weighted average of V). q_rot: fp16 [B][Hq][d] RoPE'd at the new token's

@@ -173,6 +173,66 @@ def test_rope_append_fused_matches_separate_calls(T, d, hq, hkv, rope, prompt):
         assert (sep.layers[0].h_n_sink == fus.layers[0].h_n_sink).all()
 
 
+@pytest.mark.parametrize("d,kb,vb,codec", [(128, 4, 4, "int"), (64, 4, 2, "int"),
+                                            (64, 2, 2, "int"), (128, 4, 2, "pq")])
+def test_rope_append_with_demotion_matches_separate_calls(T, d, kb, vb, codec):
+    """fade_rope_append with demote: the demotion (K and V quantise-packed, or V PQ-encoded,
+    into the next middle slot, the score moved), the RoPE of q and k and the append, in one
+    launch, bit for bit as fade_cache_demote, fade_rope_apply twice and fade_cache_append."""
+    import torch
+
+    from synth import draw_prompt, draw_vectors
+    from synth.draws import pq_calibration
+    from tiered_mixed_precision_gb300.model import FadeCache
+
+    wl = get_workload(2).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2, head_dim=d,
+                                middle_k_bits=kb, middle_v_bits=vb, prompt_len=100, steps=3)
+
+    def make():
+        cfg = T.Config.from_workload(wl, mid_capacity=200)
+        cfg.v_codec = codec
+        fc = FadeCache(cfg, 1, 100, 120, "cuda")
+        if codec == "pq":
+            rows = pq_calibration(wl, 256)
+            cb = rows.reshape(256, d // 4, 4).transpose(1, 0, 2).copy()
+            fc.set_pq_codebook(torch.from_numpy(cb).cuda())
+        pr = draw_prompt(wl, 0)
+        fc.prefill(0, torch.from_numpy(pr["k"]).cuda(), torch.from_numpy(pr["v"]).cuda())
+        return fc
+
+    sep, fus = make(), make()
+    assert (sep.layers[0].h_n_recent == wl.recent_window).all()   # every step demotes
+    B, hq, hkv = wl.batch, wl.num_q_heads, wl.num_kv_heads
+    for step in range(3):
+        q = torch.from_numpy(draw_vectors(wl, "q", (B, hq, d), "fuse_dem", step)).cuda()
+        k = torch.from_numpy(draw_vectors(wl, "k", (B, hkv, d), "fuse_dem", step)).cuda()
+        v = torch.from_numpy(draw_vectors(wl, "v", (B, hkv, d), "fuse_dem", step)).cuda()
+        for fc in (sep, fus):
+            fc.set_positions(fc.next_positions())
+        c, L = sep.cfg, sep.layers[0]
+        k_rot = torch.empty_like(k)
+        T.fade.fade_cache_demote(L)
+        T.fade.fade_rope_apply(c, sep.table, sep.max_pos, q, sep.q_rot, B, hq, sep.pos, 0)
+        T.fade.fade_rope_apply(c, sep.table, sep.max_pos, k, k_rot, B, hkv, sep.pos, 0)
+        T.fade.fade_cache_append(L, k_rot, v)
+        T.fade.fade_rope_append(fus.layers[0], fus.table, fus.max_pos, q, k, v, fus.pos,
+                                fus.q_rot, demote=True)
+        torch.cuda.synchronize()
+        assert torch.equal(sep.q_rot.view(torch.int16), fus.q_rot.view(torch.int16)), step
+        for b in range(B):
+            for h in range(hkv):
+                x, y = sep.unit_state(0, b, h), fus.unit_state(0, b, h)
+                for key in x:
+                    if isinstance(x[key], np.ndarray):
+                        assert np.array_equal(x[key], y[key]), (step, b, h, key)
+                    else:
+                        assert x[key] == y[key], (step, b, h, key)
+        for name in ("h_n_sink", "h_n_mid", "h_n_recent"):
+            assert (getattr(sep.layers[0], name) == getattr(fus.layers[0], name)).all(), name
+        assert fus.layers[0].meta.cpu().numpy()[:, :, 3].tolist() == \
+            sep.layers[0].meta.cpu().numpy()[:, :, 3].tolist()   # ring heads
+
+
 def _small(key):
     if key == "1":
         return get_workload(1).scaled(steps=6), None

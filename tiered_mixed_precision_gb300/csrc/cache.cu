@@ -347,6 +347,27 @@ __global__ void reset_kernel(int32_t* meta, int n) {
   if (i < n) meta[i] = 0;
 }
 
+// One warp: the oldest ring token (slot `head`) of a unit quantise-packed into middle slot
+// n_mid of buffer `cur` (K at KB bits; V at VB bits, or PQ-encoded), its score moved with it.
+// The unit's counts are the caller's to update.
+template <int D, int KB, int VB>
+__device__ __forceinline__ void warp_demote_unit(const LayerArgs& a, int unit, int n_mid, int cur,
+                                                 int head) {
+  const size_t rrow = ((size_t)unit * a.W + head) * D;
+  const size_t mrow = (size_t)unit * a.C + n_mid;
+  warp_quantize_row<D, KB>(a.rec_k + rrow, (cur ? a.mk[1] : a.mk[0]) + mrow * (D * KB / 8),
+                           (cur ? a.mks[1] : a.mks[0]) + mrow * (D / kGroup));
+  if (a.pq)
+    warp_pq_encode_row<D>(a.rec_v + rrow, a.pq_cb, (cur ? a.mv[1] : a.mv[0]) + mrow * (D / 4),
+                          (cur ? a.mvs[1] : a.mvs[0]) + mrow * (D / kGroup));
+  else
+    warp_quantize_row<D, VB>(a.rec_v + rrow, (cur ? a.mv[1] : a.mv[0]) + mrow * (D * VB / 8),
+                             (cur ? a.mvs[1] : a.mvs[0]) + mrow * (D / kGroup));
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0)
+    (cur ? a.mid_sc[1] : a.mid_sc[0])[mrow] = a.rec_sc[(size_t)unit * a.W + head];
+}
+
 // One warp per unit: if the ring is full, quantise its oldest token into middle slot N_MID.
 template <int D, int KB, int VB>
 __global__ void __launch_bounds__(32) demote_kernel(LayerArgs a) {
@@ -359,19 +380,9 @@ __global__ void __launch_bounds__(32) demote_kernel(LayerArgs a) {
     if (threadIdx.x == 0) record_status(a.status, kCheckDemoteSlot);
     return;
   }
-  const size_t rrow = ((size_t)unit * a.W + head) * D;
-  const size_t mrow = (size_t)unit * a.C + n_mid;
-  warp_quantize_row<D, KB>(a.rec_k + rrow, (cur ? a.mk[1] : a.mk[0]) + mrow * (D * KB / 8),
-                           (cur ? a.mks[1] : a.mks[0]) + mrow * (D / kGroup));
-  if (a.pq)
-    warp_pq_encode_row<D>(a.rec_v + rrow, a.pq_cb, (cur ? a.mv[1] : a.mv[0]) + mrow * (D / 4),
-                          (cur ? a.mvs[1] : a.mvs[0]) + mrow * (D / kGroup));
-  else
-    warp_quantize_row<D, VB>(a.rec_v + rrow, (cur ? a.mv[1] : a.mv[0]) + mrow * (D * VB / 8),
-                             (cur ? a.mvs[1] : a.mvs[0]) + mrow * (D / kGroup));
+  warp_demote_unit<D, KB, VB>(a, unit, n_mid, cur, head);
   __syncwarp();
   if (threadIdx.x == 0) {
-    (cur ? a.mid_sc[1] : a.mid_sc[0])[mrow] = a.rec_sc[(size_t)unit * a.W + head];
     m[FADE_META_N_MID] = n_mid + 1;
     m[FADE_META_N_RECENT] = n_rec - 1;
     m[FADE_META_HEAD] = (head + 1) % a.W;
@@ -426,8 +437,13 @@ __global__ void __launch_bounds__(32) append_kernel(LayerArgs a, const uint16_t*
 // cos and sin, the remaining slots copy their two pass-through channels; no table: a copy),
 // the queries into q_rot and the key straight into the slot append_kernel gives it (a sink
 // while fewer than n_sink are held, else the newest ring entry), with its value and score 0.
-template <int D>
-__global__ void __launch_bounds__(128)
+// DEMOTE: first, if the ring is full, warp 0 demotes its oldest token exactly as demote_kernel
+// does (while the other warps rotate queries); the new token then takes the freed slot.
+#ifndef FADE_ROPE_APPEND_THREADS
+#define FADE_ROPE_APPEND_THREADS 256
+#endif
+template <int D, int KB, int VB, bool DEMOTE>
+__global__ void __launch_bounds__(FADE_ROPE_APPEND_THREADS)
     rope_append_kernel(LayerArgs a, const float* __restrict__ table, int max_pos, int rh,
                        const uint16_t* __restrict__ q_raw, const uint16_t* __restrict__ k_raw,
                        const uint16_t* __restrict__ v, const int32_t* __restrict__ pos,
@@ -436,6 +452,21 @@ __global__ void __launch_bounds__(128)
   const int h = blockIdx.x, b = blockIdx.y, unit = b * a.H + h;
   const int G = Hq / a.H;
   const int p = table ? min(max(pos[b], 0), max_pos - 1) : 0;
+  int32_t* m = a.meta + unit * kF;
+  const int n_sink = m[FADE_META_N_SINK], n_rec0 = m[FADE_META_N_RECENT];
+  const int head0 = m[FADE_META_HEAD];
+  int n_rec = n_rec0, head = head0;
+  const bool demote = DEMOTE && n_rec0 == a.W;  // uniform per CTA
+  if (demote) {
+    const int n_mid = m[FADE_META_N_MID], cur = m[FADE_META_CUR];
+    if (n_mid >= a.C || head0 < 0 || head0 >= a.W) {  // the host checks capacity
+      if (threadIdx.x == 0) record_status(a.status, kCheckDemoteSlot);
+      return;
+    }
+    if (threadIdx.x < 32) warp_demote_unit<D, KB, VB>(a, unit, n_mid, cur, head0);
+    n_rec = n_rec0 - 1;
+    head = (head0 + 1) % a.W;
+  }
   // one slot of vector x (D channels) into y
   auto rot = [&](const uint16_t* x, uint16_t* y, int k) {
     if (!table) {
@@ -457,8 +488,7 @@ __global__ void __launch_bounds__(128)
     const size_t base = ((size_t)b * Hq + (size_t)h * G + i / half) * D;
     rot(q_raw + base, q_rot + base, i % half);
   }
-  int32_t* m = a.meta + unit * kF;
-  const int n_sink = m[FADE_META_N_SINK], n_rec = m[FADE_META_N_RECENT];
+  if (demote) __syncthreads();  // the demoted slot is read before the new token overwrites it
   const bool to_sink = n_sink < a.S;
   if (!to_sink && n_rec >= a.W) {  // the host checks capacity; never overwrite the ring
     if (threadIdx.x == 0) record_status(a.status, kCheckAppendSlot);
@@ -473,7 +503,7 @@ __global__ void __launch_bounds__(128)
     dv = a.sink_v + row * D;
     dsc = a.sink_sc + row;
   } else {
-    row = (size_t)unit * a.W + (m[FADE_META_HEAD] + n_rec) % a.W;
+    row = (size_t)unit * a.W + (head + n_rec) % a.W;
     dk = a.rec_k + row * D;
     dv = a.rec_v + row * D;
     dsc = a.rec_sc + row;
@@ -483,6 +513,10 @@ __global__ void __launch_bounds__(128)
   __syncthreads();  // every thread has read the counts
   if (threadIdx.x == 0) {
     *dsc = 0.f;
+    if (demote) {
+      m[FADE_META_N_MID] += 1;
+      m[FADE_META_HEAD] = head;
+    }
     if (to_sink)
       m[FADE_META_N_SINK] = n_sink + 1;
     else
@@ -1692,11 +1726,27 @@ extern "C" fade_status_t fade_cache_append(const fade_config_t* c, fade_layer_t*
   return FADE_OK;
 }
 
+template <int D, int KB, int VB>
+struct RopeAppendLaunch {
+  static fade_status_t run(const LayerArgs& a, bool demote, const float* t, int max_pos, int rh,
+                           const uint16_t* q_raw, const uint16_t* k_raw, const uint16_t* v,
+                           const int32_t* pos, uint16_t* q_rot, int Hq, int B, cudaStream_t s) {
+    const dim3 grid(a.H, B);
+    if (demote)
+      rope_append_kernel<D, KB, VB, true><<<grid, FADE_ROPE_APPEND_THREADS, 0, s>>>(
+          a, t, max_pos, rh, q_raw, k_raw, v, pos, q_rot, Hq);
+    else
+      rope_append_kernel<D, 4, 2, false><<<grid, FADE_ROPE_APPEND_THREADS, 0, s>>>(
+          a, t, max_pos, rh, q_raw, k_raw, v, pos, q_rot, Hq);
+    return launch_status("fade_rope_append");
+  }
+};
+
 extern "C" fade_status_t fade_rope_append(const fade_config_t* c, fade_layer_t* L,
                                           const float* table, int32_t max_pos,
                                           const uint16_t* q_raw, const uint16_t* k_raw,
                                           const uint16_t* v, const int32_t* pos,
-                                          uint16_t* q_rot, void* stream) {
+                                          uint16_t* q_rot, int32_t demote, void* stream) {
   clear_error();
   FADE_RANGE("fade_rope_append");
   fade_status_t st = validate_config(c);
@@ -1707,22 +1757,24 @@ extern "C" fade_status_t fade_rope_append(const fade_config_t* c, fade_layer_t* 
   const bool rope = c->rope.kind != FADE_ROPE_NONE;
   if (rope && (!table || max_pos < 1))
     return set_error(FADE_ERR_INVALID_ARGUMENT, "NULL RoPE table");
-  for (int b = 0; b < c->batch; ++b)
-    if (L->h_n_sink[b] >= c->n_sink && L->h_n_recent[b] >= c->recent_window)
-      return set_error(FADE_ERR_CAPACITY, "row %d: recent window full (demote first)", b);
-  const LayerArgs a = make_args(c, L, nullptr);
-  const dim3 grid(c->num_kv_heads, c->batch);
-  const float* t = rope ? table : nullptr;
-  const int rh = rotary_width(c) / 2;
-  cudaStream_t s = as_stream(stream);
-  if (c->head_dim == 64)
-    rope_append_kernel<64><<<grid, 128, 0, s>>>(a, t, max_pos, rh, q_raw, k_raw, v, pos, q_rot,
-                                                c->num_q_heads);
-  else
-    rope_append_kernel<128><<<grid, 128, 0, s>>>(a, t, max_pos, rh, q_raw, k_raw, v, pos, q_rot,
-                                                 c->num_q_heads);
-  if ((st = launch_status("fade_rope_append"))) return st;
   for (int b = 0; b < c->batch; ++b) {
+    const bool full = L->h_n_recent[b] == c->recent_window;
+    if (demote && full && L->h_n_mid[b] + 1 > c->mid_capacity)
+      return set_error(FADE_ERR_CAPACITY, "row %d: middle tier full (%d slots)", b,
+                       c->mid_capacity);
+    if (!demote && L->h_n_sink[b] >= c->n_sink && full)
+      return set_error(FADE_ERR_CAPACITY, "row %d: recent window full (demote first)", b);
+  }
+  const LayerArgs a = make_args(c, L, nullptr);
+  if ((st = dispatch_dkv<RopeAppendLaunch>(c, a, demote != 0, rope ? table : nullptr, max_pos,
+                                           rotary_width(c) / 2, q_raw, k_raw, v, pos, q_rot,
+                                           c->num_q_heads, c->batch, as_stream(stream))))
+    return st;
+  for (int b = 0; b < c->batch; ++b) {
+    if (demote && L->h_n_recent[b] == c->recent_window) {
+      L->h_n_mid[b] += 1;
+      L->h_n_recent[b] -= 1;
+    }
     if (L->h_n_sink[b] < c->n_sink)
       L->h_n_sink[b] += 1;
     else

@@ -110,7 +110,7 @@ def lib():
             "fade_evict_rerope": (c_i32, [S(ConfigT), S(LayerT), c_vp, c_i32, c_vp]),
             "fade_cache_append": (c_i32, [S(ConfigT), S(LayerT), c_vp, c_vp, c_vp]),
             "fade_rope_append": (c_i32, [S(ConfigT), S(LayerT), c_vp, c_i32, c_vp, c_vp, c_vp,
-                                         c_vp, c_vp, c_vp]),
+                                         c_vp, c_vp, c_i32, c_vp]),
             "fade_decode_attention": (c_i32, [S(ConfigT), S(LayerT), c_vp, c_vp, c_vp, c_vp,
                                               c_vp, c_sz, c_vp]),
             "fade_h2o_accumulate": (c_i32, [S(ConfigT), S(LayerT), c_vp, c_vp, c_vp]),
@@ -401,13 +401,13 @@ def fade_cache_append(layer: TieredLayer, k_rot, v, stream=None):
 
 
 def fade_rope_append(layer: TieredLayer, table, max_pos, q_raw, k_raw, v, pos, q_rot,
-                     stream=None):
+                     demote=False, stream=None):
     """RoPE of q_raw into q_rot and of k_raw at pos[b] (device i32 [B]), and the append of the
     rotated key and v, in one launch (the same bits as fade_rope_apply twice and
-    fade_cache_append)."""
+    fade_cache_append); demote: fade_cache_demote first, in the same launch."""
     _check(lib().fade_rope_append(ctypes.byref(layer.cfg.c()), ctypes.byref(layer.c),
                                   _ptr(table), max_pos, _ptr(q_raw), _ptr(k_raw), _ptr(v),
-                                  _ptr(pos), _ptr(q_rot), _stream(stream)))
+                                  _ptr(pos), _ptr(q_rot), int(bool(demote)), _stream(stream)))
 
 
 def fade_decode_attention(layer: TieredLayer, q_rot, out, logits_ws, ml_ws, ws, stream=None):

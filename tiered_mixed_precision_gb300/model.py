@@ -57,10 +57,16 @@ class FadeCache:
         self._pos_host = torch.zeros(cfg.batch, dtype=torch.int32).pin_memory() \
             if self.device.type == "cuda" else torch.zeros(cfg.batch, dtype=torch.int32)
         self.needs_logits = cfg.policy in ("h2o", "ema")
-        # rotated copy of the step's q (the caller's raw inputs stay intact; the rotated key
-        # goes straight into its cache slot)
+        # rotated copies of the step's q and k (the caller's raw inputs stay intact)
         self.q_rot = torch.empty((cfg.batch, cfg.num_q_heads, cfg.head_dim), dtype=torch.float16,
                                  device=self.device)
+        self.k_rot = torch.empty((cfg.batch, cfg.num_kv_heads, cfg.head_dim),
+                                 dtype=torch.float16, device=self.device)
+        # RoPE and the append (and, without eviction, the demotion) in one launch for layers of
+        # at most FUSED_PROLOGUE_UNITS units, where launch latency dominates (measured faster at
+        # 2, 32 and 64 units); larger layers keep the separate launches (faster at 512 units,
+        # where they spread the same work over more threads)
+        self.fused_prologue = cfg.batch * cfg.num_kv_heads <= self.FUSED_PROLOGUE_UNITS
         self.timers = None      # optional {"attention": [...], "evict": [...]} of event pairs
         self._graph_events = []  # timing events referenced by captured graphs
         self.launches = 0       # kernels enqueued by step_layer calls
@@ -71,6 +77,8 @@ class FadeCache:
     # ------------------------------------------------------------------ session persistence
     # Page "FADE：面向LLM推理的注意力感知分层KV缓存压缩技术", §会话持久化: the compressed cache is
     # saved and restored (cache_state_dict / load_cache_state_dict, then torch.save / torch.load).
+    FUSED_PROLOGUE_UNITS = 128
+
     _STATE_BUFFERS = ("sink_k", "sink_v", "recent_k", "recent_v", "mid_k_codes", "mid_k_scales",
                       "mid_v_codes", "mid_v_scales", "sink_scores", "mid_scores", "recent_scores",
                       "meta")
@@ -195,14 +203,27 @@ class FadeCache:
         self.launches += n
 
     def attend_layer(self, layer: int, q_raw: torch.Tensor, k_raw: torch.Tensor,
-                     v: torch.Tensor, out: torch.Tensor):
-        """The rest of a layer's decode step: RoPE of the new q (into a work buffer) and k at
-        the positions last set by ``set_positions`` and the append of the new token, in one
-        launch (``fade_rope_append``); attention; H2O / EMA accumulation."""
+                     v: torch.Tensor, out: torch.Tensor, demote: bool = False):
+        """The rest of a layer's decode step: RoPE of the new q and k (into work buffers) at the
+        positions last set by ``set_positions`` and the append of the new token (with
+        ``demote`` the demotion first), in one launch (``fade_rope_append``) when the layer is
+        small (``fused_prologue``), else as separate launches; attention; H2O / EMA
+        accumulation."""
         c = self.cfg
         L = self.layers[layer]
-        F.fade_rope_append(L, self.table, self.max_pos, q_raw, k_raw, v, self.pos, self.q_rot)
-        n = 1
+        if self.fused_prologue:
+            F.fade_rope_append(L, self.table, self.max_pos, q_raw, k_raw, v, self.pos,
+                               self.q_rot, demote=demote)
+            n = 1
+        else:
+            if demote:
+                F.fade_cache_demote(L)
+            F.fade_rope_apply(c, self.table, self.max_pos, q_raw, self.q_rot, c.batch,
+                              c.num_q_heads, self.pos, 0)
+            F.fade_rope_apply(c, self.table, self.max_pos, k_raw, self.k_rot, c.batch,
+                              c.num_kv_heads, self.pos, 0)
+            F.fade_cache_append(L, self.k_rot, v)
+            n = (1 if demote else 0) + (3 if c.rope_kind != "none" else 1)
         t = self._tick("attention")
         F.fade_decode_attention(L, self.q_rot, out, self.logits if self.needs_logits else None,
                                 self.ml, self.ws)
@@ -219,7 +240,11 @@ class FadeCache:
                    out: torch.Tensor):
         """One decode step of one layer in the method's order: demote, evict + re-position,
         append, attention, accumulation. q_raw [B][Hq][d], k_raw/v [B][Hkv][d] fp16, pre-RoPE;
-        out [B][Hq][d] fp16."""
+        out [B][Hq][d] fp16. A cache that never evicts has nothing between its demotion and
+        its append, so both go into the RoPE + append launch."""
+        if not self.cfg.evicts:
+            self.attend_layer(layer, q_raw, k_raw, v, out, demote=True)
+            return
         self.maintain_layer(layer)
         self.attend_layer(layer, q_raw, k_raw, v, out)
 
