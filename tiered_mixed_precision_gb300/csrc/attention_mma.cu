@@ -39,9 +39,10 @@ constexpr int kF = FADE_META_FIELDS;
 constexpr int kTileTok = FADE_ATTN_TILE_TOKENS;  // tokens per TMA tile
 // Warp layout per (head_dim, query heads per KV head): consumer warps per CTA, each taking an
 // equal share of a tile (32 or 64 tokens), one producer warp, and the resident-CTA hint given to
-// the register allocator. Eight consumers (two CTAs per SM) when the accumulators are small
-// (G <= 4); four (one CTA) for G = 8, whose accumulators would not fit the smaller budget.
-// FADE_MMA_WIDE=0 forces four consumers everywhere; FADE_MMA_STAGES_128 sets the pipeline
+// the register allocator. Eight consumers: two CTAs per SM when the accumulators are small
+// (G <= 4), one CTA for G = 8 (whose accumulators need the larger register budget); PQ-coded V
+// at G = 8 keeps four (its codebook and V tiles fill the shared memory). FADE_MMA_WIDE=0 forces
+// four consumers everywhere; FADE_MMA_STAGES_128 sets the pipeline
 // depth for head_dim 128.
 #ifndef FADE_MMA_WIDE
 #define FADE_MMA_WIDE 1
@@ -72,12 +73,12 @@ constexpr bool kF16Mma = FADE_F16_MMA != 0;
 #endif
 template <int D, int G, bool PQ = false>
 struct MmaShape {
-  static constexpr int CONS = (FADE_MMA_WIDE && G <= 4) ? 8 : 4;
+  static constexpr int CONS = (FADE_MMA_WIDE && (G <= 4 || !PQ)) ? 8 : 4;
   static constexpr int THREADS = 32 * (CONS + 1);
   static constexpr int WARP_TOK = kTileTok / CONS;  // tokens per consumer warp per tile
   static constexpr int MT = WARP_TOK / 16;          // 16-token M-tiles per consumer warp
   // PQ-coded V keeps the codebook and per-warp V tiles in shared memory: one CTA per SM
-  static constexpr int MINB = PQ ? 1 : (CONS == 8 ? FADE_MMA_CTAS_PER_SM : 1);
+  static constexpr int MINB = PQ ? 1 : ((CONS == 8 && G <= 4) ? FADE_MMA_CTAS_PER_SM : 1);
 };
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -102,8 +103,8 @@ struct MmaArgs {
 };
 
 // Stage layout of the ring for V codes of VB bits (2, or 4: the safe preset) and NST stages (0:
-// the default for the head dimension).
-template <int D, int VB = 2, int NST = 0>
+// the default for the head dimension); MROWS (consumer warps x query heads) rows of the merge.
+template <int D, int VB = 2, int NST = 0, int MROWS = 32>
 struct MmaCfg {
   static constexpr int KROW = D / 2;        // INT4 codes per token (bytes)
   static constexpr int VROW = D * VB / 8;   // INT2 / INT4 V codes per token (bytes)
@@ -120,7 +121,7 @@ struct MmaCfg {
   static constexpr int MERGE_OFF = NSTAGE * STAGE;
   // (acc rows padded by one float: the fragment-layout writes then hit 16 banks, not 4)
   static constexpr int WO_ROW = D + 1;
-  static constexpr int MERGE_BYTES = (64 + 64 + 32 * WO_ROW + 64) * 4;
+  static constexpr int MERGE_BYTES = (64 + 64 + MROWS * WO_ROW + 64) * 4;
   static constexpr int INFO_OFF = MERGE_OFF + MERGE_BYTES;  // per stage: kInfo ints
   static constexpr int BAR_OFF = INFO_OFF + NSTAGE * 8 * 4;
   static constexpr int SMEM = BAR_OFF + 2 * NSTAGE * 8 + 1024;  // + alignment slack
@@ -134,7 +135,7 @@ __host__ __device__ constexpr int mma_stages() {
   return (VB == 4 && D == 128) ? (MmaShape<D, G, PQ>::MINB > 1 ? 2 : 4) : 0;
 }
 template <int D, int G, bool PQ, int VB>
-using MmaCfgOf = MmaCfg<D, VB, mma_stages<D, G, PQ, VB>()>;
+using MmaCfgOf = MmaCfg<D, VB, mma_stages<D, G, PQ, VB>(), MmaShape<D, G, PQ>::CONS * G>;
 
 // Shared memory added for PQ-coded V, after the layout above: the layer's codebook stored
 // centroid-major ([256][D/4] entries of 4 fp16 channels, so that the 32 lanes of a warp, one
@@ -441,9 +442,9 @@ __device__ __forceinline__ void consume_tile(
   constexpr int NT = (2 * G + 7) / 8;
   constexpr int NHALF = D / 64;
   const int g = lane >> 2, t = lane & 3;
-  float sc[MmaShape<D, G>::MT][NT][2];  // logits (exp2 domain) of tokens g, g+8 of each M-tile
+  float sc[MmaShape<D, G, PQ>::MT][NT][2];  // logits (exp2 domain) of tokens g, g+8 of each M-tile
 #pragma unroll
-  for (int mt = 0; mt < MmaShape<D, G>::MT; ++mt) {
+  for (int mt = 0; mt < MmaShape<D, G, PQ>::MT; ++mt) {
     const int r0 = wr0 + mt * 16;
     uint32_t kw_lo[NHALF], kw_hi[NHALF];
     scale_words<D>(stage + lo_.ks + mt * 16 * Cfg::SROW * 2, kw_lo);
@@ -503,7 +504,7 @@ __device__ __forceinline__ void consume_tile(
   for (int j = 0; j < NT; ++j) {
     float mx = sc[0][j][0];
 #pragma unroll
-    for (int mt = 0; mt < MmaShape<D, G>::MT; ++mt) mx = fmaxf(mx, fmaxf(sc[mt][j][0], sc[mt][j][1]));
+    for (int mt = 0; mt < MmaShape<D, G, PQ>::MT; ++mt) mx = fmaxf(mx, fmaxf(sc[mt][j][0], sc[mt][j][1]));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -513,7 +514,7 @@ __device__ __forceinline__ void consume_tile(
     m2[j] = mn;
     float ps = 0.f;
 #pragma unroll
-    for (int mt = 0; mt < MmaShape<D, G>::MT; ++mt)
+    for (int mt = 0; mt < MmaShape<D, G, PQ>::MT; ++mt)
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const float pr = ex2(sc[mt][j][r] - mn);
@@ -544,7 +545,7 @@ __device__ __forceinline__ void consume_tile(
     constexpr int SUBS = PC::SUBS;
     const uint32_t vt_ld = vt + ((lane & 7) + 8 * (lane >> 4)) * PC::VT_ROW + ((lane >> 3) & 1) * 16;
 #pragma unroll
-    for (int mt = 0; mt < MmaShape<D, G>::MT; ++mt) {
+    for (int mt = 0; mt < MmaShape<D, G, PQ>::MT; ++mt) {
       const int r0 = wr0 + mt * 16;
 #pragma unroll kPqDecodeUnroll
       for (int i = lane; i < 16 * SUBS; i += 32) {
@@ -580,7 +581,7 @@ __device__ __forceinline__ void consume_tile(
   // PV over the warp's M-tiles (16 tokens each = one MMA k-step). B operand: the probability
   // (fp16) times the V scale of the column's group (fp16 multiply), transposed into place.
 #pragma unroll
-  for (int mt = 0; mt < MmaShape<D, G>::MT; ++mt) {
+  for (int mt = 0; mt < MmaShape<D, G, PQ>::MT; ++mt) {
     const int r0 = wr0 + mt * 16;
     uint32_t vw_lo[NHALF], vw_hi[NHALF];
     scale_words<D>(stage + lo_.vs + mt * 16 * Cfg::SROW * 2, vw_lo);
@@ -721,7 +722,7 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
                     const __grid_constant__ CUtensorMap trk, const __grid_constant__ CUtensorMap trv,
                     MmaArgs a, const __grid_constant__ StreamK sk) {
   using Cfg = MmaCfgOf<D, G, PQ, VB>;
-  constexpr int kConsumers = MmaShape<D, G>::CONS;
+  constexpr int kConsumers = MmaShape<D, G, PQ>::CONS;
   constexpr int NT = (2 * G + 7) / 8;    // 8-column n-tiles of (head, group parity)
   constexpr int NHALF = D / 64;          // 64-channel halves (accumulator sets)
   constexpr int NSTAGE = Cfg::NSTAGE;
@@ -737,6 +738,7 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
   float* wl = wm + 64;                                          // [kConsumers][8]
   float* wf = wl + 64;                                          // [G][kConsumers]
   float* wo = wf + 64;                                  // [kConsumers][G][WO_ROW]
+  static_assert(kConsumers * G <= 64, "warp-merge arrays of 64 (warp, head) entries");
   constexpr int WR = Cfg::WO_ROW;
   __shared__ int s_abort;
 
@@ -877,7 +879,7 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
 
   // ------------------------------------------------------------ consumers
   const float c2 = a.inv_sqrt_d * kLog2e;
-  const int wr0 = warp * MmaShape<D, G>::WARP_TOK;
+  const int wr0 = warp * MmaShape<D, G, PQ>::WARP_TOK;
   const LaneOffsets<D, VB> lo_ = lane_offsets<D, VB>(wr0, lane);
   const bool want_logits = a.logits != nullptr;
   // PQ-coded V: this warp's decoded V tile and the codebook (unused otherwise)
@@ -1260,23 +1262,28 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
     consumer_bar<kConsumers>();
     const size_t pbase = ((size_t)(b * a.Hq + hq0)) * a.nsplit + split;
     if (warp == 0) {
-      // lane (h, w) = (lane / kConsumers, lane % kConsumers): head h's max over the warps, the
-      // weight 2^(m_w - M) of warp w, and the weighted mass, reduced across the w lanes
-      static_assert(G * kConsumers <= 32, "one lane per (head, warp)");
-      const int h = lane / kConsumers, w = lane % kConsumers;
-      const bool act = lane < G * kConsumers;
-      const float mw = act ? wm[w * 8 + h] : -INFINITY;
-      float M = mw;
+      // entry e = base + lane is (head h, warp w) = (e / kConsumers, e % kConsumers): head h's
+      // max over the warps, the weight 2^(m_w - M) of warp w, and the weighted mass, reduced
+      // across the w lanes (whole heads per pass of 32 entries: kConsumers divides 32)
 #pragma unroll
-      for (int o = kConsumers / 2; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-      float L = act ? wl[w * 8 + h] * f : 0.f;
+      for (int base = 0; base < G * kConsumers; base += 32) {
+        const int e = base + lane;
+        const int h = e / kConsumers, w = e % kConsumers;
+        const bool act = e < G * kConsumers;
+        const float mw = act ? wm[w * 8 + h] : -INFINITY;
+        float M = mw;
 #pragma unroll
-      for (int o = kConsumers / 2; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-      if (act) wf[h * kConsumers + w] = f;
-      if (act && w == 0 && write_ok) {
-        a.part_ml[(pbase + (size_t)h * a.nsplit) * 2] = M * kLn2;  // natural-log units
-        a.part_ml[(pbase + (size_t)h * a.nsplit) * 2 + 1] = L;
+        for (int o = kConsumers / 2; o; o >>= 1)
+          M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+        float L = act ? wl[w * 8 + h] * f : 0.f;
+#pragma unroll
+        for (int o = kConsumers / 2; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        if (act) wf[h * kConsumers + w] = f;
+        if (act && w == 0 && write_ok) {
+          a.part_ml[(pbase + (size_t)h * a.nsplit) * 2] = M * kLn2;  // natural-log units
+          a.part_ml[(pbase + (size_t)h * a.nsplit) * 2 + 1] = L;
+        }
       }
     }
     consumer_bar<kConsumers>();
