@@ -239,3 +239,51 @@ def test_attention_tiled_query_rejects_invalid_config(T):
 def test_tile_constant_matches_the_header(T):
     m = re.search(r"#define\s+FADE_ATTN_TILE_TOKENS\s+(\d+)", open(HEADER).read())
     assert m and int(m.group(1)) == T.fade.ATTN_TILE_TOKENS
+
+
+def test_growing_graph_key_follows_the_tile_counts(T):
+    """The growing-step graph is keyed on every layer's and row's count of middle tiles at the
+    coming attention call (one more middle token than the mirror holds) when attention runs on
+    the tensor-core kernel, and on nothing for the CUDA-core kernel."""
+    from types import SimpleNamespace
+
+    from tiered_mixed_precision_gb300.model import FadeCache
+
+    t = T.fade.ATTN_TILE_TOKENS
+
+    def key(cfg, mids):
+        layers = [SimpleNamespace(h_n_mid=np.array(m, np.int32)) for m in mids]
+        return FadeCache.growing_graph_key(SimpleNamespace(cfg=cfg, layers=layers))
+
+    tiled = _cfg(T, middle_v_bits=4, batch=2)
+    assert key(tiled, [[t - 2, 0], [3 * t - 1, 5]]) == ((1, 1), (3, 1))
+    assert key(tiled, [[t - 1, 0], [3 * t, 5]]) == ((1, 1), (4, 1))   # the second layer crosses
+    assert key(tiled, [[t - 1, 0]]) != key(tiled, [[t, 0]])          # 256 -> 257 at the call
+    split = _cfg(T, middle_k_bits=2, middle_v_bits=2, batch=2)
+    assert key(split, [[10, 20]]) == ()
+
+
+def test_rope_append_validates_before_any_launch(T):
+    """fade_rope_append rejects NULL inputs and both capacity overflows (the recent window full
+    without demotion; the middle tier full with it) on the host, leaving the mirror as it was."""
+    import torch
+
+    cfg = _cfg(T, batch=2)   # mid_capacity 401
+    layer = T.TieredLayer(cfg, 16, device="cpu")
+    x = torch.zeros(4, dtype=torch.float16)
+    layer.h_n_sink[:] = 4
+    layer.h_n_recent[:] = [64, 10]
+    layer.h_n_mid[:] = [401, 3]
+
+    class S:  # a stream object whose handle is never used
+        cuda_stream = 0
+    with pytest.raises(T.FadeError) as e:
+        T.fade.fade_rope_append(layer, None, 10, None, x, x, x, x, stream=S())
+    assert e.value.status == 1
+    with pytest.raises(T.FadeError) as e:   # row 0's ring is full and nothing demotes
+        T.fade.fade_rope_append(layer, x, 10, x, x, x, x, x, demote=False, stream=S())
+    assert e.value.status == 3
+    with pytest.raises(T.FadeError) as e:   # row 0 would demote into a full middle tier
+        T.fade.fade_rope_append(layer, x, 10, x, x, x, x, x, demote=True, stream=S())
+    assert e.value.status == 3
+    assert layer.h_n_recent.tolist() == [64, 10] and layer.h_n_mid.tolist() == [401, 3]
