@@ -28,7 +28,9 @@
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
+#include <unordered_map>
 
 #include "fade_internal.cuh"
 
@@ -394,9 +396,9 @@ struct LaneOffsets {
 
 // INT4 V rows have the K rows' width and swizzle, so they are addressed like the K rows (the
 // 16-byte chunks 2s and 2s + 1, i.e. the quantisation groups of half s, of tokens 0-15).
-template <int D, int VB>
+template <int D, int G, bool PQ, int VB>
 __device__ __forceinline__ LaneOffsets<D, VB> lane_offsets(int wr0, int lane) {
-  using Cfg = MmaCfg<D, VB>;
+  using Cfg = MmaCfgOf<D, G, PQ, VB>;
   LaneOffsets<D, VB> o;
   const int lr = (lane & 7) + ((lane >> 3) & 1) * 8, hi = lane >> 4, g = lane >> 2;
   if constexpr (D == 128) {
@@ -438,7 +440,7 @@ __device__ __forceinline__ void consume_tile(
     const uint32_t (&qb)[D / 64][4][(2 * G + 7) / 8][2], float (&m2)[(2 * G + 7) / 8],
     float (&lsum)[(2 * G + 7) / 8], float (&o)[D / 64][4][(2 * G + 7) / 8][4], float c2,
     float* logit_row, uint32_t vt, uint32_t cbs) {
-  using Cfg = MmaCfg<D, VB>;
+  using Cfg = MmaCfgOf<D, G, PQ, VB>;
   constexpr int NT = (2 * G + 7) / 8;
   constexpr int NHALF = D / 64;
   const int g = lane >> 2, t = lane & 3;
@@ -576,8 +578,7 @@ __device__ __forceinline__ void consume_tile(
         }
       __syncwarp();  // the tile is read before the next M-tile overwrites it
     }
-    return;
-  }
+  } else {
   // PV over the warp's M-tiles (16 tokens each = one MMA k-step). B operand: the probability
   // (fp16) times the V scale of the column's group (fp16 multiply), transposed into place.
 #pragma unroll
@@ -648,6 +649,7 @@ __device__ __forceinline__ void consume_tile(
 #undef FADE_PV
       }
     }
+  }
   }
 }
 
@@ -880,7 +882,7 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
   // ------------------------------------------------------------ consumers
   const float c2 = a.inv_sqrt_d * kLog2e;
   const int wr0 = warp * MmaShape<D, G, PQ>::WARP_TOK;
-  const LaneOffsets<D, VB> lo_ = lane_offsets<D, VB>(wr0, lane);
+  const LaneOffsets<D, VB> lo_ = lane_offsets<D, G, PQ, VB>(wr0, lane);
   const bool want_logits = a.logits != nullptr;
   // PQ-coded V: this warp's decoded V tile and the codebook (unused otherwise)
   const uint32_t vt = sbase + PqCfg<D>::VT_OFF + warp * 16 * PqCfg<D>::VT_ROW;
@@ -1358,6 +1360,56 @@ fade_status_t encode_f16_rows(CUtensorMap* m, const void* base, unsigned long lo
   return FADE_OK;
 }
 
+// Tensor maps by their full set of inputs: a map holds only the base address, the sizes,
+// strides, box and swizzle, so equal inputs give an equal map, and encoding is host work on
+// every call otherwise. Bounded: cleared when it reaches kMapCacheMax entries.
+struct MapKey {
+  int dev;
+  const void* base;
+  unsigned long long rows;
+  int inner;     // code rows: bytes per row; fp16 rows: channels
+  int box_rows;  // fp16 rows only
+  int kind;      // 0: code rows, 1: fp16 rows
+  bool operator==(const MapKey& o) const {
+    return dev == o.dev && base == o.base && rows == o.rows && inner == o.inner &&
+           box_rows == o.box_rows && kind == o.kind;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    size_t h = std::hash<const void*>()(k.base);
+    for (unsigned long long v : {(unsigned long long)k.dev, k.rows, (unsigned long long)k.inner,
+                                 (unsigned long long)k.box_rows, (unsigned long long)k.kind})
+      h = h * 1000003u ^ std::hash<unsigned long long>()(v);
+    return h;
+  }
+};
+constexpr size_t kMapCacheMax = 8192;
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
+fade_status_t cached_map(CUtensorMap* out, const void* base, unsigned long long rows, int inner,
+                         int box_rows, int kind) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  const MapKey k{dev, base, rows, inner, box_rows, kind};
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    const auto it = g_maps.find(k);
+    if (it != g_maps.end()) {
+      *out = it->second;
+      return FADE_OK;
+    }
+  }
+  const fade_status_t s = kind == 0 ? encode_rows(out, base, rows, inner)
+                                    : encode_f16_rows(out, base, rows, inner, box_rows);
+  if (s) return s;
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  if (g_maps.size() >= kMapCacheMax) g_maps.clear();
+  g_maps.emplace(k, *out);
+  return FADE_OK;
+}
+
 template <int D, int G, bool PQ, int VB>
 fade_status_t launch_mma(const fade_config_t* c, const fade_layer_t* L, MmaArgs a,
                          const StreamK& sk, cudaStream_t st) {
@@ -1373,8 +1425,8 @@ fade_status_t launch_mma(const fade_config_t* c, const fade_layer_t* L, MmaArgs 
   CUtensorMap tk[2], tv[2];
   fade_status_t s;
   for (int i = 0; i < 2; ++i) {
-    if ((s = encode_rows(&tk[i], L->mid_k_codes[i], rows, Cfg::KROW))) return s;
-    if ((s = encode_rows(&tv[i], L->mid_v_codes[i], rows, Cfg::VROW))) return s;
+    if ((s = cached_map(&tk[i], L->mid_k_codes[i], rows, Cfg::KROW, 0, 0))) return s;
+    if ((s = cached_map(&tv[i], L->mid_v_codes[i], rows, Cfg::VROW, 0, 0))) return s;
   }
   // the FP16 tiers of an item go through the ring when their swizzled regions (1024-byte
   // aligned, one per 64-channel half of the sinks and of the ring), plus 16 rows of reads
@@ -1387,11 +1439,11 @@ fade_status_t launch_mma(const fade_config_t* c, const fade_layer_t* L, MmaArgs 
   a.f16_rreg = staged ? rreg : 0;
   CUtensorMap tsk, tsv, trk, trv;
   if (staged) {
-    if ((s = encode_f16_rows(&trk, L->recent_k, units * W, D, W))) return s;
-    if ((s = encode_f16_rows(&trv, L->recent_v, units * W, D, W))) return s;
+    if ((s = cached_map(&trk, L->recent_k, units * W, D, W, 1))) return s;
+    if ((s = cached_map(&trv, L->recent_v, units * W, D, W, 1))) return s;
     if (S > 0) {
-      if ((s = encode_f16_rows(&tsk, L->sink_k, units * S, D, S))) return s;
-      if ((s = encode_f16_rows(&tsv, L->sink_v, units * S, D, S))) return s;
+      if ((s = cached_map(&tsk, L->sink_k, units * S, D, S, 1))) return s;
+      if ((s = cached_map(&tsv, L->sink_v, units * S, D, S, 1))) return s;
     } else {  // no sinks: never read
       tsk = trk;
       tsv = trv;
@@ -1400,9 +1452,16 @@ fade_status_t launch_mma(const fade_config_t* c, const fade_layer_t* L, MmaArgs 
     tsk = tsv = trk = trv = tk[0];
   }
   auto kern = attn_mid_mma_kernel<D, G, PQ, VB>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
-      cudaSuccess)
-    return launch_status("fade_decode_attention (middle tier) shared-memory opt-in");
+  // the shared-memory opt-in, once per device for this instantiation (devices 0..63)
+  static std::atomic<unsigned long long> smem_set{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 64;
+  if (dev >= 64 || !((smem_set.load() >> dev) & 1ull)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+        cudaSuccess)
+      return launch_status("fade_decode_attention (middle tier) shared-memory opt-in");
+    if (dev < 64) smem_set.fetch_or(1ull << dev);
+  }
   // persistent grid: the schedule's CTAs (as many as fit on the device at once)
   kern<<<sk.P, MmaShape<D, G, PQ>::THREADS, kSmem, st>>>(tk[0], tk[1], tv[0], tv[1], tsk, tsv,
                                                          trk, trv, a, sk);
