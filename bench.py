@@ -191,7 +191,8 @@ def evict_bytes(cfg, layer, n_ev=1):
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 CSRC = os.path.join(ROOT, "tiered_mixed_precision_gb300", "csrc")
 TRAFFIC_SOURCES = {
-    "attention": ["attention_mma.cu", "attention.cu", "fade_internal.cuh"],
+    "attention": ["attention_mma.cuh", "attention_mma.cu", "attention_mma_k2.cu", "attention.cu",
+                  "fade_internal.cuh"],
     "evict_rerope": ["cache.cu", "fade_internal.cuh"],
 }
 

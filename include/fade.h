@@ -389,13 +389,12 @@ fade_status_t fade_decode_attention(const fade_config_t* cfg, const fade_layer_t
 /* Tokens per middle tile of the tensor-core attention kernel's schedule. */
 #define FADE_ATTN_TILE_TOKENS 256
 
-/* Host: 1 if fade_decode_attention runs the tensor-core kernel for this configuration (INT4
- * middle K with INT2, INT4 or PQ-coded V), 0 if the CUDA-core split kernel (any other code
- * widths), -1 for an invalid configuration (fade_last_error says why). The tensor-core launch
- * is scheduled (stream-K) from every row's number of FADE_ATTN_TILE_TOKENS-token middle tiles
- * as the host mirror holds them at the call, and reads every other count on the device: a
- * captured call (CUDA graph) stays valid while those tile counts are unchanged. The CUDA-core
- * launch is sized by mid_capacity and stays valid while the cache grows. */
+/* Host: 1 if fade_decode_attention's launch is scheduled by middle tiles (the tensor-core
+ * kernel, which every valid configuration runs: INT4 or INT2 middle K with INT2, INT4 or
+ * PQ-coded V), 0 otherwise, -1 for an invalid configuration (fade_last_error says why). The
+ * launch is scheduled (stream-K) from every row's number of FADE_ATTN_TILE_TOKENS-token middle
+ * tiles as the host mirror holds them at the call, and reads every other count on the device:
+ * a captured call (CUDA graph) stays valid while those tile counts are unchanged. */
 int32_t fade_attention_tiled(const fade_config_t* cfg);
 
 /* Decode attention for callers that cannot allocate device memory. The pages have no

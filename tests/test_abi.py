@@ -222,8 +222,9 @@ def test_debug_build_compiles_and_exports_every_symbol():
     (dict(middle_v_bits=4), True),                           # INT4 V (safe preset)
     (dict(v_codec="pq"), True),                              # PQ-coded V
     (dict(head_dim=64, middle_v_bits=4, num_q_heads=16), True),
-    (dict(middle_k_bits=2, middle_v_bits=2), False),         # INT2 K: CUDA-core kernel
-    (dict(middle_k_bits=2, middle_v_bits=4), False),
+    (dict(middle_k_bits=2, middle_v_bits=2), True),          # INT2 K
+    (dict(middle_k_bits=2, middle_v_bits=4), True),
+    (dict(middle_k_bits=2, middle_v_bits=2, v_codec="pq"), True),
 ])
 def test_attention_tiled_query(T, kw, tiled):
     """fade_attention_tiled names the configurations whose attention runs the tensor-core
@@ -243,8 +244,8 @@ def test_tile_constant_matches_the_header(T):
 
 def test_growing_graph_key_follows_the_tile_counts(T):
     """The growing-step graph is keyed on every layer's and row's count of middle tiles at the
-    coming attention call (one more middle token than the mirror holds) when attention runs on
-    the tensor-core kernel, and on nothing for the CUDA-core kernel."""
+    coming attention call (one more middle token than the mirror holds): the counts the
+    tensor-core kernel's schedule is built from, for INT4 and INT2 K alike."""
     from types import SimpleNamespace
 
     from tiered_mixed_precision_gb300.model import FadeCache
@@ -259,8 +260,8 @@ def test_growing_graph_key_follows_the_tile_counts(T):
     assert key(tiled, [[t - 2, 0], [3 * t - 1, 5]]) == ((1, 1), (3, 1))
     assert key(tiled, [[t - 1, 0], [3 * t, 5]]) == ((1, 1), (4, 1))   # the second layer crosses
     assert key(tiled, [[t - 1, 0]]) != key(tiled, [[t, 0]])          # 256 -> 257 at the call
-    split = _cfg(T, middle_k_bits=2, middle_v_bits=2, batch=2)
-    assert key(split, [[10, 20]]) == ()
+    k2 = _cfg(T, middle_k_bits=2, middle_v_bits=2, batch=2)
+    assert key(k2, [[10, 20]]) == ((1, 1),)
 
 
 def test_rope_append_validates_before_any_launch(T):

@@ -300,6 +300,15 @@ def _small(key):
         return get_workload(3).scaled(layers=1, batch=2, num_q_heads=16, num_kv_heads=2,
                                       middle_v_bits=4, prompt_len=900, int4_budget=500,
                                       steps=6), None
+    # INT2 K on the tensor-core kernel at the query-group sizes the other INT2-K cases miss
+    if key == "k2v2_g8_d128":
+        return get_workload(4).scaled(layers=1, batch=2, num_q_heads=16, num_kv_heads=2,
+                                      middle_k_bits=2, prompt_len=1300, int4_budget=700,
+                                      steps=5), None
+    if key == "k2v4_g1_d64_h2o":
+        return get_workload(3).scaled(layers=1, batch=2, num_q_heads=4, num_kv_heads=4,
+                                      middle_k_bits=2, middle_v_bits=4, prompt_len=900,
+                                      int4_budget=500, steps=6), None
     if key == "v4_g8_d128_grow":  # the safe preset's shape, six tiles per unit, no eviction
         return get_workload(2).scaled(layers=1, batch=2, prompt_len=1400, steps=4), None
     # degenerate cases of the method
@@ -363,7 +372,7 @@ def _small(key):
                                  "d64_g8", "d128_g8", "d64_k2v4_h2o", "d128_k4v4_pos",
                                  "d64_k2v2_ema", "d128_k2v2_pos", "d64_k4v4_pos",
                                  "v4_g1_h2o_d128", "v4_g2_ema_d64", "v4_g8_d64_h2o",
-                                 "v4_g8_d128_grow",
+                                 "v4_g8_d128_grow", "k2v2_g8_d128", "k2v4_g1_d64_h2o",
                                  "deg_nosink", "deg_w1_h2o", "deg_budget0", "deg_short_ragged",
                                  "deg_norope_ema", "rope_linear_pos", "rope_ntk_h2o",
                                  "rope_yarn_ema", "rope_dynamic_pos", "prop_pos_r64",

@@ -76,11 +76,12 @@ def test_pq_train_bit_exact(T, key, n, iters):
 
 
 @pytest.mark.parametrize("key,policy,kbits", [(4, "position", 4), (3, "h2o", 4), (5, "ema", 4),
-                                             (1, "none", 4), (4, "h2o", 2)])
+                                             (1, "none", 4), (4, "h2o", 2), (3, "ema", 2)])
 def test_pq_lockstep(T, key, policy, kbits):
     """The whole step with PQ-coded middle V: prefill tiering, demotion (encode), eviction
-    and compaction (codes move as bytes), CUDA-core attention (centroids from shared memory)
-    and score accumulation, compared with the oracle after every call."""
+    and compaction (codes move as bytes), tensor-core attention (centroids decoded through
+    shared memory; INT4 or INT2 K) and score accumulation, compared with the oracle after
+    every call."""
     over = dict(layers=1, batch=2, ragged=None, prompt_len=600, int4_budget=200, steps=6,
                 policy=policy, middle_k_bits=kbits)
     if key == 5:

@@ -1,5 +1,5 @@
-// Decode attention over the tiered cache (split-KV), the split combine, and H2O / EMA score
-// accumulation.
+// Decode attention over the tiered cache: the entry point (schedule, workspace), the combine of
+// the tensor-core kernel's partials (attention_mma.cu), and H2O / EMA score accumulation.
 // Sources: page "FADE：面向LLM推理的注意力感知分层KV缓存压缩技术" — §项目结构与代码质量 (kernels/:
 // fused INT4 dequant + SDPA), §四种驱逐策略详解 1 (H2O: keep the highest accumulated attention)
 // and 2 (EMA of attention during decode); page "探秘Transformer系列之（25）--- KV Cache优化之处理
@@ -13,352 +13,14 @@ namespace fade {
 namespace {
 
 constexpr int kF = FADE_META_FIELDS;
-constexpr int kThreads = 128;  // one token per thread in the score phase
-constexpr int kTile = 128;     // tokens per shared-memory tile
-constexpr int kPad = 16;       // bytes of padding per staged row (bank spread)
 
+// What the combine reads: the partials of every (row, query head) and each unit's count.
 struct AttnArgs {
-  const uint16_t* q;                    // [B][Hq][D]
-  const uint16_t *sink_k, *sink_v, *rec_k, *rec_v;
-  const uint8_t *mk[2], *mv[2];
-  const uint16_t *mks[2], *mvs[2];
-  const int32_t* meta;
-  float* logits;                        // nullable, [B][Hq][NS]
   float* part_ml;                       // [B][Hq][nsplit][2]
   float* part_acc;                      // [B][Hq][nsplit][D]
-  const int32_t* seg_count;             // [B][H]: partials of each unit (stream-K combine)
-  int Hq, H, S, W, C, NS, chunk, nsplit;
-  float scale;                          // 1/sqrt(D)
-  const uint16_t* pq_cb;                // PQ-coded V: the layer's codebook [D/4][256][4]
+  const int32_t* seg_count;             // [B][H]: partials of each unit
+  int Hq, H, nsplit;
 };
-
-template <int D, int KB, int VB, int G, bool PQ>
-struct Smem {
-  static constexpr int KROW = D * KB / 8, VROW = D * VB / 8, SROW = D / kGroup;
-  static constexpr int KROWP = KROW + kPad, VROWP = VROW + kPad;
-  static constexpr int FROWP = D * 2 + kPad;  // fp16 row, padded
-  static constexpr int MID_BYTES = kTile * (KROWP + VROWP + 2 * SROW * 2);
-  static constexpr int CB_BYTES = PQ ? kPqCentroids * D * 2 : 0;  // PQ codebook (middle splits)
-  static constexpr int F16_BYTES = kTile * 2 * FROWP;
-  static constexpr int MIDCB_BYTES = MID_BYTES + CB_BYTES;
-  static constexpr int TILE_BYTES = MIDCB_BYTES > F16_BYTES ? MIDCB_BYTES : F16_BYTES;
-  static constexpr int NSUB = kThreads / (D / 4);  // token subsets in the value phase
-  static constexpr int Q_OFF = 0;                              // float [D][G]
-  static constexpr int P_OFF = Q_OFF + D * G * 4;               // float [G][kTile]
-  static constexpr int R_OFF = P_OFF + G * kTile * 4;           // float [4][G] + [G]*3
-  static constexpr int T_OFF = R_OFF + (4 * G + 4 * G) * 4;     // tile buffers
-  static constexpr int CB_OFF = T_OFF + MID_BYTES;              // codebook after the mid tile
-  static constexpr int A_OFF = T_OFF;                           // acc reduction (reuses tile)
-  static constexpr int TOTAL = T_OFF + (TILE_BYTES > NSUB * G * D * 4 ? TILE_BYTES : NSUB * G * D * 4);
-};
-
-// Copy `n` rows of `bytes` (a multiple of 16) from global rows given by `src_row(t)` into
-// padded shared rows.
-template <typename RowFn>
-__device__ __forceinline__ void stage_rows(uint8_t* dst, int dst_stride, int bytes, int n,
-                                           RowFn src_row) {
-  const int per = bytes / 16;
-  for (int i = threadIdx.x; i < n * per; i += kThreads) {
-    const int t = i / per, c = i % per;
-    *reinterpret_cast<uint4*>(dst + t * dst_stride + c * 16) =
-        *reinterpret_cast<const uint4*>(src_row(t) + c * 16);
-  }
-}
-
-template <int D, int KB, int VB, int G, bool PQ>
-__global__ void __launch_bounds__(kThreads) attn_split_kernel(AttnArgs a) {
-  using L = Smem<D, KB, VB, G, PQ>;
-  extern __shared__ __align__(16) uint8_t smem[];
-  float* qs = reinterpret_cast<float*>(smem + L::Q_OFF);    // [D][G]
-  float* ps = reinterpret_cast<float*>(smem + L::P_OFF);    // [G][kTile]
-  float* red = reinterpret_cast<float*>(smem + L::R_OFF);   // [4][G] then [4][G]
-  uint8_t* tile = smem + L::T_OFF;
-
-  const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
-  const int unit = b * a.H + hk;
-  const int32_t* m = a.meta + unit * kF;
-  const int n_sink = m[FADE_META_N_SINK], n_mid = m[FADE_META_N_MID];
-  const int n_rec = m[FADE_META_N_RECENT], head = m[FADE_META_HEAD], cur = m[FADE_META_CUR];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int hq0 = hk * G;
-
-  // token range of this split: split 0 = FP16 tiers, split s >= 1 = middle chunk s-1
-  int n_tok;
-  int lo = 0;
-  if (split == 0) {
-    n_tok = n_sink + n_rec;
-  } else {
-    lo = (split - 1) * a.chunk;
-    n_tok = max(0, min(n_mid, lo + a.chunk) - lo);
-  }
-  const size_t pbase = ((size_t)(b * a.Hq + hq0)) * a.nsplit + split;  // (b, hq0, split)
-  if (n_tok == 0) {
-    for (int i = tid; i < G * D; i += kThreads) {
-      const int h = i / D, c = i % D;
-      a.part_acc[(pbase + (size_t)h * a.nsplit) * D + c] = 0.f;
-    }
-    if (tid < G) {
-      a.part_ml[(pbase + (size_t)tid * a.nsplit) * 2 + 0] = -INFINITY;
-      a.part_ml[(pbase + (size_t)tid * a.nsplit) * 2 + 1] = 0.f;
-    }
-    return;
-  }
-
-  for (int i = tid; i < G * D; i += kThreads) {
-    const int h = i / D, c = i % D;
-    qs[c * G + h] = h2f(a.q[((size_t)(b * a.Hq + hq0 + h)) * D + c]);
-  }
-  // PQ-coded V: the codebook sits in shared memory for the whole middle split (it stays
-  // clear of the tile, which the loop below refills)
-  const uint2* cbs = reinterpret_cast<const uint2*>(smem + L::CB_OFF);
-  if constexpr (PQ) {
-    if (split != 0)
-      for (int i = tid; i < L::CB_BYTES / 16; i += kThreads)
-        reinterpret_cast<uint4*>(smem + L::CB_OFF)[i] = reinterpret_cast<const uint4*>(a.pq_cb)[i];
-  }
-
-  constexpr int QUADS = D / 4, NSUB = L::NSUB;
-  const int cq = tid % QUADS, ts = tid / QUADS;
-  float acc[G][4];
-#pragma unroll
-  for (int h = 0; h < G; ++h)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[h][j] = 0.f;
-  float m_run[G], l_run[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    m_run[h] = -INFINITY;
-    l_run[h] = 0.f;
-  }
-
-  const size_t urow_mid = (size_t)unit * a.C;
-  for (int t0 = 0; t0 < n_tok; t0 += kTile) {
-    const int nt = min(kTile, n_tok - t0);
-    __syncthreads();  // previous tile fully consumed
-    uint8_t *kt, *vt;
-    uint16_t *kst = nullptr, *vst = nullptr;
-    if (split == 0) {
-      kt = tile;
-      vt = tile + kTile * L::FROWP;
-      auto krow = [&](int t) {
-        const int u = t0 + t;
-        const size_t r = u < n_sink ? ((size_t)unit * a.S + u) * D
-                                    : ((size_t)unit * a.W + (head + u - n_sink) % a.W) * D;
-        return reinterpret_cast<const uint8_t*>((u < n_sink ? a.sink_k : a.rec_k) + r);
-      };
-      auto vrow = [&](int t) {
-        const int u = t0 + t;
-        const size_t r = u < n_sink ? ((size_t)unit * a.S + u) * D
-                                    : ((size_t)unit * a.W + (head + u - n_sink) % a.W) * D;
-        return reinterpret_cast<const uint8_t*>((u < n_sink ? a.sink_v : a.rec_v) + r);
-      };
-      stage_rows(kt, L::FROWP, D * 2, nt, krow);
-      stage_rows(vt, L::FROWP, D * 2, nt, vrow);
-    } else {
-      kt = tile;
-      vt = tile + kTile * L::KROWP;
-      kst = reinterpret_cast<uint16_t*>(vt + kTile * L::VROWP);
-      vst = kst + kTile * L::SROW;
-      const size_t r0 = urow_mid + lo + t0;
-      const uint8_t* kg = (cur ? a.mk[1] : a.mk[0]) + r0 * L::KROW;
-      const uint8_t* vg = (cur ? a.mv[1] : a.mv[0]) + r0 * L::VROW;
-      stage_rows(kt, L::KROWP, L::KROW, nt, [&](int t) { return kg + (size_t)t * L::KROW; });
-      stage_rows(vt, L::VROWP, L::VROW, nt, [&](int t) { return vg + (size_t)t * L::VROW; });
-      const uint32_t* ksg =
-          reinterpret_cast<const uint32_t*>((cur ? a.mks[1] : a.mks[0]) + r0 * L::SROW);
-      const uint32_t* vsg =
-          reinterpret_cast<const uint32_t*>((cur ? a.mvs[1] : a.mvs[0]) + r0 * L::SROW);
-      const int words = nt * L::SROW / 2;
-      for (int i = tid; i < words; i += kThreads) {
-        reinterpret_cast<uint32_t*>(kst)[i] = ksg[i];
-        if constexpr (!PQ) reinterpret_cast<uint32_t*>(vst)[i] = vsg[i];
-      }
-    }
-    __syncthreads();
-
-    // ---- scores: thread tid owns token tid of the tile
-    float s[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) s[h] = -INFINITY;
-    if (tid < nt) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) s[h] = 0.f;
-      if (split == 0) {
-        const uint16_t* kr = reinterpret_cast<const uint16_t*>(kt + tid * L::FROWP);
-        for (int c = 0; c < D; ++c) {
-          const float kv = h2f(kr[c]);
-#pragma unroll
-          for (int h = 0; h < G; ++h) s[h] = fmaf(qs[c * G + h], kv, s[h]);
-        }
-      } else {
-        const uint8_t* kr = kt + tid * L::KROWP;
-        const uint16_t* sr = kst + tid * L::SROW;
-#pragma unroll 1
-        for (int g = 0; g < D / kGroup; ++g) {
-          float part[G];
-#pragma unroll
-          for (int h = 0; h < G; ++h) part[h] = 0.f;
-          const uint8_t* gr = kr + g * (kGroup * KB / 8);
-#pragma unroll
-          for (int w = 0; w < kGroup * KB / 32; ++w) {
-            const uint32_t word = reinterpret_cast<const uint32_t*>(gr)[w];
-#pragma unroll
-            for (int e = 0; e < 32 / KB; ++e) {
-              const uint32_t u = (word >> (KB * e)) & ((1u << KB) - 1u);
-              const float code = (float)(int(u) - (int(u >> (KB - 1)) << KB));
-              const int c = g * kGroup + w * (32 / KB) + e;
-#pragma unroll
-              for (int h = 0; h < G; ++h) part[h] = fmaf(qs[c * G + h], code, part[h]);
-            }
-          }
-          const float sc = h2f(sr[g]);
-#pragma unroll
-          for (int h = 0; h < G; ++h) s[h] = fmaf(part[h], sc, s[h]);
-        }
-      }
-#pragma unroll
-      for (int h = 0; h < G; ++h) s[h] *= a.scale;
-      if (a.logits) {
-        const int u = t0 + tid;
-        int slot;
-        if (split == 0)
-          slot = u < n_sink ? u : a.S + a.C + (head + u - n_sink) % a.W;
-        else
-          slot = a.S + lo + u;
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-          a.logits[((size_t)(b * a.Hq + hq0 + h)) * a.NS + slot] = s[h];
-      }
-    }
-    // ---- tile max per head
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float v = warp_max(s[h]);
-      if (lane == 0) red[warp * G + h] = v;
-    }
-    __syncthreads();
-    float alpha[G], mnew[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float tm = fmaxf(fmaxf(red[h], red[G + h]), fmaxf(red[2 * G + h], red[3 * G + h]));
-      mnew[h] = fmaxf(m_run[h], tm);
-      alpha[h] = __expf(m_run[h] - mnew[h]);  // m_run = -inf -> 0
-    }
-    float psum[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float p = (tid < nt) ? __expf(s[h] - mnew[h]) : 0.f;
-      ps[h * kTile + tid] = p;
-      psum[h] = warp_sum(p);
-    }
-    if (lane == 0)
-#pragma unroll
-      for (int h = 0; h < G; ++h) red[4 * G + warp * G + h] = psum[h];
-    __syncthreads();
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float ts_ = red[4 * G + h] + red[5 * G + h] + red[6 * G + h] + red[7 * G + h];
-      l_run[h] = l_run[h] * alpha[h] + ts_;
-      m_run[h] = mnew[h];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[h][j] *= alpha[h];
-    }
-
-    // ---- values: thread owns channels 4cq..4cq+3 for tokens ts, ts+NSUB, ...
-    for (int t = ts; t < nt; t += NSUB) {
-      float v4[4];
-      if (split == 0) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(vt + t * L::FROWP + cq * 8);
-        const __half2 h01 = *reinterpret_cast<const __half2*>(&raw.x);
-        const __half2 h23 = *reinterpret_cast<const __half2*>(&raw.y);
-        const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-        v4[0] = f01.x;
-        v4[1] = f01.y;
-        v4[2] = f23.x;
-        v4[3] = f23.y;
-      } else if constexpr (PQ) {
-        // channels 4cq..4cq+3 are sub-space cq: one code byte, one 8-byte centroid
-        const uint32_t code = vt[t * L::VROWP + cq];
-        const uint2 raw = cbs[cq * kPqCentroids + code];
-        const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-        const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-        v4[0] = f01.x;
-        v4[1] = f01.y;
-        v4[2] = f23.x;
-        v4[3] = f23.y;
-      } else {
-        const float sc = h2f(vst[t * L::SROW + (4 * cq) / kGroup]);
-        const uint8_t* vr = vt + t * L::VROWP;
-        uint32_t bits;
-        if (VB == 2)
-          bits = vr[cq];
-        else
-          bits = *reinterpret_cast<const uint16_t*>(vr + 2 * cq);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t u = (bits >> (VB * j)) & ((1u << VB) - 1u);
-          v4[j] = (float)(int(u) - (int(u >> (VB - 1)) << VB)) * sc;
-        }
-      }
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float p = ps[h * kTile + t];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[h][j] = fmaf(p, v4[j], acc[h][j]);
-      }
-    }
-  }
-
-  // ---- reduce value accumulators over token subsets, write the split's partial
-  __syncthreads();
-  float* ar = reinterpret_cast<float*>(smem + L::A_OFF);  // [NSUB][G][D]
-#pragma unroll
-  for (int h = 0; h < G; ++h)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) ar[(ts * G + h) * D + 4 * cq + j] = acc[h][j];
-  __syncthreads();
-  for (int i = tid; i < G * D; i += kThreads) {
-    const int h = i / D, c = i % D;
-    float v = 0.f;
-#pragma unroll
-    for (int k = 0; k < NSUB; ++k) v += ar[(k * G + h) * D + c];
-    a.part_acc[(pbase + (size_t)h * a.nsplit) * D + c] = v;
-  }
-#pragma unroll
-  for (int h = 0; h < G; ++h)
-    if (tid == h) {
-      a.part_ml[(pbase + (size_t)h * a.nsplit) * 2 + 0] = m_run[h];
-      a.part_ml[(pbase + (size_t)h * a.nsplit) * 2 + 1] = l_run[h];
-    }
-}
-
-// One CTA of D threads per (row, query head): merge the split partials of the CUDA-core
-// kernel (split 0 + one per chunk of the middle tier).
-template <int D>
-__global__ void __launch_bounds__(D) attn_combine_kernel(AttnArgs a, uint16_t* __restrict__ out,
-                                                         float* __restrict__ ml) {
-  const int bh = blockIdx.x;
-  const int b = bh / a.Hq, hq = bh % a.Hq;
-  const int G = a.Hq / a.H;
-  const int unit = b * a.H + hq / G;
-  const int n_mid = a.meta[unit * kF + FADE_META_N_MID];
-  const int ns = min(a.nsplit, 1 + (n_mid + a.chunk - 1) / a.chunk);
-  const float* pm = a.part_ml + (size_t)bh * a.nsplit * 2;
-  const float* pa = a.part_acc + (size_t)bh * a.nsplit * D;
-  float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, pm[2 * s]);
-  float Lsum = 0.f, o = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float w = (pm[2 * s] == -INFINITY) ? 0.f : __expf(pm[2 * s] - M);
-    Lsum = fmaf(pm[2 * s + 1], w, Lsum);
-    o = fmaf(pa[(size_t)s * D + threadIdx.x], w, o);
-  }
-  out[(size_t)bh * D + threadIdx.x] = f2h(o / Lsum);
-  if (threadIdx.x == 0) {
-    ml[2 * bh] = M;
-    ml[2 * bh + 1] = Lsum;
-  }
-}
 
 // The tensor-core kernel's partials (split 0 + one per stream-K segment of the unit).
 // One CTA per unit (row, KV head), one warp per query head, D/32 channels per lane. No
@@ -602,59 +264,6 @@ __global__ void __launch_bounds__(256) h2o_accumulate4_kernel(AccArgs a) {
   }
 }
 
-template <int D, int KB, int VB, int G, bool PQ>
-fade_status_t launch_split(const AttnArgs& a, int B, cudaStream_t st, int nx) {
-  using L = Smem<D, KB, VB, G, PQ>;
-  // opt in to more than 48 KB of dynamic shared memory (cheap; done on every launch so it
-  // holds for whichever device is current)
-  if (cudaFuncSetAttribute(attn_split_kernel<D, KB, VB, G, PQ>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL) != cudaSuccess)
-    return launch_status("fade_decode_attention shared-memory opt-in");
-  attn_split_kernel<D, KB, VB, G, PQ><<<dim3(nx, a.H, B), kThreads, L::TOTAL, st>>>(a);
-  return launch_status("fade_decode_attention split");
-}
-
-template <int D, int KB, int VB, bool PQ = false>
-fade_status_t launch_split_g(const AttnArgs& a, int G, int B, cudaStream_t st, int nx) {
-  switch (G) {
-    case 1: return launch_split<D, KB, VB, 1, PQ>(a, B, st, nx);
-    case 2: return launch_split<D, KB, VB, 2, PQ>(a, B, st, nx);
-    case 4: return launch_split<D, KB, VB, 4, PQ>(a, B, st, nx);
-    case 8: return launch_split<D, KB, VB, 8, PQ>(a, B, st, nx);
-  }
-  return set_error(FADE_ERR_UNSUPPORTED, "query heads per KV head %d", G);
-}
-
-// Launches splits [0, nx) of the CUDA-core kernel.
-fade_status_t launch_split_any(const fade_config_t* c, const AttnArgs& a, cudaStream_t st, int nx) {
-  const int G = c->num_q_heads / c->num_kv_heads, B = c->batch;
-  const int d = c->head_dim, kb = c->middle_k_bits, vb = c->middle_v_bits;
-  if (c->v_codec == FADE_V_PQ) {  // PQ codes occupy the INT2 rows (validated)
-    if (d == 64) return kb == 4 ? launch_split_g<64, 4, 2, true>(a, G, B, st, nx)
-                                : launch_split_g<64, 2, 2, true>(a, G, B, st, nx);
-    return kb == 4 ? launch_split_g<128, 4, 2, true>(a, G, B, st, nx)
-                   : launch_split_g<128, 2, 2, true>(a, G, B, st, nx);
-  }
-#define FADE_CASE(D_, KB_, VB_) \
-  if (d == D_ && kb == KB_ && vb == VB_) return launch_split_g<D_, KB_, VB_>(a, G, B, st, nx);
-  FADE_CASE(64, 4, 2) FADE_CASE(64, 4, 4) FADE_CASE(64, 2, 2) FADE_CASE(64, 2, 4)
-  FADE_CASE(128, 4, 2) FADE_CASE(128, 4, 4) FADE_CASE(128, 2, 2) FADE_CASE(128, 2, 4)
-#undef FADE_CASE
-  return set_error(FADE_ERR_UNSUPPORTED, "unsupported (head_dim, k_bits, v_bits)");
-}
-
-// Middle tokens per split: enough CTAs to fill the GPU several times over, splits of equal
-// size, each a whole number of tiles.
-int choose_chunk(int max_mid, int units, int tile, long long target_ctas) {
-  if (max_mid <= 0) return tile;
-  long long want = ((long long)max_mid * units + target_ctas - 1) / target_ctas;
-  if (want < tile) want = tile;
-  const long long n = (max_mid + want - 1) / want;
-  long long ch = (max_mid + n - 1) / n;
-  ch = ((ch + tile - 1) / tile) * tile;
-  return (int)ch;
-}
-
 }  // namespace
 }  // namespace fade
 
@@ -680,45 +289,14 @@ extern "C" fade_status_t fade_decode_attention(const fade_config_t* c, const fad
   if (max_mid == 0 && max_fp16 == 0)
     return set_error(FADE_ERR_INVALID_ARGUMENT, "the cache is empty");
   const int units = c->batch * c->num_kv_heads;
+  if (!mid_mma_supported(c))
+    return set_error(FADE_ERR_UNSUPPORTED, "no tensor-core attention for these code widths");
+  StreamK sk{};  // the stream-K schedule of the middle tiles (from the host mirror)
+  build_stream_k(c, L, mid_mma_ctas(c), &sk);
   AttnArgs a;
-  a.q = q_rot;
-  a.sink_k = L->sink_k;
-  a.sink_v = L->sink_v;
-  a.rec_k = L->recent_k;
-  a.rec_v = L->recent_v;
-  for (int i = 0; i < 2; ++i) {
-    a.mk[i] = L->mid_k_codes[i];
-    a.mv[i] = L->mid_v_codes[i];
-    a.mks[i] = L->mid_k_scales[i];
-    a.mvs[i] = L->mid_v_scales[i];
-  }
-  a.meta = L->meta;
-  a.logits = logits_ws;
   a.Hq = c->num_q_heads;
   a.H = c->num_kv_heads;
-  a.S = c->n_sink;
-  a.W = c->recent_window;
-  a.C = mid_stride(c);
-  a.NS = a.S + a.C + a.W;
-  const bool mma = mid_mma_supported(c);
-  StreamK sk{};  // the tensor-core kernel's stream-K schedule (unused by the CUDA-core kernel)
-  if (mma) {
-    build_stream_k(c, L, mid_mma_ctas(c), &sk);
-    a.chunk = kTileTokens;
-    a.nsplit = 1 + sk.smax;
-  } else {
-    sk.P = 0;
-    // splits sized by the middle capacity, not the current count: the launch is then the
-    // same at every step while the cache grows (a captured step can be replayed), and splits
-    // past a unit's tokens write empty partials. PQ: fewer, longer middle splits, so that
-    // staging the codebook (256 x d fp16 from L2) stays small beside the split's own bytes
-    a.chunk = choose_chunk(c->mid_capacity, units,
-                           c->v_codec == FADE_V_PQ ? 16 * kTile : kTile,
-                           (c->v_codec == FADE_V_PQ ? 4LL : 8LL) * 152);
-    a.nsplit = 1 + (c->mid_capacity + a.chunk - 1) / a.chunk;
-  }
-  a.scale = 1.0f / sqrtf((float)c->head_dim);
-  a.pq_cb = L->pq_codebook;
+  a.nsplit = 1 + sk.smax;
   const size_t part = (size_t)c->batch * c->num_q_heads * a.nsplit * (c->head_dim + 2) * 4;
   const size_t need = part + (size_t)units * 4;
   if (ws_bytes < need)
@@ -729,39 +307,27 @@ extern "C" fade_status_t fade_decode_attention(const fade_config_t* c, const fad
   int32_t* seg_count = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + part);
   a.seg_count = seg_count;
   cudaStream_t s = as_stream(stream);
-  if (mma) {
-    // one launch: FP16 tiers (split 0) and the packed middle tier (tensor cores)
-    if ((st = launch_mid_mma(c, L, q_rot, logits_ws, a.part_ml, a.part_acc, seg_count, sk,
-                             a.nsplit, s)))
-      return st;
-  } else if ((st = launch_split_any(c, a, s, a.nsplit))) {
+  // one launch: FP16 tiers (split 0) and the packed middle tier (tensor cores)
+  if ((st = launch_mid_mma(c, L, q_rot, logits_ws, a.part_ml, a.part_acc, seg_count, sk,
+                           a.nsplit, s)))
     return st;
-  }
-  const int bh = c->batch * c->num_q_heads;
-  if (mma) {
-    // the combine launches as a programmatic dependent of the attention kernel (its CTAs are
-    // scheduled while the attention grid drains and wait on the device for its completion)
-    cudaLaunchConfig_t lc{};
-    lc.gridDim = dim3(units);
-    lc.blockDim = dim3(32 * (a.Hq / a.H));
-    lc.dynamicSmemBytes = 0;
-    lc.stream = s;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
-    lc.attrs = at;
-    lc.numAttrs = 1;
-    const cudaError_t e =
-        c->head_dim == 64
-            ? cudaLaunchKernelEx(&lc, attn_combine_sk_kernel<64>, a, out, ml_ws)
-            : cudaLaunchKernelEx(&lc, attn_combine_sk_kernel<128>, a, out, ml_ws);
-    if (e != cudaSuccess)
-      return set_error(FADE_ERR_CUDA, "fade_decode_attention combine: %s", cudaGetErrorString(e));
-  } else if (c->head_dim == 64) {
-    attn_combine_kernel<64><<<bh, 64, 0, s>>>(a, out, ml_ws);
-  } else {
-    attn_combine_kernel<128><<<bh, 128, 0, s>>>(a, out, ml_ws);
-  }
+  // the combine launches as a programmatic dependent of the attention kernel (its CTAs are
+  // scheduled while the attention grid drains and wait on the device for its completion)
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(units);
+  lc.blockDim = dim3(32 * (a.Hq / a.H));
+  lc.dynamicSmemBytes = 0;
+  lc.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  const cudaError_t e =
+      c->head_dim == 64 ? cudaLaunchKernelEx(&lc, attn_combine_sk_kernel<64>, a, out, ml_ws)
+                        : cudaLaunchKernelEx(&lc, attn_combine_sk_kernel<128>, a, out, ml_ws);
+  if (e != cudaSuccess)
+    return set_error(FADE_ERR_CUDA, "fade_decode_attention combine: %s", cudaGetErrorString(e));
   return launch_status("fade_decode_attention combine");
 }
 

@@ -116,8 +116,9 @@ __host__ __device__ inline int sk_segments(const StreamK& k, int b, int h) {
   return sk_nonempty(k, sk_cta_of(k, g0), sk_cta_of(k, g0 + rt - 1));
 }
 
-// Decode attention for INT4 K / INT2 V: split 0 covers the FP16 tiers on the CUDA cores,
-// splits 1.. the middle tier on the tensor cores. Defined in attention_mma.cu.
+// Decode attention on the tensor cores (INT4 or INT2 K; INT2, INT4 or PQ-coded V): split 0
+// covers the FP16 tiers, splits 1.. the segments of the middle tier. Defined in
+// attention_mma.cu (kernels in attention_mma.cuh; INT2-K instantiations in attention_mma_k2.cu).
 bool mid_mma_supported(const fade_config_t* c);
 // Persistent CTAs the kernel runs with on the current device.
 int mid_mma_ctas(const fade_config_t* c);

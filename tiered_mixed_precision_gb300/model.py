@@ -395,11 +395,10 @@ class FadeCache:
                    for L in self.layers)
 
     def growing_graph_key(self) -> tuple:
-        """What a captured growing step depends on beyond the device-side counts: with the
-        tensor-core attention kernel, every layer's and row's number of middle tiles at the
-        coming step's attention call (after its demotion: one more middle token), from which
-        the launch's stream-K schedule is built; nothing with the CUDA-core kernel, whose
-        launch is sized by the middle capacity."""
+        """What a captured growing step depends on beyond the device-side counts: every
+        layer's and row's number of middle tiles at the coming step's attention call (after its
+        demotion: one more middle token), from which the attention launch's stream-K schedule
+        is built (empty if a configuration's launch were not scheduled by tiles)."""
         if not F.fade_attention_tiled(self.cfg):
             return ()
         t = F.ATTN_TILE_TOKENS
