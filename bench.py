@@ -74,6 +74,9 @@ def parse_args():
     p.add_argument("--v-codec", default="int", choices=["int", "pq"],
                    help="middle-tier V: INT codes with scales, or product-quantised (a codebook "
                         "trained on the GPU from synthetic calibration rows before timing)")
+    p.add_argument("--k-bits", type=int, default=None, choices=[2, 4],
+                   help="middle-tier K code width instead of the workload's (a custom variant "
+                        "of the workload, named with a _k<bits> suffix; no CPU baseline)")
     p.add_argument("--no-pipeline", action="store_true",
                    help="in the graph, run each layer's maintenance before its attention instead "
                         "of overlapping it with the following layers")
@@ -365,6 +368,8 @@ def run_ours(args, rank, world):
         wl = wl.scaled(layers=args.layers)
     if args.batch:
         wl = wl.scaled(batch=args.batch)
+    if args.k_bits:
+        wl = wl.scaled(middle_k_bits=args.k_bits, name=f"{wl.name}_k{args.k_bits}")
     lens = ragged_context_lengths(wl)
     maxP = int(lens.max())
     K, W = args.steps, args.warmup
@@ -668,7 +673,8 @@ def run_ours(args, rank, world):
                    "recent_window": wl.recent_window, "int4_budget": wl.int4_budget,
                    "policy": wl.policy, "k_bits": wl.middle_k_bits, "v_bits": wl.middle_v_bits,
                    "shared_rows": bool(args.shared_rows), "v_codec": args.v_codec,
-                   "storage": ("fp16 sinks/recent, packed INT4 K / INT2 V middle"
+                   "storage": (f"fp16 sinks/recent, packed INT{wl.middle_k_bits} K / "
+                               f"INT{wl.middle_v_bits} V middle"
                                if args.v_codec == "int" else
                                f"fp16 sinks/recent, packed INT{wl.middle_k_bits} K / PQ V middle "
                                f"(256 centroids per 4-channel sub-space, codebook trained on "
@@ -743,7 +749,7 @@ def main():
     res = run_ours(args, rank, world)
     progress("GPU arm done")
     if rank == 0:
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and not args.k_bits:
             cb = run_oracle_sample(args.workload, steps=3, warmup=1, budget_s=20.0)
             progress("oracle sample done")
             res["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
