@@ -173,35 +173,47 @@ def test_rope_append_fused_matches_separate_calls(T, d, hq, hkv, rope, prompt):
         assert (sep.layers[0].h_n_sink == fus.layers[0].h_n_sink).all()
 
 
-@pytest.mark.parametrize("d,kb,vb,codec", [(128, 4, 4, "int"), (64, 4, 2, "int"),
-                                            (64, 2, 2, "int"), (128, 4, 2, "pq")])
-def test_rope_append_with_demotion_matches_separate_calls(T, d, kb, vb, codec):
+@pytest.mark.parametrize("d,kb,vb,codec,ragged", [(128, 4, 4, "int", None),
+                                                   (64, 4, 2, "int", None),
+                                                   (64, 2, 2, "int", None),
+                                                   (128, 4, 2, "pq", None),
+                                                   (128, 4, 4, "int", (30, 140))])
+def test_rope_append_with_demotion_matches_separate_calls(T, d, kb, vb, codec, ragged):
     """fade_rope_append with demote: the demotion (K and V quantise-packed, or V PQ-encoded,
     into the next middle slot, the score moved), the RoPE of q and k and the append, in one
     launch, bit for bit as fade_cache_demote, fade_rope_apply twice and fade_cache_append."""
     import torch
 
     from synth import draw_prompt, draw_vectors
-    from synth.draws import pq_calibration
+    from synth.draws import pq_calibration, ragged_context_lengths
     from tiered_mixed_precision_gb300.model import FadeCache
 
-    wl = get_workload(2).scaled(layers=1, batch=2, num_q_heads=8, num_kv_heads=2, head_dim=d,
-                                middle_k_bits=kb, middle_v_bits=vb, prompt_len=100, steps=3)
+    # ragged: rows of 35 to 80 prompt tokens, so some rings are full (those rows demote) and
+    # others are not, in the same launch
+    wl = get_workload(2).scaled(layers=1, batch=4 if ragged else 2, num_q_heads=8,
+                                num_kv_heads=2, head_dim=d, middle_k_bits=kb, middle_v_bits=vb,
+                                prompt_len=140 if ragged else 100, steps=3, ragged=ragged)
+    lens = ragged_context_lengths(wl)
+    P = int(lens.max())
 
     def make():
         cfg = T.Config.from_workload(wl, mid_capacity=200)
         cfg.v_codec = codec
-        fc = FadeCache(cfg, 1, 100, 120, "cuda")
+        fc = FadeCache(cfg, 1, P, P + 20, "cuda")
         if codec == "pq":
             rows = pq_calibration(wl, 256)
             cb = rows.reshape(256, d // 4, 4).transpose(1, 0, 2).copy()
             fc.set_pq_codebook(torch.from_numpy(cb).cuda())
-        pr = draw_prompt(wl, 0)
-        fc.prefill(0, torch.from_numpy(pr["k"]).cuda(), torch.from_numpy(pr["v"]).cuda())
+        pr = draw_prompt(wl, 0, P)
+        fc.prefill(0, torch.from_numpy(pr["k"]).cuda(), torch.from_numpy(pr["v"]).cuda(), lens)
         return fc
 
     sep, fus = make(), make()
-    assert (sep.layers[0].h_n_recent == wl.recent_window).all()   # every step demotes
+    full = sep.layers[0].h_n_recent == wl.recent_window
+    if ragged:
+        assert full.any() and not full.all()   # both kinds of row in the launch
+    else:
+        assert full.all()                      # every step demotes
     B, hq, hkv = wl.batch, wl.num_q_heads, wl.num_kv_heads
     for step in range(3):
         q = torch.from_numpy(draw_vectors(wl, "q", (B, hq, d), "fuse_dem", step)).cuda()
