@@ -1,5 +1,5 @@
 // Decode attention over the tiered cache: the entry point (schedule, workspace), the combine of
-// the tensor-core kernel's partials (attention_mma.cu), and H2O / EMA score accumulation.
+// the tensor-core kernel's partials (attention_mma.cuh), and H2O / EMA score accumulation.
 // Sources: page "FADE：面向LLM推理的注意力感知分层KV缓存压缩技术" — §项目结构与代码质量 (kernels/:
 // fused INT4 dequant + SDPA), §四种驱逐策略详解 1 (H2O: keep the highest accumulated attention)
 // and 2 (EMA of attention during decode); page "探秘Transformer系列之（25）--- KV Cache优化之处理

@@ -62,6 +62,9 @@ struct MmaArgs {
 fade_status_t launch_mid_mma_k2(const fade_config_t* c, const fade_layer_t* L, MmaArgs a,
                                 const StreamK& sk, cudaStream_t st);
 
+// Everything below has internal linkage: attention_mma.cu (INT4 K) and attention_mma_k2.cu
+// (INT2 K) each include this header and hold their own instantiations, and their own host-side
+// tensor-map cache.
 namespace {
 
 constexpr int kF = FADE_META_FIELDS;
