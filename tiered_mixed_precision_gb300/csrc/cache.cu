@@ -350,38 +350,55 @@ __global__ void reset_kernel(int32_t* meta, int n) {
 // One warp: the oldest ring token (slot `head`) of a unit quantise-packed into middle slot
 // n_mid of buffer `cur` (K at KB bits; V at VB bits, or PQ-encoded), its score moved with it.
 // The unit's counts are the caller's to update.
-template <int D, int KB, int VB>
-__device__ __forceinline__ void warp_demote_unit(const LayerArgs& a, int unit, int n_mid, int cur,
-                                                 int head) {
+// The two halves of a demotion, each for one warp: K codes and scales plus the score, and V.
+template <int D, int KB>
+__device__ __forceinline__ void warp_demote_k(const LayerArgs& a, int unit, int n_mid, int cur,
+                                              int head) {
   const size_t rrow = ((size_t)unit * a.W + head) * D;
   const size_t mrow = (size_t)unit * a.C + n_mid;
   warp_quantize_row<D, KB>(a.rec_k + rrow, (cur ? a.mk[1] : a.mk[0]) + mrow * (D * KB / 8),
                            (cur ? a.mks[1] : a.mks[0]) + mrow * (D / kGroup));
+  if ((threadIdx.x & 31) == 0)
+    (cur ? a.mid_sc[1] : a.mid_sc[0])[mrow] = a.rec_sc[(size_t)unit * a.W + head];
+}
+template <int D, int VB>
+__device__ __forceinline__ void warp_demote_v(const LayerArgs& a, int unit, int n_mid, int cur,
+                                              int head) {
+  const size_t rrow = ((size_t)unit * a.W + head) * D;
+  const size_t mrow = (size_t)unit * a.C + n_mid;
   if (a.pq)
     warp_pq_encode_row<D>(a.rec_v + rrow, a.pq_cb, (cur ? a.mv[1] : a.mv[0]) + mrow * (D / 4),
                           (cur ? a.mvs[1] : a.mvs[0]) + mrow * (D / kGroup));
   else
     warp_quantize_row<D, VB>(a.rec_v + rrow, (cur ? a.mv[1] : a.mv[0]) + mrow * (D * VB / 8),
                              (cur ? a.mvs[1] : a.mvs[0]) + mrow * (D / kGroup));
+}
+template <int D, int KB, int VB>
+__device__ __forceinline__ void warp_demote_unit(const LayerArgs& a, int unit, int n_mid, int cur,
+                                                 int head) {
+  warp_demote_k<D, KB>(a, unit, n_mid, cur, head);
+  warp_demote_v<D, VB>(a, unit, n_mid, cur, head);
   __syncwarp();
-  if ((threadIdx.x & 31) == 0)
-    (cur ? a.mid_sc[1] : a.mid_sc[0])[mrow] = a.rec_sc[(size_t)unit * a.W + head];
 }
 
-// One warp per unit: if the ring is full, quantise its oldest token into middle slot N_MID.
+// Two warps per unit: if the ring is full, quantise its oldest token into middle slot N_MID
+// (warp 0 its K and score, warp 1 its V, side by side).
 template <int D, int KB, int VB>
-__global__ void __launch_bounds__(32) demote_kernel(LayerArgs a) {
+__global__ void __launch_bounds__(64) demote_kernel(LayerArgs a) {
   const int unit = blockIdx.y * a.H + blockIdx.x;
   int32_t* m = a.meta + unit * kF;
   const int n_rec = m[FADE_META_N_RECENT];
-  if (n_rec != a.W) return;
+  if (n_rec != a.W) return;  // uniform per CTA
   const int n_mid = m[FADE_META_N_MID], cur = m[FADE_META_CUR], head = m[FADE_META_HEAD];
   if (n_mid >= a.C || head < 0 || head >= a.W) {  // the host checks capacity; never overrun
     if (threadIdx.x == 0) record_status(a.status, kCheckDemoteSlot);
     return;
   }
-  warp_demote_unit<D, KB, VB>(a, unit, n_mid, cur, head);
-  __syncwarp();
+  if (threadIdx.x < 32)
+    warp_demote_k<D, KB>(a, unit, n_mid, cur, head);
+  else
+    warp_demote_v<D, VB>(a, unit, n_mid, cur, head);
+  __syncthreads();  // both warps have read the counts and the ring slot
   if (threadIdx.x == 0) {
     m[FADE_META_N_MID] = n_mid + 1;
     m[FADE_META_N_RECENT] = n_rec - 1;
@@ -1525,7 +1542,7 @@ fade_status_t dispatch_dkv(const fade_config_t* c, Args&&... args) {
 template <int D, int KB, int VB>
 struct DemoteLaunch {
   static fade_status_t run(const LayerArgs& a, int B, cudaStream_t st) {
-    demote_kernel<D, KB, VB><<<dim3(a.H, B), 32, 0, st>>>(a);
+    demote_kernel<D, KB, VB><<<dim3(a.H, B), 64, 0, st>>>(a);
     return launch_status("fade_cache_demote");
   }
 };
