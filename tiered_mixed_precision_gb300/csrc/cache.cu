@@ -373,13 +373,6 @@ __device__ __forceinline__ void warp_demote_v(const LayerArgs& a, int unit, int 
     warp_quantize_row<D, VB>(a.rec_v + rrow, (cur ? a.mv[1] : a.mv[0]) + mrow * (D * VB / 8),
                              (cur ? a.mvs[1] : a.mvs[0]) + mrow * (D / kGroup));
 }
-template <int D, int KB, int VB>
-__device__ __forceinline__ void warp_demote_unit(const LayerArgs& a, int unit, int n_mid, int cur,
-                                                 int head) {
-  warp_demote_k<D, KB>(a, unit, n_mid, cur, head);
-  warp_demote_v<D, VB>(a, unit, n_mid, cur, head);
-  __syncwarp();
-}
 
 // Two warps per unit: if the ring is full, quantise its oldest token into middle slot N_MID
 // (warp 0 its K and score, warp 1 its V, side by side).
@@ -454,11 +447,14 @@ __global__ void __launch_bounds__(32) append_kernel(LayerArgs a, const uint16_t*
 // cos and sin, the remaining slots copy their two pass-through channels; no table: a copy),
 // the queries into q_rot and the key straight into the slot append_kernel gives it (a sink
 // while fewer than n_sink are held, else the newest ring entry), with its value and score 0.
-// DEMOTE: first, if the ring is full, warp 0 demotes its oldest token exactly as demote_kernel
-// does (while the other warps rotate queries); the new token then takes the freed slot.
+// DEMOTE: first, if the ring is full, warps 0 and 1 demote its oldest token exactly as
+// demote_kernel does (while the other warps rotate queries); the new token then takes the freed
+// slot.
 #ifndef FADE_ROPE_APPEND_THREADS
 #define FADE_ROPE_APPEND_THREADS 256
 #endif
+static_assert(FADE_ROPE_APPEND_THREADS >= 64 && FADE_ROPE_APPEND_THREADS % 32 == 0,
+              "two demoting warps");
 template <int D, int KB, int VB, bool DEMOTE>
 __global__ void __launch_bounds__(FADE_ROPE_APPEND_THREADS)
     rope_append_kernel(LayerArgs a, const float* __restrict__ table, int max_pos, int rh,
@@ -480,7 +476,10 @@ __global__ void __launch_bounds__(FADE_ROPE_APPEND_THREADS)
       if (threadIdx.x == 0) record_status(a.status, kCheckDemoteSlot);
       return;
     }
-    if (threadIdx.x < 32) warp_demote_unit<D, KB, VB>(a, unit, n_mid, cur, head0);
+    if (threadIdx.x < 32)
+      warp_demote_k<D, KB>(a, unit, n_mid, cur, head0);
+    else if (threadIdx.x < 64)
+      warp_demote_v<D, VB>(a, unit, n_mid, cur, head0);
     n_rec = n_rec0 - 1;
     head = (head0 + 1) % a.W;
   }
