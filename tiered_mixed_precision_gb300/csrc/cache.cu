@@ -453,8 +453,8 @@ __global__ void __launch_bounds__(32) append_kernel(LayerArgs a, const uint16_t*
 #ifndef FADE_ROPE_APPEND_THREADS
 #define FADE_ROPE_APPEND_THREADS 256
 #endif
-static_assert(FADE_ROPE_APPEND_THREADS >= 64 && FADE_ROPE_APPEND_THREADS % 32 == 0,
-              "two demoting warps");
+static_assert(FADE_ROPE_APPEND_THREADS >= 128 && FADE_ROPE_APPEND_THREADS % 32 == 0,
+              "two demoting warps; one thread per channel of the new token (D <= 128)");
 template <int D, int KB, int VB, bool DEMOTE>
 __global__ void __launch_bounds__(FADE_ROPE_APPEND_THREADS)
     rope_append_kernel(LayerArgs a, const float* __restrict__ table, int max_pos, int rh,
@@ -483,27 +483,42 @@ __global__ void __launch_bounds__(FADE_ROPE_APPEND_THREADS)
     n_rec = n_rec0 - 1;
     head = (head0 + 1) % a.W;
   }
-  // one slot of vector x (D channels) into y
-  auto rot = [&](const uint16_t* x, uint16_t* y, int k) {
+  // slot k of vector x (D channels): its two output channels c0, c1 and their values
+  auto rot = [&](const uint16_t* x, int k, int& c0, int& c1, uint16_t& y0, uint16_t& y1) {
     if (!table) {
-      y[k] = x[k];
-      y[k + half] = x[k + half];
+      c0 = k;
+      c1 = k + half;
+      y0 = x[c0];
+      y1 = x[c1];
     } else if (k >= rh) {
-      const int c = 2 * rh + 2 * (k - rh);
-      y[c] = x[c];
-      y[c + 1] = x[c + 1];
+      c0 = 2 * rh + 2 * (k - rh);
+      c1 = c0 + 1;
+      y0 = x[c0];
+      y1 = x[c1];
     } else {
-      float y1, y2;
+      float f1, f2;
       rotate_pair(h2f(x[k]), h2f(x[k + rh]), rope_cos(table, half, p, k),
-                  rope_sin(table, half, p, k), y1, y2);
-      y[k] = f2h(y1);
-      y[k + rh] = f2h(y2);
+                  rope_sin(table, half, p, k), f1, f2);
+      c0 = k;
+      c1 = k + rh;
+      y0 = f2h(f1);
+      y1 = f2h(f2);
     }
   };
   for (int i = threadIdx.x; i < G * half; i += blockDim.x) {
     const size_t base = ((size_t)b * Hq + (size_t)h * G + i / half) * D;
-    rot(q_raw + base, q_rot + base, i % half);
+    int c0, c1;
+    uint16_t y0, y1;
+    rot(q_raw + base, i % half, c0, c1, y0, y1);
+    q_rot[base + c0] = y0;
+    q_rot[base + c1] = y1;
   }
+  // the new token's key slot (thread k < D/2) rotated and its value channel (thread c < D) read
+  // now; both are stored once the demotion has read the slot they may overwrite
+  int kc0 = 0, kc1 = 0;
+  uint16_t ky0 = 0, ky1 = 0, vy = 0;
+  if (threadIdx.x < half) rot(k_raw + (size_t)unit * D, threadIdx.x, kc0, kc1, ky0, ky1);
+  if (threadIdx.x < D) vy = v[(size_t)unit * D + threadIdx.x];
   if (demote) __syncthreads();  // the demoted slot is read before the new token overwrites it
   const bool to_sink = n_sink < a.S;
   if (!to_sink && n_rec >= a.W) {  // the host checks capacity; never overwrite the ring
@@ -524,8 +539,11 @@ __global__ void __launch_bounds__(FADE_ROPE_APPEND_THREADS)
     dv = a.rec_v + row * D;
     dsc = a.rec_sc + row;
   }
-  for (int k = threadIdx.x; k < half; k += blockDim.x) rot(k_raw + (size_t)unit * D, dk, k);
-  for (int c = threadIdx.x; c < D; c += blockDim.x) dv[c] = v[(size_t)unit * D + c];
+  if (threadIdx.x < half) {
+    dk[kc0] = ky0;
+    dk[kc1] = ky1;
+  }
+  if (threadIdx.x < D) dv[threadIdx.x] = vy;
   __syncthreads();  // every thread has read the counts
   if (threadIdx.x == 0) {
     *dsc = 0.f;
