@@ -48,6 +48,8 @@ __global__ void __launch_bounds__(256) attn_combine_sk_kernel(AttnArgs a,
   // the attention grid's last CTAs still run; wait here until that grid has completed and its
   // partials are visible (a no-op when launched without the dependency)
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the score update that may follow is a programmatic dependent in turn
+  asm volatile("griddepcontrol.launch_dependents;");
   const int ns = max(1, min(a.nsplit, a.seg_count[unit]));
   float M = -INFINITY, L = 0.f, o[CPL];
 #pragma unroll
@@ -123,6 +125,9 @@ struct AccArgs {
 // slots the unit does not hold the values are read and dropped). One round trip to memory
 // per thread, then the update.
 __global__ void __launch_bounds__(256) h2o_accumulate_kernel(AccArgs a) {
+  // launched as a programmatic dependent of the attention call's combine: wait here until that
+  // grid has completed and its (M, L) are visible (a no-op when launched without the dependency)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= a.NS) return;
   const int hk = blockIdx.y, b = blockIdx.z, unit = b * a.H + hk;
@@ -195,6 +200,7 @@ __global__ void __launch_bounds__(256) h2o_accumulate_kernel(AccArgs a) {
 // kernel's, term for term.
 template <int G>
 __global__ void __launch_bounds__(256) h2o_accumulate4_kernel(AccArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // as in h2o_accumulate_kernel
   const int j0 = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
   if (j0 >= a.NS) return;
   const int hk = blockIdx.y, b = blockIdx.z, unit = b * a.H + hk;
@@ -358,19 +364,34 @@ extern "C" fade_status_t fade_h2o_accumulate(const fade_config_t* c, fade_layer_
   a.policy = c->policy;
   a.decay = c->ema_decay;
   const int G = c->num_q_heads / c->num_kv_heads;
-  cudaStream_t cs = as_stream(stream);
+  // a programmatic dependent of the kernel before it on the stream (the attention call's
+  // combine, in a decode step): its CTAs are scheduled while that grid drains and wait on the
+  // device for its completion
+  cudaLaunchConfig_t lc{};
+  lc.blockDim = dim3(256);
+  lc.dynamicSmemBytes = 0;
+  lc.stream = as_stream(stream);
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  cudaError_t e;
   if (a.S % 4 == 0 && a.NS % 4 == 0 && al16(a.logits) && al16(a.sink_sc) && al16(a.mid_sc[0]) &&
       al16(a.mid_sc[1]) && al16(a.rec_sc)) {
-    const dim3 grid(ceil_div(a.NS / 4, 256), c->num_kv_heads, c->batch);
+    lc.gridDim = dim3(ceil_div(a.NS / 4, 256), c->num_kv_heads, c->batch);
     switch (G) {
-      case 1: h2o_accumulate4_kernel<1><<<grid, 256, 0, cs>>>(a); break;
-      case 2: h2o_accumulate4_kernel<2><<<grid, 256, 0, cs>>>(a); break;
-      case 4: h2o_accumulate4_kernel<4><<<grid, 256, 0, cs>>>(a); break;
-      default: h2o_accumulate4_kernel<8><<<grid, 256, 0, cs>>>(a); break;
+      case 1: e = cudaLaunchKernelEx(&lc, h2o_accumulate4_kernel<1>, a); break;
+      case 2: e = cudaLaunchKernelEx(&lc, h2o_accumulate4_kernel<2>, a); break;
+      case 4: e = cudaLaunchKernelEx(&lc, h2o_accumulate4_kernel<4>, a); break;
+      default: e = cudaLaunchKernelEx(&lc, h2o_accumulate4_kernel<8>, a); break;
     }
   } else {
-    h2o_accumulate_kernel<<<dim3(ceil_div(a.NS, 256), c->num_kv_heads, c->batch), 256, 0, cs>>>(a);
+    lc.gridDim = dim3(ceil_div(a.NS, 256), c->num_kv_heads, c->batch);
+    e = cudaLaunchKernelEx(&lc, h2o_accumulate_kernel, a);
   }
+  if (e != cudaSuccess)
+    return set_error(FADE_ERR_CUDA, "fade_h2o_accumulate: %s", cudaGetErrorString(e));
   return launch_status("fade_h2o_accumulate");
 }
