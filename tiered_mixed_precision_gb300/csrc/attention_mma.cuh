@@ -816,6 +816,11 @@ attn_mid_mma_kernel(const __grid_constant__ CUtensorMap tk0, const __grid_consta
   }
   __syncthreads();
   volatile int* abort = &s_abort;
+  // when launched as a programmatic dependent of the kernel before it (the append of the new
+  // token; a layer with fewer middle tiles than CTAs): everything above reads only the schedule
+  // and this CTA's shared memory; wait here until that grid has completed and its writes
+  // (counts, ring rows, rotated queries) are visible (a no-op otherwise)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // the combine kernel that follows is a programmatic dependent: let it be scheduled now (its
   // CTAs take SM slots as this grid's CTAs exit and wait on the device for this grid's end)
   asm volatile("griddepcontrol.launch_dependents;");
@@ -1521,9 +1526,24 @@ fade_status_t launch_mma(const fade_config_t* c, const fade_layer_t* L, MmaArgs 
       return launch_status("fade_decode_attention (middle tier) shared-memory opt-in");
     if (dev < 64) smem_set.fetch_or(1ull << dev);
   }
-  // persistent grid: the schedule's CTAs (as many as fit on the device at once)
-  kern<<<sk.P, MmaShape<D, G, PQ>::THREADS, kSmem, st>>>(tk[0], tk[1], tv[0], tv[1], tsk, tsv,
-                                                         trk, trv, a, sk);
+  // persistent grid: the schedule's CTAs (as many as fit on the device at once). A layer with
+  // fewer middle tiles than CTAs is bound by launch latency: its kernel is a programmatic
+  // dependent of the kernel before it on the stream (its prologue overlaps that kernel's end)
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(sk.P);
+  lc.blockDim = dim3(MmaShape<D, G, PQ>::THREADS);
+  lc.dynamicSmemBytes = kSmem;
+  lc.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = sk.row_start[sk.B] < sk.P ? 1 : 0;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  const cudaError_t e =
+      cudaLaunchKernelEx(&lc, kern, tk[0], tk[1], tv[0], tv[1], tsk, tsv, trk, trv, a, sk);
+  if (e != cudaSuccess)
+    return set_error(FADE_ERR_CUDA, "fade_decode_attention (middle tier): %s",
+                     cudaGetErrorString(e));
   return launch_status("fade_decode_attention (middle tier)");
 }
 

@@ -461,6 +461,8 @@ __global__ void __launch_bounds__(FADE_ROPE_APPEND_THREADS)
                        const uint16_t* __restrict__ q_raw, const uint16_t* __restrict__ k_raw,
                        const uint16_t* __restrict__ v, const int32_t* __restrict__ pos,
                        uint16_t* __restrict__ q_rot, int Hq) {
+  // the attention kernel that follows may be a programmatic dependent: let it be scheduled now
+  asm volatile("griddepcontrol.launch_dependents;");
   constexpr int half = D / 2;
   const int h = blockIdx.x, b = blockIdx.y, unit = b * a.H + h;
   const int G = Hq / a.H;
