@@ -128,6 +128,8 @@ __global__ void __launch_bounds__(256) h2o_accumulate_kernel(AccArgs a) {
   // launched as a programmatic dependent of the attention call's combine: wait here until that
   // grid has completed and its (M, L) are visible (a no-op when launched without the dependency)
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next layer's RoPE + append launch may be a programmatic dependent in turn
+  asm volatile("griddepcontrol.launch_dependents;");
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= a.NS) return;
   const int hk = blockIdx.y, b = blockIdx.z, unit = b * a.H + hk;
@@ -201,6 +203,7 @@ __global__ void __launch_bounds__(256) h2o_accumulate_kernel(AccArgs a) {
 template <int G>
 __global__ void __launch_bounds__(256) h2o_accumulate4_kernel(AccArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");  // as in h2o_accumulate_kernel
+  asm volatile("griddepcontrol.launch_dependents;");
   const int j0 = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
   if (j0 >= a.NS) return;
   const int hk = blockIdx.y, b = blockIdx.z, unit = b * a.H + hk;

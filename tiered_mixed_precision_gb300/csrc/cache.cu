@@ -476,6 +476,7 @@ __global__ void __launch_bounds__(FADE_ROPE_APPEND_THREADS)
     const int n_mid = m[FADE_META_N_MID], cur = m[FADE_META_CUR];
     if (n_mid >= a.C || head0 < 0 || head0 >= a.W) {  // the host checks capacity
       if (threadIdx.x == 0) record_status(a.status, kCheckDemoteSlot);
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // see the end of the kernel
       return;
     }
     if (threadIdx.x < 32)
@@ -525,6 +526,7 @@ __global__ void __launch_bounds__(FADE_ROPE_APPEND_THREADS)
   const bool to_sink = n_sink < a.S;
   if (!to_sink && n_rec >= a.W) {  // the host checks capacity; never overwrite the ring
     if (threadIdx.x == 0) record_status(a.status, kCheckAppendSlot);
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // see the end of the kernel
     return;
   }
   size_t row;
@@ -558,6 +560,11 @@ __global__ void __launch_bounds__(FADE_ROPE_APPEND_THREADS)
     else
       m[FADE_META_N_RECENT] = n_rec + 1;
   }
+  // launched as a programmatic dependent of the previous layer's last kernel (the score update
+  // or the combine), which this kernel's work does not touch: finish only once that grid has
+  // completed, so that whatever follows this kernel finds it done (the attention call reuses the
+  // workspaces it reads)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ----------------------------------------------------------------- eviction (decode)
@@ -1767,13 +1774,24 @@ struct RopeAppendLaunch {
   static fade_status_t run(const LayerArgs& a, bool demote, const float* t, int max_pos, int rh,
                            const uint16_t* q_raw, const uint16_t* k_raw, const uint16_t* v,
                            const int32_t* pos, uint16_t* q_rot, int Hq, int B, cudaStream_t s) {
-    const dim3 grid(a.H, B);
-    if (demote)
-      rope_append_kernel<D, KB, VB, true><<<grid, FADE_ROPE_APPEND_THREADS, 0, s>>>(
-          a, t, max_pos, rh, q_raw, k_raw, v, pos, q_rot, Hq);
-    else
-      rope_append_kernel<D, 4, 2, false><<<grid, FADE_ROPE_APPEND_THREADS, 0, s>>>(
-          a, t, max_pos, rh, q_raw, k_raw, v, pos, q_rot, Hq);
+    // a programmatic dependent of the kernel before it on the stream (see the kernel's end)
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(a.H, B);
+    lc.blockDim = dim3(FADE_ROPE_APPEND_THREADS);
+    lc.dynamicSmemBytes = 0;
+    lc.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    const cudaError_t e =
+        demote ? cudaLaunchKernelEx(&lc, rope_append_kernel<D, KB, VB, true>, a, t, max_pos, rh,
+                                    q_raw, k_raw, v, pos, q_rot, Hq)
+               : cudaLaunchKernelEx(&lc, rope_append_kernel<D, 4, 2, false>, a, t, max_pos, rh,
+                                    q_raw, k_raw, v, pos, q_rot, Hq);
+    if (e != cudaSuccess)
+      return set_error(FADE_ERR_CUDA, "fade_rope_append: %s", cudaGetErrorString(e));
     return launch_status("fade_rope_append");
   }
 };
