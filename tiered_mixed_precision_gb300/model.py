@@ -399,11 +399,17 @@ class FadeCache:
         layer's and row's number of middle tiles at the coming step's attention call (after its
         demotion: one more middle token), from which the attention launch's stream-K schedule
         is built (empty if a configuration's launch were not scheduled by tiles)."""
-        if not F.fade_attention_tiled(self.cfg):
+        tiled = getattr(self, "_attn_tiled", None)
+        if tiled is None:   # a property of the configuration: asked once
+            tiled = self._attn_tiled = bool(F.fade_attention_tiled(self.cfg))
+        if not tiled or not self.layers:
             return ()
+        # one array operation for all layers (this runs on the host before every replay)
         t = F.ATTN_TILE_TOKENS
-        return tuple(tuple(((L.h_n_mid.astype(np.int64) + 1 + t - 1) // t).tolist())
-                     for L in self.layers)
+        tiles = ((np.concatenate([L.h_n_mid for L in self.layers]).astype(np.int64) + t) //
+                 t).tolist()
+        B = len(tiles) // len(self.layers)
+        return tuple(tuple(tiles[i * B:(i + 1) * B]) for i in range(len(self.layers)))
 
     def capture_growing_step(self, q, k, v, out):
         """Capture every layer's step (positions excluded: ``replay_growing`` sets them) as a
