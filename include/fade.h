@@ -295,6 +295,13 @@ fade_status_t fade_pq_train(const uint16_t* calib, int64_t n_vec, int32_t dim,
  * (FADE_ERR_CAPACITY: a full middle tier or recent window) the mirror is left unchanged. */
 fade_status_t fade_cache_advance_host(const fade_config_t* cfg, fade_layer_t* layer);
 
+/* fade_cache_advance_host for n_layers layers of one configuration in one call (layers: HOST
+ * array of n_layers layer pointers, n_layers >= 0): every layer's rows are checked before any
+ * count is stored, so on an error no mirror changes. For a caller replaying a captured step of
+ * many layers, whose host work per step this keeps to one call. */
+fade_status_t fade_cache_advance_host_layers(const fade_config_t* cfg, fade_layer_t* const* layers,
+                                             int32_t n_layers);
+
 /* Empty the cache: zero the device metadata and the host mirror. */
 fade_status_t fade_cache_reset(const fade_config_t* cfg, fade_layer_t* layer, void* stream);
 

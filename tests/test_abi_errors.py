@@ -149,3 +149,39 @@ def test_pq_layer_refuses_to_encode_before_its_codebook_is_set(T):
     assert L.pq_codebook_set
     L.c.status = None   # now the C side runs its own checks (and refuses this layer)
     _expect(T, 1, T.fade_cache_demote, L)
+
+
+def test_advance_host_layers_matches_per_layer_calls_and_is_all_or_nothing(T):
+    """fade_cache_advance_host_layers advances every layer's mirror as per-layer calls would;
+    when one layer's row would overflow, no layer's mirror changes."""
+    def layers(n):
+        out = [_layer(T) for _ in range(n)]
+        for i, L in enumerate(out):
+            L.h_n_sink[:] = [2, i % 2]      # row 0: sinks full; row 1: the append adds a sink
+            L.h_n_recent[:] = [4, 0]        # row 0: the window is full, a demotion is due
+            L.h_n_mid[:] = [i % 4, 0]       # some rows then exceed the budget (3) and evict
+        return out
+
+    def expect(status, *args):
+        with pytest.raises(T.FadeError) as e:
+            T.fade_cache_advance_host_layers(*args)
+        assert e.value.status == status, str(e.value)
+
+    a, b = layers(5), layers(5)
+    for L in a:
+        T.fade_cache_advance_host(L)
+    T.fade_cache_advance_host_layers(b[0].cfg, T.fade.layer_pointer_array(b), len(b))
+    for x, y in zip(a, b):
+        for name in ("h_n_sink", "h_n_mid", "h_n_recent"):
+            assert np.array_equal(getattr(x, name), getattr(y, name)), name
+    # the last layer's first row has a full window and a full middle tier: nothing is stored
+    c = layers(3)
+    c[2].h_n_mid[0] = c[2].cfg.mid_capacity
+    before = [(L.h_n_sink.copy(), L.h_n_mid.copy(), L.h_n_recent.copy()) for L in c]
+    expect(3, c[0].cfg, T.fade.layer_pointer_array(c), 3)
+    for L, (s_, m_, r_) in zip(c, before):
+        assert np.array_equal(L.h_n_sink, s_) and np.array_equal(L.h_n_mid, m_)
+        assert np.array_equal(L.h_n_recent, r_)
+    # an empty list is a no-op; a negative count is rejected
+    T.fade_cache_advance_host_layers(c[0].cfg, None, 0)
+    expect(1, c[0].cfg, None, -1)

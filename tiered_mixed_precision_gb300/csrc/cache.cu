@@ -1837,37 +1837,64 @@ extern "C" fade_status_t fade_rope_append(const fade_config_t* c, fade_layer_t* 
   return FADE_OK;
 }
 
+namespace {
+// One step's count changes of one layer's mirror: pass 0 checks every row, pass 1 stores.
+fade_status_t advance_host_pass(const fade_config_t* c, fade_layer_t* L, int pass) {
+  const bool evicts = c->policy != FADE_EVICT_NONE && c->int4_budget >= 0;
+  for (int b = 0; b < c->batch; ++b) {
+    int s = L->h_n_sink[b], m = L->h_n_mid[b], r = L->h_n_recent[b];
+    if (r == c->recent_window) {  // demote
+      if (m + 1 > c->mid_capacity)
+        return set_error(FADE_ERR_CAPACITY, "row %d: middle tier full (%d slots)", b,
+                         c->mid_capacity);
+      m += 1;
+      r -= 1;
+    }
+    if (evicts && m > c->int4_budget) m = c->int4_budget;  // evict
+    if (s >= c->n_sink && r >= c->recent_window)             // append
+      return set_error(FADE_ERR_CAPACITY, "row %d: recent window full (demote first)", b);
+    if (s < c->n_sink)
+      s += 1;
+    else
+      r += 1;
+    if (pass == 1) {
+      L->h_n_sink[b] = s;
+      L->h_n_mid[b] = m;
+      L->h_n_recent[b] = r;
+    }
+  }
+  return FADE_OK;
+}
+}  // namespace
+
 extern "C" fade_status_t fade_cache_advance_host(const fade_config_t* c, fade_layer_t* L) {
   clear_error();
   fade_status_t st = validate_config(c);
   if (st) return st;
   if (!L || !L->h_n_sink || !L->h_n_mid || !L->h_n_recent)
     return set_error(FADE_ERR_INVALID_ARGUMENT, "host mirror arrays are NULL");
-  const bool evicts = c->policy != FADE_EVICT_NONE && c->int4_budget >= 0;
   // every row's counts after the step, checked before any of them is stored
+  if ((st = advance_host_pass(c, L, 0))) return st;
+  return advance_host_pass(c, L, 1);
+}
+
+extern "C" fade_status_t fade_cache_advance_host_layers(const fade_config_t* c,
+                                                        fade_layer_t* const* layers,
+                                                        int32_t n_layers) {
+  clear_error();
+  fade_status_t st = validate_config(c);
+  if (st) return st;
+  if (n_layers < 0 || (n_layers > 0 && !layers))
+    return set_error(FADE_ERR_INVALID_ARGUMENT, "bad layer array");
+  for (int i = 0; i < n_layers; ++i) {
+    const fade_layer_t* L = layers[i];
+    if (!L || !L->h_n_sink || !L->h_n_mid || !L->h_n_recent)
+      return set_error(FADE_ERR_INVALID_ARGUMENT, "layer %d: host mirror arrays are NULL", i);
+  }
+  // every layer's rows checked before any count is stored
   for (int pass = 0; pass < 2; ++pass)
-    for (int b = 0; b < c->batch; ++b) {
-      int s = L->h_n_sink[b], m = L->h_n_mid[b], r = L->h_n_recent[b];
-      if (r == c->recent_window) {  // demote
-        if (m + 1 > c->mid_capacity)
-          return set_error(FADE_ERR_CAPACITY, "row %d: middle tier full (%d slots)", b,
-                           c->mid_capacity);
-        m += 1;
-        r -= 1;
-      }
-      if (evicts && m > c->int4_budget) m = c->int4_budget;  // evict
-      if (s >= c->n_sink && r >= c->recent_window)             // append
-        return set_error(FADE_ERR_CAPACITY, "row %d: recent window full (demote first)", b);
-      if (s < c->n_sink)
-        s += 1;
-      else
-        r += 1;
-      if (pass == 1) {
-        L->h_n_sink[b] = s;
-        L->h_n_mid[b] = m;
-        L->h_n_recent[b] = r;
-      }
-    }
+    for (int i = 0; i < n_layers; ++i)
+      if ((st = advance_host_pass(c, layers[i], pass))) return st;
   return FADE_OK;
 }
 

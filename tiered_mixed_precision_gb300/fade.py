@@ -117,6 +117,7 @@ def lib():
             "fade_next_position": (c_i32, [S(ConfigT), S(LayerT), c_i32]),
             "fade_compressed_bytes": (ctypes.c_uint64, [S(ConfigT), S(LayerT)]),
             "fade_cache_advance_host": (c_i32, [S(ConfigT), S(LayerT)]),
+            "fade_cache_advance_host_layers": (c_i32, [S(ConfigT), c_vp, c_i32]),
             "fade_pq_encode": (c_i32, [c_vp, c_vp, c_i64, c_i32, c_vp, c_vp]),
             "fade_pq_decode": (c_i32, [c_vp, c_vp, c_i64, c_i32, c_vp, c_vp]),
             "fade_pq_train": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_i32, c_vp, c_vp, c_sz, c_vp]),
@@ -430,6 +431,18 @@ def fade_next_position(layer: TieredLayer, row: int) -> int:
 
 def fade_cache_advance_host(layer: TieredLayer):
     _check(lib().fade_cache_advance_host(ctypes.byref(layer.cfg.c()), ctypes.byref(layer.c)))
+
+
+def layer_pointer_array(layers):
+    """A host array of the layers' C structs (for fade_cache_advance_host_layers); it stays
+    valid while the layers live."""
+    arr = (ctypes.POINTER(LayerT) * len(layers))(*[ctypes.pointer(L.c) for L in layers])
+    return arr
+
+
+def fade_cache_advance_host_layers(cfg: "Config", layer_array, n_layers: int):
+    """fade_cache_advance_host for every layer of ``layer_array`` (``layer_pointer_array``)."""
+    _check(lib().fade_cache_advance_host_layers(ctypes.byref(cfg.c()), layer_array, n_layers))
 
 
 def fade_compressed_bytes(layer: TieredLayer) -> int:

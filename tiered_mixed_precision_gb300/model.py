@@ -458,8 +458,9 @@ class FadeCache:
         ev.record()
         self._pos_ring_ev[i] = ev
         graph.replay()
-        for L in self.layers:
-            F.fade_cache_advance_host(L)
+        if getattr(self, "_layer_array", None) is None:
+            self._layer_array = F.layer_pointer_array(self.layers)
+        F.fade_cache_advance_host_layers(self.cfg, self._layer_array, len(self.layers))
 
     def _tick(self, name):
         if self.timers is None:
